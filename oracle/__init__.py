@@ -1,0 +1,227 @@
+"""CPU oracle for decode over a budget-bounded KV cache with eviction.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers. The product path never
+imports this package, and this package never imports the product package.
+
+The arithmetic lives in ``kvevict_oracle.c`` (plain C, fp64, one unit at a
+time, literal step order). This module compiles it with gcc on first use and
+marshals arguments through ctypes; it adds no arithmetic of its own.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvevict_oracle.c")
+_LIB = os.path.join(_HERE, "liborc_kvevict.so")
+
+H2O, SINK_WINDOW, RANDOM = 0, 1, 2
+OK, EINVAL, ECAPACITY, ESTATE = 0, -1, -2, -3
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc, no fast-math, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                               "-fno-fast-math", "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            P, I, U64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_double
+            L.orc_new.restype = P
+            L.orc_new.argtypes = [I, I, I, I, I, I, I, I, I, U64, I, I, I]
+            L.orc_free.argtypes = [P]
+            for name in ("orc_capacity", "orc_steps", "orc_prompt_len", "orc_cuts", "orc_count",
+                         "orc_greedy_disagreements"):
+                getattr(L, name).argtypes = [P]
+                getattr(L, name).restype = I
+            L.orc_last_victim_pos.argtypes = [P]
+            L.orc_last_victim_pos.restype = ctypes.c_int32
+            L.orc_evicted_mass.argtypes = [P]
+            L.orc_evicted_mass.restype = D
+            L.orc_new_score.argtypes = [P]
+            L.orc_new_score.restype = D
+            L.orc_positions.argtypes = [P, P]
+            L.orc_scores.argtypes = [P, P]
+            L.orc_slot_kv.argtypes = [P, I, P, P]
+            L.orc_attend.argtypes = [P, P, P, P, P]
+            L.orc_attend.restype = I
+            L.orc_choose.argtypes = [P]
+            L.orc_choose.restype = I
+            L.orc_commit.argtypes = [P, I]
+            L.orc_commit.restype = I
+            L.orc_prefill.argtypes = [P, P, P, I]
+            L.orc_prefill.restype = I
+            L.orc_step.argtypes = [P, P, P, P, P]
+            L.orc_step.restype = I
+            L.orc_run.argtypes = [P, I, I, P, P, P, P, I]
+            L.orc_run.restype = I
+            L.orc_online_cores.restype = I
+            L.orc_philox4x64_10.argtypes = [P, P, P]
+            L.orc_random_key.argtypes = [U64, I, I, I, I, I]
+            L.orc_random_key.restype = U64
+            _lib = L
+    return _lib
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Unit:
+    """One (sequence, layer, KV head) cache held by the oracle."""
+
+    def __init__(self, policy: int, n_sink: int, n_heavy: int, n_recent: int, budget: int, r: int,
+                 max_prompt: int, group: int, head_dim: int, seed: int = 0, seq: int = 0, layer: int = 0,
+                 head: int = 0):
+        self._L = lib()
+        self.h = self._L.orc_new(policy, n_sink, n_heavy, n_recent, budget, r, max_prompt, group, head_dim,
+                                 seed, seq, layer, head)
+        if not self.h:
+            raise ValueError("oracle: invalid unit configuration")
+        self.policy, self.G, self.d = policy, group, head_dim
+        self.cap = self._L.orc_capacity(self.h)
+
+    @classmethod
+    def for_workload(cls, w, seq: int, layer: int, kv_head: int) -> "Unit":
+        return cls(w.policy, w.n_sink, w.n_heavy, w.n_recent, w.budget, w.r, w.max_prompt, w.group,
+                   w.head_dim, w.seed, seq, layer, kv_head)
+
+    def __del__(self):
+        h, self.h = getattr(self, "h", None), None
+        if h:
+            self._L.orc_free(h)
+
+    # -- steps ---------------------------------------------------------------
+    def prefill(self, k, v) -> None:
+        k, v = _f32(k), _f32(v)
+        rc = self._L.orc_prefill(self.h, _ptr(k), _ptr(v), k.shape[0])
+        if rc:
+            raise RuntimeError(f"oracle prefill failed: {rc}")
+
+    def attend(self, q, k_new, v_new) -> np.ndarray:
+        q, k, v = _f32(q), _f32(k_new), _f32(v_new)
+        out = np.empty((self.G, self.d), dtype=np.float64)
+        rc = self._L.orc_attend(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(out))
+        if rc:
+            raise RuntimeError(f"oracle attend failed: {rc}")
+        return out
+
+    def choose(self) -> int:
+        s = self._L.orc_choose(self.h)
+        if s < 0:
+            raise RuntimeError(f"oracle choose failed: {s}")
+        return s
+
+    def commit(self, slot: int) -> None:
+        rc = self._L.orc_commit(self.h, int(slot))
+        if rc:
+            raise RuntimeError(f"oracle commit failed: {rc}")
+
+    def step(self, q, k_new, v_new):
+        out = self.attend(q, k_new, v_new)
+        slot = self.choose()
+        self.commit(slot)
+        return out, slot
+
+    # -- state ---------------------------------------------------------------
+    def positions(self) -> np.ndarray:
+        a = np.empty(self.cap, dtype=np.int32)
+        self._L.orc_positions(self.h, _ptr(a))
+        return a
+
+    def scores(self) -> np.ndarray:
+        a = np.empty(self.cap, dtype=np.float64)
+        self._L.orc_scores(self.h, _ptr(a))
+        return a
+
+    def slot_kv(self, slot: int):
+        k = np.empty(self.d, dtype=np.float32)
+        v = np.empty(self.d, dtype=np.float32)
+        self._L.orc_slot_kv(self.h, int(slot), _ptr(k), _ptr(v))
+        return k, v
+
+    @property
+    def steps(self) -> int:
+        return self._L.orc_steps(self.h)
+
+    @property
+    def count(self) -> int:
+        return self._L.orc_count(self.h)
+
+    @property
+    def cuts(self) -> int:
+        return self._L.orc_cuts(self.h)
+
+    @property
+    def prompt_len(self) -> int:
+        return self._L.orc_prompt_len(self.h)
+
+    @property
+    def evicted_mass(self) -> float:
+        return self._L.orc_evicted_mass(self.h)
+
+    @property
+    def last_victim_pos(self) -> int:
+        return self._L.orc_last_victim_pos(self.h)
+
+    @property
+    def new_score(self) -> float:
+        return self._L.orc_new_score(self.h)
+
+    @property
+    def greedy_disagreements(self) -> int:
+        return self._L.orc_greedy_disagreements(self.h)
+
+
+def run(units, q, k, v, n_threads: int = 0, keep_out: bool = False):
+    """n_steps decode steps on each unit, units spread over threads.
+
+    q: [n_units, n_steps, G, d]; k, v: [n_units, n_steps, d].
+    """
+    L = lib()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    n_units, n_steps = q.shape[0], q.shape[1]
+    arr = (ctypes.c_void_p * n_units)(*[u.h for u in units])
+    out = np.empty(q.shape, dtype=np.float64) if keep_out else None
+    rc = L.orc_run(ctypes.cast(arr, ctypes.c_void_p), n_units, n_steps, _ptr(q), _ptr(k), _ptr(v),
+                   _ptr(out) if keep_out else None, int(n_threads))
+    if rc:
+        raise RuntimeError(f"oracle run failed: {rc}")
+    return out
+
+
+def online_cores() -> int:
+    return lib().orc_online_cores()
+
+
+def philox4x64_10(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, dtype=np.uint64)
+    kk = np.ascontiguousarray(key, dtype=np.uint64)
+    out = np.empty(4, dtype=np.uint64)
+    lib().orc_philox4x64_10(_ptr(c), _ptr(kk), _ptr(out))
+    return out
+
+
+def random_key(seed: int, seq: int, layer: int, head: int, step: int, pos: int) -> int:
+    return int(lib().orc_random_key(seed, seq, layer, head, step, pos))

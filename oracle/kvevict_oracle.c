@@ -1,0 +1,493 @@
+/*
+ * kvevict_oracle.c -- plain, slow CPU oracle for one decode step of attention
+ * over a budget-bounded KV cache with eviction.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg may load this code. The product path never
+ * calls it, and it shares no code, header, table or helper with the CUDA
+ * library.
+ *
+ * Arithmetic is fp64 throughout. Inputs are kept exactly as given (fp32
+ * values, or bf16 values held in fp32) and widened to fp64 when used.
+ * Everything is per unit: one (sequence, layer, KV head) cache, independent
+ * of every other unit.
+ *
+ * Sources (page title, then section):
+ *  - "KV Cache 驱逐策略：从 LRU 到 H2O" (wiblog.cn), "注意力分数" and the
+ *    eviction flowchart: each generated token attends over the cache, every
+ *    cached token's cumulative attention score is updated, and eviction only
+ *    happens once the pool is full.
+ *  - "h2o: heavy-hitter oracle ..." summary (fmread.com), the Algorithm 1
+ *    paragraph: budget K; at step i the candidate set is S_{i-1} plus {i};
+ *    if it exceeds K, remove the element v whose removal leaves the remaining
+ *    set with the highest cumulative score.
+ *  - "Attention Sinks 与 KV Cache 淘汰策略" (10100.com), section 4.1
+ *    (StreamingLLM: first 4 tokens locked as sinks, ring buffer for the most
+ *    recent W) and section 4.2 (H2O: sink + heavy hitters + recent window;
+ *    per-step loop attend -> accumulate -> select -> evict).
+ *  - "Random Attention" summary (ai-feeds.com), "方法": keep every prompt
+ *    token; for generated tokens over budget K, evict uniformly at random,
+ *    independently per attention head, with a periodic budget K and buffer r.
+ *  - Philox4x64-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+ *    Easy as 1, 2, 3", SC'11.
+ *
+ * Readings where the pages leave a step open (each one also listed with the
+ * design notes):
+ *  - the new token attends over the retained set plus itself; eviction comes
+ *    after attention and accumulation, and the new token takes the victim's
+ *    slot;
+ *  - the H2O recent window is a position window that includes the new token:
+ *    a token is a candidate iff n_sink <= pos <= p - n_recent;
+ *  - f_score is additive, so the remaining set's score after removing v is
+ *    F(T) - s(v); ties go to the lower score, then the older position;
+ *  - one decision per unit; with GQA the unit's score is the mean of its G
+ *    query heads' probabilities;
+ *  - prompt tokens enter with score 0 through the same admission rule (the
+ *    API gives prefill no queries);
+ *  - softmax scale 1/sqrt(d), no position encoding;
+ *  - Random: a cut happens when the generated count reaches K + r and removes
+ *    the r generated tokens with the smallest 64-bit Philox key (ties: older
+ *    position), counter (pos, step, layer * 2^16 + head, seq), key
+ *    (seed, 0x5EED0001).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { ORC_H2O = 0, ORC_SINK_WINDOW = 1, ORC_RANDOM = 2 };
+enum { ORC_OK = 0, ORC_EINVAL = -1, ORC_ECAPACITY = -2, ORC_ESTATE = -3 };
+
+#define ORC_RANDOM_KEY_TAG 0x5EED0001ull
+
+typedef struct orc_unit {
+    int policy, n_sink, n_heavy, n_recent, budget, r, max_prompt, cap, G, d;
+    uint64_t seed;
+    int seq, layer, head;
+    int prompt_len;      /* prompt tokens appended so far */
+    int t;               /* decode steps committed */
+    int n_gen;           /* generated tokens currently held (Random) */
+    int n_cuts;
+    int32_t *pos;        /* [cap] position held by each slot, -1 = empty */
+    float *k, *v;        /* [cap][d] */
+    double *score;       /* [cap] cumulative attention score (H2O) */
+    double evicted_mass; /* sum of the scores of evicted tokens (H2O) */
+    /* the token of the step in progress */
+    int have_new;
+    int is_prompt;
+    int32_t new_pos;
+    float *k_new, *v_new;
+    double score_new;
+    int32_t last_victim_pos; /* position removed by the last commit, -1 if none */
+    int greedy_disagreements; /* argmax F(T\{v}) != argmin (score, pos): must stay 0 */
+} orc_unit;
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x64-10 (SC'11).                                                    */
+/* ------------------------------------------------------------------------ */
+
+static void mulhilo64(uint64_t a, uint64_t b, uint64_t *hi, uint64_t *lo)
+{
+    unsigned __int128 p = (unsigned __int128)a * (unsigned __int128)b;
+    *hi = (uint64_t)(p >> 64);
+    *lo = (uint64_t)p;
+}
+
+void orc_philox4x64_10(const uint64_t ctr_in[4], const uint64_t key_in[2], uint64_t out[4])
+{
+    /* Round multipliers and Weyl key increments from the SC'11 paper. */
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint64_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) { k0 += W0; k1 += W1; }
+        uint64_t hi0, lo0, hi1, lo1;
+        mulhilo64(M0, c0, &hi0, &lo0);
+        mulhilo64(M1, c2, &hi1, &lo1);
+        uint64_t n0 = hi1 ^ c1 ^ k0;
+        uint64_t n1 = lo1;
+        uint64_t n2 = hi0 ^ c3 ^ k1;
+        uint64_t n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The eviction key Random Attention draws for one generated token at one cut. */
+uint64_t orc_random_key(uint64_t seed, int seq, int layer, int head, int step, int pos)
+{
+    uint64_t ctr[4] = {(uint64_t)(uint32_t)pos, (uint64_t)(uint32_t)step,
+                       ((uint64_t)(uint32_t)layer << 16) + (uint64_t)(uint32_t)head,
+                       (uint64_t)(uint32_t)seq};
+    uint64_t key[2] = {seed, ORC_RANDOM_KEY_TAG};
+    uint64_t out[4];
+    orc_philox4x64_10(ctr, key, out);
+    return out[0];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Unit lifetime.                                                            */
+/* ------------------------------------------------------------------------ */
+
+orc_unit *orc_new(int policy, int n_sink, int n_heavy, int n_recent, int budget, int r, int max_prompt,
+                  int G, int d, uint64_t seed, int seq, int layer, int head)
+{
+    if (G < 1 || d < 1 || budget < 1) return NULL;
+    if (policy == ORC_H2O) {
+        if (n_sink < 0 || n_heavy < 0 || n_recent < 1 || n_sink + n_heavy + n_recent != budget) return NULL;
+    } else if (policy == ORC_SINK_WINDOW) {
+        if (n_sink < 0 || n_heavy != 0 || n_recent < 1 || n_sink + n_recent != budget) return NULL;
+    } else if (policy == ORC_RANDOM) {
+        if (r < 1 || max_prompt < 0) return NULL;
+    } else {
+        return NULL;
+    }
+    orc_unit *u = (orc_unit *)calloc(1, sizeof(orc_unit));
+    if (!u) return NULL;
+    u->policy = policy; u->n_sink = n_sink; u->n_heavy = n_heavy; u->n_recent = n_recent;
+    u->budget = budget; u->r = r; u->max_prompt = max_prompt; u->G = G; u->d = d;
+    u->seed = seed; u->seq = seq; u->layer = layer; u->head = head;
+    u->cap = (policy == ORC_RANDOM) ? max_prompt + budget + r : budget;
+    u->pos = (int32_t *)malloc(sizeof(int32_t) * (size_t)u->cap);
+    u->k = (float *)calloc((size_t)u->cap * (size_t)d, sizeof(float));
+    u->v = (float *)calloc((size_t)u->cap * (size_t)d, sizeof(float));
+    u->score = (double *)calloc((size_t)u->cap, sizeof(double));
+    u->k_new = (float *)calloc((size_t)d, sizeof(float));
+    u->v_new = (float *)calloc((size_t)d, sizeof(float));
+    if (!u->pos || !u->k || !u->v || !u->score || !u->k_new || !u->v_new) {
+        free(u->pos); free(u->k); free(u->v); free(u->score); free(u->k_new); free(u->v_new); free(u);
+        return NULL;
+    }
+    for (int s = 0; s < u->cap; ++s) u->pos[s] = -1;
+    u->last_victim_pos = -1;
+    return u;
+}
+
+void orc_free(orc_unit *u)
+{
+    if (!u) return;
+    free(u->pos); free(u->k); free(u->v); free(u->score); free(u->k_new); free(u->v_new);
+    free(u);
+}
+
+int orc_capacity(const orc_unit *u) { return u->cap; }
+int orc_steps(const orc_unit *u) { return u->t; }
+int orc_prompt_len(const orc_unit *u) { return u->prompt_len; }
+int orc_cuts(const orc_unit *u) { return u->n_cuts; }
+int orc_greedy_disagreements(const orc_unit *u) { return u->greedy_disagreements; }
+double orc_evicted_mass(const orc_unit *u) { return u->evicted_mass; }
+int32_t orc_last_victim_pos(const orc_unit *u) { return u->last_victim_pos; }
+double orc_new_score(const orc_unit *u) { return u->score_new; }
+
+void orc_positions(const orc_unit *u, int32_t *dst) { memcpy(dst, u->pos, sizeof(int32_t) * (size_t)u->cap); }
+void orc_scores(const orc_unit *u, double *dst) { memcpy(dst, u->score, sizeof(double) * (size_t)u->cap); }
+
+/* Copy out the stored K/V of one slot (test use). */
+void orc_slot_kv(const orc_unit *u, int slot, float *k, float *v)
+{
+    memcpy(k, u->k + (size_t)slot * u->d, sizeof(float) * (size_t)u->d);
+    memcpy(v, u->v + (size_t)slot * u->d, sizeof(float) * (size_t)u->d);
+}
+
+int orc_count(const orc_unit *u)
+{
+    int n = 0;
+    for (int s = 0; s < u->cap; ++s) n += (u->pos[s] >= 0);
+    return n;
+}
+
+static int first_free_slot(const orc_unit *u)
+{
+    for (int s = 0; s < u->cap; ++s)
+        if (u->pos[s] < 0) return s;
+    return -1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step (i)+(ii): attention of the new token's G queries over the retained   */
+/* tokens plus the new token itself, and the cumulative-score update.        */
+/* ------------------------------------------------------------------------ */
+
+int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_new, double *out)
+{
+    if (u->have_new) return ORC_ESTATE;
+    const int G = u->G, d = u->d, cap = u->cap;
+    const double scale = 1.0 / sqrt((double)d);
+    memcpy(u->k_new, k_new, sizeof(float) * (size_t)d);
+    memcpy(u->v_new, v_new, sizeof(float) * (size_t)d);
+    u->new_pos = u->prompt_len + u->t;
+    u->is_prompt = 0;
+
+    double *z = (double *)malloc(sizeof(double) * (size_t)(cap + 1));
+    double *mass = (double *)calloc((size_t)(cap + 1), sizeof(double)); /* sum over heads of p */
+    if (!z || !mass) { free(z); free(mass); return ORC_ECAPACITY; }
+
+    for (int g = 0; g < G; ++g) {
+        const float *qg = q + (size_t)g * d;
+        /* logits of every retained token, in slot order, then the new token */
+        double m = -INFINITY;
+        for (int s = 0; s <= cap; ++s) {
+            const float *ks;
+            if (s < cap) {
+                if (u->pos[s] < 0) continue;
+                ks = u->k + (size_t)s * d;
+            } else {
+                ks = u->k_new;
+            }
+            double dot = 0.0;
+            for (int i = 0; i < d; ++i) dot += (double)qg[i] * (double)ks[i];
+            z[s] = dot * scale;
+            if (z[s] > m) m = z[s];
+        }
+        double l = 0.0;
+        for (int s = 0; s <= cap; ++s) {
+            if (s < cap && u->pos[s] < 0) continue;
+            l += exp(z[s] - m);
+        }
+        double *og = out + (size_t)g * d;
+        for (int i = 0; i < d; ++i) og[i] = 0.0;
+        for (int s = 0; s <= cap; ++s) {
+            if (s < cap && u->pos[s] < 0) continue;
+            double p = exp(z[s] - m) / l;
+            const float *vs = (s < cap) ? u->v + (size_t)s * d : u->v_new;
+            for (int i = 0; i < d; ++i) og[i] += p * (double)vs[i];
+            mass[s] += p;
+        }
+    }
+    /* H2O: every retained token's cumulative score grows by this step's
+     * probability (mean over the unit's G query heads); the new token starts
+     * with its own. Sink-window and Random keep no scores. */
+    if (u->policy == ORC_H2O) {
+        for (int s = 0; s < cap; ++s)
+            if (u->pos[s] >= 0) u->score[s] += mass[s] / (double)G;
+        u->score_new = mass[cap] / (double)G;
+    } else {
+        u->score_new = 0.0;
+    }
+    free(z);
+    free(mass);
+    u->have_new = 1;
+    return ORC_OK;
+}
+
+/* A prompt token is admitted like a decode token, with score 0 and no
+ * attention. */
+static int stage_prompt_token(orc_unit *u, const float *k, const float *v)
+{
+    if (u->have_new) return ORC_ESTATE;
+    if (u->t > 0) return ORC_ESTATE;
+    if (u->policy == ORC_RANDOM && u->prompt_len >= u->max_prompt) return ORC_ECAPACITY;
+    memcpy(u->k_new, k, sizeof(float) * (size_t)u->d);
+    memcpy(u->v_new, v, sizeof(float) * (size_t)u->d);
+    u->new_pos = u->prompt_len;
+    u->is_prompt = 1;
+    u->score_new = 0.0;
+    u->have_new = 1;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step (iii): where the new token goes.                                     */
+/* ------------------------------------------------------------------------ */
+
+/* H2O, Algorithm 1: T = S u {new}; if |T| > K remove the eligible v that
+ * maximises F(T \ {v}). Returns the slot the new token takes. */
+static int choose_h2o(orc_unit *u)
+{
+    int count = orc_count(u);
+    if (count + 1 <= u->budget) return first_free_slot(u);
+
+    const int32_t p = u->new_pos;
+    double total = u->score_new; /* F(T) */
+    for (int s = 0; s < u->cap; ++s)
+        if (u->pos[s] >= 0) total += u->score[s];
+
+    int best = -1;
+    double best_F = -INFINITY, best_s = 0.0;
+    int32_t best_pos = 0;
+    for (int s = 0; s < u->cap; ++s) {
+        int32_t ps = u->pos[s];
+        if (ps < 0) continue;
+        if (!(ps >= u->n_sink && ps <= p - u->n_recent)) continue; /* sink or recent: protected */
+        double F = total - u->score[s]; /* the remaining set's cumulative score */
+        int better = 0;
+        if (best < 0 || F > best_F) better = 1;
+        else if (F == best_F && (u->score[s] < best_s || (u->score[s] == best_s && ps < best_pos))) better = 1;
+        if (better) { best = s; best_F = F; best_s = u->score[s]; best_pos = ps; }
+    }
+    /* The new token is never a candidate: it sits inside the recent window. */
+
+    /* Cross-check against the plain argmin of (score, position). */
+    int am = -1;
+    for (int s = 0; s < u->cap; ++s) {
+        int32_t ps = u->pos[s];
+        if (ps < 0 || !(ps >= u->n_sink && ps <= p - u->n_recent)) continue;
+        if (am < 0 || u->score[s] < u->score[am] || (u->score[s] == u->score[am] && ps < u->pos[am])) am = s;
+    }
+    if (am != best) u->greedy_disagreements++;
+    return best;
+}
+
+/* StreamingLLM, written as the ring it is: the first n_sink positions are
+ * locked; the window holds the newest n_recent tokens and a new token
+ * overwrites the oldest window entry. */
+static int choose_sink_window(orc_unit *u)
+{
+    if (u->new_pos < u->n_sink) return first_free_slot(u);
+    int in_window = 0, oldest = -1;
+    for (int s = 0; s < u->cap; ++s) {
+        if (u->pos[s] < u->n_sink) continue; /* empty or sink */
+        in_window++;
+        if (oldest < 0 || u->pos[s] < u->pos[oldest]) oldest = s;
+    }
+    if (in_window < u->n_recent) return first_free_slot(u);
+    return oldest;
+}
+
+int orc_choose(orc_unit *u)
+{
+    if (!u->have_new) return ORC_ESTATE;
+    switch (u->policy) {
+    case ORC_H2O: return choose_h2o(u);
+    case ORC_SINK_WINDOW: return choose_sink_window(u);
+    default: return first_free_slot(u); /* Random: the lowest free slot */
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step (iv): admit the new token into `slot`, evicting what it held.        */
+/* ------------------------------------------------------------------------ */
+
+typedef struct { uint64_t key; int32_t pos; int slot; } orc_draw;
+
+static int cmp_draw(const void *a, const void *b)
+{
+    const orc_draw *x = (const orc_draw *)a, *y = (const orc_draw *)b;
+    if (x->key != y->key) return x->key < y->key ? -1 : 1;
+    return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+/* Random Attention's periodic cut: every generated token gets a fresh 64-bit
+ * key for this step; the r smallest leave. The prompt is never touched. */
+static void random_cut(orc_unit *u, int step)
+{
+    int n = 0;
+    orc_draw *dr = (orc_draw *)malloc(sizeof(orc_draw) * (size_t)u->cap);
+    for (int s = 0; s < u->cap; ++s) {
+        if (u->pos[s] < u->prompt_len) continue; /* empty or prompt */
+        dr[n].key = orc_random_key(u->seed, u->seq, u->layer, u->head, step, u->pos[s]);
+        dr[n].pos = u->pos[s];
+        dr[n].slot = s;
+        n++;
+    }
+    qsort(dr, (size_t)n, sizeof(orc_draw), cmp_draw);
+    for (int i = 0; i < u->r && i < n; ++i) u->pos[dr[i].slot] = -1;
+    u->n_gen = n - (u->r < n ? u->r : n);
+    u->n_cuts++;
+    free(dr);
+}
+
+int orc_commit(orc_unit *u, int slot)
+{
+    if (!u->have_new) return ORC_ESTATE;
+    if (slot < 0 || slot >= u->cap) return ORC_EINVAL;
+    u->last_victim_pos = u->pos[slot];
+    if (u->pos[slot] >= 0 && u->policy == ORC_H2O) u->evicted_mass += u->score[slot];
+    u->pos[slot] = u->new_pos;
+    memcpy(u->k + (size_t)slot * u->d, u->k_new, sizeof(float) * (size_t)u->d);
+    memcpy(u->v + (size_t)slot * u->d, u->v_new, sizeof(float) * (size_t)u->d);
+    u->score[slot] = u->score_new;
+    u->have_new = 0;
+    if (u->is_prompt) {
+        u->prompt_len++;
+        return ORC_OK;
+    }
+    if (u->policy == ORC_RANDOM) {
+        u->n_gen++;
+        if (u->n_gen == u->budget + u->r) random_cut(u, u->t);
+    }
+    u->t++;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Conveniences built only from the steps above.                             */
+/* ------------------------------------------------------------------------ */
+
+/* Append n prompt tokens ([n][d] each), one at a time. */
+int orc_prefill(orc_unit *u, const float *k, const float *v, int n)
+{
+    for (int i = 0; i < n; ++i) {
+        int rc = stage_prompt_token(u, k + (size_t)i * u->d, v + (size_t)i * u->d);
+        if (rc) return rc;
+        int slot = orc_choose(u);
+        if (slot < 0) { u->have_new = 0; return ORC_ECAPACITY; }
+        orc_commit(u, slot);
+    }
+    return ORC_OK;
+}
+
+/* One full decode step with the oracle's own decision. Returns the slot taken. */
+int orc_step(orc_unit *u, const float *q, const float *k_new, const float *v_new, double *out)
+{
+    int rc = orc_attend(u, q, k_new, v_new, out);
+    if (rc) return rc;
+    int slot = orc_choose(u);
+    if (slot < 0) { u->have_new = 0; return ORC_ECAPACITY; }
+    rc = orc_commit(u, slot);
+    return rc ? rc : slot;
+}
+
+/* Runs n_steps decode steps on each of n_units units, units spread over
+ * n_threads threads (0 = all online cores). Inputs per unit u and step t:
+ * q at q + ((u * n_steps + t) * G * d), k_new/v_new at ((u * n_steps + t) * d).
+ * out (optional) like q, fp64. Returns 0 or the first error. */
+typedef struct {
+    orc_unit **units; int n_units, n_steps, tid, n_threads;
+    const float *q, *k, *v; double *out; int rc;
+} orc_job;
+
+static void *run_job(void *arg)
+{
+    orc_job *j = (orc_job *)arg;
+    for (int i = j->tid; i < j->n_units; i += j->n_threads) {
+        orc_unit *u = j->units[i];
+        size_t gd = (size_t)u->G * u->d;
+        double *scratch = (double *)malloc(sizeof(double) * gd);
+        for (int t = 0; t < j->n_steps; ++t) {
+            size_t row = (size_t)i * j->n_steps + t;
+            double *o = j->out ? j->out + row * gd : scratch;
+            int rc = orc_step(u, j->q + row * gd, j->k + row * u->d, j->v + row * u->d, o);
+            if (rc < 0) { j->rc = rc; break; }
+        }
+        free(scratch);
+    }
+    return NULL;
+}
+
+int orc_online_cores(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }
+
+int orc_run(orc_unit **units, int n_units, int n_steps, const float *q, const float *k, const float *v,
+            double *out, int n_threads)
+{
+    if (n_threads <= 0) n_threads = orc_online_cores();
+    if (n_threads > n_units) n_threads = n_units;
+    if (n_threads < 1) n_threads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    orc_job *jobs = (orc_job *)calloc((size_t)n_threads, sizeof(orc_job));
+    for (int i = 0; i < n_threads; ++i) {
+        jobs[i] = (orc_job){units, n_units, n_steps, i, n_threads, q, k, v, out, 0};
+        pthread_create(&th[i], NULL, run_job, &jobs[i]);
+    }
+    int rc = 0;
+    for (int i = 0; i < n_threads; ++i) {
+        pthread_join(th[i], NULL);
+        if (jobs[i].rc && !rc) rc = jobs[i].rc;
+    }
+    free(th);
+    free(jobs);
+    return rc;
+}

@@ -1,0 +1,52 @@
+"""Algorithmic byte counts for one decode step (the roofline numerator).
+
+These count what the method itself has to move through HBM per unit (one
+(sequence, layer, KV head)) per decode step, independent of any kernel:
+
+  * K/V of every retained token plus the new token's K/V:  (n_ret + 1) * 2 * d * e
+  * the new token's K/V written into its slot:            2 * d * e
+  * the G queries read and the G outputs written:          2 * G * d * e
+  * H2O: the cumulative scores read and written (fp32), the new token's
+    score and position written:                            8 * n_ret + 8
+  * Random: the slot-position table read to skip holes:   4 * n_slots
+    and, on a cut step, the generated tokens' positions read and the freed
+    slots written:                                         4 * (K + r) + 4 * r
+
+KV cache size (the pages' sizing formula): 2 (K and V) * layers * KV heads *
+head_dim * bytes per element * tokens.
+"""
+from __future__ import annotations
+
+from .configs import POLICY_H2O, POLICY_RANDOM, Workload
+
+
+def kv_cache_bytes(n_layers: int, n_kv_heads: int, head_dim: int, elem_bytes: int, tokens: int) -> int:
+    return 2 * n_layers * n_kv_heads * head_dim * elem_bytes * tokens
+
+
+def score_bytes(tokens: int, score_elem_bytes: int = 4) -> int:
+    return tokens * score_elem_bytes
+
+
+def unit_step_bytes(w: Workload, n_retained: int, n_slots: int | None = None, cut: bool = False) -> int:
+    d, e, G = w.head_dim, w.elem_bytes, w.group
+    b = (n_retained + 1) * 2 * d * e + 2 * d * e + 2 * G * d * e
+    if w.policy == POLICY_H2O:
+        b += 8 * n_retained + 8
+    if w.policy == POLICY_RANDOM:
+        b += 4 * (n_slots if n_slots is not None else w.capacity)
+        if cut:
+            b += 4 * (w.budget + w.r) + 4 * w.r
+    return b
+
+
+def steady_layer_step_bytes(w: Workload) -> int:
+    """Bytes of one layer-step over all B * Hkv units once the cache is full."""
+    units = w.batch * w.n_kv_heads
+    if w.policy == POLICY_RANDOM:
+        # generated count cycles K .. K+r-1 before each step's insert; mean K + (r-1)/2
+        n_ret = w.prompt_len + w.budget + (w.r - 1) / 2.0
+        per = unit_step_bytes(w, int(round(n_ret)), w.prompt_len + w.budget + w.r)
+        cut_extra = (4 * (w.budget + w.r) + 4 * w.r) / w.r
+        return int(units * (per + cut_extra))
+    return units * unit_step_bytes(w, w.capacity)
