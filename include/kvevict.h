@@ -1,0 +1,202 @@
+/*
+ * kvevict.h -- C ABI of libkvevict.so: the decode step of attention over a
+ * budget-bounded KV cache with eviction, on one NVIDIA GB300 (sm_103a).
+ *
+ * One handle holds the KV cache of a whole model for B sequences: for every
+ * (layer, sequence, KV head) "unit" a fixed array of C slots, each slot
+ * holding one retained token's key, value, position and (H2O only) its
+ * cumulative attention score. A decode step for one layer does, for every
+ * unit, in one launch:
+ *   1. attention of the unit's G query heads over the retained tokens plus
+ *      the new token (split over the CTAs of a thread-block cluster, softmax
+ *      partials combined through distributed shared memory);
+ *   2. H2O: each retained token's cumulative score grows by its normalised
+ *      attention probability (mean over the G query heads); the new token
+ *      starts with its own;
+ *   3. the eviction decision (H2O: lowest score among non-sink tokens
+ *      outside the recent window; StreamingLLM: the token leaving the ring
+ *      window; Random Attention: a periodic uniform-random cut);
+ *   4. the new token's key/value written in place into the freed slot.
+ *
+ * Sources (page title and section):
+ *  - "KV Cache 驱逐策略：从 LRU 到 H2O" (wiblog.cn): cumulative attention
+ *    score as the eviction signal, eviction only when the pool is full, the
+ *    eviction flowchart.
+ *  - "h2o: heavy-hitter oracle for efficient generative inference" summary
+ *    (fmread.com): Algorithm 1 -- budget K, candidate set S_{i-1} + {i},
+ *    remove the element whose removal keeps the highest cumulative score.
+ *  - "Attention Sinks 与 KV Cache 淘汰策略" (10100.com): section 4.1
+ *    (StreamingLLM: 4 sink tokens locked + rolling window, ring buffer),
+ *    section 4.2 (H2O: sink + heavy hitters + recent window).
+ *  - "Random Attention" summary (ai-feeds.com), 方法: keep the prompt; evict
+ *    generated tokens uniformly at random, independently per head, with a
+ *    periodic budget K and buffer r.
+ *
+ * Conventions for every call:
+ *  - Returns KVEVICT_OK (0) or a negative kvevict_status. Argument and state
+ *    errors are found on the host before anything is launched; the call then
+ *    has no effect. Nothing in the device code traps: anomalies found on the
+ *    GPU set bits of a device error word that kvevict_check() reads.
+ *  - All work is queued asynchronously on the handle's CUDA stream; device
+ *    pointers passed in must stay valid until the stream has passed the call.
+ *  - Device tensors are dense, row-major, of the handle's dtype (fp32 or
+ *    bf16), 16-byte aligned.
+ *  - Not thread-safe: one host thread drives one handle at a time.
+ */
+#ifndef KVEVICT_H
+#define KVEVICT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVEVICT_API_VERSION 1
+
+typedef struct kvevict_handle *kvevict_t;
+
+typedef enum {
+    KVEVICT_H2O = 0,          /* sink + heavy hitters + recent window */
+    KVEVICT_SINK_WINDOW = 1,  /* StreamingLLM: sink + ring window, no scores */
+    KVEVICT_RANDOM = 2        /* Random Attention: prompt kept, periodic random cut */
+} kvevict_policy;
+
+typedef enum { KVEVICT_F32 = 0, KVEVICT_BF16 = 1 } kvevict_dtype;
+
+typedef enum {
+    KVEVICT_OK = 0,
+    KVEVICT_ERR_INVALID_ARG = -1, /* bad argument, shape, pointer or alignment */
+    KVEVICT_ERR_CAPACITY = -2,    /* prompt beyond max_prompt (Random), state buffer too small */
+    KVEVICT_ERR_STATE = -3,       /* call out of order (prefill after decode, layer out of range) */
+    KVEVICT_ERR_CUDA = -4,        /* a CUDA runtime call failed */
+    KVEVICT_ERR_DEVICE = -5       /* kvevict_check found device error bits */
+} kvevict_status;
+
+/* Bits of the device error word (kvevict_check). */
+#define KVEVICT_DEV_NONFINITE 0x1u    /* a softmax denominator was not finite or not positive */
+#define KVEVICT_DEV_NO_CANDIDATE 0x2u /* H2O found no evictable token; the new token was dropped */
+#define KVEVICT_DEV_WAIT_TIMEOUT 0x4u /* a pipeline wait gave up after its time limit */
+#define KVEVICT_DEV_BAD_SLOT 0x8u     /* a free-list entry was out of range; the new token was dropped */
+
+/*
+ * Whole configuration of a handle.
+ *   policy, n_sink, n_heavy, n_recent, budget, r, seed: the eviction method.
+ *     H2O:         budget K = n_sink + n_heavy + n_recent, n_recent >= 1; a
+ *                  token at position j is a candidate at the step that
+ *                  appends position p iff n_sink <= j <= p - n_recent.
+ *     SINK_WINDOW: budget = n_sink + n_recent, n_heavy = 0, n_recent >= 1.
+ *     RANDOM:      budget K = generated tokens kept after a cut, r >= 1 the
+ *                  buffer/period, K + r <= 8192; n_sink = n_heavy =
+ *                  n_recent = 0; seed keys the Philox4x64-10 draws.
+ *   batch, n_layers, n_q_heads, n_kv_heads, head_dim: model shape;
+ *     n_q_heads / n_kv_heads = G in {1, 2, 4, 8}; head_dim in {64, 128}.
+ *   dtype: KVEVICT_F32 or KVEVICT_BF16 for K, V, q and out.
+ *   max_prompt: RANDOM only, the longest prompt a unit may hold.
+ * Slot capacity per unit: C = budget (H2O, SINK_WINDOW) or
+ * max_prompt + budget + r (RANDOM).
+ */
+typedef struct {
+    int policy;
+    int n_sink, n_heavy, n_recent, budget, r;
+    uint64_t seed;
+    int batch, n_layers, n_q_heads, n_kv_heads, head_dim;
+    int dtype;
+    int max_prompt;
+} kvevict_config;
+
+typedef struct {
+    int64_t decode_steps;   /* layer-steps issued (one per kvevict_decode_step call) */
+    int64_t prefill_tokens; /* prompt tokens appended, summed over layers */
+    int64_t evictions;      /* tokens evicted, summed over units and layers */
+    int64_t cuts;           /* Random cuts, summed over layers (each cuts every unit of the layer) */
+    int split;              /* CTAs per unit in the decode launch (thread-block cluster size) */
+    int capacity;           /* slots per unit */
+} kvevict_stats;
+
+/* Bytes of device memory a handle with this configuration needs (cache,
+ * positions, scores, free lists, error word, host-path staging). Host only:
+ * launches nothing, needs no GPU. Returns INVALID_ARG for a configuration
+ * the library does not accept. */
+int kvevict_state_bytes(const kvevict_config *cfg, size_t *bytes);
+
+/* Creates a handle. `state` is device memory of at least
+ * kvevict_state_bytes() bytes, 256-byte aligned, owned by the caller (the
+ * Python binding allocates it with PyTorch) and used by the handle until
+ * kvevict_destroy. `cuda_stream` is a cudaStream_t (NULL: the legacy default
+ * stream). The cache starts empty (every position -1, every score 0); that
+ * initialisation is queued on the stream. */
+int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_t state_bytes,
+                   void *cuda_stream);
+
+/* Appends n_tokens prompt tokens to every unit of `layer`, with no attention
+ * (the API gives the prompt no queries): each enters with score 0 through the
+ * policy's admission rule, so H2O and SINK_WINDOW keep the n_sink first and
+ * the newest C - n_sink prompt tokens, and RANDOM keeps them all.
+ * K, V: device, [batch][n_kv_heads][n_tokens][head_dim]. May be called several
+ * times (chunks) before the layer's first decode step; STATE after it.
+ * RANDOM: CAPACITY if the layer's prompt would exceed max_prompt. */
+int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_tokens);
+
+/* One decode step of `layer` for every sequence (the four steps above).
+ *   q:     device, [batch][n_q_heads][head_dim]; query heads g*G .. g*G+G-1
+ *          share KV head g.
+ *   k_new, v_new: device, [batch][n_kv_heads][head_dim], the new token.
+ *   out:   device, [batch][n_q_heads][head_dim], attention output.
+ * Steps of one layer must be issued in token order; layers are independent.
+ * The new token's position is the layer's prompt length plus its decode
+ * steps so far. One kernel launch; RANDOM adds a cut launch every r steps. */
+int kvevict_decode_step(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new, void *out);
+
+/* kvevict_decode_step with HOST buffers of the same layouts (pinned memory
+ * for asynchronous copies). Copies the inputs in, runs the step and copies
+ * out back on the handle's stream, then waits for the stream. */
+int kvevict_decode_step_host(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new,
+                             void *out);
+
+/* Position held by every slot of `layer`, -1 for an empty slot:
+ * dst [batch][n_kv_heads][C] int32, device (dst_is_device = 1, asynchronous)
+ * or host (dst_is_device = 0, the call waits for the stream). */
+int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_device);
+
+/* Cumulative H2O scores of every slot of `layer`, [batch][n_kv_heads][C]
+ * fp32 (empty slots hold stale values; read them with the positions).
+ * INVALID_ARG for policies that keep no scores. Same dst rules as above. */
+int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device);
+
+/* Decode-step trace of `layer`: while set, decode step t (0-based, counted
+ * from this call), for t < n_steps, writes for every unit four int32 into
+ * dev_buf[t][batch][n_kv_heads][4] (device, 16-byte aligned): the slot the
+ * new token took, the position that slot held before (-1 if it was empty:
+ * otherwise the evicted token), the evicted token's cumulative score and the
+ * new token's score (fp32 bit patterns; 0 for policies without scores).
+ * dev_buf = NULL clears it. */
+int kvevict_set_trace(kvevict_t h, int layer, int32_t *dev_buf, int n_steps);
+
+/* Host-side counters of `layer`: prompt tokens appended, decode steps issued
+ * and tokens held per unit (after the last issued step). Any pointer may be
+ * NULL. */
+int kvevict_layer_state(kvevict_t h, int layer, int *prompt_len, int *steps, int *count);
+
+/* CTAs per unit of the decode launch (1, 2, 4, 8 or 16; 0 = automatic).
+ * A tuning knob: results do not depend on it beyond fp32 rounding order. */
+int kvevict_set_split(kvevict_t h, int split);
+
+int kvevict_get_stats(kvevict_t h, kvevict_stats *out);
+
+/* Waits for the stream, reads the device error word into *device_error (may
+ * be NULL) and clears it. Returns DEVICE if any bit was set, CUDA if the
+ * stream reported an error. */
+int kvevict_check(kvevict_t h, uint32_t *device_error);
+
+const char *kvevict_strerror(int code);
+
+/* Releases the host handle. The caller still owns and frees `state`. */
+void kvevict_destroy(kvevict_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVEVICT_H */

@@ -1,0 +1,84 @@
+"""ctypes declarations of libkvevict.so (include/kvevict.h).
+
+No fallback: if the library has not been built, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvevict.so")
+
+H2O, SINK_WINDOW, RANDOM = 0, 1, 2
+F32, BF16 = 0, 1
+
+OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_STATE, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5
+DEV_NONFINITE, DEV_NO_CANDIDATE, DEV_WAIT_TIMEOUT, DEV_BAD_SLOT = 0x1, 0x2, 0x4, 0x8
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("policy", ctypes.c_int), ("n_sink", ctypes.c_int), ("n_heavy", ctypes.c_int),
+                ("n_recent", ctypes.c_int), ("budget", ctypes.c_int), ("r", ctypes.c_int),
+                ("seed", ctypes.c_uint64), ("batch", ctypes.c_int), ("n_layers", ctypes.c_int),
+                ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("max_prompt", ctypes.c_int)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("decode_steps", ctypes.c_int64), ("prefill_tokens", ctypes.c_int64),
+                ("evictions", ctypes.c_int64), ("cuts", ctypes.c_int64), ("split", ctypes.c_int),
+                ("capacity", ctypes.c_int)]
+
+
+class KVEvictError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.kvevict_state_bytes.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(SZ)]
+            L.kvevict_create.argtypes = [ctypes.POINTER(P), ctypes.POINTER(Config), P, SZ, P]
+            L.kvevict_prefill.argtypes = [P, I, P, P, I]
+            L.kvevict_decode_step.argtypes = [P, I, P, P, P, P]
+            L.kvevict_decode_step_host.argtypes = [P, I, P, P, P, P]
+            L.kvevict_slot_positions.argtypes = [P, I, P, I]
+            L.kvevict_scores.argtypes = [P, I, P, I]
+            L.kvevict_set_trace.argtypes = [P, I, P, I]
+            L.kvevict_layer_state.argtypes = [P, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
+            L.kvevict_set_split.argtypes = [P, I]
+            L.kvevict_get_stats.argtypes = [P, ctypes.POINTER(Stats)]
+            L.kvevict_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            L.kvevict_strerror.argtypes = [I]
+            L.kvevict_strerror.restype = ctypes.c_char_p
+            L.kvevict_destroy.argtypes = [P]
+            L.kvevict_destroy.restype = None
+            for n in ("kvevict_state_bytes", "kvevict_create", "kvevict_prefill", "kvevict_decode_step",
+                      "kvevict_decode_step_host", "kvevict_slot_positions", "kvevict_scores", "kvevict_set_trace",
+                      "kvevict_layer_state", "kvevict_set_split", "kvevict_get_stats", "kvevict_check"):
+                getattr(L, n).restype = I
+            _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().kvevict_strerror(code).decode()
+
+
+def check(code: int, what: str) -> None:
+    if code != OK:
+        raise KVEvictError(code, what)

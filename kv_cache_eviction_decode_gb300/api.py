@@ -1,0 +1,157 @@
+"""Python binding of libkvevict.so: argument marshalling only.
+
+PyTorch supplies device memory (the handle's state buffer) and the CUDA
+stream; every step of the decode path runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import BF16, F32, H2O, RANDOM, SINK_WINDOW, Config, Stats, check, lib
+
+_DT = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+class KVEvictCache:
+    """KV cache of n_layers x batch x n_kv_heads units with budget-bounded eviction."""
+
+    def __init__(self, *, policy: int, budget: int, batch: int, n_layers: int, n_q_heads: int, n_kv_heads: int,
+                 head_dim: int, dtype: int, n_sink: int = 0, n_heavy: int = 0, n_recent: int = 0, r: int = 0,
+                 seed: int = 0, max_prompt: int = 0, device=None, stream: torch.cuda.Stream | None = None):
+        self._L = lib()
+        self.cfg = Config(policy, n_sink, n_heavy, n_recent, budget, r, seed, batch, n_layers, n_q_heads,
+                          n_kv_heads, head_dim, dtype, max_prompt)
+        nbytes = ctypes.c_size_t(0)
+        check(self._L.kvevict_state_bytes(ctypes.byref(self.cfg), ctypes.byref(nbytes)), "kvevict_state_bytes")
+        self.device = torch.device(device if device is not None else "cuda")
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.state = torch.empty(nbytes.value, dtype=torch.uint8, device=self.device)
+        self.h = ctypes.c_void_p()
+        check(self._L.kvevict_create(ctypes.byref(self.h), ctypes.byref(self.cfg), _ptr(self.state), nbytes.value,
+                                     self.stream.cuda_stream), "kvevict_create")
+        self.dtype = _DT[dtype]
+        self.B, self.L, self.Hq, self.Hkv, self.D = batch, n_layers, n_q_heads, n_kv_heads, head_dim
+        self.capacity = self.stats()["capacity"]
+        self._trace = {}
+
+    @classmethod
+    def from_workload(cls, w, device=None, stream=None) -> "KVEvictCache":
+        return cls(policy=w.policy, n_sink=w.n_sink, n_heavy=w.n_heavy, n_recent=w.n_recent, budget=w.budget,
+                   r=w.r, seed=w.seed, batch=w.batch, n_layers=w.n_layers, n_q_heads=w.n_q_heads,
+                   n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, dtype=w.dtype, max_prompt=w.max_prompt,
+                   device=device, stream=stream)
+
+    def close(self) -> None:
+        if getattr(self, "h", None) and self.h.value:
+            self._L.kvevict_destroy(self.h)
+            self.h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---------------------------------------------------------------- checks
+    def _dev(self, t: torch.Tensor, shape, name: str, dtype=None) -> torch.Tensor:
+        dtype = self.dtype if dtype is None else dtype
+        if t.device != self.device or t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}: need a contiguous {dtype} tensor of shape {tuple(shape)} on {self.device}, "
+                             f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+        return t
+
+    def _host(self, t: torch.Tensor, shape, name: str) -> torch.Tensor:
+        if t.device.type != "cpu" or t.dtype != self.dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}: need a contiguous CPU {self.dtype} tensor of shape {tuple(shape)}")
+        return t
+
+    # ----------------------------------------------------------------- steps
+    def prefill(self, layer: int, K: torch.Tensor, V: torch.Tensor) -> None:
+        n = K.shape[2]
+        shp = (self.B, self.Hkv, n, self.D)
+        self._dev(K, shp, "K")
+        self._dev(V, shp, "V")
+        check(self._L.kvevict_prefill(self.h, layer, _ptr(K), _ptr(V), n), "kvevict_prefill")
+
+    def decode_step(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+        self._dev(q, (self.B, self.Hq, self.D), "q")
+        self._dev(k_new, (self.B, self.Hkv, self.D), "k_new")
+        self._dev(v_new, (self.B, self.Hkv, self.D), "v_new")
+        if out is None:
+            out = torch.empty((self.B, self.Hq, self.D), dtype=self.dtype, device=self.device)
+        self._dev(out, (self.B, self.Hq, self.D), "out")
+        check(self._L.kvevict_decode_step(self.h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out)),
+              "kvevict_decode_step")
+        return out
+
+    def decode_step_host(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                         out: torch.Tensor) -> torch.Tensor:
+        self._host(q, (self.B, self.Hq, self.D), "q")
+        self._host(k_new, (self.B, self.Hkv, self.D), "k_new")
+        self._host(v_new, (self.B, self.Hkv, self.D), "v_new")
+        self._host(out, (self.B, self.Hq, self.D), "out")
+        check(self._L.kvevict_decode_step_host(self.h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out)),
+              "kvevict_decode_step_host")
+        return out
+
+    # ----------------------------------------------------------------- state
+    def slot_positions(self, layer: int, out: torch.Tensor | None = None) -> torch.Tensor:
+        shp = (self.B, self.Hkv, self.capacity)
+        if out is None:
+            out = torch.empty(shp, dtype=torch.int32, device=self.device)
+        on_dev = out.device.type == "cuda"
+        if on_dev:
+            self._dev(out, shp, "out", torch.int32)
+        check(self._L.kvevict_slot_positions(self.h, layer, _ptr(out), 1 if on_dev else 0), "kvevict_slot_positions")
+        return out
+
+    def scores(self, layer: int, out: torch.Tensor | None = None) -> torch.Tensor:
+        shp = (self.B, self.Hkv, self.capacity)
+        if out is None:
+            out = torch.empty(shp, dtype=torch.float32, device=self.device)
+        on_dev = out.device.type == "cuda"
+        if on_dev:
+            self._dev(out, shp, "out", torch.float32)
+        check(self._L.kvevict_scores(self.h, layer, _ptr(out), 1 if on_dev else 0), "kvevict_scores")
+        return out
+
+    def set_trace(self, layer: int, buf: torch.Tensor | None) -> None:
+        if buf is None:
+            check(self._L.kvevict_set_trace(self.h, layer, None, 0), "kvevict_set_trace")
+            self._trace.pop(layer, None)
+            return
+        if buf.dtype != torch.int32 or buf.device != self.device or not buf.is_contiguous() or \
+                tuple(buf.shape[1:]) != (self.B, self.Hkv, 4):
+            raise ValueError("trace buffer: contiguous int32 [n_steps, batch, n_kv_heads, 4] on the device")
+        self._trace[layer] = buf  # keep it alive while the library writes it
+        check(self._L.kvevict_set_trace(self.h, layer, _ptr(buf), buf.shape[0]), "kvevict_set_trace")
+
+    def layer_state(self, layer: int):
+        a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        check(self._L.kvevict_layer_state(self.h, layer, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+              "kvevict_layer_state")
+        return a.value, b.value, c.value
+
+    def set_split(self, split: int) -> None:
+        check(self._L.kvevict_set_split(self.h, split), "kvevict_set_split")
+
+    def stats(self) -> dict:
+        s = Stats()
+        check(self._L.kvevict_get_stats(self.h, ctypes.byref(s)), "kvevict_get_stats")
+        return {f: getattr(s, f) for f, _ in Stats._fields_}
+
+    def check(self) -> int:
+        """Waits for the stream; returns the device error word (0 = clean) and clears it."""
+        w = ctypes.c_uint32(0)
+        rc = self._L.kvevict_check(self.h, ctypes.byref(w))
+        if rc not in (_lib.OK, _lib.ERR_DEVICE):
+            check(rc, "kvevict_check")
+        return w.value

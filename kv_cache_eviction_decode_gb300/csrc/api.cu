@@ -1,0 +1,522 @@
+// api.cu -- host runtime of libkvevict.so: argument checks, the device state
+// layout, per-layer step bookkeeping and the launches. See include/kvevict.h.
+//
+// Every per-layer quantity the kernels need besides the data (how many slots
+// are occupied, where an insert goes before the cache is full, when Random
+// cuts) depends only on the number of prompt tokens and decode steps so far,
+// never on values, so it is tracked here on the host and passed by value.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "aux_kernels.h"
+#include "decode_dispatch.h"
+#include "decode_kernel.cuh"
+#include "kvevict.h"
+
+using namespace kvevict;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kSMs = 152;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    int C = 0, G = 0, elem = 0;
+    size_t units = 0;         // B * Hkv
+    size_t layer_slots = 0;   // units * C
+    size_t kv_layer_bytes = 0;
+    size_t off_k = 0, off_v = 0, off_pos = 0, off_score = 0, off_free = 0, off_err = 0;
+    size_t off_sq = 0, off_sk = 0, off_sv = 0, off_so = 0;
+    size_t total = 0;
+    size_t q_bytes = 0, kvtok_bytes = 0;  // one layer-step's q/out and k_new/v_new
+};
+
+int validate(const kvevict_config *c)
+{
+    if (!c) return KVEVICT_ERR_INVALID_ARG;
+    if (c->batch < 1 || c->batch > 65535 || c->n_layers < 1 || c->n_kv_heads < 1 || c->n_kv_heads > 65535 ||
+        c->n_q_heads < 1)
+        return KVEVICT_ERR_INVALID_ARG;
+    if (c->n_q_heads % c->n_kv_heads) return KVEVICT_ERR_INVALID_ARG;
+    const int G = c->n_q_heads / c->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return KVEVICT_ERR_INVALID_ARG;
+    if (c->head_dim != 64 && c->head_dim != 128) return KVEVICT_ERR_INVALID_ARG;
+    if (c->dtype != KVEVICT_F32 && c->dtype != KVEVICT_BF16) return KVEVICT_ERR_INVALID_ARG;
+    if (c->budget < 1) return KVEVICT_ERR_INVALID_ARG;
+    switch (c->policy) {
+    case KVEVICT_H2O:
+        if (c->n_sink < 0 || c->n_heavy < 0 || c->n_recent < 1 ||
+            static_cast<long long>(c->n_sink) + c->n_heavy + c->n_recent != c->budget)
+            return KVEVICT_ERR_INVALID_ARG;
+        break;
+    case KVEVICT_SINK_WINDOW:
+        if (c->n_sink < 0 || c->n_heavy != 0 || c->n_recent < 1 ||
+            static_cast<long long>(c->n_sink) + c->n_recent != c->budget)
+            return KVEVICT_ERR_INVALID_ARG;
+        break;
+    case KVEVICT_RANDOM:
+        if (c->r < 1 || c->max_prompt < 0 || c->n_sink != 0 || c->n_heavy != 0 || c->n_recent != 0)
+            return KVEVICT_ERR_INVALID_ARG;
+        if (static_cast<long long>(c->budget) + c->r > kMaxRandomCandidates) return KVEVICT_ERR_INVALID_ARG;
+        break;
+    default:
+        return KVEVICT_ERR_INVALID_ARG;
+    }
+    const long long C = c->policy == KVEVICT_RANDOM ? static_cast<long long>(c->max_prompt) + c->budget + c->r
+                                                    : c->budget;
+    if (C > (1 << 24)) return KVEVICT_ERR_INVALID_ARG;
+    return KVEVICT_OK;
+}
+
+Layout make_layout(const kvevict_config *c)
+{
+    Layout L;
+    L.G = c->n_q_heads / c->n_kv_heads;
+    L.elem = c->dtype == KVEVICT_F32 ? 4 : 2;
+    L.C = c->policy == KVEVICT_RANDOM ? c->max_prompt + c->budget + c->r : c->budget;
+    L.units = static_cast<size_t>(c->batch) * c->n_kv_heads;
+    L.layer_slots = L.units * L.C;
+    L.kv_layer_bytes = L.layer_slots * c->head_dim * L.elem;
+    const size_t nl = c->n_layers;
+    size_t off = 0;
+    L.off_k = off; off = align_up(off + nl * L.kv_layer_bytes);
+    L.off_v = off; off = align_up(off + nl * L.kv_layer_bytes);
+    L.off_pos = off; off = align_up(off + nl * L.layer_slots * 4);
+    L.off_score = off; if (c->policy == KVEVICT_H2O) off = align_up(off + nl * L.layer_slots * 4);
+    L.off_free = off; if (c->policy == KVEVICT_RANDOM) off = align_up(off + nl * L.units * c->r * 4);
+    L.off_err = off; off = align_up(off + 16);
+    L.q_bytes = static_cast<size_t>(c->batch) * c->n_q_heads * c->head_dim * L.elem;
+    L.kvtok_bytes = L.units * c->head_dim * L.elem;
+    L.off_sq = off; off = align_up(off + L.q_bytes);
+    L.off_sk = off; off = align_up(off + L.kvtok_bytes);
+    L.off_sv = off; off = align_up(off + L.kvtok_bytes);
+    L.off_so = off; off = align_up(off + L.q_bytes);
+    L.total = off;
+    return L;
+}
+
+struct LayerState {
+    int prompt_len = 0;
+    int t = 0;           // decode steps issued
+    int count = 0;       // tokens held per unit (H2O, sink-window)
+    int n_gen = 0;       // generated tokens held per unit (Random)
+    bool cut_done = false;
+    int fl_idx = 0;      // next free-list entry (Random after a cut)
+    int32_t *trace = nullptr;
+    int trace_len = 0, trace_t = 0;
+};
+
+}  // namespace
+
+struct kvevict_handle {
+    kvevict_config cfg;
+    Layout L;
+    uint8_t *state = nullptr;
+    cudaStream_t stream = nullptr;
+    int split = 1;
+    bool split_auto = true;
+    std::vector<LayerState> layers;
+    kvevict_stats stats{};
+    // decode kernel configured for (split, holes): function, shared memory, zcap
+    struct Configured { int split = 0; DecodeKernelInfo ki{}; size_t smem = 0; int zc = 0; } configured[2];
+};
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return KVEVICT_OK;
+    std::fprintf(stderr, "kvevict: CUDA error %s\n", cudaGetErrorString(e));
+    return KVEVICT_ERR_CUDA;
+}
+
+int auto_split(const kvevict_config &c, const Layout &L)
+{
+    // Enough CTAs for several waves over the 152 SMs, and a few hundred
+    // slots or more per CTA so the pipeline has work to overlap.
+    // Automatic choice stays within portable cluster sizes (<= 8 CTAs).
+    constexpr int kAutoMax = 8;
+    int S = 1;
+    while (S < kAutoMax && (L.C + S - 1) / S > 512) S *= 2;
+    while (S < kAutoMax && static_cast<long long>(L.units) * S < 4LL * kSMs && L.C / (2 * S) >= 128) S *= 2;
+    (void)c;
+    return S;
+}
+
+int max_slots_per_cta(const Layout &L, int S)
+{
+    const int tiles = (L.C + kTile - 1) / kTile;
+    return ((tiles + S - 1) / S) * kTile;
+}
+
+int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInfo *ki, size_t *smem, int *zc)
+{
+    if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, ki)) return KVEVICT_ERR_INVALID_ARG;
+    *zc = ki->zcap(max_slots_per_cta(h->L, S));
+    *smem = ki->smem_bytes(*zc);
+    if (*smem > 227 * 1024) return KVEVICT_ERR_INVALID_ARG;
+    cudaError_t e = cudaFuncSetAttribute(ki->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(*smem));
+    if (e == cudaSuccess && S > 8) e = cudaFuncSetAttribute(ki->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cuda_status(e);
+}
+
+template <typename T> T *at(const kvevict_handle *h, size_t off) { return reinterpret_cast<T *>(h->state + off); }
+
+int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, const void *vn, void *out)
+{
+    const kvevict_config &c = h->cfg;
+    const Layout &L = h->L;
+    LayerState &ls = h->layers[layer];
+
+    DecodeParams P{};
+    P.q = q; P.k_new = kn; P.v_new = vn; P.out = out;
+    P.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
+    P.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
+    P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_slots;
+    P.score = c.policy == KVEVICT_H2O ? at<float>(h, L.off_score) + layer * L.layer_slots : nullptr;
+    P.freelist = c.policy == KVEVICT_RANDOM ? at<int32_t>(h, L.off_free) + layer * L.units * c.r : nullptr;
+    P.freelist_len = c.r;
+    P.err = at<uint32_t>(h, L.off_err);
+    P.Hkv = c.n_kv_heads;
+    P.C = L.C;
+    P.p = ls.prompt_len + ls.t;
+    P.n_sink = c.n_sink;
+    P.n_recent = c.n_recent;
+    P.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
+    P.trace = (ls.trace && ls.trace_t < ls.trace_len) ? ls.trace + static_cast<size_t>(ls.trace_t) * L.units * 4 : nullptr;
+
+    bool holes = false;
+    long long evicted = 0;
+    switch (c.policy) {
+    case KVEVICT_SINK_WINDOW:
+        P.n_active = ls.count;
+        P.mode = kInsertAt;
+        P.dest_slot = P.p < c.n_sink ? P.p : c.n_sink + (P.p - c.n_sink) % c.n_recent;
+        if (ls.count == L.C) evicted = static_cast<long long>(L.units);
+        break;
+    case KVEVICT_H2O:
+        P.n_active = ls.count;
+        if (ls.count < L.C) {
+            P.mode = kInsertAt;
+            P.dest_slot = ls.count;
+        } else {
+            P.mode = kH2OEvict;
+            evicted = static_cast<long long>(L.units);
+        }
+        break;
+    default:  // Random
+        if (!ls.cut_done) {
+            P.n_active = ls.prompt_len + ls.n_gen;
+            P.mode = kInsertAt;
+            P.dest_slot = ls.prompt_len + ls.n_gen;
+        } else {
+            P.n_active = ls.prompt_len + c.budget + c.r;
+            P.mode = kFromFreeList;
+            P.freelist_idx = ls.fl_idx;
+            holes = true;
+        }
+        break;
+    }
+
+    auto &cfgd = h->configured[holes ? 1 : 0];
+    if (cfgd.split != h->split) {
+        int rc0 = configure_kernel(h, h->split, holes, &cfgd.ki, &cfgd.smem, &cfgd.zc);
+        if (rc0) return rc0;
+        cfgd.split = h->split;
+    }
+    const DecodeKernelInfo &ki = cfgd.ki;
+    const size_t smem = cfgd.smem;
+    int rc = KVEVICT_OK;
+    P.split = h->split;
+    P.zcap = cfgd.zc;
+
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(h->split, c.n_kv_heads, c.batch);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = h->stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = h->split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 2;
+    void *args[] = {&P};
+    rc = cuda_status(cudaLaunchKernelExC(&lc, ki.fn, args));
+    if (rc) return rc;
+
+    // Bookkeeping of what the step did.
+    if (P.trace) ls.trace_t++;
+    h->stats.decode_steps++;
+    h->stats.evictions += evicted;
+    switch (c.policy) {
+    case KVEVICT_SINK_WINDOW:
+    case KVEVICT_H2O:
+        ls.count = std::min(L.C, ls.count + 1);
+        break;
+    default:
+        ls.n_gen++;
+        if (ls.cut_done) ls.fl_idx++;
+        if (ls.n_gen == c.budget + c.r) {
+            CutParams cp{};
+            cp.pos = P.pos;
+            cp.freelist = const_cast<int32_t *>(P.freelist);
+            cp.seed = c.seed;
+            cp.layer = layer;
+            cp.step = ls.t;
+            cp.Hkv = c.n_kv_heads;
+            cp.C = L.C;
+            cp.first_slot = ls.prompt_len;
+            cp.n_cand = c.budget + c.r;
+            cp.n_pow2 = 1;
+            while (cp.n_pow2 < cp.n_cand) cp.n_pow2 <<= 1;
+            cp.r = c.r;
+            rc = cuda_status(launch_random_cut(cp, c.batch, h->stream));
+            if (rc) return rc;
+            ls.n_gen = c.budget;
+            ls.cut_done = true;
+            ls.fl_idx = 0;
+            h->stats.cuts++;
+            h->stats.evictions += static_cast<long long>(L.units) * c.r;
+        }
+        break;
+    }
+    ls.t++;
+    return KVEVICT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvevict_state_bytes(const kvevict_config *cfg, size_t *bytes)
+{
+    int rc = validate(cfg);
+    if (rc) return rc;
+    if (!bytes) return KVEVICT_ERR_INVALID_ARG;
+    *bytes = make_layout(cfg).total;
+    return KVEVICT_OK;
+}
+
+int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_t state_bytes, void *cuda_stream)
+{
+    if (!out) return KVEVICT_ERR_INVALID_ARG;
+    *out = nullptr;
+    int rc = validate(cfg);
+    if (rc) return rc;
+    Layout L = make_layout(cfg);
+    if (!state || (reinterpret_cast<uintptr_t>(state) & (kAlign - 1))) return KVEVICT_ERR_INVALID_ARG;
+    if (state_bytes < L.total) return KVEVICT_ERR_CAPACITY;
+    kvevict_handle *h = new (std::nothrow) kvevict_handle();
+    if (!h) return KVEVICT_ERR_CAPACITY;
+    h->cfg = *cfg;
+    h->L = L;
+    h->state = static_cast<uint8_t *>(state);
+    h->stream = static_cast<cudaStream_t>(cuda_stream);
+    h->layers.resize(cfg->n_layers);
+    h->split = auto_split(*cfg, L);
+    // Empty cache: every position -1, every score 0, no error bits.
+    cudaError_t e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_slots * 4, h->stream);
+    if (e == cudaSuccess && cfg->policy == KVEVICT_H2O)
+        e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_slots * 4, h->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_status(e);
+    }
+    h->stats.split = h->split;
+    h->stats.capacity = L.C;
+    *out = h;
+    return KVEVICT_OK;
+}
+
+int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_tokens)
+{
+    if (!h || layer < 0 || layer >= h->cfg.n_layers) return h ? KVEVICT_ERR_STATE : KVEVICT_ERR_INVALID_ARG;
+    if (n_tokens < 0 || (n_tokens > 0 && (!K || !V || !aligned16(K) || !aligned16(V)))) return KVEVICT_ERR_INVALID_ARG;
+    LayerState &ls = h->layers[layer];
+    if (ls.t > 0) return KVEVICT_ERR_STATE;
+    const kvevict_config &c = h->cfg;
+    const Layout &L = h->L;
+    if (c.policy == KVEVICT_RANDOM && static_cast<long long>(ls.prompt_len) + n_tokens > c.max_prompt)
+        return KVEVICT_ERR_CAPACITY;
+    if (static_cast<long long>(ls.prompt_len) + n_tokens > (1LL << 30)) return KVEVICT_ERR_INVALID_ARG;
+    if (n_tokens == 0) return KVEVICT_OK;
+
+    PrefillParams P{};
+    P.K = K; P.V = V;
+    P.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
+    P.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
+    P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_slots;
+    P.score = c.policy == KVEVICT_H2O ? at<float>(h, L.off_score) + layer * L.layer_slots : nullptr;
+    P.n_tok = n_tokens;
+    P.p0 = ls.prompt_len;
+    P.C = L.C;
+    P.Hkv = c.n_kv_heads;
+    P.head_dim = c.head_dim;
+    P.elem_bytes = L.elem;
+    if (c.policy == KVEVICT_RANDOM) {
+        P.n_sink = 0;
+        P.ring_len = 0;
+        P.a0 = 0; P.a1 = n_tokens;
+        P.b0 = P.b1 = 0;
+    } else {
+        P.n_sink = c.n_sink;
+        P.ring_len = L.C - c.n_sink;
+        P.a0 = 0;
+        P.a1 = std::min(n_tokens, std::max(0, c.n_sink - P.p0));
+        P.b0 = std::max({0, c.n_sink - P.p0, n_tokens - P.ring_len});
+        P.b1 = n_tokens;
+        if (P.b0 > P.b1) P.b0 = P.b1;
+    }
+    launch_prefill(P, (P.a1 - P.a0) + (P.b1 - P.b0), c.batch, h->stream);
+    int rc = cuda_status(cudaGetLastError());
+    if (rc) return rc;
+    ls.prompt_len += n_tokens;
+    ls.count = c.policy == KVEVICT_RANDOM ? ls.prompt_len : std::min(L.C, ls.prompt_len);
+    h->stats.prefill_tokens += n_tokens;
+    return KVEVICT_OK;
+}
+
+int kvevict_decode_step(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new, void *out)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out)) return KVEVICT_ERR_INVALID_ARG;
+    if (h->layers[layer].prompt_len + static_cast<long long>(h->layers[layer].t) >= (1LL << 31) - 1)
+        return KVEVICT_ERR_STATE;
+    return launch_decode(h, layer, q, k_new, v_new, out);
+}
+
+int kvevict_decode_step_host(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new, void *out)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
+    const Layout &L = h->L;
+    void *dq = h->state + L.off_sq, *dk = h->state + L.off_sk, *dv = h->state + L.off_sv, *dout = h->state + L.off_so;
+    cudaError_t e = cudaMemcpyAsync(dq, q, L.q_bytes, cudaMemcpyHostToDevice, h->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k_new, L.kvtok_bytes, cudaMemcpyHostToDevice, h->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v_new, L.kvtok_bytes, cudaMemcpyHostToDevice, h->stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    int rc = launch_decode(h, layer, dq, dk, dv, dout);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(out, dout, L.q_bytes, cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    return cuda_status(e);
+}
+
+int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_device)
+{
+    if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    const Layout &L = h->L;
+    const void *src = at<int32_t>(h, L.off_pos) + layer * L.layer_slots;
+    cudaError_t e = cudaMemcpyAsync(dst, src, L.layer_slots * 4,
+                                    dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
+    return cuda_status(e);
+}
+
+int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
+{
+    if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
+    if (h->cfg.policy != KVEVICT_H2O) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    const Layout &L = h->L;
+    const void *src = at<float>(h, L.off_score) + layer * L.layer_slots;
+    cudaError_t e = cudaMemcpyAsync(dst, src, L.layer_slots * 4,
+                                    dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
+    return cuda_status(e);
+}
+
+int kvevict_set_trace(kvevict_t h, int layer, int32_t *dev_buf, int n_steps)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    if (dev_buf && (n_steps < 0 || !aligned16(dev_buf))) return KVEVICT_ERR_INVALID_ARG;
+    LayerState &ls = h->layers[layer];
+    ls.trace = dev_buf;
+    ls.trace_len = dev_buf ? n_steps : 0;
+    ls.trace_t = 0;
+    return KVEVICT_OK;
+}
+
+int kvevict_layer_state(kvevict_t h, int layer, int *prompt_len, int *steps, int *count)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    const LayerState &ls = h->layers[layer];
+    if (prompt_len) *prompt_len = ls.prompt_len;
+    if (steps) *steps = ls.t;
+    if (count) *count = h->cfg.policy == KVEVICT_RANDOM ? ls.prompt_len + ls.n_gen : ls.count;
+    return KVEVICT_OK;
+}
+
+int kvevict_set_split(kvevict_t h, int split)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (split == 0) {
+        h->split = auto_split(h->cfg, h->L);
+    } else {
+        if (split < 1 || split > kMaxSplit || (split & (split - 1))) return KVEVICT_ERR_INVALID_ARG;
+        DecodeKernelInfo ki;
+        if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, false, &ki)) return KVEVICT_ERR_INVALID_ARG;
+        if (ki.smem_bytes(ki.zcap(max_slots_per_cta(h->L, split))) > 227 * 1024) return KVEVICT_ERR_INVALID_ARG;
+        h->split = split;
+    }
+    h->stats.split = h->split;
+    return KVEVICT_OK;
+}
+
+int kvevict_get_stats(kvevict_t h, kvevict_stats *out)
+{
+    if (!h || !out) return KVEVICT_ERR_INVALID_ARG;
+    *out = h->stats;
+    return KVEVICT_OK;
+}
+
+int kvevict_check(kvevict_t h, uint32_t *device_error)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    uint32_t w = 0;
+    e = cudaMemcpy(&w, h->state + h->L.off_err, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->state + h->L.off_err, 0, 4, h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (device_error) *device_error = w;
+    return w ? KVEVICT_ERR_DEVICE : KVEVICT_OK;
+}
+
+const char *kvevict_strerror(int code)
+{
+    switch (code) {
+    case KVEVICT_OK: return "ok";
+    case KVEVICT_ERR_INVALID_ARG: return "invalid argument";
+    case KVEVICT_ERR_CAPACITY: return "capacity exceeded";
+    case KVEVICT_ERR_STATE: return "call out of order or layer out of range";
+    case KVEVICT_ERR_CUDA: return "CUDA runtime error";
+    case KVEVICT_ERR_DEVICE: return "device error bits set";
+    default: return "unknown status";
+    }
+}
+
+void kvevict_destroy(kvevict_t h) { delete h; }
+
+}  // extern "C"

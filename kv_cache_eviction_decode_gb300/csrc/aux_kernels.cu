@@ -1,0 +1,141 @@
+// aux_kernels.cu -- prompt prefill and the Random Attention periodic cut.
+#include "aux_kernels.h"
+#include "device_common.cuh"
+
+namespace kvevict {
+
+// ---------------------------------------------------------------- prefill
+// Prompt tokens enter with score 0 and no attention. For H2O (all scores
+// equal, ties to the older position) and StreamingLLM that keeps the first
+// n_sink positions in slots 0..n_sink-1 and the newest C - n_sink in ring
+// order: slot(p) = n_sink + (p - n_sink) mod (C - n_sink). Random keeps every
+// prompt token: slot(p) = p. Rows of this chunk: range A = [a0, a1) (sinks or,
+// for Random, everything), range B = [b0, b1) (kept ring rows). One warp per
+// row, 16-byte vector copies.
+__global__ void __launch_bounds__(256) prefill_kernel(const PrefillParams P)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int idx = blockIdx.x * 8 + warp;
+    const int na = P.a1 - P.a0;
+    int i;
+    if (idx < na) i = P.a0 + idx;
+    else if (idx - na < P.b1 - P.b0) i = P.b0 + (idx - na);
+    else return;
+    const int p = P.p0 + i;
+    const int slot = (P.ring_len > 0 && p >= P.n_sink) ? P.n_sink + (p - P.n_sink) % P.ring_len : p;
+    const size_t unit = static_cast<size_t>(blockIdx.z) * P.Hkv + blockIdx.y;
+    const size_t row_bytes = static_cast<size_t>(P.head_dim) * P.elem_bytes;
+    const int vecs = static_cast<int>(row_bytes / 16);
+    const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.K) +
+                                                      (unit * P.n_tok + i) * row_bytes);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.V) +
+                                                      (unit * P.n_tok + i) * row_bytes);
+    uint4 *kd = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.kc) + (unit * P.C + slot) * row_bytes);
+    uint4 *vd = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.vc) + (unit * P.C + slot) * row_bytes);
+    for (int v = lane; v < vecs; v += 32) {
+        kd[v] = ks[v];
+        vd[v] = vs[v];
+    }
+    if (lane == 0) {
+        P.pos[unit * P.C + slot] = p;
+        if (P.score) P.score[unit * P.C + slot] = 0.f;
+    }
+}
+
+// ------------------------------------------------------------ random cut
+// Random Attention ("Random Attention" summary, 方法): the prompt is kept;
+// when a unit holds K + r generated tokens, each unit independently evicts r
+// of them uniformly at random. Every generated token gets a fresh 64-bit
+// Philox key for this step; the r smallest (key, position) leave. One CTA per
+// unit: keys into shared memory, bitonic sort of (key, position << 32 | slot),
+// then the r freed slots are written to the unit's free list in ascending
+// slot order (the next r decode steps fill them lowest first).
+__global__ void __launch_bounds__(kCutThreads) random_cut_kernel(const CutParams P)
+{
+    extern __shared__ __align__(16) uint64_t cut_smem[];
+    uint64_t *key = cut_smem;
+    uint64_t *aux = cut_smem + P.n_pow2;
+    int32_t *freed = reinterpret_cast<int32_t *>(cut_smem + 2 * static_cast<size_t>(P.n_pow2));
+    const int tid = threadIdx.x;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const size_t unit = static_cast<size_t>(b) * P.Hkv + h;
+    int32_t *pos = P.pos + unit * P.C;
+
+    grid_dependency_wait();
+
+    for (int i = tid; i < P.n_pow2; i += blockDim.x) {
+        if (i < P.n_cand) {
+            const int slot = P.first_slot + i;
+            const int32_t ps = pos[slot];
+            key[i] = random_evict_key(P.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(P.layer),
+                                      static_cast<uint32_t>(h), static_cast<uint32_t>(P.step),
+                                      static_cast<uint32_t>(ps));
+            aux[i] = (static_cast<uint64_t>(static_cast<uint32_t>(ps)) << 32) | static_cast<uint32_t>(slot);
+        } else {
+            key[i] = ~0ull;
+            aux[i] = ~0ull;
+        }
+    }
+    __syncthreads();
+    // Bitonic sort, ascending by (key, aux).
+    for (int k = 2; k <= P.n_pow2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < P.n_pow2; i += blockDim.x) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const bool up = (i & k) == 0;
+                    const uint64_t ka = key[i], kb = key[ixj], xa = aux[i], xb = aux[ixj];
+                    const bool a_gt_b = ka > kb || (ka == kb && xa > xb);
+                    if (a_gt_b == up) {
+                        key[i] = kb; key[ixj] = ka;
+                        aux[i] = xb; aux[ixj] = xa;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = tid; i < P.r; i += blockDim.x) freed[i] = static_cast<int32_t>(aux[i] & 0xFFFFFFFFu);
+    __syncthreads();
+    // Ascending slot order by rank counting (slots are distinct).
+    for (int i = tid; i < P.r; i += blockDim.x) {
+        const int32_t s = freed[i];
+        int rnk = 0;
+        for (int j = 0; j < P.r; ++j) rnk += freed[j] < s;
+        P.freelist[unit * P.r + rnk] = s;
+        pos[s] = -1;
+    }
+}
+
+void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st)
+{
+    if (rows <= 0) return;
+    dim3 grid((rows + 7) / 8, p.Hkv, B);
+    prefill_kernel<<<grid, 256, 0, st>>>(p);
+}
+
+size_t cut_smem_bytes(int n_pow2, int r)
+{
+    return 2 * sizeof(uint64_t) * static_cast<size_t>(n_pow2) + sizeof(int32_t) * static_cast<size_t>(r);
+}
+
+cudaError_t launch_random_cut(const CutParams &p, int B, cudaStream_t st)
+{
+    const size_t smem = cut_smem_bytes(p.n_pow2, p.r);
+    cudaError_t e = cudaFuncSetAttribute(random_cut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.Hkv, B, 1);
+    cfg.blockDim = dim3(kCutThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, random_cut_kernel, p);
+}
+
+}  // namespace kvevict

@@ -1,0 +1,35 @@
+// aux_kernels.h -- host-visible parameters of the prefill and Random-cut kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvevict {
+
+constexpr int kCutThreads = 512;
+constexpr int kMaxRandomCandidates = 8192;  // K + r, sorted in shared memory
+
+struct PrefillParams {
+    const void *K, *V;  // [B][Hkv][n_tok][D]
+    void *kc, *vc;      // layer cache [B][Hkv][C][D]
+    int32_t *pos;
+    float *score;       // or null
+    int n_tok, p0, C, Hkv, head_dim, elem_bytes;
+    int n_sink, ring_len;  // ring_len = C - n_sink for ring policies, 0 for Random
+    int a0, a1, b0, b1;    // chunk rows to copy
+};
+
+struct CutParams {
+    int32_t *pos;       // layer [B][Hkv][C]
+    int32_t *freelist;  // layer [B][Hkv][r]
+    uint64_t seed;
+    int layer, step, Hkv, C;
+    int first_slot, n_cand, n_pow2, r;
+};
+
+void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st);
+size_t cut_smem_bytes(int n_pow2, int r);
+cudaError_t launch_random_cut(const CutParams &p, int B, cudaStream_t st);
+
+}  // namespace kvevict

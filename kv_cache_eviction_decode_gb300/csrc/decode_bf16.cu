@@ -1,0 +1,35 @@
+// decode_bf16.cu -- decode-step kernel instantiations for __nv_bfloat16 caches.
+#include "decode_dispatch.h"
+#include "decode_kernel.cuh"
+
+namespace kvevict {
+namespace {
+
+template <int D, int G, bool H> DecodeKernelInfo info()
+{
+    using L = DecodeLayout<__nv_bfloat16, D, G>;
+    return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<__nv_bfloat16, D, G, H>),
+                            [](int zc) { return L::bytes(zc); }, [](int n) { return L::zcap(n); }};
+}
+
+template <int D, bool H> bool pick_g(int G, DecodeKernelInfo *out)
+{
+    switch (G) {
+    case 1: *out = info<D, 1, H>(); return true;
+    case 2: *out = info<D, 2, H>(); return true;
+    case 4: *out = info<D, 4, H>(); return true;
+    case 8: *out = info<D, 8, H>(); return true;
+    default: return false;
+    }
+}
+
+}  // namespace
+
+bool decode_kernel_bf16(int head_dim, int G, bool holes, DecodeKernelInfo *out)
+{
+    if (head_dim == 64) return holes ? pick_g<64, true>(G, out) : pick_g<64, false>(G, out);
+    if (head_dim == 128) return holes ? pick_g<128, true>(G, out) : pick_g<128, false>(G, out);
+    return false;
+}
+
+}  // namespace kvevict

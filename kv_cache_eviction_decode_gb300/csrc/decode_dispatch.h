@@ -1,0 +1,24 @@
+// decode_dispatch.h -- lookup of the decode-step kernel instantiation for a
+// (dtype, head_dim, group size, holes) combination.
+#pragma once
+
+#include <cstddef>
+
+namespace kvevict {
+
+struct DecodeKernelInfo {
+    const void *fn;                    // __global__ decode_step_kernel<...>
+    size_t (*smem_bytes)(int zcap);    // dynamic shared memory for a given zcap
+    int (*zcap)(int max_slots_per_cta);
+};
+
+// dtype: 0 fp32, 1 bf16. Returns false if the combination is not built.
+bool decode_kernel_f32(int head_dim, int G, bool holes, DecodeKernelInfo *out);
+bool decode_kernel_bf16(int head_dim, int G, bool holes, DecodeKernelInfo *out);
+
+inline bool decode_kernel(int dtype, int head_dim, int G, bool holes, DecodeKernelInfo *out)
+{
+    return dtype == 0 ? decode_kernel_f32(head_dim, G, holes, out) : decode_kernel_bf16(head_dim, G, holes, out);
+}
+
+}  // namespace kvevict

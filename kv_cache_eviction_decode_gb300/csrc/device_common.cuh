@@ -1,0 +1,247 @@
+// device_common.cuh -- small inline-PTX helpers for sm_103a: mbarriers, bulk
+// (TMA) global->shared copies, thread-block-cluster barriers and distributed
+// shared memory, the global timer used to bound every wait, and the device
+// Philox4x64-10 generator.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kvevict.h"
+
+namespace kvevict {
+
+// Every spin on an mbarrier gives up after this long and reports
+// KVEVICT_DEV_WAIT_TIMEOUT instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; false after
+// kWaitLimitNs (the caller then records KVEVICT_DEV_WAIT_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ------------------------------------------------------ bulk (TMA) copies
+// Contiguous global -> shared copy by the tensor-memory-access unit; the
+// bytes complete on `bar`. dst and src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Same, with an L2 evict-first hint: each KV byte is read once per step.
+__device__ __forceinline__ void bulk_g2s_stream(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                                uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// ------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Full cluster barrier: every thread of every CTA in the cluster; release
+// and acquire order shared and global memory at cluster scope.
+__device__ __forceinline__ void cluster_sync()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void *local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t ld_peer_u64(uint32_t addr)
+{
+    uint64_t v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int32_t ld_peer_s32(uint32_t addr)
+{
+    int32_t v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ----------------------------------------------- programmatic dependent launch
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Consumer-warps-only barrier (named barrier 1).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------- elements
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    __device__ __forceinline__ static float to_f32(float x) { return x; }
+    __device__ __forceinline__ static float from_f32(float x) { return x; }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    __device__ __forceinline__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+    __device__ __forceinline__ static __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
+};
+
+// Loads N consecutive elements at p (N * sizeof(T) bytes, naturally aligned)
+// as fp32. One vector load for the sizes used here (4..16 bytes).
+template <typename T, int N> __device__ __forceinline__ void load_f32(const T *p, float (&out)[N]);
+
+template <> __device__ __forceinline__ void load_f32<float, 2>(const float *p, float (&o)[2])
+{
+    float2 v = *reinterpret_cast<const float2 *>(p);
+    o[0] = v.x; o[1] = v.y;
+}
+template <> __device__ __forceinline__ void load_f32<float, 4>(const float *p, float (&o)[4])
+{
+    float4 v = *reinterpret_cast<const float4 *>(p);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float &lo, float &hi)
+{
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+}
+template <> __device__ __forceinline__ void load_f32<__nv_bfloat16, 2>(const __nv_bfloat16 *p, float (&o)[2])
+{
+    uint32_t w = *reinterpret_cast<const uint32_t *>(p);
+    bf16x2_to_f32(w, o[0], o[1]);
+}
+template <> __device__ __forceinline__ void load_f32<__nv_bfloat16, 4>(const __nv_bfloat16 *p, float (&o)[4])
+{
+    uint2 w = *reinterpret_cast<const uint2 *>(p);
+    bf16x2_to_f32(w.x, o[0], o[1]);
+    bf16x2_to_f32(w.y, o[2], o[3]);
+}
+
+// ------------------------------------------------------------ Philox4x64-10
+// Counter-based generator of Salmon et al., "Parallel Random Numbers: As Easy
+// as 1, 2, 3" (SC'11): ten rounds of two 64x64->128 multiplies with a Weyl
+// sequence added to the key between rounds.
+struct U64x4 { uint64_t x, y, z, w; };
+
+__device__ __forceinline__ U64x4 philox4x64_10(U64x4 c, uint64_t k0, uint64_t k1)
+{
+    constexpr uint64_t kMul0 = 0xD2E7470EE14C6C93ull, kMul1 = 0xCA5A826395121157ull;
+    constexpr uint64_t kWeyl0 = 0x9E3779B97F4A7C15ull, kWeyl1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t hi_a = __umul64hi(kMul0, c.x), lo_a = kMul0 * c.x;
+        const uint64_t hi_b = __umul64hi(kMul1, c.z), lo_b = kMul1 * c.z;
+        c = U64x4{hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a};
+        k0 += kWeyl0;
+        k1 += kWeyl1;
+    }
+    return c;
+}
+
+// Eviction key of one generated token at one Random Attention cut: counter
+// (position, step, layer * 2^16 + KV head, sequence), key (seed, 0x5EED0001),
+// first output word.
+constexpr uint64_t kRandomKeyTag = 0x5EED0001ull;
+
+__device__ __forceinline__ uint64_t random_evict_key(uint64_t seed, uint32_t seq, uint32_t layer, uint32_t head,
+                                                     uint32_t step, uint32_t pos)
+{
+    U64x4 c{pos, step, (static_cast<uint64_t>(layer) << 16) + head, seq};
+    return philox4x64_10(c, seed, kRandomKeyTag).x;
+}
+
+}  // namespace kvevict

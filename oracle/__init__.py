@@ -62,6 +62,8 @@ def lib():
             L.orc_slot_kv.argtypes = [P, I, P, P]
             L.orc_attend.argtypes = [P, P, P, P, P]
             L.orc_attend.restype = I
+            L.orc_stage.argtypes = [P, P, P]
+            L.orc_stage.restype = I
             L.orc_choose.argtypes = [P]
             L.orc_choose.restype = I
             L.orc_commit.argtypes = [P, I]
@@ -126,6 +128,13 @@ class Unit:
         if rc:
             raise RuntimeError(f"oracle attend failed: {rc}")
         return out
+
+    def stage(self, k_new, v_new) -> None:
+        """Stage a decode token without attention (sink-window and Random only)."""
+        k, v = _f32(k_new), _f32(v_new)
+        rc = self._L.orc_stage(self.h, _ptr(k), _ptr(v))
+        if rc:
+            raise RuntimeError(f"oracle stage failed: {rc}")
 
     def choose(self) -> int:
         s = self._L.orc_choose(self.h)

@@ -273,6 +273,23 @@ int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_n
     return ORC_OK;
 }
 
+/* Stages a decode token without computing attention. Only for the
+ * policies whose retained set never depends on attention (StreamingLLM,
+ * Random): their slot tables can then be replayed cheaply over long traces,
+ * with orc_attend used only at the steps whose outputs are compared. */
+int orc_stage(orc_unit *u, const float *k_new, const float *v_new)
+{
+    if (u->have_new) return ORC_ESTATE;
+    if (u->policy == ORC_H2O) return ORC_EINVAL;
+    memcpy(u->k_new, k_new, sizeof(float) * (size_t)u->d);
+    memcpy(u->v_new, v_new, sizeof(float) * (size_t)u->d);
+    u->new_pos = u->prompt_len + u->t;
+    u->is_prompt = 0;
+    u->score_new = 0.0;
+    u->have_new = 1;
+    return ORC_OK;
+}
+
 /* A prompt token is admitted like a decode token, with score 0 and no
  * attention. */
 static int stage_prompt_token(orc_unit *u, const float *k, const float *v)
