@@ -1,0 +1,417 @@
+"""Decode throughput with eviction on one GB300 (or N replicas under torchrun).
+
+A step is one token for the whole batch through every layer: n_layers calls
+of kvevict_decode_step (attention + score + evict + in-place insert), each one
+kernel launch (Random adds a cut launch every r steps). Inputs for the timed
+steps are generated on the device beforehand; the per-layer KV working set
+(>1 GB for the default workload) is far larger than the 129 MB L2, so no L2
+flush is needed between steps.
+
+Default workload: StreamingLLM sink + window (4 + 1020 slots), bf16, B=64,
+32 layers x 32 heads, head_dim 128, steady state (cache full).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import configs, synth, traffic  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+CSRC = os.path.join(ROOT, "kv_cache_eviction_decode_gb300", "csrc")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from a committed ncu capture, or None if
+    absent or taken on other kernel sources."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (one process per GPU; replicas, no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on the host cores, on a sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(w, n_units: int, target_s: float, max_steps: int = 4096):
+    """Times the oracle on n_units units of one layer, already in steady state
+    (prompt or fill built by the oracle's own prefill), over as many decode
+    steps as fit ~target_s. Returns (unit_steps_per_s, threads, description, seconds)."""
+    import numpy as np
+    import oracle
+    P = w.prompt_len if w.prompt_len else w.capacity  # stream-from-empty workloads: fill the cache first
+    ids = []
+    for i in range(n_units):
+        seq, h = divmod(i, w.n_kv_heads)
+        ids.append((seq % w.batch, h))
+    units = []
+    for seq, h in ids:
+        x = synth.UnitInputs(w, seq, 0, h, 1, P)
+        u = oracle.Unit.for_workload(w, seq, 0, h)
+        u.prefill(x.prompt_k, x.prompt_v)
+        if w.policy == configs.POLICY_RANDOM:  # reach the post-cut steady state with staged tokens
+            z = np.zeros(w.head_dim, np.float32)
+            for _ in range(w.budget + w.r):
+                u.stage(z, z)
+                u.commit(u.choose())
+        units.append(u)
+    threads = min(oracle.online_cores(), n_units)
+
+    def timed(xs, a, b):
+        q = np.stack([x.q[a:b] for x in xs])
+        k = np.stack([x.k_new[a:b] for x in xs])
+        v = np.stack([x.v_new[a:b] for x in xs])
+        t0 = time.perf_counter()
+        oracle.run(units, q, k, v, n_threads=threads)
+        return time.perf_counter() - t0
+
+    xs = [synth.UnitInputs(w, seq, 0, h, 1, P) for seq, h in ids]
+    one = timed(xs, 0, 1)
+    M = int(max(1, min(max_steps, target_s / max(one, 1e-6))))
+    xs = [synth.UnitInputs(w, seq, 0, h, 1 + M, P) for seq, h in ids]
+    dt = timed(xs, 1, 1 + M)
+    desc = (f"{n_units} units of one layer (of {w.batch * w.n_kv_heads} per layer, {w.n_layers} layers) "
+            f"x {M} decode steps from a full cache, {dt:.1f} s")
+    return n_units * M / dt, threads, desc, dt
+
+
+def cpu_tokens_per_s(w, unit_steps_per_s: float) -> float:
+    units_per_token_step = w.batch * w.n_kv_heads * w.n_layers
+    return unit_steps_per_s / units_per_token_step * w.batch
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def steady_state(cache, w, device):
+    """Brings every layer to the workload's steady state before timing."""
+    import torch
+    if w.policy == configs.POLICY_SINK_WINDOW and w.prompt_len == 0:
+        # The sink-window state depends on positions only: a full cache from
+        # the prefill of the first C tokens equals C streamed decode steps.
+        P = w.capacity
+    else:
+        P = w.prompt_len
+    for layer in range(w.n_layers):
+        if P:
+            K, V = synth.device_prompt(w, layer, device, P)
+            cache.prefill(layer, K, V)
+            del K, V
+    torch.cuda.synchronize(device)
+    return P
+
+
+def run_ours(args, w, rank, world, device):
+    import torch
+    from kv_cache_eviction_decode_gb300 import KVEvictCache, lib
+
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        cache = KVEvictCache.from_workload(w, device=device, stream=stream)
+        if args.split:
+            cache.set_split(args.split)
+        P = steady_state(cache, w, device)
+        L, B, Hq, Hkv, D = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+        n_pre = 0
+        if w.policy == configs.POLICY_RANDOM:  # pass the first cut
+            n_pre = w.budget + w.r
+        n_win = args.warmup + args.steps
+        q, kn, vn = synth.device_window(w, P + n_pre, n_win, device)
+        out = torch.empty((2, L, B, Hq, D), dtype=q.dtype, device=device)
+        Lb = lib()
+        h = cache.h
+        dec = Lb.kvevict_decode_step
+
+        def token_step(s):
+            for layer in range(L):
+                rc = dec(h, layer, q[s, layer].data_ptr(), kn[s, layer].data_ptr(), vn[s, layer].data_ptr(),
+                         out[s & 1, layer].data_ptr())
+                if rc:
+                    raise RuntimeError(f"kvevict_decode_step failed: {rc}")
+
+        for i in range(n_pre):  # Random: generated tokens up to the first cut
+            token_step(i % n_win)
+        for s in range(args.warmup):
+            token_step(s)
+        stream.synchronize()
+        launches_before = cache.stats()
+        barrier(device)
+        torch.cuda.synchronize(device)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(device.index) as clk:
+            ev0.record(stream)
+            for s in range(args.warmup, n_win):
+                token_step(s)
+            ev1.record(stream)
+            ev1.synchronize()
+        torch.cuda.synchronize(device)
+        barrier(device)
+        err = cache.check()
+        if err:
+            raise RuntimeError(f"device error word {err:#x}")
+        st = cache.stats()
+        dt_ms = ev0.elapsed_time(ev1)
+        dt_ms = reduce_max(dt_ms, device)
+        decode_launches = st["decode_steps"] - launches_before["decode_steps"]
+        cut_launches = st["cuts"] - launches_before["cuts"]
+
+        # isolated kernel time of single launches (events around each), for context
+        iso = []
+        for s in range(min(8, n_win)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dec(h, s % L, q[s, s % L].data_ptr(), kn[s, s % L].data_ptr(), vn[s, s % L].data_ptr(),
+                out[0, 0].data_ptr())
+            e1.record(stream)
+            e1.synchronize()
+            iso.append(e0.elapsed_time(e1))
+
+        # end to end through the host-buffer C-ABI call
+        e2e = None
+        if not args.no_e2e:
+            qh = q[:2].cpu().pin_memory()
+            kh = kn[:2].cpu().pin_memory()
+            vh = vn[:2].cpu().pin_memory()
+            oh = torch.empty((L, B, Hq, D), dtype=q.dtype).pin_memory()
+            dech = Lb.kvevict_decode_step_host
+            n_e2e = max(2, min(args.steps, 10))
+            barrier(device)
+            torch.cuda.synchronize(device)
+            t0 = time.perf_counter()
+            for s in range(n_e2e):
+                for layer in range(L):
+                    rc = dech(h, layer, qh[s & 1, layer].data_ptr(), kh[s & 1, layer].data_ptr(),
+                              vh[s & 1, layer].data_ptr(), oh[layer].data_ptr())
+                    if rc:
+                        raise RuntimeError(f"kvevict_decode_step_host failed: {rc}")
+            e2e_s = reduce_max(time.perf_counter() - t0, device)
+            h2d = L * (q[0, 0].numel() + kn[0, 0].numel() + vn[0, 0].numel()) * q.element_size()
+            d2h = L * out[0, 0].numel() * q.element_size()
+            e2e = {"value": world * B * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "steps": n_e2e}
+        cache.close()
+    return dict(dt_ms=dt_ms, clocks=clk.summary(), decode_launches=decode_launches, cut_launches=cut_launches,
+                iso_ms=iso, e2e=e2e, split=st["split"])
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="sink_window")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--split", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small profiling captures only; the line then names it)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    w = configs.get(args.workload)
+    if args.layers:
+        w = w.with_(n_layers=args.layers, name=f"{w.name}_layers{args.layers}")
+    rank, world, local = dist_env()
+    metric = "decode tokens/s/GPU with eviction; attn+score+evict HBM GB/s vs 8 TB/s roofline"
+    dtype = "bf16" if w.dtype == configs.DTYPE_BF16 else "f32"
+    cfg = {"workload": w.name, "policy": configs.POLICY_NAMES[w.policy], "batch": w.batch, "layers": w.n_layers,
+           "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "budget": w.budget,
+           "n_sink": w.n_sink, "n_heavy": w.n_heavy, "n_recent": w.n_recent, "r": w.r,
+           "prompt_len": w.prompt_len, "capacity_slots": w.capacity,
+           "l2": "inputs larger than L2 (KV of one layer-step %.2f GB)" % (traffic.steady_layer_step_bytes(w) / 1e9)}
+
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle, timed as it stands on the host
+        # cores; rank 0 only.
+        if rank != 0:
+            return
+        rate, threads, desc, dt = oracle_sample_rate(w, n_units=min(64, w.batch * w.n_kv_heads),
+                                                     target_s=max(1.0, args.cpu_seconds / 2))
+        vals = []
+        for _ in range(max(1, min(args.steps, 3))):
+            r, threads, desc, dt = oracle_sample_rate(w, n_units=min(64, w.batch * w.n_kv_heads),
+                                                      target_s=max(1.0, args.cpu_seconds / 2))
+            vals.append(cpu_tokens_per_s(w, r))
+        v = statistics.median(vals)
+        print(json.dumps({"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 1,
+                          "steps": len(vals), "warmup": 1, "ms_per_step": 1000.0 * w.batch / v,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": cfg,
+                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                           "sample": desc},
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    device = torch.device(f"cuda:{local}")
+    r = run_ours(args, w, rank, world, device)
+
+    dt_s = r["dt_ms"] / 1e3
+    tokens = world * w.batch * args.steps
+    value = tokens / dt_s
+    launches = r["decode_launches"]
+    avg_launch_s = dt_s / max(1, launches)
+    layer_bytes = traffic.steady_layer_step_bytes(w)
+    achieved = layer_bytes / avg_launch_s / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    out = {
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["dt_ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+        "data": "synthetic (seeded N(0,1) Q/K/V with hub and sink keys, generated on the device)",
+        "config": dict(cfg, split=r["split"], timing="CUDA events on the launching stream; no L2 flush needed"),
+        "layer_step_us": 1e6 * avg_launch_s,
+        "kernel_us_isolated": 1e3 * statistics.median(r["iso_ms"]) if r["iso_ms"] else None,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": profiled_traffic(w.name), "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": layer_bytes,
+                     "frac_of_8TBs": achieved / 8000.0,
+                     "note": "avg launch duration = timed region / decode launches (includes launch gaps)"},
+        "gpu_launches": launches + r["cut_launches"],
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, desc, _ = oracle_sample_rate(w, n_units=min(64, w.batch * w.n_kv_heads),
+                                                    target_s=args.cpu_seconds)
+        out["cpu_baseline"] = {"value": cpu_tokens_per_s(w, rate), "unit": "tokens/s", "cores": threads,
+                               "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

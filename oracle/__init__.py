@@ -57,6 +57,8 @@ def lib():
             L.orc_evicted_mass.restype = D
             L.orc_new_score.argtypes = [P]
             L.orc_new_score.restype = D
+            L.orc_pos_at.argtypes = [P, I]
+            L.orc_pos_at.restype = ctypes.c_int32
             L.orc_positions.argtypes = [P, P]
             L.orc_scores.argtypes = [P, P]
             L.orc_slot_kv.argtypes = [P, I, P, P]
@@ -158,6 +160,9 @@ class Unit:
         a = np.empty(self.cap, dtype=np.int32)
         self._L.orc_positions(self.h, _ptr(a))
         return a
+
+    def pos_at(self, slot: int) -> int:
+        return int(self._L.orc_pos_at(self.h, int(slot)))
 
     def scores(self) -> np.ndarray:
         a = np.empty(self.cap, dtype=np.float64)

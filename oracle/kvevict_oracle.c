@@ -192,6 +192,11 @@ void orc_slot_kv(const orc_unit *u, int slot, float *k, float *v)
     memcpy(v, u->v + (size_t)slot * u->d, sizeof(float) * (size_t)u->d);
 }
 
+int32_t orc_pos_at(const orc_unit *u, int slot)
+{
+    return (slot >= 0 && slot < u->cap) ? u->pos[slot] : -2;
+}
+
 int orc_count(const orc_unit *u)
 {
     int n = 0;

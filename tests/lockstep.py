@@ -158,18 +158,17 @@ def replay_unit(w: Workload, unit, x, run: GpuRun, n_steps: int, out_steps=None,
             u.stage(x.k_new[t] if x is not None else zero, x.v_new[t] if x is not None else zero)
         slot = u.choose()
         gslot, gold = int(tr[t, 0]), int(tr[t, 1])
-        before = u.positions()
         if gslot != slot:
             assert w.policy == POLICY_H2O, f"{unit} step {t}: GPU slot {gslot}, oracle slot {slot}"
             sc = u.scores()
             a, b = sc[slot], sc[gslot]
             rel = abs(a - b) / max(a, b, 1e-300)
             assert 0 <= gslot < u.cap and rel < NEAR_TIE_REL, \
-                f"{unit} step {t}: GPU evicted slot {gslot} (pos {before[gslot]}, score {b:.9g}), " \
-                f"oracle slot {slot} (pos {before[slot]}, score {a:.9g}), rel {rel:.3e}"
+                f"{unit} step {t}: GPU evicted slot {gslot} (pos {u.pos_at(gslot)}, score {b:.9g}), " \
+                f"oracle slot {slot} (pos {u.pos_at(slot)}, score {a:.9g}), rel {rel:.3e}"
             rep.near_ties += 1
             slot = gslot
-        assert gold == before[slot], f"{unit} step {t}: GPU evicted position {gold}, oracle {before[slot]}"
+        assert gold == u.pos_at(slot), f"{unit} step {t}: GPU evicted position {gold}, oracle {u.pos_at(slot)}"
         u.commit(slot)
         if t in snaps:
             np.testing.assert_array_equal(u.positions(), snaps[t][seq, h].numpy(), err_msg=f"{unit} table, step {t}")
