@@ -113,6 +113,7 @@ typedef struct {
     int64_t cuts;           /* Random cuts, summed over layers (each cuts every unit of the layer) */
     int split;              /* CTAs per unit in the decode launch (thread-block cluster size) */
     int capacity;           /* slots per unit */
+    int clusters;           /* clusters in the last decode launch's persistent grid (0 before any) */
 } kvevict_stats;
 
 /* Bytes of device memory a handle with this configuration needs (cache,
@@ -182,6 +183,12 @@ int kvevict_layer_state(kvevict_t h, int layer, int *prompt_len, int *steps, int
 /* CTAs per unit of the decode launch (1, 2, 4, 8 or 16; 0 = automatic).
  * A tuning knob: results do not depend on it beyond fp32 rounding order. */
 int kvevict_set_split(kvevict_t h, int split);
+
+/* Number of clusters in the decode launch's persistent grid (each cluster
+ * loops over units; 0 = automatic: as many as fit on the GPU at once, chosen
+ * to divide the units evenly where possible). A tuning knob like
+ * kvevict_set_split; results do not depend on it. */
+int kvevict_set_clusters(kvevict_t h, int clusters);
 
 int kvevict_get_stats(kvevict_t h, kvevict_stats *out);
 

@@ -143,6 +143,9 @@ class KVEvictCache:
     def set_split(self, split: int) -> None:
         check(self._L.kvevict_set_split(self.h, split), "kvevict_set_split")
 
+    def set_clusters(self, clusters: int) -> None:
+        check(self._L.kvevict_set_clusters(self.h, clusters), "kvevict_set_clusters")
+
     def stats(self) -> dict:
         s = Stats()
         check(self._L.kvevict_get_stats(self.h, ctypes.byref(s)), "kvevict_get_stats")

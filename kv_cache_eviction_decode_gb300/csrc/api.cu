@@ -29,8 +29,10 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
     int C = 0, G = 0, elem = 0;
+    int Cs = 0;               // per-unit stride of pos/score: C rounded up to 4 (16-byte rows)
     size_t units = 0;         // B * Hkv
-    size_t layer_slots = 0;   // units * C
+    size_t layer_slots = 0;   // units * C (K/V rows)
+    size_t layer_pslots = 0;  // units * Cs (pos/score entries)
     size_t kv_layer_bytes = 0;
     size_t off_k = 0, off_v = 0, off_pos = 0, off_score = 0, off_free = 0, off_err = 0;
     size_t off_sq = 0, off_sk = 0, off_sv = 0, off_so = 0;
@@ -81,15 +83,17 @@ Layout make_layout(const kvevict_config *c)
     L.G = c->n_q_heads / c->n_kv_heads;
     L.elem = c->dtype == KVEVICT_F32 ? 4 : 2;
     L.C = c->policy == KVEVICT_RANDOM ? c->max_prompt + c->budget + c->r : c->budget;
+    L.Cs = (L.C + 3) / 4 * 4;
     L.units = static_cast<size_t>(c->batch) * c->n_kv_heads;
     L.layer_slots = L.units * L.C;
+    L.layer_pslots = L.units * L.Cs;
     L.kv_layer_bytes = L.layer_slots * c->head_dim * L.elem;
     const size_t nl = c->n_layers;
     size_t off = 0;
     L.off_k = off; off = align_up(off + nl * L.kv_layer_bytes);
     L.off_v = off; off = align_up(off + nl * L.kv_layer_bytes);
-    L.off_pos = off; off = align_up(off + nl * L.layer_slots * 4);
-    L.off_score = off; if (c->policy == KVEVICT_H2O) off = align_up(off + nl * L.layer_slots * 4);
+    L.off_pos = off; off = align_up(off + nl * L.layer_pslots * 4);
+    L.off_score = off; if (c->policy == KVEVICT_H2O) off = align_up(off + nl * L.layer_pslots * 4);
     L.off_free = off; if (c->policy == KVEVICT_RANDOM) off = align_up(off + nl * L.units * c->r * 4);
     L.off_err = off; off = align_up(off + 16);
     L.q_bytes = static_cast<size_t>(c->batch) * c->n_q_heads * c->head_dim * L.elem;
@@ -121,11 +125,17 @@ struct kvevict_handle {
     uint8_t *state = nullptr;
     cudaStream_t stream = nullptr;
     int split = 1;
-    bool split_auto = true;
+    int clusters_req = 0;  // persistent grid size in clusters; 0 = automatic
     std::vector<LayerState> layers;
     kvevict_stats stats{};
     // decode kernel configured for (split, holes): function, shared memory, zcap
-    struct Configured { int split = 0; DecodeKernelInfo ki{}; size_t smem = 0; int zc = 0; } configured[2];
+    struct Configured {
+        int split = 0, clusters_req = -1;
+        DecodeKernelInfo ki{};
+        size_t smem = 0;
+        int zc = 0;
+        int clusters = 0;  // persistent grid, in clusters
+    } configured[2];
 };
 
 namespace {
@@ -139,37 +149,96 @@ int cuda_status(cudaError_t e)
     return KVEVICT_ERR_CUDA;
 }
 
-int auto_split(const kvevict_config &c, const Layout &L)
-{
-    // Enough CTAs for several waves over the 152 SMs, and a few hundred
-    // slots or more per CTA so the pipeline has work to overlap.
-    // Automatic choice stays within portable cluster sizes (<= 8 CTAs).
-    constexpr int kAutoMax = 8;
-    int S = 1;
-    while (S < kAutoMax && (L.C + S - 1) / S > 512) S *= 2;
-    while (S < kAutoMax && static_cast<long long>(L.units) * S < 4LL * kSMs && L.C / (2 * S) >= 128) S *= 2;
-    (void)c;
-    return S;
-}
-
 int max_slots_per_cta(const Layout &L, int S)
 {
     const int tiles = (L.C + kTile - 1) / kTile;
     return ((tiles + S - 1) / S) * kTile;
 }
 
+int n_aux_arrays(const kvevict_config &c, bool holes) { return c.policy == KVEVICT_H2O ? 2 : (holes ? 1 : 0); }
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+size_t decode_smem(const kvevict_handle *h, int S, bool holes)
+{
+    DecodeKernelInfo ki;
+    if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, &ki)) return ~size_t(0);
+    return ki.smem_bytes(ki.zcap(max_slots_per_cta(h->L, S)), n_aux_arrays(h->cfg, holes));
+}
+
+// CTAs per unit. The persistent kernel streams best with one CTA per unit: a
+// cluster adds two barriers and a DSMEM exchange per unit. Split a unit over
+// a cluster when its logits do not fit one CTA's shared memory, or when there
+// are too few units to give every resident CTA (2 per SM) one while each CTA
+// keeps >= 256 slots.
+int auto_split(const kvevict_handle *h)
+{
+    const Layout &L = h->L;
+    const bool random = h->cfg.policy == KVEVICT_RANDOM;
+    for (int S = 1; S <= kMaxSplit; S *= 2) {
+        if (decode_smem(h, S, random) > kMaxSmem) continue;
+        if (S < 8 && static_cast<long long>(L.units) * S < 2LL * kSMs && L.C / (2 * S) >= 256) continue;
+        return S;
+    }
+    return kMaxSplit;
+}
+
 int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInfo *ki, size_t *smem, int *zc)
 {
     if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, ki)) return KVEVICT_ERR_INVALID_ARG;
     *zc = ki->zcap(max_slots_per_cta(h->L, S));
-    *smem = ki->smem_bytes(*zc);
-    if (*smem > 227 * 1024) return KVEVICT_ERR_INVALID_ARG;
+    *smem = ki->smem_bytes(*zc, n_aux_arrays(h->cfg, holes));
+    if (*smem > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
     cudaError_t e = cudaFuncSetAttribute(ki->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(*smem));
     if (e == cudaSuccess && S > 8) e = cudaFuncSetAttribute(ki->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return cuda_status(e);
 }
 
 template <typename T> T *at(const kvevict_handle *h, size_t off) { return reinterpret_cast<T *>(h->state + off); }
+
+// Persistent grid size, in clusters: at most what the GPU holds at once, and
+// where possible a count that divides the units evenly (every cluster then
+// does the same number of units and none idles in the last round).
+int pick_clusters(const kvevict_handle *h, int S, const DecodeKernelInfo &ki, size_t smem, int *clusters)
+{
+    const int units = static_cast<int>(h->L.units);
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(S, 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int maxc = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&maxc, ki.fn, &lc);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (maxc < 1) return KVEVICT_ERR_INVALID_ARG;  // a cluster of this size does not fit
+    if (h->clusters_req > 0) {
+        *clusters = std::min(h->clusters_req, units);
+        return KVEVICT_OK;
+    }
+    if (units <= maxc) {
+        *clusters = units;
+        return KVEVICT_OK;
+    }
+    int best = maxc;
+    long long best_waste = -1;
+    for (int n = maxc; n >= (3 * maxc + 3) / 4; --n) {
+        const long long rounds = (units + n - 1) / n;
+        const long long waste = rounds * n - units;
+        if (best_waste < 0 || waste < best_waste) {
+            best = n;
+            best_waste = waste;
+        }
+        if (waste == 0) break;
+    }
+    *clusters = best;
+    return KVEVICT_OK;
+}
 
 int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, const void *vn, void *out)
 {
@@ -181,12 +250,13 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     P.q = q; P.k_new = kn; P.v_new = vn; P.out = out;
     P.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
     P.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
-    P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_slots;
-    P.score = c.policy == KVEVICT_H2O ? at<float>(h, L.off_score) + layer * L.layer_slots : nullptr;
+    P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
+    P.score = c.policy == KVEVICT_H2O ? at<float>(h, L.off_score) + layer * L.layer_pslots : nullptr;
     P.freelist = c.policy == KVEVICT_RANDOM ? at<int32_t>(h, L.off_free) + layer * L.units * c.r : nullptr;
+    P.units = static_cast<int>(L.units);
+    P.cstride = L.Cs;
     P.freelist_len = c.r;
     P.err = at<uint32_t>(h, L.off_err);
-    P.Hkv = c.n_kv_heads;
     P.C = L.C;
     P.p = ls.prompt_len + ls.t;
     P.n_sink = c.n_sink;
@@ -228,10 +298,13 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     }
 
     auto &cfgd = h->configured[holes ? 1 : 0];
-    if (cfgd.split != h->split) {
+    if (cfgd.split != h->split || cfgd.clusters_req != h->clusters_req) {
         int rc0 = configure_kernel(h, h->split, holes, &cfgd.ki, &cfgd.smem, &cfgd.zc);
         if (rc0) return rc0;
+        rc0 = pick_clusters(h, h->split, cfgd.ki, cfgd.smem, &cfgd.clusters);
+        if (rc0) return rc0;
         cfgd.split = h->split;
+        cfgd.clusters_req = h->clusters_req;
     }
     const DecodeKernelInfo &ki = cfgd.ki;
     const size_t smem = cfgd.smem;
@@ -240,7 +313,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     P.zcap = cfgd.zc;
 
     cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(h->split, c.n_kv_heads, c.batch);
+    lc.gridDim = dim3(cfgd.clusters * h->split, 1, 1);
     lc.blockDim = dim3(kThreads, 1, 1);
     lc.dynamicSmemBytes = smem;
     lc.stream = h->stream;
@@ -278,6 +351,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
             cp.step = ls.t;
             cp.Hkv = c.n_kv_heads;
             cp.C = L.C;
+            cp.cstride = L.Cs;
             cp.first_slot = ls.prompt_len;
             cp.n_cand = c.budget + c.r;
             cp.n_pow2 = 1;
@@ -326,11 +400,11 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
     h->state = static_cast<uint8_t *>(state);
     h->stream = static_cast<cudaStream_t>(cuda_stream);
     h->layers.resize(cfg->n_layers);
-    h->split = auto_split(*cfg, L);
+    h->split = auto_split(h);
     // Empty cache: every position -1, every score 0, no error bits.
-    cudaError_t e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_slots * 4, h->stream);
+    cudaError_t e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_pslots * 4, h->stream);
     if (e == cudaSuccess && cfg->policy == KVEVICT_H2O)
-        e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_slots * 4, h->stream);
+        e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_pslots * 4, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
     if (e != cudaSuccess) {
         delete h;
@@ -359,11 +433,12 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
     P.K = K; P.V = V;
     P.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
     P.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
-    P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_slots;
-    P.score = c.policy == KVEVICT_H2O ? at<float>(h, L.off_score) + layer * L.layer_slots : nullptr;
+    P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
+    P.score = c.policy == KVEVICT_H2O ? at<float>(h, L.off_score) + layer * L.layer_pslots : nullptr;
     P.n_tok = n_tokens;
     P.p0 = ls.prompt_len;
     P.C = L.C;
+    P.cstride = L.Cs;
     P.Hkv = c.n_kv_heads;
     P.head_dim = c.head_dim;
     P.elem_bytes = L.elem;
@@ -424,9 +499,9 @@ int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_devi
     if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     const Layout &L = h->L;
-    const void *src = at<int32_t>(h, L.off_pos) + layer * L.layer_slots;
-    cudaError_t e = cudaMemcpyAsync(dst, src, L.layer_slots * 4,
-                                    dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
+    const void *src = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
+    cudaError_t e = cudaMemcpy2DAsync(dst, L.C * 4, src, L.Cs * 4, L.C * 4, L.units,
+                                      dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
     if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
     return cuda_status(e);
 }
@@ -437,9 +512,9 @@ int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
     if (h->cfg.policy != KVEVICT_H2O) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     const Layout &L = h->L;
-    const void *src = at<float>(h, L.off_score) + layer * L.layer_slots;
-    cudaError_t e = cudaMemcpyAsync(dst, src, L.layer_slots * 4,
-                                    dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
+    const void *src = at<float>(h, L.off_score) + layer * L.layer_pslots;
+    cudaError_t e = cudaMemcpy2DAsync(dst, L.C * 4, src, L.Cs * 4, L.C * 4, L.units,
+                                      dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
     if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
     return cuda_status(e);
 }
@@ -471,15 +546,21 @@ int kvevict_set_split(kvevict_t h, int split)
 {
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     if (split == 0) {
-        h->split = auto_split(h->cfg, h->L);
+        h->split = auto_split(h);
     } else {
         if (split < 1 || split > kMaxSplit || (split & (split - 1))) return KVEVICT_ERR_INVALID_ARG;
-        DecodeKernelInfo ki;
-        if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, false, &ki)) return KVEVICT_ERR_INVALID_ARG;
-        if (ki.smem_bytes(ki.zcap(max_slots_per_cta(h->L, split))) > 227 * 1024) return KVEVICT_ERR_INVALID_ARG;
+        if (decode_smem(h, split, h->cfg.policy == KVEVICT_RANDOM) > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
         h->split = split;
     }
     h->stats.split = h->split;
+    return KVEVICT_OK;
+}
+
+int kvevict_set_clusters(kvevict_t h, int clusters)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (clusters < 0) return KVEVICT_ERR_INVALID_ARG;
+    h->clusters_req = clusters;
     return KVEVICT_OK;
 }
 
@@ -487,6 +568,7 @@ int kvevict_get_stats(kvevict_t h, kvevict_stats *out)
 {
     if (!h || !out) return KVEVICT_ERR_INVALID_ARG;
     *out = h->stats;
+    out->clusters = h->configured[0].clusters ? h->configured[0].clusters : h->configured[1].clusters;
     return KVEVICT_OK;
 }
 

@@ -37,8 +37,8 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillParams P)
         vd[v] = vs[v];
     }
     if (lane == 0) {
-        P.pos[unit * P.C + slot] = p;
-        if (P.score) P.score[unit * P.C + slot] = 0.f;
+        P.pos[unit * P.cstride + slot] = p;
+        if (P.score) P.score[unit * P.cstride + slot] = 0.f;
     }
 }
 
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kCutThreads) random_cut_kernel(const CutParams
     const int tid = threadIdx.x;
     const int h = blockIdx.x, b = blockIdx.y;
     const size_t unit = static_cast<size_t>(b) * P.Hkv + h;
-    int32_t *pos = P.pos + unit * P.C;
+    int32_t *pos = P.pos + unit * P.cstride;
 
     grid_dependency_wait();
 

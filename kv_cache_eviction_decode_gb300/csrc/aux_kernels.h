@@ -15,7 +15,7 @@ struct PrefillParams {
     void *kc, *vc;      // layer cache [B][Hkv][C][D]
     int32_t *pos;
     float *score;       // or null
-    int n_tok, p0, C, Hkv, head_dim, elem_bytes;
+    int n_tok, p0, C, cstride, Hkv, head_dim, elem_bytes;
     int n_sink, ring_len;  // ring_len = C - n_sink for ring policies, 0 for Random
     int a0, a1, b0, b1;    // chunk rows to copy
 };
@@ -24,7 +24,7 @@ struct CutParams {
     int32_t *pos;       // layer [B][Hkv][C]
     int32_t *freelist;  // layer [B][Hkv][r]
     uint64_t seed;
-    int layer, step, Hkv, C;
+    int layer, step, Hkv, C, cstride;
     int first_slot, n_cand, n_pow2, r;
 };
 

@@ -8,7 +8,7 @@ namespace kvevict {
 
 struct DecodeKernelInfo {
     const void *fn;                    // __global__ decode_step_kernel<...>
-    size_t (*smem_bytes)(int zcap);    // dynamic shared memory for a given zcap
+    size_t (*smem_bytes)(int zcap, int n_aux);  // dynamic shared memory (n_aux: 0, 1 or 2 prefetched arrays)
     int (*zcap)(int max_slots_per_cta);
 };
 

@@ -9,7 +9,7 @@ template <int D, int G, bool H> DecodeKernelInfo info()
 {
     using L = DecodeLayout<float, D, G>;
     return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<float, D, G, H>),
-                            [](int zc) { return L::bytes(zc); }, [](int n) { return L::zcap(n); }};
+                            [](int zc, int n_aux) { return L::bytes(zc, n_aux); }, [](int n) { return L::zcap(n); }};
 }
 
 template <int D, bool H> bool pick_g(int G, DecodeKernelInfo *out)

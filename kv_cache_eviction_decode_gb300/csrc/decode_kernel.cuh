@@ -1,39 +1,47 @@
 // decode_kernel.cuh -- the fused decode step over a budget-bounded KV cache.
 //
-// One launch per layer-step. Grid (split, Hkv, B): the `split` CTAs of one
-// thread-block cluster share one (sequence, KV head) unit and divide its
-// occupied slots into contiguous ranges of 32-slot tiles. Per CTA:
+// One persistent launch per layer-step. The grid is n_clusters thread-block
+// clusters of `split` CTAs. Cluster c processes the units (sequence, KV head)
+// c, c + n_clusters, ...; inside a cluster the CTAs divide each unit's
+// occupied slots into contiguous ranges of 32-slot tiles.
 //
-//   producer warp   one elected lane streams the CTA's K tiles, then its V
-//                   tiles, global -> shared with bulk (TMA) copies into a
-//                   ring of stages, each completing on a full-mbarrier; the
-//                   consumers free a stage through its empty-mbarrier.
-//   K phase         each consumer warp takes whole K tiles and forms the
-//                   logits z = q.k / sqrt(d) of the G query heads for the 32
-//                   slots: every lane holds d/32 coordinates of q and of each
-//                   key, and a 31-shuffle butterfly transposes the partial
-//                   sums so lane i ends with one (head, slot) logit. The
-//                   logits stay in shared memory (the score pass needs them).
-//   V phase         with the CTA-local max m_c known, p = 2^(z - m_c) is
-//                   written back over z and o += p v is accumulated.
-//   combine         (m_c, l_c, o_c) of every CTA in the cluster are read
-//                   through distributed shared memory; each CTA writes its
-//                   share of out = sum_c o_c 2^(m_c - m) / l.
-//   scores (H2O)    every retained slot's cumulative score grows by
-//                   (1/G) sum_g p_g 2^(m_c - m) / l; the eligible slot with the
-//                   smallest (score, position) is the CTA's candidate, and a
-//                   second cluster exchange picks the victim.
-//   insert          the new token's K/V, position and score are written in
-//                   place into the victim's slot (H2O), the closed-form ring
-//                   slot (StreamingLLM), the next empty slot, or the next
-//                   entry of the unit's free list (Random after a cut).
+// Memory pipeline: a ring of NST shared-memory stages, each filled by one
+// bulk (TMA) global->shared copy of a 32-slot K or V tile that completes on
+// the stage's mbarrier. The CTA's tiles form one sequence over all of its
+// units (unit 0's K tiles, its V tiles, unit 1's K tiles, ...). Thread 0
+// issues the first NST copies; after that, the warp that consumes tile s
+// issues the copy of tile s + NST into the stage it has just freed. The ring
+// therefore keeps streaming across unit boundaries: the next unit's first
+// tiles land while the current unit's combine and score epilogue run. The
+// next unit's slot positions (and H2O scores) are prefetched the same way
+// into a second, double-buffered shared-memory area.
 //
-// Method (page title and section): attention over the retained cache then
-// cumulative-score update then eviction, "KV Cache 驱逐策略：从 LRU 到 H2O"
-// flowchart and "Attention Sinks 与 KV Cache 淘汰策略" section 4.2 loop;
-// greedy removal of the lowest-score candidate, "h2o: heavy-hitter oracle"
-// summary, Algorithm 1; sink + ring window, same page section 4.1; GQA score =
-// mean over the query heads of one KV head.
+// Per unit, every CTA:
+//   K phase   each warp takes whole K tiles and forms the logits
+//             z = q.k / sqrt(d) of the G query heads for 32 slots: every lane
+//             holds d/32 coordinates of q and of each key, and a 31-shuffle
+//             butterfly transposes the partial sums so lane i ends with one
+//             (head, slot) logit. Logits stay in shared memory (log2 units).
+//   V phase   with the CTA-local max m_c known, p = 2^(z - m_c) is written
+//             back over z and o += p v is accumulated.
+//   combine   (m_c, l_c, o_c) of every CTA in the cluster are read through
+//             distributed shared memory; each CTA writes its share of
+//             out = sum_c o_c 2^(m_c - m) / l.
+//   scores    (H2O) every retained slot's cumulative score grows by
+//             (1/G) sum_g p_g 2^(m_c - m) / l; the eligible slot with the
+//             smallest (score, position) is the CTA's candidate, and a
+//             second cluster exchange picks the victim.
+//   insert    the new token's K/V, position and score are written in place
+//             into the victim's slot (H2O), the closed-form ring slot
+//             (StreamingLLM), the next empty slot, or the next entry of the
+//             unit's free list (Random after a cut).
+//
+// Method (page title and section): attention over the retained cache, then
+// the cumulative-score update, then eviction -- "KV Cache 驱逐策略：从 LRU 到
+// H2O" flowchart and "Attention Sinks 与 KV Cache 淘汰策略" section 4.2 loop;
+// greedy removal of the lowest-score candidate -- "h2o: heavy-hitter oracle"
+// summary, Algorithm 1; sink + ring window -- same page section 4.1; the GQA
+// score is the mean over the query heads of one KV head.
 #pragma once
 
 #include <cfloat>
@@ -43,10 +51,9 @@
 
 namespace kvevict {
 
-constexpr int kTile = 32;           // slots per pipeline stage
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kTile = 32;  // slots per pipeline stage
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSplit = 16;
 
 enum InsertMode : int {
@@ -66,13 +73,15 @@ struct DecodeParams {
     const int32_t *freelist;  // [B][Hkv][freelist_len]
     int32_t *trace;      // [B][Hkv][4] or null: slot, evicted position, evicted score, new score
     uint32_t *err;
-    int Hkv, C;
+    int units;           // B * Hkv
+    int C;
+    int cstride;         // per-unit stride of pos/score (C rounded up to 4: 16-byte rows)
     int n_active;        // slots [0, n_active) may hold tokens
     int p;               // position of the new token
     int mode, dest_slot, freelist_idx, freelist_len;
     int n_sink, n_recent;
     int split;           // CTAs per unit (cluster size)
-    int zcap;            // per-head stride of the logit buffer
+    int zcap;            // per-head stride of the logit buffer (and aux slots)
     float scale_log2;    // log2(e) / sqrt(D)
 };
 
@@ -81,16 +90,19 @@ template <typename T, int D, int G> struct DecodeLayout {
     static constexpr int kEPL = D / 32;  // key/value coordinates per lane
     static constexpr int kR = 32 / G;    // slots per butterfly chunk
     static constexpr int kStageBytes = kTile * D * static_cast<int>(sizeof(T));
-    static constexpr int kStages = (65536 / kStageBytes) < 4 ? 4 : (65536 / kStageBytes);
+    static constexpr int kStages = (81920 / kStageBytes) < 6 ? 6 : (81920 / kStageBytes);
     static constexpr int kStageArea = kStages * kStageBytes;
-    static_assert(kConsumerWarps * G * D * 4 <= kStageArea, "partial outputs must fit the stage area");
+    static constexpr int kPartBytes = kWarps * G * D * 4;
     static_assert(G >= 1 && G <= 8 && (G & (G - 1)) == 0, "G in {1,2,4,8}");
 
     struct Misc {
         uint64_t full[kStages];
-        uint64_t empty[kStages];
-        float wmax[kConsumerWarps][G];
-        float wsum[kConsumerWarps][G];
+        uint64_t auxbar[2];
+        uint32_t issued[kStages];  // copies issued per stage (drain after a timeout)
+        uint32_t aux_issued[2];
+        int abort;
+        float wmax[kWarps][G];
+        float wsum[kWarps][G];
         float m[G];        // this CTA's max logit per head (log2 units)
         float l[G];        // this CTA's softmax denominator relative to m
         float o[G][D];     // this CTA's unnormalised output relative to m
@@ -101,23 +113,26 @@ template <typename T, int D, int G> struct DecodeLayout {
         int dest;
         uint64_t best_key;
         int32_t best_slot;
-        uint64_t wkey[kConsumerWarps + 1];
-        int32_t wslot[kConsumerWarps + 1];
+        uint64_t wkey[kWarps];
+        int32_t wslot[kWarps];
     };
 
-    // zcap = C-per-CTA rounded to whole tiles; for G > 1 padded so that
-    // zcap == R (mod 32): the G lanes groups then hit distinct banks.
+    // zcap = slots per CTA rounded to whole tiles; for G > 1 padded so that
+    // zcap == R (mod 32): the lane groups of different heads then hit
+    // distinct shared-memory banks.
     __host__ __device__ static int zcap(int max_slots_per_cta)
     {
         int z = ((max_slots_per_cta + kTile - 1) / kTile) * kTile;
         return G > 1 ? z + kR : z;
     }
     __host__ __device__ static size_t off_z() { return kStageArea; }
-    __host__ __device__ static size_t off_misc(int zc)
-    {
-        return kStageArea + ((static_cast<size_t>(G) * zc * 4 + 127) / 128) * 128;
-    }
-    __host__ __device__ static size_t bytes(int zc) { return off_misc(zc) + sizeof(Misc); }
+    __host__ __device__ static size_t off_part(int zc) { return kStageArea + ((static_cast<size_t>(G) * zc * 4 + 127) / 128) * 128; }
+    // aux: 2 buffers, each holding the unit's slot positions and, with
+    // scores (H2O), the cumulative scores: n_arrays = 0 (none), 1 or 2.
+    __host__ __device__ static size_t off_aux(int zc) { return off_part(zc) + kPartBytes; }
+    __host__ __device__ static size_t aux_bytes(int zc) { return ((static_cast<size_t>(zc) * 4 + 15) / 16) * 16; }
+    __host__ __device__ static size_t off_misc(int zc, int n_arrays) { return off_aux(zc) + 2 * n_arrays * aux_bytes(zc); }
+    __host__ __device__ static size_t bytes(int zc, int n_arrays) { return off_misc(zc, n_arrays) + sizeof(Misc); }
 };
 
 // Butterfly transpose-reduce: lane L holds 32 partial sums v[0..31]; after
@@ -152,40 +167,85 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
+// The CTA's share of one launch: which units, which tiles of each.
+struct Work {
+    int cluster_id, n_clusters, n_units;  // units this cluster processes
+    int nt, s_lo, s_hi, n_mine;           // tiles / slot range per unit
+    int total_seq;                        // K and V tiles over all units
+};
+
+template <typename T, int D> struct TileSource {
+    const T *kc, *vc;
+    size_t C;
+    __device__ __forceinline__ void issue(const Work &W, int s, T *stage, uint64_t *bar) const
+    {
+        const int two_nt = 2 * W.nt;
+        const int i = s / two_nt, loc = s - i * two_nt;
+        const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
+        const int tile = loc < W.nt ? loc : loc - W.nt;
+        const int slot0 = W.s_lo + tile * kTile;
+        const int rows = min(kTile, W.s_hi - slot0);
+        const uint32_t bytes = static_cast<uint32_t>(rows * D * sizeof(T));
+        const T *src = (loc < W.nt ? kc : vc) + (unit * C + slot0) * D;
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s_stream(stage, src, bytes, bar, l2_policy_evict_first());
+    }
+};
+
+// Two CTAs per SM for G <= 2 (registers capped at 128 per thread).
+template <int G> constexpr int min_blocks() { return G <= 2 ? 2 : 1; }
+
 template <typename T, int D, int G, bool HOLES>
-__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ DecodeParams P)
+__global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(const __grid_constant__ DecodeParams P)
 {
     using L = DecodeLayout<T, D, G>;
     constexpr int EPL = L::kEPL, R = L::kR, NST = L::kStages;
     using E = Elem<T>;
 
     extern __shared__ __align__(128) uint8_t smem[];
-    T *stage = reinterpret_cast<T *>(smem);
+    T *ring = reinterpret_cast<T *>(smem);
     const int zc = P.zcap;
     float *zbuf = reinterpret_cast<float *>(smem + L::off_z());
-    auto &M = *reinterpret_cast<typename L::Misc *>(smem + L::off_misc(zc));
+    float *part = reinterpret_cast<float *>(smem + L::off_part(zc));
+    uint8_t *aux = smem + L::off_aux(zc);
+    const size_t auxb = L::aux_bytes(zc);
+    // slot positions (and H2O scores) are prefetched per unit only when used
+    const bool need_aux = P.score != nullptr || HOLES;
+    const int n_aux = P.score != nullptr ? 2 : (HOLES ? 1 : 0);
+    auto &M = *reinterpret_cast<typename L::Misc *>(smem + L::off_misc(zc, n_aux));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = static_cast<int>(cluster_rank());
     const int S = P.split;
-    const int h = blockIdx.y, b = blockIdx.z;
-    const size_t unit = static_cast<size_t>(b) * P.Hkv + h;
     const size_t C = static_cast<size_t>(P.C);
+    const size_t CS = static_cast<size_t>(P.cstride);
+    const bool has_score = P.score != nullptr;
 
-    // This CTA's contiguous range of whole tiles among the occupied slots.
-    const int nt_all = (P.n_active + kTile - 1) / kTile;
-    const int t_lo = static_cast<int>(static_cast<long long>(rank) * nt_all / S);
-    const int t_hi = static_cast<int>(static_cast<long long>(rank + 1) * nt_all / S);
-    const int nt = t_hi - t_lo;
-    const int s_lo = t_lo * kTile;
-    const int s_hi = min(t_hi * kTile, P.n_active);
-    const int n_mine = max(0, s_hi - s_lo);
+    Work W;
+    W.cluster_id = blockIdx.x / S;
+    W.n_clusters = gridDim.x / S;
+    W.n_units = W.cluster_id < P.units ? (P.units - W.cluster_id + W.n_clusters - 1) / W.n_clusters : 0;
+    {
+        const int nt_all = (P.n_active + kTile - 1) / kTile;
+        const int t_lo = static_cast<int>(static_cast<long long>(rank) * nt_all / S);
+        const int t_hi = static_cast<int>(static_cast<long long>(rank + 1) * nt_all / S);
+        W.nt = t_hi - t_lo;
+        W.s_lo = t_lo * kTile;
+        W.s_hi = min(t_hi * kTile, P.n_active);
+        W.n_mine = max(0, W.s_hi - W.s_lo);
+        W.total_seq = W.n_units * 2 * W.nt;
+    }
+    TileSource<T, D> src{static_cast<const T *>(P.kc), static_cast<const T *>(P.vc), C};
 
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(&M.full[i], 1);
-            mbar_init(&M.empty[i], 1);
+            M.issued[i] = 0;
         }
+        mbar_init(&M.auxbar[0], 1);
+        mbar_init(&M.auxbar[1], 1);
+        M.aux_issued[0] = M.aux_issued[1] = 0;
+        M.abort = 0;
         mbar_fence_init();
     }
     __syncthreads();
@@ -195,66 +255,146 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     grid_dependency_wait();
     grid_launch_dependents();
 
-    const T *kbase = static_cast<const T *>(P.kc) + unit * C * D;
-    const T *vbase = static_cast<const T *>(P.vc) + unit * C * D;
+    // Bulk copy of one unit's slot positions (and scores) into aux buffer b.
+    auto issue_aux = [&](int i) {
+        const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
+        const int b = i & 1;
+        const uint32_t bytes = static_cast<uint32_t>(((W.n_mine * 4 + 15) / 16) * 16);
+        const uint32_t tx = has_score ? 2 * bytes : bytes;
+        mbar_arrive_expect_tx(&M.auxbar[b], tx);
+        bulk_g2s(aux + (n_aux * b) * auxb, P.pos + unit * CS + W.s_lo, bytes, &M.auxbar[b]);
+        if (has_score) bulk_g2s(aux + (n_aux * b + 1) * auxb, P.score + unit * CS + W.s_lo, bytes, &M.auxbar[b]);
+        M.aux_issued[b]++;
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < min(NST, W.total_seq); ++s)
+            src.issue(W, s, ring + static_cast<size_t>(s) * kTile * D, &M.full[s]);
+        if (need_aux && W.n_units > 0 && W.n_mine > 0) issue_aux(0);
+        __threadfence_block();
+        for (int s = 0; s < min(NST, W.total_seq); ++s) M.issued[s] = 1;
+    }
+
     const int g_lane = lane / R;  // the head this lane's logits belong to
+    bool ok = true;               // false after a timed-out wait: skip work, keep barriers
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            for (int s = 0; s < 2 * nt; ++s) {
-                const int st = s % NST, round = s / NST;
-                if (round > 0 && !mbar_wait(&M.empty[st], (round - 1) & 1)) {
-                    atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
-                    break;
-                }
-                const int tile = s < nt ? s : s - nt;
-                const int slot0 = s_lo + tile * kTile;
-                const int rows = min(kTile, s_hi - slot0);
-                const uint32_t bytes = static_cast<uint32_t>(rows * D * sizeof(T));
-                const T *src = (s < nt ? kbase : vbase) + static_cast<size_t>(slot0) * D;
-                mbar_arrive_expect_tx(&M.full[st], bytes);
-                bulk_g2s_stream(stage + static_cast<size_t>(st) * kTile * D, src, bytes, &M.full[st], pol);
-                issued = s + 1;
-            }
-            // No copy may still be landing in shared memory when the CTA
-            // leaves: wait for the last stages issued (earlier ones were
-            // consumed before their stage was reused).
-            for (int s = max(0, issued - NST); s < issued; ++s)
-                if (!mbar_wait(&M.full[s % NST], (s / NST) & 1)) atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
+    volatile int *abort_flag = &M.abort;
+    volatile uint32_t *issued = M.issued;
+    // Tile s is copy number c = s / NST into stage s % NST. Its consumer
+    // first waits until that copy has been issued (by the consumer of tile
+    // s - NST, usually another warp): the stage's mbarrier is then in phase c
+    // or c + 1 -- never behind -- so the parity wait below tests phase c. The
+    // copy after it (tile s + NST) is only issued once tile s is consumed.
+    auto wait_stage = [&](int s) -> bool {
+        if (!ok || *abort_flag) {
+            ok = false;
+            return false;
         }
-    } else {
-        // ------------------------------------------------------------ consumers
-        const T *qp = static_cast<const T *>(P.q) + unit * G * D;
-        float qf[G][EPL];
-#pragma unroll
-        for (int g = 0; g < G; ++g) load_f32<T, EPL>(qp + g * D + lane * EPL, qf[g]);
+        const int st = s % NST;
+        const uint32_t need = static_cast<uint32_t>(s / NST) + 1;
+        if (issued[st] < need) {
+            const uint64_t t0 = global_timer_ns();
+            for (uint32_t it = 1; issued[st] < need; ++it) {
+                if ((it & 63u) == 0 && (global_timer_ns() - t0 > kWaitLimitNs || *abort_flag)) {
+                    atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
+                    ok = false;
+                    *abort_flag = 1;
+                    return false;
+                }
+            }
+        }
+        __threadfence_block();
+        if (!mbar_wait(&M.full[st], (s / NST) & 1)) {
+            atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
+            ok = false;
+            *abort_flag = 1;
+            return false;
+        }
+        return true;
+    };
+    auto release_stage = [&](int s) {
+        __syncwarp();
+        const int nx = s + NST;
+        if (lane == 0 && nx < W.total_seq && ok) {
+            const int st = s % NST;
+            src.issue(W, nx, ring + static_cast<size_t>(st) * kTile * D, &M.full[st]);
+            __threadfence_block();
+            issued[st] = issued[st] + 1;
+        }
+    };
 
-        if (rank == 0 && warp == 0) {  // the new token's logits
-            float kf[EPL];
-            load_f32<T, EPL>(static_cast<const T *>(P.k_new) + unit * D + lane * EPL, kf);
+    // Register prefetch of a unit's q (all lanes) and new token (rank 0).
+    float qn[G][EPL], kn_next[EPL], vn_next[EPL];
+    auto load_unit_inputs = [&](size_t u) {
+        const T *qp = static_cast<const T *>(P.q) + u * G * D;
+#pragma unroll
+        for (int g = 0; g < G; ++g) load_f32<T, EPL>(qp + g * D + lane * EPL, qn[g]);
+        if (rank == 0 && warp == 0) {
+            load_f32<T, EPL>(static_cast<const T *>(P.k_new) + u * D + lane * EPL, kn_next);
+            load_f32<T, EPL>(static_cast<const T *>(P.v_new) + u * D + lane * EPL, vn_next);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) kn_next[e] = vn_next[e] = 0.f;
+        }
+    };
+    if (W.n_units > 0) load_unit_inputs(static_cast<size_t>(W.cluster_id));
+
+    for (int i = 0; i < W.n_units; ++i) {
+        const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
+        const int seq0 = i * 2 * W.nt;
+        const int32_t *apos = reinterpret_cast<const int32_t *>(aux + (n_aux * (i & 1)) * auxb);
+        const float *ascore = reinterpret_cast<const float *>(aux + (n_aux * (i & 1) + 1) * auxb);
+        // Prefetch the next unit's positions/scores into the other buffer:
+        // its previous contents (unit i - 1) were awaited and used already.
+        if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
+
+        // q of this unit (prefetched during the previous unit) and the next
+        // unit's q, k_new, v_new into registers for the next iteration.
+        float qf[G][EPL], kf_new[EPL], vf_new[EPL];
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) qf[g][e] = qn[g][e];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            kf_new[e] = kn_next[e];
+            vf_new[e] = vn_next[e];
+        }
+        if (i + 1 < W.n_units) load_unit_inputs(unit + W.n_clusters);
+        // the new token's logits (rank 0, warp 0)
+        if (rank == 0 && warp == 0) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float s = warp_sum(dot_n(qf[g], kf));
+                const float s = warp_sum(dot_n(qf[g], kf_new));
                 if (lane == 0) M.znew[g] = s * P.scale_log2;
             }
         }
-
-        // K phase: logits of this CTA's slots, kept in shared memory.
-        float mx = -INFINITY;
-        bool ok = true;
-        for (int s = warp; s < nt; s += kConsumerWarps) {
-            const int st = s % NST;
-            if (!mbar_wait(&M.full[st], (s / NST) & 1)) {
+        // positions (and scores) of this unit's slots; every unit that
+        // prefetched them waits for them exactly once
+        bool aux_ready = false;
+        auto wait_aux = [&]() {
+            if (aux_ready || W.n_mine == 0 || !need_aux) return;
+            aux_ready = true;
+            if (!ok || *abort_flag) {
+                ok = false;
+                return;
+            }
+            if (!mbar_wait(&M.auxbar[i & 1], (i >> 1) & 1)) {
                 atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
                 ok = false;
-                break;
+                *abort_flag = 1;
             }
-            const T *tk = stage + static_cast<size_t>(st) * kTile * D;
-            const int base = s * kTile;
-            const int rows = min(kTile, n_mine - base);
+        };
+        if (HOLES) wait_aux();
+
+        // ---------------------------------------------------------- K phase
+        float mx = -INFINITY;
+        for (int s_loc = warp; s_loc < W.nt; s_loc += kWarps) {
+            const int s = seq0 + s_loc;
+            if (!wait_stage(s)) break;
+            const T *tk = ring + static_cast<size_t>(s % NST) * kTile * D;
+            const int base = s_loc * kTile;
+            const int rows = min(kTile, W.n_mine - base);
 #pragma unroll
             for (int c = 0; c < G; ++c) {
                 float vals[32];
@@ -268,28 +408,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 const float sum = transpose_reduce32(vals, lane);
                 const int row = c * R + (lane % R);
                 bool valid = row < rows;
-                if (HOLES && valid) valid = P.pos[unit * C + s_lo + base + row] >= 0;
+                if (HOLES && valid) valid = apos[base + row] >= 0;
                 const float z = valid ? sum * P.scale_log2 : -INFINITY;
                 zbuf[g_lane * zc + base + row] = z;
                 mx = fmaxf(mx, z);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&M.empty[st]);
+            release_stage(s);
         }
 #pragma unroll
         for (int off = 1; off < R; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         if (lane % R == 0) M.wmax[warp][g_lane] = mx;
-        named_sync(1, kConsumerThreads);
+        __syncthreads();
         if (warp == 0 && lane < G) {
             float m = -INFINITY;
-            for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, M.wmax[w][lane]);
+            for (int w = 0; w < kWarps; ++w) m = fmaxf(m, M.wmax[w][lane]);
             if (rank == 0) m = fmaxf(m, M.znew[lane]);
             M.m[lane] = m;
         }
-        named_sync(1, kConsumerThreads);
+        __syncthreads();
         const float m_mine = M.m[g_lane];
 
-        // V phase.
+        // ---------------------------------------------------------- V phase
         float acc[G][EPL];
 #pragma unroll
         for (int g = 0; g < G; ++g)
@@ -297,26 +436,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
         float lsum = 0.f;
         if (rank == 0 && warp == 0) {
-            float vf[EPL];
-            load_f32<T, EPL>(static_cast<const T *>(P.v_new) + unit * D + lane * EPL, vf);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float pn = exp2f(M.znew[g] - M.m[g]);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pn, vf[e], acc[g][e]);
+                for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pn, vf_new[e], acc[g][e]);
                 if (lane == g * R) lsum += pn;
                 if (lane == 0) M.pnew[g] = pn;
             }
         }
-        const int first_v = nt + ((warp - nt % kConsumerWarps) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-        for (int s = first_v; ok && s < 2 * nt; s += kConsumerWarps) {
-            const int st = s % NST;
-            if (!mbar_wait(&M.full[st], (s / NST) & 1)) {
-                atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
-                break;
-            }
-            const int base = (s - nt) * kTile;
-            const int rows = min(kTile, n_mine - base);
+        const int first_v = W.nt + ((warp - W.nt % kWarps) % kWarps + kWarps) % kWarps;
+        for (int s_loc = first_v; s_loc < 2 * W.nt; s_loc += kWarps) {
+            const int s = seq0 + s_loc;
+            if (!wait_stage(s)) break;
+            const int base = (s_loc - W.nt) * kTile;
+            const int rows = min(kTile, W.n_mine - base);
             // probabilities of this tile: lane L owns (head L/R, slots L%R + c*R)
 #pragma unroll
             for (int c = 0; c < G; ++c) {
@@ -327,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 lsum += pr;
             }
             __syncwarp();
-            const T *tv = stage + static_cast<size_t>(st) * kTile * D;
+            const T *tv = ring + static_cast<size_t>(s % NST) * kTile * D;
             int r = 0;
             if (!HOLES) {
                 for (; r + 4 <= rows; r += 4) {
@@ -363,117 +497,113 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pr[g], vf[e], acc[g][e]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&M.empty[st]);
+            release_stage(s);
         }
 #pragma unroll
         for (int off = 1; off < R; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
         if (lane % R == 0) M.wsum[warp][g_lane] = lsum;
-
-        // Reduce the consumer warps' partial outputs through the (now idle)
-        // stage area.
-        named_sync(1, kConsumerThreads);
-        float *part = reinterpret_cast<float *>(smem);
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
             for (int e = 0; e < EPL; ++e) part[(warp * G + g) * D + lane * EPL + e] = acc[g][e];
-        named_sync(1, kConsumerThreads);
-        for (int i = tid; i < G * D; i += kConsumerThreads) {
+        __syncthreads();
+        for (int j = tid; j < G * D; j += kThreads) {
             float o = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w) o += part[w * G * D + i];
-            M.o[i / D][i % D] = o;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) o += part[w * G * D + j];
+            M.o[j / D][j % D] = o;
         }
         if (tid < G) {
             float l = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w) l += M.wsum[w][tid];
+            for (int w = 0; w < kWarps; ++w) l += M.wsum[w][tid];
             M.l[tid] = l;
         }
-    }
-    __syncthreads();
-    cluster_sync();  // (1) every CTA's (m, l, o) is ready
+        __syncthreads();
+        cluster_sync();  // (1) every CTA's (m, l, o) is ready
 
-    // ---------------------------------------------------------------- combine
-    if (tid < G) {
-        float mg = -INFINITY;
-        for (int c = 0; c < S; ++c) mg = fmaxf(mg, ld_peer_f32(peer_addr(&M.m[tid], c)));
-        float lg = 0.f;
-        for (int c = 0; c < S; ++c) {
-            const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
-            const float lc = ld_peer_f32(peer_addr(&M.l[tid], c));
-            if (mc != -INFINITY) lg += lc * exp2f(mc - mg);
+        // ------------------------------------------------------------ combine
+        if (tid < G) {
+            float mg = -INFINITY;
+            for (int c = 0; c < S; ++c) mg = fmaxf(mg, ld_peer_f32(peer_addr(&M.m[tid], c)));
+            float lg = 0.f;
+            for (int c = 0; c < S; ++c) {
+                const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
+                const float lc = ld_peer_f32(peer_addr(&M.l[tid], c));
+                if (mc != -INFINITY) lg += lc * exp2f(mc - mg);
+            }
+            if (rank == 0 && !(lg > 0.f && lg <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
+            const float inv = 1.f / lg;
+            for (int c = 0; c < S; ++c) {
+                const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
+                M.fac[c][tid] = (mc == -INFINITY) ? 0.f : exp2f(mc - mg) * inv;
+            }
         }
-        if (rank == 0 && !(lg > 0.f && lg <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
-        const float inv = 1.f / lg;
-        for (int c = 0; c < S; ++c) {
-            const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
-            M.fac[c][tid] = (mc == -INFINITY) ? 0.f : exp2f(mc - mg) * inv;
+        __syncthreads();
+        {
+            constexpr int GD = G * D;
+            const int i0 = rank * GD / S, i1 = (rank + 1) * GD / S;
+            T *outp = static_cast<T *>(P.out) + unit * GD;
+            for (int j = i0 + tid; j < i1; j += kThreads) {
+                const int g = j / D, e = j % D;
+                float o = 0.f;
+                for (int c = 0; c < S; ++c) o = fmaf(ld_peer_f32(peer_addr(&M.o[g][e], c)), M.fac[c][g], o);
+                outp[j] = E::from_f32(o);
+            }
         }
-    }
-    __syncthreads();
-    {
-        constexpr int GD = G * D;
-        const int i0 = rank * GD / S, i1 = (rank + 1) * GD / S;
-        T *outp = static_cast<T *>(P.out) + unit * GD;
-        for (int i = i0 + tid; i < i1; i += kThreads) {
-            const int g = i / D, e = i % D;
-            float o = 0.f;
-            for (int c = 0; c < S; ++c) o = fmaf(ld_peer_f32(peer_addr(&M.o[g][e], c)), M.fac[c][g], o);
-            outp[i] = E::from_f32(o);
-        }
-    }
 
-    // ------------------------------------------------ cumulative scores (H2O)
-    if (P.score != nullptr) {
-        float fself[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
-        uint64_t best = ~0ull;
-        int32_t bslot = -1;
+        // ------------------------------------------ cumulative scores (H2O)
         const bool evict = P.mode == kH2OEvict;
-        for (int j = tid; j < n_mine; j += kThreads) {
-            float a = 0.f;
+        if (has_score) {
+            wait_aux();
+            float fself[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
-            const size_t gi = unit * C + s_lo + j;
-            const float sc = P.score[gi] + a;
-            P.score[gi] = sc;
-            if (evict) {
-                const int ps = P.pos[gi];
-                if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
-                    const uint64_t key = (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
-                    if (key < best) {
-                        best = key;
-                        bslot = s_lo + j;
+            for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
+            uint64_t best = ~0ull;
+            int32_t bslot = -1;
+            for (int j = tid; j < W.n_mine; j += kThreads) {
+                float a = 0.f;
+#pragma unroll
+                for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
+                const float sc = ascore[j] + a;
+                P.score[unit * CS + W.s_lo + j] = sc;
+                if (evict) {
+                    const int ps = apos[j];
+                    if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
+                        const uint64_t key =
+                            (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
+                        if (key < best) {
+                            best = key;
+                            bslot = W.s_lo + j;
+                        }
                     }
                 }
             }
-        }
-        if (rank == 0 && tid == 0) {
-            float a = 0.f;
+            if (rank == 0 && tid == 0) {
+                float a = 0.f;
 #pragma unroll
-            for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], M.fac[0][g], a);
-            M.anew = a * (1.0f / G);
-        }
-        if (evict) {
+                for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], M.fac[0][g], a);
+                M.anew = a * (1.0f / G);
+            }
+            if (evict) {
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const uint64_t ok = __shfl_xor_sync(0xffffffffu, best, off);
-                const int32_t os = __shfl_xor_sync(0xffffffffu, bslot, off);
-                if (ok < best) {
-                    best = ok;
-                    bslot = os;
+                for (int off = 16; off >= 1; off >>= 1) {
+                    const uint64_t ok2 = __shfl_xor_sync(0xffffffffu, best, off);
+                    const int32_t os = __shfl_xor_sync(0xffffffffu, bslot, off);
+                    if (ok2 < best) {
+                        best = ok2;
+                        bslot = os;
+                    }
+                }
+                if (lane == 0) {
+                    M.wkey[warp] = best;
+                    M.wslot[warp] = bslot;
                 }
             }
-            if (lane == 0) {
-                M.wkey[warp] = best;
-                M.wslot[warp] = bslot;
-            }
             __syncthreads();
-            if (tid == 0) {
+            if (evict && tid == 0) {
                 uint64_t k = ~0ull;
                 int32_t sl = -1;
-                for (int w = 0; w <= kConsumerWarps; ++w)
+                for (int w = 0; w < kWarps; ++w)
                     if (M.wkey[w] < k) {
                         k = M.wkey[w];
                         sl = M.wslot[w];
@@ -482,61 +612,72 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 M.best_slot = sl;
             }
         }
+
+        // ------------------------------------------------------------- insert
+        int dest = -1;
+        bool writer = false;
+        if (evict) {
+            cluster_sync();  // (2) every CTA's candidate is ready
+            if (tid == 0) {
+                uint64_t k = ~0ull;
+                int32_t sl = -1;
+                for (int c = 0; c < S; ++c) {
+                    const uint64_t kc = ld_peer_u64(peer_addr(&M.best_key, c));
+                    const int32_t scs = ld_peer_s32(peer_addr(&M.best_slot, c));
+                    if (kc < k) {
+                        k = kc;
+                        sl = scs;
+                    }
+                }
+                if (sl < 0 && rank == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                M.dest = sl;
+            }
+            __syncthreads();
+            dest = M.dest;
+            writer = dest >= W.s_lo && dest < W.s_hi;  // the CTA that attended the victim
+        } else {
+            __syncthreads();
+            dest = P.mode == kInsertAt ? P.dest_slot : P.freelist[unit * P.freelist_len + P.freelist_idx];
+            writer = rank == 0;
+            if (dest < 0 || dest >= P.C) {
+                if (writer && tid == 0) atomicOr(P.err, KVEVICT_DEV_BAD_SLOT);
+                dest = -1;
+            }
+        }
+        if (writer && dest >= 0) {
+            const T *kn = static_cast<const T *>(P.k_new) + unit * D;
+            const T *vn = static_cast<const T *>(P.v_new) + unit * D;
+            T *kd = static_cast<T *>(P.kc) + (unit * C + dest) * D;
+            T *vd = static_cast<T *>(P.vc) + (unit * C + dest) * D;
+            for (int j = tid; j < D; j += kThreads) {
+                kd[j] = kn[j];
+                vd[j] = vn[j];
+            }
+            if (tid == 0) {
+                const int32_t old_pos = P.pos[unit * CS + dest];
+                const float old_score = has_score ? P.score[unit * CS + dest] : 0.f;
+                const float an = has_score ? ld_peer_f32(peer_addr(&M.anew, 0)) : 0.f;
+                P.pos[unit * CS + dest] = P.p;
+                if (has_score) P.score[unit * CS + dest] = an;
+                if (P.trace != nullptr)
+                    reinterpret_cast<int4 *>(P.trace)[unit] =
+                        make_int4(dest, old_pos, __float_as_int(old_score), __float_as_int(an));
+            }
+        }
+        // Unit i + 2 reuses this unit's aux buffer: every thread is past its
+        // last read of it at the barriers below.
+        __syncthreads();
+        cluster_sync();  // (last) no CTA moves on while a peer may still read its shared memory
     }
 
-    // ------------------------------------------------------------- insert
-    int dest = -1;
-    bool writer = false;
-    if (P.mode == kH2OEvict) {
-        cluster_sync();  // (2) every CTA's candidate is ready
-        if (tid == 0) {
-            uint64_t k = ~0ull;
-            int32_t sl = -1;
-            for (int c = 0; c < S; ++c) {
-                const uint64_t kc = ld_peer_u64(peer_addr(&M.best_key, c));
-                const int32_t sc = ld_peer_s32(peer_addr(&M.best_slot, c));
-                if (kc < k) {
-                    k = kc;
-                    sl = sc;
-                }
-            }
-            if (sl < 0 && rank == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
-            M.dest = sl;
-        }
-        __syncthreads();
-        dest = M.dest;
-        writer = dest >= s_lo && dest < s_hi;  // the CTA that attended the victim
-    } else {
-        __syncthreads();
-        dest = P.mode == kInsertAt ? P.dest_slot
-                                   : P.freelist[unit * P.freelist_len + P.freelist_idx];
-        writer = rank == 0;
-        if (dest < 0 || dest >= P.C) {
-            if (writer && tid == 0) atomicOr(P.err, KVEVICT_DEV_BAD_SLOT);
-            dest = -1;
-        }
+    // After a timed-out wait some copies may still be landing: wait for them
+    // (bounded) before the CTA exits.
+    if (tid == 0 && M.abort) {
+        for (int st = 0; st < NST; ++st)
+            if (M.issued[st] > 0) mbar_wait(&M.full[st], (M.issued[st] - 1) & 1);
+        for (int b = 0; b < 2; ++b)
+            if (M.aux_issued[b] > 0) mbar_wait(&M.auxbar[b], (M.aux_issued[b] - 1) & 1);
     }
-    if (writer && dest >= 0) {
-        const T *kn = static_cast<const T *>(P.k_new) + unit * D;
-        const T *vn = static_cast<const T *>(P.v_new) + unit * D;
-        T *kd = static_cast<T *>(P.kc) + (unit * C + dest) * D;
-        T *vd = static_cast<T *>(P.vc) + (unit * C + dest) * D;
-        for (int i = tid; i < D; i += kThreads) {
-            kd[i] = kn[i];
-            vd[i] = vn[i];
-        }
-        if (tid == 0) {
-            const int32_t old_pos = P.pos[unit * C + dest];
-            const float old_score = P.score != nullptr ? P.score[unit * C + dest] : 0.f;
-            const float an = P.score != nullptr ? ld_peer_f32(peer_addr(&M.anew, 0)) : 0.f;
-            P.pos[unit * C + dest] = P.p;
-            if (P.score != nullptr) P.score[unit * C + dest] = an;
-            if (P.trace != nullptr)
-                reinterpret_cast<int4 *>(P.trace)[unit] = make_int4(dest, old_pos, __float_as_int(old_score),
-                                                                    __float_as_int(an));
-        }
-    }
-    cluster_sync();  // (last) no CTA leaves while a peer may still read its shared memory
 }
 
 }  // namespace kvevict

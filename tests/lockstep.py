@@ -52,11 +52,13 @@ def host_inputs(w, units, n_steps, prompt_len):
 
 
 def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, device, snap_steps=(),
-            split: int | None = None, out_seqs=None, seed: int = 0) -> GpuRun:
+            split: int | None = None, out_seqs=None, seed: int = 0, clusters: int | None = None) -> GpuRun:
     """Runs n_steps decode steps of the given layers at the workload's shape."""
     cache = KVEvictCache.from_workload(w, device=device)
     if split:
         cache.set_split(split)
+    if clusters:
+        cache.set_clusters(clusters)
     B, Hq, Hkv, D, G = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.group
     dt = torch_dtype(w)
     gen = torch.Generator(device=device)

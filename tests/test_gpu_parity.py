@@ -71,6 +71,27 @@ def test_h2o_small_splits(cuda_device, split):
         ls.check_selector(w, run, layer, w.prompt_len)
 
 
+@pytest.mark.parametrize("policy,split,clusters", [
+    (configs.POLICY_H2O, 1, 3), (configs.POLICY_H2O, 2, 5), (configs.POLICY_SINK_WINDOW, 1, 2),
+    (configs.POLICY_SINK_WINDOW, 4, 3), (configs.POLICY_RANDOM, 2, 3)])
+def test_persistent_loop_with_refills(cuda_device, policy, split, clusters):
+    """Few clusters, many units each, and more K/V tiles per unit than ring
+    stages: the ring keeps streaming across unit boundaries and every stage is
+    refilled many times."""
+    kw = {configs.POLICY_H2O: dict(n_sink=4, n_heavy=300, n_recent=100, budget=404, prompt_len=500),
+          configs.POLICY_SINK_WINDOW: dict(n_sink=4, n_recent=700, budget=704, prompt_len=720),
+          configs.POLICY_RANDOM: dict(budget=60, r=12, max_prompt=400, prompt_len=390)}[policy]
+    T = 90
+    w = _small(policy, configs.DTYPE_F32, G=2, d=64, B=5, L=1, decode_steps=T, **kw)
+    units = _all_units(w, [0])
+    inputs = ls.host_inputs(w, units, T, w.prompt_len)
+    run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=range(0, T, 9), split=split,
+                     clusters=clusters)
+    assert run.err == 0
+    reps = ls.replay_all(w, units, inputs, run, T)
+    print(f"persistent policy {policy} split {split} clusters {clusters}:", _report(reps))
+
+
 @pytest.mark.parametrize("G,d", [(1, 128), (4, 128), (8, 64)])
 def test_h2o_small_bf16_gqa(cuda_device, G, d):
     w = _small(configs.POLICY_H2O, configs.DTYPE_BF16, G=G, d=d, n_sink=2, n_heavy=50, n_recent=44, budget=96,
