@@ -236,6 +236,8 @@ def run_ours(args, w, rank, world, device):
             cache.set_split(args.split)
         if args.clusters:
             cache.set_clusters(args.clusters)
+        if args.path:
+            cache.set_path(args.path)
         P = steady_state(cache, w, device)
         L, B, Hq, Hkv, D = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
         n_pre = 0
@@ -319,7 +321,7 @@ def run_ours(args, w, rank, world, device):
                    "d2h_bytes_per_step": d2h, "steps": n_e2e}
         cache.close()
     return dict(dt_ms=dt_ms, clocks=clk.summary(), decode_launches=decode_launches, cut_launches=cut_launches,
-                iso_ms=iso, e2e=e2e, split=st["split"], clusters=st["clusters"])
+                iso_ms=iso, e2e=e2e, split=st["split"], clusters=st["clusters"], tensor_cores=st["tensor_cores"])
 
 
 def main():
@@ -331,6 +333,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--split", type=int, default=0)
     ap.add_argument("--clusters", type=int, default=0, help="persistent grid size in clusters (0 = automatic)")
+    ap.add_argument("--path", type=int, default=0, help="0 automatic, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
@@ -394,7 +397,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": r["dt_ms"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded N(0,1) Q/K/V with hub and sink keys, generated on the device)",
-        "config": dict(cfg, split=r["split"], clusters=r["clusters"],
+        "config": dict(cfg, split=r["split"], clusters=r["clusters"], tensor_cores=bool(r["tensor_cores"]),
                        timing="CUDA events on the launching stream; no L2 flush needed"),
         "layer_step_us": 1e6 * avg_launch_s,
         "kernel_us_isolated": 1e3 * statistics.median(r["iso_ms"]) if r["iso_ms"] else None,

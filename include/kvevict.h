@@ -114,6 +114,7 @@ typedef struct {
     int split;              /* CTAs per unit in the decode launch (thread-block cluster size) */
     int capacity;           /* slots per unit */
     int clusters;           /* clusters in the last decode launch's persistent grid (0 before any) */
+    int tensor_cores;       /* 1 if the decode path uses the tensor cores (mma), 0 for CUDA cores */
 } kvevict_stats;
 
 /* Bytes of device memory a handle with this configuration needs (cache,
@@ -183,6 +184,15 @@ int kvevict_layer_state(kvevict_t h, int layer, int *prompt_len, int *steps, int
 /* CTAs per unit of the decode launch (1, 2, 4, 8 or 16; 0 = automatic).
  * A tuning knob: results do not depend on it beyond fp32 rounding order. */
 int kvevict_set_split(kvevict_t h, int split);
+
+/* Decode arithmetic: 0 = automatic (tensor cores for bf16 caches with
+ * G >= 2, CUDA cores otherwise), 1 = CUDA cores, 2 = tensor cores (bf16
+ * only; mma.sync m16n8k16 with the G query heads padded to 16 rows). A
+ * tuning and test knob: both paths compute the same step, they differ in
+ * rounding only (the tensor-core path rounds probabilities to bf16 for PV).
+ * INVALID_ARG if the path is not available for the handle's dtype or its
+ * shared memory would not fit. */
+int kvevict_set_path(kvevict_t h, int path);
 
 /* Number of clusters in the decode launch's persistent grid (each cluster
  * loops over units; 0 = automatic: as many as fit on the GPU at once, chosen

@@ -29,7 +29,7 @@ class Config(ctypes.Structure):
 class Stats(ctypes.Structure):
     _fields_ = [("decode_steps", ctypes.c_int64), ("prefill_tokens", ctypes.c_int64),
                 ("evictions", ctypes.c_int64), ("cuts", ctypes.c_int64), ("split", ctypes.c_int),
-                ("capacity", ctypes.c_int), ("clusters", ctypes.c_int)]
+                ("capacity", ctypes.c_int), ("clusters", ctypes.c_int), ("tensor_cores", ctypes.c_int)]
 
 
 class KVEvictError(RuntimeError):
@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
             L.kvevict_layer_state.argtypes = [P, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
             L.kvevict_set_split.argtypes = [P, I]
             L.kvevict_set_clusters.argtypes = [P, I]
+            L.kvevict_set_path.argtypes = [P, I]
             L.kvevict_get_stats.argtypes = [P, ctypes.POINTER(Stats)]
             L.kvevict_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             L.kvevict_strerror.argtypes = [I]
@@ -70,7 +71,8 @@ def lib() -> ctypes.CDLL:
             L.kvevict_destroy.restype = None
             for n in ("kvevict_state_bytes", "kvevict_create", "kvevict_prefill", "kvevict_decode_step",
                       "kvevict_decode_step_host", "kvevict_slot_positions", "kvevict_scores", "kvevict_set_trace",
-                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_get_stats",
+                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path",
+                      "kvevict_get_stats",
                       "kvevict_check"):
                 getattr(L, n).restype = I
             _lib = L

@@ -143,6 +143,10 @@ class KVEvictCache:
     def set_split(self, split: int) -> None:
         check(self._L.kvevict_set_split(self.h, split), "kvevict_set_split")
 
+    def set_path(self, path: int) -> None:
+        """0 automatic, 1 CUDA cores, 2 tensor cores (bf16 only)."""
+        check(self._L.kvevict_set_path(self.h, path), "kvevict_set_path")
+
     def set_clusters(self, clusters: int) -> None:
         check(self._L.kvevict_set_clusters(self.h, clusters), "kvevict_set_clusters")
 

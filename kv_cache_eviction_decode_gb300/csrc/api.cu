@@ -5,6 +5,9 @@
 // are occupied, where an insert goes before the cache is full, when Random
 // cuts) depends only on the number of prompt tokens and decode steps so far,
 // never on values, so it is tracked here on the host and passed by value.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
@@ -126,11 +129,16 @@ struct kvevict_handle {
     cudaStream_t stream = nullptr;
     int split = 1;
     int clusters_req = 0;  // persistent grid size in clusters; 0 = automatic
+    int last_layer = -1;   // layer of the last kernel this handle queued (-1: none, or unknown)
+    int path_req = 0;      // 0 automatic, 1 CUDA cores, 2 tensor cores
+    bool use_mma = false;  // decode path in use
+    std::vector<CUtensorMap> tmk, tmv;  // per layer (bf16 caches)
     std::vector<LayerState> layers;
     kvevict_stats stats{};
     // decode kernel configured for (split, holes): function, shared memory, zcap
     struct Configured {
         int split = 0, clusters_req = -1;
+        bool mma = false;
         DecodeKernelInfo ki{};
         size_t smem = 0;
         int zc = 0;
@@ -162,7 +170,7 @@ constexpr size_t kMaxSmem = 227 * 1024;
 size_t decode_smem(const kvevict_handle *h, int S, bool holes)
 {
     DecodeKernelInfo ki;
-    if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, &ki)) return ~size_t(0);
+    if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, &ki)) return ~size_t(0);
     return ki.smem_bytes(ki.zcap(max_slots_per_cta(h->L, S)), n_aux_arrays(h->cfg, holes));
 }
 
@@ -185,7 +193,7 @@ int auto_split(const kvevict_handle *h)
 
 int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInfo *ki, size_t *smem, int *zc)
 {
-    if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, ki)) return KVEVICT_ERR_INVALID_ARG;
+    if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, ki)) return KVEVICT_ERR_INVALID_ARG;
     *zc = ki->zcap(max_slots_per_cta(h->L, S));
     *smem = ki->smem_bytes(*zc, n_aux_arrays(h->cfg, holes));
     if (*smem > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
@@ -195,6 +203,35 @@ int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInf
 }
 
 template <typename T> T *at(const kvevict_handle *h, size_t off) { return reinterpret_cast<T *>(h->state + off); }
+
+// 2-D tensor map over one layer's K or V cache: rows = units * C, each of
+// head_dim bf16; boxes of 32 rows x 64 elements, 128-byte swizzle.
+int make_tensor_map(CUtensorMap *out, void *base, uint64_t rows, int head_dim)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return KVEVICT_ERR_CUDA;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::fprintf(stderr, "kvevict: cuTensorMapEncodeTiled failed (%d)\n", static_cast<int>(r));
+        return KVEVICT_ERR_CUDA;
+    }
+    return KVEVICT_OK;
+}
+
+bool mma_possible(const kvevict_config &c) { return c.dtype == KVEVICT_BF16; }
+bool mma_auto(const kvevict_config &c) { return mma_possible(c) && c.n_q_heads / c.n_kv_heads >= 2; }
 
 // Persistent grid size, in clusters: at most what the GPU holds at once, and
 // where possible a count that divides the units evenly (every cluster then
@@ -298,19 +335,26 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     }
 
     auto &cfgd = h->configured[holes ? 1 : 0];
-    if (cfgd.split != h->split || cfgd.clusters_req != h->clusters_req) {
+    if (cfgd.split != h->split || cfgd.clusters_req != h->clusters_req || cfgd.mma != h->use_mma) {
         int rc0 = configure_kernel(h, h->split, holes, &cfgd.ki, &cfgd.smem, &cfgd.zc);
         if (rc0) return rc0;
         rc0 = pick_clusters(h, h->split, cfgd.ki, cfgd.smem, &cfgd.clusters);
         if (rc0) return rc0;
         cfgd.split = h->split;
         cfgd.clusters_req = h->clusters_req;
+        cfgd.mma = h->use_mma;
     }
     const DecodeKernelInfo &ki = cfgd.ki;
     const size_t smem = cfgd.smem;
     int rc = KVEVICT_OK;
     P.split = h->split;
     P.zcap = cfgd.zc;
+    P.prefetch_early = (h->last_layer >= 0 && h->last_layer != layer) ? 1 : 0;
+    if (h->use_mma) {
+        static_assert(sizeof(CUtensorMap) == sizeof(TensorMapBytes), "tensor map size");
+        std::memcpy(&P.tmk, &h->tmk[layer], sizeof(CUtensorMap));
+        std::memcpy(&P.tmv, &h->tmv[layer], sizeof(CUtensorMap));
+    }
 
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(cfgd.clusters * h->split, 1, 1);
@@ -329,6 +373,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     void *args[] = {&P};
     rc = cuda_status(cudaLaunchKernelExC(&lc, ki.fn, args));
     if (rc) return rc;
+    h->last_layer = layer;
 
     // Bookkeeping of what the step did.
     if (P.trace) ls.trace_t++;
@@ -352,6 +397,9 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
             cp.Hkv = c.n_kv_heads;
             cp.C = L.C;
             cp.cstride = L.Cs;
+            cp.kc = P.kc;
+            cp.vc = P.vc;
+            cp.row_bytes = c.head_dim * L.elem;
             cp.first_slot = ls.prompt_len;
             cp.n_cand = c.budget + c.r;
             cp.n_pow2 = 1;
@@ -400,9 +448,24 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
     h->state = static_cast<uint8_t *>(state);
     h->stream = static_cast<cudaStream_t>(cuda_stream);
     h->layers.resize(cfg->n_layers);
+    h->use_mma = mma_auto(*cfg);
+    if (mma_possible(*cfg)) {
+        h->tmk.resize(cfg->n_layers);
+        h->tmv.resize(cfg->n_layers);
+        for (int l = 0; l < cfg->n_layers; ++l) {
+            int rc0 = make_tensor_map(&h->tmk[l], h->state + L.off_k + l * L.kv_layer_bytes, L.layer_slots, cfg->head_dim);
+            if (!rc0) rc0 = make_tensor_map(&h->tmv[l], h->state + L.off_v + l * L.kv_layer_bytes, L.layer_slots, cfg->head_dim);
+            if (rc0) {
+                delete h;
+                return rc0;
+            }
+        }
+    }
     h->split = auto_split(h);
-    // Empty cache: every position -1, every score 0, no error bits.
-    cudaError_t e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_pslots * 4, h->stream);
+    // Empty cache: K/V zero (every row a tile may touch is finite), every
+    // position -1, every score 0, no error bits.
+    cudaError_t e = cudaMemsetAsync(h->state + L.off_k, 0, L.off_pos - L.off_k, h->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_pslots * 4, h->stream);
     if (e == cudaSuccess && cfg->policy == KVEVICT_H2O)
         e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_pslots * 4, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
@@ -459,6 +522,7 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
     launch_prefill(P, (P.a1 - P.a0) + (P.b1 - P.b0), c.batch, h->stream);
     int rc = cuda_status(cudaGetLastError());
     if (rc) return rc;
+    h->last_layer = layer;
     ls.prompt_len += n_tokens;
     ls.count = c.policy == KVEVICT_RANDOM ? ls.prompt_len : std::min(L.C, ls.prompt_len);
     h->stats.prefill_tokens += n_tokens;
@@ -483,6 +547,7 @@ int kvevict_decode_step_host(kvevict_t h, int layer, const void *q, const void *
     if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
     const Layout &L = h->L;
     void *dq = h->state + L.off_sq, *dk = h->state + L.off_sk, *dv = h->state + L.off_sv, *dout = h->state + L.off_so;
+    h->last_layer = -1;  // the launch follows copies, not a kernel of this handle
     cudaError_t e = cudaMemcpyAsync(dq, q, L.q_bytes, cudaMemcpyHostToDevice, h->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k_new, L.kvtok_bytes, cudaMemcpyHostToDevice, h->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v_new, L.kvtok_bytes, cudaMemcpyHostToDevice, h->stream);
@@ -556,6 +621,22 @@ int kvevict_set_split(kvevict_t h, int split)
     return KVEVICT_OK;
 }
 
+int kvevict_set_path(kvevict_t h, int path)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (path < 0 || path > 2) return KVEVICT_ERR_INVALID_ARG;
+    if (path == 2 && !mma_possible(h->cfg)) return KVEVICT_ERR_INVALID_ARG;
+    const bool mma = path == 0 ? mma_auto(h->cfg) : path == 2;
+    const bool old = h->use_mma;
+    h->use_mma = mma;
+    if (decode_smem(h, h->split, h->cfg.policy == KVEVICT_RANDOM) > kMaxSmem) {
+        h->use_mma = old;
+        return KVEVICT_ERR_INVALID_ARG;
+    }
+    h->path_req = path;
+    return KVEVICT_OK;
+}
+
 int kvevict_set_clusters(kvevict_t h, int clusters)
 {
     if (!h) return KVEVICT_ERR_INVALID_ARG;
@@ -569,6 +650,7 @@ int kvevict_get_stats(kvevict_t h, kvevict_stats *out)
     if (!h || !out) return KVEVICT_ERR_INVALID_ARG;
     *out = h->stats;
     out->clusters = h->configured[0].clusters ? h->configured[0].clusters : h->configured[1].clusters;
+    out->tensor_cores = h->use_mma ? 1 : 0;
     return KVEVICT_OK;
 }
 

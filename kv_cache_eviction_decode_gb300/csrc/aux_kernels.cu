@@ -105,6 +105,14 @@ __global__ void __launch_bounds__(kCutThreads) random_cut_kernel(const CutParams
         P.freelist[unit * P.r + rnk] = s;
         pos[s] = -1;
     }
+    // Zero the freed rows: until refilled they are masked out, and a zero
+    // row is finite whatever value the evicted token held.
+    const int vecs = P.row_bytes / 16;
+    for (int i = tid; i < P.r * vecs; i += blockDim.x) {
+        const size_t row = unit * P.C + freed[i / vecs];
+        reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.kc) + row * P.row_bytes)[i % vecs] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.vc) + row * P.row_bytes)[i % vecs] = make_uint4(0, 0, 0, 0);
+    }
 }
 
 void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st)

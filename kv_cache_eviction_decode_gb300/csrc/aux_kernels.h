@@ -21,8 +21,10 @@ struct PrefillParams {
 };
 
 struct CutParams {
-    int32_t *pos;       // layer [B][Hkv][C]
+    int32_t *pos;       // layer [B][Hkv][cstride]
     int32_t *freelist;  // layer [B][Hkv][r]
+    void *kc, *vc;      // layer cache [B][Hkv][C][D]: freed rows are zeroed
+    int row_bytes;
     uint64_t seed;
     int layer, step, Hkv, C, cstride;
     int first_slot, n_cand, n_pow2, r;

@@ -5,30 +5,36 @@
 namespace kvevict {
 namespace {
 
-template <int D, int G, bool H> DecodeKernelInfo info()
+template <int D, int G, bool H, bool MMA> DecodeKernelInfo info()
 {
-    using L = DecodeLayout<__nv_bfloat16, D, G>;
-    return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<__nv_bfloat16, D, G, H>),
+    using L = DecodeLayout<__nv_bfloat16, D, G, MMA>;
+    return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<__nv_bfloat16, D, G, H, MMA>),
                             [](int zc, int n_aux) { return L::bytes(zc, n_aux); }, [](int n) { return L::zcap(n); }};
 }
 
-template <int D, bool H> bool pick_g(int G, DecodeKernelInfo *out)
+template <int D, bool H, bool MMA> bool pick_g(int G, DecodeKernelInfo *out)
 {
     switch (G) {
-    case 1: *out = info<D, 1, H>(); return true;
-    case 2: *out = info<D, 2, H>(); return true;
-    case 4: *out = info<D, 4, H>(); return true;
-    case 8: *out = info<D, 8, H>(); return true;
+    case 1: *out = info<D, 1, H, MMA>(); return true;
+    case 2: *out = info<D, 2, H, MMA>(); return true;
+    case 4: *out = info<D, 4, H, MMA>(); return true;
+    case 8: *out = info<D, 8, H, MMA>(); return true;
     default: return false;
     }
 }
 
 }  // namespace
 
-bool decode_kernel_bf16(int head_dim, int G, bool holes, DecodeKernelInfo *out)
+bool decode_kernel_bf16(int head_dim, int G, bool holes, bool mma, DecodeKernelInfo *out)
 {
-    if (head_dim == 64) return holes ? pick_g<64, true>(G, out) : pick_g<64, false>(G, out);
-    if (head_dim == 128) return holes ? pick_g<128, true>(G, out) : pick_g<128, false>(G, out);
+    if (head_dim == 64) {
+        if (mma) return holes ? pick_g<64, true, true>(G, out) : pick_g<64, false, true>(G, out);
+        return holes ? pick_g<64, true, false>(G, out) : pick_g<64, false, false>(G, out);
+    }
+    if (head_dim == 128) {
+        if (mma) return holes ? pick_g<128, true, true>(G, out) : pick_g<128, false, true>(G, out);
+        return holes ? pick_g<128, true, false>(G, out) : pick_g<128, false, false>(G, out);
+    }
     return false;
 }
 

@@ -12,13 +12,15 @@ struct DecodeKernelInfo {
     int (*zcap)(int max_slots_per_cta);
 };
 
-// dtype: 0 fp32, 1 bf16. Returns false if the combination is not built.
+// dtype: 0 fp32, 1 bf16; mma: the tensor-core path (bf16 only). Returns
+// false if the combination is not built.
 bool decode_kernel_f32(int head_dim, int G, bool holes, DecodeKernelInfo *out);
-bool decode_kernel_bf16(int head_dim, int G, bool holes, DecodeKernelInfo *out);
+bool decode_kernel_bf16(int head_dim, int G, bool holes, bool mma, DecodeKernelInfo *out);
 
-inline bool decode_kernel(int dtype, int head_dim, int G, bool holes, DecodeKernelInfo *out)
+inline bool decode_kernel(int dtype, int head_dim, int G, bool holes, bool mma, DecodeKernelInfo *out)
 {
-    return dtype == 0 ? decode_kernel_f32(head_dim, G, holes, out) : decode_kernel_bf16(head_dim, G, holes, out);
+    if (dtype == 0) return !mma && decode_kernel_f32(head_dim, G, holes, out);
+    return decode_kernel_bf16(head_dim, G, holes, mma, out);
 }
 
 }  // namespace kvevict

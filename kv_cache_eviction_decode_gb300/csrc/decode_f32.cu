@@ -5,20 +5,20 @@
 namespace kvevict {
 namespace {
 
-template <int D, int G, bool H> DecodeKernelInfo info()
+template <int D, int G, bool H, bool MMA> DecodeKernelInfo info()
 {
-    using L = DecodeLayout<float, D, G>;
-    return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<float, D, G, H>),
+    using L = DecodeLayout<float, D, G, MMA>;
+    return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<float, D, G, H, MMA>),
                             [](int zc, int n_aux) { return L::bytes(zc, n_aux); }, [](int n) { return L::zcap(n); }};
 }
 
-template <int D, bool H> bool pick_g(int G, DecodeKernelInfo *out)
+template <int D, bool H, bool MMA> bool pick_g(int G, DecodeKernelInfo *out)
 {
     switch (G) {
-    case 1: *out = info<D, 1, H>(); return true;
-    case 2: *out = info<D, 2, H>(); return true;
-    case 4: *out = info<D, 4, H>(); return true;
-    case 8: *out = info<D, 8, H>(); return true;
+    case 1: *out = info<D, 1, H, MMA>(); return true;
+    case 2: *out = info<D, 2, H, MMA>(); return true;
+    case 4: *out = info<D, 4, H, MMA>(); return true;
+    case 8: *out = info<D, 8, H, MMA>(); return true;
     default: return false;
     }
 }
@@ -27,8 +27,8 @@ template <int D, bool H> bool pick_g(int G, DecodeKernelInfo *out)
 
 bool decode_kernel_f32(int head_dim, int G, bool holes, DecodeKernelInfo *out)
 {
-    if (head_dim == 64) return holes ? pick_g<64, true>(G, out) : pick_g<64, false>(G, out);
-    if (head_dim == 128) return holes ? pick_g<128, true>(G, out) : pick_g<128, false>(G, out);
+    if (head_dim == 64) return holes ? pick_g<64, true, false>(G, out) : pick_g<64, false, false>(G, out);
+    if (head_dim == 128) return holes ? pick_g<128, true, false>(G, out) : pick_g<128, false, false>(G, out);
     return false;
 }
 

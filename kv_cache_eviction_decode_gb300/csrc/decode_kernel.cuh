@@ -5,28 +5,34 @@
 // c, c + n_clusters, ...; inside a cluster the CTAs divide each unit's
 // occupied slots into contiguous ranges of 32-slot tiles.
 //
-// Memory pipeline: a ring of NST shared-memory stages, each filled by one
-// bulk (TMA) global->shared copy of a 32-slot K or V tile that completes on
-// the stage's mbarrier. The CTA's tiles form one sequence over all of its
-// units (unit 0's K tiles, its V tiles, unit 1's K tiles, ...). Thread 0
-// issues the first NST copies; after that, the warp that consumes tile s
-// issues the copy of tile s + NST into the stage it has just freed. The ring
-// therefore keeps streaming across unit boundaries: the next unit's first
-// tiles land while the current unit's combine and score epilogue run. The
-// next unit's slot positions (and H2O scores) are prefetched the same way
-// into a second, double-buffered shared-memory area.
+// Memory pipeline: a ring of NST shared-memory stages, each filled by TMA
+// copies of one 32-slot K or V tile that complete on the stage's mbarrier:
+// one 1-D bulk copy (CUDA-core path), or two 2-D tensor-map boxes of 32 x 64
+// bf16 with the 128-byte swizzle (tensor-core path; conflict-free ldmatrix).
+// The CTA's tiles form one sequence over all of its units (unit 0's K tiles,
+// its V tiles, unit 1's K tiles, ...). Thread 0 issues the first NST copies;
+// after that, the warp that consumes tile s issues the copy of tile s + NST
+// into the stage it has just freed, so the ring keeps streaming across unit
+// boundaries: the next unit's first tiles land while the current unit's
+// combine and score epilogue run. The next unit's slot positions (and H2O
+// scores) are prefetched into a double-buffered shared-memory area, and its
+// q / k_new into registers.
 //
 // Per unit, every CTA:
-//   K phase   each warp takes whole K tiles and forms the logits
-//             z = q.k / sqrt(d) of the G query heads for 32 slots: every lane
-//             holds d/32 coordinates of q and of each key, and a 31-shuffle
-//             butterfly transposes the partial sums so lane i ends with one
-//             (head, slot) logit. Logits stay in shared memory (log2 units).
+//   K phase   logits z = q.k / sqrt(d) of the G query heads for each slot,
+//             kept in shared memory (log2 units):
+//               CUDA cores   every lane holds d/32 coordinates of q and of
+//                            each key; a 31-shuffle butterfly transposes the
+//                            partial sums so lane i ends with one logit;
+//               tensor cores S = Q K^T with mma.sync m16n8k16 (bf16 in, fp32
+//                            accumulate): the G heads (padded to 16) are M,
+//                            8 slots are N, head_dim is K; K rows by ldmatrix.
 //   V phase   with the CTA-local max m_c known, p = 2^(z - m_c) is written
-//             back over z and o += p v is accumulated.
+//             back over z and o += p v is accumulated (tensor cores: P as the
+//             A operand in registers, V by ldmatrix.trans).
 //   combine   (m_c, l_c, o_c) of every CTA in the cluster are read through
 //             distributed shared memory; each CTA writes its share of
-//             out = sum_c o_c 2^(m_c - m) / l.
+//             out = sum_c o_c 2^(m_c - m) / l. Rank 0 adds the new token.
 //   scores    (H2O) every retained slot's cumulative score grows by
 //             (1/G) sum_g p_g 2^(m_c - m) / l; the eligible slot with the
 //             smallest (score, position) is the CTA's candidate, and a
@@ -55,6 +61,7 @@ constexpr int kTile = 32;  // slots per pipeline stage
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSplit = 16;
+constexpr int kSmemAlign = 1024;  // 128-byte swizzle atoms are 1 KB
 
 enum InsertMode : int {
     kInsertAt = 0,     // the host gives the slot (empty slot, or the ring slot)
@@ -62,14 +69,21 @@ enum InsertMode : int {
     kFromFreeList = 2  // Random after a cut: next entry of the unit's free list
 };
 
+// Opaque 128-byte tensor map (CUtensorMap), 64-byte aligned as a kernel
+// parameter requires.
+struct alignas(64) TensorMapBytes {
+    uint64_t word[16];
+};
+
 struct DecodeParams {
+    TensorMapBytes tmk, tmv;  // tensor maps of this layer's K and V (tensor-core path)
     const void *q;       // [B][Hkv*G][D]
     const void *k_new;   // [B][Hkv][D]
     const void *v_new;   // [B][Hkv][D]
     void *out;           // [B][Hkv*G][D]
     void *kc, *vc;       // this layer's cache, [B][Hkv][C][D]
-    int32_t *pos;        // [B][Hkv][C]
-    float *score;        // [B][Hkv][C], or null when the policy keeps no scores
+    int32_t *pos;        // [B][Hkv][cstride]
+    float *score;        // [B][Hkv][cstride], or null when the policy keeps no scores
     const int32_t *freelist;  // [B][Hkv][freelist_len]
     int32_t *trace;      // [B][Hkv][4] or null: slot, evicted position, evicted score, new score
     uint32_t *err;
@@ -82,23 +96,27 @@ struct DecodeParams {
     int n_sink, n_recent;
     int split;           // CTAs per unit (cluster size)
     int zcap;            // per-head stride of the logit buffer (and aux slots)
+    int prefetch_early;  // the launch before this one did not touch this layer: cache tiles may be
+                         // fetched before the programmatic-dependency wait (inputs still after it)
     float scale_log2;    // log2(e) / sqrt(D)
 };
 
-// Shared-memory layout, shared by host (size) and device (offsets).
-template <typename T, int D, int G> struct DecodeLayout {
-    static constexpr int kEPL = D / 32;  // key/value coordinates per lane
-    static constexpr int kR = 32 / G;    // slots per butterfly chunk
+// Shared-memory layout, shared by host (size) and device (offsets). All
+// offsets are from a base aligned up to kSmemAlign inside the allocation.
+template <typename T, int D, int G, bool MMA> struct DecodeLayout {
+    static constexpr int kEPL = D / 32;  // key/value coordinates per lane (CUDA-core path)
+    static constexpr int kR = 32 / G;    // slots per butterfly chunk (CUDA-core path)
     static constexpr int kStageBytes = kTile * D * static_cast<int>(sizeof(T));
     static constexpr int kStages = (81920 / kStageBytes) < 6 ? 6 : (81920 / kStageBytes);
     static constexpr int kStageArea = kStages * kStageBytes;
     static constexpr int kPartBytes = kWarps * G * D * 4;
     static_assert(G >= 1 && G <= 8 && (G & (G - 1)) == 0, "G in {1,2,4,8}");
+    static_assert(!MMA || (sizeof(T) == 2 && D % 64 == 0), "tensor-core path: bf16, head_dim multiple of 64");
 
     struct Misc {
         uint64_t full[kStages];
         uint64_t auxbar[2];
-        uint32_t issued[kStages];  // copies issued per stage (drain after a timeout)
+        uint32_t issued[kStages];  // copies issued per stage
         uint32_t aux_issued[2];
         int abort;
         float wmax[kWarps][G];
@@ -117,13 +135,13 @@ template <typename T, int D, int G> struct DecodeLayout {
         int32_t wslot[kWarps];
     };
 
-    // zcap = slots per CTA rounded to whole tiles; for G > 1 padded so that
-    // zcap == R (mod 32): the lane groups of different heads then hit
-    // distinct shared-memory banks.
+    // zcap = slots per CTA rounded to whole tiles, padded so that the head
+    // rows of the logit buffer start on different banks: == R (mod 32) for
+    // the butterfly's lane groups, == 8 (mod 32) for the mma fragments.
     __host__ __device__ static int zcap(int max_slots_per_cta)
     {
         int z = ((max_slots_per_cta + kTile - 1) / kTile) * kTile;
-        return G > 1 ? z + kR : z;
+        return MMA ? z + 8 : (G > 1 ? z + kR : z);
     }
     __host__ __device__ static size_t off_z() { return kStageArea; }
     __host__ __device__ static size_t off_part(int zc) { return kStageArea + ((static_cast<size_t>(G) * zc * 4 + 127) / 128) * 128; }
@@ -132,7 +150,7 @@ template <typename T, int D, int G> struct DecodeLayout {
     __host__ __device__ static size_t off_aux(int zc) { return off_part(zc) + kPartBytes; }
     __host__ __device__ static size_t aux_bytes(int zc) { return ((static_cast<size_t>(zc) * 4 + 15) / 16) * 16; }
     __host__ __device__ static size_t off_misc(int zc, int n_arrays) { return off_aux(zc) + 2 * n_arrays * aux_bytes(zc); }
-    __host__ __device__ static size_t bytes(int zc, int n_arrays) { return off_misc(zc, n_arrays) + sizeof(Misc); }
+    __host__ __device__ static size_t bytes(int zc, int n_arrays) { return off_misc(zc, n_arrays) + sizeof(Misc) + kSmemAlign; }
 };
 
 // Butterfly transpose-reduce: lane L holds 32 partial sums v[0..31]; after
@@ -174,35 +192,73 @@ struct Work {
     int total_seq;                        // K and V tiles over all units
 };
 
-template <typename T, int D> struct TileSource {
+// Tile s of the CTA's sequence: unit, K or V, which 32 slots.
+struct TileAt {
+    size_t unit;
+    bool is_k;
+    int slot0, rows;
+};
+
+__device__ __forceinline__ TileAt tile_at(const Work &W, int s)
+{
+    const int two_nt = 2 * W.nt;
+    const int i = s / two_nt, loc = s - i * two_nt;
+    TileAt t;
+    t.unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
+    t.is_k = loc < W.nt;
+    t.slot0 = W.s_lo + (t.is_k ? loc : loc - W.nt) * kTile;
+    t.rows = min(kTile, W.s_hi - t.slot0);
+    return t;
+}
+
+// CUDA-core path: one contiguous bulk copy per tile (only the valid rows).
+template <typename T, int D> struct BulkTileSource {
     const T *kc, *vc;
     size_t C;
     __device__ __forceinline__ void issue(const Work &W, int s, T *stage, uint64_t *bar) const
     {
-        const int two_nt = 2 * W.nt;
-        const int i = s / two_nt, loc = s - i * two_nt;
-        const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
-        const int tile = loc < W.nt ? loc : loc - W.nt;
-        const int slot0 = W.s_lo + tile * kTile;
-        const int rows = min(kTile, W.s_hi - slot0);
-        const uint32_t bytes = static_cast<uint32_t>(rows * D * sizeof(T));
-        const T *src = (loc < W.nt ? kc : vc) + (unit * C + slot0) * D;
+        const TileAt t = tile_at(W, s);
+        const uint32_t bytes = static_cast<uint32_t>(t.rows * D * sizeof(T));
+        const T *src = (t.is_k ? kc : vc) + (t.unit * C + t.slot0) * D;
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s_stream(stage, src, bytes, bar, l2_policy_evict_first());
     }
 };
 
-// Two CTAs per SM for G <= 2 (registers capped at 128 per thread).
-template <int G> constexpr int min_blocks() { return G <= 2 ? 2 : 1; }
+// Tensor-core path: D/64 tensor-map boxes of 32 rows x 64 bf16 per tile,
+// 128-byte swizzled. A box always moves 32 full rows (rows past the unit's
+// range belong to the next unit or are zero-filled past the tensor's end).
+template <int D> struct TmaTileSource {
+    const void *tmk, *tmv;
+    size_t C;
+    __device__ __forceinline__ void issue(const Work &W, int s, __nv_bfloat16 *stage, uint64_t *bar) const
+    {
+        const TileAt t = tile_at(W, s);
+        const int row = static_cast<int>(t.unit * C + t.slot0);
+        const void *tm = t.is_k ? tmk : tmv;
+        const uint64_t pol = l2_policy_evict_first();
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kTile * D * 2));
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b)
+            tma_load_2d(reinterpret_cast<uint8_t *>(stage) + b * kTile * 128, tm, b * 64, row, bar, pol);
+    }
+};
 
-template <typename T, int D, int G, bool HOLES>
-__global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(const __grid_constant__ DecodeParams P)
+// Two CTAs per SM (registers <= 128) for G <= 2; for larger G the logits
+// and accumulators need more registers and shared memory holds one CTA.
+template <int G, bool MMA> constexpr int min_blocks() { return G <= 2 ? 2 : 1; }
+
+template <typename T, int D, int G, bool HOLES, bool MMA>
+__global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_kernel(const __grid_constant__ DecodeParams P)
 {
-    using L = DecodeLayout<T, D, G>;
+    using L = DecodeLayout<T, D, G, MMA>;
     constexpr int EPL = L::kEPL, R = L::kR, NST = L::kStages;
+    constexpr int KSTEPS = D / 16;  // mma k-steps over head_dim
     using E = Elem<T>;
 
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + kSmemAlign - 1) &
+                                                ~static_cast<uintptr_t>(kSmemAlign - 1));
     T *ring = reinterpret_cast<T *>(smem);
     const int zc = P.zcap;
     float *zbuf = reinterpret_cast<float *>(smem + L::off_z());
@@ -235,7 +291,15 @@ __global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(
         W.n_mine = max(0, W.s_hi - W.s_lo);
         W.total_seq = W.n_units * 2 * W.nt;
     }
-    TileSource<T, D> src{static_cast<const T *>(P.kc), static_cast<const T *>(P.vc), C};
+    BulkTileSource<T, D> bulk_src{static_cast<const T *>(P.kc), static_cast<const T *>(P.vc), C};
+    TmaTileSource<D> tma_src{&P.tmk, &P.tmv, C};
+    auto issue_tile = [&](int s, int st) {
+        T *stage = ring + static_cast<size_t>(st) * kTile * D;
+        if constexpr (MMA)
+            tma_src.issue(W, s, reinterpret_cast<__nv_bfloat16 *>(stage), &M.full[st]);
+        else
+            bulk_src.issue(W, s, stage, &M.full[st]);
+    };
 
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) {
@@ -247,13 +311,12 @@ __global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(
         M.aux_issued[0] = M.aux_issued[1] = 0;
         M.abort = 0;
         mbar_fence_init();
+        if constexpr (MMA) {
+            prefetch_tensormap(&P.tmk);
+            prefetch_tensormap(&P.tmv);
+        }
     }
     __syncthreads();
-
-    // Everything below reads memory the previous launch on the stream may
-    // have written.
-    grid_dependency_wait();
-    grid_launch_dependents();
 
     // Bulk copy of one unit's slot positions (and scores) into aux buffer b.
     auto issue_aux = [&](int i) {
@@ -267,17 +330,23 @@ __global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(
         M.aux_issued[b]++;
     };
 
-    if (tid == 0) {
-        for (int s = 0; s < min(NST, W.total_seq); ++s)
-            src.issue(W, s, ring + static_cast<size_t>(s) * kTile * D, &M.full[s]);
+    auto issue_first = [&]() {
+        for (int s = 0; s < min(NST, W.total_seq); ++s) issue_tile(s, s);
         if (need_aux && W.n_units > 0 && W.n_mine > 0) issue_aux(0);
         __threadfence_block();
         for (int s = 0; s < min(NST, W.total_seq); ++s) M.issued[s] = 1;
-    }
+    };
+    // This layer's cache (and positions/scores) can only be written by a
+    // launch for this layer. When the launch before this one was for another
+    // layer, the first tiles are fetched while that launch is still running;
+    // the inputs q/k/v (which a preceding kernel may produce) are read only
+    // after the programmatic-dependency wait.
+    if (P.prefetch_early && tid == 0) issue_first();
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (!P.prefetch_early && tid == 0) issue_first();
 
-    const int g_lane = lane / R;  // the head this lane's logits belong to
-    bool ok = true;               // false after a timed-out wait: skip work, keep barriers
-
+    bool ok = true;  // false after a timed-out wait: skip work, keep barriers
     volatile int *abort_flag = &M.abort;
     volatile uint32_t *issued = M.issued;
     // Tile s is copy number c = s / NST into stage s % NST. Its consumer
@@ -317,24 +386,50 @@ __global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(
         const int nx = s + NST;
         if (lane == 0 && nx < W.total_seq && ok) {
             const int st = s % NST;
-            src.issue(W, nx, ring + static_cast<size_t>(st) * kTile * D, &M.full[st]);
+            issue_tile(nx, st);
             __threadfence_block();
             issued[st] = issued[st] + 1;
         }
     };
 
-    // Register prefetch of a unit's q (all lanes) and new token (rank 0).
-    float qn[G][EPL], kn_next[EPL], vn_next[EPL];
+    // Per-lane view of the logits: the CUDA-core butterfly gives lane L the
+    // head L / R; the mma fragments give lane L the head L / 4 (valid if < G).
+    const int g_lane = MMA ? (lane >> 2) : (lane / R);
+    const int t4 = lane & 3;
+    const bool lane_has_head = g_lane < G;
+    constexpr int kHeadLanes = MMA ? 4 : R;  // lanes sharing one head's partials
+
+    // Register prefetch of a unit's q (CUDA-core path: d-slices; mma path: A
+    // fragments) and, for rank 0 warp 0, the new token's key in the same
+    // layout.
+    constexpr int QG = MMA ? 1 : G, QE = MMA ? 1 : EPL, QK = MMA ? KSTEPS : 1;
+    float qn[QG][QE];
+    uint32_t qan[QK][2];
+    float kn_next[QE];
+    uint32_t kan[QK][2];
     auto load_unit_inputs = [&](size_t u) {
         const T *qp = static_cast<const T *>(P.q) + u * G * D;
+        if constexpr (MMA) {
+            const T *kp = static_cast<const T *>(P.k_new) + u * D + 2 * t4;
 #pragma unroll
-        for (int g = 0; g < G; ++g) load_f32<T, EPL>(qp + g * D + lane * EPL, qn[g]);
-        if (rank == 0 && warp == 0) {
-            load_f32<T, EPL>(static_cast<const T *>(P.k_new) + u * D + lane * EPL, kn_next);
-            load_f32<T, EPL>(static_cast<const T *>(P.v_new) + u * D + lane * EPL, vn_next);
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                if (lane_has_head) {
+                    const T *row = qp + g_lane * D + 16 * kk + 2 * t4;
+                    qan[kk][0] = *reinterpret_cast<const uint32_t *>(row);
+                    qan[kk][1] = *reinterpret_cast<const uint32_t *>(row + 8);
+                } else {
+                    qan[kk][0] = qan[kk][1] = 0u;
+                }
+                if (rank == 0 && warp == 0) {
+                    kan[kk][0] = *reinterpret_cast<const uint32_t *>(kp + 16 * kk);
+                    kan[kk][1] = *reinterpret_cast<const uint32_t *>(kp + 16 * kk + 8);
+                }
+            }
         } else {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) kn_next[e] = vn_next[e] = 0.f;
+            for (int g = 0; g < G; ++g) load_f32<T, EPL>(qp + g * D + lane * EPL, qn[g]);
+            if (rank == 0 && warp == 0)
+                load_f32<T, EPL>(static_cast<const T *>(P.k_new) + u * D + lane * EPL, kn_next);
         }
     };
     if (W.n_units > 0) load_unit_inputs(static_cast<size_t>(W.cluster_id));
@@ -348,25 +443,51 @@ __global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(
         // its previous contents (unit i - 1) were awaited and used already.
         if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
 
-        // q of this unit (prefetched during the previous unit) and the next
-        // unit's q, k_new, v_new into registers for the next iteration.
-        float qf[G][EPL], kf_new[EPL], vf_new[EPL];
+        // This unit's q (prefetched during the previous unit); start the
+        // next unit's loads.
+        float qf[QG][QE], kf_new[QE];
+        uint32_t qa[QK][2], ka[QK][2];
+        if constexpr (MMA) {
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                qa[kk][0] = qan[kk][0];
+                qa[kk][1] = qan[kk][1];
+                ka[kk][0] = kan[kk][0];
+                ka[kk][1] = kan[kk][1];
+            }
+        } else {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) qf[g][e] = qn[g][e];
+            for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            kf_new[e] = kn_next[e];
-            vf_new[e] = vn_next[e];
+                for (int e = 0; e < EPL; ++e) qf[g][e] = qn[g][e];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) kf_new[e] = kn_next[e];
         }
         if (i + 1 < W.n_units) load_unit_inputs(unit + W.n_clusters);
         // the new token's logits (rank 0, warp 0)
         if (rank == 0 && warp == 0) {
+            if constexpr (MMA) {
+                // lane (g, t) holds q[g][16kk + 2t + {0,1,8,9}] and the same
+                // coordinates of k_new: partial dot, then sum over t.
+                float s = 0.f;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float s = warp_sum(dot_n(qf[g], kf_new));
-                if (lane == 0) M.znew[g] = s * P.scale_log2;
+                for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float q0, q1, k0, k1;
+                        bf16x2_to_f32(qa[kk][h], q0, q1);
+                        bf16x2_to_f32(ka[kk][h], k0, k1);
+                        s = fmaf(q0, k0, fmaf(q1, k1, s));
+                    }
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (t4 == 0 && lane_has_head) M.znew[g_lane] = s * P.scale_log2;
+            } else {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float s = warp_sum(dot_n(qf[g], kf_new));
+                    if (lane == 0) M.znew[g] = s * P.scale_log2;
+                }
             }
         }
         // positions (and scores) of this unit's slots; every unit that
@@ -395,29 +516,64 @@ __global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(
             const T *tk = ring + static_cast<size_t>(s % NST) * kTile * D;
             const int base = s_loc * kTile;
             const int rows = min(kTile, W.n_mine - base);
+            if constexpr (MMA) {
+                const uint32_t sb = smem_u32(tk);
+                float c[4][4];
 #pragma unroll
-            for (int c = 0; c < G; ++c) {
-                float vals[32];
+                for (int j = 0; j < 4; ++j) {
+                    c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float kf[EPL];
-                    load_f32<T, EPL>(tk + (c * R + r) * D + lane * EPL, kf);
-#pragma unroll
-                    for (int g = 0; g < G; ++g) vals[g * R + r] = dot_n(qf[g], kf);
+                    for (int kp = 0; kp < KSTEPS / 2; ++kp) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(sb + swz128_offset(j * 8 + (lane & 7), 4 * kp + (lane >> 3)), b0, b1, b2, b3);
+                        const uint32_t a0[4] = {qa[2 * kp][0], 0u, qa[2 * kp][1], 0u};
+                        const uint32_t a1[4] = {qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u};
+                        mma_bf16_16816(c[j], a0, b0, b1);
+                        mma_bf16_16816(c[j], a1, b2, b3);
+                    }
                 }
-                const float sum = transpose_reduce32(vals, lane);
-                const int row = c * R + (lane % R);
-                bool valid = row < rows;
-                if (HOLES && valid) valid = apos[base + row] >= 0;
-                const float z = valid ? sum * P.scale_log2 : -INFINITY;
-                zbuf[g_lane * zc + base + row] = z;
-                mx = fmaxf(mx, z);
+                if (lane_has_head) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float z2[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int row = j * 8 + 2 * t4 + e;
+                            bool valid = row < rows;
+                            if (HOLES && valid) valid = apos[base + row] >= 0;
+                            z2[e] = valid ? c[j][e] * P.scale_log2 : -INFINITY;
+                            mx = fmaxf(mx, z2[e]);
+                        }
+                        *reinterpret_cast<float2 *>(zbuf + g_lane * zc + base + j * 8 + 2 * t4) =
+                            make_float2(z2[0], z2[1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < G; ++c) {
+                    float vals[32];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        float kf[EPL];
+                        load_f32<T, EPL>(tk + (c * R + r) * D + lane * EPL, kf);
+#pragma unroll
+                        for (int g = 0; g < G; ++g) vals[g * R + r] = dot_n(qf[g], kf);
+                    }
+                    const float sum = transpose_reduce32(vals, lane);
+                    const int row = c * R + (lane % R);
+                    bool valid = row < rows;
+                    if (HOLES && valid) valid = apos[base + row] >= 0;
+                    const float z = valid ? sum * P.scale_log2 : -INFINITY;
+                    zbuf[g_lane * zc + base + row] = z;
+                    mx = fmaxf(mx, z);
+                }
             }
             release_stage(s);
         }
+        // per-warp max per head (the lanes of one head form an aligned group)
 #pragma unroll
-        for (int off = 1; off < R; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        if (lane % R == 0) M.wmax[warp][g_lane] = mx;
+        for (int off = 1; off < kHeadLanes; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane % kHeadLanes == 0 && lane_has_head) M.wmax[warp][g_lane] = mx;
         __syncthreads();
         if (warp == 0 && lane < G) {
             float m = -INFINITY;
@@ -426,24 +582,20 @@ __global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(
             M.m[lane] = m;
         }
         __syncthreads();
-        const float m_mine = M.m[g_lane];
+        const float m_mine = lane_has_head ? M.m[g_lane] : 0.f;
 
         // ---------------------------------------------------------- V phase
-        float acc[G][EPL];
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
         float lsum = 0.f;
-        if (rank == 0 && warp == 0) {
+        float acc[MMA ? 1 : G][MMA ? 1 : EPL];  // CUDA-core accumulators
+        float oacc[MMA ? D / 8 : 1][4];         // mma accumulators (rows = heads)
+        if constexpr (MMA) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float pn = exp2f(M.znew[g] - M.m[g]);
+            for (int jd = 0; jd < D / 8; ++jd) oacc[jd][0] = oacc[jd][1] = oacc[jd][2] = oacc[jd][3] = 0.f;
+        } else {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pn, vf_new[e], acc[g][e]);
-                if (lane == g * R) lsum += pn;
-                if (lane == 0) M.pnew[g] = pn;
-            }
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
         }
         const int first_v = W.nt + ((warp - W.nt % kWarps) % kWarps + kWarps) % kWarps;
         for (int s_loc = first_v; s_loc < 2 * W.nt; s_loc += kWarps) {
@@ -451,71 +603,117 @@ __global__ void __launch_bounds__(kThreads, min_blocks<G>()) decode_step_kernel(
             if (!wait_stage(s)) break;
             const int base = (s_loc - W.nt) * kTile;
             const int rows = min(kTile, W.n_mine - base);
-            // probabilities of this tile: lane L owns (head L/R, slots L%R + c*R)
-#pragma unroll
-            for (int c = 0; c < G; ++c) {
-                float *zp = zbuf + g_lane * zc + base + c * R + (lane % R);
-                const float z = *zp;
-                const float pr = (z == -INFINITY) ? 0.f : exp2f(z - m_mine);
-                *zp = pr;
-                lsum += pr;
-            }
-            __syncwarp();
             const T *tv = ring + static_cast<size_t>(s % NST) * kTile * D;
-            int r = 0;
-            if (!HOLES) {
-                for (; r + 4 <= rows; r += 4) {
-                    float4 p4[G];
+            if constexpr (MMA) {
+                const uint32_t sb = smem_u32(tv);
 #pragma unroll
-                    for (int g = 0; g < G; ++g) p4[g] = *reinterpret_cast<const float4 *>(zbuf + g * zc + base + r);
+                for (int ks = 0; ks < 2; ++ks) {
+                    uint32_t pa[4] = {0u, 0u, 0u, 0u};
+                    if (lane_has_head) {
+                        float pr[4];
 #pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        float vf[EPL];
-                        load_f32<T, EPL>(tv + (r + rr) * D + lane * EPL, vf);
+                        for (int hh = 0; hh < 2; ++hh) {
+                            float2 *zp = reinterpret_cast<float2 *>(zbuf + g_lane * zc + base + ks * 16 + hh * 8 + 2 * t4);
+                            const float2 z = *zp;
+                            const float p0 = (z.x == -INFINITY) ? 0.f : exp2f(z.x - m_mine);
+                            const float p1 = (z.y == -INFINITY) ? 0.f : exp2f(z.y - m_mine);
+                            *zp = make_float2(p0, p1);
+                            lsum += p0 + p1;
+                            pr[2 * hh] = p0;
+                            pr[2 * hh + 1] = p1;
+                        }
+                        pa[0] = pack_bf16x2(pr[0], pr[1]);
+                        pa[2] = pack_bf16x2(pr[2], pr[3]);
+                    }
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float pv = rr == 0 ? p4[g].x : rr == 1 ? p4[g].y : rr == 2 ? p4[g].z : p4[g].w;
+                    for (int jd = 0; jd < D / 8; jd += 2) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_trans(sb + swz128_offset(ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7), jd + (lane >> 4)),
+                                      b0, b1, b2, b3);
+                        mma_bf16_16816(oacc[jd], pa, b0, b1);
+                        mma_bf16_16816(oacc[jd + 1], pa, b2, b3);
+                    }
+                }
+            } else {
+                // probabilities of this tile: lane L owns (head L/R, slots L%R + c*R)
 #pragma unroll
-                            for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pv, vf[e], acc[g][e]);
+                for (int c = 0; c < G; ++c) {
+                    float *zp = zbuf + g_lane * zc + base + c * R + (lane % R);
+                    const float z = *zp;
+                    const float pr = (z == -INFINITY) ? 0.f : exp2f(z - m_mine);
+                    *zp = pr;
+                    lsum += pr;
+                }
+                __syncwarp();
+                int r = 0;
+                if (!HOLES) {
+                    for (; r + 4 <= rows; r += 4) {
+                        float4 p4[G];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) p4[g] = *reinterpret_cast<const float4 *>(zbuf + g * zc + base + r);
+#pragma unroll
+                        for (int rr = 0; rr < 4; ++rr) {
+                            float vf[EPL];
+                            load_f32<T, EPL>(tv + (r + rr) * D + lane * EPL, vf);
+#pragma unroll
+                            for (int g = 0; g < G; ++g) {
+                                const float pv = rr == 0 ? p4[g].x : rr == 1 ? p4[g].y : rr == 2 ? p4[g].z : p4[g].w;
+#pragma unroll
+                                for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pv, vf[e], acc[g][e]);
+                            }
                         }
                     }
                 }
-            }
-            for (; r < rows; ++r) {
-                float pr[G];
-                bool any = false;
+                for (; r < rows; ++r) {
+                    float pr[G];
+                    bool any = false;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    pr[g] = zbuf[g * zc + base + r];
-                    any |= pr[g] != 0.f;
+                    for (int g = 0; g < G; ++g) {
+                        pr[g] = zbuf[g * zc + base + r];
+                        any |= pr[g] != 0.f;
+                    }
+                    if (HOLES && !any) continue;  // an empty slot (same for every lane)
+                    float vf[EPL];
+                    load_f32<T, EPL>(tv + r * D + lane * EPL, vf);
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pr[g], vf[e], acc[g][e]);
                 }
-                if (HOLES && !any) continue;  // an empty slot (same for every lane)
-                float vf[EPL];
-                load_f32<T, EPL>(tv + r * D + lane * EPL, vf);
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pr[g], vf[e], acc[g][e]);
             }
             release_stage(s);
         }
 #pragma unroll
-        for (int off = 1; off < R; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-        if (lane % R == 0) M.wsum[warp][g_lane] = lsum;
+        for (int off = 1; off < kHeadLanes; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        if (lane % kHeadLanes == 0 && lane_has_head) M.wsum[warp][g_lane] = lsum;
+        if constexpr (MMA) {
+            if (lane_has_head) {
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+                for (int jd = 0; jd < D / 8; ++jd)
+                    *reinterpret_cast<float2 *>(part + (warp * G + g_lane) * D + jd * 8 + 2 * t4) =
+                        make_float2(oacc[jd][0], oacc[jd][1]);
+            }
+        } else {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) part[(warp * G + g) * D + lane * EPL + e] = acc[g][e];
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) part[(warp * G + g) * D + lane * EPL + e] = acc[g][e];
+        }
+        // CTA totals; rank 0 adds the new token, p_new = 2^(z_new - m).
+        if (rank == 0 && tid < G) M.pnew[tid] = exp2f(M.znew[tid] - M.m[tid]);
         __syncthreads();
         for (int j = tid; j < G * D; j += kThreads) {
             float o = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) o += part[w * G * D + j];
+            if (rank == 0)
+                o = fmaf(M.pnew[j / D], E::to_f32(static_cast<const T *>(P.v_new)[unit * D + (j % D)]), o);
             M.o[j / D][j % D] = o;
         }
         if (tid < G) {
             float l = 0.f;
             for (int w = 0; w < kWarps; ++w) l += M.wsum[w][tid];
+            if (rank == 0) l += M.pnew[tid];
             M.l[tid] = l;
         }
         __syncthreads();

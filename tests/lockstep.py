@@ -43,6 +43,7 @@ class GpuRun:
     score_snap: dict = field(default_factory=dict)  # layer -> {t: float32 [B, Hkv, C]}
     err: int = 0
     split: int = 0
+    tensor_cores: int = 0
 
 
 def host_inputs(w, units, n_steps, prompt_len):
@@ -52,19 +53,28 @@ def host_inputs(w, units, n_steps, prompt_len):
 
 
 def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, device, snap_steps=(),
-            split: int | None = None, out_seqs=None, seed: int = 0, clusters: int | None = None) -> GpuRun:
-    """Runs n_steps decode steps of the given layers at the workload's shape."""
+            split: int | None = None, out_seqs=None, seed: int = 0, clusters: int | None = None,
+            interleave: bool = True, path: int | None = None) -> GpuRun:
+    """Runs n_steps decode steps of the given layers at the workload's shape.
+
+    interleave=True issues the steps token by token over the layers, as a
+    model does (layer 0, 1, ... of token t, then token t + 1); otherwise all
+    steps of one layer, then the next layer."""
     cache = KVEvictCache.from_workload(w, device=device)
     if split:
         cache.set_split(split)
     if clusters:
         cache.set_clusters(clusters)
+    if path:
+        cache.set_path(path)
     B, Hq, Hkv, D, G = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.group
     dt = torch_dtype(w)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed * 1000 + 17)
-    run = GpuRun(split=cache.stats()["split"])
+    st = cache.stats()
+    run = GpuRun(split=st["split"], tensor_cores=st["tensor_cores"])
     snap_steps = set(snap_steps)
+    bufs = {}
     for layer in layers:
         mine = {u: x for u, x in inputs.items() if u[1] == layer}
         if prompt_len > 0:
@@ -88,15 +98,29 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
         run.score_snap[layer] = {}
         if w.policy == POLICY_H2O:
             run.score_snap[layer][-1] = cache.scores(layer).cpu()
-        for t in range(n_steps):
-            cache.decode_step(layer, q[t], k[t], v[t], out[t])
-            if t in snap_steps:
-                run.pos_snap[layer][t] = cache.slot_positions(layer).cpu()
-                if w.policy == POLICY_H2O:
-                    run.score_snap[layer][t] = cache.scores(layer).cpu()
-        run.err |= cache.check()
-        run.trace[layer] = trace.cpu().numpy()
         seqs = out_seqs if out_seqs is not None else sorted({u[0] for u in mine})
+        bufs[layer] = (q, k, v, out, trace, seqs)
+
+    def step(layer, t):
+        q, k, v, out, _, _ = bufs[layer]
+        cache.decode_step(layer, q[t], k[t], v[t], out[t])
+        if t in snap_steps:
+            run.pos_snap[layer][t] = cache.slot_positions(layer).cpu()
+            if w.policy == POLICY_H2O:
+                run.score_snap[layer][t] = cache.scores(layer).cpu()
+
+    if interleave:
+        for t in range(n_steps):
+            for layer in layers:
+                step(layer, t)
+    else:
+        for layer in layers:
+            for t in range(n_steps):
+                step(layer, t)
+    run.err |= cache.check()
+    for layer in layers:
+        q, k, v, out, trace, seqs = bufs.pop(layer)
+        run.trace[layer] = trace.cpu().numpy()
         run.out[layer] = {s: out[:, s].float().cpu().numpy() for s in seqs}
         del q, k, v, out
     cache.close()

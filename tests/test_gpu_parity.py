@@ -63,7 +63,7 @@ def test_h2o_small_splits(cuda_device, split):
     units = _all_units(w, [0, 1])
     inputs = ls.host_inputs(w, units, w.decode_steps, w.prompt_len)
     run = ls.run_gpu(w, [0, 1], w.decode_steps, inputs, w.prompt_len, cuda_device,
-                     snap_steps=range(0, w.decode_steps, 3), split=split)
+                     snap_steps=range(0, w.decode_steps, 3), split=split, interleave=split != 2)
     assert run.split == split and run.err == 0
     reps = ls.replay_all(w, units, inputs, run, w.decode_steps)
     print(f"split {split}:", _report(reps))
@@ -92,17 +92,35 @@ def test_persistent_loop_with_refills(cuda_device, policy, split, clusters):
     print(f"persistent policy {policy} split {split} clusters {clusters}:", _report(reps))
 
 
-@pytest.mark.parametrize("G,d", [(1, 128), (4, 128), (8, 64)])
-def test_h2o_small_bf16_gqa(cuda_device, G, d):
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("G,d", [(1, 128), (2, 64), (4, 128), (8, 64), (8, 128)])
+def test_h2o_small_bf16_gqa(cuda_device, G, d, path):
+    """bf16 GQA on both decode paths: CUDA cores (1) and tensor cores (2)."""
     w = _small(configs.POLICY_H2O, configs.DTYPE_BF16, G=G, d=d, n_sink=2, n_heavy=50, n_recent=44, budget=96,
                prompt_len=150, decode_steps=70)
     units = _all_units(w, [0])
     inputs = ls.host_inputs(w, units, w.decode_steps, w.prompt_len)
-    run = ls.run_gpu(w, [0], w.decode_steps, inputs, w.prompt_len, cuda_device, snap_steps=range(0, 70, 7))
-    assert run.err == 0
+    run = ls.run_gpu(w, [0], w.decode_steps, inputs, w.prompt_len, cuda_device, snap_steps=range(0, 70, 7),
+                     path=path)
+    assert run.err == 0 and run.tensor_cores == (path == 2)
     reps = ls.replay_all(w, units, inputs, run, w.decode_steps)
-    print(f"G={G} d={d}:", _report(reps))
+    print(f"G={G} d={d} path={path}:", _report(reps))
     ls.check_selector(w, run, 0, w.prompt_len)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_random_small_gqa_paths(cuda_device, path):
+    """Random Attention with holes on both paths (G=4, bf16), several units
+    per cluster."""
+    w = _small(configs.POLICY_RANDOM, configs.DTYPE_BF16, G=4, d=128, B=4, L=2, budget=64, r=16,
+               prompt_len=100, max_prompt=110, decode_steps=150)
+    units = _all_units(w, [0, 1])
+    inputs = ls.host_inputs(w, units, w.decode_steps, w.prompt_len)
+    run = ls.run_gpu(w, [0, 1], w.decode_steps, inputs, w.prompt_len, cuda_device, snap_steps=range(0, 150, 5),
+                     path=path, clusters=3)
+    assert run.err == 0 and run.tensor_cores == (path == 2)
+    reps = ls.replay_all(w, units, inputs, run, w.decode_steps)
+    print(f"random G=4 path={path}:", _report(reps))
 
 
 @pytest.mark.parametrize("P,T", [(0, 80), (45, 40)])
