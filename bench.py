@@ -241,7 +241,9 @@ def run_ours(args, w, rank, world, device):
         P = steady_state(cache, w, device)
         L, B, Hq, Hkv, D = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
         n_pre = 0
-        if w.policy == configs.POLICY_RANDOM:  # pass the first cut
+        if args.no_preroll:
+            pass
+        elif w.policy == configs.POLICY_RANDOM:  # pass the first cut
             n_pre = w.budget + w.r
         elif w.policy == configs.POLICY_H2O and P < w.capacity:  # fill the cache: every timed step evicts
             n_pre = w.capacity - P
@@ -321,7 +323,8 @@ def run_ours(args, w, rank, world, device):
                    "d2h_bytes_per_step": d2h, "steps": n_e2e}
         cache.close()
     return dict(dt_ms=dt_ms, clocks=clk.summary(), decode_launches=decode_launches, cut_launches=cut_launches,
-                iso_ms=iso, e2e=e2e, split=st["split"], clusters=st["clusters"], tensor_cores=st["tensor_cores"])
+                iso_ms=iso, e2e=e2e, split=st["split"], clusters=st["clusters"], tensor_cores=st["tensor_cores"],
+                ring_stages=st["ring_stages"])
 
 
 def main():
@@ -339,6 +342,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling captures only; the line then names it)")
+    ap.add_argument("--no-preroll", action="store_true",
+                    help="time from the state right after prefill (small profiling captures only)")
+    ap.add_argument("--prompt", type=int, default=-1,
+                    help="override the prompt length (small profiling captures only; decode launch shape unchanged "
+                         "once the cache is full)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -346,6 +354,9 @@ def main():
     w = configs.get(args.workload)
     if args.layers:
         w = w.with_(n_layers=args.layers, name=f"{w.name}_layers{args.layers}")
+    if args.prompt >= 0:
+        w = w.with_(prompt_len=args.prompt, max_prompt=max(w.max_prompt, args.prompt) if w.max_prompt else 0,
+                    name=f"{w.name}_prompt{args.prompt}")
     rank, world, local = dist_env()
     metric = "decode tokens/s/GPU with eviction; attn+score+evict HBM GB/s vs 8 TB/s roofline"
     dtype = "bf16" if w.dtype == configs.DTYPE_BF16 else "f32"
@@ -398,6 +409,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded N(0,1) Q/K/V with hub and sink keys, generated on the device)",
         "config": dict(cfg, split=r["split"], clusters=r["clusters"], tensor_cores=bool(r["tensor_cores"]),
+                       ring_stages=r["ring_stages"],
                        timing="CUDA events on the launching stream; no L2 flush needed"),
         "layer_step_us": 1e6 * avg_launch_s,
         "kernel_us_isolated": 1e3 * statistics.median(r["iso_ms"]) if r["iso_ms"] else None,

@@ -115,6 +115,7 @@ typedef struct {
     int capacity;           /* slots per unit */
     int clusters;           /* clusters in the last decode launch's persistent grid (0 before any) */
     int tensor_cores;       /* 1 if the decode path uses the tensor cores (mma), 0 for CUDA cores */
+    int ring_stages;        /* shared-memory ring stages of the last decode launch (32 slots of K or V each) */
 } kvevict_stats;
 
 /* Bytes of device memory a handle with this configuration needs (cache,

@@ -29,7 +29,8 @@ class Config(ctypes.Structure):
 class Stats(ctypes.Structure):
     _fields_ = [("decode_steps", ctypes.c_int64), ("prefill_tokens", ctypes.c_int64),
                 ("evictions", ctypes.c_int64), ("cuts", ctypes.c_int64), ("split", ctypes.c_int),
-                ("capacity", ctypes.c_int), ("clusters", ctypes.c_int), ("tensor_cores", ctypes.c_int)]
+                ("capacity", ctypes.c_int), ("clusters", ctypes.c_int), ("tensor_cores", ctypes.c_int),
+                ("ring_stages", ctypes.c_int)]
 
 
 class KVEvictError(RuntimeError):

@@ -141,7 +141,7 @@ struct kvevict_handle {
         bool mma = false;
         DecodeKernelInfo ki{};
         size_t smem = 0;
-        int zc = 0;
+        int zc = 0, nst = 0;
         int clusters = 0;  // persistent grid, in clusters
     } configured[2];
 };
@@ -167,11 +167,25 @@ int n_aux_arrays(const kvevict_config &c, bool holes) { return c.policy == KVEVI
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
-size_t decode_smem(const kvevict_handle *h, int S, bool holes)
+// Ring stages filling the shared-memory budget of the kernel's target
+// occupancy (two CTAs per SM when its registers allow, else one).
+int ring_stages(const DecodeKernelInfo &ki, size_t fixed)
+{
+    const size_t budget2 = 113 * 1024, budget1 = kMaxSmem;
+    const size_t budget = (ki.ctas_per_sm >= 2 && fixed + kMinStages * ki.stage_bytes <= budget2) ? budget2 : budget1;
+    if (fixed + kMinStages * static_cast<size_t>(ki.stage_bytes) > budget) return 0;
+    return static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / ki.stage_bytes));
+}
+
+size_t decode_smem(const kvevict_handle *h, int S, bool holes, int *nst_out = nullptr)
 {
     DecodeKernelInfo ki;
     if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, &ki)) return ~size_t(0);
-    return ki.smem_bytes(ki.zcap(max_slots_per_cta(h->L, S)), n_aux_arrays(h->cfg, holes));
+    const size_t fixed = ki.fixed_bytes(ki.zcap(max_slots_per_cta(h->L, S)), n_aux_arrays(h->cfg, holes));
+    const int nst = ring_stages(ki, fixed);
+    if (nst_out) *nst_out = nst;
+    if (nst == 0) return ~size_t(0);
+    return fixed + static_cast<size_t>(nst) * ki.stage_bytes;
 }
 
 // CTAs per unit. The persistent kernel streams best with one CTA per unit: a
@@ -191,12 +205,12 @@ int auto_split(const kvevict_handle *h)
     return kMaxSplit;
 }
 
-int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInfo *ki, size_t *smem, int *zc)
+int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInfo *ki, size_t *smem, int *zc, int *nst)
 {
     if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, ki)) return KVEVICT_ERR_INVALID_ARG;
     *zc = ki->zcap(max_slots_per_cta(h->L, S));
-    *smem = ki->smem_bytes(*zc, n_aux_arrays(h->cfg, holes));
-    if (*smem > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
+    *smem = decode_smem(h, S, holes, nst);
+    if (*smem > kMaxSmem || *nst == 0) return KVEVICT_ERR_INVALID_ARG;
     cudaError_t e = cudaFuncSetAttribute(ki->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(*smem));
     if (e == cudaSuccess && S > 8) e = cudaFuncSetAttribute(ki->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return cuda_status(e);
@@ -233,9 +247,10 @@ int make_tensor_map(CUtensorMap *out, void *base, uint64_t rows, int head_dim)
 bool mma_possible(const kvevict_config &c) { return c.dtype == KVEVICT_BF16; }
 bool mma_auto(const kvevict_config &c) { return mma_possible(c) && c.n_q_heads / c.n_kv_heads >= 2; }
 
-// Persistent grid size, in clusters: at most what the GPU holds at once, and
-// where possible a count that divides the units evenly (every cluster then
-// does the same number of units and none idles in the last round).
+// Persistent grid size, in clusters: at most what the GPU holds at once.
+// With few units per cluster, a count that divides the units evenly (every
+// cluster then does the same number of units and none idles in the last
+// round); with many, all of them.
 int pick_clusters(const kvevict_handle *h, int S, const DecodeKernelInfo &ki, size_t smem, int *clusters)
 {
     const int units = static_cast<int>(h->L.units);
@@ -260,6 +275,12 @@ int pick_clusters(const kvevict_handle *h, int S, const DecodeKernelInfo &ki, si
     }
     if (units <= maxc) {
         *clusters = units;
+        return KVEVICT_OK;
+    }
+    // Many units per cluster: the last round's imbalance is small and every
+    // resident slot streaming beats an even split over fewer clusters.
+    if ((units + maxc - 1) / maxc >= 5) {
+        *clusters = maxc;
         return KVEVICT_OK;
     }
     int best = maxc;
@@ -336,7 +357,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
 
     auto &cfgd = h->configured[holes ? 1 : 0];
     if (cfgd.split != h->split || cfgd.clusters_req != h->clusters_req || cfgd.mma != h->use_mma) {
-        int rc0 = configure_kernel(h, h->split, holes, &cfgd.ki, &cfgd.smem, &cfgd.zc);
+        int rc0 = configure_kernel(h, h->split, holes, &cfgd.ki, &cfgd.smem, &cfgd.zc, &cfgd.nst);
         if (rc0) return rc0;
         rc0 = pick_clusters(h, h->split, cfgd.ki, cfgd.smem, &cfgd.clusters);
         if (rc0) return rc0;
@@ -349,6 +370,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     int rc = KVEVICT_OK;
     P.split = h->split;
     P.zcap = cfgd.zc;
+    P.nst = cfgd.nst;
     P.prefetch_early = (h->last_layer >= 0 && h->last_layer != layer) ? 1 : 0;
     if (h->use_mma) {
         static_assert(sizeof(CUtensorMap) == sizeof(TensorMapBytes), "tensor map size");
@@ -651,6 +673,7 @@ int kvevict_get_stats(kvevict_t h, kvevict_stats *out)
     *out = h->stats;
     out->clusters = h->configured[0].clusters ? h->configured[0].clusters : h->configured[1].clusters;
     out->tensor_cores = h->use_mma ? 1 : 0;
+    out->ring_stages = h->configured[0].nst ? h->configured[0].nst : h->configured[1].nst;
     return KVEVICT_OK;
 }
 

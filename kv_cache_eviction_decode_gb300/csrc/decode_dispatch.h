@@ -8,8 +8,10 @@ namespace kvevict {
 
 struct DecodeKernelInfo {
     const void *fn;                    // __global__ decode_step_kernel<...>
-    size_t (*smem_bytes)(int zcap, int n_aux);  // dynamic shared memory (n_aux: 0, 1 or 2 prefetched arrays)
+    size_t (*fixed_bytes)(int zcap, int n_aux);  // dynamic shared memory besides the ring (n_aux: 0, 1 or 2)
     int (*zcap)(int max_slots_per_cta);
+    int stage_bytes;   // one ring stage
+    int ctas_per_sm;   // register-limited target occupancy (1 or 2)
 };
 
 // dtype: 0 fp32, 1 bf16; mma: the tensor-core path (bf16 only). Returns

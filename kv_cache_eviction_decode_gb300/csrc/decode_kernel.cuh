@@ -15,8 +15,8 @@
 // into the stage it has just freed, so the ring keeps streaming across unit
 // boundaries: the next unit's first tiles land while the current unit's
 // combine and score epilogue run. The next unit's slot positions (and H2O
-// scores) are prefetched into a double-buffered shared-memory area, and its
-// q / k_new into registers.
+// scores) are prefetched into a shared-memory area as soon as the current
+// unit is done with it, and its q / k_new into registers.
 //
 // Per unit, every CTA:
 //   K phase   logits z = q.k / sqrt(d) of the G query heads for each slot,
@@ -62,6 +62,8 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSplit = 16;
 constexpr int kSmemAlign = 1024;  // 128-byte swizzle atoms are 1 KB
+constexpr int kMaxStages = 32;    // ring stages (the host fills the shared-memory budget)
+constexpr int kMinStages = 4;
 
 enum InsertMode : int {
     kInsertAt = 0,     // the host gives the slot (empty slot, or the ring slot)
@@ -96,6 +98,7 @@ struct DecodeParams {
     int n_sink, n_recent;
     int split;           // CTAs per unit (cluster size)
     int zcap;            // per-head stride of the logit buffer (and aux slots)
+    int nst;             // ring stages, kMinStages..kMaxStages
     int prefetch_early;  // the launch before this one did not touch this layer: cache tiles may be
                          // fetched before the programmatic-dependency wait (inputs still after it)
     float scale_log2;    // log2(e) / sqrt(D)
@@ -107,17 +110,15 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
     static constexpr int kEPL = D / 32;  // key/value coordinates per lane (CUDA-core path)
     static constexpr int kR = 32 / G;    // slots per butterfly chunk (CUDA-core path)
     static constexpr int kStageBytes = kTile * D * static_cast<int>(sizeof(T));
-    static constexpr int kStages = (81920 / kStageBytes) < 6 ? 6 : (81920 / kStageBytes);
-    static constexpr int kStageArea = kStages * kStageBytes;
     static constexpr int kPartBytes = kWarps * G * D * 4;
     static_assert(G >= 1 && G <= 8 && (G & (G - 1)) == 0, "G in {1,2,4,8}");
     static_assert(!MMA || (sizeof(T) == 2 && D % 64 == 0), "tensor-core path: bf16, head_dim multiple of 64");
 
     struct Misc {
-        uint64_t full[kStages];
-        uint64_t auxbar[2];
-        uint32_t issued[kStages];  // copies issued per stage
-        uint32_t aux_issued[2];
+        uint64_t full[kMaxStages];
+        uint64_t auxbar;
+        uint32_t issued[kMaxStages];  // copies issued per stage
+        uint32_t aux_issued;
         int abort;
         float wmax[kWarps][G];
         float wsum[kWarps][G];
@@ -143,14 +144,17 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
         int z = ((max_slots_per_cta + kTile - 1) / kTile) * kTile;
         return MMA ? z + 8 : (G > 1 ? z + kR : z);
     }
-    __host__ __device__ static size_t off_z() { return kStageArea; }
-    __host__ __device__ static size_t off_part(int zc) { return kStageArea + ((static_cast<size_t>(G) * zc * 4 + 127) / 128) * 128; }
-    // aux: 2 buffers, each holding the unit's slot positions and, with
-    // scores (H2O), the cumulative scores: n_arrays = 0 (none), 1 or 2.
-    __host__ __device__ static size_t off_aux(int zc) { return off_part(zc) + kPartBytes; }
+    // Layout: [ring: nst stages][logits][warp partials][aux][misc].
+    __host__ __device__ static size_t off_z(int nst) { return static_cast<size_t>(nst) * kStageBytes; }
+    __host__ __device__ static size_t off_part(int zc, int nst) { return off_z(nst) + ((static_cast<size_t>(G) * zc * 4 + 127) / 128) * 128; }
+    // aux: the unit's slot positions and, with scores (H2O), the cumulative
+    // scores: n_arrays = 0 (none), 1 or 2.
+    __host__ __device__ static size_t off_aux(int zc, int nst) { return off_part(zc, nst) + kPartBytes; }
     __host__ __device__ static size_t aux_bytes(int zc) { return ((static_cast<size_t>(zc) * 4 + 15) / 16) * 16; }
-    __host__ __device__ static size_t off_misc(int zc, int n_arrays) { return off_aux(zc) + 2 * n_arrays * aux_bytes(zc); }
-    __host__ __device__ static size_t bytes(int zc, int n_arrays) { return off_misc(zc, n_arrays) + sizeof(Misc) + kSmemAlign; }
+    __host__ __device__ static size_t off_misc(int zc, int n_arrays, int nst) { return off_aux(zc, nst) + n_arrays * aux_bytes(zc); }
+    __host__ __device__ static size_t bytes(int zc, int n_arrays, int nst) { return off_misc(zc, n_arrays, nst) + sizeof(Misc) + kSmemAlign; }
+    // Shared memory besides the ring.
+    __host__ __device__ static size_t fixed_bytes(int zc, int n_arrays) { return bytes(zc, n_arrays, 0); }
 };
 
 // Butterfly transpose-reduce: lane L holds 32 partial sums v[0..31]; after
@@ -252,7 +256,8 @@ template <typename T, int D, int G, bool HOLES, bool MMA>
 __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_kernel(const __grid_constant__ DecodeParams P)
 {
     using L = DecodeLayout<T, D, G, MMA>;
-    constexpr int EPL = L::kEPL, R = L::kR, NST = L::kStages;
+    constexpr int EPL = L::kEPL, R = L::kR;
+    const int NST = P.nst;
     constexpr int KSTEPS = D / 16;  // mma k-steps over head_dim
     using E = Elem<T>;
 
@@ -261,14 +266,14 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
                                                 ~static_cast<uintptr_t>(kSmemAlign - 1));
     T *ring = reinterpret_cast<T *>(smem);
     const int zc = P.zcap;
-    float *zbuf = reinterpret_cast<float *>(smem + L::off_z());
-    float *part = reinterpret_cast<float *>(smem + L::off_part(zc));
-    uint8_t *aux = smem + L::off_aux(zc);
+    float *zbuf = reinterpret_cast<float *>(smem + L::off_z(NST));
+    float *part = reinterpret_cast<float *>(smem + L::off_part(zc, NST));
+    uint8_t *aux = smem + L::off_aux(zc, NST);
     const size_t auxb = L::aux_bytes(zc);
     // slot positions (and H2O scores) are prefetched per unit only when used
     const bool need_aux = P.score != nullptr || HOLES;
     const int n_aux = P.score != nullptr ? 2 : (HOLES ? 1 : 0);
-    auto &M = *reinterpret_cast<typename L::Misc *>(smem + L::off_misc(zc, n_aux));
+    auto &M = *reinterpret_cast<typename L::Misc *>(smem + L::off_misc(zc, n_aux, NST));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = static_cast<int>(cluster_rank());
@@ -306,9 +311,8 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
             mbar_init(&M.full[i], 1);
             M.issued[i] = 0;
         }
-        mbar_init(&M.auxbar[0], 1);
-        mbar_init(&M.auxbar[1], 1);
-        M.aux_issued[0] = M.aux_issued[1] = 0;
+        mbar_init(&M.auxbar, 1);
+        M.aux_issued = 0;
         M.abort = 0;
         mbar_fence_init();
         if constexpr (MMA) {
@@ -318,16 +322,16 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
     }
     __syncthreads();
 
-    // Bulk copy of one unit's slot positions (and scores) into aux buffer b.
+    // Bulk copy of the i-th unit's slot positions (and scores) into the aux
+    // area; it completes phase i of the aux mbarrier.
     auto issue_aux = [&](int i) {
         const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
-        const int b = i & 1;
         const uint32_t bytes = static_cast<uint32_t>(((W.n_mine * 4 + 15) / 16) * 16);
         const uint32_t tx = has_score ? 2 * bytes : bytes;
-        mbar_arrive_expect_tx(&M.auxbar[b], tx);
-        bulk_g2s(aux + (n_aux * b) * auxb, P.pos + unit * CS + W.s_lo, bytes, &M.auxbar[b]);
-        if (has_score) bulk_g2s(aux + (n_aux * b + 1) * auxb, P.score + unit * CS + W.s_lo, bytes, &M.auxbar[b]);
-        M.aux_issued[b]++;
+        mbar_arrive_expect_tx(&M.auxbar, tx);
+        bulk_g2s(aux, P.pos + unit * CS + W.s_lo, bytes, &M.auxbar);
+        if (has_score) bulk_g2s(aux + auxb, P.score + unit * CS + W.s_lo, bytes, &M.auxbar);
+        M.aux_issued++;
     };
 
     auto issue_first = [&]() {
@@ -437,11 +441,8 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
     for (int i = 0; i < W.n_units; ++i) {
         const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
         const int seq0 = i * 2 * W.nt;
-        const int32_t *apos = reinterpret_cast<const int32_t *>(aux + (n_aux * (i & 1)) * auxb);
-        const float *ascore = reinterpret_cast<const float *>(aux + (n_aux * (i & 1) + 1) * auxb);
-        // Prefetch the next unit's positions/scores into the other buffer:
-        // its previous contents (unit i - 1) were awaited and used already.
-        if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
+        const int32_t *apos = reinterpret_cast<const int32_t *>(aux);
+        const float *ascore = reinterpret_cast<const float *>(aux + auxb);
 
         // This unit's q (prefetched during the previous unit); start the
         // next unit's loads.
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
                 ok = false;
                 return;
             }
-            if (!mbar_wait(&M.auxbar[i & 1], (i >> 1) & 1)) {
+            if (!mbar_wait(&M.auxbar, i & 1)) {
                 atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
                 ok = false;
                 *abort_flag = 1;
@@ -862,9 +863,10 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
                         make_int4(dest, old_pos, __float_as_int(old_score), __float_as_int(an));
             }
         }
-        // Unit i + 2 reuses this unit's aux buffer: every thread is past its
-        // last read of it at the barriers below.
+        // Every thread is past its last read of this unit's aux data (and has
+        // waited for it): the next unit's positions/scores may come in.
         __syncthreads();
+        if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
         cluster_sync();  // (last) no CTA moves on while a peer may still read its shared memory
     }
 
@@ -873,8 +875,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
     if (tid == 0 && M.abort) {
         for (int st = 0; st < NST; ++st)
             if (M.issued[st] > 0) mbar_wait(&M.full[st], (M.issued[st] - 1) & 1);
-        for (int b = 0; b < 2; ++b)
-            if (M.aux_issued[b] > 0) mbar_wait(&M.auxbar[b], (M.aux_issued[b] - 1) & 1);
+        if (M.aux_issued > 0) mbar_wait(&M.auxbar, (M.aux_issued - 1) & 1);
     }
 }
 
