@@ -371,11 +371,11 @@ def main():
         # cores; rank 0 only.
         if rank != 0:
             return
-        rate, threads, desc, dt = oracle_sample_rate(w, n_units=min(64, w.batch * w.n_kv_heads),
+        rate, threads, desc, dt = oracle_sample_rate(w, n_units=min(256, w.batch * w.n_kv_heads),
                                                      target_s=max(1.0, args.cpu_seconds / 2))
         vals = []
         for _ in range(max(1, min(args.steps, 3))):
-            r, threads, desc, dt = oracle_sample_rate(w, n_units=min(64, w.batch * w.n_kv_heads),
+            r, threads, desc, dt = oracle_sample_rate(w, n_units=min(256, w.batch * w.n_kv_heads),
                                                       target_s=max(1.0, args.cpu_seconds / 2))
             vals.append(cpu_tokens_per_s(w, r))
         v = statistics.median(vals)
@@ -423,7 +423,7 @@ def main():
         "e2e": r["e2e"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, threads, desc, _ = oracle_sample_rate(w, n_units=min(64, w.batch * w.n_kv_heads),
+        rate, threads, desc, _ = oracle_sample_rate(w, n_units=min(256, w.batch * w.n_kv_heads),
                                                     target_s=args.cpu_seconds)
         out["cpu_baseline"] = {"value": cpu_tokens_per_s(w, rate), "unit": "tokens/s", "cores": threads,
                                "kind": "oracle", "sample": desc}

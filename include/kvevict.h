@@ -186,9 +186,10 @@ int kvevict_layer_state(kvevict_t h, int layer, int *prompt_len, int *steps, int
  * A tuning knob: results do not depend on it beyond fp32 rounding order. */
 int kvevict_set_split(kvevict_t h, int split);
 
-/* Decode arithmetic: 0 = automatic (tensor cores for bf16 caches with
- * G >= 2, CUDA cores otherwise), 1 = CUDA cores, 2 = tensor cores (bf16
- * only; mma.sync m16n8k16 with the G query heads padded to 16 rows). A
+/* Decode arithmetic: 0 = automatic (tensor cores for bf16 caches, CUDA
+ * cores for fp32), 1 = CUDA cores, 2 = tensor cores (bf16 only; mma.sync
+ * m16n8k16 with 16 slots / 16 head_dim rows as M and the G query heads,
+ * padded to 8, as N). A
  * tuning and test knob: both paths compute the same step, they differ in
  * rounding only (the tensor-core path rounds probabilities to bf16 for PV).
  * INVALID_ARG if the path is not available for the handle's dtype or its

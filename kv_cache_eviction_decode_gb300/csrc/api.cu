@@ -245,7 +245,9 @@ int make_tensor_map(CUtensorMap *out, void *base, uint64_t rows, int head_dim)
 }
 
 bool mma_possible(const kvevict_config &c) { return c.dtype == KVEVICT_BF16; }
-bool mma_auto(const kvevict_config &c) { return mma_possible(c) && c.n_q_heads / c.n_kv_heads >= 2; }
+// Tensor cores for every bf16 cache: at G = 1 they still cut the issue
+// count per slot about tenfold against the CUDA-core butterfly.
+bool mma_auto(const kvevict_config &c) { return mma_possible(c); }
 
 // Persistent grid size, in clusters: at most what the GPU holds at once.
 // With few units per cluster, a count that divides the units evenly (every

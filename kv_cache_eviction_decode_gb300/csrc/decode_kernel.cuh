@@ -24,12 +24,15 @@
 //               CUDA cores   every lane holds d/32 coordinates of q and of
 //                            each key; a 31-shuffle butterfly transposes the
 //                            partial sums so lane i ends with one logit;
-//               tensor cores S = Q K^T with mma.sync m16n8k16 (bf16 in, fp32
-//                            accumulate): the G heads (padded to 16) are M,
-//                            8 slots are N, head_dim is K; K rows by ldmatrix.
+//               tensor cores S^T = K Q^T with mma.sync m16n8k16 (bf16 in,
+//                            fp32 accumulate): 16 slots are M, the G heads
+//                            (padded to 8) are N, head_dim is K; K rows come
+//                            in by ldmatrix, q is the B operand in registers.
 //   V phase   with the CTA-local max m_c known, p = 2^(z - m_c) is written
-//             back over z and o += p v is accumulated (tensor cores: P as the
-//             A operand in registers, V by ldmatrix.trans).
+//             back over z and o += p v is accumulated (tensor cores:
+//             O^T = V^T P^T with 16 head_dim rows as M, V by ldmatrix.trans,
+//             P as the B operand in registers; the warps' partial outputs
+//             are summed in a tree in fragment order).
 //   combine   (m_c, l_c, o_c) of every CTA in the cluster are read through
 //             distributed shared memory; each CTA writes its share of
 //             out = sum_c o_c 2^(m_c - m) / l. Rank 0 adds the new token.
@@ -110,7 +113,9 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
     static constexpr int kEPL = D / 32;  // key/value coordinates per lane (CUDA-core path)
     static constexpr int kR = 32 / G;    // slots per butterfly chunk (CUDA-core path)
     static constexpr int kStageBytes = kTile * D * static_cast<int>(sizeof(T));
-    static constexpr int kPartBytes = kWarps * G * D * 4;
+    // warp partial outputs: CUDA cores [warp][G][D]; tensor cores, the tree
+    // reduction's half [kWarps/2][D/16][32 lanes][4] in fragment order
+    static constexpr int kPartBytes = MMA ? (kWarps / 2) * (D / 16) * 32 * 4 * 4 : kWarps * G * D * 4;
     static_assert(G >= 1 && G <= 8 && (G & (G - 1)) == 0, "G in {1,2,4,8}");
     static_assert(!MMA || (sizeof(T) == 2 && D % 64 == 0), "tensor-core path: bf16, head_dim multiple of 64");
 
@@ -138,7 +143,8 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
 
     // zcap = slots per CTA rounded to whole tiles, padded so that the head
     // rows of the logit buffer start on different banks: == R (mod 32) for
-    // the butterfly's lane groups, == 8 (mod 32) for the mma fragments.
+    // the butterfly's lane groups, == 8 (mod 32) for the mma path's float2
+    // accesses by (head = lane / 4, slot pair = lane % 4).
     __host__ __device__ static int zcap(int max_slots_per_cta)
     {
         int z = ((max_slots_per_cta + kTile - 1) / kTile) * kTile;
@@ -510,7 +516,8 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
         if (HOLES) wait_aux();
 
         // ---------------------------------------------------------- K phase
-        float mx = -INFINITY;
+        float mx = -INFINITY;   // max of this lane's head (mma path: head 2t)
+        float mx1 = -INFINITY;  // mma path: head 2t + 1
         for (int s_loc = warp; s_loc < W.nt; s_loc += kWarps) {
             const int s = seq0 + s_loc;
             if (!wait_stage(s)) break;
@@ -518,35 +525,51 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
             const int base = s_loc * kTile;
             const int rows = min(kTile, W.n_mine - base);
             if constexpr (MMA) {
+                // S^T (32 slots x 8 heads) = K (32 x D) Q^T, two 16-slot
+                // m-tiles; fragment c = (slot g, heads 2t, 2t+1), (slot g+8, ...)
                 const uint32_t sb = smem_u32(tk);
-                float c[4][4];
+                const int mi = lane >> 3, ri = lane & 7;
+                // four independent accumulation chains: (m-tile, k-step parity)
+                float cc[2][2][4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+                for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                    for (int kp = 0; kp < KSTEPS / 2; ++kp) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(sb + swz128_offset(j * 8 + (lane & 7), 4 * kp + (lane >> 3)), b0, b1, b2, b3);
-                        const uint32_t a0[4] = {qa[2 * kp][0], 0u, qa[2 * kp][1], 0u};
-                        const uint32_t a1[4] = {qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u};
-                        mma_bf16_16816(c[j], a0, b0, b1);
-                        mma_bf16_16816(c[j], a1, b2, b3);
+                    for (int par = 0; par < 2; ++par) cc[mt][par][0] = cc[mt][par][1] = cc[mt][par][2] = cc[mt][par][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        uint32_t a[4];
+                        ldsm_x4(sb + swz128_offset(mt * 16 + (mi & 1) * 8 + ri, 2 * kk + (mi >> 1)), a[0], a[1], a[2],
+                                a[3]);
+                        mma_bf16_16816(cc[mt][kk & 1], a, qa[kk][0], qa[kk][1]);
                     }
-                }
-                if (lane_has_head) {
+                // fragment: (slot r0 = mt*16 + g | r0 + 8, heads 2t, 2t+1).
+                // Branch-free: slot validity once per row (the aux buffer covers
+                // the whole tile, rows past `rows` are masked), head validity
+                // is a per-lane constant.
+                const bool h0_ok = 2 * t4 < G, h1_ok = 2 * t4 + 1 < G;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float z2[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int row = j * 8 + 2 * t4 + e;
-                            bool valid = row < rows;
-                            if (HOLES && valid) valid = apos[base + row] >= 0;
-                            z2[e] = valid ? c[j][e] * P.scale_log2 : -INFINITY;
-                            mx = fmaxf(mx, z2[e]);
-                        }
-                        *reinterpret_cast<float2 *>(zbuf + g_lane * zc + base + j * 8 + 2 * t4) =
-                            make_float2(z2[0], z2[1]);
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int r0 = mt * 16 + g_lane, r1 = r0 + 8;
+                    bool v0 = r0 < rows, v1 = r1 < rows;
+                    if (HOLES) {
+                        v0 = v0 && apos[base + r0] >= 0;
+                        v1 = v1 && apos[base + r1] >= 0;
+                    }
+                    const float z00 = v0 ? (cc[mt][0][0] + cc[mt][1][0]) * P.scale_log2 : -INFINITY;
+                    const float z01 = v0 ? (cc[mt][0][1] + cc[mt][1][1]) * P.scale_log2 : -INFINITY;
+                    const float z10 = v1 ? (cc[mt][0][2] + cc[mt][1][2]) * P.scale_log2 : -INFINITY;
+                    const float z11 = v1 ? (cc[mt][0][3] + cc[mt][1][3]) * P.scale_log2 : -INFINITY;
+                    if (h0_ok) {
+                        zbuf[(2 * t4) * zc + base + r0] = z00;
+                        zbuf[(2 * t4) * zc + base + r1] = z10;
+                        mx = fmaxf(mx, fmaxf(z00, z10));
+                    }
+                    if (h1_ok) {
+                        zbuf[(2 * t4 + 1) * zc + base + r0] = z01;
+                        zbuf[(2 * t4 + 1) * zc + base + r1] = z11;
+                        mx1 = fmaxf(mx1, fmaxf(z01, z11));
                     }
                 }
             } else {
@@ -571,10 +594,24 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
             }
             release_stage(s);
         }
-        // per-warp max per head (the lanes of one head form an aligned group)
+        // per-warp max per head
+        if constexpr (MMA) {
+            // lanes with the same t hold heads 2t, 2t+1 for different slots
 #pragma unroll
-        for (int off = 1; off < kHeadLanes; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        if (lane % kHeadLanes == 0 && lane_has_head) M.wmax[warp][g_lane] = mx;
+            for (int off = 4; off < 32; off <<= 1) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            if (g_lane == 0) {
+                if (2 * t4 < G) M.wmax[warp][2 * t4] = mx;
+                if (2 * t4 + 1 < G) M.wmax[warp][2 * t4 + 1] = mx1;
+            }
+        } else {
+            // the lanes of one head form an aligned group
+#pragma unroll
+            for (int off = 1; off < kHeadLanes; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (lane % kHeadLanes == 0 && lane_has_head) M.wmax[warp][g_lane] = mx;
+        }
         __syncthreads();
         if (warp == 0 && lane < G) {
             float m = -INFINITY;
@@ -588,10 +625,10 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
         // ---------------------------------------------------------- V phase
         float lsum = 0.f;
         float acc[MMA ? 1 : G][MMA ? 1 : EPL];  // CUDA-core accumulators
-        float oacc[MMA ? D / 8 : 1][4];         // mma accumulators (rows = heads)
+        float oacc[MMA ? D / 16 : 1][4];        // mma accumulators: O^T (16 head_dim rows x 8 heads) per m-tile
         if constexpr (MMA) {
 #pragma unroll
-            for (int jd = 0; jd < D / 8; ++jd) oacc[jd][0] = oacc[jd][1] = oacc[jd][2] = oacc[jd][3] = 0.f;
+            for (int md = 0; md < D / 16; ++md) oacc[md][0] = oacc[md][1] = oacc[md][2] = oacc[md][3] = 0.f;
         } else {
 #pragma unroll
             for (int g = 0; g < G; ++g)
@@ -607,8 +644,11 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
             const T *tv = ring + static_cast<size_t>(s % NST) * kTile * D;
             if constexpr (MMA) {
                 const uint32_t sb = smem_u32(tv);
+                const int mi = lane >> 3, ri = lane & 7;
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
+                    // B = P^T fragment: (slots 2t, 2t+1 | 2t+8, 2t+9 of this
+                    // 16-slot step, head g); this lane computes those p.
                     uint32_t pa[4] = {0u, 0u, 0u, 0u};
                     if (lane_has_head) {
                         float pr[4];
@@ -627,12 +667,12 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
                         pa[2] = pack_bf16x2(pr[2], pr[3]);
                     }
 #pragma unroll
-                    for (int jd = 0; jd < D / 8; jd += 2) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_trans(sb + swz128_offset(ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7), jd + (lane >> 4)),
-                                      b0, b1, b2, b3);
-                        mma_bf16_16816(oacc[jd], pa, b0, b1);
-                        mma_bf16_16816(oacc[jd + 1], pa, b2, b3);
+                    for (int md = 0; md < D / 16; ++md) {
+                        // A = V^T (16 head_dim rows x 16 slots) from the [slot][d] tile
+                        uint32_t a[4];
+                        ldsm_x4_trans(sb + swz128_offset(ks * 16 + (mi >> 1) * 8 + ri, 2 * md + (mi & 1)), a[0], a[1],
+                                      a[2], a[3]);
+                        mma_bf16_16816(oacc[md], a, pa[0], pa[2]);
                     }
                 }
             } else {
@@ -687,29 +727,61 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
 #pragma unroll
         for (int off = 1; off < kHeadLanes; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
         if (lane % kHeadLanes == 0 && lane_has_head) M.wsum[warp][g_lane] = lsum;
+        // CTA totals; rank 0 adds the new token, p_new = 2^(z_new - m).
+        if (rank == 0 && tid < G) M.pnew[tid] = exp2f(M.znew[tid] - M.m[tid]);
         if constexpr (MMA) {
-            if (lane_has_head) {
+            // Tree over the warps in fragment order: in each round the upper
+            // half stores, the lower half adds.
+            float4 *pf = reinterpret_cast<float4 *>(part);
 #pragma unroll
-                for (int jd = 0; jd < D / 8; ++jd)
-                    *reinterpret_cast<float2 *>(part + (warp * G + g_lane) * D + jd * 8 + 2 * t4) =
-                        make_float2(oacc[jd][0], oacc[jd][1]);
+            for (int half = kWarps / 2; half >= 1; half >>= 1) {
+                if (warp >= half && warp < 2 * half) {
+#pragma unroll
+                    for (int md = 0; md < D / 16; ++md)
+                        pf[((warp - half) * (D / 16) + md) * 32 + lane] =
+                            make_float4(oacc[md][0], oacc[md][1], oacc[md][2], oacc[md][3]);
+                }
+                __syncthreads();
+                if (warp < half) {
+#pragma unroll
+                    for (int md = 0; md < D / 16; ++md) {
+                        const float4 v = pf[(warp * (D / 16) + md) * 32 + lane];
+                        oacc[md][0] += v.x;
+                        oacc[md][1] += v.y;
+                        oacc[md][2] += v.z;
+                        oacc[md][3] += v.w;
+                    }
+                }
+                __syncthreads();
             }
+            if (warp == 0) {  // O^T fragment: (d = 16md + g | +8, heads 2t, 2t+1)
+#pragma unroll
+                for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = 2 * t4 + (e & 1), d = md * 16 + g_lane + (e >> 1) * 8;
+                        if (h < G) M.o[h][d] = oacc[md][e];
+                    }
+            }
+            __syncthreads();
+            if (rank == 0)
+                for (int j = tid; j < G * D; j += kThreads)
+                    M.o[j / D][j % D] =
+                        fmaf(M.pnew[j / D], E::to_f32(static_cast<const T *>(P.v_new)[unit * D + (j % D)]), M.o[j / D][j % D]);
         } else {
 #pragma unroll
             for (int g = 0; g < G; ++g)
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) part[(warp * G + g) * D + lane * EPL + e] = acc[g][e];
-        }
-        // CTA totals; rank 0 adds the new token, p_new = 2^(z_new - m).
-        if (rank == 0 && tid < G) M.pnew[tid] = exp2f(M.znew[tid] - M.m[tid]);
-        __syncthreads();
-        for (int j = tid; j < G * D; j += kThreads) {
-            float o = 0.f;
+            __syncthreads();
+            for (int j = tid; j < G * D; j += kThreads) {
+                float o = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) o += part[w * G * D + j];
-            if (rank == 0)
-                o = fmaf(M.pnew[j / D], E::to_f32(static_cast<const T *>(P.v_new)[unit * D + (j % D)]), o);
-            M.o[j / D][j % D] = o;
+                for (int w = 0; w < kWarps; ++w) o += part[w * G * D + j];
+                if (rank == 0)
+                    o = fmaf(M.pnew[j / D], E::to_f32(static_cast<const T *>(P.v_new)[unit * D + (j % D)]), o);
+                M.o[j / D][j % D] = o;
+            }
         }
         if (tid < G) {
             float l = 0.f;
