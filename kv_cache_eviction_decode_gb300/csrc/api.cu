@@ -258,7 +258,7 @@ int pick_clusters(const kvevict_handle *h, int S, const DecodeKernelInfo &ki, si
     const int units = static_cast<int>(h->L.units);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(S, 1, 1);
-    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.blockDim = dim3(ki.threads, 1, 1);
     lc.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -382,7 +382,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
 
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(cfgd.clusters * h->split, 1, 1);
-    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.blockDim = dim3(ki.threads, 1, 1);
     lc.dynamicSmemBytes = smem;
     lc.stream = h->stream;
     cudaLaunchAttribute attr[2];

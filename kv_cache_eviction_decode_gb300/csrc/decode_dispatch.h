@@ -12,6 +12,7 @@ struct DecodeKernelInfo {
     int (*zcap)(int max_slots_per_cta);
     int stage_bytes;   // one ring stage
     int ctas_per_sm;   // register-limited target occupancy (1 or 2)
+    int threads;       // CTA size
 };
 
 // dtype: 0 fp32, 1 bf16; mma: the tensor-core path (bf16 only). Returns

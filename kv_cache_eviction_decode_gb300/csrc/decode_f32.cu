@@ -10,7 +10,7 @@ template <int D, int G, bool H, bool MMA> DecodeKernelInfo info()
     using L = DecodeLayout<float, D, G, MMA>;
     return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<float, D, G, H, MMA>),
                             [](int zc, int n_aux) { return L::fixed_bytes(zc, n_aux); }, [](int n) { return L::zcap(n); },
-                            L::kStageBytes, min_blocks<G, MMA>()};
+                            L::kStageBytes, min_blocks<G, MMA>(), L::kThreads};
 }
 
 template <int D, bool H, bool MMA> bool pick_g(int G, DecodeKernelInfo *out)

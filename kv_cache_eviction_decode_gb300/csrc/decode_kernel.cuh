@@ -61,9 +61,12 @@
 namespace kvevict {
 
 constexpr int kTile = 32;  // slots per pipeline stage
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSplit = 16;
+
+// Warps per CTA. 8 everywhere: 16 warps for the one-CTA-per-SM kernels
+// (G >= 4) were measured slower -- the 128-register cap and the larger
+// partial-output buffer cost more than the extra latency hiding gained.
+template <int G, bool MMA> constexpr int warps_for() { return 8; }
 constexpr int kSmemAlign = 1024;  // 128-byte swizzle atoms are 1 KB
 constexpr int kMaxStages = 32;    // ring stages (the host fills the shared-memory budget)
 constexpr int kMinStages = 4;
@@ -110,6 +113,8 @@ struct DecodeParams {
 // Shared-memory layout, shared by host (size) and device (offsets). All
 // offsets are from a base aligned up to kSmemAlign inside the allocation.
 template <typename T, int D, int G, bool MMA> struct DecodeLayout {
+    static constexpr int kWarps = warps_for<G, MMA>();
+    static constexpr int kThreads = kWarps * 32;
     static constexpr int kEPL = D / 32;  // key/value coordinates per lane (CUDA-core path)
     static constexpr int kR = 32 / G;    // slots per butterfly chunk (CUDA-core path)
     static constexpr int kStageBytes = kTile * D * static_cast<int>(sizeof(T));
@@ -254,14 +259,16 @@ template <int D> struct TmaTileSource {
     }
 };
 
-// Two CTAs per SM (registers <= 128) for G <= 2; for larger G the logits
-// and accumulators need more registers and shared memory holds one CTA.
+// Two CTAs per SM (registers <= 128) for G <= 2; for larger G shared memory
+// holds one CTA and the registers are left free.
 template <int G, bool MMA> constexpr int min_blocks() { return G <= 2 ? 2 : 1; }
 
 template <typename T, int D, int G, bool HOLES, bool MMA>
-__global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_kernel(const __grid_constant__ DecodeParams P)
+__global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA>()))
+    decode_step_kernel(const __grid_constant__ DecodeParams P)
 {
     using L = DecodeLayout<T, D, G, MMA>;
+    constexpr int kWarps = L::kWarps, kThreads = L::kThreads;
     constexpr int EPL = L::kEPL, R = L::kR;
     const int NST = P.nst;
     constexpr int KSTEPS = D / 16;  // mma k-steps over head_dim
@@ -343,8 +350,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
     auto issue_first = [&]() {
         for (int s = 0; s < min(NST, W.total_seq); ++s) issue_tile(s, s);
         if (need_aux && W.n_units > 0 && W.n_mine > 0) issue_aux(0);
-        __threadfence_block();
-        for (int s = 0; s < min(NST, W.total_seq); ++s) M.issued[s] = 1;
+        for (int s = 0; s < min(NST, W.total_seq); ++s) st_release_cta(&M.issued[s], 1u);
     };
     // This layer's cache (and positions/scores) can only be written by a
     // launch for this layer. When the launch before this one was for another
@@ -358,7 +364,6 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
 
     bool ok = true;  // false after a timed-out wait: skip work, keep barriers
     volatile int *abort_flag = &M.abort;
-    volatile uint32_t *issued = M.issued;
     // Tile s is copy number c = s / NST into stage s % NST. Its consumer
     // first waits until that copy has been issued (by the consumer of tile
     // s - NST, usually another warp): the stage's mbarrier is then in phase c
@@ -371,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
         }
         const int st = s % NST;
         const uint32_t need = static_cast<uint32_t>(s / NST) + 1;
-        if (issued[st] < need) {
+        if (ld_acquire_cta(&M.issued[st]) < need) {
             const uint64_t t0 = global_timer_ns();
-            for (uint32_t it = 1; issued[st] < need; ++it) {
+            for (uint32_t it = 1; ld_acquire_cta(&M.issued[st]) < need; ++it) {
                 if ((it & 63u) == 0 && (global_timer_ns() - t0 > kWaitLimitNs || *abort_flag)) {
                     atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
                     ok = false;
@@ -382,7 +387,6 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
                 }
             }
         }
-        __threadfence_block();
         if (!mbar_wait(&M.full[st], (s / NST) & 1)) {
             atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
             ok = false;
@@ -397,8 +401,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
         if (lane == 0 && nx < W.total_seq && ok) {
             const int st = s % NST;
             issue_tile(nx, st);
-            __threadfence_block();
-            issued[st] = issued[st] + 1;
+            st_release_cta(&M.issued[st], M.issued[st] + 1);  // after the arrive.expect_tx
         }
     };
 
@@ -417,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
     uint32_t qan[QK][2];
     float kn_next[QE];
     uint32_t kan[QK][2];
+    float vn_next = 0.f;  // rank 0: v_new[tid] of the next unit (tid < D)
     auto load_unit_inputs = [&](size_t u) {
         const T *qp = static_cast<const T *>(P.q) + u * G * D;
         if constexpr (MMA) {
@@ -441,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
             if (rank == 0 && warp == 0)
                 load_f32<T, EPL>(static_cast<const T *>(P.k_new) + u * D + lane * EPL, kn_next);
         }
+        if (rank == 0 && tid < D) vn_next = E::to_f32(static_cast<const T *>(P.v_new)[u * D + tid]);
     };
     if (W.n_units > 0) load_unit_inputs(static_cast<size_t>(W.cluster_id));
 
@@ -454,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
         // next unit's loads.
         float qf[QG][QE], kf_new[QE];
         uint32_t qa[QK][2], ka[QK][2];
+        const float v_new_mine = vn_next;  // rank 0: v_new[tid] of this unit
         if constexpr (MMA) {
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -764,10 +770,9 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
                     }
             }
             __syncthreads();
-            if (rank == 0)
-                for (int j = tid; j < G * D; j += kThreads)
-                    M.o[j / D][j % D] =
-                        fmaf(M.pnew[j / D], E::to_f32(static_cast<const T *>(P.v_new)[unit * D + (j % D)]), M.o[j / D][j % D]);
+            if (rank == 0 && tid < D)
+#pragma unroll
+                for (int g = 0; g < G; ++g) M.o[g][tid] = fmaf(M.pnew[g], v_new_mine, M.o[g][tid]);
         } else {
 #pragma unroll
             for (int g = 0; g < G; ++g)
@@ -778,10 +783,12 @@ __global__ void __launch_bounds__(kThreads, (min_blocks<G, MMA>())) decode_step_
                 float o = 0.f;
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) o += part[w * G * D + j];
-                if (rank == 0)
-                    o = fmaf(M.pnew[j / D], E::to_f32(static_cast<const T *>(P.v_new)[unit * D + (j % D)]), o);
                 M.o[j / D][j % D] = o;
             }
+            __syncthreads();
+            if (rank == 0 && tid < D)
+#pragma unroll
+                for (int g = 0; g < G; ++g) M.o[g][tid] = fmaf(M.pnew[g], v_new_mine, M.o[g][tid]);
         }
         if (tid < G) {
             float l = 0.f;

@@ -227,6 +227,19 @@ __device__ __forceinline__ void grid_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Shared-memory flag access with acquire / release ordering at CTA scope.
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_cta(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
 // Consumer-warps-only barrier (named barrier 1).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
 {
