@@ -238,6 +238,8 @@ def run_ours(args, w, rank, world, device):
             cache.set_clusters(args.clusters)
         if args.path:
             cache.set_path(args.path)
+        if args.ring:
+            cache.set_ring(args.ring)
         P = steady_state(cache, w, device)
         L, B, Hq, Hkv, D = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
         n_pre = 0
@@ -337,6 +339,7 @@ def main():
     ap.add_argument("--split", type=int, default=0)
     ap.add_argument("--clusters", type=int, default=0, help="persistent grid size in clusters (0 = automatic)")
     ap.add_argument("--path", type=int, default=0, help="0 automatic, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--ring", type=int, default=0, help="cap on ring stages per CTA (0 = fill shared memory)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -196,6 +196,12 @@ int kvevict_set_split(kvevict_t h, int split);
  * shared memory would not fit. */
 int kvevict_set_path(kvevict_t h, int path);
 
+/* At most this many shared-memory ring stages (32-slot K or V tiles) per CTA
+ * in the decode launch; 0 = as many as the shared-memory budget allows (the
+ * default). A tuning knob: results do not depend on it. INVALID_ARG outside
+ * 4..32. */
+int kvevict_set_ring(kvevict_t h, int stages);
+
 /* Number of clusters in the decode launch's persistent grid (each cluster
  * loops over units; 0 = automatic: as many as fit on the GPU at once, chosen
  * to divide the units evenly where possible). A tuning knob like

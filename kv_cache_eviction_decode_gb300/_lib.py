@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
             L.kvevict_set_split.argtypes = [P, I]
             L.kvevict_set_clusters.argtypes = [P, I]
             L.kvevict_set_path.argtypes = [P, I]
+            L.kvevict_set_ring.argtypes = [P, I]
             L.kvevict_get_stats.argtypes = [P, ctypes.POINTER(Stats)]
             L.kvevict_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             L.kvevict_strerror.argtypes = [I]
@@ -72,7 +73,7 @@ def lib() -> ctypes.CDLL:
             L.kvevict_destroy.restype = None
             for n in ("kvevict_state_bytes", "kvevict_create", "kvevict_prefill", "kvevict_decode_step",
                       "kvevict_decode_step_host", "kvevict_slot_positions", "kvevict_scores", "kvevict_set_trace",
-                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path",
+                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",
                       "kvevict_check"):
                 getattr(L, n).restype = I

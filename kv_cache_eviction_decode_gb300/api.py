@@ -147,6 +147,9 @@ class KVEvictCache:
         """0 automatic, 1 CUDA cores, 2 tensor cores (bf16 only)."""
         check(self._L.kvevict_set_path(self.h, path), "kvevict_set_path")
 
+    def set_ring(self, stages: int) -> None:
+        check(self._L.kvevict_set_ring(self.h, stages), "kvevict_set_ring")
+
     def set_clusters(self, clusters: int) -> None:
         check(self._L.kvevict_set_clusters(self.h, clusters), "kvevict_set_clusters")
 

@@ -131,13 +131,14 @@ struct kvevict_handle {
     int clusters_req = 0;  // persistent grid size in clusters; 0 = automatic
     int last_layer = -1;   // layer of the last kernel this handle queued (-1: none, or unknown)
     int path_req = 0;      // 0 automatic, 1 CUDA cores, 2 tensor cores
+    int ring_req = 0;      // ring stages requested (0 = fill the shared-memory budget)
     bool use_mma = false;  // decode path in use
     std::vector<CUtensorMap> tmk, tmv;  // per layer (bf16 caches)
     std::vector<LayerState> layers;
     kvevict_stats stats{};
     // decode kernel configured for (split, holes): function, shared memory, zcap
     struct Configured {
-        int split = 0, clusters_req = -1;
+        int split = 0, clusters_req = -1, ring_req = -1;
         bool mma = false;
         DecodeKernelInfo ki{};
         size_t smem = 0;
@@ -182,7 +183,8 @@ size_t decode_smem(const kvevict_handle *h, int S, bool holes, int *nst_out = nu
     DecodeKernelInfo ki;
     if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, &ki)) return ~size_t(0);
     const size_t fixed = ki.fixed_bytes(ki.zcap(max_slots_per_cta(h->L, S)), n_aux_arrays(h->cfg, holes));
-    const int nst = ring_stages(ki, fixed);
+    int nst = ring_stages(ki, fixed);
+    if (h->ring_req > 0 && nst > 0) nst = std::min(nst, h->ring_req);
     if (nst_out) *nst_out = nst;
     if (nst == 0) return ~size_t(0);
     return fixed + static_cast<size_t>(nst) * ki.stage_bytes;
@@ -358,7 +360,8 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     }
 
     auto &cfgd = h->configured[holes ? 1 : 0];
-    if (cfgd.split != h->split || cfgd.clusters_req != h->clusters_req || cfgd.mma != h->use_mma) {
+    if (cfgd.split != h->split || cfgd.clusters_req != h->clusters_req || cfgd.mma != h->use_mma ||
+        cfgd.ring_req != h->ring_req) {
         int rc0 = configure_kernel(h, h->split, holes, &cfgd.ki, &cfgd.smem, &cfgd.zc, &cfgd.nst);
         if (rc0) return rc0;
         rc0 = pick_clusters(h, h->split, cfgd.ki, cfgd.smem, &cfgd.clusters);
@@ -366,6 +369,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
         cfgd.split = h->split;
         cfgd.clusters_req = h->clusters_req;
         cfgd.mma = h->use_mma;
+        cfgd.ring_req = h->ring_req;
     }
     const DecodeKernelInfo &ki = cfgd.ki;
     const size_t smem = cfgd.smem;
@@ -658,6 +662,14 @@ int kvevict_set_path(kvevict_t h, int path)
         return KVEVICT_ERR_INVALID_ARG;
     }
     h->path_req = path;
+    return KVEVICT_OK;
+}
+
+int kvevict_set_ring(kvevict_t h, int stages)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (stages != 0 && (stages < kMinStages || stages > kMaxStages)) return KVEVICT_ERR_INVALID_ARG;
+    h->ring_req = stages;
     return KVEVICT_OK;
 }
 
