@@ -118,9 +118,11 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
     static constexpr int kEPL = D / 32;  // key/value coordinates per lane (CUDA-core path)
     static constexpr int kR = 32 / G;    // slots per butterfly chunk (CUDA-core path)
     static constexpr int kStageBytes = kTile * D * static_cast<int>(sizeof(T));
-    // warp partial outputs: CUDA cores [warp][G][D]; tensor cores, the tree
-    // reduction's half [kWarps/2][D/16][32 lanes][4] in fragment order
-    static constexpr int kPartBytes = MMA ? (kWarps / 2) * (D / 16) * 32 * 4 * 4 : kWarps * G * D * 4;
+    // warp partial outputs [warp][head][kPS]; the row stride D + 4 puts the
+    // 32 lanes of one mma-fragment store on 32 different banks
+    static constexpr int kPS = D + 4;
+    static constexpr int kPartBytes = kWarps * G * kPS * 4;
+    static_assert((2 * kThreads) % D == 0, "a thread owns the same coordinate pair of every head it sums");
     static_assert(G >= 1 && G <= 8 && (G & (G - 1)) == 0, "G in {1,2,4,8}");
     static_assert(!MMA || (sizeof(T) == 2 && D % 64 == 0), "tensor-core path: bf16, head_dim multiple of 64");
 
@@ -134,13 +136,14 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
         float wsum[kWarps][G];
         float m[G];        // this CTA's max logit per head (log2 units)
         float l[G];        // this CTA's softmax denominator relative to m
-        float o[G][D];     // this CTA's unnormalised output relative to m
+        alignas(16) float o[G][D];  // this CTA's unnormalised output relative to m
         float znew[G];     // the new token's logits (rank 0)
         float pnew[G];     // 2^(znew - m) (rank 0)
         float fac[kMaxSplit][G];  // 2^(m_c - m_global) / l_global per CTA c
         float anew;        // the new token's score (rank 0)
         int dest;
         uint64_t best_key;
+        uint64_t win_key;  // the cluster's winning (score bits, position)
         int32_t best_slot;
         uint64_t wkey[kWarps];
         int32_t wslot[kWarps];
@@ -199,6 +202,26 @@ __device__ __forceinline__ float warp_sum(float x)
     for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
     return x;
 }
+
+// Butterfly argmin over the warp of (key, slot); keys are distinct except the
+// empty candidate (~0, -1), so every lane ends with the same pair.
+__device__ __forceinline__ void warp_argmin(uint64_t &key, int32_t &slot)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, off);
+        const int32_t os = __shfl_xor_sync(0xffffffffu, slot, off);
+        if (ok < key) {
+            key = ok;
+            slot = os;
+        }
+    }
+}
+
+// Two consecutive elements, moved as one naturally aligned access.
+template <typename T> struct alignas(2 * sizeof(T)) TPair {
+    T x, y;
+};
 
 // The CTA's share of one launch: which units, which tiles of each.
 struct Work {
@@ -269,7 +292,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
 {
     using L = DecodeLayout<T, D, G, MMA>;
     constexpr int kWarps = L::kWarps, kThreads = L::kThreads;
-    constexpr int EPL = L::kEPL, R = L::kR;
+    constexpr int EPL = L::kEPL, R = L::kR, kPS = L::kPS;
     const int NST = P.nst;
     constexpr int KSTEPS = D / 16;  // mma k-steps over head_dim
     using E = Elem<T>;
@@ -420,7 +443,13 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     uint32_t qan[QK][2];
     float kn_next[QE];
     uint32_t kan[QK][2];
-    float vn_next = 0.f;  // rank 0: v_new[tid] of the next unit (tid < D)
+    // Every thread: the new token's k and v at the coordinate pair (dp, dp + 1)
+    // -- rank 0 adds p_new v_new there, and the threads tid < D/2 of the CTA
+    // that stores the new token write them -- and the slot the new token goes
+    // to when the host or the free list names it.
+    const int dp = 2 * (tid % (D / 2));
+    TPair<T> kpair_next, vpair_next;
+    int dest_next = -1;
     auto load_unit_inputs = [&](size_t u) {
         const T *qp = static_cast<const T *>(P.q) + u * G * D;
         if constexpr (MMA) {
@@ -445,7 +474,9 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             if (rank == 0 && warp == 0)
                 load_f32<T, EPL>(static_cast<const T *>(P.k_new) + u * D + lane * EPL, kn_next);
         }
-        if (rank == 0 && tid < D) vn_next = E::to_f32(static_cast<const T *>(P.v_new)[u * D + tid]);
+        kpair_next = *reinterpret_cast<const TPair<T> *>(static_cast<const T *>(P.k_new) + u * D + dp);
+        vpair_next = *reinterpret_cast<const TPair<T> *>(static_cast<const T *>(P.v_new) + u * D + dp);
+        dest_next = P.mode == kFromFreeList ? P.freelist[u * P.freelist_len + P.freelist_idx] : P.dest_slot;
     };
     if (W.n_units > 0) load_unit_inputs(static_cast<size_t>(W.cluster_id));
 
@@ -459,7 +490,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         // next unit's loads.
         float qf[QG][QE], kf_new[QE];
         uint32_t qa[QK][2], ka[QK][2];
-        const float v_new_mine = vn_next;  // rank 0: v_new[tid] of this unit
+        const TPair<T> kpair = kpair_next, vpair = vpair_next;
+        const int dest_mine = dest_next;
         if constexpr (MMA) {
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -733,220 +765,292 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
 #pragma unroll
         for (int off = 1; off < kHeadLanes; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
         if (lane % kHeadLanes == 0 && lane_has_head) M.wsum[warp][g_lane] = lsum;
-        // CTA totals; rank 0 adds the new token, p_new = 2^(z_new - m).
+        // rank 0 adds the new token: p_new = 2^(z_new - m)
         if (rank == 0 && tid < G) M.pnew[tid] = exp2f(M.znew[tid] - M.m[tid]);
+        // every warp's partial output, compact: part[warp][head][kPS]
         if constexpr (MMA) {
-            // Tree over the warps in fragment order: in each round the upper
-            // half stores, the lower half adds.
-            float4 *pf = reinterpret_cast<float4 *>(part);
+            // O^T fragment: (d = 16 md + g | + 8, heads 2t, 2t + 1)
 #pragma unroll
-            for (int half = kWarps / 2; half >= 1; half >>= 1) {
-                if (warp >= half && warp < 2 * half) {
+            for (int md = 0; md < D / 16; ++md)
 #pragma unroll
-                    for (int md = 0; md < D / 16; ++md)
-                        pf[((warp - half) * (D / 16) + md) * 32 + lane] =
-                            make_float4(oacc[md][0], oacc[md][1], oacc[md][2], oacc[md][3]);
+                for (int e = 0; e < 4; ++e) {
+                    const int h = 2 * t4 + (e & 1), d = md * 16 + g_lane + (e >> 1) * 8;
+                    if (h < G) part[(warp * G + h) * kPS + d] = oacc[md][e];
                 }
-                __syncthreads();
-                if (warp < half) {
-#pragma unroll
-                    for (int md = 0; md < D / 16; ++md) {
-                        const float4 v = pf[(warp * (D / 16) + md) * 32 + lane];
-                        oacc[md][0] += v.x;
-                        oacc[md][1] += v.y;
-                        oacc[md][2] += v.z;
-                        oacc[md][3] += v.w;
-                    }
-                }
-                __syncthreads();
-            }
-            if (warp == 0) {  // O^T fragment: (d = 16md + g | +8, heads 2t, 2t+1)
-#pragma unroll
-                for (int md = 0; md < D / 16; ++md)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = 2 * t4 + (e & 1), d = md * 16 + g_lane + (e >> 1) * 8;
-                        if (h < G) M.o[h][d] = oacc[md][e];
-                    }
-            }
-            __syncthreads();
-            if (rank == 0 && tid < D)
-#pragma unroll
-                for (int g = 0; g < G; ++g) M.o[g][tid] = fmaf(M.pnew[g], v_new_mine, M.o[g][tid]);
         } else {
 #pragma unroll
             for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) part[(warp * G + g) * D + lane * EPL + e] = acc[g][e];
-            __syncthreads();
-            for (int j = tid; j < G * D; j += kThreads) {
-                float o = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) o += part[w * G * D + j];
-                M.o[j / D][j % D] = o;
-            }
-            __syncthreads();
-            if (rank == 0 && tid < D)
-#pragma unroll
-                for (int g = 0; g < G; ++g) M.o[g][tid] = fmaf(M.pnew[g], v_new_mine, M.o[g][tid]);
+                for (int e = 0; e < EPL; ++e) part[(warp * G + g) * kPS + lane * EPL + e] = acc[g][e];
         }
-        if (tid < G) {
+        __syncthreads();  // (A) partials and p_new visible; every read of this unit's tiles is done
+
+        // This CTA's totals of head g: l_g = sum over the warps (+ p_new on
+        // rank 0), o_g[d] likewise (+ p_new v_new[d] on rank 0). A thread
+        // owns the coordinate pairs (g, dp), (g, dp + 1) of its pair indices
+        // jp = tid, tid + kThreads, ... (g = 2 jp / D).
+        auto cta_l = [&](int g) {
             float l = 0.f;
-            for (int w = 0; w < kWarps; ++w) l += M.wsum[w][tid];
-            if (rank == 0) l += M.pnew[tid];
-            M.l[tid] = l;
-        }
-        __syncthreads();
-        cluster_sync();  // (1) every CTA's (m, l, o) is ready
-
-        // ------------------------------------------------------------ combine
-        if (tid < G) {
-            float mg = -INFINITY;
-            for (int c = 0; c < S; ++c) mg = fmaxf(mg, ld_peer_f32(peer_addr(&M.m[tid], c)));
-            float lg = 0.f;
-            for (int c = 0; c < S; ++c) {
-                const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
-                const float lc = ld_peer_f32(peer_addr(&M.l[tid], c));
-                if (mc != -INFINITY) lg += lc * exp2f(mc - mg);
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) l += M.wsum[w][g];
+            if (rank == 0) l += M.pnew[g];
+            return l;
+        };
+        auto cta_o = [&](int g, float &ox, float &oy) {
+            ox = 0.f;
+            oy = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float2 v = *reinterpret_cast<const float2 *>(part + (w * G + g) * kPS + dp);
+                ox += v.x;
+                oy += v.y;
             }
-            if (rank == 0 && !(lg > 0.f && lg <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
-            const float inv = 1.f / lg;
-            for (int c = 0; c < S; ++c) {
-                const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
-                M.fac[c][tid] = (mc == -INFINITY) ? 0.f : exp2f(mc - mg) * inv;
+            if (rank == 0) {
+                ox = fmaf(M.pnew[g], E::to_f32(vpair.x), ox);
+                oy = fmaf(M.pnew[g], E::to_f32(vpair.y), oy);
             }
-        }
-        __syncthreads();
-        {
-            constexpr int GD = G * D;
-            const int i0 = rank * GD / S, i1 = (rank + 1) * GD / S;
-            T *outp = static_cast<T *>(P.out) + unit * GD;
-            for (int j = i0 + tid; j < i1; j += kThreads) {
-                const int g = j / D, e = j % D;
-                float o = 0.f;
-                for (int c = 0; c < S; ++c) o = fmaf(ld_peer_f32(peer_addr(&M.o[g][e], c)), M.fac[c][g], o);
-                outp[j] = E::from_f32(o);
-            }
-        }
-
-        // ------------------------------------------ cumulative scores (H2O)
+        };
+        constexpr int kPairs = G * D / 2;
         const bool evict = P.mode == kH2OEvict;
-        if (has_score) {
-            wait_aux();
-            float fself[G];
+        int dest = -1;             // slot that receives the new token
+        bool writer = false;       // this CTA writes it
+        uint64_t win_key = ~0ull;  // H2O eviction: (score bits, position) of the evicted token
+        float anew = 0.f;          // the new token's score (rank 0)
+
+        if (S == 1) {
+            // ------------------------------ output, one CTA per unit: o / l
+            T *outp = static_cast<T *>(P.out) + unit * (G * D);
+            for (int jp = tid; jp < kPairs; jp += kThreads) {
+                const int g = (2 * jp) / D;
+                float ox, oy;
+                cta_o(g, ox, oy);
+                const float inv = 1.f / cta_l(g);
+                TPair<T> o2;
+                o2.x = E::from_f32(ox * inv);
+                o2.y = E::from_f32(oy * inv);
+                *reinterpret_cast<TPair<T> *>(outp + 2 * jp) = o2;
+            }
+            if (tid < G) {
+                const float l = cta_l(tid);
+                if (!(l > 0.f && l <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
+            }
+            if (has_score) {
+                // ------------------------------ cumulative scores (H2O)
+                wait_aux();
+                float invl[G], fself[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
-            uint64_t best = ~0ull;
-            int32_t bslot = -1;
-            for (int j = tid; j < W.n_mine; j += kThreads) {
-                float a = 0.f;
+                for (int g = 0; g < G; ++g) {
+                    invl[g] = 1.f / cta_l(g);
+                    fself[g] = invl[g] * (1.0f / G);
+                }
+                uint64_t best = ~0ull;
+                int32_t bslot = -1;
+                for (int j = tid; j < W.n_mine; j += kThreads) {
+                    float a = 0.f;
 #pragma unroll
-                for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
-                const float sc = ascore[j] + a;
-                P.score[unit * CS + W.s_lo + j] = sc;
-                if (evict) {
-                    const int ps = apos[j];
-                    if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
-                        const uint64_t key =
-                            (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
-                        if (key < best) {
-                            best = key;
-                            bslot = W.s_lo + j;
+                    for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
+                    const float sc = ascore[j] + a;
+                    P.score[unit * CS + j] = sc;
+                    if (evict) {
+                        const int ps = apos[j];
+                        if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
+                            const uint64_t key =
+                                (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
+                            if (key < best) {
+                                best = key;
+                                bslot = j;
+                            }
                         }
                     }
                 }
-            }
-            if (rank == 0 && tid == 0) {
-                float a = 0.f;
+                if (tid == 0) {
+                    float a = 0.f;
 #pragma unroll
-                for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], M.fac[0][g], a);
-                M.anew = a * (1.0f / G);
-            }
-            if (evict) {
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
-                    const uint64_t ok2 = __shfl_xor_sync(0xffffffffu, best, off);
-                    const int32_t os = __shfl_xor_sync(0xffffffffu, bslot, off);
-                    if (ok2 < best) {
-                        best = ok2;
-                        bslot = os;
+                    for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], invl[g], a);
+                    anew = a * (1.0f / G);
+                }
+                if (evict) {
+                    warp_argmin(best, bslot);
+                    if (lane == 0) {
+                        M.wkey[warp] = best;
+                        M.wslot[warp] = bslot;
                     }
                 }
-                if (lane == 0) {
-                    M.wkey[warp] = best;
-                    M.wslot[warp] = bslot;
+                __syncthreads();  // (B) candidates visible; every read of this unit's aux data is done
+                if (evict) {
+                    // every warp reduces the warps' candidates itself
+                    uint64_t k = lane < kWarps ? M.wkey[lane] : ~0ull;
+                    int32_t sl = lane < kWarps ? M.wslot[lane] : -1;
+                    warp_argmin(k, sl);
+                    win_key = k;
+                    dest = sl;
+                    if (sl < 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                }
+            }
+            // the next unit's positions/scores may come in
+            if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
+            if (!evict) dest = dest_mine;
+            writer = true;
+        } else {
+            // ------------------------------ totals for the cluster exchange
+            for (int jp = tid; jp < kPairs; jp += kThreads) {
+                const int g = (2 * jp) / D;
+                float ox, oy;
+                cta_o(g, ox, oy);
+                *reinterpret_cast<float2 *>(&M.o[g][2 * jp - g * D]) = make_float2(ox, oy);
+            }
+            if (tid < G) M.l[tid] = cta_l(tid);
+            __syncthreads();
+            cluster_sync();  // (1) every CTA's (m, l, o) is ready
+
+            // -------------------------------------------------------- combine
+            if (tid < G) {
+                float mg = -INFINITY;
+                for (int c = 0; c < S; ++c) mg = fmaxf(mg, ld_peer_f32(peer_addr(&M.m[tid], c)));
+                float lg = 0.f;
+                for (int c = 0; c < S; ++c) {
+                    const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
+                    const float lc = ld_peer_f32(peer_addr(&M.l[tid], c));
+                    if (mc != -INFINITY) lg += lc * exp2f(mc - mg);
+                }
+                if (rank == 0 && !(lg > 0.f && lg <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
+                const float inv = 1.f / lg;
+                for (int c = 0; c < S; ++c) {
+                    const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
+                    M.fac[c][tid] = (mc == -INFINITY) ? 0.f : exp2f(mc - mg) * inv;
                 }
             }
             __syncthreads();
-            if (evict && tid == 0) {
-                uint64_t k = ~0ull;
-                int32_t sl = -1;
-                for (int w = 0; w < kWarps; ++w)
-                    if (M.wkey[w] < k) {
-                        k = M.wkey[w];
-                        sl = M.wslot[w];
-                    }
-                M.best_key = k;
-                M.best_slot = sl;
+            {
+                constexpr int GD = G * D;
+                const int i0 = rank * GD / S, i1 = (rank + 1) * GD / S;
+                T *outp = static_cast<T *>(P.out) + unit * GD;
+                for (int j = i0 + tid; j < i1; j += kThreads) {
+                    const int g = j / D, e = j % D;
+                    float o = 0.f;
+                    for (int c = 0; c < S; ++c) o = fmaf(ld_peer_f32(peer_addr(&M.o[g][e], c)), M.fac[c][g], o);
+                    outp[j] = E::from_f32(o);
+                }
             }
+
+            // ------------------------------------------ cumulative scores (H2O)
+            if (has_score) {
+                wait_aux();
+                float fself[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
+                uint64_t best = ~0ull;
+                int32_t bslot = -1;
+                for (int j = tid; j < W.n_mine; j += kThreads) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
+                    const float sc = ascore[j] + a;
+                    P.score[unit * CS + W.s_lo + j] = sc;
+                    if (evict) {
+                        const int ps = apos[j];
+                        if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
+                            const uint64_t key =
+                                (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
+                            if (key < best) {
+                                best = key;
+                                bslot = W.s_lo + j;
+                            }
+                        }
+                    }
+                }
+                if (rank == 0 && tid == 0) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], M.fac[0][g], a);
+                    M.anew = a * (1.0f / G);
+                }
+                if (evict) {
+                    warp_argmin(best, bslot);
+                    if (lane == 0) {
+                        M.wkey[warp] = best;
+                        M.wslot[warp] = bslot;
+                    }
+                }
+                __syncthreads();
+                if (evict && tid == 0) {
+                    uint64_t k = ~0ull;
+                    int32_t sl = -1;
+                    for (int w = 0; w < kWarps; ++w)
+                        if (M.wkey[w] < k) {
+                            k = M.wkey[w];
+                            sl = M.wslot[w];
+                        }
+                    M.best_key = k;
+                    M.best_slot = sl;
+                }
+            }
+
+            // --------------------------------------------------------- insert
+            if (evict) {
+                cluster_sync();  // (2) every CTA's candidate is ready
+                if (tid == 0) {
+                    uint64_t k = ~0ull;
+                    int32_t sl = -1;
+                    for (int c = 0; c < S; ++c) {
+                        const uint64_t kc = ld_peer_u64(peer_addr(&M.best_key, c));
+                        const int32_t scs = ld_peer_s32(peer_addr(&M.best_slot, c));
+                        if (kc < k) {
+                            k = kc;
+                            sl = scs;
+                        }
+                    }
+                    if (sl < 0 && rank == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                    M.dest = sl;
+                    M.win_key = k;
+                }
+                __syncthreads();
+                dest = M.dest;
+                win_key = M.win_key;
+                writer = dest >= W.s_lo && dest < W.s_hi;  // the CTA that attended the victim
+            } else {
+                __syncthreads();
+                dest = dest_mine;
+                writer = rank == 0;
+            }
+            if (writer && tid == 0 && has_score) anew = ld_peer_f32(peer_addr(&M.anew, 0));
         }
 
         // ------------------------------------------------------------- insert
-        int dest = -1;
-        bool writer = false;
-        if (evict) {
-            cluster_sync();  // (2) every CTA's candidate is ready
-            if (tid == 0) {
-                uint64_t k = ~0ull;
-                int32_t sl = -1;
-                for (int c = 0; c < S; ++c) {
-                    const uint64_t kc = ld_peer_u64(peer_addr(&M.best_key, c));
-                    const int32_t scs = ld_peer_s32(peer_addr(&M.best_slot, c));
-                    if (kc < k) {
-                        k = kc;
-                        sl = scs;
-                    }
-                }
-                if (sl < 0 && rank == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
-                M.dest = sl;
-            }
-            __syncthreads();
-            dest = M.dest;
-            writer = dest >= W.s_lo && dest < W.s_hi;  // the CTA that attended the victim
-        } else {
-            __syncthreads();
-            dest = P.mode == kInsertAt ? P.dest_slot : P.freelist[unit * P.freelist_len + P.freelist_idx];
-            writer = rank == 0;
-            if (dest < 0 || dest >= P.C) {
-                if (writer && tid == 0) atomicOr(P.err, KVEVICT_DEV_BAD_SLOT);
-                dest = -1;
-            }
+        // The new token's K/V row (prefetched pairs), position and score go
+        // in place into slot `dest`.
+        if (!evict && (dest < 0 || dest >= P.C)) {
+            if (writer && tid == 0) atomicOr(P.err, KVEVICT_DEV_BAD_SLOT);
+            dest = -1;
         }
         if (writer && dest >= 0) {
-            const T *kn = static_cast<const T *>(P.k_new) + unit * D;
-            const T *vn = static_cast<const T *>(P.v_new) + unit * D;
-            T *kd = static_cast<T *>(P.kc) + (unit * C + dest) * D;
-            T *vd = static_cast<T *>(P.vc) + (unit * C + dest) * D;
-            for (int j = tid; j < D; j += kThreads) {
-                kd[j] = kn[j];
-                vd[j] = vn[j];
+            if (tid < D / 2) {
+                *reinterpret_cast<TPair<T> *>(static_cast<T *>(P.kc) + (unit * C + dest) * D + dp) = kpair;
+                *reinterpret_cast<TPair<T> *>(static_cast<T *>(P.vc) + (unit * C + dest) * D + dp) = vpair;
             }
             if (tid == 0) {
-                const int32_t old_pos = P.pos[unit * CS + dest];
-                const float old_score = has_score ? P.score[unit * CS + dest] : 0.f;
-                const float an = has_score ? ld_peer_f32(peer_addr(&M.anew, 0)) : 0.f;
+                // the evicted token's position and score are the winning key;
+                // otherwise they are read only when a trace is kept
+                int32_t old_pos = static_cast<int32_t>(static_cast<uint32_t>(win_key));
+                float old_score = __uint_as_float(static_cast<uint32_t>(win_key >> 32));
+                if (!evict && P.trace != nullptr) {
+                    old_pos = P.pos[unit * CS + dest];
+                    old_score = has_score ? P.score[unit * CS + dest] : 0.f;
+                }
                 P.pos[unit * CS + dest] = P.p;
-                if (has_score) P.score[unit * CS + dest] = an;
+                if (has_score) P.score[unit * CS + dest] = anew;
                 if (P.trace != nullptr)
                     reinterpret_cast<int4 *>(P.trace)[unit] =
-                        make_int4(dest, old_pos, __float_as_int(old_score), __float_as_int(an));
+                        make_int4(dest, old_pos, __float_as_int(old_score), __float_as_int(anew));
             }
         }
-        // Every thread is past its last read of this unit's aux data (and has
-        // waited for it): the next unit's positions/scores may come in.
-        __syncthreads();
-        if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
-        cluster_sync();  // (last) no CTA moves on while a peer may still read its shared memory
+        if (S > 1) {
+            // Every thread is past its last read of this unit's aux data (and
+            // has waited for it): the next unit's positions/scores may come in.
+            __syncthreads();
+            if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
+            cluster_sync();  // (last) no CTA moves on while a peer may still read its shared memory
+        }
     }
 
     // After a timed-out wait some copies may still be landing: wait for them
