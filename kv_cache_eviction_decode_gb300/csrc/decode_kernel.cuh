@@ -135,16 +135,18 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
         float wmax[kWarps][G];
         float wsum[kWarps][G];
         float m[G];        // this CTA's max logit per head (log2 units)
-        float l[G];        // this CTA's softmax denominator relative to m
-        alignas(16) float o[G][D];  // this CTA's unnormalised output relative to m
         float znew[G];     // the new token's logits (rank 0)
         float pnew[G];     // 2^(znew - m) (rank 0)
         float fac[kMaxSplit][G];  // 2^(m_c - m_global) / l_global per CTA c
-        float anew;        // the new token's score (rank 0)
-        int dest;
-        uint64_t best_key;
-        uint64_t win_key;  // the cluster's winning (score bits, position)
-        int32_t best_slot;
+        // cluster exchange, double-buffered by unit parity: (m, l) of every
+        // CTA per head; from every CTA, its partial output over the
+        // coordinates this CTA owns; every CTA's eviction candidate; rank
+        // 0's new-token score
+        float2 xml[2][kMaxSplit][G];
+        alignas(16) float xo[2][G * D];
+        uint64_t xkey[2][kMaxSplit];
+        int32_t xslot[2][kMaxSplit];
+        float xanew[2];
         uint64_t wkey[kWarps];
         int32_t wslot[kWarps];
     };
@@ -892,44 +894,54 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             if (!evict) dest = dest_mine;
             writer = true;
         } else {
-            // ------------------------------ totals for the cluster exchange
+            // ------------------------------------------ cluster exchange
+            // Every CTA pushes its (m, l) to all CTAs of the cluster and its
+            // output partial to the CTA that owns those coordinates (CTA r
+            // owns the slice [r SL, (r + 1) SL), SL = G D / S), then all wait
+            // once. The buffers alternate between units: a CTA writes a
+            // peer's buffer of parity b again only after both passed this
+            // barrier of the next unit, when the peer has finished reading it.
+            const int b = i & 1;
+            constexpr int GD = G * D;
+            const int SL = GD / S;
             for (int jp = tid; jp < kPairs; jp += kThreads) {
                 const int g = (2 * jp) / D;
                 float ox, oy;
                 cta_o(g, ox, oy);
-                *reinterpret_cast<float2 *>(&M.o[g][2 * jp - g * D]) = make_float2(ox, oy);
+                const int j = 2 * jp, r = j / SL;
+                st_peer_f32x2(peer_addr(&M.xo[b][rank * SL + (j - r * SL)], r), make_float2(ox, oy));
             }
-            if (tid < G) M.l[tid] = cta_l(tid);
-            __syncthreads();
-            cluster_sync();  // (1) every CTA's (m, l, o) is ready
+            if (tid < G) {
+                const float2 ml = make_float2(M.m[tid], cta_l(tid));
+                for (int c = 0; c < S; ++c) st_peer_f32x2(peer_addr(&M.xml[b][rank][tid], c), ml);
+            }
+            cluster_sync();  // (1) every CTA's (m, l) and partials are here
 
             // -------------------------------------------------------- combine
             if (tid < G) {
                 float mg = -INFINITY;
-                for (int c = 0; c < S; ++c) mg = fmaxf(mg, ld_peer_f32(peer_addr(&M.m[tid], c)));
+                for (int c = 0; c < S; ++c) mg = fmaxf(mg, M.xml[b][c][tid].x);
                 float lg = 0.f;
                 for (int c = 0; c < S; ++c) {
-                    const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
-                    const float lc = ld_peer_f32(peer_addr(&M.l[tid], c));
-                    if (mc != -INFINITY) lg += lc * exp2f(mc - mg);
+                    const float2 ml = M.xml[b][c][tid];
+                    if (ml.x != -INFINITY) lg += ml.y * exp2f(ml.x - mg);
                 }
                 if (rank == 0 && !(lg > 0.f && lg <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
                 const float inv = 1.f / lg;
                 for (int c = 0; c < S; ++c) {
-                    const float mc = ld_peer_f32(peer_addr(&M.m[tid], c));
+                    const float mc = M.xml[b][c][tid].x;
                     M.fac[c][tid] = (mc == -INFINITY) ? 0.f : exp2f(mc - mg) * inv;
                 }
             }
             __syncthreads();
             {
-                constexpr int GD = G * D;
-                const int i0 = rank * GD / S, i1 = (rank + 1) * GD / S;
+                const int i0 = rank * SL;
                 T *outp = static_cast<T *>(P.out) + unit * GD;
-                for (int j = i0 + tid; j < i1; j += kThreads) {
-                    const int g = j / D, e = j % D;
+                for (int k = tid; k < SL; k += kThreads) {
+                    const int g = (i0 + k) / D;
                     float o = 0.f;
-                    for (int c = 0; c < S; ++c) o = fmaf(ld_peer_f32(peer_addr(&M.o[g][e], c)), M.fac[c][g], o);
-                    outp[j] = E::from_f32(o);
+                    for (int c = 0; c < S; ++c) o = fmaf(M.xo[b][c * SL + k], M.fac[c][g], o);
+                    outp[i0 + k] = E::from_f32(o);
                 }
             }
 
@@ -963,7 +975,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     float a = 0.f;
 #pragma unroll
                     for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], M.fac[0][g], a);
-                    M.anew = a * (1.0f / G);
+                    anew = a * (1.0f / G);
                 }
                 if (evict) {
                     warp_argmin(best, bslot);
@@ -972,48 +984,38 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                         M.wslot[warp] = bslot;
                     }
                 }
-                __syncthreads();
-                if (evict && tid == 0) {
-                    uint64_t k = ~0ull;
-                    int32_t sl = -1;
-                    for (int w = 0; w < kWarps; ++w)
-                        if (M.wkey[w] < k) {
-                            k = M.wkey[w];
-                            sl = M.wslot[w];
-                        }
-                    M.best_key = k;
-                    M.best_slot = sl;
+                __syncthreads();  // candidates visible; every read of this unit's aux data is done
+                if (evict && warp == 0) {
+                    // this CTA's candidate to every CTA; rank 0's new-token score too
+                    uint64_t k = lane < kWarps ? M.wkey[lane] : ~0ull;
+                    int32_t sl = lane < kWarps ? M.wslot[lane] : -1;
+                    warp_argmin(k, sl);
+                    if (lane < S) {
+                        st_peer_u64(peer_addr(&M.xkey[b][rank], lane), k);
+                        st_peer_s32(peer_addr(&M.xslot[b][rank], lane), sl);
+                    }
+                    if (rank == 0 && lane == 0)
+                        for (int c = 0; c < S; ++c) st_peer_f32(peer_addr(&M.xanew[b], c), anew);
                 }
             }
+            // the next unit's positions/scores may come in
+            if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
 
-            // --------------------------------------------------------- insert
+            // --------------------------------------------------------- victim
             if (evict) {
-                cluster_sync();  // (2) every CTA's candidate is ready
-                if (tid == 0) {
-                    uint64_t k = ~0ull;
-                    int32_t sl = -1;
-                    for (int c = 0; c < S; ++c) {
-                        const uint64_t kc = ld_peer_u64(peer_addr(&M.best_key, c));
-                        const int32_t scs = ld_peer_s32(peer_addr(&M.best_slot, c));
-                        if (kc < k) {
-                            k = kc;
-                            sl = scs;
-                        }
-                    }
-                    if (sl < 0 && rank == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
-                    M.dest = sl;
-                    M.win_key = k;
-                }
-                __syncthreads();
-                dest = M.dest;
-                win_key = M.win_key;
+                cluster_sync();  // (2) every CTA's candidate is here
+                uint64_t k = lane < S ? M.xkey[b][lane] : ~0ull;
+                int32_t sl = lane < S ? M.xslot[b][lane] : -1;
+                warp_argmin(k, sl);
+                win_key = k;
+                dest = sl;
+                if (sl < 0 && rank == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
                 writer = dest >= W.s_lo && dest < W.s_hi;  // the CTA that attended the victim
+                if (writer && has_score) anew = M.xanew[b];
             } else {
-                __syncthreads();
                 dest = dest_mine;
                 writer = rank == 0;
             }
-            if (writer && tid == 0 && has_score) anew = ld_peer_f32(peer_addr(&M.anew, 0));
         }
 
         // ------------------------------------------------------------- insert
@@ -1044,14 +1046,9 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                         make_int4(dest, old_pos, __float_as_int(old_score), __float_as_int(anew));
             }
         }
-        if (S > 1) {
-            // Every thread is past its last read of this unit's aux data (and
-            // has waited for it): the next unit's positions/scores may come in.
-            __syncthreads();
-            if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
-            cluster_sync();  // (last) no CTA moves on while a peer may still read its shared memory
-        }
     }
+    // No CTA leaves while a peer might still store into its shared memory.
+    if (S > 1) cluster_sync();
 
     // After a timed-out wait some copies may still be landing: wait for them
     // (bounded) before the CTA exits.

@@ -216,6 +216,28 @@ __device__ __forceinline__ int32_t ld_peer_s32(uint32_t addr)
     return v;
 }
 
+// Stores into the shared memory of a CTA of the cluster (addresses from
+// peer_addr); ordered before a later barrier.cluster.arrive.release.
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_peer_f32x2(uint32_t addr, float2 v)
+{
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_peer_u64(uint32_t addr, uint64_t v)
+{
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_peer_s32(uint32_t addr, int32_t v)
+{
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // ----------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void grid_dependency_wait()
 {
