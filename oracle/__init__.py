@@ -72,6 +72,8 @@ def lib():
             L.orc_commit.restype = I
             L.orc_prefill.argtypes = [P, P, P, I]
             L.orc_prefill.restype = I
+            L.orc_prefill_scored.argtypes = [P, P, P, P, I, P]
+            L.orc_prefill_scored.restype = I
             L.orc_step.argtypes = [P, P, P, P, P]
             L.orc_step.restype = I
             L.orc_run.argtypes = [P, I, I, P, P, P, P, I]
@@ -122,6 +124,19 @@ class Unit:
         rc = self._L.orc_prefill(self.h, _ptr(k), _ptr(v), k.shape[0])
         if rc:
             raise RuntimeError(f"oracle prefill failed: {rc}")
+
+    def prefill_scored(self, q, k, v) -> np.ndarray:
+        """Q-seeded prefill of an empty H2O unit: q [G][P][d], k/v [P][d].
+        Returns the P prompt scores (before the cut to the budget)."""
+        q, k, v = _f32(q), _f32(k), _f32(v)
+        P = k.shape[0]
+        if q.shape != (self.G, P, self.d) or v.shape != k.shape:
+            raise ValueError("oracle prefill_scored: q must be [G][P][d], k and v [P][d]")
+        scores = np.empty(P, dtype=np.float64)
+        rc = self._L.orc_prefill_scored(self.h, _ptr(q), _ptr(k), _ptr(v), P, _ptr(scores))
+        if rc:
+            raise RuntimeError(f"oracle prefill_scored failed: {rc}")
+        return scores
 
     def attend(self, q, k_new, v_new) -> np.ndarray:
         q, k, v = _f32(q), _f32(k_new), _f32(v_new)

@@ -452,6 +452,92 @@ int orc_prefill(orc_unit *u, const float *k, const float *v, int n)
     return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Q-seeded prefill (H2O).                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* The prompt is scored by its own causal attention, then cut to the budget by
+ * the greedy rule of Algorithm 1 ("h2o: heavy-hitter oracle" summary: the
+ * score is the cumulative attention a token receives; remove the v whose
+ * removal leaves the highest total):
+ *   z_gij   = q_gi . k_j / sqrt(d)          for j <= i   (query i, key j)
+ *   p_gij   = exp(z_gij - m_gi) / l_gi      softmax over j <= i
+ *   score_j = (1/G) sum_g sum_{i >= j} p_gij
+ * While more than K prompt tokens remain, remove the eligible v (n_sink <= pos
+ * <= (P - 1) - n_recent) maximising F(T \ {v}); the scores do not change
+ * between removals (no attention happens in between). The kept tokens fill
+ * slots 0, 1, ... in ascending position order and keep their scores.
+ * q is [G][P][d], k and v are [P][d]; scores_out (optional) receives the P
+ * prompt scores before the cut. Only on an empty H2O unit. */
+int orc_prefill_scored(orc_unit *u, const float *q, const float *k, const float *v, int P, double *scores_out)
+{
+    if (u->policy != ORC_H2O || u->prompt_len != 0 || u->t != 0 || u->have_new) return ORC_ESTATE;
+    if (P < 1) return ORC_EINVAL;
+    const int d = u->d, G = u->G;
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    double *score = (double *)calloc((size_t)P, sizeof(double));
+    double *z = (double *)malloc(sizeof(double) * (size_t)P);
+    char *alive = (char *)malloc((size_t)P);
+    if (!score || !z || !alive) { free(score); free(z); free(alive); return ORC_ECAPACITY; }
+
+    for (int g = 0; g < G; ++g) {
+        for (int i = 0; i < P; ++i) {
+            const float *qi = q + ((size_t)g * P + i) * d;
+            double m = -INFINITY;
+            for (int j = 0; j <= i; ++j) {
+                double dot = 0.0;
+                for (int e = 0; e < d; ++e) dot += (double)qi[e] * (double)k[(size_t)j * d + e];
+                z[j] = dot * inv_sqrt_d;
+                if (z[j] > m) m = z[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j <= i; ++j) l += exp(z[j] - m);
+            for (int j = 0; j <= i; ++j) score[j] += exp(z[j] - m) / l;
+        }
+    }
+    for (int j = 0; j < P; ++j) score[j] /= (double)G;
+    if (scores_out) memcpy(scores_out, score, sizeof(double) * (size_t)P);
+
+    /* Greedy cut to the budget, one removal at a time. */
+    for (int j = 0; j < P; ++j) alive[j] = 1;
+    int n_alive = P;
+    const int last = P - 1;
+    while (n_alive > u->budget) {
+        double total = 0.0; /* F(T) */
+        for (int j = 0; j < P; ++j)
+            if (alive[j]) total += score[j];
+        int best = -1, am = -1;
+        double best_F = -INFINITY;
+        for (int j = 0; j < P; ++j) {
+            if (!alive[j] || !(j >= u->n_sink && j <= last - u->n_recent)) continue;
+            double F = total - score[j];
+            if (best < 0 || F > best_F || (F == best_F && (score[j] < score[best] || (score[j] == score[best] && j < best)))) {
+                best = j;
+                best_F = F;
+            }
+            if (am < 0 || score[j] < score[am] || (score[j] == score[am] && j < am)) am = j;
+        }
+        if (best < 0) break; /* nothing eligible: cannot happen when K = n_sink + n_heavy + n_recent */
+        if (am != best) u->greedy_disagreements++;
+        alive[best] = 0;
+        u->evicted_mass += score[best];
+        n_alive--;
+    }
+
+    int slot = 0;
+    for (int j = 0; j < P && slot < u->cap; ++j) {
+        if (!alive[j]) continue;
+        u->pos[slot] = j;
+        memcpy(u->k + (size_t)slot * d, k + (size_t)j * d, sizeof(float) * (size_t)d);
+        memcpy(u->v + (size_t)slot * d, v + (size_t)j * d, sizeof(float) * (size_t)d);
+        u->score[slot] = score[j];
+        slot++;
+    }
+    u->prompt_len = P;
+    free(score); free(z); free(alive);
+    return ORC_OK;
+}
+
 /* One full decode step with the oracle's own decision. Returns the slot taken. */
 int orc_step(orc_unit *u, const float *q, const float *k_new, const float *v_new, double *out)
 {
