@@ -36,10 +36,9 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 CSRC = os.path.join(ROOT, "kv_cache_eviction_decode_gb300", "csrc")
 
 
-# Sources that decide what the decode launch does and how it is configured;
-# a committed traffic figure counts only for the kernel built from these.
-DECODE_SOURCES = ("api.cu", "decode_bf16.cu", "decode_dispatch.h", "decode_f32.cu", "decode_kernel.cuh",
-                  "device_common.cuh")
+# The decode kernel's device sources; a committed traffic figure counts only
+# for the kernel built from these.
+DECODE_SOURCES = ("decode_bf16.cu", "decode_dispatch.h", "decode_f32.cu", "decode_kernel.cuh", "device_common.cuh")
 
 
 def kernel_source_hash() -> str:
