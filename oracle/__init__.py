@@ -74,6 +74,8 @@ def lib():
             L.orc_prefill.restype = I
             L.orc_prefill_scored.argtypes = [P, P, P, P, I, P]
             L.orc_prefill_scored.restype = I
+            L.orc_prompt_tail_scores.argtypes = [P, P, I, I, I, I, P]
+            L.orc_prompt_tail_scores.restype = I
             L.orc_step.argtypes = [P, P, P, P, P]
             L.orc_step.restype = I
             L.orc_run.argtypes = [P, I, I, P, P, P, P, I]
@@ -237,6 +239,20 @@ def run(units, q, k, v, n_threads: int = 0, keep_out: bool = False):
                    _ptr(out) if keep_out else None, int(n_threads))
     if rc:
         raise RuntimeError(f"oracle run failed: {rc}")
+    return out
+
+
+def prompt_tail_scores(q, k, j0: int) -> np.ndarray:
+    """Prompt scores of the keys j >= j0 (q [G][P][d], k [P][d]): the column
+    sums over the rows i >= j of the causal softmax, mean over G."""
+    q, k = _f32(q), _f32(k)
+    G, P, d = q.shape
+    if k.shape != (P, d):
+        raise ValueError("prompt_tail_scores: k must be [P][d]")
+    out = np.empty(P - j0, dtype=np.float64)
+    rc = lib().orc_prompt_tail_scores(_ptr(q), _ptr(k), G, P, d, j0, _ptr(out))
+    if rc:
+        raise RuntimeError(f"oracle prompt_tail_scores failed: {rc}")
     return out
 
 

@@ -538,6 +538,37 @@ int orc_prefill_scored(orc_unit *u, const float *q, const float *k, const float 
     return ORC_OK;
 }
 
+/* The same prompt scores for the keys j >= j0 only: score_j needs the rows
+ * i >= j, so only the rows i >= j0 are evaluated, each with its full softmax
+ * over j' <= i. q is [G][P][d], k is [P][d]; out receives P - j0 values.
+ * Independent of any unit: a sampled check of long prompts. */
+int orc_prompt_tail_scores(const float *q, const float *k, int G, int P, int d, int j0, double *out)
+{
+    if (G < 1 || P < 1 || d < 1 || j0 < 0 || j0 >= P) return ORC_EINVAL;
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    double *z = (double *)malloc(sizeof(double) * (size_t)P);
+    if (!z) return ORC_ECAPACITY;
+    for (int j = j0; j < P; ++j) out[j - j0] = 0.0;
+    for (int g = 0; g < G; ++g) {
+        for (int i = j0; i < P; ++i) {
+            const float *qi = q + ((size_t)g * P + i) * d;
+            double m = -INFINITY;
+            for (int j = 0; j <= i; ++j) {
+                double dot = 0.0;
+                for (int e = 0; e < d; ++e) dot += (double)qi[e] * (double)k[(size_t)j * d + e];
+                z[j] = dot * inv_sqrt_d;
+                if (z[j] > m) m = z[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j <= i; ++j) l += exp(z[j] - m);
+            for (int j = j0; j <= i; ++j) out[j - j0] += exp(z[j] - m) / l;
+        }
+    }
+    for (int j = j0; j < P; ++j) out[j - j0] /= (double)G;
+    free(z);
+    return ORC_OK;
+}
+
 /* One full decode step with the oracle's own decision. Returns the slot taken. */
 int orc_step(orc_unit *u, const float *q, const float *k_new, const float *v_new, double *out)
 {

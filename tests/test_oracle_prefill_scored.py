@@ -173,3 +173,17 @@ def test_exact_tie_evicts_the_older():
     assert s[4] == 0.0 and s[7] == 0.0 and np.all(np.delete(s, [4, 7]) > 0)
     kept = set(u.positions()[:11].tolist())
     assert kept == set(range(P)) - {4}
+
+
+@pytest.mark.parametrize("j0", [0, 1, 57, 79])
+def test_tail_scores_equal_sdpa_and_full(j0):
+    import oracle
+    rng = np.random.default_rng(40 + j0)
+    G, P, d = 4, 80, 16
+    q, k, v = _inputs(rng, G, P, d)
+    tail = oracle.prompt_tail_scores(q, k, j0)
+    ref = _sdpa_column_sums(q, k).mean(axis=0)[j0:]
+    np.testing.assert_allclose(tail, ref, rtol=0, atol=1e-12)
+    u = Unit(H2O, 2, P, 3, P + 5, 0, 0, G, d)
+    full = u.prefill_scored(q, k, v)
+    np.testing.assert_allclose(tail, full[j0:], rtol=0, atol=1e-13)
