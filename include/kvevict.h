@@ -142,6 +142,36 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
  * RANDOM: CAPACITY if the layer's prompt would exceed max_prompt. */
 int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_tokens);
 
+/* Q-seeded prefill of an empty H2O layer ("h2o: heavy-hitter oracle" summary,
+ * Algorithm 1: a token's score is the cumulative attention it receives; over
+ * budget, remove the token whose removal leaves the highest total). The prompt
+ * scores itself with its own causal attention:
+ *   score_j = (1/G) sum over the G query heads g of the KV head, sum over
+ *             prompt queries i >= j, of softmax_j(q_gi . k_j / sqrt(d)) (j <= i),
+ * then, if prompt_len > budget, the n_sink first and n_recent last positions
+ * stay and, of the others, the prompt_len - budget with the smallest (score,
+ * position) leave (the greedy rule with scores that do not change during the
+ * cut). The kept tokens fill slots 0, 1, ... in ascending position order, with
+ * their scores; decode steps then add to those scores. (Calling
+ * kvevict_decode_step for each prompt token instead applies Algorithm 1 from
+ * the first token, with eviction during the prompt.)
+ *   Q:    device, [batch][n_q_heads][prompt_len][head_dim] bf16;
+ *   K, V: device, [batch][n_kv_heads][prompt_len][head_dim] bf16;
+ *   workspace: device, 256-byte aligned, at least
+ *         kvevict_prefill_scored_workspace_bytes() bytes, owned by the caller.
+ *         Layout: per query row the log2 of its softmax normaliser, fp32
+ *         [batch * n_q_heads][Ps] with Ps = prompt_len rounded up to 128; then,
+ *         at the next 256-byte boundary, every prompt token's score before the
+ *         cut, fp32 [batch][n_kv_heads][prompt_len]. Both are valid once the
+ *         stream has passed the call; the caller may reuse the memory after.
+ * The attention statistics run on the tcgen05 tensor cores (bf16 in, fp32
+ * accumulate). INVALID_ARG unless the policy is H2O and the dtype bf16, for
+ * prompt_len outside 1..49152, for null or misaligned pointers or a short
+ * workspace; STATE if the layer already holds tokens or has decoded. */
+int kvevict_prefill_scored_workspace_bytes(kvevict_t h, int prompt_len, size_t *bytes);
+int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K, const void *V, int prompt_len,
+                           void *workspace, size_t workspace_bytes);
+
 /* One decode step of `layer` for every sequence (the four steps above).
  *   q:     device, [batch][n_q_heads][head_dim]; query heads g*G .. g*G+G-1
  *          share KV head g.

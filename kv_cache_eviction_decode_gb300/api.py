@@ -80,6 +80,34 @@ class KVEvictCache:
         self._dev(V, shp, "V")
         check(self._L.kvevict_prefill(self.h, layer, _ptr(K), _ptr(V), n), "kvevict_prefill")
 
+    def prefill_scored_workspace_bytes(self, prompt_len: int) -> int:
+        n = ctypes.c_size_t()
+        check(self._L.kvevict_prefill_scored_workspace_bytes(self.h, prompt_len, ctypes.byref(n)),
+              "kvevict_prefill_scored_workspace_bytes")
+        return n.value
+
+    def prefill_scored(self, layer: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
+                       workspace: torch.Tensor | None = None) -> torch.Tensor:
+        """Q-seeded prefill of an empty H2O layer: Q [B][Hq][P][d], K/V [B][Hkv][P][d].
+        Returns the prompt scores before the cut, [B][Hkv][P] fp32: a view of
+        the workspace, valid once the stream has passed the call."""
+        n = K.shape[2]
+        self._dev(Q, (self.B, self.Hq, n, self.D), "Q")
+        self._dev(K, (self.B, self.Hkv, n, self.D), "K")
+        self._dev(V, (self.B, self.Hkv, n, self.D), "V")
+        need = self.prefill_scored_workspace_bytes(n)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        if workspace.device != self.device or workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace: need {need} bytes on {self.device}")
+        check(self._L.kvevict_prefill_scored(self.h, layer, _ptr(Q), _ptr(K), _ptr(V), n, _ptr(workspace),
+                                             workspace.numel() * workspace.element_size()),
+              "kvevict_prefill_scored")
+        ps = (n + 127) // 128 * 128
+        off = (self.B * self.Hq * ps * 4 + 255) // 256 * 256
+        raw = workspace.view(torch.uint8).reshape(-1)[off:off + self.B * self.Hkv * n * 4]
+        return raw.view(torch.float32).view(self.B, self.Hkv, n)
+
     def decode_step(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                     out: torch.Tensor | None = None) -> torch.Tensor:
         self._dev(q, (self.B, self.Hq, self.D), "q")

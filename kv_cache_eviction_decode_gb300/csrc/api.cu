@@ -20,6 +20,7 @@
 #include "decode_dispatch.h"
 #include "decode_kernel.cuh"
 #include "kvevict.h"
+#include "prompt_attn.h"
 
 using namespace kvevict;
 
@@ -220,9 +221,10 @@ int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInf
 
 template <typename T> T *at(const kvevict_handle *h, size_t off) { return reinterpret_cast<T *>(h->state + off); }
 
-// 2-D tensor map over one layer's K or V cache: rows = units * C, each of
-// head_dim bf16; boxes of 32 rows x 64 elements, 128-byte swizzle.
-int make_tensor_map(CUtensorMap *out, void *base, uint64_t rows, int head_dim)
+// 2-D tensor map over rows of head_dim bf16 (a layer's K or V cache: rows =
+// units * C; prompt Q or K: rows = heads * P); boxes of box_rows rows x 64
+// elements, 128-byte swizzle.
+int make_tensor_map(CUtensorMap *out, const void *base, uint64_t rows, int head_dim, int box_rows = kTile)
 {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     if (!encode) {
@@ -234,9 +236,9 @@ int make_tensor_map(CUtensorMap *out, void *base, uint64_t rows, int head_dim)
     }
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), rows};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -554,6 +556,110 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
     ls.prompt_len += n_tokens;
     ls.count = c.policy == KVEVICT_RANDOM ? ls.prompt_len : std::min(L.C, ls.prompt_len);
     h->stats.prefill_tokens += n_tokens;
+    return KVEVICT_OK;
+}
+
+namespace {
+
+// Workspace of the Q-seeded prefill: per query row its log-normaliser
+// ([B * Hq][Ps], Ps = P rounded up to a tile, so each tile's 128 entries are
+// addressable), then per key its score ([B * Hkv][P]).
+struct ScoredWorkspace {
+    size_t stats_off = 0, score_off = 0, bytes = 0;
+    int Ps = 0;
+};
+
+ScoredWorkspace scored_workspace(const kvevict_config &c, int P)
+{
+    ScoredWorkspace w;
+    w.Ps = (P + kPromptTile - 1) / kPromptTile * kPromptTile;
+    w.stats_off = 0;
+    w.score_off = align_up(static_cast<size_t>(c.batch) * c.n_q_heads * w.Ps * 4);
+    w.bytes = w.score_off + align_up(static_cast<size_t>(c.batch) * c.n_kv_heads * P * 4);
+    return w;
+}
+
+}  // namespace
+
+int kvevict_prefill_scored_workspace_bytes(kvevict_t h, int prompt_len, size_t *bytes)
+{
+    if (!h || !bytes || prompt_len < 1 || prompt_len > kPromptMaxLen) return KVEVICT_ERR_INVALID_ARG;
+    *bytes = scored_workspace(h->cfg, prompt_len).bytes;
+    return KVEVICT_OK;
+}
+
+int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K, const void *V, int prompt_len,
+                           void *workspace, size_t workspace_bytes)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    const kvevict_config &c = h->cfg;
+    const Layout &L = h->L;
+    const int P = prompt_len;
+    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16) return KVEVICT_ERR_INVALID_ARG;
+    if (P < 1 || P > kPromptMaxLen) return KVEVICT_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !workspace || !aligned16(Q) || !aligned16(K) || !aligned16(V) ||
+        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return KVEVICT_ERR_INVALID_ARG;
+    const ScoredWorkspace ws = scored_workspace(c, P);
+    if (workspace_bytes < ws.bytes) return KVEVICT_ERR_INVALID_ARG;
+    const long long q_rows = static_cast<long long>(c.batch) * c.n_q_heads * P;
+    if (q_rows >= (1LL << 31)) return KVEVICT_ERR_INVALID_ARG;  // tensor-map row coordinates are int32
+    if (static_cast<long long>(c.batch) * c.n_q_heads > 65535) return KVEVICT_ERR_INVALID_ARG;  // grid height
+    LayerState &ls = h->layers[layer];
+    if (ls.prompt_len != 0 || ls.t != 0) return KVEVICT_ERR_STATE;
+
+    uint8_t *wsb = static_cast<uint8_t *>(workspace);
+    PromptAttnParams ap{};
+    CUtensorMap tq, tk;
+    int rc = make_tensor_map(&tq, Q, static_cast<uint64_t>(q_rows), c.head_dim, kPromptTile);
+    if (rc == KVEVICT_OK)
+        rc = make_tensor_map(&tk, K, static_cast<uint64_t>(c.batch) * c.n_kv_heads * P, c.head_dim, kPromptTile);
+    if (rc) return rc;
+    static_assert(sizeof(CUtensorMap) == sizeof(PromptTmap), "tensor map size");
+    ap.stats = reinterpret_cast<float *>(wsb + ws.stats_off);
+    ap.score = reinterpret_cast<float *>(wsb + ws.score_off);
+    ap.P = P;
+    ap.Ps = ws.Ps;
+    ap.G = L.G;
+    ap.Hq = c.n_q_heads;
+    ap.Hkv = c.n_kv_heads;
+    ap.q_lo = 0;
+    ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
+    ap.err = at<uint32_t>(h, L.off_err);
+    // pass 1: A = query tiles, B = key tiles; pass 2: A = key tiles, B = query tiles
+    std::memcpy(&ap.tma, &tq, sizeof tq);
+    std::memcpy(&ap.tmb, &tk, sizeof tk);
+    cudaError_t e = launch_prompt_rowstats(ap, c.head_dim, c.batch, h->stream);
+    if (e == cudaSuccess) {
+        std::memcpy(&ap.tma, &tk, sizeof tk);
+        std::memcpy(&ap.tmb, &tq, sizeof tq);
+        e = launch_prompt_colsum(ap, c.head_dim, c.batch, h->stream);
+    }
+    if (e == cudaSuccess) {
+        PromptSelectParams sp{};
+        sp.score = ap.score;
+        sp.K = K;
+        sp.V = V;
+        sp.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
+        sp.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
+        sp.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
+        sp.cscore = at<float>(h, L.off_score) + layer * L.layer_pslots;
+        sp.P = P;
+        sp.C = L.C;
+        sp.cstride = L.Cs;
+        sp.row_bytes = c.head_dim * L.elem;
+        sp.budget = c.budget;
+        sp.n_sink = c.n_sink;
+        sp.n_recent = c.n_recent;
+        sp.err = ap.err;
+        e = launch_prompt_select(sp, static_cast<int>(L.units), h->stream);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    h->last_layer = layer;
+    ls.prompt_len = P;
+    ls.count = std::min(L.C, P);
+    h->stats.prefill_tokens += P;
     return KVEVICT_OK;
 }
 

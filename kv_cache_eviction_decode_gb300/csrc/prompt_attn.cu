@@ -1,0 +1,431 @@
+// prompt_attn.cu -- Q-seeded prefill: the prompt's causal attention scores the
+// prompt, then the budget is enforced by the greedy rule of Algorithm 1
+// ("h2o: heavy-hitter oracle" summary: the cumulative attention a token
+// receives is its score; remove the token whose removal keeps the highest
+// total). With z_gij = q_gi . k_j / sqrt(d) over j <= i:
+//   pass 1  per query row i of head g: ms_gi = m_gi + log2(l_gi), the log2 of
+//           its softmax normaliser (m the row max, l the row sum, log2 units);
+//   pass 2  per key j: score_j = (1/G) sum_g sum_{i >= j} 2^(z_gij - ms_gi);
+//   cut     keep the n_sink first and n_recent last positions and, of the
+//           rest, all but the P - K with the smallest (score, position).
+//
+// Passes 1 and 2 are one kernel body on the 5th-generation tensor cores: a
+// CTA keeps one 128-row tile A (pass 1: 128 queries; pass 2: 128 keys) in
+// shared memory and streams 128-row tiles B (pass 1: the keys up to the
+// diagonal; pass 2: the queries from the diagonal on, for each of the G query
+// heads). tcgen05.mma computes A B^T (128 x 128, fp32) into one of two TMEM
+// accumulators while the epilogue warps read the other; every thread owns one
+// row of A, so both reductions (over a query row, over a key column of the
+// attention matrix) stay inside a thread.
+//
+// Warps: 0-7 epilogue (two per TMEM lane quadrant, each taking 64 of the 128
+// columns), 8 TMA producer (and TMEM allocation), 9 MMA issuer.
+#include <cfloat>
+#include <cmath>
+
+#include "device_common.cuh"
+#include "prompt_attn.h"
+#include "tc5_common.cuh"
+
+namespace kvevict {
+
+namespace {
+
+constexpr int kPT = kPromptTile;
+constexpr int kPStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+constexpr int kPThreads = (kEpiWarps + 2) * 32;
+constexpr uint32_t kTmemCols = 256;  // two 128-column fp32 accumulators
+
+enum PromptMode : int { kRowStats = 0, kColSum = 1 };
+
+template <int D> struct PromptLayout {
+    static constexpr int kTileBytes = kPT * D * 2;
+    static constexpr int kBoxBytes = kPT * 128;  // one 128-row x 64-column box
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kTileBytes;
+    static constexpr int kOffBar = kOffB + kPStages * kTileBytes;
+    static constexpr int kOffXchg = kOffBar + 256;
+    static constexpr int kBytes = kOffXchg + kPT * 8 + 1024;  // + slack to align the base to 1 KB
+};
+
+__device__ __forceinline__ void flag_timeout(uint32_t *err) { atomicOr(err, KVEVICT_DEV_WAIT_TIMEOUT); }
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_constant__ PromptAttnParams p)
+{
+    using L = PromptLayout<D>;
+    extern __shared__ uint8_t praw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(praw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
+    uint64_t *a_full = bars;
+    uint64_t *b_full = bars + 1;
+    uint64_t *b_empty = b_full + kPStages;
+    uint64_t *s_full = b_empty + kPStages;
+    uint64_t *s_empty = s_full + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(s_empty + 2);
+    float2 *xchg = reinterpret_cast<float2 *>(sm + L::kOffXchg);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nT = (p.P + kPT - 1) / kPT;
+    const int qlo_t = p.q_lo / kPT;
+    // This CTA: pass 1 -- query tile `tile` of query head `head` (= b * Hq + qh),
+    // B tiles = key tiles 0..tile of its KV head; pass 2 -- key tile `tile` of
+    // unit `head` (= b * Hkv + kvh), B tiles = (query head g, query tile qt)
+    // for g < G and qt from max(tile, first query tile) on.
+    const int head = blockIdx.y;
+    const int tile = MODE == kRowStats ? nT - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    const int qt0 = max(tile, qlo_t), nq = nT - qt0;
+    const int n_b = MODE == kRowStats ? tile + 1 : p.G * nq;
+    const int a_row = head * p.P + tile * kPT;
+    auto b_row = [&](int n) -> int {
+        if (MODE == kRowStats) {
+            const int b = head / p.Hq, qh = head - b * p.Hq;
+            return (b * p.Hkv + qh / p.G) * p.P + n * kPT;
+        } else {
+            const int b = head / p.Hkv, kvh = head - b * p.Hkv;
+            const int g = n / nq, qt = qt0 + (n - g * nq);
+            return (b * p.Hq + kvh * p.G + g) * p.P + qt * kPT;
+        }
+    };
+
+    if (tid == 0) {
+        mbar_init(a_full, 1);
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&b_full[s], 1);
+            mbar_init(&b_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_empty[s], kEpiWarps);
+        }
+        mbar_fence_init();
+    }
+    if (warp == kProdWarp) tmem_alloc(tslot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tslot);
+
+    int issued_b = 0;     // producer: B tiles whose copies were issued
+    int issued_mma = 0;   // MMA issuer: tiles whose MMAs were issued
+
+    if (warp == kProdWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(a_full, L::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_2d_plain(sm + L::kOffA + c * L::kBoxBytes, &p.tma, c * 64, a_row, a_full);
+            for (int n = 0; n < n_b; ++n) {
+                const int s = n % kPStages;
+                if (n >= kPStages && !mbar_wait(&b_empty[s], ((n / kPStages) - 1) & 1)) {
+                    flag_timeout(p.err);
+                    break;
+                }
+                mbar_arrive_expect_tx(&b_full[s], L::kTileBytes);
+                const int row = b_row(n);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_2d_plain(sm + L::kOffB + s * L::kTileBytes + c * L::kBoxBytes, &p.tmb, c * 64, row,
+                                      &b_full[s]);
+                issued_b = n + 1;
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kPT, kPT);
+            bool ok = mbar_wait(a_full, 0);
+            for (int n = 0; ok && n < n_b; ++n) {
+                const int s = n % kPStages, acc = n & 1;
+                if (!mbar_wait(&b_full[s], (n / kPStages) & 1)) ok = false;
+                else if (n >= 2 && !mbar_wait(&s_empty[acc], ((n >> 1) - 1) & 1)) ok = false;
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sm + L::kOffA), b0 = smem_u32(sm + L::kOffB + s * L::kTileBytes);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t koff = static_cast<uint32_t>((k >> 2) * L::kBoxBytes + (k & 3) * 32);
+                    tc_mma_bf16(tmem + static_cast<uint32_t>(acc * kPT), smem_desc_sw128(a0 + koff),
+                                smem_desc_sw128(b0 + koff), idesc, k > 0);
+                }
+                tc_commit(&b_empty[s]);
+                tc_commit(&s_full[acc]);
+                issued_mma = n + 1;
+            }
+            if (!ok) flag_timeout(p.err);
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int quad = warp & 3, half = warp >> 2;
+        const int row = quad * 32 + lane;      // TMEM lane = row of the A tile
+        const int a_idx = tile * kPT + row;    // pass 1: query i; pass 2: key j
+        const uint32_t lane_field = static_cast<uint32_t>(quad * 32) << 16;
+        float m = -INFINITY, l = 0.f;          // pass 1: running max and sum (log2 units)
+        float acc = 0.f;                       // pass 2: mass received
+        bool ok = true;
+        for (int n = 0; n < n_b; ++n) {
+            const int sb = n & 1;
+            // the TMEM loads below are warp-collective: the whole warp agrees on `ok`
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (n >> 1) & 1))) {
+                ok = false;
+                if (lane == 0) flag_timeout(p.err);
+            }
+            tc_fence_after();
+            if (ok) {
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_field + static_cast<uint32_t>(sb * kPT + half * 64 + c0), r);
+                    tc_wait_ld();
+                    const int col0 = half * 64 + c0;
+                    if (MODE == kRowStats) {
+                        // keys j = n * 128 + col0 + e; below the diagonal tile all are valid
+                        const int j0 = n * kPT + col0;
+                        const bool diag = n == tile;
+                        float z[32];
+                        float cm = -INFINITY;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int j = j0 + e;
+                            z[e] = (!diag || (j <= a_idx && j < p.P)) ? __uint_as_float(r[e]) * p.scale_log2
+                                                                      : -INFINITY;
+                            cm = fmaxf(cm, z[e]);
+                        }
+                        if (cm > m) {
+                            l *= exp2f(m - cm);
+                            m = cm;
+                        }
+                        if (m != -INFINITY) {
+                            float s = 0.f;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) s += exp2f(z[e] - m);
+                            l += s;
+                        }
+                    } else {
+                        // queries i = qt * 128 + col0 + e of query head g
+                        const int g = n / nq, qt = qt0 + (n - g * nq);
+                        const int i0 = qt * kPT + col0;
+                        const int b = head / p.Hkv, kvh = head - b * p.Hkv;
+                        const float4 *st = reinterpret_cast<const float4 *>(
+                            p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + i0);
+                        const bool full = qt > tile && i0 + 32 <= p.P && i0 >= p.q_lo;
+                        float s = 0.f;
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 ms = __ldg(st + e4);
+                            const float mv[4] = {ms.x, ms.y, ms.z, ms.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int e = e4 * 4 + t, i = i0 + e;
+                                const float z = __uint_as_float(r[e]) * p.scale_log2 - mv[t];
+                                if (full || (i >= a_idx && i < p.P && i >= p.q_lo)) s += exp2f(z);
+                            }
+                        }
+                        acc += s;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[sb]);
+        }
+        // the two column halves of each row meet: warps 4-7 hand over to 0-3
+        if (half == 1) xchg[row] = MODE == kRowStats ? make_float2(m, l) : make_float2(acc, 0.f);
+        named_bar_sync(1, kEpiWarps * 32);
+        if (half == 0 && ok) {
+            const float2 o = xchg[row];
+            if (MODE == kRowStats) {
+                const float mm = fmaxf(m, o.x);
+                const float ll = (m == -INFINITY ? 0.f : l * exp2f(m - mm)) + (o.x == -INFINITY ? 0.f : o.y * exp2f(o.x - mm));
+                if (a_idx < p.P) p.stats[static_cast<size_t>(head) * p.Ps + a_idx] = mm + log2f(ll);
+            } else {
+                if (a_idx < p.P) p.score[static_cast<size_t>(head) * p.P + a_idx] = (acc + o.x) * (1.f / p.G);
+            }
+        }
+    }
+
+    // Teardown. After a timed-out wait, let the copies and MMAs already issued
+    // finish (bounded) before the TMEM and the shared memory go away.
+    if (warp == kProdWarp && lane == 0) {
+        for (int n = max(0, issued_b - kPStages); n < issued_b; ++n)
+            mbar_wait(&b_full[n % kPStages], (n / kPStages) & 1);
+    }
+    if (warp == kMmaWarp && lane == 0) {
+        for (int n = max(0, issued_mma - 2); n < issued_mma; ++n) mbar_wait(&s_full[n & 1], (n >> 1) & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProdWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ cut
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane)
+{
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+    }
+    return v;
+}
+
+// Keeps the first n_sink and last n_recent positions and, of the others, all
+// but the P - K smallest (score, position) keys; the kept tokens fill slots
+// 0, 1, ... in ascending position order. One CTA per unit: the unit's score
+// bits (non-negative floats, so their bit patterns order like the values) in
+// shared memory; the cut threshold by binary search on the bit pattern; ties
+// at the threshold go in position order, oldest first.
+__global__ void __launch_bounds__(kSelThreads) prompt_select_kernel(const PromptSelectParams p)
+{
+    extern __shared__ uint32_t sbits[];
+    __shared__ int red[kSelWarps];
+    __shared__ int total;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t unit = blockIdx.x;
+    const int P = p.P;
+    const int e_lo = p.n_sink, e_hi = P - p.n_recent;  // eligible positions [e_lo, e_hi)
+    for (int j = tid; j < P; j += kSelThreads) {
+        const float s = p.score[unit * P + j];
+        if (!(s >= 0.f && s <= FLT_MAX)) atomicOr(p.err, KVEVICT_DEV_NONFINITE);
+        sbits[j] = __float_as_uint(s);
+    }
+    __syncthreads();
+
+    // block-wide sum of v; every thread gets it
+    auto block_sum = [&](int v) -> int {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) red[warp] = v;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < kSelWarps ? red[lane] : 0;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
+            if (lane == 0) total = w;
+        }
+        __syncthreads();
+        const int t = total;
+        __syncthreads();
+        return t;
+    };
+    // exclusive prefix of v over the threads in order (x) and the total (y)
+    auto block_scan = [&](int v) -> int2 {
+        const int inc = warp_incl_scan(v, lane);
+        if (lane == 31) red[warp] = inc;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = lane < kSelWarps ? red[lane] : 0;
+            const int winc = warp_incl_scan(w, lane);
+            if (lane < kSelWarps) red[lane] = winc - w;  // exclusive warp offsets
+            if (lane == kSelWarps - 1) total = winc;
+        }
+        __syncthreads();
+        const int2 r = make_int2(red[warp] + inc - v, total);
+        __syncthreads();
+        return r;
+    };
+
+    const int E = P > p.budget ? P - p.budget : 0;  // tokens to remove
+    uint32_t T = 0;
+    int need = 0;
+    if (E > 0) {
+        // smallest bit pattern T with #{eligible: bits <= T} >= E
+        uint32_t lo = 0, hi = 0xFFFFFFFFu;
+        while (lo < hi) {
+            const uint32_t mid = lo + (hi - lo) / 2;
+            int c = 0;
+            for (int j = e_lo + tid; j < e_hi; j += kSelThreads) c += sbits[j] <= mid;
+            if (block_sum(c) >= E) hi = mid;
+            else lo = mid + 1;
+        }
+        T = lo;
+        int c = 0;
+        for (int j = e_lo + tid; j < e_hi; j += kSelThreads) c += sbits[j] < T;
+        need = E - block_sum(c);  // how many of the tokens at exactly T go, oldest first
+    }
+
+    int tie_base = 0, slot_base = 0;
+    for (int j0 = 0; j0 < P; j0 += kSelThreads) {
+        const int j = j0 + tid;
+        const bool in = j < P;
+        const bool elig = in && j >= e_lo && j < e_hi;
+        const uint32_t b = in ? sbits[j] : 0u;
+        const bool tie = E > 0 && elig && b == T;
+        const int2 ts = block_scan(tie ? 1 : 0);
+        const int tie_rank = tie_base + ts.x;
+        const bool evict = E > 0 && elig && (b < T || (tie && tie_rank < need));
+        const bool keep = in && !evict;
+        const int2 ks = block_scan(keep ? 1 : 0);
+        const int slot = slot_base + ks.x;
+        if (keep && slot < p.C) {
+            p.pos[unit * p.cstride + slot] = j;
+            p.cscore[unit * p.cstride + slot] = __uint_as_float(b);
+        }
+        tie_base += ts.y;
+        slot_base += ks.y;
+    }
+    __syncthreads();  // the positions written above are visible to the whole CTA
+
+    // copy the kept rows: one warp per slot, K then V in 16-byte vectors
+    const int kept = min(slot_base, p.C);
+    const int vecs = p.row_bytes / 16;
+    for (int s = warp; s < kept; s += kSelWarps) {
+        const int j = p.pos[unit * p.cstride + s];
+        for (int vi = lane; vi < 2 * vecs; vi += 32) {
+            const int which = vi / vecs, off = vi - which * vecs;
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(which ? p.V : p.K) +
+                                                               (unit * P + j) * static_cast<size_t>(p.row_bytes));
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(which ? p.vc : p.kc) +
+                                                   (unit * p.C + s) * static_cast<size_t>(p.row_bytes));
+            dst[off] = src[off];
+        }
+    }
+}
+
+template <int D, int MODE> cudaError_t launch_attn(const PromptAttnParams &p, int B, cudaStream_t st)
+{
+    const int smem = PromptLayout<D>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(prompt_attn_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int nT = (p.P + kPT - 1) / kPT;
+    const int tiles = MODE == kRowStats ? nT - p.q_lo / kPT : nT;
+    const int heads = MODE == kRowStats ? B * p.Hq : B * p.Hkv;
+    if (tiles <= 0 || heads <= 0) return cudaSuccess;
+    prompt_attn_kernel<D, MODE><<<dim3(tiles, heads), kPThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t prompt_attn_smem(int head_dim) { return head_dim == 64 ? PromptLayout<64>::kBytes : PromptLayout<128>::kBytes; }
+
+cudaError_t launch_prompt_rowstats(const PromptAttnParams &p, int head_dim, int B, cudaStream_t st)
+{
+    return head_dim == 64 ? launch_attn<64, kRowStats>(p, B, st) : launch_attn<128, kRowStats>(p, B, st);
+}
+
+cudaError_t launch_prompt_colsum(const PromptAttnParams &p, int head_dim, int B, cudaStream_t st)
+{
+    return head_dim == 64 ? launch_attn<64, kColSum>(p, B, st) : launch_attn<128, kColSum>(p, B, st);
+}
+
+cudaError_t launch_prompt_select(const PromptSelectParams &p, int units, cudaStream_t st)
+{
+    const size_t smem = static_cast<size_t>(p.P) * 4;
+    cudaError_t e = cudaFuncSetAttribute(prompt_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    prompt_select_kernel<<<units, kSelThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvevict

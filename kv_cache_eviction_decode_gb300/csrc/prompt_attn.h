@@ -1,0 +1,49 @@
+// prompt_attn.h -- host-visible parameters of the prompt-scoring kernels
+// (Q-seeded prefill): causal attention statistics of the prompt on the
+// tcgen05 tensor cores, then the cut to the budget.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvevict {
+
+constexpr int kPromptTile = 128;          // query / key rows per MMA tile (M and N)
+constexpr int kPromptMaxLen = 49152;      // selection keeps one unit's score bits in shared memory
+
+// Opaque 128-byte tensor map (CUtensorMap), 64-byte aligned as a kernel
+// parameter requires.
+struct alignas(64) PromptTmap {
+    uint64_t word[16];
+};
+
+struct PromptAttnParams {
+    PromptTmap tma, tmb;  // A-side rows (the tile a CTA keeps) and B-side rows (the tiles it streams)
+    float *stats;         // [B * Hq][Ps]: per query row, m + log2(l) of its softmax (log2 units)
+    float *score;         // [B * Hkv][P]: per key, the mass it receives, mean over the G query heads
+    int P, Ps, G, Hq, Hkv, q_lo;
+    float scale_log2;     // log2(e) / sqrt(d)
+    uint32_t *err;
+};
+
+struct PromptSelectParams {
+    const float *score;   // [B * Hkv][P]
+    const void *K, *V;    // prompt [B][Hkv][P][d]
+    void *kc, *vc;        // layer cache [B][Hkv][C][d]
+    int32_t *pos;         // layer [B][Hkv][cstride]
+    float *cscore;        // layer [B][Hkv][cstride]
+    int P, C, cstride, row_bytes;
+    int budget, n_sink, n_recent;
+    uint32_t *err;
+};
+
+// Bytes of shared memory the scoring kernels use for head_dim d.
+size_t prompt_attn_smem(int head_dim);
+// Pass 1 (row statistics) and pass 2 (column sums); d in {64, 128}.
+cudaError_t launch_prompt_rowstats(const PromptAttnParams &p, int head_dim, int B, cudaStream_t st);
+cudaError_t launch_prompt_colsum(const PromptAttnParams &p, int head_dim, int B, cudaStream_t st);
+// The cut to the budget and the copy of the kept rows into the cache.
+cudaError_t launch_prompt_select(const PromptSelectParams &p, int units, cudaStream_t st);
+
+}  // namespace kvevict

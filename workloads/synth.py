@@ -145,6 +145,21 @@ def device_prompt(w: Workload, layer: int, device, prompt_len: int | None = None
     return K, V
 
 
+def device_prompt_queries(w: Workload, layer: int, device, prompt_len: int | None = None, gen=None):
+    """Prompt queries for one layer, [B, Hq, P, d] in the workload dtype
+    (seeded N(0, 1), like the decode queries)."""
+    torch = _torch()
+    P = w.prompt_len if prompt_len is None else prompt_len
+    dt = torch.bfloat16 if w.dtype == DTYPE_BF16 else torch.float32
+    if gen is None:
+        gen = torch.Generator(device=device)
+        gen.manual_seed(w.seed * 2000003 + layer)
+    Q = torch.empty((w.batch, w.n_q_heads, P, w.head_dim), dtype=dt, device=device)
+    for b in range(w.batch):
+        Q[b] = torch.randn((w.n_q_heads, P, w.head_dim), generator=gen, device=device).to(dt)
+    return Q
+
+
 def device_window(w: Workload, start_pos: int, n_steps: int, device, gen=None):
     """Decode inputs for n_steps token-steps of all layers.
 
