@@ -172,6 +172,26 @@ int kvevict_prefill_scored_workspace_bytes(kvevict_t h, int prompt_len, size_t *
 int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K, const void *V, int prompt_len,
                            void *workspace, size_t workspace_bytes);
 
+/* kvevict_prefill_scored without caller memory. The pages have no
+ * counterpart: this is for callers that cannot allocate device memory when
+ * they prefill -- a serving framework that reserved the GPU's free memory for
+ * its own pool at start-up, or a latency-bound path that cannot take the
+ * device-wide synchronisation cudaMalloc and cudaFree may cause. It does what
+ * kvevict_prefill_scored does (same arguments, results and errors), but its
+ * scratch is a fixed 16 MiB array inside the library that every GPU loading
+ * the library holds until the process exits; it calls no allocator.
+ *   - Returns CAPACITY (and says so on stderr) when the prompt needs more
+ *     scratch than 16 MiB (kvevict_prefill_scored_workspace_bytes tells how
+ *     much); use kvevict_prefill_scored with a workspace then.
+ *   - The first call on a device, made with that device current, looks up the
+ *     array's address on that device; make that first call before any stream
+ *     capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (other streams, other handles) race and corrupt each other; order them.
+ *     Nothing in it needs to start at zero. */
+int kvevict_prefill_scored_static(kvevict_t h, int layer, const void *Q, const void *K, const void *V,
+                                  int prompt_len);
+
 /* One decode step of `layer` for every sequence (the four steps above).
  *   q:     device, [batch][n_q_heads][head_dim]; query heads g*G .. g*G+G-1
  *          share KV head g.
