@@ -26,6 +26,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -333,6 +335,169 @@ def run_ours(args, w, rank, world, device):
                 ring_stages=st["ring_stages"])
 
 
+# ---------------------------------------------------------------------------
+# Q-seeded prefill (H2O): prompt scoring on the tensor cores, then the cut
+# ---------------------------------------------------------------------------
+
+def prefill_flops(w, P: int) -> int:
+    """Algorithmic FLOPs of one layer's scoring: two passes over the causal
+    triangle of q.k (2 d flops per product) for every query head."""
+    return w.batch * w.n_q_heads * 2 * P * (P + 1) * w.head_dim
+
+
+def measured_bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def oracle_prefill_rate(w, P: int, target_s: float):
+    """Oracle units (one sequence's KV head) scored per second, timed as the
+    oracle stands, one unit per thread on every host core. A unit whose full
+    prompt would not finish within the budget is timed on a shorter prompt and
+    scaled by the FLOP ratio (said in the sample text)."""
+    import concurrent.futures as cf
+    import oracle
+    threads = oracle.online_cores()
+    G, d = w.group, w.head_dim
+    rng = np.random.default_rng(w.seed)
+    # per-unit cost model from the oracle's own loop: G * P^2 / 2 rows-by-keys products of d
+    Pt = P
+    est = G * P * P / 2 * d / 4e8  # about 0.4 G multiply-adds per second per core
+    if est > target_s / 2:
+        Pt = max(256, int(P * (target_s / 2 / est) ** 0.5))
+    def unit(i):
+        q = rng.standard_normal((G, Pt, d)).astype(np.float32)
+        k = rng.standard_normal((Pt, d)).astype(np.float32)
+        v = rng.standard_normal((Pt, d)).astype(np.float32)
+        u = oracle.Unit(oracle.H2O, w.n_sink, w.n_heavy, w.n_recent, w.budget, 0, 0, G, d)
+        u.prefill_scored(q, k, v)
+    t0 = time.perf_counter()
+    done = 0
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while time.perf_counter() - t0 < target_s or done == 0:
+            list(ex.map(unit, range(threads)))
+            done += threads
+    dt = time.perf_counter() - t0
+    rate = done / dt
+    scale = (Pt * (Pt + 1)) / (P * (P + 1))
+    desc = f"{done} units (one sequence x KV head) of prompt {Pt}, {dt:.1f} s"
+    if Pt != P:
+        desc += f"; scaled to prompt {P} by the FLOP ratio {scale:.4g}"
+    return rate * scale, threads, desc
+
+
+def prefill_phase(args, w, rank, world, local):
+    metric = "Q-seeded prefill prompt tokens/s (H2O scoring + cut); tensor TFLOP/s vs bf16 peak"
+    P = w.prompt_len
+    if w.policy != configs.POLICY_H2O or w.dtype != configs.DTYPE_BF16 or P < 1:
+        raise SystemExit("--phase prefill needs an H2O bf16 workload with a prompt")
+    cfg = {"workload": w.name, "phase": "prefill_scored", "policy": "h2o", "batch": w.batch, "q_heads": w.n_q_heads,
+           "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "prompt_len": P, "budget": w.budget,
+           "n_sink": w.n_sink, "n_heavy": w.n_heavy, "n_recent": w.n_recent}
+    flops = prefill_flops(w, P)
+    tokens = w.batch * P  # prompt tokens per call (one layer)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rate, threads, desc = oracle_prefill_rate(w, P, max(2.0, args.cpu_seconds))
+        v = rate * P / w.n_kv_heads
+        print(json.dumps({"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 1,
+                          "steps": 1, "warmup": 0, "ms_per_step": 1000.0 * tokens / v, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": cfg,
+                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                           "sample": desc},
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    from kv_cache_eviction_decode_gb300 import KVEvictCache
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    n_calls = args.warmup + args.steps
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        Q = synth.device_prompt_queries(w, 0, device, P)
+        K, V = synth.device_prompt(w, 0, device, P)
+        # one layer per call: the scored prefill fills an empty layer
+        cache = KVEvictCache.from_workload(w.with_(n_layers=n_calls + (0 if args.no_e2e else 2)), device=device,
+                                           stream=stream)
+        ws = torch.empty(cache.prefill_scored_workspace_bytes(P), dtype=torch.uint8, device=device)
+        for i in range(args.warmup):
+            cache.prefill_scored(i, Q, K, V, workspace=ws)
+        stream.synchronize()
+        barrier(device)
+        torch.cuda.synchronize(device)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(device.index) as clk:
+            ev0.record(stream)
+            for i in range(args.warmup, n_calls):
+                cache.prefill_scored(i, Q, K, V, workspace=ws)
+            ev1.record(stream)
+            ev1.synchronize()
+        torch.cuda.synchronize(device)
+        barrier(device)
+        err = cache.check()
+        if err:
+            raise RuntimeError(f"device error word {err:#x}")
+        dt_ms = reduce_max(ev0.elapsed_time(ev1), device)
+        e2e = None
+        if not args.no_e2e:
+            # through the binding from pinned host buffers: Q/K/V in, the slot table out
+            Qh, Kh, Vh = Q.cpu().pin_memory(), K.cpu().pin_memory(), V.cpu().pin_memory()
+            pos_h = torch.empty((w.batch, w.n_kv_heads, cache.capacity), dtype=torch.int32).pin_memory()
+            Qd, Kd, Vd = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+            barrier(device)
+            torch.cuda.synchronize(device)
+            t0 = time.perf_counter()
+            for j, layer in enumerate((n_calls, n_calls + 1)):
+                Qd.copy_(Qh, non_blocking=True)
+                Kd.copy_(Kh, non_blocking=True)
+                Vd.copy_(Vh, non_blocking=True)
+                cache.prefill_scored(layer, Qd, Kd, Vd, workspace=ws)
+                pos_h.copy_(cache.slot_positions(layer), non_blocking=True)
+                stream.synchronize()
+            e2e_s = reduce_max(time.perf_counter() - t0, device)
+            e2e = {"value": world * tokens * 2 / e2e_s, "unit": "tokens/s",
+                   "h2d_bytes_per_step": (Q.numel() + K.numel() + V.numel()) * Q.element_size(),
+                   "d2h_bytes_per_step": pos_h.numel() * 4, "steps": 2}
+        cache.close()
+    per_call_s = dt_ms / 1e3 / args.steps
+    value = world * tokens / per_call_s
+    peak, peak_kind = measured_bf16_peak()
+    achieved = flops / per_call_s / 1e12
+    out = {
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V with hub and sink keys)",
+        "config": dict(cfg, timing="CUDA events on the launching stream; a step = one layer's scored prefill "
+                                   "(3 launches); Q/K/V of one layer exceed L2"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "algorithmic_flops_per_step": flops,
+                     "exp2_per_step": w.batch * w.n_q_heads * P * (P + 1),
+                     "note": "two tcgen05 passes over the causal triangle of q.k; the exp2 per product also bounds"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, desc = oracle_prefill_rate(w, P, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": rate * P / w.n_kv_heads, "unit": "tokens/s", "cores": threads,
+                               "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -351,6 +516,8 @@ def main():
                     help="override the layer count (small profiling captures only; the line then names it)")
     ap.add_argument("--no-preroll", action="store_true",
                     help="time from the state right after prefill (small profiling captures only)")
+    ap.add_argument("--phase", default="decode", choices=["decode", "prefill"],
+                    help="decode (default): the decode step; prefill: the Q-seeded prefill of one layer (H2O)")
     ap.add_argument("--prompt", type=int, default=-1,
                     help="override the prompt length (small profiling captures only; decode launch shape unchanged "
                          "once the cache is full)")
@@ -372,6 +539,9 @@ def main():
            "n_sink": w.n_sink, "n_heavy": w.n_heavy, "n_recent": w.n_recent, "r": w.r,
            "prompt_len": w.prompt_len, "capacity_slots": w.capacity,
            "l2": "inputs larger than L2 (KV of one layer-step %.2f GB)" % (traffic.steady_layer_step_bytes(w) / 1e9)}
+
+    if args.phase == "prefill":
+        return prefill_phase(args, w, rank, world, local)
 
     if args.impl == "reference":
         # The reference arm is the CPU oracle, timed as it stands on the host

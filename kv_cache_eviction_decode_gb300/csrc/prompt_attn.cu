@@ -18,8 +18,8 @@
 // row of A, so both reductions (over a query row, over a key column of the
 // attention matrix) stay inside a thread.
 //
-// Warps: 0-7 epilogue (two per TMEM lane quadrant, each taking 64 of the 128
-// columns), 8 TMA producer (and TMEM allocation), 9 MMA issuer.
+// Warps: 0-15 epilogue (four per TMEM lane quadrant, each taking 32 of the
+// 128 columns), 16 TMA producer (and TMEM allocation), 17 MMA issuer.
 #include <cfloat>
 #include <cmath>
 
@@ -33,7 +33,8 @@ namespace {
 
 constexpr int kPT = kPromptTile;
 constexpr int kPStages = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kSlices = kEpiWarps / 4;  // column slices per row (warps sharing a lane quadrant)
 constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
 constexpr int kPThreads = (kEpiWarps + 2) * 32;
 constexpr uint32_t kTmemCols = 256;  // two 128-column fp32 accumulators
@@ -47,10 +48,19 @@ template <int D> struct PromptLayout {
     static constexpr int kOffB = kTileBytes;
     static constexpr int kOffBar = kOffB + kPStages * kTileBytes;
     static constexpr int kOffXchg = kOffBar + 256;
-    static constexpr int kBytes = kOffXchg + kPT * 8 + 1024;  // + slack to align the base to 1 KB
+    static constexpr int kBytes = kOffXchg + (kSlices - 1) * kPT * 8 + 1024;  // + slack to align the base to 1 KB
 };
 
 __device__ __forceinline__ void flag_timeout(uint32_t *err) { atomicOr(err, KVEVICT_DEV_WAIT_TIMEOUT); }
+
+// 2^x by the special-function unit (PTX ex2.approx, subnormal results flushed
+// to zero); x = -inf gives 0.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_constant__ PromptAttnParams p)
@@ -159,90 +169,105 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
         }
     } else {
         // ----------------------------------------------------------- epilogue
-        const int quad = warp & 3, half = warp >> 2;
+        const int quad = warp & 3, slice = warp >> 2;
         const int row = quad * 32 + lane;      // TMEM lane = row of the A tile
         const int a_idx = tile * kPT + row;    // pass 1: query i; pass 2: key j
         const uint32_t lane_field = static_cast<uint32_t>(quad * 32) << 16;
+        const int col0 = slice * 32;           // this warp's 32 columns of each tile
+        const float c = p.scale_log2;
         float m = -INFINITY, l = 0.f;          // pass 1: running max and sum (log2 units)
         float acc = 0.f;                       // pass 2: mass received
         bool ok = true;
         for (int n = 0; n < n_b; ++n) {
             const int sb = n & 1;
-            // the TMEM loads below are warp-collective: the whole warp agrees on `ok`
+            // the TMEM load below is warp-collective: the whole warp agrees on `ok`
             if (ok && !__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (n >> 1) & 1))) {
                 ok = false;
                 if (lane == 0) flag_timeout(p.err);
             }
             tc_fence_after();
             if (ok) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_field + static_cast<uint32_t>(sb * kPT + col0), r);
+                tc_wait_ld();
+                if (MODE == kRowStats) {
+                    // keys j = n * 128 + col0 + e; only the diagonal tile is masked
+                    const int j0 = n * kPT + col0;
+                    float v[32];
+                    if (n == tile) {
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_field + static_cast<uint32_t>(sb * kPT + half * 64 + c0), r);
-                    tc_wait_ld();
-                    const int col0 = half * 64 + c0;
-                    if (MODE == kRowStats) {
-                        // keys j = n * 128 + col0 + e; below the diagonal tile all are valid
-                        const int j0 = n * kPT + col0;
-                        const bool diag = n == tile;
-                        float z[32];
-                        float cm = -INFINITY;
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int j = j0 + e;
-                            z[e] = (!diag || (j <= a_idx && j < p.P)) ? __uint_as_float(r[e]) * p.scale_log2
-                                                                      : -INFINITY;
-                            cm = fmaxf(cm, z[e]);
-                        }
-                        if (cm > m) {
-                            l *= exp2f(m - cm);
-                            m = cm;
-                        }
-                        if (m != -INFINITY) {
-                            float s = 0.f;
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) s += exp2f(z[e] - m);
-                            l += s;
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = (j0 + e <= a_idx && j0 + e < p.P) ? __uint_as_float(r[e]) : -INFINITY;
                     } else {
-                        // queries i = qt * 128 + col0 + e of query head g
-                        const int g = n / nq, qt = qt0 + (n - g * nq);
-                        const int i0 = qt * kPT + col0;
-                        const int b = head / p.Hkv, kvh = head - b * p.Hkv;
-                        const float4 *st = reinterpret_cast<const float4 *>(
-                            p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + i0);
-                        const bool full = qt > tile && i0 + 32 <= p.P && i0 >= p.q_lo;
-                        float s = 0.f;
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 ms = __ldg(st + e4);
-                            const float mv[4] = {ms.x, ms.y, ms.z, ms.w};
-#pragma unroll
-                            for (int t = 0; t < 4; ++t) {
-                                const int e = e4 * 4 + t, i = i0 + e;
-                                const float z = __uint_as_float(r[e]) * p.scale_log2 - mv[t];
-                                if (full || (i >= a_idx && i < p.P && i >= p.q_lo)) s += exp2f(z);
-                            }
-                        }
-                        acc += s;
+                        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
                     }
+                    float cm = v[0];
+#pragma unroll
+                    for (int e = 1; e < 32; ++e) cm = fmaxf(cm, v[e]);
+                    cm *= c;  // c > 0: the max of the scaled logits
+                    if (cm > m) {
+                        l *= ex2(m - cm);
+                        m = cm;
+                    }
+                    if (m != -INFINITY) {
+                        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            s0 += ex2(fmaf(v[e], c, -m));
+                            s1 += ex2(fmaf(v[e + 1], c, -m));
+                        }
+                        l += s0 + s1;
+                    }
+                } else {
+                    // queries i = qt * 128 + col0 + e of query head g
+                    const int g = n / nq, qt = qt0 + (n - g * nq);
+                    const int i0 = qt * kPT + col0;
+                    const int b = head / p.Hkv, kvh = head - b * p.Hkv;
+                    const float4 *st = reinterpret_cast<const float4 *>(
+                        p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + i0);
+                    const bool full = qt > tile && i0 + 32 <= p.P && i0 >= p.q_lo;
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 ms = __ldg(st + e4);
+                        const float mv[4] = {ms.x, ms.y, ms.z, ms.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int e = e4 * 4 + t, i = i0 + e;
+                            const float pr = ex2(fmaf(__uint_as_float(r[e]), c, -mv[t]));
+                            const float add = (full || (i >= a_idx && i < p.P && i >= p.q_lo)) ? pr : 0.f;
+                            if (t & 1) s1 += add;
+                            else s0 += add;
+                        }
+                    }
+                    acc += s0 + s1;
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[sb]);
         }
-        // the two column halves of each row meet: warps 4-7 hand over to 0-3
-        if (half == 1) xchg[row] = MODE == kRowStats ? make_float2(m, l) : make_float2(acc, 0.f);
+        // the column slices of each row meet: slices 1.. hand over to slice 0
+        if (slice > 0) xchg[(slice - 1) * kPT + row] = MODE == kRowStats ? make_float2(m, l) : make_float2(acc, 0.f);
         named_bar_sync(1, kEpiWarps * 32);
-        if (half == 0 && ok) {
-            const float2 o = xchg[row];
+        if (slice == 0 && ok) {
             if (MODE == kRowStats) {
-                const float mm = fmaxf(m, o.x);
-                const float ll = (m == -INFINITY ? 0.f : l * exp2f(m - mm)) + (o.x == -INFINITY ? 0.f : o.y * exp2f(o.x - mm));
+                float mm = m;
+#pragma unroll
+                for (int k = 0; k < kSlices - 1; ++k) mm = fmaxf(mm, xchg[k * kPT + row].x);
+                float ll = m == -INFINITY ? 0.f : l * ex2(m - mm);
+#pragma unroll
+                for (int k = 0; k < kSlices - 1; ++k) {
+                    const float2 o = xchg[k * kPT + row];
+                    if (o.x != -INFINITY) ll += o.y * ex2(o.x - mm);
+                }
                 if (a_idx < p.P) p.stats[static_cast<size_t>(head) * p.Ps + a_idx] = mm + log2f(ll);
             } else {
-                if (a_idx < p.P) p.score[static_cast<size_t>(head) * p.P + a_idx] = (acc + o.x) * (1.f / p.G);
+                float tot = acc;
+#pragma unroll
+                for (int k = 0; k < kSlices - 1; ++k) tot += xchg[k * kPT + row].x;
+                if (a_idx < p.P) p.score[static_cast<size_t>(head) * p.P + a_idx] = tot * (1.f / p.G);
             }
         }
     }
