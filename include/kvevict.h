@@ -159,7 +159,7 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
  *   K, V: device, [batch][n_kv_heads][prompt_len][head_dim] bf16;
  *   workspace: device, 256-byte aligned, at least
  *         kvevict_prefill_scored_workspace_bytes() bytes, owned by the caller.
- *         Layout: per query row the log2 of its softmax normaliser, fp32
+ *         Layout: per query row minus the log2 of its softmax normaliser, fp32
  *         [batch * n_q_heads][Ps] with Ps = prompt_len rounded up to 128; then,
  *         at the next 256-byte boundary, every prompt token's score before the
  *         cut, fp32 [batch][n_kv_heads][prompt_len]. Both are valid once the

@@ -4,7 +4,8 @@
 // receives is its score; remove the token whose removal keeps the highest
 // total). With z_gij = q_gi . k_j / sqrt(d) over j <= i:
 //   pass 1  per query row i of head g: ms_gi = m_gi + log2(l_gi), the log2 of
-//           its softmax normaliser (m the row max, l the row sum, log2 units);
+//           its softmax normaliser (m the row max, l the row sum, log2 units),
+//           stored negated;
 //   pass 2  per key j: score_j = (1/G) sum_g sum_{i >= j} 2^(z_gij - ms_gi);
 //   cut     keep the n_sink first and n_recent last positions and, of the
 //           rest, all but the P - K with the smallest (score, position).
@@ -60,6 +61,27 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Two fp32 lanes per instruction (Blackwell's packed f32x2 FMA and add).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
 template <int D, int MODE>
@@ -211,13 +233,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                         m = cm;
                     }
                     if (m != -INFINITY) {
-                        float s0 = 0.f, s1 = 0.f;
+                        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
+                        float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            s0 += ex2(fmaf(v[e], c, -m));
-                            s1 += ex2(fmaf(v[e + 1], c, -m));
+                            const float2 z = ffma2(make_float2(v[e], v[e + 1]), c2, nm2);
+                            s2 = fadd2(s2, make_float2(ex2(z.x), ex2(z.y)));
                         }
-                        l += s0 + s1;
+                        l += s2.x + s2.y;
                     }
                 } else {
                     // queries i = qt * 128 + col0 + e of query head g
@@ -227,21 +250,36 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                     const float4 *st = reinterpret_cast<const float4 *>(
                         p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + i0);
                     const bool full = qt > tile && i0 + 32 <= p.P && i0 >= p.q_lo;
-                    float s0 = 0.f, s1 = 0.f;
+                    const float2 c2 = make_float2(c, c);
+                    float2 s2 = make_float2(0.f, 0.f);
+                    if (full) {  // every query of these 32 columns attends this key
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 ms = __ldg(st + e4);
-                        const float mv[4] = {ms.x, ms.y, ms.z, ms.w};
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 nms = __ldg(st + e4);  // minus the log2 normalisers
+                            const int e = e4 * 4;
+                            const float2 za = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2,
+                                                    make_float2(nms.x, nms.y));
+                            const float2 zb = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])),
+                                                    c2, make_float2(nms.z, nms.w));
+                            s2 = fadd2(s2, make_float2(ex2(za.x), ex2(za.y)));
+                            s2 = fadd2(s2, make_float2(ex2(zb.x), ex2(zb.y)));
+                        }
+                    } else {
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const int e = e4 * 4 + t, i = i0 + e;
-                            const float pr = ex2(fmaf(__uint_as_float(r[e]), c, -mv[t]));
-                            const float add = (full || (i >= a_idx && i < p.P && i >= p.q_lo)) ? pr : 0.f;
-                            if (t & 1) s1 += add;
-                            else s0 += add;
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 nms = __ldg(st + e4);
+                            const float mv[4] = {nms.x, nms.y, nms.z, nms.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int e = e4 * 4 + t, i = i0 + e;
+                                const float pr = ex2(fmaf(__uint_as_float(r[e]), c, mv[t]));
+                                const float add = (i >= a_idx && i < p.P && i >= p.q_lo) ? pr : 0.f;
+                                if (t & 1) s2.y += add;
+                                else s2.x += add;
+                            }
                         }
                     }
-                    acc += s0 + s1;
+                    acc += s2.x + s2.y;
                 }
             }
             tc_fence_before();
@@ -262,7 +300,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                     const float2 o = xchg[k * kPT + row];
                     if (o.x != -INFINITY) ll += o.y * ex2(o.x - mm);
                 }
-                if (a_idx < p.P) p.stats[static_cast<size_t>(head) * p.Ps + a_idx] = mm + log2f(ll);
+                if (a_idx < p.P) p.stats[static_cast<size_t>(head) * p.Ps + a_idx] = -(mm + log2f(ll));
             } else {
                 float tot = acc;
 #pragma unroll

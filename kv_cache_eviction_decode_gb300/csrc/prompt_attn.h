@@ -20,7 +20,7 @@ struct alignas(64) PromptTmap {
 
 struct PromptAttnParams {
     PromptTmap tma, tmb;  // A-side rows (the tile a CTA keeps) and B-side rows (the tiles it streams)
-    float *stats;         // [B * Hq][Ps]: per query row, m + log2(l) of its softmax (log2 units)
+    float *stats;         // [B * Hq][Ps]: per query row, -(m + log2(l)) of its softmax (log2 units)
     float *score;         // [B * Hkv][P]: per key, the mass it receives, mean over the G query heads
     int P, Ps, G, Hq, Hkv, q_lo;
     float scale_log2;     // log2(e) / sqrt(d)
