@@ -74,6 +74,8 @@ def lib():
             L.orc_prefill.restype = I
             L.orc_prefill_scored.argtypes = [P, P, P, P, I, P]
             L.orc_prefill_scored.restype = I
+            L.orc_prefill_snapkv.argtypes = [P, P, P, P, I, I, I, P]
+            L.orc_prefill_snapkv.restype = I
             L.orc_prompt_tail_scores.argtypes = [P, P, I, I, I, I, P]
             L.orc_prompt_tail_scores.restype = I
             L.orc_step.argtypes = [P, P, P, P, P]
@@ -139,6 +141,19 @@ class Unit:
         if rc:
             raise RuntimeError(f"oracle prefill_scored failed: {rc}")
         return scores
+
+    def prefill_snapkv(self, q_obs, k, v, topk: int) -> np.ndarray:
+        """SnapKV selection on an empty H2O unit: q_obs [G][w][d] (the last w
+        prompt tokens' queries), k/v [P][d]. Returns the votes [G][P]."""
+        q_obs, k, v = _f32(q_obs), _f32(k), _f32(v)
+        P, w = k.shape[0], q_obs.shape[1]
+        if q_obs.shape != (self.G, w, self.d) or v.shape != k.shape:
+            raise ValueError("oracle prefill_snapkv: q_obs must be [G][w][d], k and v [P][d]")
+        votes = np.empty((self.G, P), dtype=np.float64)
+        rc = self._L.orc_prefill_snapkv(self.h, _ptr(q_obs), _ptr(k), _ptr(v), P, w, topk, _ptr(votes))
+        if rc:
+            raise RuntimeError(f"oracle prefill_snapkv failed: {rc}")
+        return votes
 
     def attend(self, q, k_new, v_new) -> np.ndarray:
         q, k, v = _f32(q), _f32(k_new), _f32(v_new)

@@ -569,6 +569,101 @@ int orc_prompt_tail_scores(const float *q, const float *k, int G, int P, int d, 
     return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* SnapKV prefill selection (H2O handle).                                    */
+/* ------------------------------------------------------------------------ */
+
+/* "Attention Sinks 与 KV Cache 淘汰策略" section 4.3 (SnapKV): after the prompt,
+ * the last w prompt tokens (the observation window) vote for the prefix.
+ *   votes_gj = sum over window queries i = P-w .. P-1 of head g of
+ *              softmax_j(q_gi . k_j / sqrt(d)) over j <= i     (sum pooling)
+ *   pooled_gj = max of votes_gj' over |j' - j| <= 3 within the prefix
+ *              [0, P-w)                                          (max pooling, 7)
+ *   each head g keeps its `topk` prefix positions with the largest pooled
+ *   vote (ties: the newer position), the window is kept, and a KV head keeps
+ *   the union over its G query heads.
+ * The kept tokens fill slots 0, 1, ... in ascending position order; each
+ * starts with score (1/G) sum_g votes_gj, the attention it received from the
+ * window's queries. q_obs is [G][w][d] (the window's queries), k and v are
+ * [P][d]; votes_out (optional) receives votes [G][P]. Only on an empty H2O
+ * unit; ECAPACITY if the kept set does not fit the unit. */
+int orc_prefill_snapkv(orc_unit *u, const float *q_obs, const float *k, const float *v, int P, int w, int topk,
+                       double *votes_out)
+{
+    if (u->policy != ORC_H2O || u->prompt_len != 0 || u->t != 0 || u->have_new) return ORC_ESTATE;
+    if (P < 1 || w < 1 || w >= P || topk < 0) return ORC_EINVAL;
+    const int d = u->d, G = u->G, n_pre = P - w;
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    double *votes = (double *)calloc((size_t)G * P, sizeof(double));
+    double *z = (double *)malloc(sizeof(double) * (size_t)P);
+    double *pooled = (double *)malloc(sizeof(double) * (size_t)(n_pre > 0 ? n_pre : 1));
+    char *kept = (char *)calloc((size_t)P, 1);
+    char *taken = (char *)malloc((size_t)(n_pre > 0 ? n_pre : 1));
+    if (!votes || !z || !pooled || !kept || !taken) {
+        free(votes); free(z); free(pooled); free(kept); free(taken);
+        return ORC_ECAPACITY;
+    }
+    for (int g = 0; g < G; ++g) {
+        double *vg = votes + (size_t)g * P;
+        for (int t = 0; t < w; ++t) {
+            const int i = n_pre + t;
+            const float *qi = q_obs + ((size_t)g * w + t) * d;
+            double m = -INFINITY;
+            for (int j = 0; j <= i; ++j) {
+                double dot = 0.0;
+                for (int e = 0; e < d; ++e) dot += (double)qi[e] * (double)k[(size_t)j * d + e];
+                z[j] = dot * inv_sqrt_d;
+                if (z[j] > m) m = z[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j <= i; ++j) l += exp(z[j] - m);
+            for (int j = 0; j <= i; ++j) vg[j] += exp(z[j] - m) / l;
+        }
+        /* max pooling over the prefix, then this head's top-k, one at a time */
+        for (int j = 0; j < n_pre; ++j) {
+            double mx = -INFINITY;
+            for (int jj = j - 3; jj <= j + 3; ++jj)
+                if (jj >= 0 && jj < n_pre && vg[jj] > mx) mx = vg[jj];
+            pooled[j] = mx;
+            taken[j] = 0;
+        }
+        const int want = topk < n_pre ? topk : n_pre;
+        for (int c = 0; c < want; ++c) {
+            int best = -1;
+            for (int j = 0; j < n_pre; ++j) {
+                if (taken[j]) continue;
+                if (best < 0 || pooled[j] > pooled[best] || (pooled[j] == pooled[best] && j > best)) best = j;
+            }
+            taken[best] = 1;
+            kept[best] = 1;
+        }
+    }
+    for (int j = n_pre; j < P; ++j) kept[j] = 1;
+    if (votes_out) memcpy(votes_out, votes, sizeof(double) * (size_t)G * P);
+
+    int n_kept = 0;
+    for (int j = 0; j < P; ++j) n_kept += kept[j];
+    int rc = ORC_OK;
+    if (n_kept > u->cap) {
+        rc = ORC_ECAPACITY;
+    } else {
+        int slot = 0;
+        for (int j = 0; j < P; ++j) {
+            if (!kept[j]) continue;
+            double sc = 0.0;
+            for (int g = 0; g < G; ++g) sc += votes[(size_t)g * P + j];
+            u->pos[slot] = j;
+            memcpy(u->k + (size_t)slot * d, k + (size_t)j * d, sizeof(float) * (size_t)d);
+            memcpy(u->v + (size_t)slot * d, v + (size_t)j * d, sizeof(float) * (size_t)d);
+            u->score[slot] = sc / (double)G;
+            slot++;
+        }
+        u->prompt_len = P;
+    }
+    free(votes); free(z); free(pooled); free(kept); free(taken);
+    return rc;
+}
+
 /* One full decode step with the oracle's own decision. Returns the slot taken. */
 int orc_step(orc_unit *u, const float *q, const float *k_new, const float *v_new, double *out)
 {
