@@ -172,6 +172,37 @@ int kvevict_prefill_scored_workspace_bytes(kvevict_t h, int prompt_len, size_t *
 int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K, const void *V, int prompt_len,
                            void *workspace, size_t workspace_bytes);
 
+/* SnapKV prefill of an empty H2O layer ("Attention Sinks 与 KV Cache 淘汰策略"
+ * section 4.3): the last `window` prompt tokens' queries vote for the earlier
+ * positions, and only what they pick is kept.
+ *   votes_gj  = sum over the window's queries i of query head g of
+ *               softmax_j(q_gi . k_j / sqrt(d)) over j <= i;
+ *   pooled_gj = max of votes_gj' over |j' - j| <= 3 within the prefix
+ *               [0, prompt_len - window);
+ *   each query head keeps its k_per_head prefix positions with the largest
+ *   pooled vote (ties: the newer position); a KV head keeps the union over
+ *   its G query heads plus the window.
+ * The kept tokens fill slots 0, 1, ... in ascending position order, each with
+ * the score (1/G) sum_g votes_gj (the attention it received from the window);
+ * the other slots stay empty. The next decode steps of the layer put the new
+ * token into each unit's lowest empty slot while it has one and evict by
+ * score after that.
+ *   Q_obs: device, [batch][n_q_heads][window][head_dim] bf16, the queries of
+ *          prompt positions prompt_len - window .. prompt_len - 1;
+ *   K, V:  device, [batch][n_kv_heads][prompt_len][head_dim] bf16;
+ *   workspace: device, 256-byte aligned, at least
+ *          kvevict_prefill_snapkv_workspace_bytes() bytes, owned by the caller.
+ *          Layout: the window rows' normalisers, fp32 [batch * n_q_heads][Ps]
+ *          (Ps: the window's tiles of 128 rows); then, at the next 256-byte
+ *          boundary, the votes, fp32 [batch][n_q_heads][prompt_len].
+ * INVALID_ARG unless the policy is H2O and the dtype bf16, for 1 <= window <
+ * prompt_len <= 49152 not holding, for G * k_per_head + window above the
+ * capacity (the union must fit), for null or misaligned pointers or a short
+ * workspace; STATE if the layer already holds tokens or has decoded. */
+int kvevict_prefill_snapkv_workspace_bytes(kvevict_t h, int prompt_len, int window, size_t *bytes);
+int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void *K, const void *V, int prompt_len,
+                           int window, int k_per_head, void *workspace, size_t workspace_bytes);
+
 /* kvevict_prefill_scored without caller memory. The pages have no
  * counterpart: this is for callers that cannot allocate device memory when
  * they prefill -- a serving framework that reserved the GPU's free memory for

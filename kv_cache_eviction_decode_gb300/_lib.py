@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
             L.kvevict_prefill_scored_workspace_bytes.argtypes = [P, I, ctypes.POINTER(SZ)]
             L.kvevict_prefill_scored.argtypes = [P, I, P, P, P, I, P, SZ]
             L.kvevict_prefill_scored_static.argtypes = [P, I, P, P, P, I]
+            L.kvevict_prefill_snapkv_workspace_bytes.argtypes = [P, I, I, ctypes.POINTER(SZ)]
+            L.kvevict_prefill_snapkv.argtypes = [P, I, P, P, P, I, I, I, P, SZ]
             L.kvevict_decode_step.argtypes = [P, I, P, P, P, P]
             L.kvevict_decode_step_host.argtypes = [P, I, P, P, P, P]
             L.kvevict_slot_positions.argtypes = [P, I, P, I]
@@ -75,7 +77,8 @@ def lib() -> ctypes.CDLL:
             L.kvevict_destroy.argtypes = [P]
             L.kvevict_destroy.restype = None
             for n in ("kvevict_state_bytes", "kvevict_create", "kvevict_prefill", "kvevict_prefill_scored_workspace_bytes",
-                      "kvevict_prefill_scored", "kvevict_prefill_scored_static", "kvevict_decode_step",
+                      "kvevict_prefill_scored", "kvevict_prefill_scored_static",
+                      "kvevict_prefill_snapkv_workspace_bytes", "kvevict_prefill_snapkv", "kvevict_decode_step",
                       "kvevict_decode_step_host", "kvevict_slot_positions", "kvevict_scores", "kvevict_set_trace",
                       "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",

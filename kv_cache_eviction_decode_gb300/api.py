@@ -108,6 +108,36 @@ class KVEvictCache:
         raw = workspace.view(torch.uint8).reshape(-1)[off:off + self.B * self.Hkv * n * 4]
         return raw.view(torch.float32).view(self.B, self.Hkv, n)
 
+    def prefill_snapkv_workspace_bytes(self, prompt_len: int, window: int) -> int:
+        n = ctypes.c_size_t()
+        check(self._L.kvevict_prefill_snapkv_workspace_bytes(self.h, prompt_len, window, ctypes.byref(n)),
+              "kvevict_prefill_snapkv_workspace_bytes")
+        return n.value
+
+    def prefill_snapkv(self, layer: int, Q_obs: torch.Tensor, K: torch.Tensor, V: torch.Tensor, k_per_head: int,
+                       workspace: torch.Tensor | None = None) -> torch.Tensor:
+        """SnapKV prefill of an empty H2O layer: Q_obs [B][Hq][w][d] (the last w
+        prompt tokens' queries), K/V [B][Hkv][P][d]. Returns the votes
+        [B][Hq][P] fp32: a view of the workspace, valid once the stream has
+        passed the call."""
+        n, w = K.shape[2], Q_obs.shape[2]
+        self._dev(Q_obs, (self.B, self.Hq, w, self.D), "Q_obs")
+        self._dev(K, (self.B, self.Hkv, n, self.D), "K")
+        self._dev(V, (self.B, self.Hkv, n, self.D), "V")
+        need = self.prefill_snapkv_workspace_bytes(n, w)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        if workspace.device != self.device or workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace: need {need} bytes on {self.device}")
+        check(self._L.kvevict_prefill_snapkv(self.h, layer, _ptr(Q_obs), _ptr(K), _ptr(V), n, w, k_per_head,
+                                             _ptr(workspace), workspace.numel() * workspace.element_size()),
+              "kvevict_prefill_snapkv")
+        qs0 = (n - w) // 128 * 128
+        ps = (n - qs0 + 127) // 128 * 128
+        off = (self.B * self.Hq * ps * 4 + 255) // 256 * 256
+        raw = workspace.view(torch.uint8).reshape(-1)[off:off + self.B * self.Hq * n * 4]
+        return raw.view(torch.float32).view(self.B, self.Hq, n)
+
     def decode_step(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                     out: torch.Tensor | None = None) -> torch.Tensor:
         self._dev(q, (self.B, self.Hq, self.D), "q")

@@ -119,6 +119,7 @@ struct LayerState {
     int fl_idx = 0;      // next free-list entry (Random after a cut)
     int32_t *trace = nullptr;
     int trace_len = 0, trace_t = 0;
+    int fill_left = 0;   // H2O after a SnapKV prefill: steps left in which a unit may still have empty slots
 };
 
 }  // namespace
@@ -339,7 +340,10 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
         break;
     case KVEVICT_H2O:
         P.n_active = ls.count;
-        if (ls.count < L.C) {
+        if (ls.fill_left > 0) {  // after a SnapKV prefill: per-unit empty slots
+            P.mode = kH2OFill;
+            holes = true;
+        } else if (ls.count < L.C) {
             P.mode = kInsertAt;
             P.dest_slot = ls.count;
         } else {
@@ -413,6 +417,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     case KVEVICT_SINK_WINDOW:
     case KVEVICT_H2O:
         ls.count = std::min(L.C, ls.count + 1);
+        if (ls.fill_left > 0) ls.fill_left--;
         break;
     default:
         ls.n_gen++;
@@ -625,6 +630,9 @@ int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K,
     ap.Hq = c.n_q_heads;
     ap.Hkv = c.n_kv_heads;
     ap.q_lo = 0;
+    ap.q_stride = P;
+    ap.q_first = 0;
+    ap.per_head = 0;
     ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
     ap.err = at<uint32_t>(h, L.off_err);
     // pass 1: A = query tiles, B = key tiles; pass 2: A = key tiles, B = query tiles
@@ -659,6 +667,123 @@ int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K,
     h->last_layer = layer;
     ls.prompt_len = P;
     ls.count = std::min(L.C, P);
+    h->stats.prefill_tokens += P;
+    return KVEVICT_OK;
+}
+
+namespace {
+
+// Workspace of the SnapKV prefill: the normalisers of the window's query rows
+// ([B * Hq][Ps], from the window's first tile on), then the votes of every
+// query head on every prompt key ([B * Hq][P]).
+struct SnapWorkspace {
+    size_t stats_off = 0, votes_off = 0, bytes = 0;
+    int Ps = 0, qs0 = 0;
+};
+
+SnapWorkspace snap_workspace(const kvevict_config &c, int P, int window)
+{
+    SnapWorkspace w;
+    w.qs0 = (P - window) / kPromptTile * kPromptTile;
+    w.Ps = (P - w.qs0 + kPromptTile - 1) / kPromptTile * kPromptTile;
+    w.stats_off = 0;
+    w.votes_off = align_up(static_cast<size_t>(c.batch) * c.n_q_heads * w.Ps * 4);
+    w.bytes = w.votes_off + align_up(static_cast<size_t>(c.batch) * c.n_q_heads * P * 4);
+    return w;
+}
+
+}  // namespace
+
+int kvevict_prefill_snapkv_workspace_bytes(kvevict_t h, int prompt_len, int window, size_t *bytes)
+{
+    if (!h || !bytes || prompt_len < 2 || prompt_len > kPromptMaxLen || window < 1 || window >= prompt_len)
+        return KVEVICT_ERR_INVALID_ARG;
+    *bytes = snap_workspace(h->cfg, prompt_len, window).bytes;
+    return KVEVICT_OK;
+}
+
+int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void *K, const void *V, int prompt_len,
+                           int window, int k_per_head, void *workspace, size_t workspace_bytes)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    const kvevict_config &c = h->cfg;
+    const Layout &L = h->L;
+    const int P = prompt_len;
+    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16) return KVEVICT_ERR_INVALID_ARG;
+    if (P < 2 || P > kPromptMaxLen || window < 1 || window >= P || k_per_head < 0) return KVEVICT_ERR_INVALID_ARG;
+    // the union of the G heads' top-k lists plus the window must fit the unit
+    if (static_cast<long long>(L.G) * k_per_head + window > L.C) return KVEVICT_ERR_INVALID_ARG;
+    if (!Q_obs || !K || !V || !workspace || !aligned16(Q_obs) || !aligned16(K) || !aligned16(V) ||
+        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return KVEVICT_ERR_INVALID_ARG;
+    const SnapWorkspace ws = snap_workspace(c, P, window);
+    if (workspace_bytes < ws.bytes) return KVEVICT_ERR_INVALID_ARG;
+    if (static_cast<long long>(c.batch) * c.n_q_heads > 65535 ||
+        static_cast<long long>(c.batch) * c.n_kv_heads * P >= (1LL << 31))
+        return KVEVICT_ERR_INVALID_ARG;
+    LayerState &ls = h->layers[layer];
+    if (ls.prompt_len != 0 || ls.t != 0) return KVEVICT_ERR_STATE;
+
+    uint8_t *wsb = static_cast<uint8_t *>(workspace);
+    CUtensorMap tq, tk;
+    int rc = make_tensor_map(&tq, Q_obs, static_cast<uint64_t>(c.batch) * c.n_q_heads * window, c.head_dim,
+                             kPromptTile);
+    if (rc == KVEVICT_OK)
+        rc = make_tensor_map(&tk, K, static_cast<uint64_t>(c.batch) * c.n_kv_heads * P, c.head_dim, kPromptTile);
+    if (rc) return rc;
+    PromptAttnParams ap{};
+    ap.stats = reinterpret_cast<float *>(wsb + ws.stats_off);
+    ap.score = reinterpret_cast<float *>(wsb + ws.votes_off);
+    ap.P = P;
+    ap.Ps = ws.Ps;
+    ap.G = L.G;
+    ap.Hq = c.n_q_heads;
+    ap.Hkv = c.n_kv_heads;
+    ap.q_lo = P - window;
+    ap.q_stride = window;
+    ap.q_first = P - window;
+    ap.per_head = 1;
+    ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
+    ap.err = at<uint32_t>(h, L.off_err);
+    std::memcpy(&ap.tma, &tq, sizeof tq);
+    std::memcpy(&ap.tmb, &tk, sizeof tk);
+    cudaError_t e = launch_prompt_rowstats(ap, c.head_dim, c.batch, h->stream);
+    if (e == cudaSuccess) {
+        std::memcpy(&ap.tma, &tk, sizeof tk);
+        std::memcpy(&ap.tmb, &tq, sizeof tq);
+        e = launch_prompt_colsum(ap, c.head_dim, c.batch, h->stream);
+    }
+    if (e == cudaSuccess) {
+        SnapSelectParams sp{};
+        sp.votes = ap.score;
+        sp.K = K;
+        sp.V = V;
+        sp.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
+        sp.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
+        sp.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
+        sp.cscore = at<float>(h, L.off_score) + layer * L.layer_pslots;
+        sp.P = P;
+        sp.C = L.C;
+        sp.cstride = L.Cs;
+        sp.row_bytes = c.head_dim * L.elem;
+        sp.G = L.G;
+        sp.Hq = c.n_q_heads;
+        sp.Hkv = c.n_kv_heads;
+        sp.window = window;
+        sp.topk = k_per_head;
+        sp.err = ap.err;
+        e = launch_snapkv_select(sp, static_cast<int>(L.units), h->stream);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    h->last_layer = layer;
+    ls.prompt_len = P;
+    // Every unit keeps between min(k, P - window) + window and the capacity
+    // tokens, in slots from 0 on; the rest of its slots are empty. Decode
+    // steps fill each unit's lowest empty slot until every unit is surely
+    // full, then evict as usual.
+    ls.count = L.C;
+    ls.fill_left = L.C - (std::min(k_per_head, P - window) + window);
     h->stats.prefill_tokens += P;
     return KVEVICT_OK;
 }

@@ -54,6 +54,7 @@
 #pragma once
 
 #include <cfloat>
+#include <climits>
 #include <cmath>
 
 #include "device_common.cuh"
@@ -74,7 +75,9 @@ constexpr int kMinStages = 4;
 enum InsertMode : int {
     kInsertAt = 0,     // the host gives the slot (empty slot, or the ring slot)
     kH2OEvict = 1,     // cache full: evict the lowest-score eligible token
-    kFromFreeList = 2  // Random after a cut: next entry of the unit's free list
+    kFromFreeList = 2, // Random after a cut: next entry of the unit's free list
+    kH2OFill = 3       // H2O with per-unit empty slots (after a SnapKV prefill): the unit's
+                       // lowest empty slot if it has one, else evict as kH2OEvict
 };
 
 // Opaque 128-byte tensor map (CUtensorMap), 64-byte aligned as a kernel
@@ -146,9 +149,11 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
         alignas(16) float xo[2][G * D];
         uint64_t xkey[2][kMaxSplit];
         int32_t xslot[2][kMaxSplit];
+        int32_t xempty[2][kMaxSplit];  // fill mode: every CTA's lowest empty slot
         float xanew[2];
         uint64_t wkey[kWarps];
         int32_t wslot[kWarps];
+        int32_t wempty[kWarps];
     };
 
     // zcap = slots per CTA rounded to whole tiles, padded so that the head
@@ -218,6 +223,13 @@ __device__ __forceinline__ void warp_argmin(uint64_t &key, int32_t &slot)
             slot = os;
         }
     }
+}
+
+__device__ __forceinline__ int32_t warp_min_s32(int32_t v)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
 }
 
 // Two consecutive elements, moved as one naturally aligned access.
@@ -813,7 +825,9 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             }
         };
         constexpr int kPairs = G * D / 2;
-        const bool evict = P.mode == kH2OEvict;
+        const bool fill = P.mode == kH2OFill;
+        const bool evict = P.mode == kH2OEvict || fill;  // a victim is chosen (fill: unless a slot is empty)
+        constexpr uint64_t kEmptyKey = 0x00000000FFFFFFFFull;  // trace of a fill: position -1, score 0
         int dest = -1;             // slot that receives the new token
         bool writer = false;       // this CTA writes it
         uint64_t win_key = ~0ull;  // H2O eviction: (score bits, position) of the evicted token
@@ -846,7 +860,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     fself[g] = invl[g] * (1.0f / G);
                 }
                 uint64_t best = ~0ull;
-                int32_t bslot = -1;
+                int32_t bslot = -1, emin = INT_MAX;
                 for (int j = tid; j < W.n_mine; j += kThreads) {
                     float a = 0.f;
 #pragma unroll
@@ -855,6 +869,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     P.score[unit * CS + j] = sc;
                     if (evict) {
                         const int ps = apos[j];
+                        if (fill && ps < 0 && j < emin) emin = j;
                         if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
                             const uint64_t key =
                                 (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
@@ -873,9 +888,11 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 }
                 if (evict) {
                     warp_argmin(best, bslot);
+                    if (fill) emin = warp_min_s32(emin);
                     if (lane == 0) {
                         M.wkey[warp] = best;
                         M.wslot[warp] = bslot;
+                        M.wempty[warp] = emin;
                     }
                 }
                 __syncthreads();  // (B) candidates visible; every read of this unit's aux data is done
@@ -884,9 +901,15 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     uint64_t k = lane < kWarps ? M.wkey[lane] : ~0ull;
                     int32_t sl = lane < kWarps ? M.wslot[lane] : -1;
                     warp_argmin(k, sl);
-                    win_key = k;
-                    dest = sl;
-                    if (sl < 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                    const int32_t em = fill ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
+                    if (em != INT_MAX) {  // an empty slot: no eviction
+                        win_key = kEmptyKey;
+                        dest = em;
+                    } else {
+                        win_key = k;
+                        dest = sl;
+                        if (sl < 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                    }
                 }
             }
             // the next unit's positions/scores may come in
@@ -952,7 +975,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
 #pragma unroll
                 for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
                 uint64_t best = ~0ull;
-                int32_t bslot = -1;
+                int32_t bslot = -1, emin = INT_MAX;
                 for (int j = tid; j < W.n_mine; j += kThreads) {
                     float a = 0.f;
 #pragma unroll
@@ -961,6 +984,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     P.score[unit * CS + W.s_lo + j] = sc;
                     if (evict) {
                         const int ps = apos[j];
+                        if (fill && ps < 0 && W.s_lo + j < emin) emin = W.s_lo + j;
                         if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
                             const uint64_t key =
                                 (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
@@ -979,20 +1003,25 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 }
                 if (evict) {
                     warp_argmin(best, bslot);
+                    if (fill) emin = warp_min_s32(emin);
                     if (lane == 0) {
                         M.wkey[warp] = best;
                         M.wslot[warp] = bslot;
+                        M.wempty[warp] = emin;
                     }
                 }
                 __syncthreads();  // candidates visible; every read of this unit's aux data is done
                 if (evict && warp == 0) {
-                    // this CTA's candidate to every CTA; rank 0's new-token score too
+                    // this CTA's candidate (and, filling, its lowest empty slot) to every
+                    // CTA; rank 0's new-token score too
                     uint64_t k = lane < kWarps ? M.wkey[lane] : ~0ull;
                     int32_t sl = lane < kWarps ? M.wslot[lane] : -1;
                     warp_argmin(k, sl);
+                    const int32_t em = fill ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
                     if (lane < S) {
                         st_peer_u64(peer_addr(&M.xkey[b][rank], lane), k);
                         st_peer_s32(peer_addr(&M.xslot[b][rank], lane), sl);
+                        st_peer_s32(peer_addr(&M.xempty[b][rank], lane), em);
                     }
                     if (rank == 0 && lane == 0)
                         for (int c = 0; c < S; ++c) st_peer_f32(peer_addr(&M.xanew[b], c), anew);
@@ -1007,9 +1036,15 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 uint64_t k = lane < S ? M.xkey[b][lane] : ~0ull;
                 int32_t sl = lane < S ? M.xslot[b][lane] : -1;
                 warp_argmin(k, sl);
-                win_key = k;
-                dest = sl;
-                if (sl < 0 && rank == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                const int32_t em = fill ? warp_min_s32(lane < S ? M.xempty[b][lane] : INT_MAX) : INT_MAX;
+                if (em != INT_MAX) {  // an empty slot: no eviction
+                    win_key = kEmptyKey;
+                    dest = em;
+                } else {
+                    win_key = k;
+                    dest = sl;
+                    if (sl < 0 && rank == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                }
                 writer = dest >= W.s_lo && dest < W.s_hi;  // the CTA that attended the victim
                 if (writer && has_score) anew = M.xanew[b];
             } else {

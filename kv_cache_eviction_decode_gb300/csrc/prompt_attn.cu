@@ -49,7 +49,8 @@ template <int D> struct PromptLayout {
     static constexpr int kOffB = kTileBytes;
     static constexpr int kOffBar = kOffB + kPStages * kTileBytes;
     static constexpr int kOffXchg = kOffBar + 256;
-    static constexpr int kBytes = kOffXchg + (kSlices - 1) * kPT * 8 + 1024;  // + slack to align the base to 1 KB
+    static constexpr int kOffPart = kOffXchg + (kSlices - 1) * kPT * 8;  // per-head partials [8][kSlices][128]
+    static constexpr int kBytes = kOffPart + 8 * kSlices * kPT * 4 + 1024;  // + slack to align the base to 1 KB
 };
 
 __device__ __forceinline__ void flag_timeout(uint32_t *err) { atomicOr(err, KVEVICT_DEV_WAIT_TIMEOUT); }
@@ -98,10 +99,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
     uint64_t *s_empty = s_full + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(s_empty + 2);
     float2 *xchg = reinterpret_cast<float2 *>(sm + L::kOffXchg);
+    float *hpart = reinterpret_cast<float *>(sm + L::kOffPart);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nT = (p.P + kPT - 1) / kPT;
     const int qlo_t = p.q_lo / kPT;
+    const int qs0 = qlo_t * kPT;  // first query row with statistics
     // This CTA: pass 1 -- query tile `tile` of query head `head` (= b * Hq + qh),
     // B tiles = key tiles 0..tile of its KV head; pass 2 -- key tile `tile` of
     // unit `head` (= b * Hkv + kvh), B tiles = (query head g, query tile qt)
@@ -110,7 +113,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
     const int tile = MODE == kRowStats ? nT - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
     const int qt0 = max(tile, qlo_t), nq = nT - qt0;
     const int n_b = MODE == kRowStats ? tile + 1 : p.G * nq;
-    const int a_row = head * p.P + tile * kPT;
+    // Q rows: query i of query head h is row h * q_stride + i - q_first (rows
+    // before a head's first given query belong to the previous head or lie
+    // before the tensor: they only feed masked rows and columns)
+    const int a_row = MODE == kRowStats ? head * p.q_stride + tile * kPT - p.q_first : head * p.P + tile * kPT;
     auto b_row = [&](int n) -> int {
         if (MODE == kRowStats) {
             const int b = head / p.Hq, qh = head - b * p.Hq;
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
         } else {
             const int b = head / p.Hkv, kvh = head - b * p.Hkv;
             const int g = n / nq, qt = qt0 + (n - g * nq);
-            return (b * p.Hq + kvh * p.G + g) * p.P + qt * kPT;
+            return (b * p.Hq + kvh * p.G + g) * p.q_stride + qt * kPT - p.q_first;
         }
     };
 
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                     const int i0 = qt * kPT + col0;
                     const int b = head / p.Hkv, kvh = head - b * p.Hkv;
                     const float4 *st = reinterpret_cast<const float4 *>(
-                        p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + i0);
+                        p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + (i0 - qs0));
                     const bool full = qt > tile && i0 + 32 <= p.P && i0 >= p.q_lo;
                     const float2 c2 = make_float2(c, c);
                     float2 s2 = make_float2(0.f, 0.f);
@@ -280,7 +286,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                         }
                     }
                     acc += s2.x + s2.y;
+                    if (p.per_head && n - g * nq == nq - 1) {  // the last tile of query head g
+                        hpart[(g * kSlices + slice) * kPT + row] = acc;
+                        acc = 0.f;
+                    }
                 }
+            } else if (MODE == kColSum && p.per_head) {
+                const int g = n / nq;
+                if (n - g * nq == nq - 1) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
             }
             tc_fence_before();
             __syncwarp();
@@ -300,7 +313,17 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                     const float2 o = xchg[k * kPT + row];
                     if (o.x != -INFINITY) ll += o.y * ex2(o.x - mm);
                 }
-                if (a_idx < p.P) p.stats[static_cast<size_t>(head) * p.Ps + a_idx] = -(mm + log2f(ll));
+                if (a_idx < p.P) p.stats[static_cast<size_t>(head) * p.Ps + (a_idx - qs0)] = -(mm + log2f(ll));
+            } else if (p.per_head) {
+                if (a_idx < p.P) {
+                    const int b = head / p.Hkv, kvh = head - b * p.Hkv;
+                    for (int g = 0; g < p.G; ++g) {
+                        float tot = 0.f;
+#pragma unroll
+                        for (int k = 0; k < kSlices; ++k) tot += hpart[(g * kSlices + k) * kPT + row];
+                        p.score[static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.P + a_idx] = tot;
+                    }
+                }
             } else {
                 float tot = acc;
 #pragma unroll
@@ -341,6 +364,86 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane)
     return v;
 }
 
+// Block-wide reductions of the selection kernels (kSelThreads threads; `red`
+// holds kSelWarps ints, `total` one; both free again on return).
+struct BlockOps {
+    int *red, *total;
+    int lane, warp;
+    // the sum of v over the block, in every thread
+    __device__ int sum(int v) const
+    {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) red[warp] = v;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < kSelWarps ? red[lane] : 0;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
+            if (lane == 0) *total = w;
+        }
+        __syncthreads();
+        const int t = *total;
+        __syncthreads();
+        return t;
+    }
+    // exclusive prefix of v over the threads in order (x) and the total (y)
+    __device__ int2 scan(int v) const
+    {
+        const int inc = warp_incl_scan(v, lane);
+        if (lane == 31) red[warp] = inc;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = lane < kSelWarps ? red[lane] : 0;
+            const int winc = warp_incl_scan(w, lane);
+            if (lane < kSelWarps) red[lane] = winc - w;  // exclusive warp offsets
+            if (lane == kSelWarps - 1) *total = winc;
+        }
+        __syncthreads();
+        const int2 r = make_int2(red[warp] + inc - v, *total);
+        __syncthreads();
+        return r;
+    }
+};
+
+// The E smallest (bit pattern, position) keys among bits[lo, hi), E >= 1:
+// the smallest T with #{bits <= T} >= E, and how many of the keys equal to T
+// are among them (`need`, the oldest positions first).
+__device__ void cut_threshold(const uint32_t *bits, int lo, int hi, int E, const BlockOps &ops, uint32_t &T,
+                              int &need)
+{
+    uint32_t a = 0, b = 0xFFFFFFFFu;
+    while (a < b) {
+        const uint32_t mid = a + (b - a) / 2;
+        int c = 0;
+        for (int j = lo + static_cast<int>(threadIdx.x); j < hi; j += kSelThreads) c += bits[j] <= mid;
+        if (ops.sum(c) >= E) b = mid;
+        else a = mid + 1;
+    }
+    T = a;
+    int c = 0;
+    for (int j = lo + static_cast<int>(threadIdx.x); j < hi; j += kSelThreads) c += bits[j] < T;
+    need = E - ops.sum(c);
+}
+
+// Copies K and V rows of the slots [0, kept) from the prompt rows named by pos.
+__device__ void copy_kept_rows(const void *K, const void *V, void *kc, void *vc, const int32_t *pos, size_t unit,
+                               int P, int C, int row_bytes, int kept, int warp, int lane)
+{
+    const int vecs = row_bytes / 16;
+    for (int s = warp; s < kept; s += kSelWarps) {
+        const int j = pos[s];
+        for (int vi = lane; vi < 2 * vecs; vi += 32) {
+            const int which = vi / vecs, off = vi - which * vecs;
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(which ? V : K) +
+                                                               (unit * P + j) * static_cast<size_t>(row_bytes));
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(which ? vc : kc) +
+                                                   (unit * C + s) * static_cast<size_t>(row_bytes));
+            dst[off] = src[off];
+        }
+    }
+}
+
 // Keeps the first n_sink and last n_recent positions and, of the others, all
 // but the P - K smallest (score, position) keys; the kept tokens fill slots
 // 0, 1, ... in ascending position order. One CTA per unit: the unit's score
@@ -353,6 +456,7 @@ __global__ void __launch_bounds__(kSelThreads) prompt_select_kernel(const Prompt
     __shared__ int red[kSelWarps];
     __shared__ int total;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const BlockOps ops{red, &total, lane, warp};
     const size_t unit = blockIdx.x;
     const int P = p.P;
     const int e_lo = p.n_sink, e_hi = P - p.n_recent;  // eligible positions [e_lo, e_hi)
@@ -363,58 +467,10 @@ __global__ void __launch_bounds__(kSelThreads) prompt_select_kernel(const Prompt
     }
     __syncthreads();
 
-    // block-wide sum of v; every thread gets it
-    auto block_sum = [&](int v) -> int {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) red[warp] = v;
-        __syncthreads();
-        if (warp == 0) {
-            int w = lane < kSelWarps ? red[lane] : 0;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
-            if (lane == 0) total = w;
-        }
-        __syncthreads();
-        const int t = total;
-        __syncthreads();
-        return t;
-    };
-    // exclusive prefix of v over the threads in order (x) and the total (y)
-    auto block_scan = [&](int v) -> int2 {
-        const int inc = warp_incl_scan(v, lane);
-        if (lane == 31) red[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            const int w = lane < kSelWarps ? red[lane] : 0;
-            const int winc = warp_incl_scan(w, lane);
-            if (lane < kSelWarps) red[lane] = winc - w;  // exclusive warp offsets
-            if (lane == kSelWarps - 1) total = winc;
-        }
-        __syncthreads();
-        const int2 r = make_int2(red[warp] + inc - v, total);
-        __syncthreads();
-        return r;
-    };
-
     const int E = P > p.budget ? P - p.budget : 0;  // tokens to remove
     uint32_t T = 0;
     int need = 0;
-    if (E > 0) {
-        // smallest bit pattern T with #{eligible: bits <= T} >= E
-        uint32_t lo = 0, hi = 0xFFFFFFFFu;
-        while (lo < hi) {
-            const uint32_t mid = lo + (hi - lo) / 2;
-            int c = 0;
-            for (int j = e_lo + tid; j < e_hi; j += kSelThreads) c += sbits[j] <= mid;
-            if (block_sum(c) >= E) hi = mid;
-            else lo = mid + 1;
-        }
-        T = lo;
-        int c = 0;
-        for (int j = e_lo + tid; j < e_hi; j += kSelThreads) c += sbits[j] < T;
-        need = E - block_sum(c);  // how many of the tokens at exactly T go, oldest first
-    }
+    if (E > 0) cut_threshold(sbits, e_lo, e_hi, E, ops, T, need);
 
     int tie_base = 0, slot_base = 0;
     for (int j0 = 0; j0 < P; j0 += kSelThreads) {
@@ -423,11 +479,10 @@ __global__ void __launch_bounds__(kSelThreads) prompt_select_kernel(const Prompt
         const bool elig = in && j >= e_lo && j < e_hi;
         const uint32_t b = in ? sbits[j] : 0u;
         const bool tie = E > 0 && elig && b == T;
-        const int2 ts = block_scan(tie ? 1 : 0);
-        const int tie_rank = tie_base + ts.x;
-        const bool evict = E > 0 && elig && (b < T || (tie && tie_rank < need));
+        const int2 ts = ops.scan(tie ? 1 : 0);
+        const bool evict = E > 0 && elig && (b < T || (tie && tie_base + ts.x < need));
         const bool keep = in && !evict;
-        const int2 ks = block_scan(keep ? 1 : 0);
+        const int2 ks = ops.scan(keep ? 1 : 0);
         const int slot = slot_base + ks.x;
         if (keep && slot < p.C) {
             p.pos[unit * p.cstride + slot] = j;
@@ -437,21 +492,83 @@ __global__ void __launch_bounds__(kSelThreads) prompt_select_kernel(const Prompt
         slot_base += ks.y;
     }
     __syncthreads();  // the positions written above are visible to the whole CTA
+    copy_kept_rows(p.K, p.V, p.kc, p.vc, p.pos + unit * p.cstride, unit, P, p.C, p.row_bytes, min(slot_base, p.C),
+                   warp, lane);
+}
 
-    // copy the kept rows: one warp per slot, K then V in 16-byte vectors
-    const int kept = min(slot_base, p.C);
-    const int vecs = p.row_bytes / 16;
-    for (int s = warp; s < kept; s += kSelWarps) {
-        const int j = p.pos[unit * p.cstride + s];
-        for (int vi = lane; vi < 2 * vecs; vi += 32) {
-            const int which = vi / vecs, off = vi - which * vecs;
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(which ? p.V : p.K) +
-                                                               (unit * P + j) * static_cast<size_t>(p.row_bytes));
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(which ? p.vc : p.kc) +
-                                                   (unit * p.C + s) * static_cast<size_t>(p.row_bytes));
-            dst[off] = src[off];
+// SnapKV ("Attention Sinks 与 KV Cache 淘汰策略" section 4.3): for each query
+// head g of the unit's KV head, the votes of the prefix [0, P - window) are
+// max-pooled over 7 positions (within the prefix) and the head keeps its topk
+// largest pooled votes (ties: the newer position); the unit keeps the union
+// over its G query heads plus the window, in slots 0, 1, ... in ascending
+// position order, each token with the mean over g of its votes. One CTA per
+// unit: a head's pooled bits and the kept bitmap in shared memory.
+__global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(const SnapSelectParams p)
+{
+    extern __shared__ uint32_t ssm[];
+    const int P = p.P, n_pre = P - p.window;
+    uint32_t *pbits = ssm;               // [n_pre]
+    uint32_t *keep = ssm + n_pre;        // [ceil(P / 32)] bitmap
+    __shared__ int red[kSelWarps];
+    __shared__ int total;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const BlockOps ops{red, &total, lane, warp};
+    const size_t unit = blockIdx.x;
+    const int b = static_cast<int>(unit) / p.Hkv, kvh = static_cast<int>(unit) - b * p.Hkv;
+    const int nw = (P + 31) / 32;
+    for (int i = tid; i < nw; i += kSelThreads) keep[i] = 0u;
+    __syncthreads();
+    for (int j = n_pre + tid; j < P; j += kSelThreads) atomicOr(&keep[j >> 5], 1u << (j & 31));  // the window
+
+    const int take = min(p.topk, n_pre);
+    const int E = n_pre - take;  // prefix positions a head does not take
+    for (int g = 0; g < p.G; ++g) {
+        const float *vg = p.votes + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * P;
+        __syncthreads();  // the previous head is done with pbits
+        for (int j = tid; j < n_pre; j += kSelThreads) {
+            float mx = vg[j];
+            for (int jj = max(0, j - 3); jj <= min(n_pre - 1, j + 3); ++jj) mx = fmaxf(mx, vg[jj]);
+            if (!(mx >= 0.f && mx <= FLT_MAX)) atomicOr(p.err, KVEVICT_DEV_NONFINITE);
+            pbits[j] = __float_as_uint(mx);
+        }
+        __syncthreads();
+        if (take == 0) continue;
+        uint32_t T = 0;
+        int need = 0;
+        if (E > 0) cut_threshold(pbits, 0, n_pre, E, ops, T, need);
+        // taken: not among the E smallest (bits, position)
+        int tie_base = 0;
+        for (int j0 = 0; j0 < n_pre; j0 += kSelThreads) {
+            const int j = j0 + tid;
+            const bool in = j < n_pre;
+            const uint32_t bt = in ? pbits[j] : 0u;
+            const bool tie = E > 0 && in && bt == T;
+            const int2 ts = ops.scan(tie ? 1 : 0);
+            const bool left = E > 0 && in && (bt < T || (tie && tie_base + ts.x < need));
+            if (in && !left) atomicOr(&keep[j >> 5], 1u << (j & 31));
+            tie_base += ts.y;
         }
     }
+    __syncthreads();
+
+    int slot_base = 0;
+    for (int j0 = 0; j0 < P; j0 += kSelThreads) {
+        const int j = j0 + tid;
+        const bool k = j < P && ((keep[j >> 5] >> (j & 31)) & 1u);
+        const int2 ks = ops.scan(k ? 1 : 0);
+        const int slot = slot_base + ks.x;
+        if (k && slot < p.C) {
+            float sc = 0.f;
+            for (int g = 0; g < p.G; ++g) sc += p.votes[static_cast<size_t>(b * p.Hq + kvh * p.G + g) * P + j];
+            p.pos[unit * p.cstride + slot] = j;
+            p.cscore[unit * p.cstride + slot] = sc * (1.f / p.G);
+        }
+        slot_base += ks.y;
+    }
+    if (slot_base > p.C && tid == 0) atomicOr(p.err, KVEVICT_DEV_BAD_SLOT);
+    __syncthreads();
+    copy_kept_rows(p.K, p.V, p.kc, p.vc, p.pos + unit * p.cstride, unit, P, p.C, p.row_bytes, min(slot_base, p.C),
+                   warp, lane);
 }
 
 template <int D, int MODE> cudaError_t launch_attn(const PromptAttnParams &p, int B, cudaStream_t st)
@@ -479,6 +596,16 @@ cudaError_t launch_prompt_rowstats(const PromptAttnParams &p, int head_dim, int 
 cudaError_t launch_prompt_colsum(const PromptAttnParams &p, int head_dim, int B, cudaStream_t st)
 {
     return head_dim == 64 ? launch_attn<64, kColSum>(p, B, st) : launch_attn<128, kColSum>(p, B, st);
+}
+
+cudaError_t launch_snapkv_select(const SnapSelectParams &p, int units, cudaStream_t st)
+{
+    const size_t smem = static_cast<size_t>(p.P - p.window) * 4 + static_cast<size_t>((p.P + 31) / 32) * 4;
+    cudaError_t e = cudaFuncSetAttribute(snapkv_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    snapkv_select_kernel<<<units, kSelThreads, smem, st>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_prompt_select(const PromptSelectParams &p, int units, cudaStream_t st)

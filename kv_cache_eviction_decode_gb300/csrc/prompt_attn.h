@@ -20,9 +20,16 @@ struct alignas(64) PromptTmap {
 
 struct PromptAttnParams {
     PromptTmap tma, tmb;  // A-side rows (the tile a CTA keeps) and B-side rows (the tiles it streams)
-    float *stats;         // [B * Hq][Ps]: per query row, -(m + log2(l)) of its softmax (log2 units)
-    float *score;         // [B * Hkv][P]: per key, the mass it receives, mean over the G query heads
-    int P, Ps, G, Hq, Hkv, q_lo;
+    float *stats;         // [B * Hq][Ps]: per query row i >= qs0 (q_lo rounded down to a tile),
+                          // -(m + log2(l)) of its softmax (log2 units), at index i - qs0
+    float *score;         // per key, the mass it receives from the queries i >= q_lo:
+                          // [B * Hkv][P], mean over the G query heads, or, with per_head,
+                          // [B * Hq][P], one row per query head
+    int P, Ps, G, Hq, Hkv;
+    int q_lo;             // first query that takes part
+    int q_stride;         // rows per query head in the Q tensor
+    int q_first;          // query index of each head's first Q row (queries before it are not given)
+    int per_head;
     float scale_log2;     // log2(e) / sqrt(d)
     uint32_t *err;
 };
@@ -38,6 +45,17 @@ struct PromptSelectParams {
     uint32_t *err;
 };
 
+struct SnapSelectParams {
+    const float *votes;   // [B * Hq][P]: per query head, the window's softmax mass on every key
+    const void *K, *V;    // prompt [B][Hkv][P][d]
+    void *kc, *vc;        // layer cache [B][Hkv][C][d]
+    int32_t *pos;         // layer [B][Hkv][cstride]
+    float *cscore;        // layer [B][Hkv][cstride]
+    int P, C, cstride, row_bytes;
+    int G, Hq, Hkv, window, topk;
+    uint32_t *err;
+};
+
 // Bytes of shared memory the scoring kernels use for head_dim d.
 size_t prompt_attn_smem(int head_dim);
 // Pass 1 (row statistics) and pass 2 (column sums); d in {64, 128}.
@@ -45,5 +63,7 @@ cudaError_t launch_prompt_rowstats(const PromptAttnParams &p, int head_dim, int 
 cudaError_t launch_prompt_colsum(const PromptAttnParams &p, int head_dim, int B, cudaStream_t st);
 // The cut to the budget and the copy of the kept rows into the cache.
 cudaError_t launch_prompt_select(const PromptSelectParams &p, int units, cudaStream_t st);
+// SnapKV: pooling, per-head top-k, the union with the window, the copy.
+cudaError_t launch_snapkv_select(const SnapSelectParams &p, int units, cudaStream_t st);
 
 }  // namespace kvevict
