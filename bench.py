@@ -498,6 +498,132 @@ def prefill_phase(args, w, rank, world, local):
         dist.destroy_process_group()
 
 
+def snapkv_phase(args, w, rank, world, local):
+    """One layer's SnapKV prefill per step: the window's votes on the tensor
+    cores, pooling, per-head top-k, union, copy. Bound by HBM: the prompt's K
+    is read once, the votes go out and back, the kept rows are copied."""
+    metric = "SnapKV prefill prompt tokens/s (window votes + selection); HBM GB/s vs measured copy"
+    P, win = w.prompt_len, args.window
+    if w.policy != configs.POLICY_H2O or w.dtype != configs.DTYPE_BF16 or P <= win:
+        raise SystemExit("--phase snapkv needs an H2O bf16 workload with a prompt longer than the window")
+    topk = args.topk or max(0, (w.capacity - win) // w.group)
+    cfg = {"workload": w.name, "phase": "prefill_snapkv", "policy": "h2o", "batch": w.batch,
+           "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "prompt_len": P,
+           "window": win, "topk_per_head": topk, "capacity_slots": w.capacity}
+    tokens = w.batch * P
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import concurrent.futures as cf
+        import oracle
+        threads = oracle.online_cores()
+        G, d = w.group, w.head_dim
+        rng = np.random.default_rng(w.seed)
+        def unit(i):
+            q = rng.standard_normal((G, win, d)).astype(np.float32)
+            k = rng.standard_normal((P, d)).astype(np.float32)
+            u = oracle.Unit(oracle.H2O, w.n_sink, w.n_heavy, w.n_recent, w.budget, 0, 0, G, d)
+            u.prefill_snapkv(q, k, k, topk)
+        t0, done = time.perf_counter(), 0
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            while time.perf_counter() - t0 < max(2.0, args.cpu_seconds) or done == 0:
+                list(ex.map(unit, range(threads)))
+                done += threads
+        dt = time.perf_counter() - t0
+        v = done / dt * P / w.n_kv_heads
+        desc = f"{done} units (one sequence x KV head) of prompt {P}, {dt:.1f} s"
+        print(json.dumps({"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 1,
+                          "steps": 1, "warmup": 0, "ms_per_step": 1000.0 * tokens / v, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": cfg,
+                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                           "sample": desc},
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    from kv_cache_eviction_decode_gb300 import KVEvictCache
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    n_calls = args.warmup + args.steps
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        Qo = synth.device_prompt_queries(w, 0, device, P)[:, :, P - win:].contiguous()
+        K, V = synth.device_prompt(w, 0, device, P)
+        cache = KVEvictCache.from_workload(w.with_(n_layers=n_calls + (0 if args.no_e2e else 2)), device=device,
+                                           stream=stream)
+        ws = torch.empty(cache.prefill_snapkv_workspace_bytes(P, win), dtype=torch.uint8, device=device)
+        for i in range(args.warmup):
+            cache.prefill_snapkv(i, Qo, K, V, topk, workspace=ws)
+        stream.synchronize()
+        barrier(device)
+        torch.cuda.synchronize(device)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(device.index) as clk:
+            ev0.record(stream)
+            for i in range(args.warmup, n_calls):
+                cache.prefill_snapkv(i, Qo, K, V, topk, workspace=ws)
+            ev1.record(stream)
+            ev1.synchronize()
+        torch.cuda.synchronize(device)
+        barrier(device)
+        err = cache.check()
+        if err:
+            raise RuntimeError(f"device error word {err:#x}")
+        dt_ms = reduce_max(ev0.elapsed_time(ev1), device)
+        kept = int((cache.slot_positions(n_calls - 1) >= 0).sum().item())
+        e2e = None
+        if not args.no_e2e:
+            Qh, Kh, Vh = Qo.cpu().pin_memory(), K.cpu().pin_memory(), V.cpu().pin_memory()
+            pos_h = torch.empty((w.batch, w.n_kv_heads, cache.capacity), dtype=torch.int32).pin_memory()
+            Qd, Kd, Vd = torch.empty_like(Qo), torch.empty_like(K), torch.empty_like(V)
+            barrier(device)
+            torch.cuda.synchronize(device)
+            t0 = time.perf_counter()
+            for layer in (n_calls, n_calls + 1):
+                Qd.copy_(Qh, non_blocking=True)
+                Kd.copy_(Kh, non_blocking=True)
+                Vd.copy_(Vh, non_blocking=True)
+                cache.prefill_snapkv(layer, Qd, Kd, Vd, topk, workspace=ws)
+                pos_h.copy_(cache.slot_positions(layer), non_blocking=True)
+                stream.synchronize()
+            e2e_s = reduce_max(time.perf_counter() - t0, device)
+            e2e = {"value": world * tokens * 2 / e2e_s, "unit": "tokens/s",
+                   "h2d_bytes_per_step": (Qo.numel() + K.numel() + V.numel()) * Qo.element_size(),
+                   "d2h_bytes_per_step": pos_h.numel() * 4, "steps": 2}
+        cache.close()
+    e = 2
+    row = w.head_dim * e
+    algo = (w.batch * w.n_kv_heads * P * row            # the prompt's K, read once
+            + w.batch * w.n_q_heads * win * row          # the window's queries
+            + 2 * w.batch * w.n_q_heads * P * 4          # votes written, read back
+            + 2 * 2 * kept * row)                        # kept K and V rows: read, write
+    per_call_s = dt_ms / 1e3 / args.steps
+    peak, peak_kind = measured_hbm_peak()
+    achieved = algo / per_call_s / 1e9
+    out = {
+        "metric": metric, "value": world * tokens / per_call_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V with hub and sink keys)",
+        "config": dict(cfg, timing="CUDA events on the launching stream; a step = one layer's SnapKV prefill "
+                                   "(3 launches); the prompt's K exceeds L2", kept_tokens=kept),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_kind": peak_kind, "algorithmic_bytes_per_step": algo,
+                     "frac_of_8TBs": achieved / 8000.0},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,8 +642,11 @@ def main():
                     help="override the layer count (small profiling captures only; the line then names it)")
     ap.add_argument("--no-preroll", action="store_true",
                     help="time from the state right after prefill (small profiling captures only)")
-    ap.add_argument("--phase", default="decode", choices=["decode", "prefill"],
-                    help="decode (default): the decode step; prefill: the Q-seeded prefill of one layer (H2O)")
+    ap.add_argument("--phase", default="decode", choices=["decode", "prefill", "snapkv"],
+                    help="decode (default): the decode step; prefill: the Q-seeded prefill of one layer (H2O); "
+                         "snapkv: the SnapKV prefill selection of one layer (H2O)")
+    ap.add_argument("--window", type=int, default=32, help="SnapKV observation window")
+    ap.add_argument("--topk", type=int, default=0, help="SnapKV positions per query head (0: fill the budget)")
     ap.add_argument("--prompt", type=int, default=-1,
                     help="override the prompt length (small profiling captures only; decode launch shape unchanged "
                          "once the cache is full)")
@@ -542,6 +671,8 @@ def main():
 
     if args.phase == "prefill":
         return prefill_phase(args, w, rank, world, local)
+    if args.phase == "snapkv":
+        return snapkv_phase(args, w, rank, world, local)
 
     if args.impl == "reference":
         # The reference arm is the CPU oracle, timed as it stands on the host
