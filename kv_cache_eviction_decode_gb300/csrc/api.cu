@@ -744,6 +744,9 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
     ap.q_stride = window;
     ap.q_first = P - window;
     ap.per_head = 1;
+    // stack the G heads' window rows into shared tiles when every 32-row chunk belongs to one head
+    ap.stacked = window % 32 == 0;
+    if (ap.stacked) ap.Ps = (L.G * window + kPromptTile - 1) / kPromptTile * kPromptTile;
     ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
     ap.err = at<uint32_t>(h, L.off_err);
     std::memcpy(&ap.tma, &tq, sizeof tq);

@@ -85,7 +85,10 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b)
     return d;
 }
 
-template <int D, int MODE>
+// STACK (SnapKV, window a multiple of 32): the G query heads' window rows,
+// contiguous in Q, form one stacked row axis r = g * w + t per unit (query
+// head g, query position P - w + t), tiled by 128 across heads.
+template <int D, int MODE, bool STACK>
 __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_constant__ PromptAttnParams p)
 {
     using L = PromptLayout<D>;
@@ -110,14 +113,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
     // unit `head` (= b * Hkv + kvh), B tiles = (query head g, query tile qt)
     // for g < G and qt from max(tile, first query tile) on.
     const int head = blockIdx.y;
-    const int tile = MODE == kRowStats ? nT - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    const int Lq = p.G * p.q_stride;  // STACK: stacked rows per unit
+    const int nLq = (Lq + kPT - 1) / kPT;
+    const int tile = MODE == kRowStats && !STACK ? nT - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
     const int qt0 = max(tile, qlo_t), nq = nT - qt0;
-    const int n_b = MODE == kRowStats ? tile + 1 : p.G * nq;
+    const int n_b = STACK ? (MODE == kRowStats ? nT : nLq) : (MODE == kRowStats ? tile + 1 : p.G * nq);
     // Q rows: query i of query head h is row h * q_stride + i - q_first (rows
     // before a head's first given query belong to the previous head or lie
     // before the tensor: they only feed masked rows and columns)
-    const int a_row = MODE == kRowStats ? head * p.q_stride + tile * kPT - p.q_first : head * p.P + tile * kPT;
+    const int a_row = STACK ? (MODE == kRowStats ? head * Lq + tile * kPT : head * p.P + tile * kPT)
+                            : (MODE == kRowStats ? head * p.q_stride + tile * kPT - p.q_first : head * p.P + tile * kPT);
     auto b_row = [&](int n) -> int {
+        if (STACK) return MODE == kRowStats ? head * p.P + n * kPT : head * Lq + n * kPT;
         if (MODE == kRowStats) {
             const int b = head / p.Hq, qh = head - b * p.Hq;
             return (b * p.Hkv + qh / p.G) * p.P + n * kPT;
@@ -206,6 +213,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
         float m = -INFINITY, l = 0.f;          // pass 1: running max and sum (log2 units)
         float acc = 0.f;                       // pass 2: mass received
         bool ok = true;
+        int cur_g = 0;                         // STACK pass 2: query head of the running sum
+        if (MODE == kColSum && STACK)
+            for (int g = 0; g < p.G; ++g) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
         for (int n = 0; n < n_b; ++n) {
             const int sb = n & 1;
             // the TMEM load below is warp-collective: the whole warp agrees on `ok`
@@ -219,13 +229,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                 tmem_ld32(tmem + lane_field + static_cast<uint32_t>(sb * kPT + col0), r);
                 tc_wait_ld();
                 if (MODE == kRowStats) {
-                    // keys j = n * 128 + col0 + e; only the diagonal tile is masked
+                    // keys j = n * 128 + col0 + e; only the diagonal tile is masked (STACK: the
+                    // keys from the window on, against this row's query position)
                     const int j0 = n * kPT + col0;
+                    const int qi = STACK ? p.P - p.q_stride + a_idx % p.q_stride : a_idx;
                     float v[32];
-                    if (n == tile) {
+                    if (STACK ? j0 + 32 > p.P - p.q_stride : n == tile) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            v[e] = (j0 + e <= a_idx && j0 + e < p.P) ? __uint_as_float(r[e]) : -INFINITY;
+                            v[e] = (j0 + e <= qi && j0 + e < p.P) ? __uint_as_float(r[e]) : -INFINITY;
                     } else {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
@@ -247,6 +259,48 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                             s2 = fadd2(s2, make_float2(ex2(z.x), ex2(z.y)));
                         }
                         l += s2.x + s2.y;
+                    }
+                } else if (STACK) {
+                    // stacked rows r0 .. r0 + 31 (one query head: w is a multiple of 32)
+                    const int r0 = n * kPT + col0;
+                    if (r0 < Lq) {
+                        const int g = r0 / p.q_stride, i0 = p.P - p.q_stride + (r0 - g * p.q_stride);
+                        if (g != cur_g) {
+                            hpart[(cur_g * kSlices + slice) * kPT + row] = acc;
+                            acc = 0.f;
+                            cur_g = g;
+                        }
+                        const float4 *st = reinterpret_cast<const float4 *>(p.stats + static_cast<size_t>(head) * p.Ps + r0);
+                        const float2 c2 = make_float2(c, c);
+                        float2 s2 = make_float2(0.f, 0.f);
+                        if (a_idx < p.P - p.q_stride) {  // a key before the window: every window query sees it
+#pragma unroll
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 nms = __ldg(st + e4);
+                                const int e = e4 * 4;
+                                const float2 za = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                                        c2, make_float2(nms.x, nms.y));
+                                const float2 zb = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])),
+                                                        c2, make_float2(nms.z, nms.w));
+                                s2 = fadd2(s2, make_float2(ex2(za.x), ex2(za.y)));
+                                s2 = fadd2(s2, make_float2(ex2(zb.x), ex2(zb.y)));
+                            }
+                        } else {
+#pragma unroll
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 nms = __ldg(st + e4);
+                                const float mv[4] = {nms.x, nms.y, nms.z, nms.w};
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) {
+                                    const int e = e4 * 4 + t;
+                                    const float pr = ex2(fmaf(__uint_as_float(r[e]), c, mv[t]));
+                                    const float add = (i0 + e >= a_idx) ? pr : 0.f;
+                                    if (t & 1) s2.y += add;
+                                    else s2.x += add;
+                                }
+                            }
+                        }
+                        acc += s2.x + s2.y;
                     }
                 } else {
                     // queries i = qt * 128 + col0 + e of query head g
@@ -291,7 +345,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                         acc = 0.f;
                     }
                 }
-            } else if (MODE == kColSum && p.per_head) {
+            } else if (MODE == kColSum && p.per_head && !STACK) {
                 const int g = n / nq;
                 if (n - g * nq == nq - 1) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
             }
@@ -299,6 +353,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[sb]);
         }
+        if (MODE == kColSum && STACK) hpart[(cur_g * kSlices + slice) * kPT + row] = acc;
         // the column slices of each row meet: slices 1.. hand over to slice 0
         if (slice > 0) xchg[(slice - 1) * kPT + row] = MODE == kRowStats ? make_float2(m, l) : make_float2(acc, 0.f);
         named_bar_sync(1, kEpiWarps * 32);
@@ -313,8 +368,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                     const float2 o = xchg[k * kPT + row];
                     if (o.x != -INFINITY) ll += o.y * ex2(o.x - mm);
                 }
-                if (a_idx < p.P) p.stats[static_cast<size_t>(head) * p.Ps + (a_idx - qs0)] = -(mm + log2f(ll));
-            } else if (p.per_head) {
+                if (STACK ? a_idx < Lq : a_idx < p.P)
+                    p.stats[static_cast<size_t>(head) * p.Ps + (STACK ? a_idx : a_idx - qs0)] = -(mm + log2f(ll));
+            } else if (p.per_head || STACK) {
                 if (a_idx < p.P) {
                     const int b = head / p.Hkv, kvh = head - b * p.Hkv;
                     for (int g = 0; g < p.G; ++g) {
@@ -571,17 +627,24 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(const SnapSe
                    warp, lane);
 }
 
-template <int D, int MODE> cudaError_t launch_attn(const PromptAttnParams &p, int B, cudaStream_t st)
+template <int D, int MODE, bool STACK> cudaError_t launch_attn_t(const PromptAttnParams &p, int B, cudaStream_t st)
 {
     const int smem = PromptLayout<D>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(prompt_attn_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(prompt_attn_kernel<D, MODE, STACK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nT = (p.P + kPT - 1) / kPT;
-    const int tiles = MODE == kRowStats ? nT - p.q_lo / kPT : nT;
-    const int heads = MODE == kRowStats ? B * p.Hq : B * p.Hkv;
+    const int nLq = (p.G * p.q_stride + kPT - 1) / kPT;
+    const int tiles = STACK ? (MODE == kRowStats ? nLq : nT) : (MODE == kRowStats ? nT - p.q_lo / kPT : nT);
+    const int heads = STACK ? B * p.Hkv : (MODE == kRowStats ? B * p.Hq : B * p.Hkv);
     if (tiles <= 0 || heads <= 0) return cudaSuccess;
-    prompt_attn_kernel<D, MODE><<<dim3(tiles, heads), kPThreads, smem, st>>>(p);
+    prompt_attn_kernel<D, MODE, STACK><<<dim3(tiles, heads), kPThreads, smem, st>>>(p);
     return cudaGetLastError();
+}
+
+template <int D, int MODE> cudaError_t launch_attn(const PromptAttnParams &p, int B, cudaStream_t st)
+{
+    return p.stacked ? launch_attn_t<D, MODE, true>(p, B, st) : launch_attn_t<D, MODE, false>(p, B, st);
 }
 
 }  // namespace

@@ -30,6 +30,8 @@ struct PromptAttnParams {
     int q_stride;         // rows per query head in the Q tensor
     int q_first;          // query index of each head's first Q row (queries before it are not given)
     int per_head;
+    int stacked;          // SnapKV with a window of a multiple of 32: the G heads' window rows stacked
+                          // (row g * q_stride + t); stats then [B * Hkv][Ps] over the stacked rows
     float scale_log2;     // log2(e) / sqrt(d)
     uint32_t *err;
 };

@@ -101,7 +101,8 @@ def _cache(device, B, Hq, Hkv, d, n_sink, n_heavy, n_recent):
 
 
 @pytest.mark.parametrize("G,d,P,w,k", [(1, 64, 90, 8, 10), (4, 128, 300, 32, 20), (8, 128, 700, 32, 12),
-                                       (2, 64, 257, 16, 100), (4, 64, 140, 20, 0)])
+                                       (2, 64, 257, 16, 100), (4, 64, 140, 20, 0), (4, 128, 500, 64, 30),
+                                       (8, 64, 333, 96, 10)])
 def test_snapkv_prefill_small(cuda_device, G, d, P, w, k):
     gen = torch.Generator().manual_seed(7000 + G * P + k)
     B, Hkv = 2, 2
