@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvevict_oracle.c")
 _LIB = os.path.join(_HERE, "liborc_kvevict.so")
 
-H2O, SINK_WINDOW, RANDOM = 0, 1, 2
+H2O, SINK_WINDOW, RANDOM, H2O_BLOCK = 0, 1, 2, 3
 OK, EINVAL, ECAPACITY, ESTATE = 0, -1, -2, -3
 
 _lock = threading.Lock()
@@ -52,6 +52,8 @@ def lib():
                 getattr(L, name).argtypes = [P]
                 getattr(L, name).restype = I
             L.orc_last_victim_pos.argtypes = [P]
+            L.orc_last_block.argtypes = [P]
+            L.orc_last_block.restype = I
             L.orc_last_victim_pos.restype = ctypes.c_int32
             L.orc_evicted_mass.argtypes = [P]
             L.orc_evicted_mass.restype = D
@@ -234,6 +236,10 @@ class Unit:
     @property
     def new_score(self) -> float:
         return self._L.orc_new_score(self.h)
+
+    @property
+    def last_block(self) -> int:
+        return self._L.orc_last_block(self.h)
 
     @property
     def greedy_disagreements(self) -> int:

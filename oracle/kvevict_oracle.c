@@ -57,7 +57,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_H2O = 0, ORC_SINK_WINDOW = 1, ORC_RANDOM = 2 };
+enum { ORC_H2O = 0, ORC_SINK_WINDOW = 1, ORC_RANDOM = 2, ORC_H2O_BLOCK = 3 };
 enum { ORC_OK = 0, ORC_EINVAL = -1, ORC_ECAPACITY = -2, ORC_ESTATE = -3 };
 
 #define ORC_RANDOM_KEY_TAG 0x5EED0001ull
@@ -82,6 +82,7 @@ typedef struct orc_unit {
     double score_new;
     int32_t last_victim_pos; /* position removed by the last commit, -1 if none */
     int greedy_disagreements; /* argmax F(T\{v}) != argmin (score, pos): must stay 0 */
+    int last_block;      /* H2O_BLOCK: block released for the token of the last step, -1 if none */
 } orc_unit;
 
 /* ------------------------------------------------------------------------ */
@@ -142,6 +143,14 @@ orc_unit *orc_new(int policy, int n_sink, int n_heavy, int n_recent, int budget,
         if (n_sink < 0 || n_heavy != 0 || n_recent < 1 || n_sink + n_recent != budget) return NULL;
     } else if (policy == ORC_RANDOM) {
         if (r < 1 || max_prompt < 0) return NULL;
+    } else if (policy == ORC_H2O_BLOCK) {
+        /* r is the block size; the budget is whole blocks, and besides the
+         * blocks holding sinks at least one block lies outside the recent
+         * window, so a full cache always has a block to release */
+        if (n_sink < 0 || n_heavy < 0 || n_recent < 1 || n_sink + n_heavy + n_recent != budget) return NULL;
+        if (r < 1 || budget % r != 0) return NULL;
+        const int nb = budget / r, nsb = (n_sink + r - 1) / r;
+        if ((long long)(nb - nsb - 1) * r < n_recent) return NULL;
     } else {
         return NULL;
     }
@@ -163,6 +172,7 @@ orc_unit *orc_new(int policy, int n_sink, int n_heavy, int n_recent, int budget,
     }
     for (int s = 0; s < u->cap; ++s) u->pos[s] = -1;
     u->last_victim_pos = -1;
+    u->last_block = -1;
     return u;
 }
 
@@ -180,6 +190,7 @@ int orc_cuts(const orc_unit *u) { return u->n_cuts; }
 int orc_greedy_disagreements(const orc_unit *u) { return u->greedy_disagreements; }
 double orc_evicted_mass(const orc_unit *u) { return u->evicted_mass; }
 int32_t orc_last_victim_pos(const orc_unit *u) { return u->last_victim_pos; }
+int orc_last_block(const orc_unit *u) { return u->last_block; }
 double orc_new_score(const orc_unit *u) { return u->score_new; }
 
 void orc_positions(const orc_unit *u, int32_t *dst) { memcpy(dst, u->pos, sizeof(int32_t) * (size_t)u->cap); }
@@ -216,9 +227,61 @@ static int first_free_slot(const orc_unit *u)
 /* tokens plus the new token itself, and the cumulative-score update.        */
 /* ------------------------------------------------------------------------ */
 
+/* Block-granular H2O ("Attention Sinks 与 KV Cache 淘汰策略" section 5: a paged
+ * cache releases whole blocks, and the block that matters least goes first).
+ * The slots form blocks of r consecutive slots. When a token needs a slot and
+ * the cache is full, one block is released before that token attends: among
+ * the blocks whose tokens all lie outside the sinks and the recent window
+ * (n_sink <= pos <= p - n_recent, p the incoming token's position), the block
+ * B that leaves the remaining set with the highest cumulative score F(T \ B)
+ * = F(T) - sum of B's scores; ties go to the lower sum, then to the block
+ * holding the oldest token. Its slots become free; the incoming token and the
+ * next ones take them lowest first. */
+static int release_block(orc_unit *u, int32_t p)
+{
+    const int bs = u->r, nb = u->cap / bs;
+    double total = 0.0;
+    for (int s = 0; s < u->cap; ++s)
+        if (u->pos[s] >= 0) total += u->score[s];
+    int best = -1, am = -1;
+    double best_F = -INFINITY, best_sum = 0.0, am_sum = 0.0;
+    int32_t best_min = 0, am_min = 0;
+    for (int b = 0; b < nb; ++b) {
+        double sum = 0.0;
+        int32_t mn = INT32_MAX, mx = -1;
+        int full = 1;
+        for (int s = b * bs; s < (b + 1) * bs; ++s) {
+            if (u->pos[s] < 0) { full = 0; break; }
+            sum += u->score[s];
+            if (u->pos[s] < mn) mn = u->pos[s];
+            if (u->pos[s] > mx) mx = u->pos[s];
+        }
+        if (!full || mn < u->n_sink || mx > p - u->n_recent) continue;
+        const double F = total - sum;
+        if (best < 0 || F > best_F || (F == best_F && (sum < best_sum || (sum == best_sum && mn < best_min)))) {
+            best = b; best_F = F; best_sum = sum; best_min = mn;
+        }
+        if (am < 0 || sum < am_sum || (sum == am_sum && mn < am_min)) { am = b; am_sum = sum; am_min = mn; }
+    }
+    if (best < 0) return ORC_ECAPACITY;
+    if (am != best) u->greedy_disagreements++;
+    for (int s = best * bs; s < (best + 1) * bs; ++s) {
+        u->evicted_mass += u->score[s];
+        u->pos[s] = -1;
+        u->score[s] = 0.0;
+    }
+    u->last_block = best;
+    return ORC_OK;
+}
+
 int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_new, double *out)
 {
     if (u->have_new) return ORC_ESTATE;
+    u->last_block = -1;
+    if (u->policy == ORC_H2O_BLOCK && orc_count(u) == u->cap) {
+        int rc = release_block(u, u->prompt_len + u->t);
+        if (rc) return rc;
+    }
     const int G = u->G, d = u->d, cap = u->cap;
     const double scale = 1.0 / sqrt((double)d);
     memcpy(u->k_new, k_new, sizeof(float) * (size_t)d);
@@ -265,7 +328,7 @@ int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_n
     /* H2O: every retained token's cumulative score grows by this step's
      * probability (mean over the unit's G query heads); the new token starts
      * with its own. Sink-window and Random keep no scores. */
-    if (u->policy == ORC_H2O) {
+    if (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK) {
         for (int s = 0; s < cap; ++s)
             if (u->pos[s] >= 0) u->score[s] += mass[s] / (double)G;
         u->score_new = mass[cap] / (double)G;
@@ -285,7 +348,7 @@ int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_n
 int orc_stage(orc_unit *u, const float *k_new, const float *v_new)
 {
     if (u->have_new) return ORC_ESTATE;
-    if (u->policy == ORC_H2O) return ORC_EINVAL;
+    if (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK) return ORC_EINVAL;
     memcpy(u->k_new, k_new, sizeof(float) * (size_t)u->d);
     memcpy(u->v_new, v_new, sizeof(float) * (size_t)u->d);
     u->new_pos = u->prompt_len + u->t;
@@ -302,6 +365,11 @@ static int stage_prompt_token(orc_unit *u, const float *k, const float *v)
     if (u->have_new) return ORC_ESTATE;
     if (u->t > 0) return ORC_ESTATE;
     if (u->policy == ORC_RANDOM && u->prompt_len >= u->max_prompt) return ORC_ECAPACITY;
+    u->last_block = -1;
+    if (u->policy == ORC_H2O_BLOCK && orc_count(u) == u->cap) {
+        int rc = release_block(u, u->prompt_len);
+        if (rc) return rc;
+    }
     memcpy(u->k_new, k, sizeof(float) * (size_t)u->d);
     memcpy(u->v_new, v, sizeof(float) * (size_t)u->d);
     u->new_pos = u->prompt_len;
@@ -375,7 +443,7 @@ int orc_choose(orc_unit *u)
     switch (u->policy) {
     case ORC_H2O: return choose_h2o(u);
     case ORC_SINK_WINDOW: return choose_sink_window(u);
-    default: return first_free_slot(u); /* Random: the lowest free slot */
+    default: return first_free_slot(u); /* Random, H2O_BLOCK: the lowest free slot */
     }
 }
 
@@ -417,7 +485,7 @@ int orc_commit(orc_unit *u, int slot)
     if (!u->have_new) return ORC_ESTATE;
     if (slot < 0 || slot >= u->cap) return ORC_EINVAL;
     u->last_victim_pos = u->pos[slot];
-    if (u->pos[slot] >= 0 && u->policy == ORC_H2O) u->evicted_mass += u->score[slot];
+    if (u->pos[slot] >= 0 && (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK)) u->evicted_mass += u->score[slot];
     u->pos[slot] = u->new_pos;
     memcpy(u->k + (size_t)slot * u->d, u->k_new, sizeof(float) * (size_t)u->d);
     memcpy(u->v + (size_t)slot * u->d, u->v_new, sizeof(float) * (size_t)u->d);
