@@ -253,7 +253,8 @@ def run_ours(args, w, rank, world, device):
             pass
         elif w.policy == configs.POLICY_RANDOM:  # pass the first cut
             n_pre = w.budget + w.r
-        elif w.policy == configs.POLICY_H2O and P < w.capacity:  # fill the cache: every timed step evicts
+        elif w.policy in (configs.POLICY_H2O, configs.POLICY_H2O_BLOCK) and P < w.capacity:
+            # fill the cache: every timed step evicts (H2O_BLOCK: releases a block every r steps)
             n_pre = w.capacity - P
         n_win = args.warmup + args.steps
         q, kn, vn = synth.device_window(w, P + n_pre, n_win, device)

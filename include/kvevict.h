@@ -60,7 +60,8 @@ typedef struct kvevict_handle *kvevict_t;
 typedef enum {
     KVEVICT_H2O = 0,          /* sink + heavy hitters + recent window */
     KVEVICT_SINK_WINDOW = 1,  /* StreamingLLM: sink + ring window, no scores */
-    KVEVICT_RANDOM = 2        /* Random Attention: prompt kept, periodic random cut */
+    KVEVICT_RANDOM = 2,       /* Random Attention: prompt kept, periodic random cut */
+    KVEVICT_H2O_BLOCK = 3     /* H2O scores, whole blocks of r slots released at a time */
 } kvevict_policy;
 
 typedef enum { KVEVICT_F32 = 0, KVEVICT_BF16 = 1 } kvevict_dtype;
@@ -90,11 +91,22 @@ typedef enum {
  *     RANDOM:      budget K = generated tokens kept after a cut, r >= 1 the
  *                  buffer/period, K + r <= 8192; n_sink = n_heavy =
  *                  n_recent = 0; seed keys the Philox4x64-10 draws.
+ *     H2O_BLOCK:   as H2O, with r >= 1 the block size: the slots form blocks
+ *                  of r consecutive slots, budget a multiple of r, and at
+ *                  least one block besides those holding sinks lies outside
+ *                  the recent window ((budget / r - ceil(n_sink / r) - 1) r
+ *                  >= n_recent). When a token needs a slot and the cache is
+ *                  full, the block wholly outside the sinks and the recent
+ *                  window (n_sink <= pos <= p - n_recent) with the smallest
+ *                  (sum of cumulative scores, oldest position) is released
+ *                  before the token attends ("Attention Sinks 与 KV Cache 淘汰
+ *                  策略" section 5: a paged cache frees whole blocks); the token
+ *                  and the next r - 1 fill its slots in order.
  *   batch, n_layers, n_q_heads, n_kv_heads, head_dim: model shape;
  *     n_q_heads / n_kv_heads = G in {1, 2, 4, 8}; head_dim in {64, 128}.
  *   dtype: KVEVICT_F32 or KVEVICT_BF16 for K, V, q and out.
  *   max_prompt: RANDOM only, the longest prompt a unit may hold.
- * Slot capacity per unit: C = budget (H2O, SINK_WINDOW) or
+ * Slot capacity per unit: C = budget (H2O, SINK_WINDOW, H2O_BLOCK) or
  * max_prompt + budget + r (RANDOM).
  */
 typedef struct {
@@ -110,7 +122,7 @@ typedef struct {
     int64_t decode_steps;   /* layer-steps issued (one per kvevict_decode_step call) */
     int64_t prefill_tokens; /* prompt tokens appended, summed over layers */
     int64_t evictions;      /* tokens evicted, summed over units and layers */
-    int64_t cuts;           /* Random cuts, summed over layers (each cuts every unit of the layer) */
+    int64_t cuts;           /* Random cuts or H2O_BLOCK releases, summed over layers (each over every unit) */
     int split;              /* CTAs per unit in the decode launch (thread-block cluster size) */
     int capacity;           /* slots per unit */
     int clusters;           /* clusters in the last decode launch's persistent grid (0 before any) */

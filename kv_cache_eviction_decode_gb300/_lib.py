@@ -11,7 +11,7 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvevict.so")
 
-H2O, SINK_WINDOW, RANDOM = 0, 1, 2
+H2O, SINK_WINDOW, RANDOM, H2O_BLOCK = 0, 1, 2, 3
 F32, BF16 = 0, 1
 
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_STATE, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5

@@ -31,6 +31,9 @@ constexpr int kSMs = 152;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Policies that keep cumulative attention scores.
+bool scored(int policy) { return policy == KVEVICT_H2O || policy == KVEVICT_H2O_BLOCK; }
+
 struct Layout {
     int C = 0, G = 0, elem = 0;
     int Cs = 0;               // per-unit stride of pos/score: C rounded up to 4 (16-byte rows)
@@ -67,6 +70,16 @@ int validate(const kvevict_config *c)
             static_cast<long long>(c->n_sink) + c->n_recent != c->budget)
             return KVEVICT_ERR_INVALID_ARG;
         break;
+    case KVEVICT_H2O_BLOCK:
+        if (c->n_sink < 0 || c->n_heavy < 0 || c->n_recent < 1 ||
+            static_cast<long long>(c->n_sink) + c->n_heavy + c->n_recent != c->budget)
+            return KVEVICT_ERR_INVALID_ARG;
+        if (c->r < 1 || c->budget % c->r != 0) return KVEVICT_ERR_INVALID_ARG;
+        {
+            const long long nb = c->budget / c->r, nsb = (static_cast<long long>(c->n_sink) + c->r - 1) / c->r;
+            if ((nb - nsb - 1) * c->r < c->n_recent) return KVEVICT_ERR_INVALID_ARG;
+        }
+        break;
     case KVEVICT_RANDOM:
         if (c->r < 1 || c->max_prompt < 0 || c->n_sink != 0 || c->n_heavy != 0 || c->n_recent != 0)
             return KVEVICT_ERR_INVALID_ARG;
@@ -97,8 +110,9 @@ Layout make_layout(const kvevict_config *c)
     L.off_k = off; off = align_up(off + nl * L.kv_layer_bytes);
     L.off_v = off; off = align_up(off + nl * L.kv_layer_bytes);
     L.off_pos = off; off = align_up(off + nl * L.layer_pslots * 4);
-    L.off_score = off; if (c->policy == KVEVICT_H2O) off = align_up(off + nl * L.layer_pslots * 4);
-    L.off_free = off; if (c->policy == KVEVICT_RANDOM) off = align_up(off + nl * L.units * c->r * 4);
+    L.off_score = off; if (scored(c->policy)) off = align_up(off + nl * L.layer_pslots * 4);
+    L.off_free = off;
+    if (c->policy == KVEVICT_RANDOM || c->policy == KVEVICT_H2O_BLOCK) off = align_up(off + nl * L.units * c->r * 4);
     L.off_err = off; off = align_up(off + 16);
     L.q_bytes = static_cast<size_t>(c->batch) * c->n_q_heads * c->head_dim * L.elem;
     L.kvtok_bytes = L.units * c->head_dim * L.elem;
@@ -120,6 +134,9 @@ struct LayerState {
     int32_t *trace = nullptr;
     int trace_len = 0, trace_t = 0;
     int fill_left = 0;   // H2O after a SnapKV prefill: steps left in which a unit may still have empty slots
+    int blk_left = 0;    // H2O_BLOCK: slots of the open (released) block not yet refilled
+    int blk_next = 0;    // H2O_BLOCK: next slot of the open block when every unit's is the same
+    bool blk_uniform = false;  // H2O_BLOCK: the open block is the same slot range in every unit
 };
 
 }  // namespace
@@ -166,7 +183,7 @@ int max_slots_per_cta(const Layout &L, int S)
     return ((tiles + S - 1) / S) * kTile;
 }
 
-int n_aux_arrays(const kvevict_config &c, bool holes) { return c.policy == KVEVICT_H2O ? 2 : (holes ? 1 : 0); }
+int n_aux_arrays(const kvevict_config &c, bool holes) { return scored(c.policy) ? 2 : (holes ? 1 : 0); }
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
@@ -316,8 +333,10 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     P.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
     P.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
     P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
-    P.score = c.policy == KVEVICT_H2O ? at<float>(h, L.off_score) + layer * L.layer_pslots : nullptr;
-    P.freelist = c.policy == KVEVICT_RANDOM ? at<int32_t>(h, L.off_free) + layer * L.units * c.r : nullptr;
+    P.score = scored(c.policy) ? at<float>(h, L.off_score) + layer * L.layer_pslots : nullptr;
+    P.freelist = (c.policy == KVEVICT_RANDOM || c.policy == KVEVICT_H2O_BLOCK)
+                     ? at<int32_t>(h, L.off_free) + layer * L.units * c.r
+                     : nullptr;
     P.units = static_cast<int>(L.units);
     P.cstride = L.Cs;
     P.freelist_len = c.r;
@@ -331,7 +350,48 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
 
     bool holes = false;
     long long evicted = 0;
+    bool released = false;  // H2O_BLOCK: a block was released for this token
     switch (c.policy) {
+    case KVEVICT_H2O_BLOCK:
+        if (ls.count < L.C) {  // the cache is still filling
+            P.n_active = ls.count;
+            P.mode = kInsertAt;
+            P.dest_slot = ls.count;
+        } else {
+            P.n_active = L.C;
+            holes = true;
+            if (ls.blk_left == 0) {  // full: release a block before this token attends
+                BlockReleaseParams bp{};
+                bp.pos = P.pos;
+                bp.score = P.score;
+                bp.freelist = const_cast<int32_t *>(P.freelist);
+                bp.kc = P.kc;
+                bp.vc = P.vc;
+                bp.row_bytes = c.head_dim * L.elem;
+                bp.C = L.C;
+                bp.cstride = L.Cs;
+                bp.bs = c.r;
+                bp.n_sink = c.n_sink;
+                bp.n_recent = c.n_recent;
+                bp.p = P.p;
+                bp.err = P.err;
+                int rc0 = cuda_status(launch_block_release(bp, static_cast<int>(L.units), h->stream));
+                if (rc0) return rc0;
+                h->last_layer = layer;  // the release wrote this layer: no early prefetch
+                released = true;
+                evicted = static_cast<long long>(L.units) * c.r;
+                h->stats.cuts++;
+                P.mode = kFromFreeList;
+                P.freelist_idx = 0;
+            } else if (ls.blk_uniform) {
+                P.mode = kInsertAt;
+                P.dest_slot = ls.blk_next;
+            } else {
+                P.mode = kFromFreeList;
+                P.freelist_idx = c.r - ls.blk_left;
+            }
+        }
+        break;
     case KVEVICT_SINK_WINDOW:
         P.n_active = ls.count;
         P.mode = kInsertAt;
@@ -419,6 +479,17 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
         ls.count = std::min(L.C, ls.count + 1);
         if (ls.fill_left > 0) ls.fill_left--;
         break;
+    case KVEVICT_H2O_BLOCK:
+        if (ls.count < L.C) {
+            ls.count++;
+        } else if (released) {
+            ls.blk_left = c.r - 1;
+            ls.blk_uniform = false;
+        } else {
+            ls.blk_left--;
+            ls.blk_next++;
+        }
+        break;
     default:
         ls.n_gen++;
         if (ls.cut_done) ls.fl_idx++;
@@ -501,7 +572,7 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
     // position -1, every score 0, no error bits.
     cudaError_t e = cudaMemsetAsync(h->state + L.off_k, 0, L.off_pos - L.off_k, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_pslots * 4, h->stream);
-    if (e == cudaSuccess && cfg->policy == KVEVICT_H2O)
+    if (e == cudaSuccess && scored(cfg->policy))
         e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_pslots * 4, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
     if (e != cudaSuccess) {
@@ -532,7 +603,7 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
     P.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
     P.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
     P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
-    P.score = c.policy == KVEVICT_H2O ? at<float>(h, L.off_score) + layer * L.layer_pslots : nullptr;
+    P.score = scored(c.policy) ? at<float>(h, L.off_score) + layer * L.layer_pslots : nullptr;
     P.n_tok = n_tokens;
     P.p0 = ls.prompt_len;
     P.C = L.C;
@@ -553,6 +624,40 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
         P.b0 = std::max({0, c.n_sink - P.p0, n_tokens - P.ring_len});
         P.b1 = n_tokens;
         if (P.b0 > P.b1) P.b0 = P.b1;
+    }
+    if (c.policy == KVEVICT_H2O_BLOCK) {
+        // the whole prompt in one call: the closed-form layout covers it
+        if (ls.prompt_len != 0) return KVEVICT_ERR_STATE;
+        BlockPrefillParams bp{};
+        bp.K = K;
+        bp.V = V;
+        bp.kc = P.kc;
+        bp.vc = P.vc;
+        bp.pos = P.pos;
+        bp.score = P.score;
+        bp.n_tok = n_tokens;
+        bp.C = L.C;
+        bp.cstride = L.Cs;
+        bp.Hkv = c.n_kv_heads;
+        bp.row_bytes = c.head_dim * L.elem;
+        bp.bs = c.r;
+        bp.nsb = (c.n_sink + c.r - 1) / c.r;
+        launch_block_prefill(bp, c.batch, h->stream);
+        int rc = cuda_status(cudaGetLastError());
+        if (rc) return rc;
+        h->last_layer = layer;
+        ls.prompt_len = n_tokens;
+        ls.count = std::min(L.C, n_tokens);
+        ls.blk_left = 0;
+        if (n_tokens > L.C && (n_tokens - L.C) % c.r) {  // the last released block is partly refilled
+            const int nb = L.C / c.r, released = (n_tokens - L.C + c.r - 1) / c.r;
+            const int blk = bp.nsb + (released - 1) % (nb - bp.nsb);
+            ls.blk_next = blk * c.r + (n_tokens - L.C) % c.r;
+            ls.blk_left = c.r - (n_tokens - L.C) % c.r;
+            ls.blk_uniform = true;
+        }
+        h->stats.prefill_tokens += n_tokens;
+        return KVEVICT_OK;
     }
     launch_prefill(P, (P.a1 - P.a0) + (P.b1 - P.b0), c.batch, h->stream);
     int rc = cuda_status(cudaGetLastError());
@@ -836,7 +941,7 @@ int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_devi
 int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
 {
     if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
-    if (h->cfg.policy != KVEVICT_H2O) return KVEVICT_ERR_INVALID_ARG;
+    if (!scored(h->cfg.policy)) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     const Layout &L = h->L;
     const void *src = at<float>(h, L.off_score) + layer * L.layer_pslots;

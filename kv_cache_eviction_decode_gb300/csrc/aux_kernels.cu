@@ -1,4 +1,6 @@
 // aux_kernels.cu -- prompt prefill and the Random Attention periodic cut.
+#include <climits>
+
 #include "aux_kernels.h"
 #include "device_common.cuh"
 
@@ -113,6 +115,149 @@ __global__ void __launch_bounds__(kCutThreads) random_cut_kernel(const CutParams
         reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.kc) + row * P.row_bytes)[i % vecs] = make_uint4(0, 0, 0, 0);
         reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.vc) + row * P.row_bytes)[i % vecs] = make_uint4(0, 0, 0, 0);
     }
+}
+
+// ------------------------------------------------- block-granular H2O
+// Prompt admission for block-granular H2O ("Attention Sinks 与 KV Cache 淘汰
+// 策略" section 5: whole blocks are released). Every prompt token enters with
+// score 0, so when the cache is full the released block is the eligible one
+// holding the oldest token: the blocks holding sinks never leave and the
+// others are released round robin, each refilled by the next bs positions.
+// Slot-centric: one warp per slot works out which position the slot holds
+// at the end of the prompt (or none: the unfilled rest of the block released
+// last) and copies its row.
+__global__ void __launch_bounds__(256) prefill_block_kernel(const BlockPrefillParams P)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = blockIdx.x * 8 + warp;
+    if (s >= P.C) return;
+    const size_t unit = static_cast<size_t>(blockIdx.z) * P.Hkv + blockIdx.y;
+    const int b = s / P.bs, o = s - b * P.bs, nb = P.C / P.bs;
+    int src;
+    if (P.n_tok <= P.C || b < P.nsb) {
+        src = s < P.n_tok ? s : -1;
+    } else {
+        const int released = (P.n_tok - P.C + P.bs - 1) / P.bs;  // releases so far
+        const int nr = nb - P.nsb, idx = b - P.nsb;
+        if (released - 1 < idx) {
+            src = s;  // never released: the original prompt position
+        } else {
+            const int last = idx + nr * ((released - 1 - idx) / nr);  // its last release (0-based)
+            src = P.C + last * P.bs + o;
+            if (src >= P.n_tok) src = -1;
+        }
+    }
+    const int vecs = P.row_bytes / 16;
+    uint4 *kd = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.kc) + (unit * P.C + s) * P.row_bytes);
+    uint4 *vd = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.vc) + (unit * P.C + s) * P.row_bytes);
+    const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.K) +
+                                                      (unit * P.n_tok + (src < 0 ? 0 : src)) * P.row_bytes);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.V) +
+                                                      (unit * P.n_tok + (src < 0 ? 0 : src)) * P.row_bytes);
+    for (int v = lane; v < vecs; v += 32) {
+        kd[v] = src < 0 ? make_uint4(0, 0, 0, 0) : ks[v];
+        vd[v] = src < 0 ? make_uint4(0, 0, 0, 0) : vs[v];
+    }
+    if (lane == 0) {
+        P.pos[unit * P.cstride + s] = src;
+        P.score[unit * P.cstride + s] = 0.f;
+    }
+}
+
+// The release: among the blocks of bs consecutive slots whose tokens all lie
+// outside the sinks and the recent window (n_sink <= pos <= p - n_recent), the
+// one with the smallest (sum of scores, oldest position) leaves -- the block
+// whose removal keeps the highest remaining cumulative score. Its slots are
+// emptied (position -1, score 0, K/V rows zeroed so that every row a tile may
+// touch is finite) and listed, ascending, in the unit's free list, which the
+// next bs decode steps fill. One CTA per unit.
+__global__ void __launch_bounds__(256) block_release_kernel(const BlockReleaseParams P)
+{
+    __shared__ uint64_t wkey[8];
+    __shared__ int32_t wblk[8];
+    __shared__ int32_t chosen;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t unit = blockIdx.x;
+    const int32_t *pos = P.pos + unit * P.cstride;
+    const float *sc = P.score + unit * P.cstride;
+    const int nb = P.C / P.bs;
+    uint64_t best = ~0ull;
+    int32_t bblk = -1;
+    for (int b = tid; b < nb; b += blockDim.x) {
+        float sum = 0.f;
+        int32_t mn = INT_MAX, mx = -1;
+        bool full = true;
+        for (int o = 0; o < P.bs; ++o) {
+            const int32_t ps = pos[b * P.bs + o];
+            if (ps < 0) {
+                full = false;
+                break;
+            }
+            sum += sc[b * P.bs + o];
+            mn = min(mn, ps);
+            mx = max(mx, ps);
+        }
+        if (!full || mn < P.n_sink || mx > P.p - P.n_recent) continue;
+        const uint64_t key = (static_cast<uint64_t>(__float_as_uint(sum)) << 32) | static_cast<uint32_t>(mn);
+        if (key < best) {
+            best = key;
+            bblk = b;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const uint64_t ok = __shfl_xor_sync(0xffffffffu, best, off);
+        const int32_t ob = __shfl_xor_sync(0xffffffffu, bblk, off);
+        if (ok < best) {
+            best = ok;
+            bblk = ob;
+        }
+    }
+    if (lane == 0) {
+        wkey[warp] = best;
+        wblk[warp] = bblk;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint64_t k = ~0ull;
+        int32_t bk = -1;
+        for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w)
+            if (wkey[w] < k) {
+                k = wkey[w];
+                bk = wblk[w];
+            }
+        chosen = bk;
+        if (bk < 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+    }
+    __syncthreads();
+    const int blk = chosen;
+    int32_t *posw = P.pos + unit * P.cstride;
+    for (int o = tid; o < P.bs; o += blockDim.x) {
+        P.freelist[unit * P.bs + o] = blk < 0 ? -1 : blk * P.bs + o;  // -1: the decode step drops its token
+        if (blk >= 0) {
+            posw[blk * P.bs + o] = -1;
+            P.score[unit * P.cstride + blk * P.bs + o] = 0.f;
+        }
+    }
+    if (blk < 0) return;
+    const int vecs = P.row_bytes / 16;
+    for (int i = tid; i < P.bs * vecs; i += blockDim.x) {
+        const size_t row = unit * P.C + blk * P.bs + i / vecs;
+        reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.kc) + row * P.row_bytes)[i % vecs] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4 *>(static_cast<uint8_t *>(P.vc) + row * P.row_bytes)[i % vecs] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+void launch_block_prefill(const BlockPrefillParams &p, int B, cudaStream_t st)
+{
+    dim3 grid((p.C + 7) / 8, p.Hkv, B);
+    prefill_block_kernel<<<grid, 256, 0, st>>>(p);
+}
+
+cudaError_t launch_block_release(const BlockReleaseParams &p, int units, cudaStream_t st)
+{
+    block_release_kernel<<<units, 256, 0, st>>>(p);
+    return cudaGetLastError();
 }
 
 void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st)

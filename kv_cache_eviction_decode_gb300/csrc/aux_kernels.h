@@ -30,7 +30,31 @@ struct CutParams {
     int first_slot, n_cand, n_pow2, r;
 };
 
+// Block-granular H2O prefill: the slot-centric closed form of admitting the
+// prompt one token at a time with score 0 (see prefill_block_kernel).
+struct BlockPrefillParams {
+    const void *K, *V;  // [B][Hkv][n_tok][D]
+    void *kc, *vc;      // layer cache [B][Hkv][C][D]
+    int32_t *pos;       // [B][Hkv][cstride]
+    float *score;
+    int n_tok, C, cstride, Hkv, row_bytes;
+    int bs, nsb;        // block size, blocks holding sinks
+};
+
+// Block-granular H2O release: frees one block per unit and lists its slots.
+struct BlockReleaseParams {
+    int32_t *pos;       // layer [B][Hkv][cstride]
+    float *score;
+    int32_t *freelist;  // layer [B][Hkv][bs]
+    void *kc, *vc;      // layer cache [B][Hkv][C][D]: freed rows are zeroed
+    int row_bytes, C, cstride, bs;
+    int n_sink, n_recent, p;  // p: position of the token the release makes room for
+    uint32_t *err;
+};
+
 void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st);
+void launch_block_prefill(const BlockPrefillParams &p, int B, cudaStream_t st);
+cudaError_t launch_block_release(const BlockReleaseParams &p, int units, cudaStream_t st);
 size_t cut_smem_bytes(int n_pow2, int r);
 cudaError_t launch_random_cut(const CutParams &p, int B, cudaStream_t st);
 

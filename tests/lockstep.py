@@ -24,11 +24,16 @@ import torch
 import oracle
 from kv_cache_eviction_decode_gb300 import KVEvictCache
 from workloads import synth
-from workloads.configs import DTYPE_BF16, POLICY_H2O, POLICY_RANDOM, Workload
+from workloads.configs import DTYPE_BF16, POLICY_H2O, POLICY_H2O_BLOCK, POLICY_RANDOM, Workload
 
 NEAR_TIE_REL = 1e-5
 BF16_REL_TOL = 2e-2
 F32_ABS_TOL = 1e-4
+
+
+def scored(w: Workload) -> bool:
+    """Policies whose retained set depends on cumulative attention scores."""
+    return w.policy in (POLICY_H2O, POLICY_H2O_BLOCK)
 
 
 def torch_dtype(w: Workload):
@@ -96,7 +101,7 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
         cache.set_trace(layer, trace)
         run.pos_snap[layer] = {-1: cache.slot_positions(layer).cpu()}
         run.score_snap[layer] = {}
-        if w.policy == POLICY_H2O:
+        if scored(w):
             run.score_snap[layer][-1] = cache.scores(layer).cpu()
         seqs = out_seqs if out_seqs is not None else sorted({u[0] for u in mine})
         bufs[layer] = (q, k, v, out, trace, seqs)
@@ -106,7 +111,7 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
         cache.decode_step(layer, q[t], k[t], v[t], out[t])
         if t in snap_steps:
             run.pos_snap[layer][t] = cache.slot_positions(layer).cpu()
-            if w.policy == POLICY_H2O:
+            if scored(w):
                 run.score_snap[layer][t] = cache.scores(layer).cpu()
 
     if interleave:
@@ -172,7 +177,7 @@ def replay_unit(w: Workload, unit, x, run: GpuRun, n_steps: int, out_steps=None,
     zero = np.zeros(w.head_dim, np.float32)
     for t in range(n_steps):
         want_out = x is not None and (out_steps is None or t in out_steps)
-        if w.policy == POLICY_H2O or want_out:
+        if scored(w) or want_out:
             ref = u.attend(x.q[t], x.k_new[t], x.v_new[t])
             if want_out:
                 got = run.out[layer][seq][t, h * G:(h + 1) * G]

@@ -17,11 +17,13 @@ from dataclasses import dataclass, replace
 POLICY_H2O = 0
 POLICY_SINK_WINDOW = 1
 POLICY_RANDOM = 2
+POLICY_H2O_BLOCK = 3
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
 
-POLICY_NAMES = {POLICY_H2O: "h2o", POLICY_SINK_WINDOW: "sink_window", POLICY_RANDOM: "random"}
+POLICY_NAMES = {POLICY_H2O: "h2o", POLICY_SINK_WINDOW: "sink_window", POLICY_RANDOM: "random",
+                POLICY_H2O_BLOCK: "h2o_block"}
 
 
 @dataclass(frozen=True)
@@ -113,7 +115,13 @@ H2O_REASONING = Workload(
     n_sink=8192, n_heavy=1024, n_recent=1024, budget=10240, r=0,
     prompt_len=8192, decode_steps=32768, seed=2029)
 
-ALL = {w.name: w for w in (H2O_TINY, SINK_WINDOW, H2O_MHA, H2O_GQA, RANDOM_REASONING, H2O_REASONING)}
+# Block-granular H2O on the MHA shape: blocks of 16 slots (a PagedAttention
+# block) and of 256; r is the block size.
+H2O_BLOCK16 = H2O_MHA.with_(name="h2o_block16_bf16_b16_l32_h32_d128_k1024", policy=POLICY_H2O_BLOCK, r=16)
+H2O_BLOCK256 = H2O_MHA.with_(name="h2o_block256_bf16_b16_l32_h32_d128_k1024", policy=POLICY_H2O_BLOCK, r=256)
+
+ALL = {w.name: w for w in (H2O_TINY, SINK_WINDOW, H2O_MHA, H2O_GQA, RANDOM_REASONING, H2O_REASONING, H2O_BLOCK16,
+                           H2O_BLOCK256)}
 
 # Short names used on command lines.
 ALIASES = {
@@ -123,6 +131,8 @@ ALIASES = {
     "h2o_gqa": H2O_GQA.name,
     "random": RANDOM_REASONING.name,
     "h2o_reasoning": H2O_REASONING.name,
+    "h2o_block16": H2O_BLOCK16.name,
+    "h2o_block256": H2O_BLOCK256.name,
 }
 
 

@@ -17,7 +17,7 @@ head_dim * bytes per element * tokens.
 """
 from __future__ import annotations
 
-from .configs import POLICY_H2O, POLICY_RANDOM, Workload
+from .configs import POLICY_H2O, POLICY_H2O_BLOCK, POLICY_RANDOM, Workload
 
 
 def kv_cache_bytes(n_layers: int, n_kv_heads: int, head_dim: int, elem_bytes: int, tokens: int) -> int:
@@ -31,7 +31,7 @@ def score_bytes(tokens: int, score_elem_bytes: int = 4) -> int:
 def unit_step_bytes(w: Workload, n_retained: int, n_slots: int | None = None, cut: bool = False) -> int:
     d, e, G = w.head_dim, w.elem_bytes, w.group
     b = (n_retained + 1) * 2 * d * e + 2 * d * e + 2 * G * d * e
-    if w.policy == POLICY_H2O:
+    if w.policy in (POLICY_H2O, POLICY_H2O_BLOCK):
         b += 8 * n_retained + 8
     if w.policy == POLICY_RANDOM:
         b += 4 * (n_slots if n_slots is not None else w.capacity)
@@ -49,4 +49,13 @@ def steady_layer_step_bytes(w: Workload) -> int:
         per = unit_step_bytes(w, int(round(n_ret)), w.prompt_len + w.budget + w.r)
         cut_extra = (4 * (w.budget + w.r) + 4 * w.r) / w.r
         return int(units * (per + cut_extra))
+    if w.policy == POLICY_H2O_BLOCK:
+        # a release every r steps empties a block of r slots that the next r
+        # tokens refill: on average C - (r + 1) / 2 tokens are attended; the
+        # release reads every slot's position and score and writes r slots
+        # (position, score, zeroed K/V rows, free-list entry)
+        bs, d, e = w.r, w.head_dim, w.elem_bytes
+        n_ret = w.capacity - (bs + 1) / 2.0
+        release = 8 * w.capacity + bs * (8 + 2 * d * e + 4)
+        return int(units * (unit_step_bytes(w, int(round(n_ret))) + release / bs))
     return units * unit_step_bytes(w, w.capacity)
