@@ -80,6 +80,10 @@ def lib():
             L.orc_prefill_snapkv.restype = I
             L.orc_prompt_tail_scores.argtypes = [P, P, I, I, I, I, P]
             L.orc_prompt_tail_scores.restype = I
+            L.orc_set_score_storage.argtypes = [P, ctypes.c_double, I]
+            L.orc_set_score_storage.restype = I
+            L.orc_round_half.argtypes = [ctypes.c_double]
+            L.orc_round_half.restype = ctypes.c_double
             L.orc_step.argtypes = [P, P, P, P, P]
             L.orc_step.restype = I
             L.orc_run.argtypes = [P, I, I, P, P, P, P, I]
@@ -130,6 +134,11 @@ class Unit:
         rc = self._L.orc_prefill(self.h, _ptr(k), _ptr(v), k.shape[0])
         if rc:
             raise RuntimeError(f"oracle prefill failed: {rc}")
+
+    def set_score_storage(self, forget: float = 0.0, half: bool = False) -> None:
+        rc = self._L.orc_set_score_storage(self.h, forget, 1 if half else 0)
+        if rc:
+            raise RuntimeError(f"oracle set_score_storage failed: {rc}")
 
     def prefill_scored(self, q, k, v) -> np.ndarray:
         """Q-seeded prefill of an empty H2O unit: q [G][P][d], k/v [P][d].
@@ -275,6 +284,11 @@ def prompt_tail_scores(q, k, j0: int) -> np.ndarray:
     if rc:
         raise RuntimeError(f"oracle prompt_tail_scores failed: {rc}")
     return out
+
+
+def round_half(x: float) -> float:
+    """The oracle's binary16 rounding of a non-negative value."""
+    return lib().orc_round_half(float(x))
 
 
 def online_cores() -> int:

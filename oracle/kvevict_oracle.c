@@ -83,6 +83,8 @@ typedef struct orc_unit {
     int32_t last_victim_pos; /* position removed by the last commit, -1 if none */
     int greedy_disagreements; /* argmax F(T\{v}) != argmin (score, pos): must stay 0 */
     int last_block;      /* H2O_BLOCK: block released for the token of the last step, -1 if none */
+    double forget;       /* score storage: s <- (1 - forget) s + a each step (0: exact accumulation) */
+    int half;            /* score storage: every stored score rounded to IEEE binary16 */
 } orc_unit;
 
 /* ------------------------------------------------------------------------ */
@@ -130,6 +132,25 @@ uint64_t orc_random_key(uint64_t seed, int seq, int layer, int head, int step, i
 }
 
 /* ------------------------------------------------------------------------ */
+/* IEEE 754 binary16 rounding (round to nearest, ties to even).               */
+/* ------------------------------------------------------------------------ */
+
+/* The binary16 value nearest to x (x >= 0, finite): 11 significant bits for
+ * normal values (x >= 2^-14), a fixed spacing of 2^-24 below, +inf from
+ * 65520 on (the halfway point past the largest finite value, 65504). */
+double orc_round_half(double x)
+{
+    if (!(x > 0.0)) return x == 0.0 ? 0.0 : x;
+    if (x >= 65520.0) return INFINITY;
+    int e;
+    frexp(x, &e);                       /* x = f 2^e, f in [0.5, 1): 2^(e-1) <= x < 2^e */
+    int q = e - 1 - 10;                 /* the spacing 2^q of 11-bit significands at x */
+    if (q < -24) q = -24;               /* subnormal range */
+    const double ulp = ldexp(1.0, q);
+    return nearbyint(x / ulp) * ulp;    /* default rounding mode: ties to even */
+}
+
+/* ------------------------------------------------------------------------ */
 /* Unit lifetime.                                                            */
 /* ------------------------------------------------------------------------ */
 
@@ -174,6 +195,23 @@ orc_unit *orc_new(int policy, int n_sink, int n_heavy, int n_recent, int budget,
     u->last_victim_pos = -1;
     u->last_block = -1;
     return u;
+}
+
+/* Score-storage variants ("Attention Sinks 与 KV Cache 淘汰策略" section 6.2: the
+ * cumulative scores are stored in FP16, or a moving average replaces the exact
+ * accumulation): every step s <- (1 - forget) s + a for each retained token,
+ * with 0 <= forget < 1 (0 is the exact cumulative score), and with half != 0
+ * every stored score (the new token's too) is rounded to binary16 right after
+ * its update. H2O and block H2O only (half: H2O only), on an empty unit. */
+int orc_set_score_storage(orc_unit *u, double forget, int half)
+{
+    if (u->policy != ORC_H2O && u->policy != ORC_H2O_BLOCK) return ORC_EINVAL;
+    if (half && u->policy != ORC_H2O) return ORC_EINVAL;
+    if (!(forget >= 0.0 && forget < 1.0)) return ORC_EINVAL;
+    if (u->prompt_len != 0 || u->t != 0 || u->have_new) return ORC_ESTATE;
+    u->forget = forget;
+    u->half = half != 0;
+    return ORC_OK;
 }
 
 void orc_free(orc_unit *u)
@@ -329,9 +367,13 @@ int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_n
      * probability (mean over the unit's G query heads); the new token starts
      * with its own. Sink-window and Random keep no scores. */
     if (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK) {
-        for (int s = 0; s < cap; ++s)
-            if (u->pos[s] >= 0) u->score[s] += mass[s] / (double)G;
+        for (int s = 0; s < cap; ++s) {
+            if (u->pos[s] < 0) continue;
+            u->score[s] = (1.0 - u->forget) * u->score[s] + mass[s] / (double)G;
+            if (u->half) u->score[s] = orc_round_half(u->score[s]);
+        }
         u->score_new = mass[cap] / (double)G;
+        if (u->half) u->score_new = orc_round_half(u->score_new);
     } else {
         u->score_new = 0.0;
     }

@@ -1,0 +1,142 @@
+"""Pins of the oracle's score-storage variants ("Attention Sinks 与 KV Cache 淘汰
+策略" section 6.2: FP16 storage of the cumulative scores, or a moving average in
+place of the exact accumulation) to things other than itself: the binary16
+rounding against numpy's float16 conversion, the moving average against the
+per-step attention weights of torch's fp64 SDPA weighted by powers of the
+keep factor, FP16 storage against the same recursion rounded by numpy, the
+exact accumulation as the forget = 0 case, and the selection on the stored
+(rounded) scores against brute force (ties are common in FP16).
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import H2O, H2O_BLOCK, SINK_WINDOW, Unit
+
+
+def test_round_half_matches_numpy_float16():
+    rng = np.random.default_rng(3)
+    xs = np.concatenate([rng.uniform(0, 70000, 4000), np.exp(rng.uniform(-25, 11, 4000)),
+                         [0.0, 2.0**-24, 2.0**-25, 3 * 2.0**-25, 2.0**-14, 65504.0, 65519.99, 65520.0, 1e5]])
+    # the exact midpoints between neighbouring binary16 values: ties go to even
+    h = np.arange(0, 0x7BFF, 7, dtype=np.uint16).view(np.float16).astype(np.float64)
+    xs = np.concatenate([xs, (h[:-1] + h[1:]) / 2])
+    for x in xs:
+        with np.errstate(over="ignore"):
+            ref = float(np.float16(x))
+        assert oracle.round_half(float(x)) == ref, x
+
+
+def _sdpa_weights(Q, K, t, P):
+    """Attention of step t's query heads over positions 0..P+t (fp64 SDPA with
+    V = I): [G][P + t + 1]."""
+    import torch
+    import torch.nn.functional as F
+    n = P + t + 1
+    G, d = Q.shape[1], Q.shape[2]
+    q = torch.from_numpy(Q[t].astype(np.float64))[None, :, None, :]
+    k = torch.from_numpy(K[:n].astype(np.float64))[None, None].expand(1, G, n, d)
+    eye = torch.eye(n, dtype=torch.float64)[None, None].expand(1, G, n, n)
+    return F.scaled_dot_product_attention(q, k, eye)[0, :, 0, :].numpy()
+
+
+@pytest.mark.parametrize("forget,half", [(0.0, False), (0.1, False), (0.5, False), (0.0, True), (0.05, True)])
+def test_storage_recursion_against_sdpa(forget, half):
+    rng = np.random.default_rng(60 + int(forget * 100) + half)
+    P, T, G, d = 6, 30, 2, 8
+    n = P + T
+    u = Unit(H2O, 2, n, 3, n + 5, 0, 0, G, d)  # never evicts
+    u.set_score_storage(forget, half)
+    K = rng.standard_normal((n, d)).astype(np.float32)
+    Q = rng.standard_normal((T, G, d)).astype(np.float32)
+    u.prefill(K[:P], K[:P])
+    ref = np.zeros(n)
+    rnd = (lambda x: np.float16(x).astype(np.float64)) if half else (lambda x: x)
+    for t in range(T):
+        u.step(Q[t], K[P + t], K[P + t])
+        w = _sdpa_weights(Q, K, t, P).mean(axis=0)  # [P + t + 1]
+        m = P + t + 1
+        ref[:m - 1] = rnd((1.0 - forget) * ref[:m - 1] + w[:m - 1])
+        ref[m - 1] = rnd(w[m - 1])
+    pos, sc = u.positions(), u.scores()
+    got = np.zeros(n)
+    got[pos[pos >= 0]] = sc[pos >= 0]
+    if half:  # the stored values are binary16 values, equal to the numpy-rounded recursion
+        assert np.all(np.float16(got).astype(np.float64) == got)
+        np.testing.assert_allclose(got, ref, rtol=2.0**-10, atol=2.0**-24)
+    else:
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+    if forget == 0.0 and not half:
+        assert math.fsum(sc[pos >= 0]) == pytest.approx(T, rel=1e-12)
+
+
+def test_forget_zero_is_the_exact_accumulation():
+    rng = np.random.default_rng(8)
+    P, T, G, d = 5, 40, 2, 8
+    a, b = Unit(H2O, 1, 6, 3, 10, 0, 0, G, d), Unit(H2O, 1, 6, 3, 10, 0, 0, G, d)
+    b.set_score_storage(0.0, False)
+    K = rng.standard_normal((P + T, d)).astype(np.float32)
+    Q = rng.standard_normal((T, G, d)).astype(np.float32)
+    a.prefill(K[:P], K[:P])
+    b.prefill(K[:P], K[:P])
+    for t in range(T):
+        a.step(Q[t], K[P + t], K[P + t])
+        b.step(Q[t], K[P + t], K[P + t])
+    np.testing.assert_array_equal(a.positions(), b.positions())
+    np.testing.assert_array_equal(a.scores(), b.scores())
+
+
+@pytest.mark.parametrize("forget", [0.0, 0.2])
+def test_fp16_selection_equals_brute_force_on_stored_scores(forget):
+    rng = np.random.default_rng(70 + int(forget * 10))
+    n_sink, n_heavy, n_recent = 1, 3, 2
+    K_ = n_sink + n_heavy + n_recent
+    P, T, G, d = 3, 40, 2, 4
+    u = Unit(H2O, n_sink, n_heavy, n_recent, K_, 0, 0, G, d)
+    u.set_score_storage(forget, True)
+    Kk = rng.standard_normal((P + T, d)).astype(np.float32)
+    Q = rng.standard_normal((T, G, d)).astype(np.float32)
+    u.prefill(Kk[:P], Kk[:P])
+    ties = 0
+    for t in range(T):
+        p = P + t
+        u.attend(Q[t], Kk[p], Kk[p])
+        pos, sc = u.positions(), u.scores()
+        cand = {int(pos[s]): sc[s] for s in range(K_) if pos[s] >= 0}
+        cand[p] = u.new_score
+        slot = u.choose()
+        u.commit(slot)
+        if len(cand) <= K_:
+            continue
+        after = set(int(x) for x in u.positions() if x >= 0)
+        protected = {q for q in cand if q < n_sink or q > p - n_recent}
+        elig = sorted(set(cand) - protected, key=lambda q: (cand[q], q))
+        ties += len(elig) > 1 and cand[elig[0]] == cand[elig[1]]
+        best = None
+        for keep in itertools.combinations(sorted(cand), K_):
+            if not protected <= set(keep):
+                continue
+            f = math.fsum(cand[q] for q in keep)
+            gone = (set(cand) - set(keep)).pop()
+            key = (-f, cand[gone], gone)
+            if best is None or key < best[0]:
+                best = (key, set(keep))
+        assert after == best[1]
+    assert u.greedy_disagreements == 0
+
+
+def test_storage_modes_checked():
+    with pytest.raises(RuntimeError):
+        Unit(SINK_WINDOW, 1, 0, 4, 5, 0, 0, 1, 4).set_score_storage(0.1, False)
+    with pytest.raises(RuntimeError):
+        Unit(H2O_BLOCK, 1, 8, 3, 12, 3, 0, 1, 4).set_score_storage(0.0, True)  # FP16 for H2O only
+    Unit(H2O_BLOCK, 1, 8, 3, 12, 3, 0, 1, 4).set_score_storage(0.3, False)
+    with pytest.raises(RuntimeError):
+        Unit(H2O, 1, 2, 1, 4, 0, 0, 1, 4).set_score_storage(1.0, False)
+    u = Unit(H2O, 1, 2, 1, 4, 0, 0, 1, 4)
+    u.prefill(np.zeros((2, 4), np.float32), np.zeros((2, 4), np.float32))
+    with pytest.raises(RuntimeError):
+        u.set_score_storage(0.1, False)  # only on an empty unit
