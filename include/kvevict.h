@@ -106,6 +106,15 @@ typedef enum {
  *     n_q_heads / n_kv_heads = G in {1, 2, 4, 8}; head_dim in {64, 128}.
  *   dtype: KVEVICT_F32 or KVEVICT_BF16 for K, V, q and out.
  *   max_prompt: RANDOM only, the longest prompt a unit may hold.
+ *   score_forget, score_half: how H2O stores its cumulative scores ("Attention
+ *     Sinks 与 KV Cache 淘汰策略" section 6.2: FP16 storage, or a moving average
+ *     in place of the exact sum). Each step s <- (1 - score_forget) s + a, with
+ *     0 <= score_forget < 1 (0, the default: the exact cumulative score; H2O
+ *     and H2O_BLOCK). score_half = 1 stores every score as IEEE binary16
+ *     (rounded to nearest even after each update; eviction compares the stored
+ *     values), halving the score traffic; H2O only, and not with
+ *     kvevict_prefill_scored / kvevict_prefill_snapkv. kvevict_scores still
+ *     returns fp32.
  * Slot capacity per unit: C = budget (H2O, SINK_WINDOW, H2O_BLOCK) or
  * max_prompt + budget + r (RANDOM).
  */
@@ -116,6 +125,8 @@ typedef struct {
     int batch, n_layers, n_q_heads, n_kv_heads, head_dim;
     int dtype;
     int max_prompt;
+    float score_forget;
+    int score_half;
 } kvevict_config;
 
 typedef struct {

@@ -23,7 +23,8 @@ class Config(ctypes.Structure):
                 ("n_recent", ctypes.c_int), ("budget", ctypes.c_int), ("r", ctypes.c_int),
                 ("seed", ctypes.c_uint64), ("batch", ctypes.c_int), ("n_layers", ctypes.c_int),
                 ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("max_prompt", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("max_prompt", ctypes.c_int), ("score_forget", ctypes.c_float),
+                ("score_half", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):

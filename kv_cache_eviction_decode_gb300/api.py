@@ -24,10 +24,11 @@ class KVEvictCache:
 
     def __init__(self, *, policy: int, budget: int, batch: int, n_layers: int, n_q_heads: int, n_kv_heads: int,
                  head_dim: int, dtype: int, n_sink: int = 0, n_heavy: int = 0, n_recent: int = 0, r: int = 0,
-                 seed: int = 0, max_prompt: int = 0, device=None, stream: torch.cuda.Stream | None = None):
+                 seed: int = 0, max_prompt: int = 0, score_forget: float = 0.0, score_half: bool = False,
+                 device=None, stream: torch.cuda.Stream | None = None):
         self._L = lib()
         self.cfg = Config(policy, n_sink, n_heavy, n_recent, budget, r, seed, batch, n_layers, n_q_heads,
-                          n_kv_heads, head_dim, dtype, max_prompt)
+                          n_kv_heads, head_dim, dtype, max_prompt, score_forget, 1 if score_half else 0)
         nbytes = ctypes.c_size_t(0)
         check(self._L.kvevict_state_bytes(ctypes.byref(self.cfg), ctypes.byref(nbytes)), "kvevict_state_bytes")
         self.device = torch.device(device if device is not None else "cuda")
@@ -46,6 +47,7 @@ class KVEvictCache:
         return cls(policy=w.policy, n_sink=w.n_sink, n_heavy=w.n_heavy, n_recent=w.n_recent, budget=w.budget,
                    r=w.r, seed=w.seed, batch=w.batch, n_layers=w.n_layers, n_q_heads=w.n_q_heads,
                    n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, dtype=w.dtype, max_prompt=w.max_prompt,
+                   score_forget=getattr(w, "score_forget", 0.0), score_half=getattr(w, "score_half", False),
                    device=device, stream=stream)
 
     def close(self) -> None:

@@ -7,6 +7,7 @@
 // never on values, so it is tracked here on the host and passed by value.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cmath>
@@ -36,7 +37,8 @@ bool scored(int policy) { return policy == KVEVICT_H2O || policy == KVEVICT_H2O_
 
 struct Layout {
     int C = 0, G = 0, elem = 0;
-    int Cs = 0;               // per-unit stride of pos/score: C rounded up to 4 (16-byte rows)
+    int Cs = 0;               // per-unit stride of pos/score (rows start on 16 bytes)
+    int score_elem = 4;       // bytes per stored score
     size_t units = 0;         // B * Hkv
     size_t layer_slots = 0;   // units * C (K/V rows)
     size_t layer_pslots = 0;  // units * Cs (pos/score entries)
@@ -88,6 +90,11 @@ int validate(const kvevict_config *c)
     default:
         return KVEVICT_ERR_INVALID_ARG;
     }
+    if (!(c->score_forget >= 0.f && c->score_forget < 1.f) || (c->score_half != 0 && c->score_half != 1))
+        return KVEVICT_ERR_INVALID_ARG;
+    if (c->score_forget != 0.f && c->policy != KVEVICT_H2O && c->policy != KVEVICT_H2O_BLOCK)
+        return KVEVICT_ERR_INVALID_ARG;
+    if (c->score_half && c->policy != KVEVICT_H2O) return KVEVICT_ERR_INVALID_ARG;
     const long long C = c->policy == KVEVICT_RANDOM ? static_cast<long long>(c->max_prompt) + c->budget + c->r
                                                     : c->budget;
     if (C > (1 << 24)) return KVEVICT_ERR_INVALID_ARG;
@@ -100,7 +107,10 @@ Layout make_layout(const kvevict_config *c)
     L.G = c->n_q_heads / c->n_kv_heads;
     L.elem = c->dtype == KVEVICT_F32 ? 4 : 2;
     L.C = c->policy == KVEVICT_RANDOM ? c->max_prompt + c->budget + c->r : c->budget;
-    L.Cs = (L.C + 3) / 4 * 4;
+    // pos/score rows start on 16 bytes for the bulk copies: 4-byte entries need
+    // a multiple of 4, binary16 scores a multiple of 8
+    L.Cs = c->score_half ? (L.C + 7) / 8 * 8 : (L.C + 3) / 4 * 4;
+    L.score_elem = c->score_half ? 2 : 4;
     L.units = static_cast<size_t>(c->batch) * c->n_kv_heads;
     L.layer_slots = L.units * L.C;
     L.layer_pslots = L.units * L.Cs;
@@ -110,7 +120,7 @@ Layout make_layout(const kvevict_config *c)
     L.off_k = off; off = align_up(off + nl * L.kv_layer_bytes);
     L.off_v = off; off = align_up(off + nl * L.kv_layer_bytes);
     L.off_pos = off; off = align_up(off + nl * L.layer_pslots * 4);
-    L.off_score = off; if (scored(c->policy)) off = align_up(off + nl * L.layer_pslots * 4);
+    L.off_score = off; if (scored(c->policy)) off = align_up(off + nl * L.layer_pslots * L.score_elem);
     L.off_free = off;
     if (c->policy == KVEVICT_RANDOM || c->policy == KVEVICT_H2O_BLOCK) off = align_up(off + nl * L.units * c->r * 4);
     L.off_err = off; off = align_up(off + 16);
@@ -239,6 +249,12 @@ int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInf
 
 template <typename T> T *at(const kvevict_handle *h, size_t off) { return reinterpret_cast<T *>(h->state + off); }
 
+// One layer's stored cumulative scores (fp32, or binary16 with score_half).
+void *layer_scores(const kvevict_handle *h, int layer)
+{
+    return h->state + h->L.off_score + static_cast<size_t>(layer) * h->L.layer_pslots * h->L.score_elem;
+}
+
 // 2-D tensor map over rows of head_dim bf16 (a layer's K or V cache: rows =
 // units * C; prompt Q or K: rows = heads * P); boxes of box_rows rows x 64
 // elements, 128-byte swizzle.
@@ -333,7 +349,9 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     P.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
     P.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
     P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
-    P.score = scored(c.policy) ? at<float>(h, L.off_score) + layer * L.layer_pslots : nullptr;
+    P.score = scored(c.policy) ? layer_scores(h, layer) : nullptr;
+    P.score_keep = 1.f - c.score_forget;
+    P.score_half = c.score_half;
     P.freelist = (c.policy == KVEVICT_RANDOM || c.policy == KVEVICT_H2O_BLOCK)
                      ? at<int32_t>(h, L.off_free) + layer * L.units * c.r
                      : nullptr;
@@ -363,7 +381,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
             if (ls.blk_left == 0) {  // full: release a block before this token attends
                 BlockReleaseParams bp{};
                 bp.pos = P.pos;
-                bp.score = P.score;
+                bp.score = static_cast<float *>(P.score);
                 bp.freelist = const_cast<int32_t *>(P.freelist);
                 bp.kc = P.kc;
                 bp.vc = P.vc;
@@ -573,7 +591,7 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
     cudaError_t e = cudaMemsetAsync(h->state + L.off_k, 0, L.off_pos - L.off_k, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_pslots * 4, h->stream);
     if (e == cudaSuccess && scored(cfg->policy))
-        e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_pslots * 4, h->stream);
+        e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_pslots * L.score_elem, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
     if (e != cudaSuccess) {
         delete h;
@@ -603,7 +621,8 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
     P.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
     P.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
     P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
-    P.score = scored(c.policy) ? at<float>(h, L.off_score) + layer * L.layer_pslots : nullptr;
+    P.score = scored(c.policy) ? layer_scores(h, layer) : nullptr;
+    P.score_half = c.score_half;
     P.n_tok = n_tokens;
     P.p0 = ls.prompt_len;
     P.C = L.C;
@@ -634,7 +653,7 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
         bp.kc = P.kc;
         bp.vc = P.vc;
         bp.pos = P.pos;
-        bp.score = P.score;
+        bp.score = static_cast<float *>(P.score);
         bp.n_tok = n_tokens;
         bp.C = L.C;
         bp.cstride = L.Cs;
@@ -706,7 +725,7 @@ int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K,
     const kvevict_config &c = h->cfg;
     const Layout &L = h->L;
     const int P = prompt_len;
-    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16) return KVEVICT_ERR_INVALID_ARG;
+    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16 || c.score_half) return KVEVICT_ERR_INVALID_ARG;
     if (P < 1 || P > kPromptMaxLen) return KVEVICT_ERR_INVALID_ARG;
     if (!Q || !K || !V || !workspace || !aligned16(Q) || !aligned16(K) || !aligned16(V) ||
         (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
@@ -757,7 +776,7 @@ int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K,
         sp.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
         sp.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
         sp.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
-        sp.cscore = at<float>(h, L.off_score) + layer * L.layer_pslots;
+        sp.cscore = static_cast<float *>(layer_scores(h, layer));
         sp.P = P;
         sp.C = L.C;
         sp.cstride = L.Cs;
@@ -815,7 +834,7 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
     const kvevict_config &c = h->cfg;
     const Layout &L = h->L;
     const int P = prompt_len;
-    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16) return KVEVICT_ERR_INVALID_ARG;
+    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16 || c.score_half) return KVEVICT_ERR_INVALID_ARG;
     if (P < 2 || P > kPromptMaxLen || window < 1 || window >= P || k_per_head < 0) return KVEVICT_ERR_INVALID_ARG;
     // the union of the G heads' top-k lists plus the window must fit the unit
     if (static_cast<long long>(L.G) * k_per_head + window > L.C) return KVEVICT_ERR_INVALID_ARG;
@@ -870,7 +889,7 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
         sp.kc = h->state + L.off_k + layer * L.kv_layer_bytes;
         sp.vc = h->state + L.off_v + layer * L.kv_layer_bytes;
         sp.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
-        sp.cscore = at<float>(h, L.off_score) + layer * L.layer_pslots;
+        sp.cscore = static_cast<float *>(layer_scores(h, layer));
         sp.P = P;
         sp.C = L.C;
         sp.cstride = L.Cs;
@@ -944,7 +963,17 @@ int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
     if (!scored(h->cfg.policy)) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     const Layout &L = h->L;
-    const void *src = at<float>(h, L.off_score) + layer * L.layer_pslots;
+    const void *src = layer_scores(h, layer);
+    if (L.score_elem == 2) {  // binary16 storage, returned as fp32
+        if (dst_is_device) return cuda_status(launch_scores_to_f32(dst, src, L.C, L.Cs, L.units, h->stream));
+        std::vector<__half> tmp(static_cast<size_t>(L.units) * L.C);
+        cudaError_t e = cudaMemcpy2DAsync(tmp.data(), L.C * 2, src, L.Cs * 2, L.C * 2, L.units,
+                                          cudaMemcpyDeviceToHost, h->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        if (e != cudaSuccess) return cuda_status(e);
+        for (size_t i = 0; i < tmp.size(); ++i) dst[i] = __half2float(tmp[i]);
+        return KVEVICT_OK;
+    }
     cudaError_t e = cudaMemcpy2DAsync(dst, L.C * 4, src, L.Cs * 4, L.C * 4, L.units,
                                       dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
     if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);

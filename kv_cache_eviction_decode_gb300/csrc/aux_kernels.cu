@@ -1,5 +1,8 @@
 // aux_kernels.cu -- prompt prefill and the Random Attention periodic cut.
+#include <algorithm>
 #include <climits>
+
+#include <cuda_fp16.h>
 
 #include "aux_kernels.h"
 #include "device_common.cuh"
@@ -40,7 +43,10 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillParams P)
     }
     if (lane == 0) {
         P.pos[unit * P.cstride + slot] = p;
-        if (P.score) P.score[unit * P.cstride + slot] = 0.f;
+        if (P.score) {
+            if (P.score_half) static_cast<uint16_t *>(P.score)[unit * P.cstride + slot] = 0;  // +0 in binary16
+            else static_cast<float *>(P.score)[unit * P.cstride + slot] = 0.f;
+        }
     }
 }
 
@@ -257,6 +263,23 @@ void launch_block_prefill(const BlockPrefillParams &p, int B, cudaStream_t st)
 cudaError_t launch_block_release(const BlockReleaseParams &p, int units, cudaStream_t st)
 {
     block_release_kernel<<<units, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+__global__ void scores_to_f32_kernel(float *dst, const __half *src, int C, int cstride, size_t n)
+{
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t u = i / C, j = i - u * C;
+        dst[i] = __half2float(src[u * cstride + j]);
+    }
+}
+
+cudaError_t launch_scores_to_f32(float *dst, const void *src, int C, int cstride, size_t units, cudaStream_t st)
+{
+    const size_t n = units * C;
+    const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
+    scores_to_f32_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const __half *>(src), C, cstride, n);
     return cudaGetLastError();
 }
 

@@ -14,7 +14,8 @@ struct PrefillParams {
     const void *K, *V;  // [B][Hkv][n_tok][D]
     void *kc, *vc;      // layer cache [B][Hkv][C][D]
     int32_t *pos;
-    float *score;       // or null
+    void *score;        // fp32 or binary16 (score_half), or null
+    int score_half;
     int n_tok, p0, C, cstride, Hkv, head_dim, elem_bytes;
     int n_sink, ring_len;  // ring_len = C - n_sink for ring policies, 0 for Random
     int a0, a1, b0, b1;    // chunk rows to copy
@@ -53,6 +54,8 @@ struct BlockReleaseParams {
 };
 
 void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st);
+// binary16 scores [units][cstride] -> fp32 [units][C]
+cudaError_t launch_scores_to_f32(float *dst, const void *src, int C, int cstride, size_t units, cudaStream_t st);
 void launch_block_prefill(const BlockPrefillParams &p, int B, cudaStream_t st);
 cudaError_t launch_block_release(const BlockReleaseParams &p, int units, cudaStream_t st);
 size_t cut_smem_bytes(int n_pow2, int r);

@@ -57,6 +57,8 @@
 #include <climits>
 #include <cmath>
 
+#include <cuda_fp16.h>
+
 #include "device_common.cuh"
 
 namespace kvevict {
@@ -94,7 +96,7 @@ struct DecodeParams {
     void *out;           // [B][Hkv*G][D]
     void *kc, *vc;       // this layer's cache, [B][Hkv][C][D]
     int32_t *pos;        // [B][Hkv][cstride]
-    float *score;        // [B][Hkv][cstride], or null when the policy keeps no scores
+    void *score;         // [B][Hkv][cstride] fp32 (fp16 with score_half), or null when the policy keeps no scores
     const int32_t *freelist;  // [B][Hkv][freelist_len]
     int32_t *trace;      // [B][Hkv][4] or null: slot, evicted position, evicted score, new score
     uint32_t *err;
@@ -111,7 +113,30 @@ struct DecodeParams {
     int prefetch_early;  // the launch before this one did not touch this layer: cache tiles may be
                          // fetched before the programmatic-dependency wait (inputs still after it)
     float scale_log2;    // log2(e) / sqrt(D)
+    float score_keep;    // each step s <- score_keep * s + a (1: the exact cumulative score)
+    int score_half;      // scores stored as IEEE binary16 (cstride a multiple of 8)
 };
+
+// Stored cumulative scores: fp32, or binary16 rounded to nearest even.
+__device__ __forceinline__ float score_load(const DecodeParams &P, size_t i)
+{
+    return P.score_half ? __half2float(static_cast<const __half *>(P.score)[i]) : static_cast<const float *>(P.score)[i];
+}
+// Stores v and returns the value stored (v rounded when binary16).
+__device__ __forceinline__ float score_store(const DecodeParams &P, size_t i, float v)
+{
+    if (P.score_half) {
+        const __half h = __float2half_rn(v);
+        static_cast<__half *>(P.score)[i] = h;
+        return __half2float(h);
+    }
+    static_cast<float *>(P.score)[i] = v;
+    return v;
+}
+__device__ __forceinline__ float score_round(const DecodeParams &P, float v)
+{
+    return P.score_half ? __half2float(__float2half_rn(v)) : v;
+}
 
 // Shared-memory layout, shared by host (size) and device (offsets). All
 // offsets are from a base aligned up to kSmemAlign inside the allocation.
@@ -377,10 +402,14 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     auto issue_aux = [&](int i) {
         const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
         const uint32_t bytes = static_cast<uint32_t>(((W.n_mine * 4 + 15) / 16) * 16);
-        const uint32_t tx = has_score ? 2 * bytes : bytes;
+        const uint32_t sbytes = P.score_half ? static_cast<uint32_t>(((W.n_mine * 2 + 15) / 16) * 16) : bytes;
+        const uint32_t tx = has_score ? bytes + sbytes : bytes;
         mbar_arrive_expect_tx(&M.auxbar, tx);
         bulk_g2s(aux, P.pos + unit * CS + W.s_lo, bytes, &M.auxbar);
-        if (has_score) bulk_g2s(aux + auxb, P.score + unit * CS + W.s_lo, bytes, &M.auxbar);
+        if (has_score)
+            bulk_g2s(aux + auxb,
+                     static_cast<const uint8_t *>(P.score) + (unit * CS + W.s_lo) * (P.score_half ? 2 : 4), sbytes,
+                     &M.auxbar);
         M.aux_issued++;
     };
 
@@ -499,6 +528,9 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         const int seq0 = i * 2 * W.nt;
         const int32_t *apos = reinterpret_cast<const int32_t *>(aux);
         const float *ascore = reinterpret_cast<const float *>(aux + auxb);
+        const __half *ascore_h = reinterpret_cast<const __half *>(aux + auxb);
+        // this unit's stored score of local slot j, before this step
+        auto stored_score = [&](int j) { return P.score_half ? __half2float(ascore_h[j]) : ascore[j]; };
 
         // This unit's q (prefetched during the previous unit); start the
         // next unit's loads.
@@ -865,8 +897,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     float a = 0.f;
 #pragma unroll
                     for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
-                    const float sc = ascore[j] + a;
-                    P.score[unit * CS + j] = sc;
+                    const float sc = score_store(P, unit * CS + j, fmaf(P.score_keep, stored_score(j), a));
                     if (evict) {
                         const int ps = apos[j];
                         if (fill && ps < 0 && j < emin) emin = j;
@@ -884,7 +915,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     float a = 0.f;
 #pragma unroll
                     for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], invl[g], a);
-                    anew = a * (1.0f / G);
+                    anew = score_round(P, a * (1.0f / G));
                 }
                 if (evict) {
                     warp_argmin(best, bslot);
@@ -980,8 +1011,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     float a = 0.f;
 #pragma unroll
                     for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
-                    const float sc = ascore[j] + a;
-                    P.score[unit * CS + W.s_lo + j] = sc;
+                    const float sc =
+                        score_store(P, unit * CS + W.s_lo + j, fmaf(P.score_keep, stored_score(j), a));
                     if (evict) {
                         const int ps = apos[j];
                         if (fill && ps < 0 && W.s_lo + j < emin) emin = W.s_lo + j;
@@ -999,7 +1030,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     float a = 0.f;
 #pragma unroll
                     for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], M.fac[0][g], a);
-                    anew = a * (1.0f / G);
+                    anew = score_round(P, a * (1.0f / G));
                 }
                 if (evict) {
                     warp_argmin(best, bslot);
@@ -1072,10 +1103,10 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 float old_score = __uint_as_float(static_cast<uint32_t>(win_key >> 32));
                 if (!evict && P.trace != nullptr) {
                     old_pos = P.pos[unit * CS + dest];
-                    old_score = has_score ? P.score[unit * CS + dest] : 0.f;
+                    old_score = has_score ? score_load(P, unit * CS + dest) : 0.f;
                 }
                 P.pos[unit * CS + dest] = P.p;
-                if (has_score) P.score[unit * CS + dest] = anew;
+                if (has_score) score_store(P, unit * CS + dest, anew);
                 if (P.trace != nullptr)
                     reinterpret_cast<int4 *>(P.trace)[unit] =
                         make_int4(dest, old_pos, __float_as_int(old_score), __float_as_int(anew));

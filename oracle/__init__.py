@@ -120,8 +120,12 @@ class Unit:
 
     @classmethod
     def for_workload(cls, w, seq: int, layer: int, kv_head: int) -> "Unit":
-        return cls(w.policy, w.n_sink, w.n_heavy, w.n_recent, w.budget, w.r, w.max_prompt, w.group,
-                   w.head_dim, w.seed, seq, layer, kv_head)
+        u = cls(w.policy, w.n_sink, w.n_heavy, w.n_recent, w.budget, w.r, w.max_prompt, w.group,
+                w.head_dim, w.seed, seq, layer, kv_head)
+        forget, half = getattr(w, "score_forget", 0.0), getattr(w, "score_half", False)
+        if forget or half:
+            u.set_score_storage(forget, half)
+        return u
 
     def __del__(self):
         h, self.h = getattr(self, "h", None), None

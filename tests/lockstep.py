@@ -153,9 +153,14 @@ def out_tol(w):
 
 
 def score_error(w, got, ref):
+    diff = np.abs(got - ref)
+    if getattr(w, "score_half", False):
+        # binary16 storage: the GPU rounds its fp32 sum, the oracle its fp64 sum;
+        # they may land one binary16 step apart (at most 2^-10 of the value)
+        diff = np.maximum(diff - (2.0**-10 * np.abs(ref) + 2.0**-24), 0.0)
     if w.dtype == DTYPE_BF16:
-        return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-6))
-    return float(np.max(np.abs(got - ref)))
+        return float(np.max(diff) / max(np.max(np.abs(ref)), 1e-6))
+    return float(np.max(diff))
 
 
 def replay_unit(w: Workload, unit, x, run: GpuRun, n_steps: int, out_steps=None,
@@ -194,7 +199,8 @@ def replay_unit(w: Workload, unit, x, run: GpuRun, n_steps: int, out_steps=None,
             sc = u.scores()
             a, b = sc[slot], sc[gslot]
             rel = abs(a - b) / max(a, b, 1e-300)
-            assert 0 <= gslot < u.cap and rel < NEAR_TIE_REL, \
+            tie_rel = 2.0**-10 if getattr(w, "score_half", False) else NEAR_TIE_REL  # one binary16 step
+            assert 0 <= gslot < u.cap and rel < tie_rel, \
                 f"{unit} step {t}: GPU evicted slot {gslot} (pos {u.pos_at(gslot)}, score {b:.9g}), " \
                 f"oracle slot {slot} (pos {u.pos_at(slot)}, score {a:.9g}), rel {rel:.3e}"
             rep.near_ties += 1

@@ -1,0 +1,93 @@
+"""GPU parity of H2O's score-storage variants ("Attention Sinks 与 KV Cache 淘汰策略"
+section 6.2): the moving average s <- (1 - forget) s + a and binary16 storage,
+through the C ABI, in lockstep with the CPU oracle.
+
+Outputs and scores as for H2O (2e-2 relative for bf16, 1e-4 max-abs for fp32;
+binary16 scores also within one binary16 step). Victims identical, except at
+near-ties, which the oracle adopts: within 1e-5 relative for fp32 scores,
+within one binary16 step for binary16 scores (the GPU sums in fp32, the
+oracle in fp64, before the same rounding). The selector is also checked
+bit-exact on the GPU's own stored values.
+"""
+import numpy as np
+import pytest
+
+from kv_cache_eviction_decode_gb300 import BF16, F32, H2O, H2O_BLOCK, KVEvictCache, KVEvictError
+from tests import lockstep as ls
+from workloads import configs
+
+pytestmark = pytest.mark.gpu
+
+
+def _small(dtype, forget, half, policy=H2O, r=0):
+    return configs.Workload(name="score_storage", policy=policy, dtype=dtype, batch=3, n_layers=1, n_q_heads=8,
+                            n_kv_heads=4, head_dim=64, n_sink=2, n_heavy=40, n_recent=22, budget=64, r=r,
+                            prompt_len=30, decode_steps=0, seed=91, score_forget=forget, score_half=half)
+
+
+@pytest.mark.parametrize("dtype,forget,half", [(BF16, 0.1, False), (BF16, 0.0, True), (BF16, 0.05, True),
+                                               (F32, 0.02, True), (F32, 0.2, False)])
+def test_score_storage_lockstep(cuda_device, dtype, forget, half):
+    w = _small(dtype, forget, half)
+    T = 160
+    units = [(s, 0, h) for s in range(w.batch) for h in range(w.n_kv_heads)]
+    inputs = ls.host_inputs(w, units, T, w.prompt_len)
+    snaps = list(range(0, T, 16))
+    run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=snaps)
+    assert run.err == 0
+    reps = ls.replay_all(w, units, inputs, run, T)
+    worst_out = max(r.max_out_err for r in reps)
+    worst_sc = max(r.max_score_err for r in reps)
+    ties = sum(r.near_ties for r in reps)
+    print(f"forget {forget} half {half}: out {worst_out:.2e}, score {worst_sc:.2e}, near ties {ties}")
+    # the cache fills during the first budget - prompt steps: the selector decides from then on
+    assert ls.check_selector(w, run, 0, w.prompt_len) == sum(t >= w.budget - w.prompt_len for t in snaps)
+    if half:  # every stored score is a binary16 value
+        for t, sc in run.score_snap[0].items():
+            v = sc.numpy()
+            assert np.all(v.astype(np.float16).astype(np.float32) == v)
+
+
+def test_block_with_moving_average_lockstep(cuda_device):
+    w = _small(BF16, 0.05, False, policy=H2O_BLOCK, r=8)
+    T = 120
+    units = [(s, 0, h) for s in range(w.batch) for h in range(w.n_kv_heads)]
+    inputs = ls.host_inputs(w, units, T, w.prompt_len)
+    run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=range(0, T, 10))
+    assert run.err == 0
+    reps = ls.replay_all(w, units, inputs, run, T)
+    assert sum(r.near_ties for r in reps) == 0
+
+
+def test_score_storage_rejected_where_unsupported(cuda_device):
+    base = dict(batch=1, n_layers=1, n_q_heads=2, n_kv_heads=2, head_dim=64, dtype=BF16, device=cuda_device)
+    with pytest.raises(KVEvictError):  # binary16 scores: H2O only
+        KVEvictCache(policy=H2O_BLOCK, budget=64, n_sink=2, n_heavy=40, n_recent=22, r=8, score_half=True, **base)
+    with pytest.raises(KVEvictError):
+        KVEvictCache(policy=H2O, budget=64, n_sink=2, n_heavy=40, n_recent=22, score_forget=1.0, **base)
+    c = KVEvictCache(policy=H2O, budget=64, n_sink=2, n_heavy=40, n_recent=22, score_half=True, **base)
+    import torch
+    Q = torch.zeros((1, 2, 100, 64), dtype=torch.bfloat16, device=cuda_device)
+    K = torch.zeros((1, 2, 100, 64), dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(KVEvictError):  # the scored prefill writes fp32 scores
+        c.prefill_scored(0, Q, K, K)
+    c.close()
+
+
+def test_fp16_scores_full_shape(cuda_device):
+    """H2O 4 + 510 + 510 on the MHA shape with binary16 scores: B=16, 32x32
+    heads, d=128, prompt 2048, 200 steps; sequences {0, 15} x every head of
+    layers {0, 31} in lockstep."""
+    w = configs.H2O_MHA_FP16
+    T = 200
+    layers = [0, w.n_layers - 1]
+    checked = [(s, l, h) for l in layers for s in (0, w.batch - 1) for h in range(w.n_kv_heads)]
+    inputs = ls.host_inputs(w, checked, T, w.prompt_len)
+    snaps = [0, 100, T - 1]
+    run = ls.run_gpu(w, layers, T, inputs, w.prompt_len, cuda_device, snap_steps=snaps)
+    assert run.err == 0
+    reps = ls.replay_all(w, checked, inputs, run, T, out_steps=range(0, T, 7))
+    print("fp16 scores full shape: near ties", sum(r.near_ties for r in reps),
+          "max out err", max(r.max_out_err for r in reps))
+    for layer in layers:
+        assert ls.check_selector(w, run, layer, w.prompt_len) == len(snaps)

@@ -45,6 +45,8 @@ class Workload:
     decode_steps: int
     seed: int
     max_prompt: int = 0
+    score_forget: float = 0.0  # H2O score storage: s <- (1 - score_forget) s + a
+    score_half: bool = False   # H2O score storage: binary16
 
     @property
     def group(self) -> int:
@@ -120,8 +122,13 @@ H2O_REASONING = Workload(
 H2O_BLOCK16 = H2O_MHA.with_(name="h2o_block16_bf16_b16_l32_h32_d128_k1024", policy=POLICY_H2O_BLOCK, r=16)
 H2O_BLOCK256 = H2O_MHA.with_(name="h2o_block256_bf16_b16_l32_h32_d128_k1024", policy=POLICY_H2O_BLOCK, r=256)
 
+# H2O on the MHA shape with the scores stored in binary16 (half the score
+# traffic), and with a moving average (forget 0.01 per step) in place of the sum.
+H2O_MHA_FP16 = H2O_MHA.with_(name="h2o_fp16scores_bf16_b16_l32_h32_d128_k1024", score_half=True)
+H2O_MHA_EMA = H2O_MHA.with_(name="h2o_ema0.01_bf16_b16_l32_h32_d128_k1024", score_forget=0.01)
+
 ALL = {w.name: w for w in (H2O_TINY, SINK_WINDOW, H2O_MHA, H2O_GQA, RANDOM_REASONING, H2O_REASONING, H2O_BLOCK16,
-                           H2O_BLOCK256)}
+                           H2O_BLOCK256, H2O_MHA_FP16, H2O_MHA_EMA)}
 
 # Short names used on command lines.
 ALIASES = {
@@ -133,6 +140,8 @@ ALIASES = {
     "h2o_reasoning": H2O_REASONING.name,
     "h2o_block16": H2O_BLOCK16.name,
     "h2o_block256": H2O_BLOCK256.name,
+    "h2o_fp16scores": H2O_MHA_FP16.name,
+    "h2o_ema": H2O_MHA_EMA.name,
 }
 
 

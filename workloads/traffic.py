@@ -32,7 +32,7 @@ def unit_step_bytes(w: Workload, n_retained: int, n_slots: int | None = None, cu
     d, e, G = w.head_dim, w.elem_bytes, w.group
     b = (n_retained + 1) * 2 * d * e + 2 * d * e + 2 * G * d * e
     if w.policy in (POLICY_H2O, POLICY_H2O_BLOCK):
-        b += 8 * n_retained + 8
+        b += (4 if w.score_half else 8) * n_retained + (6 if w.score_half else 8)
     if w.policy == POLICY_RANDOM:
         b += 4 * (n_slots if n_slots is not None else w.capacity)
         if cut:
