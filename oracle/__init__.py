@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvevict_oracle.c")
 _LIB = os.path.join(_HERE, "liborc_kvevict.so")
 
-H2O, SINK_WINDOW, RANDOM, H2O_BLOCK = 0, 1, 2, 3
+H2O, SINK_WINDOW, RANDOM, H2O_BLOCK, H2O_POOLS = 0, 1, 2, 3, 4
 OK, EINVAL, ECAPACITY, ESTATE = 0, -1, -2, -3
 
 _lock = threading.Lock()
@@ -82,6 +82,16 @@ def lib():
             L.orc_prompt_tail_scores.restype = I
             L.orc_set_score_storage.argtypes = [P, ctypes.c_double, I]
             L.orc_set_score_storage.restype = I
+            L.orc_set_hh_threshold.argtypes = [P, ctypes.c_double]
+            L.orc_set_hh_threshold.restype = I
+            L.orc_pools.argtypes = [P, P]
+            L.orc_last_promote.argtypes = [P]
+            L.orc_last_promote.restype = I
+            L.orc_decision_margin.argtypes = [P]
+            L.orc_decision_margin.restype = D
+            L.orc_decision.argtypes = [P, P]
+            L.orc_commit_pools.argtypes = [P, I, I, I]
+            L.orc_commit_pools.restype = I
             L.orc_round_half.argtypes = [ctypes.c_double]
             L.orc_round_half.restype = ctypes.c_double
             L.orc_step.argtypes = [P, P, P, P, P]
@@ -125,6 +135,8 @@ class Unit:
         forget, half = getattr(w, "score_forget", 0.0), getattr(w, "score_half", False)
         if forget or half:
             u.set_score_storage(forget, half)
+        if w.policy == H2O_POOLS:
+            u.set_hh_threshold(w.hh_threshold)
         return u
 
     def __del__(self):
@@ -143,6 +155,12 @@ class Unit:
         rc = self._L.orc_set_score_storage(self.h, forget, 1 if half else 0)
         if rc:
             raise RuntimeError(f"oracle set_score_storage failed: {rc}")
+
+    def set_hh_threshold(self, theta: float) -> None:
+        """Two-pool H2O: promotion needs a score strictly above theta."""
+        rc = self._L.orc_set_hh_threshold(self.h, float(theta))
+        if rc:
+            raise RuntimeError(f"oracle set_hh_threshold failed: {rc}")
 
     def prefill_scored(self, q, k, v) -> np.ndarray:
         """Q-seeded prefill of an empty H2O unit: q [G][P][d], k/v [P][d].
@@ -196,6 +214,23 @@ class Unit:
         if rc:
             raise RuntimeError(f"oracle commit failed: {rc}")
 
+    def decision(self):
+        """Two-pool H2O, after choose(): (slot or capacity, new token's pool,
+        promoted slot or -1)."""
+        a = (ctypes.c_int * 3)()
+        self._L.orc_decision(self.h, a)
+        return int(a[0]), int(a[1]), int(a[2])
+
+    @property
+    def decision_margin(self) -> float:
+        """Smallest relative gap among the comparisons of the last choose()."""
+        return self._L.orc_decision_margin(self.h)
+
+    def commit_pools(self, slot: int, new_pool: int, promote: int) -> None:
+        rc = self._L.orc_commit_pools(self.h, int(slot), int(new_pool), int(promote))
+        if rc:
+            raise RuntimeError(f"oracle commit_pools failed: {rc}")
+
     def step(self, q, k_new, v_new):
         out = self.attend(q, k_new, v_new)
         slot = self.choose()
@@ -207,6 +242,17 @@ class Unit:
         a = np.empty(self.cap, dtype=np.int32)
         self._L.orc_positions(self.h, _ptr(a))
         return a
+
+    def pools(self) -> np.ndarray:
+        """Two-pool H2O: 0 recent pool, 1 heavy-hitter pool (meaningful where a slot is held)."""
+        a = np.empty(self.cap, dtype=np.int8)
+        self._L.orc_pools(self.h, _ptr(a))
+        return a
+
+    @property
+    def last_promote(self) -> int:
+        """Promotion of the last commit: slot, -2 the new token itself, -1 none."""
+        return self._L.orc_last_promote(self.h)
 
     def pos_at(self, slot: int) -> int:
         return int(self._L.orc_pos_at(self.h, int(slot)))

@@ -49,6 +49,13 @@
  *    the r generated tokens with the smallest 64-bit Philox key (ties: older
  *    position), counter (pos, step, layer * 2^16 + head, seq), key
  *    (seed, 0x5EED0001).
+ *  - two-pool H2O (the H2OCache class of "KV Cache 驱逐策略：从 LRU 到 H2O",
+ *    section "实现要点"): the new token joins the recent pool; when that pool
+ *    holds more than n_recent tokens its lowest (score, position) member
+ *    leaves, the new token included; it enters the heavy-hitter pool iff its
+ *    score is strictly above hh_threshold, else it is dropped; a heavy-hitter
+ *    pool above n_heavy drops its lowest member, the one just promoted
+ *    included. Ties go to the older position in both pools.
  */
 #include <math.h>
 #include <pthread.h>
@@ -57,7 +64,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_H2O = 0, ORC_SINK_WINDOW = 1, ORC_RANDOM = 2, ORC_H2O_BLOCK = 3 };
+enum { ORC_H2O = 0, ORC_SINK_WINDOW = 1, ORC_RANDOM = 2, ORC_H2O_BLOCK = 3, ORC_H2O_POOLS = 4 };
 enum { ORC_OK = 0, ORC_EINVAL = -1, ORC_ECAPACITY = -2, ORC_ESTATE = -3 };
 
 #define ORC_RANDOM_KEY_TAG 0x5EED0001ull
@@ -85,6 +92,14 @@ typedef struct orc_unit {
     int last_block;      /* H2O_BLOCK: block released for the token of the last step, -1 if none */
     double forget;       /* score storage: s <- (1 - forget) s + a each step (0: exact accumulation) */
     int half;            /* score storage: every stored score rounded to IEEE binary16 */
+    /* two-pool H2O */
+    signed char *pool;   /* [cap] 0: recent pool, 1: heavy-hitter pool (slots with pos >= 0) */
+    double hh_threshold; /* promotion needs a score strictly above this */
+    int dec_slot;        /* decision of the last orc_choose: slot for the new token (cap: dropped), */
+    int dec_pool;        /* the pool it joins, */
+    int dec_promote;     /* the slot of a held token moved to the heavy-hitter pool (-1: none), */
+    double dec_margin;   /* and the smallest relative gap among the comparisons that decided it */
+    int last_promote;    /* the promotion of the last commit: slot, -2 the new token itself, -1 none */
 } orc_unit;
 
 /* ------------------------------------------------------------------------ */
@@ -164,6 +179,9 @@ orc_unit *orc_new(int policy, int n_sink, int n_heavy, int n_recent, int budget,
         if (n_sink < 0 || n_heavy != 0 || n_recent < 1 || n_sink + n_recent != budget) return NULL;
     } else if (policy == ORC_RANDOM) {
         if (r < 1 || max_prompt < 0) return NULL;
+    } else if (policy == ORC_H2O_POOLS) {
+        /* no sinks: the class keeps a recent pool and a heavy-hitter pool only */
+        if (n_sink != 0 || n_heavy < 0 || n_recent < 1 || n_heavy + n_recent != budget) return NULL;
     } else if (policy == ORC_H2O_BLOCK) {
         /* r is the block size; the budget is whole blocks, and besides the
          * blocks holding sinks at least one block lies outside the recent
@@ -187,14 +205,31 @@ orc_unit *orc_new(int policy, int n_sink, int n_heavy, int n_recent, int budget,
     u->score = (double *)calloc((size_t)u->cap, sizeof(double));
     u->k_new = (float *)calloc((size_t)d, sizeof(float));
     u->v_new = (float *)calloc((size_t)d, sizeof(float));
-    if (!u->pos || !u->k || !u->v || !u->score || !u->k_new || !u->v_new) {
-        free(u->pos); free(u->k); free(u->v); free(u->score); free(u->k_new); free(u->v_new); free(u);
+    u->pool = (signed char *)calloc((size_t)u->cap, 1);
+    if (!u->pos || !u->k || !u->v || !u->score || !u->k_new || !u->v_new || !u->pool) {
+        free(u->pos); free(u->k); free(u->v); free(u->score); free(u->k_new); free(u->v_new); free(u->pool);
+        free(u);
         return NULL;
     }
     for (int s = 0; s < u->cap; ++s) u->pos[s] = -1;
     u->last_victim_pos = -1;
     u->last_block = -1;
+    u->dec_slot = -1;
+    u->dec_promote = -1;
+    u->last_promote = -1;
     return u;
+}
+
+/* The promotion threshold of two-pool H2O (the class leaves it open): a
+ * token leaving the recent pool enters the heavy-hitter pool iff its score is
+ * strictly above theta. Any value but NaN; -INFINITY promotes every token. On
+ * an empty unit. */
+int orc_set_hh_threshold(orc_unit *u, double theta)
+{
+    if (u->policy != ORC_H2O_POOLS || isnan(theta)) return ORC_EINVAL;
+    if (u->prompt_len != 0 || u->t != 0 || u->have_new) return ORC_ESTATE;
+    u->hh_threshold = theta;
+    return ORC_OK;
 }
 
 /* Score-storage variants ("Attention Sinks 与 KV Cache 淘汰策略" section 6.2: the
@@ -202,11 +237,12 @@ orc_unit *orc_new(int policy, int n_sink, int n_heavy, int n_recent, int budget,
  * accumulation): every step s <- (1 - forget) s + a for each retained token,
  * with 0 <= forget < 1 (0 is the exact cumulative score), and with half != 0
  * every stored score (the new token's too) is rounded to binary16 right after
- * its update. H2O and block H2O only (half: H2O only), on an empty unit. */
+ * its update. The score-keeping policies only (half: not block H2O), on an
+ * empty unit. */
 int orc_set_score_storage(orc_unit *u, double forget, int half)
 {
-    if (u->policy != ORC_H2O && u->policy != ORC_H2O_BLOCK) return ORC_EINVAL;
-    if (half && u->policy != ORC_H2O) return ORC_EINVAL;
+    if (u->policy != ORC_H2O && u->policy != ORC_H2O_BLOCK && u->policy != ORC_H2O_POOLS) return ORC_EINVAL;
+    if (half && u->policy == ORC_H2O_BLOCK) return ORC_EINVAL;
     if (!(forget >= 0.0 && forget < 1.0)) return ORC_EINVAL;
     if (u->prompt_len != 0 || u->t != 0 || u->have_new) return ORC_ESTATE;
     u->forget = forget;
@@ -217,7 +253,7 @@ int orc_set_score_storage(orc_unit *u, double forget, int half)
 void orc_free(orc_unit *u)
 {
     if (!u) return;
-    free(u->pos); free(u->k); free(u->v); free(u->score); free(u->k_new); free(u->v_new);
+    free(u->pos); free(u->k); free(u->v); free(u->score); free(u->k_new); free(u->v_new); free(u->pool);
     free(u);
 }
 
@@ -232,6 +268,15 @@ int orc_last_block(const orc_unit *u) { return u->last_block; }
 double orc_new_score(const orc_unit *u) { return u->score_new; }
 
 void orc_positions(const orc_unit *u, int32_t *dst) { memcpy(dst, u->pos, sizeof(int32_t) * (size_t)u->cap); }
+void orc_pools(const orc_unit *u, signed char *dst) { memcpy(dst, u->pool, (size_t)u->cap); }
+int orc_last_promote(const orc_unit *u) { return u->last_promote; }
+double orc_decision_margin(const orc_unit *u) { return u->dec_margin; }
+void orc_decision(const orc_unit *u, int *out3)
+{
+    out3[0] = u->dec_slot;
+    out3[1] = u->dec_pool;
+    out3[2] = u->dec_promote;
+}
 void orc_scores(const orc_unit *u, double *dst) { memcpy(dst, u->score, sizeof(double) * (size_t)u->cap); }
 
 /* Copy out the stored K/V of one slot (test use). */
@@ -366,7 +411,7 @@ int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_n
     /* H2O: every retained token's cumulative score grows by this step's
      * probability (mean over the unit's G query heads); the new token starts
      * with its own. Sink-window and Random keep no scores. */
-    if (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK) {
+    if (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK || u->policy == ORC_H2O_POOLS) {
         for (int s = 0; s < cap; ++s) {
             if (u->pos[s] < 0) continue;
             u->score[s] = (1.0 - u->forget) * u->score[s] + mass[s] / (double)G;
@@ -390,7 +435,7 @@ int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_n
 int orc_stage(orc_unit *u, const float *k_new, const float *v_new)
 {
     if (u->have_new) return ORC_ESTATE;
-    if (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK) return ORC_EINVAL;
+    if (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK || u->policy == ORC_H2O_POOLS) return ORC_EINVAL;
     memcpy(u->k_new, k_new, sizeof(float) * (size_t)u->d);
     memcpy(u->v_new, v_new, sizeof(float) * (size_t)u->d);
     u->new_pos = u->prompt_len + u->t;
@@ -479,12 +524,95 @@ static int choose_sink_window(orc_unit *u)
     return oldest;
 }
 
+/* (score a, position pa) below (score b, position pb): the lower score, then
+ * the older position. */
+static int key_less(double a, int32_t pa, double b, int32_t pb) { return a < b || (a == b && pa < pb); }
+
+static double rel_gap(double a, double b)
+{
+    const double m = fmax(fabs(a), fabs(b));
+    if (isinf(a) || isinf(b)) return a == b ? 0.0 : INFINITY;
+    return m > 0.0 ? fabs(a - b) / m : 0.0;
+}
+
+/* Two-pool H2O, the H2OCache class's add step ("KV Cache 驱逐策略：从 LRU 到
+ * H2O", section "实现要点"), after the scores were updated by orc_attend:
+ *   1. the new token joins the recent pool;
+ *   2. if the recent pool now holds more than n_recent tokens, its lowest
+ *      (score, position) member v leaves it (the new token is a member);
+ *   3. if score(v) > hh_threshold, v joins the heavy-hitter pool, and if that
+ *      pool now holds more than n_heavy tokens its lowest member leaves the
+ *      cache (v included); otherwise v leaves the cache.
+ * The new token, unless it is the one leaving, takes the slot of the token
+ * that left, else the lowest empty slot. Records the decision in dec_* and
+ * returns the slot, or cap when the new token itself left. */
+static int choose_pools(orc_unit *u)
+{
+    const int32_t pn = u->new_pos;
+    const double sn = u->score_new;
+    int n_rec = 0, n_hh = 0, v = -1, w = -1;
+    for (int s = 0; s < u->cap; ++s) {
+        if (u->pos[s] < 0) continue;
+        if (u->pool[s] == 0) {
+            n_rec++;
+            if (v < 0 || key_less(u->score[s], u->pos[s], u->score[v], u->pos[v])) v = s;
+        } else {
+            n_hh++;
+            if (w < 0 || key_less(u->score[s], u->pos[s], u->score[w], u->pos[w])) w = s;
+        }
+    }
+    u->dec_pool = 0;
+    u->dec_promote = -1;
+    u->dec_margin = INFINITY;
+    if (n_rec + 1 <= u->n_recent) { /* 1: room in the recent pool */
+        u->dec_slot = first_free_slot(u);
+        return u->dec_slot;
+    }
+    /* 2: v leaves the recent pool -- its lowest member, the new token included */
+    const int v_new = v < 0 || key_less(sn, pn, u->score[v], u->pos[v]);
+    const double sv = v_new ? sn : u->score[v];
+    const int32_t pv = v_new ? pn : u->pos[v];
+    if (!(sv > u->hh_threshold)) { /* 3: v leaves the cache */
+        u->dec_slot = v_new ? u->cap : v;
+    } else if (n_hh + 1 <= u->n_heavy) { /* 3: v promoted, room in the heavy-hitter pool */
+        u->dec_slot = first_free_slot(u);
+        if (v_new) u->dec_pool = 1; else u->dec_promote = v;
+    } else if (w >= 0 && key_less(u->score[w], u->pos[w], sv, pv)) { /* 3: v promoted, w leaves */
+        u->dec_slot = w;
+        if (v_new) u->dec_pool = 1; else u->dec_promote = v;
+    } else { /* 3: v promoted and, the pool's lowest, leaves at once */
+        u->dec_slot = v_new ? u->cap : v;
+    }
+
+    /* Diagnostic: the smallest relative gap of the comparisons that decided
+     * -- the two lowest of the recent pool plus the new token, score(v)
+     * against the threshold, the two lowest of the heavy-hitter pool plus v
+     * when it overflowed. */
+    double gap = rel_gap(sv, u->hh_threshold);
+    for (int s = 0; s <= u->cap; ++s) { /* s == cap: the new token */
+        const int held = s < u->cap && u->pos[s] >= 0;
+        if (s < u->cap && !held) continue;
+        const double x = s < u->cap ? u->score[s] : sn;
+        const int in_rec = s == u->cap || u->pool[s] == 0;
+        const int is_v = v_new ? s == u->cap : s == v;
+        if (in_rec && !is_v) gap = fmin(gap, rel_gap(x, sv));
+        if (sv > u->hh_threshold && n_hh + 1 > u->n_heavy && s < u->cap && !in_rec) {
+            /* the heavy-hitter pool plus v: its lowest against every other member */
+            if (key_less(u->score[w], u->pos[w], sv, pv)) gap = fmin(gap, rel_gap(s == w ? sv : x, u->score[w]));
+            else gap = fmin(gap, rel_gap(x, sv));
+        }
+    }
+    u->dec_margin = gap;
+    return u->dec_slot;
+}
+
 int orc_choose(orc_unit *u)
 {
     if (!u->have_new) return ORC_ESTATE;
     switch (u->policy) {
     case ORC_H2O: return choose_h2o(u);
     case ORC_SINK_WINDOW: return choose_sink_window(u);
+    case ORC_H2O_POOLS: return choose_pools(u);
     default: return first_free_slot(u); /* Random, H2O_BLOCK: the lowest free slot */
     }
 }
@@ -522,9 +650,52 @@ static void random_cut(orc_unit *u, int step)
     free(dr);
 }
 
+/* Two-pool H2O: admit the new token into `slot` in pool `new_pool` (slot ==
+ * cap: the new token leaves), evicting what the slot held, and move the token
+ * in slot `promote` (-1: none) to the heavy-hitter pool. Checked for
+ * consistency with the pools' sizes; any such decision is accepted, so that
+ * a caller can adopt another implementation's choice at a near-tie. */
+int orc_commit_pools(orc_unit *u, int slot, int new_pool, int promote)
+{
+    if (!u->have_new || u->policy != ORC_H2O_POOLS) return ORC_ESTATE;
+    if (slot < 0 || slot > u->cap || (new_pool != 0 && new_pool != 1)) return ORC_EINVAL;
+    if (promote >= 0 && (promote >= u->cap || promote == slot || u->pos[promote] < 0 || u->pool[promote] != 0))
+        return ORC_EINVAL;
+    if (promote < -1 || (promote >= 0 && new_pool == 1) || (slot == u->cap && (promote >= 0 || new_pool == 1)))
+        return ORC_EINVAL;
+    int n_rec = 0, n_hh = 0;
+    for (int s = 0; s < u->cap; ++s)
+        if (u->pos[s] >= 0 && s != slot) { n_rec += u->pool[s] == 0; n_hh += u->pool[s] == 1; }
+    if (promote >= 0) { n_rec--; n_hh++; }
+    if (slot < u->cap) { if (new_pool) n_hh++; else n_rec++; }
+    if (n_rec > u->n_recent || n_hh > u->n_heavy) return ORC_EINVAL;
+    if (promote >= 0) u->pool[promote] = 1;
+    u->last_promote = promote >= 0 ? promote : (new_pool ? -2 : -1);
+    u->have_new = 0;
+    if (slot == u->cap) { /* the new token leaves */
+        u->last_victim_pos = u->new_pos;
+        u->evicted_mass += u->score_new;
+    } else {
+        u->last_victim_pos = u->pos[slot];
+        if (u->pos[slot] >= 0) u->evicted_mass += u->score[slot];
+        u->pos[slot] = u->new_pos;
+        u->pool[slot] = (signed char)new_pool;
+        memcpy(u->k + (size_t)slot * u->d, u->k_new, sizeof(float) * (size_t)u->d);
+        memcpy(u->v + (size_t)slot * u->d, u->v_new, sizeof(float) * (size_t)u->d);
+        u->score[slot] = u->score_new;
+    }
+    if (u->is_prompt) u->prompt_len++;
+    else u->t++;
+    return ORC_OK;
+}
+
 int orc_commit(orc_unit *u, int slot)
 {
     if (!u->have_new) return ORC_ESTATE;
+    if (u->policy == ORC_H2O_POOLS) {
+        if (slot != u->dec_slot) return ORC_EINVAL; /* orc_commit_pools takes another decision */
+        return orc_commit_pools(u, slot, u->dec_pool, u->dec_promote);
+    }
     if (slot < 0 || slot >= u->cap) return ORC_EINVAL;
     u->last_victim_pos = u->pos[slot];
     if (u->pos[slot] >= 0 && (u->policy == ORC_H2O || u->policy == ORC_H2O_BLOCK)) u->evicted_mass += u->score[slot];
@@ -557,7 +728,8 @@ int orc_prefill(orc_unit *u, const float *k, const float *v, int n)
         if (rc) return rc;
         int slot = orc_choose(u);
         if (slot < 0) { u->have_new = 0; return ORC_ECAPACITY; }
-        orc_commit(u, slot);
+        rc = orc_commit(u, slot);
+        if (rc) return rc;
     }
     return ORC_OK;
 }
@@ -774,7 +946,8 @@ int orc_prefill_snapkv(orc_unit *u, const float *q_obs, const float *k, const fl
     return rc;
 }
 
-/* One full decode step with the oracle's own decision. Returns the slot taken. */
+/* One full decode step with the oracle's own decision. Returns the slot taken
+ * (two-pool H2O: the capacity when the new token itself left). */
 int orc_step(orc_unit *u, const float *q, const float *k_new, const float *v_new, double *out)
 {
     int rc = orc_attend(u, q, k_new, v_new, out);

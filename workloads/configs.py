@@ -18,12 +18,13 @@ POLICY_H2O = 0
 POLICY_SINK_WINDOW = 1
 POLICY_RANDOM = 2
 POLICY_H2O_BLOCK = 3
+POLICY_H2O_POOLS = 4
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
 
 POLICY_NAMES = {POLICY_H2O: "h2o", POLICY_SINK_WINDOW: "sink_window", POLICY_RANDOM: "random",
-                POLICY_H2O_BLOCK: "h2o_block"}
+                POLICY_H2O_BLOCK: "h2o_block", POLICY_H2O_POOLS: "h2o_pools"}
 
 
 @dataclass(frozen=True)
@@ -47,6 +48,7 @@ class Workload:
     max_prompt: int = 0
     score_forget: float = 0.0  # H2O score storage: s <- (1 - score_forget) s + a
     score_half: bool = False   # H2O score storage: binary16
+    hh_threshold: float = 0.0  # two-pool H2O: promotion needs a score above this
 
     @property
     def group(self) -> int:
