@@ -198,8 +198,9 @@ def oracle_sample_rate(w, n_units: int, target_s: float, max_steps: int = 4096):
     M = int(max(1, min(max_steps, target_s / max(one, 1e-6))))
     xs = [synth.UnitInputs(w, seq, 0, h, 1 + M, P) for seq, h in ids]
     dt = timed(xs, 1, 1 + M)
+    start = "the cache after the prompt" if w.policy == configs.POLICY_H2O_POOLS else "a full cache"
     desc = (f"{n_units} units of one layer (of {w.batch * w.n_kv_heads} per layer, {w.n_layers} layers) "
-            f"x {M} decode steps from a full cache, {dt:.1f} s")
+            f"x {M} decode steps from {start}, {dt:.1f} s")
     return n_units * M / dt, threads, desc, dt
 
 
@@ -256,6 +257,10 @@ def run_ours(args, w, rank, world, device):
         elif w.policy in (configs.POLICY_H2O, configs.POLICY_H2O_BLOCK) and P < w.capacity:
             # fill the cache: every timed step evicts (H2O_BLOCK: releases a block every r steps)
             n_pre = w.capacity - P
+        elif w.policy == configs.POLICY_H2O_POOLS and (w.hh_threshold >= 0 or P < w.capacity):
+            # the prompt leaves the recent pool only; the heavy-hitter pool fills with
+            # the promotions of the next steps (held counts are read after timing)
+            n_pre = 2 * w.capacity
         n_win = args.warmup + args.steps
         q, kn, vn = synth.device_window(w, P + n_pre, n_win, device)
         out = torch.empty((2, L, B, Hq, D), dtype=q.dtype, device=device)
@@ -330,10 +335,13 @@ def run_ours(args, w, rank, world, device):
             d2h = L * out[0, 0].numel() * q.element_size()
             e2e = {"value": world * B * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h, "steps": n_e2e}
+        held = None
+        if w.policy == configs.POLICY_H2O_POOLS:  # data-dependent occupancy: the mean held fraction
+            held = float(np.mean([(cache.slot_positions(layer) >= 0).float().mean().item() for layer in range(L)]))
         cache.close()
     return dict(dt_ms=dt_ms, clocks=clk.summary(), decode_launches=decode_launches, cut_launches=cut_launches,
                 iso_ms=iso, e2e=e2e, split=st["split"], clusters=st["clusters"], tensor_cores=st["tensor_cores"],
-                ring_stages=st["ring_stages"])
+                ring_stages=st["ring_stages"], held=held)
 
 
 # ---------------------------------------------------------------------------
@@ -710,6 +718,10 @@ def main():
     launches = r["decode_launches"]
     avg_launch_s = dt_s / max(1, launches)
     layer_bytes = traffic.steady_layer_step_bytes(w)
+    if r["held"] is not None:  # two-pool H2O: the tokens actually held
+        layer_bytes = w.batch * w.n_kv_heads * traffic.unit_step_bytes(w, int(round(r["held"] * w.capacity)))
+        cfg["held_fraction"] = r["held"]
+        cfg["hh_threshold"] = w.hh_threshold
     achieved = layer_bytes / avg_launch_s / 1e9
     peak, peak_kind = measured_hbm_peak()
     out = {

@@ -61,7 +61,8 @@ typedef enum {
     KVEVICT_H2O = 0,          /* sink + heavy hitters + recent window */
     KVEVICT_SINK_WINDOW = 1,  /* StreamingLLM: sink + ring window, no scores */
     KVEVICT_RANDOM = 2,       /* Random Attention: prompt kept, periodic random cut */
-    KVEVICT_H2O_BLOCK = 3     /* H2O scores, whole blocks of r slots released at a time */
+    KVEVICT_H2O_BLOCK = 3,    /* H2O scores, whole blocks of r slots released at a time */
+    KVEVICT_H2O_POOLS = 4     /* H2O scores, a recent pool and a heavy-hitter pool (hh_threshold) */
 } kvevict_policy;
 
 typedef enum { KVEVICT_F32 = 0, KVEVICT_BF16 = 1 } kvevict_dtype;
@@ -102,6 +103,19 @@ typedef enum {
  *                  before the token attends ("Attention Sinks 与 KV Cache 淘汰
  *                  策略" section 5: a paged cache frees whole blocks); the token
  *                  and the next r - 1 fill its slots in order.
+ *     H2O_POOLS:   the H2OCache class of "KV Cache 驱逐策略：从 LRU 到 H2O"
+ *                  (section "实现要点"): n_sink = 0, budget = n_recent +
+ *                  n_heavy, n_recent >= 1. Each held token belongs to the
+ *                  recent pool or the heavy-hitter pool. The new token joins
+ *                  the recent pool; when that pool then holds more than
+ *                  n_recent tokens, its member with the lowest (score,
+ *                  position) leaves it, the new token included. That token is
+ *                  promoted to the heavy-hitter pool iff its score is strictly
+ *                  above hh_threshold, and leaves the cache otherwise; a
+ *                  heavy-hitter pool above n_heavy tokens drops its lowest
+ *                  member, the promoted one included. The new token takes the
+ *                  slot of the token that left, else the lowest empty slot;
+ *                  when it leaves itself, no slot changes. Scores as H2O.
  *   batch, n_layers, n_q_heads, n_kv_heads, head_dim: model shape;
  *     n_q_heads / n_kv_heads = G in {1, 2, 4, 8}; head_dim in {64, 128}.
  *   dtype: KVEVICT_F32 or KVEVICT_BF16 for K, V, q and out.
@@ -112,9 +126,11 @@ typedef enum {
  *     0 <= score_forget < 1 (0, the default: the exact cumulative score; H2O
  *     and H2O_BLOCK). score_half = 1 stores every score as IEEE binary16
  *     (rounded to nearest even after each update; eviction compares the stored
- *     values), halving the score traffic; H2O only, and not with
+ *     values), halving the score traffic; H2O and H2O_POOLS, and not with
  *     kvevict_prefill_scored / kvevict_prefill_snapkv. kvevict_scores still
- *     returns fp32.
+ *     returns fp32. score_forget also applies to H2O_POOLS.
+ *   hh_threshold: H2O_POOLS only, the promotion threshold (any value but NaN;
+ *     the pages leave it open; -INFINITY promotes every token).
  * Slot capacity per unit: C = budget (H2O, SINK_WINDOW, H2O_BLOCK) or
  * max_prompt + budget + r (RANDOM).
  */
@@ -127,12 +143,14 @@ typedef struct {
     int max_prompt;
     float score_forget;
     int score_half;
+    float hh_threshold;
 } kvevict_config;
 
 typedef struct {
     int64_t decode_steps;   /* layer-steps issued (one per kvevict_decode_step call) */
     int64_t prefill_tokens; /* prompt tokens appended, summed over layers */
-    int64_t evictions;      /* tokens evicted, summed over units and layers */
+    int64_t evictions;      /* tokens evicted, summed over units and layers (H2O_POOLS: unit-steps in which the
+                               recent pool overflowed; a promotion into a pool with room evicts nothing) */
     int64_t cuts;           /* Random cuts or H2O_BLOCK releases, summed over layers (each over every unit) */
     int split;              /* CTAs per unit in the decode launch (thread-block cluster size) */
     int capacity;           /* slots per unit */
@@ -162,7 +180,11 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
  * the newest C - n_sink prompt tokens, and RANDOM keeps them all.
  * K, V: device, [batch][n_kv_heads][n_tokens][head_dim]. May be called several
  * times (chunks) before the layer's first decode step; STATE after it.
- * RANDOM: CAPACITY if the layer's prompt would exceed max_prompt. */
+ * RANDOM: CAPACITY if the layer's prompt would exceed max_prompt.
+ * H2O_POOLS: the whole prompt in one call (STATE otherwise); with every score
+ * 0 the recent pool's oldest member leaves each time, so hh_threshold >= 0
+ * keeps the last n_recent prompt tokens and hh_threshold < 0 the last C, the
+ * ones before the last n_recent in the heavy-hitter pool. */
 int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_tokens);
 
 /* Q-seeded prefill of an empty H2O layer ("h2o: heavy-hitter oracle" summary,
@@ -272,18 +294,27 @@ int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_devi
  * INVALID_ARG for policies that keep no scores. Same dst rules as above. */
 int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device);
 
+/* Pool of every slot of `layer` (H2O_POOLS only, else INVALID_ARG): 0 the
+ * recent pool, 1 the heavy-hitter pool, meaningful where the slot holds a
+ * token; dst [batch][n_kv_heads][C] uint8. Same dst rules as above. */
+int kvevict_slot_pools(kvevict_t h, int layer, uint8_t *dst, int dst_is_device);
+
 /* Decode-step trace of `layer`: while set, decode step t (0-based, counted
  * from this call), for t < n_steps, writes for every unit four int32 into
  * dev_buf[t][batch][n_kv_heads][4] (device, 16-byte aligned): the slot the
  * new token took, the position that slot held before (-1 if it was empty:
  * otherwise the evicted token), the evicted token's cumulative score and the
  * new token's score (fp32 bit patterns; 0 for policies without scores).
+ * H2O_POOLS: the slot is -1 when the new token itself left (the next two
+ * words are then its position and score), and the fourth word records the
+ * promotion: the slot of the token moved to the heavy-hitter pool, -2 when
+ * the new token joined that pool, -1 when nothing was promoted.
  * dev_buf = NULL clears it. */
 int kvevict_set_trace(kvevict_t h, int layer, int32_t *dev_buf, int n_steps);
 
 /* Host-side counters of `layer`: prompt tokens appended, decode steps issued
- * and tokens held per unit (after the last issued step). Any pointer may be
- * NULL. */
+ * and tokens held per unit (after the last issued step; H2O_POOLS: an upper
+ * bound, a unit may hold fewer). Any pointer may be NULL. */
 int kvevict_layer_state(kvevict_t h, int layer, int *prompt_len, int *steps, int *count);
 
 /* CTAs per unit of the decode launch (1, 2, 4, 8 or 16; 0 = automatic).

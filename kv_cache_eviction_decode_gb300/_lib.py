@@ -11,7 +11,7 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvevict.so")
 
-H2O, SINK_WINDOW, RANDOM, H2O_BLOCK = 0, 1, 2, 3
+H2O, SINK_WINDOW, RANDOM, H2O_BLOCK, H2O_POOLS = 0, 1, 2, 3, 4
 F32, BF16 = 0, 1
 
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_STATE, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5
@@ -24,7 +24,7 @@ class Config(ctypes.Structure):
                 ("seed", ctypes.c_uint64), ("batch", ctypes.c_int), ("n_layers", ctypes.c_int),
                 ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("max_prompt", ctypes.c_int), ("score_forget", ctypes.c_float),
-                ("score_half", ctypes.c_int)]
+                ("score_half", ctypes.c_int), ("hh_threshold", ctypes.c_float)]
 
 
 class Stats(ctypes.Structure):
@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
             L.kvevict_decode_step_host.argtypes = [P, I, P, P, P, P]
             L.kvevict_slot_positions.argtypes = [P, I, P, I]
             L.kvevict_scores.argtypes = [P, I, P, I]
+            L.kvevict_slot_pools.argtypes = [P, I, P, I]
             L.kvevict_set_trace.argtypes = [P, I, P, I]
             L.kvevict_layer_state.argtypes = [P, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
             L.kvevict_set_split.argtypes = [P, I]
@@ -80,7 +81,8 @@ def lib() -> ctypes.CDLL:
             for n in ("kvevict_state_bytes", "kvevict_create", "kvevict_prefill", "kvevict_prefill_scored_workspace_bytes",
                       "kvevict_prefill_scored", "kvevict_prefill_scored_static",
                       "kvevict_prefill_snapkv_workspace_bytes", "kvevict_prefill_snapkv", "kvevict_decode_step",
-                      "kvevict_decode_step_host", "kvevict_slot_positions", "kvevict_scores", "kvevict_set_trace",
+                      "kvevict_decode_step_host", "kvevict_slot_positions", "kvevict_scores", "kvevict_slot_pools",
+                      "kvevict_set_trace",
                       "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",
                       "kvevict_check"):

@@ -33,17 +33,21 @@ constexpr int kSMs = 152;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Policies that keep cumulative attention scores.
-bool scored(int policy) { return policy == KVEVICT_H2O || policy == KVEVICT_H2O_BLOCK; }
+bool scored(int policy)
+{
+    return policy == KVEVICT_H2O || policy == KVEVICT_H2O_BLOCK || policy == KVEVICT_H2O_POOLS;
+}
 
 struct Layout {
     int C = 0, G = 0, elem = 0;
     int Cs = 0;               // per-unit stride of pos/score (rows start on 16 bytes)
     int score_elem = 4;       // bytes per stored score
+    int Ps = 0;               // per-unit stride of the pool flags (two-pool H2O; rows start on 16 bytes)
     size_t units = 0;         // B * Hkv
     size_t layer_slots = 0;   // units * C (K/V rows)
     size_t layer_pslots = 0;  // units * Cs (pos/score entries)
     size_t kv_layer_bytes = 0;
-    size_t off_k = 0, off_v = 0, off_pos = 0, off_score = 0, off_free = 0, off_err = 0;
+    size_t off_k = 0, off_v = 0, off_pos = 0, off_score = 0, off_pool = 0, off_free = 0, off_err = 0;
     size_t off_sq = 0, off_sk = 0, off_sv = 0, off_so = 0;
     size_t total = 0;
     size_t q_bytes = 0, kvtok_bytes = 0;  // one layer-step's q/out and k_new/v_new
@@ -82,6 +86,11 @@ int validate(const kvevict_config *c)
             if ((nb - nsb - 1) * c->r < c->n_recent) return KVEVICT_ERR_INVALID_ARG;
         }
         break;
+    case KVEVICT_H2O_POOLS:
+        if (c->n_sink != 0 || c->n_heavy < 0 || c->n_recent < 1 ||
+            static_cast<long long>(c->n_heavy) + c->n_recent != c->budget || std::isnan(c->hh_threshold))
+            return KVEVICT_ERR_INVALID_ARG;
+        break;
     case KVEVICT_RANDOM:
         if (c->r < 1 || c->max_prompt < 0 || c->n_sink != 0 || c->n_heavy != 0 || c->n_recent != 0)
             return KVEVICT_ERR_INVALID_ARG;
@@ -92,9 +101,8 @@ int validate(const kvevict_config *c)
     }
     if (!(c->score_forget >= 0.f && c->score_forget < 1.f) || (c->score_half != 0 && c->score_half != 1))
         return KVEVICT_ERR_INVALID_ARG;
-    if (c->score_forget != 0.f && c->policy != KVEVICT_H2O && c->policy != KVEVICT_H2O_BLOCK)
-        return KVEVICT_ERR_INVALID_ARG;
-    if (c->score_half && c->policy != KVEVICT_H2O) return KVEVICT_ERR_INVALID_ARG;
+    if (c->score_forget != 0.f && !scored(c->policy)) return KVEVICT_ERR_INVALID_ARG;
+    if (c->score_half && c->policy != KVEVICT_H2O && c->policy != KVEVICT_H2O_POOLS) return KVEVICT_ERR_INVALID_ARG;
     const long long C = c->policy == KVEVICT_RANDOM ? static_cast<long long>(c->max_prompt) + c->budget + c->r
                                                     : c->budget;
     if (C > (1 << 24)) return KVEVICT_ERR_INVALID_ARG;
@@ -111,6 +119,7 @@ Layout make_layout(const kvevict_config *c)
     // a multiple of 4, binary16 scores a multiple of 8
     L.Cs = c->score_half ? (L.C + 7) / 8 * 8 : (L.C + 3) / 4 * 4;
     L.score_elem = c->score_half ? 2 : 4;
+    L.Ps = c->policy == KVEVICT_H2O_POOLS ? (L.C + 15) / 16 * 16 : 0;
     L.units = static_cast<size_t>(c->batch) * c->n_kv_heads;
     L.layer_slots = L.units * L.C;
     L.layer_pslots = L.units * L.Cs;
@@ -121,6 +130,7 @@ Layout make_layout(const kvevict_config *c)
     L.off_v = off; off = align_up(off + nl * L.kv_layer_bytes);
     L.off_pos = off; off = align_up(off + nl * L.layer_pslots * 4);
     L.off_score = off; if (scored(c->policy)) off = align_up(off + nl * L.layer_pslots * L.score_elem);
+    L.off_pool = off; off = align_up(off + nl * L.units * L.Ps);
     L.off_free = off;
     if (c->policy == KVEVICT_RANDOM || c->policy == KVEVICT_H2O_BLOCK) off = align_up(off + nl * L.units * c->r * 4);
     L.off_err = off; off = align_up(off + 16);
@@ -144,6 +154,7 @@ struct LayerState {
     int32_t *trace = nullptr;
     int trace_len = 0, trace_t = 0;
     int fill_left = 0;   // H2O after a SnapKV prefill: steps left in which a unit may still have empty slots
+    int n_rec = 0;       // H2O_POOLS: tokens in every unit's recent pool (count is then an upper bound)
     int blk_left = 0;    // H2O_BLOCK: slots of the open (released) block not yet refilled
     int blk_next = 0;    // H2O_BLOCK: next slot of the open block when every unit's is the same
     bool blk_uniform = false;  // H2O_BLOCK: the open block is the same slot range in every unit
@@ -193,7 +204,15 @@ int max_slots_per_cta(const Layout &L, int S)
     return ((tiles + S - 1) / S) * kTile;
 }
 
-int n_aux_arrays(const kvevict_config &c, bool holes) { return scored(c.policy) ? 2 : (holes ? 1 : 0); }
+int n_aux_arrays(const kvevict_config &c, bool holes)
+{
+    if (c.policy == KVEVICT_H2O_POOLS) return 3;  // positions, scores, pool flags
+    return scored(c.policy) ? 2 : (holes ? 1 : 0);
+}
+
+// Launches whose units may hold empty slots among the scanned ones (positions
+// are then read before attention).
+bool holes_policy(const kvevict_config &c) { return c.policy == KVEVICT_RANDOM || c.policy == KVEVICT_H2O_POOLS; }
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
@@ -227,9 +246,9 @@ size_t decode_smem(const kvevict_handle *h, int S, bool holes, int *nst_out = nu
 int auto_split(const kvevict_handle *h)
 {
     const Layout &L = h->L;
-    const bool random = h->cfg.policy == KVEVICT_RANDOM;
+    const bool holes = holes_policy(h->cfg);
     for (int S = 1; S <= kMaxSplit; S *= 2) {
-        if (decode_smem(h, S, random) > kMaxSmem) continue;
+        if (decode_smem(h, S, holes) > kMaxSmem) continue;
         if (S < 8 && static_cast<long long>(L.units) * S < 2LL * kSMs && L.C / (2 * S) >= 256) continue;
         return S;
     }
@@ -410,6 +429,18 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
             }
         }
         break;
+    case KVEVICT_H2O_POOLS:
+        // ls.count bounds every unit's occupancy; a unit's tokens fill slots
+        // 0, 1, ... (a slot is only freed for the token that takes it)
+        P.n_active = ls.count;
+        P.mode = kTwoPool;
+        P.pool = at<uint8_t>(h, L.off_pool) + static_cast<size_t>(layer) * L.units * L.Ps;
+        P.pstride = L.Ps;
+        P.recent_full = ls.n_rec == c.n_recent ? 1 : 0;
+        P.hh_threshold = c.hh_threshold;
+        holes = true;
+        if (P.recent_full) evicted = static_cast<long long>(L.units);
+        break;
     case KVEVICT_SINK_WINDOW:
         P.n_active = ls.count;
         P.mode = kInsertAt;
@@ -496,6 +527,10 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     case KVEVICT_H2O:
         ls.count = std::min(L.C, ls.count + 1);
         if (ls.fill_left > 0) ls.fill_left--;
+        break;
+    case KVEVICT_H2O_POOLS:
+        ls.count = std::min(L.C, ls.count + 1);
+        ls.n_rec = std::min(c.n_recent, ls.n_rec + 1);
         break;
     case KVEVICT_H2O_BLOCK:
         if (ls.count < L.C) {
@@ -592,6 +627,8 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_pslots * 4, h->stream);
     if (e == cudaSuccess && scored(cfg->policy))
         e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_pslots * L.score_elem, h->stream);
+    if (e == cudaSuccess && L.Ps > 0)
+        e = cudaMemsetAsync(h->state + L.off_pool, 0, cfg->n_layers * L.units * L.Ps, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
     if (e != cudaSuccess) {
         delete h;
@@ -638,6 +675,17 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
     } else {
         P.n_sink = c.n_sink;
         P.ring_len = L.C - c.n_sink;
+        if (c.policy == KVEVICT_H2O_POOLS) {
+            // every prompt score is 0, so the recent pool's oldest member leaves each
+            // time: dropped (threshold >= 0: the last n_recent stay, a ring of
+            // n_recent slots) or promoted (threshold < 0: the last C stay, a ring of
+            // C slots, the ones before the last n_recent in the heavy-hitter pool)
+            if (ls.prompt_len != 0) return KVEVICT_ERR_STATE;  // the whole prompt in one call
+            P.ring_len = c.hh_threshold >= 0.f ? c.n_recent : L.C;
+            P.pool = at<uint8_t>(h, L.off_pool) + static_cast<size_t>(layer) * L.units * L.Ps;
+            P.pstride = L.Ps;
+            P.hh_below = n_tokens - c.n_recent;
+        }
         P.a0 = 0;
         P.a1 = std::min(n_tokens, std::max(0, c.n_sink - P.p0));
         P.b0 = std::max({0, c.n_sink - P.p0, n_tokens - P.ring_len});
@@ -684,6 +732,10 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
     h->last_layer = layer;
     ls.prompt_len += n_tokens;
     ls.count = c.policy == KVEVICT_RANDOM ? ls.prompt_len : std::min(L.C, ls.prompt_len);
+    if (c.policy == KVEVICT_H2O_POOLS) {
+        ls.count = std::min(P.ring_len, n_tokens);
+        ls.n_rec = std::min(c.n_recent, n_tokens);
+    }
     h->stats.prefill_tokens += n_tokens;
     return KVEVICT_OK;
 }
@@ -980,6 +1032,19 @@ int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
     return cuda_status(e);
 }
 
+int kvevict_slot_pools(kvevict_t h, int layer, uint8_t *dst, int dst_is_device)
+{
+    if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
+    if (h->cfg.policy != KVEVICT_H2O_POOLS) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    const Layout &L = h->L;
+    const void *src = at<uint8_t>(h, L.off_pool) + static_cast<size_t>(layer) * L.units * L.Ps;
+    cudaError_t e = cudaMemcpy2DAsync(dst, L.C, src, L.Ps, L.C, L.units,
+                                      dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
+    return cuda_status(e);
+}
+
 int kvevict_set_trace(kvevict_t h, int layer, int32_t *dev_buf, int n_steps)
 {
     if (!h) return KVEVICT_ERR_INVALID_ARG;
@@ -1010,7 +1075,7 @@ int kvevict_set_split(kvevict_t h, int split)
         h->split = auto_split(h);
     } else {
         if (split < 1 || split > kMaxSplit || (split & (split - 1))) return KVEVICT_ERR_INVALID_ARG;
-        if (decode_smem(h, split, h->cfg.policy == KVEVICT_RANDOM) > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
+        if (decode_smem(h, split, holes_policy(h->cfg)) > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
         h->split = split;
     }
     h->stats.split = h->split;

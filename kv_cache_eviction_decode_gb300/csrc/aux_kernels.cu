@@ -13,8 +13,9 @@ namespace kvevict {
 // Prompt tokens enter with score 0 and no attention. For H2O (all scores
 // equal, ties to the older position) and StreamingLLM that keeps the first
 // n_sink positions in slots 0..n_sink-1 and the newest C - n_sink in ring
-// order: slot(p) = n_sink + (p - n_sink) mod (C - n_sink). Random keeps every
-// prompt token: slot(p) = p. Rows of this chunk: range A = [a0, a1) (sinks or,
+// order: slot(p) = n_sink + (p - n_sink) mod (C - n_sink). Two-pool H2O is a
+// ring without sinks, of n_recent or C slots, its older part flagged as heavy
+// hitters. Random keeps every prompt token: slot(p) = p. Rows of this chunk: range A = [a0, a1) (sinks or,
 // for Random, everything), range B = [b0, b1) (kept ring rows). One warp per
 // row, 16-byte vector copies.
 __global__ void __launch_bounds__(256) prefill_kernel(const PrefillParams P)
@@ -43,6 +44,7 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillParams P)
     }
     if (lane == 0) {
         P.pos[unit * P.cstride + slot] = p;
+        if (P.pool) P.pool[unit * P.pstride + slot] = p < P.hh_below ? 1 : 0;
         if (P.score) {
             if (P.score_half) static_cast<uint16_t *>(P.score)[unit * P.cstride + slot] = 0;  // +0 in binary16
             else static_cast<float *>(P.score)[unit * P.cstride + slot] = 0.f;

@@ -19,6 +19,8 @@ struct PrefillParams {
     int n_tok, p0, C, cstride, Hkv, head_dim, elem_bytes;
     int n_sink, ring_len;  // ring_len = C - n_sink for ring policies, 0 for Random
     int a0, a1, b0, b1;    // chunk rows to copy
+    uint8_t *pool;         // two-pool H2O: pool flags [B][Hkv][pstride], else null
+    int pstride, hh_below; // positions below hh_below go to the heavy-hitter pool
 };
 
 struct CutParams {

@@ -78,8 +78,9 @@ enum InsertMode : int {
     kInsertAt = 0,     // the host gives the slot (empty slot, or the ring slot)
     kH2OEvict = 1,     // cache full: evict the lowest-score eligible token
     kFromFreeList = 2, // Random after a cut: next entry of the unit's free list
-    kH2OFill = 3       // H2O with per-unit empty slots (after a SnapKV prefill): the unit's
+    kH2OFill = 3,      // H2O with per-unit empty slots (after a SnapKV prefill): the unit's
                        // lowest empty slot if it has one, else evict as kH2OEvict
+    kTwoPool = 4       // two-pool H2O: a recent pool and a heavy-hitter pool (per-slot pool flags)
 };
 
 // Opaque 128-byte tensor map (CUtensorMap), 64-byte aligned as a kernel
@@ -115,6 +116,11 @@ struct DecodeParams {
     float scale_log2;    // log2(e) / sqrt(D)
     float score_keep;    // each step s <- score_keep * s + a (1: the exact cumulative score)
     int score_half;      // scores stored as IEEE binary16 (cstride a multiple of 8)
+    // two-pool H2O (kTwoPool)
+    uint8_t *pool;       // [B][Hkv][pstride]: 0 recent pool, 1 heavy-hitter pool (slots holding a token)
+    int pstride;         // per-unit stride of the pool flags (C rounded up to 16)
+    int recent_full;     // every unit's recent pool holds n_recent tokens before this step
+    float hh_threshold;  // a token leaving the recent pool is promoted iff its score is above this
 };
 
 // Stored cumulative scores: fp32, or binary16 rounded to nearest even.
@@ -174,11 +180,16 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
         alignas(16) float xo[2][G * D];
         uint64_t xkey[2][kMaxSplit];
         int32_t xslot[2][kMaxSplit];
-        int32_t xempty[2][kMaxSplit];  // fill mode: every CTA's lowest empty slot
+        int32_t xempty[2][kMaxSplit];  // fill and two-pool modes: every CTA's lowest empty slot
+        uint64_t xkey2[2][kMaxSplit];  // two-pool mode: every CTA's heavy-hitter candidate
+        int32_t xslot2[2][kMaxSplit];
         float xanew[2];
+        float anew;  // the new token's score (one CTA per unit)
         uint64_t wkey[kWarps];
         int32_t wslot[kWarps];
         int32_t wempty[kWarps];
+        uint64_t wkey2[kWarps];
+        int32_t wslot2[kWarps];
     };
 
     // zcap = slots per CTA rounded to whole tiles, padded so that the head
@@ -193,8 +204,8 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
     // Layout: [ring: nst stages][logits][warp partials][aux][misc].
     __host__ __device__ static size_t off_z(int nst) { return static_cast<size_t>(nst) * kStageBytes; }
     __host__ __device__ static size_t off_part(int zc, int nst) { return off_z(nst) + ((static_cast<size_t>(G) * zc * 4 + 127) / 128) * 128; }
-    // aux: the unit's slot positions and, with scores (H2O), the cumulative
-    // scores: n_arrays = 0 (none), 1 or 2.
+    // aux: the unit's slot positions, with scores (H2O) the cumulative scores,
+    // and in two-pool mode the pool flags: n_arrays = 0 (none), 1, 2 or 3.
     __host__ __device__ static size_t off_aux(int zc, int nst) { return off_part(zc, nst) + kPartBytes; }
     __host__ __device__ static size_t aux_bytes(int zc) { return ((static_cast<size_t>(zc) * 4 + 15) / 16) * 16; }
     __host__ __device__ static size_t off_misc(int zc, int n_arrays, int nst) { return off_aux(zc, nst) + n_arrays * aux_bytes(zc); }
@@ -261,6 +272,50 @@ __device__ __forceinline__ int32_t warp_min_s32(int32_t v)
 template <typename T> struct alignas(2 * sizeof(T)) TPair {
     T x, y;
 };
+
+constexpr uint64_t kEmptyKey = 0x00000000FFFFFFFFull;  // no token leaves: position -1, score 0
+
+// Two-pool H2O, the add step of the H2OCache class ("KV Cache 驱逐策略：从 LRU
+// 到 H2O", section "实现要点"). The new token joins the recent pool; when that
+// pool overflows, its lowest (score, position) member v leaves it -- the new
+// token is a member -- and is promoted to the heavy-hitter pool iff its score
+// is above hh_threshold, else it leaves the cache; an overfull heavy-hitter
+// pool drops its lowest member, v included. Inputs: the recent pool's lowest
+// key kv at slot sv, the heavy-hitter pool's lowest kw at slot sw (~0 when
+// it is empty), the unit's lowest empty slot em (INT_MAX: none) and the new
+// token's key kn. A key is (score bits << 32 | position); scores are >= 0.
+struct PoolDecision {
+    int dest;          // slot that receives the new token; -1: the new token leaves
+    int new_pool;      // the pool it joins
+    int promote;       // slot of a held token moved to the heavy-hitter pool; -1: none
+    uint64_t evicted;  // key of the token that leaves the cache; kEmptyKey: none
+};
+
+__device__ __forceinline__ PoolDecision pool_decide(bool recent_full, float theta, uint64_t kv, int sv, uint64_t kw,
+                                                    int sw, int em, uint64_t kn)
+{
+    PoolDecision d{-1, 0, -1, kEmptyKey};
+    if (!recent_full) {  // room in the recent pool
+        d.dest = em;
+        return d;
+    }
+    const bool v_new = kn < kv;
+    const uint64_t k = v_new ? kn : kv;
+    if (!(__uint_as_float(static_cast<uint32_t>(k >> 32)) > theta) || (em == INT_MAX && k < kw)) {
+        d.evicted = k;  // v leaves the cache: below the threshold, or the lowest of a full pool
+        d.dest = v_new ? -1 : sv;
+        return d;
+    }
+    if (em != INT_MAX) {
+        d.dest = em;  // room in the heavy-hitter pool
+    } else {
+        d.dest = sw;  // the heavy-hitter pool's lowest leaves
+        d.evicted = kw;
+    }
+    if (v_new) d.new_pool = 1;
+    else d.promote = sv;
+    return d;
+}
 
 // The CTA's share of one launch: which units, which tiles of each.
 struct Work {
@@ -345,9 +400,10 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     float *part = reinterpret_cast<float *>(smem + L::off_part(zc, NST));
     uint8_t *aux = smem + L::off_aux(zc, NST);
     const size_t auxb = L::aux_bytes(zc);
-    // slot positions (and H2O scores) are prefetched per unit only when used
+    // slot positions (and H2O scores, pool flags) are prefetched per unit only when used
     const bool need_aux = P.score != nullptr || HOLES;
-    const int n_aux = P.score != nullptr ? 2 : (HOLES ? 1 : 0);
+    const bool pools = P.mode == kTwoPool;
+    const int n_aux = pools ? 3 : (P.score != nullptr ? 2 : (HOLES ? 1 : 0));
     auto &M = *reinterpret_cast<typename L::Misc *>(smem + L::off_misc(zc, n_aux, NST));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -403,13 +459,16 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
         const uint32_t bytes = static_cast<uint32_t>(((W.n_mine * 4 + 15) / 16) * 16);
         const uint32_t sbytes = P.score_half ? static_cast<uint32_t>(((W.n_mine * 2 + 15) / 16) * 16) : bytes;
-        const uint32_t tx = has_score ? bytes + sbytes : bytes;
+        const uint32_t pbytes = pools ? static_cast<uint32_t>(((W.n_mine + 15) / 16) * 16) : 0u;
+        const uint32_t tx = (has_score ? bytes + sbytes : bytes) + pbytes;
         mbar_arrive_expect_tx(&M.auxbar, tx);
         bulk_g2s(aux, P.pos + unit * CS + W.s_lo, bytes, &M.auxbar);
         if (has_score)
             bulk_g2s(aux + auxb,
                      static_cast<const uint8_t *>(P.score) + (unit * CS + W.s_lo) * (P.score_half ? 2 : 4), sbytes,
                      &M.auxbar);
+        if (pools)
+            bulk_g2s(aux + 2 * auxb, P.pool + unit * static_cast<size_t>(P.pstride) + W.s_lo, pbytes, &M.auxbar);
         M.aux_issued++;
     };
 
@@ -529,6 +588,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         const int32_t *apos = reinterpret_cast<const int32_t *>(aux);
         const float *ascore = reinterpret_cast<const float *>(aux + auxb);
         const __half *ascore_h = reinterpret_cast<const __half *>(aux + auxb);
+        const uint8_t *apool = aux + 2 * auxb;
         // this unit's stored score of local slot j, before this step
         auto stored_score = [&](int j) { return P.score_half ? __half2float(ascore_h[j]) : ascore[j]; };
 
@@ -858,12 +918,18 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         };
         constexpr int kPairs = G * D / 2;
         const bool fill = P.mode == kH2OFill;
-        const bool evict = P.mode == kH2OEvict || fill;  // a victim is chosen (fill: unless a slot is empty)
-        constexpr uint64_t kEmptyKey = 0x00000000FFFFFFFFull;  // trace of a fill: position -1, score 0
+        // a victim is chosen (fill: unless a slot is empty; two-pool: per the pools)
+        const bool evict = P.mode == kH2OEvict || fill || pools;
         int dest = -1;             // slot that receives the new token
         bool writer = false;       // this CTA writes it
         uint64_t win_key = ~0ull;  // H2O eviction: (score bits, position) of the evicted token
         float anew = 0.f;          // the new token's score (rank 0)
+        PoolDecision pd{-1, 0, -1, kEmptyKey};  // two-pool mode
+        // a held token is a candidate: sinks and the recent window excepted (H2O),
+        // or any held token, in the pool its flag names (two-pool)
+        auto candidate = [&](int ps) {
+            return pools ? ps >= 0 : (ps >= P.n_sink && ps <= P.p - P.n_recent);
+        };
 
         if (S == 1) {
             // ------------------------------ output, one CTA per unit: o / l
@@ -891,8 +957,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     invl[g] = 1.f / cta_l(g);
                     fself[g] = invl[g] * (1.0f / G);
                 }
-                uint64_t best = ~0ull;
-                int32_t bslot = -1, emin = INT_MAX;
+                uint64_t best = ~0ull, best2 = ~0ull;
+                int32_t bslot = -1, bslot2 = -1, emin = INT_MAX;
                 for (int j = tid; j < W.n_mine; j += kThreads) {
                     float a = 0.f;
 #pragma unroll
@@ -900,11 +966,16 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     const float sc = score_store(P, unit * CS + j, fmaf(P.score_keep, stored_score(j), a));
                     if (evict) {
                         const int ps = apos[j];
-                        if (fill && ps < 0 && j < emin) emin = j;
-                        if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
+                        if ((fill || pools) && ps < 0 && j < emin) emin = j;
+                        if (candidate(ps)) {
                             const uint64_t key =
                                 (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
-                            if (key < best) {
+                            if (pools && apool[j] != 0) {
+                                if (key < best2) {
+                                    best2 = key;
+                                    bslot2 = j;
+                                }
+                            } else if (key < best) {
                                 best = key;
                                 bslot = j;
                             }
@@ -916,14 +987,18 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
 #pragma unroll
                     for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], invl[g], a);
                     anew = score_round(P, a * (1.0f / G));
+                    M.anew = anew;
                 }
                 if (evict) {
                     warp_argmin(best, bslot);
-                    if (fill) emin = warp_min_s32(emin);
+                    if (pools) warp_argmin(best2, bslot2);
+                    if (fill || pools) emin = warp_min_s32(emin);
                     if (lane == 0) {
                         M.wkey[warp] = best;
                         M.wslot[warp] = bslot;
                         M.wempty[warp] = emin;
+                        M.wkey2[warp] = best2;
+                        M.wslot2[warp] = bslot2;
                     }
                 }
                 __syncthreads();  // (B) candidates visible; every read of this unit's aux data is done
@@ -932,8 +1007,23 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     uint64_t k = lane < kWarps ? M.wkey[lane] : ~0ull;
                     int32_t sl = lane < kWarps ? M.wslot[lane] : -1;
                     warp_argmin(k, sl);
-                    const int32_t em = fill ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
-                    if (em != INT_MAX) {  // an empty slot: no eviction
+                    int32_t em = (fill || pools) ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
+                    if (pools) {
+                        uint64_t k2 = lane < kWarps ? M.wkey2[lane] : ~0ull;
+                        int32_t sl2 = lane < kWarps ? M.wslot2[lane] : -1;
+                        warp_argmin(k2, sl2);
+                        if (P.n_active < P.C) em = min(em, P.n_active);  // the slots past the scanned ones are empty
+                        const uint64_t kn =
+                            (static_cast<uint64_t>(__float_as_uint(M.anew)) << 32) | static_cast<uint32_t>(P.p);
+                        pd = pool_decide(P.recent_full != 0, P.hh_threshold, k, sl, k2, sl2, em, kn);
+                        if (pd.dest == INT_MAX) {  // no room where the rule needs an empty slot
+                            if (tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                            pd.dest = -1;
+                            pd.promote = -1;
+                        }
+                        win_key = pd.evicted;
+                        dest = pd.dest;
+                    } else if (em != INT_MAX) {  // an empty slot: no eviction
                         win_key = kEmptyKey;
                         dest = em;
                     } else {
@@ -1005,8 +1095,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 float fself[G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
-                uint64_t best = ~0ull;
-                int32_t bslot = -1, emin = INT_MAX;
+                uint64_t best = ~0ull, best2 = ~0ull;
+                int32_t bslot = -1, bslot2 = -1, emin = INT_MAX;
                 for (int j = tid; j < W.n_mine; j += kThreads) {
                     float a = 0.f;
 #pragma unroll
@@ -1015,11 +1105,16 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                         score_store(P, unit * CS + W.s_lo + j, fmaf(P.score_keep, stored_score(j), a));
                     if (evict) {
                         const int ps = apos[j];
-                        if (fill && ps < 0 && W.s_lo + j < emin) emin = W.s_lo + j;
-                        if (ps >= P.n_sink && ps <= P.p - P.n_recent) {
+                        if ((fill || pools) && ps < 0 && W.s_lo + j < emin) emin = W.s_lo + j;
+                        if (candidate(ps)) {
                             const uint64_t key =
                                 (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
-                            if (key < best) {
+                            if (pools && apool[j] != 0) {
+                                if (key < best2) {
+                                    best2 = key;
+                                    bslot2 = W.s_lo + j;
+                                }
+                            } else if (key < best) {
                                 best = key;
                                 bslot = W.s_lo + j;
                             }
@@ -1034,25 +1129,36 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 }
                 if (evict) {
                     warp_argmin(best, bslot);
-                    if (fill) emin = warp_min_s32(emin);
+                    if (pools) warp_argmin(best2, bslot2);
+                    if (fill || pools) emin = warp_min_s32(emin);
                     if (lane == 0) {
                         M.wkey[warp] = best;
                         M.wslot[warp] = bslot;
                         M.wempty[warp] = emin;
+                        M.wkey2[warp] = best2;
+                        M.wslot2[warp] = bslot2;
                     }
                 }
                 __syncthreads();  // candidates visible; every read of this unit's aux data is done
                 if (evict && warp == 0) {
-                    // this CTA's candidate (and, filling, its lowest empty slot) to every
+                    // this CTA's candidates (and, filling, its lowest empty slot) to every
                     // CTA; rank 0's new-token score too
                     uint64_t k = lane < kWarps ? M.wkey[lane] : ~0ull;
                     int32_t sl = lane < kWarps ? M.wslot[lane] : -1;
                     warp_argmin(k, sl);
-                    const int32_t em = fill ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
+                    uint64_t k2 = lane < kWarps ? M.wkey2[lane] : ~0ull;
+                    int32_t sl2 = lane < kWarps ? M.wslot2[lane] : -1;
+                    if (pools) warp_argmin(k2, sl2);
+                    const int32_t em =
+                        (fill || pools) ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
                     if (lane < S) {
                         st_peer_u64(peer_addr(&M.xkey[b][rank], lane), k);
                         st_peer_s32(peer_addr(&M.xslot[b][rank], lane), sl);
                         st_peer_s32(peer_addr(&M.xempty[b][rank], lane), em);
+                        if (pools) {
+                            st_peer_u64(peer_addr(&M.xkey2[b][rank], lane), k2);
+                            st_peer_s32(peer_addr(&M.xslot2[b][rank], lane), sl2);
+                        }
                     }
                     if (rank == 0 && lane == 0)
                         for (int c = 0; c < S; ++c) st_peer_f32(peer_addr(&M.xanew[b], c), anew);
@@ -1067,8 +1173,23 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 uint64_t k = lane < S ? M.xkey[b][lane] : ~0ull;
                 int32_t sl = lane < S ? M.xslot[b][lane] : -1;
                 warp_argmin(k, sl);
-                const int32_t em = fill ? warp_min_s32(lane < S ? M.xempty[b][lane] : INT_MAX) : INT_MAX;
-                if (em != INT_MAX) {  // an empty slot: no eviction
+                int32_t em = (fill || pools) ? warp_min_s32(lane < S ? M.xempty[b][lane] : INT_MAX) : INT_MAX;
+                if (pools) {
+                    uint64_t k2 = lane < S ? M.xkey2[b][lane] : ~0ull;
+                    int32_t sl2 = lane < S ? M.xslot2[b][lane] : -1;
+                    warp_argmin(k2, sl2);
+                    if (P.n_active < P.C) em = min(em, P.n_active);  // the slots past the scanned ones are empty
+                    const uint64_t kn =
+                        (static_cast<uint64_t>(__float_as_uint(M.xanew[b])) << 32) | static_cast<uint32_t>(P.p);
+                    pd = pool_decide(P.recent_full != 0, P.hh_threshold, k, sl, k2, sl2, em, kn);
+                    if (pd.dest == INT_MAX) {  // no room where the rule needs an empty slot
+                        if (rank == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                        pd.dest = -1;
+                        pd.promote = -1;
+                    }
+                    win_key = pd.evicted;
+                    dest = pd.dest;
+                } else if (em != INT_MAX) {  // an empty slot: no eviction
                     win_key = kEmptyKey;
                     dest = em;
                 } else {
@@ -1076,8 +1197,9 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     dest = sl;
                     if (sl < 0 && rank == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
                 }
-                writer = dest >= W.s_lo && dest < W.s_hi;  // the CTA that attended the victim
-                if (writer && has_score) anew = M.xanew[b];
+                // the CTA that attended the victim; a slot past the scanned ones: rank 0
+                writer = (dest >= W.s_lo && dest < W.s_hi) || (dest >= P.n_active && rank == 0);
+                if (has_score) anew = M.xanew[b];
             } else {
                 dest = dest_mine;
                 writer = rank == 0;
@@ -1090,6 +1212,16 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         if (!evict && (dest < 0 || dest >= P.C)) {
             if (writer && tid == 0) atomicOr(P.err, KVEVICT_DEV_BAD_SLOT);
             dest = -1;
+        }
+        // two-pool: the promotion record of the trace (-2: the new token itself)
+        const int prec = pd.promote >= 0 ? pd.promote : (pd.new_pool ? -2 : -1);
+        if (pools && tid == 0) {
+            const bool mine = S == 1 || (pd.promote >= W.s_lo && pd.promote < W.s_hi);
+            if (pd.promote >= 0 && mine) P.pool[unit * P.pstride + pd.promote] = 1;
+            if (dest < 0 && rank == 0 && P.trace != nullptr)  // the new token itself left
+                reinterpret_cast<int4 *>(P.trace)[unit] = make_int4(
+                    -1, static_cast<int32_t>(static_cast<uint32_t>(win_key)),
+                    static_cast<int32_t>(static_cast<uint32_t>(win_key >> 32)), prec);
         }
         if (writer && dest >= 0) {
             if (tid < D / 2) {
@@ -1107,9 +1239,10 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 }
                 P.pos[unit * CS + dest] = P.p;
                 if (has_score) score_store(P, unit * CS + dest, anew);
+                if (pools) P.pool[unit * P.pstride + dest] = static_cast<uint8_t>(pd.new_pool);
                 if (P.trace != nullptr)
                     reinterpret_cast<int4 *>(P.trace)[unit] =
-                        make_int4(dest, old_pos, __float_as_int(old_score), __float_as_int(anew));
+                        make_int4(dest, old_pos, __float_as_int(old_score), pools ? prec : __float_as_int(anew));
             }
         }
     }

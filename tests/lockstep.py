@@ -10,7 +10,10 @@ what it evicted. The oracle makes its own choice; StreamingLLM and Random
 must agree bit-exactly. For H2O a different victim is accepted only as a
 near-tie (the two candidates' oracle scores within 1e-5 relative), counted,
 and the oracle then adopts the GPU's choice so both continue from the same
-retained set.
+retained set. For two-pool H2O the trace also records the promotion; a
+different decision is accepted only when one of the comparisons that made
+the oracle's (the two lowest of a pool, a score against the threshold) was
+within the same relative tolerance, and is then adopted whole.
 """
 from __future__ import annotations
 
@@ -24,7 +27,7 @@ import torch
 import oracle
 from kv_cache_eviction_decode_gb300 import KVEvictCache
 from workloads import synth
-from workloads.configs import DTYPE_BF16, POLICY_H2O, POLICY_H2O_BLOCK, POLICY_RANDOM, Workload
+from workloads.configs import DTYPE_BF16, POLICY_H2O, POLICY_H2O_BLOCK, POLICY_H2O_POOLS, POLICY_RANDOM, Workload
 
 NEAR_TIE_REL = 1e-5
 BF16_REL_TOL = 2e-2
@@ -33,7 +36,7 @@ F32_ABS_TOL = 1e-4
 
 def scored(w: Workload) -> bool:
     """Policies whose retained set depends on cumulative attention scores."""
-    return w.policy in (POLICY_H2O, POLICY_H2O_BLOCK)
+    return w.policy in (POLICY_H2O, POLICY_H2O_BLOCK, POLICY_H2O_POOLS)
 
 
 def torch_dtype(w: Workload):
@@ -46,6 +49,7 @@ class GpuRun:
     out: dict = field(default_factory=dict)         # layer -> {seq: float32 [T, Hq, D]}
     pos_snap: dict = field(default_factory=dict)    # layer -> {t: int32 [B, Hkv, C]}; t = -1 after prefill
     score_snap: dict = field(default_factory=dict)  # layer -> {t: float32 [B, Hkv, C]}
+    pool_snap: dict = field(default_factory=dict)   # layer -> {t: uint8 [B, Hkv, C]} (two-pool H2O)
     err: int = 0
     split: int = 0
     tensor_cores: int = 0
@@ -101,8 +105,11 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
         cache.set_trace(layer, trace)
         run.pos_snap[layer] = {-1: cache.slot_positions(layer).cpu()}
         run.score_snap[layer] = {}
+        run.pool_snap[layer] = {}
         if scored(w):
             run.score_snap[layer][-1] = cache.scores(layer).cpu()
+        if w.policy == POLICY_H2O_POOLS:
+            run.pool_snap[layer][-1] = cache.pools(layer).cpu()
         seqs = out_seqs if out_seqs is not None else sorted({u[0] for u in mine})
         bufs[layer] = (q, k, v, out, trace, seqs)
 
@@ -113,6 +120,8 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
             run.pos_snap[layer][t] = cache.slot_positions(layer).cpu()
             if scored(w):
                 run.score_snap[layer][t] = cache.scores(layer).cpu()
+            if w.policy == POLICY_H2O_POOLS:
+                run.pool_snap[layer][t] = cache.pools(layer).cpu()
 
     if interleave:
         for t in range(n_steps):
@@ -177,7 +186,18 @@ def replay_unit(w: Workload, unit, x, run: GpuRun, n_steps: int, out_steps=None,
         u.prefill(z, z)
     snaps = run.pos_snap[layer]
     ssnaps = run.score_snap.get(layer, {})
+    psnaps = run.pool_snap.get(layer, {})
     np.testing.assert_array_equal(u.positions(), snaps[-1][seq, h].numpy(), err_msg=f"{unit} table after prefill")
+    pools_policy = w.policy == POLICY_H2O_POOLS
+    tie_rel = 2.0**-10 if getattr(w, "score_half", False) else NEAR_TIE_REL  # one binary16 step
+
+    def check_pools(t):
+        if t in psnaps:
+            occ = u.positions() >= 0
+            np.testing.assert_array_equal(u.pools()[occ], psnaps[t][seq, h].numpy()[occ].astype(np.int8),
+                                          err_msg=f"{unit} pools, step {t}")
+
+    check_pools(-1)
     tr = run.trace[layer][:, seq, h]
     zero = np.zeros(w.head_dim, np.float32)
     for t in range(n_steps):
@@ -194,7 +214,18 @@ def replay_unit(w: Workload, unit, x, run: GpuRun, n_steps: int, out_steps=None,
             u.stage(x.k_new[t] if x is not None else zero, x.v_new[t] if x is not None else zero)
         slot = u.choose()
         gslot, gold = int(tr[t, 0]), int(tr[t, 1])
-        if gslot != slot:
+        if pools_policy:
+            mine = u.decision()
+            grec = int(tr[t, 3])
+            gdec = (u.cap if gslot < 0 else gslot, 1 if grec == -2 else 0, grec if grec >= 0 else -1)
+            if gdec != mine:
+                assert u.decision_margin < tie_rel, \
+                    f"{unit} step {t}: GPU decision {gdec}, oracle {mine} (margin {u.decision_margin:.3e})"
+                rep.near_ties += 1
+            want_old = u.prompt_len + u.steps if gdec[0] == u.cap else u.pos_at(gdec[0])
+            assert gold == want_old, f"{unit} step {t}: GPU evicted position {gold}, oracle {want_old}"
+            u.commit_pools(*gdec)
+        elif gslot != slot:
             assert w.policy == POLICY_H2O, f"{unit} step {t}: GPU slot {gslot}, oracle slot {slot}"
             sc = u.scores()
             a, b = sc[slot], sc[gslot]
@@ -205,10 +236,12 @@ def replay_unit(w: Workload, unit, x, run: GpuRun, n_steps: int, out_steps=None,
                 f"oracle slot {slot} (pos {u.pos_at(slot)}, score {a:.9g}), rel {rel:.3e}"
             rep.near_ties += 1
             slot = gslot
-        assert gold == u.pos_at(slot), f"{unit} step {t}: GPU evicted position {gold}, oracle {u.pos_at(slot)}"
-        u.commit(slot)
+        if not pools_policy:
+            assert gold == u.pos_at(slot), f"{unit} step {t}: GPU evicted position {gold}, oracle {u.pos_at(slot)}"
+            u.commit(slot)
         if t in snaps:
             np.testing.assert_array_equal(u.positions(), snaps[t][seq, h].numpy(), err_msg=f"{unit} table, step {t}")
+        check_pools(t)
         if t in ssnaps:
             pos = u.positions()
             occ = pos >= 0

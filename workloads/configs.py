@@ -129,8 +129,14 @@ H2O_BLOCK256 = H2O_MHA.with_(name="h2o_block256_bf16_b16_l32_h32_d128_k1024", po
 H2O_MHA_FP16 = H2O_MHA.with_(name="h2o_fp16scores_bf16_b16_l32_h32_d128_k1024", score_half=True)
 H2O_MHA_EMA = H2O_MHA.with_(name="h2o_ema0.01_bf16_b16_l32_h32_d128_k1024", score_forget=0.01)
 
+# Two-pool H2O on the MHA shape: a recent pool of 512 and a heavy-hitter pool of
+# 512 (no sinks); a token leaving the recent pool is promoted if its score is
+# above 2^-10, the share of one step's attention spread evenly over 1024 tokens.
+H2O_POOLS_MHA = H2O_MHA.with_(name="h2o_pools_bf16_b16_l32_h32_d128_r512_hh512", policy=POLICY_H2O_POOLS, n_sink=0,
+                              n_heavy=512, n_recent=512, hh_threshold=2.0**-10)
+
 ALL = {w.name: w for w in (H2O_TINY, SINK_WINDOW, H2O_MHA, H2O_GQA, RANDOM_REASONING, H2O_REASONING, H2O_BLOCK16,
-                           H2O_BLOCK256, H2O_MHA_FP16, H2O_MHA_EMA)}
+                           H2O_BLOCK256, H2O_MHA_FP16, H2O_MHA_EMA, H2O_POOLS_MHA)}
 
 # Short names used on command lines.
 ALIASES = {
@@ -144,6 +150,7 @@ ALIASES = {
     "h2o_block256": H2O_BLOCK256.name,
     "h2o_fp16scores": H2O_MHA_FP16.name,
     "h2o_ema": H2O_MHA_EMA.name,
+    "h2o_pools": H2O_POOLS_MHA.name,
 }
 
 

@@ -8,6 +8,8 @@ These count what the method itself has to move through HBM per unit (one
   * the G queries read and the G outputs written:          2 * G * d * e
   * H2O: the cumulative scores read and written (fp32), the new token's
     score and position written:                            8 * n_ret + 8
+  * two-pool H2O: as H2O, plus the pool flags read and the
+    new token's and a promoted token's flags written:      n_ret + 2
   * Random: the slot-position table read to skip holes:   4 * n_slots
     and, on a cut step, the generated tokens' positions read and the freed
     slots written:                                         4 * (K + r) + 4 * r
@@ -17,7 +19,7 @@ head_dim * bytes per element * tokens.
 """
 from __future__ import annotations
 
-from .configs import POLICY_H2O, POLICY_H2O_BLOCK, POLICY_RANDOM, Workload
+from .configs import POLICY_H2O, POLICY_H2O_BLOCK, POLICY_H2O_POOLS, POLICY_RANDOM, Workload
 
 
 def kv_cache_bytes(n_layers: int, n_kv_heads: int, head_dim: int, elem_bytes: int, tokens: int) -> int:
@@ -31,8 +33,10 @@ def score_bytes(tokens: int, score_elem_bytes: int = 4) -> int:
 def unit_step_bytes(w: Workload, n_retained: int, n_slots: int | None = None, cut: bool = False) -> int:
     d, e, G = w.head_dim, w.elem_bytes, w.group
     b = (n_retained + 1) * 2 * d * e + 2 * d * e + 2 * G * d * e
-    if w.policy in (POLICY_H2O, POLICY_H2O_BLOCK):
+    if w.policy in (POLICY_H2O, POLICY_H2O_BLOCK, POLICY_H2O_POOLS):
         b += (4 if w.score_half else 8) * n_retained + (6 if w.score_half else 8)
+    if w.policy == POLICY_H2O_POOLS:
+        b += n_retained + 2
     if w.policy == POLICY_RANDOM:
         b += 4 * (n_slots if n_slots is not None else w.capacity)
         if cut:
