@@ -928,7 +928,31 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
     std::memcpy(&ap.tma, &tq, sizeof tq);
     std::memcpy(&ap.tmb, &tk, sizeof tk);
     cudaError_t e = launch_prompt_rowstats(ap, c.head_dim, c.batch, h->stream);
-    if (e == cudaSuccess) {
+    const int Lq = L.G * window;
+    if (e == cudaSuccess && ap.stacked && Lq <= kSnapVotesMaxRows) {
+        // the votes streamed: the unit's stacked window rows stay resident, key tiles stream
+        CUtensorMap tqn;
+        rc = make_tensor_map(&tqn, Q_obs, static_cast<uint64_t>(c.batch) * c.n_q_heads * window, c.head_dim, Lq);
+        if (rc) return rc;
+        SnapVotesParams vp{};
+        std::memcpy(&vp.tmk, &tk, sizeof tk);
+        std::memcpy(&vp.tmq, &tqn, sizeof tqn);
+        vp.stats = ap.stats;
+        vp.votes = ap.score;
+        vp.P = P;
+        vp.Ps = ap.Ps;
+        vp.w = window;
+        vp.G = L.G;
+        vp.Hq = c.n_q_heads;
+        vp.Hkv = c.n_kv_heads;
+        vp.Lq = Lq;
+        vp.units = static_cast<int>(L.units);
+        vp.scale_log2 = ap.scale_log2;
+        vp.err = ap.err;
+        int dev = 0, sms = kSMs;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        e = launch_snapkv_votes(vp, c.head_dim, sms, h->stream);
+    } else if (e == cudaSuccess) {
         std::memcpy(&ap.tma, &tk, sizeof tk);
         std::memcpy(&ap.tmb, &tq, sizeof tq);
         e = launch_prompt_colsum(ap, c.head_dim, c.batch, h->stream);

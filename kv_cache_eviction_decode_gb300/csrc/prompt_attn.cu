@@ -21,6 +21,7 @@
 //
 // Warps: 0-15 epilogue (four per TMEM lane quadrant, each taking 32 of the
 // 128 columns), 16 TMA producer (and TMEM allocation), 17 MMA issuer.
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 
@@ -83,6 +84,25 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b)
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
+}
+
+// sum over e < 32 of 2^(r_e * c + a_e) (r the raw fp32 bits of 32 TMEM
+// columns, a[e] from `add`), in four independent packed chains.
+__device__ __forceinline__ float exp2_sum32(const uint32_t (&r)[32], float c, const float4 *add)
+{
+    const float2 c2 = make_float2(c, c);
+    float2 s[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 nms = __ldg(add + e4);
+        const int e = e4 * 4;
+        const float2 za = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, make_float2(nms.x, nms.y));
+        const float2 zb = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), c2, make_float2(nms.z, nms.w));
+        s[(e4 & 1) * 2] = fadd2(s[(e4 & 1) * 2], make_float2(ex2(za.x), ex2(za.y)));
+        s[(e4 & 1) * 2 + 1] = fadd2(s[(e4 & 1) * 2 + 1], make_float2(ex2(zb.x), ex2(zb.y)));
+    }
+    const float2 t = fadd2(fadd2(s[0], s[1]), fadd2(s[2], s[3]));
+    return t.x + t.y;
 }
 
 // STACK (SnapKV, window a multiple of 32): the G query heads' window rows,
@@ -216,6 +236,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
         int cur_g = 0;                         // STACK pass 2: query head of the running sum
         if (MODE == kColSum && STACK)
             for (int g = 0; g < p.G; ++g) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
+        // STACK pass 1: a warp whose 32 rows all lie past the stacked rows has nothing to do
+        const bool idle = MODE == kRowStats && STACK && tile * kPT + quad * 32 >= Lq;
         for (int n = 0; n < n_b; ++n) {
             const int sb = n & 1;
             // the TMEM load below is warp-collective: the whole warp agrees on `ok`
@@ -224,7 +246,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                 if (lane == 0) flag_timeout(p.err);
             }
             tc_fence_after();
-            if (ok) {
+            if (ok && !idle) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_field + static_cast<uint32_t>(sb * kPT + col0), r);
                 tc_wait_ld();
@@ -406,6 +428,217 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
     }
 }
 
+// ------------------------------------------------------- SnapKV votes, streamed
+// votes_gj = sum over the window's queries t of head g of 2^(z_gtj * c - ms_gt),
+// z = q . k (bf16 in, fp32 accumulate), ms_gt the row's log2 normaliser from
+// the row-statistics pass, for every prompt key j (masked causally inside the
+// window). One persistent CTA per SM takes a contiguous range of items (unit,
+// key tile of 128). The unit's Lq = G * w stacked window rows stay in shared
+// memory as the B operand (reloaded when the range crosses into the next
+// unit); the key tiles stream through a TMA ring as A. One tcgen05.mma of
+// M = 128 keys, N = Lq rows per K step fills one of two TMEM accumulators
+// while the epilogue reads the other: thread (quad, slice) owns key row
+// quad * 32 + lane and the query heads slice, slice + 4, ... (every 32-row
+// chunk of each), so it writes those heads' votes of its key itself.
+constexpr int kVStages = 4;
+
+template <int D> struct VotesLayout {
+    static constexpr int kATile = kPT * D * 2;           // one key tile
+    static constexpr int kBBytes = kSnapVotesMaxRows * D * 2;
+    static constexpr int kOffB = 0;
+    static constexpr int kOffA = kBBytes;
+    static constexpr int kOffBar = kOffA + kVStages * kATile;
+    static constexpr int kBytes = kOffBar + 256 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPThreads, 1) snap_votes_kernel(const __grid_constant__ SnapVotesParams p)
+{
+    using L = VotesLayout<D>;
+    extern __shared__ uint8_t vraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(vraw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
+    uint64_t *a_full = bars;                   // [kVStages]
+    uint64_t *a_empty = a_full + kVStages;     // [kVStages]
+    uint64_t *s_full = a_empty + kVStages;     // [2]
+    uint64_t *s_empty = s_full + 2;            // [2]
+    uint64_t *b_full = s_empty + 2;            // the unit's window rows landed
+    uint64_t *b_free = b_full + 1;             // every MMA on the previous unit's rows completed
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(b_free + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int N = p.Lq;                        // MMA N: stacked window rows (multiple of 32, <= 256)
+    const uint32_t tcols = N <= 16 ? 32u : (N <= 32 ? 64u : (N <= 64 ? 128u : (N <= 128 ? 256u : 512u)));
+    const int nT = (p.P + kPT - 1) / kPT;
+    const long long n_items = static_cast<long long>(p.units) * nT;
+    const int it0 = static_cast<int>(n_items * blockIdx.x / gridDim.x);
+    const int it1 = static_cast<int>(n_items * (blockIdx.x + 1) / gridDim.x);
+
+    if (tid == 0) {
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_empty[s], kEpiWarps);
+        }
+        mbar_init(b_full, 1);
+        mbar_init(b_free, 1);
+        mbar_fence_init();
+    }
+    if (warp == kProdWarp) tmem_alloc(tslot, tcols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tslot);
+
+    int issued_a = 0, issued_mma = 0, loads_b = 0;
+
+    if (warp == kProdWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int cur = -1;
+            for (int it = it0; it < it1; ++it) {
+                const int u = it / nT, kt = it - u * nT, n = it - it0;
+                if (u != cur) {
+                    // the previous unit's rows are overwritten once its MMAs are done
+                    if (loads_b > 0 && !mbar_wait(b_free, (loads_b - 1) & 1)) {
+                        flag_timeout(p.err);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(b_full, static_cast<uint32_t>(N * D * 2));
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d_plain(sm + L::kOffB + c * N * 128, &p.tmq, c * 64, u * N, b_full);
+                    ++loads_b;
+                    cur = u;
+                }
+                const int s = n % kVStages;
+                if (n >= kVStages && !mbar_wait(&a_empty[s], ((n / kVStages) - 1) & 1)) {
+                    flag_timeout(p.err);
+                    break;
+                }
+                mbar_arrive_expect_tx(&a_full[s], static_cast<uint32_t>(L::kATile));
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_2d_plain(sm + L::kOffA + s * L::kATile + c * kPT * 128, &p.tmk, c * 64,
+                                      u * p.P + kt * kPT, &a_full[s]);
+                issued_a = n + 1;
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kPT, N);
+            bool ok = true;
+            int cur = -1, nb = 0;
+            for (int it = it0; ok && it < it1; ++it) {
+                const int u = it / nT, n = it - it0, s = n % kVStages, acc = n & 1;
+                if (u != cur) {
+                    if (nb > 0) tc_commit(b_free);  // completes once the previous unit's MMAs have
+                    if (!mbar_wait(b_full, nb & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    ++nb;
+                    cur = u;
+                }
+                if (!mbar_wait(&a_full[s], (n / kVStages) & 1)) ok = false;
+                else if (n >= 2 && !mbar_wait(&s_empty[acc], ((n >> 1) - 1) & 1)) ok = false;
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sm + L::kOffA + s * L::kATile), b0 = smem_u32(sm + L::kOffB);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ka = static_cast<uint32_t>((k >> 2) * kPT * 128 + (k & 3) * 32);
+                    const uint32_t kb = static_cast<uint32_t>((k >> 2) * N * 128 + (k & 3) * 32);
+                    tc_mma_bf16(tmem + static_cast<uint32_t>(acc * N), smem_desc_sw128(a0 + ka),
+                                smem_desc_sw128(b0 + kb), idesc, k > 0);
+                }
+                tc_commit(&a_empty[s]);
+                tc_commit(&s_full[acc]);
+                issued_mma = n + 1;
+            }
+            if (!ok) flag_timeout(p.err);
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int quad = warp & 3, slice = warp >> 2;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_field = static_cast<uint32_t>(quad * 32) << 16;
+        const int per_head = p.w / 32;  // 32-row chunks per query head
+        const float c = p.scale_log2;
+        const int pre = p.P - p.w;  // keys before the window: every window query sees them
+        bool ok = true;
+        for (int it = it0; it < it1; ++it) {
+            const int u = it / nT, kt = it - u * nT, n = it - it0, sb = n & 1;
+            const int j = kt * kPT + row;  // this thread's key
+            // the TMEM loads below are warp-collective: the whole warp agrees on `ok`
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (n >> 1) & 1))) {
+                ok = false;
+                if (lane == 0) flag_timeout(p.err);
+            }
+            tc_fence_after();
+            const int b = u / p.Hkv, kvh = u - b * p.Hkv;
+            float *vout = p.votes + static_cast<size_t>(b * p.Hq + kvh * p.G) * p.P + j;
+            // this slice's query heads: g = slice, slice + 4, ... (all chunks of each)
+            for (int g = slice; ok && g < p.G; g += kSlices) {
+                float tot = 0.f;
+                for (int k = 0; k < per_head; ++k) {
+                    const int ch = g * per_head + k;
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_field + static_cast<uint32_t>(sb * N + ch * 32), r);
+                    tc_wait_ld();
+                    const float4 *st = reinterpret_cast<const float4 *>(p.stats + static_cast<size_t>(u) * p.Ps + ch * 32);
+                    if (kt * kPT + kPT <= pre) {  // a tile wholly before the window: no mask
+                        tot += exp2_sum32(r, c, st);
+                    } else {
+                        // query position of stacked row ch * 32 + e: P - w + (row mod w)
+                        const int i0 = pre + (ch * 32) % p.w;
+                        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 nms = __ldg(st + e4);
+                            const float mv[4] = {nms.x, nms.y, nms.z, nms.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int e = e4 * 4 + t;
+                                const float pr = ex2(fmaf(__uint_as_float(r[e]), c, mv[t]));
+                                const float add = (j <= i0 + e) ? pr : 0.f;
+                                if (t & 1) s1 += add;
+                                else s0 += add;
+                            }
+                        }
+                        tot += s0 + s1;
+                    }
+                }
+                if (j < p.P) vout[static_cast<size_t>(g) * p.P] = tot;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[sb]);
+        }
+    }
+
+    // Teardown: let the copies and MMAs already issued finish (bounded) before
+    // the TMEM and the shared memory go away.
+    if (warp == kProdWarp && lane == 0) {
+        for (int n = max(0, issued_a - kVStages); n < issued_a; ++n)
+            mbar_wait(&a_full[n % kVStages], (n / kVStages) & 1);
+        if (loads_b > 0) mbar_wait(b_full, (loads_b - 1) & 1);
+    }
+    if (warp == kMmaWarp && lane == 0) {
+        for (int n = max(0, issued_mma - 2); n < issued_mma; ++n) mbar_wait(&s_full[n & 1], (n >> 1) & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProdWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tcols);
+    }
+}
+
 // ------------------------------------------------------------------ cut
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
@@ -425,24 +658,6 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane)
 struct BlockOps {
     int *red, *total;
     int lane, warp;
-    // the sum of v over the block, in every thread
-    __device__ int sum(int v) const
-    {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) red[warp] = v;
-        __syncthreads();
-        if (warp == 0) {
-            int w = lane < kSelWarps ? red[lane] : 0;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
-            if (lane == 0) *total = w;
-        }
-        __syncthreads();
-        const int t = *total;
-        __syncthreads();
-        return t;
-    }
     // exclusive prefix of v over the threads in order (x) and the total (y)
     __device__ int2 scan(int v) const
     {
@@ -462,40 +677,108 @@ struct BlockOps {
     }
 };
 
-// The E smallest (bit pattern, position) keys among bits[lo, hi), E >= 1:
-// the smallest T with #{bits <= T} >= E, and how many of the keys equal to T
-// are among them (`need`, the oldest positions first).
-__device__ void cut_threshold(const uint32_t *bits, int lo, int hi, int E, const BlockOps &ops, uint32_t &T,
-                              int &need)
-{
-    uint32_t a = 0, b = 0xFFFFFFFFu;
-    while (a < b) {
-        const uint32_t mid = a + (b - a) / 2;
-        int c = 0;
-        for (int j = lo + static_cast<int>(threadIdx.x); j < hi; j += kSelThreads) c += bits[j] <= mid;
-        if (ops.sum(c) >= E) b = mid;
-        else a = mid + 1;
+// Warp w owns the positions [base, end) of [lo, hi): consecutive spans of a
+// multiple of 32 positions, in warp order. Its walk visits 32 consecutive
+// positions per step (lane l: base + 32 i + l): conflict-free in shared
+// memory, and in position order across steps, lanes and warps.
+struct WarpRange {
+    int base, end;
+    __device__ WarpRange(int lo, int hi, int warp)
+    {
+        const int span = 32 * ((hi - lo + 32 * kSelWarps - 1) / (32 * kSelWarps));
+        base = min(hi, lo + warp * span);
+        end = min(hi, base + span);
     }
-    T = a;
-    int c = 0;
-    for (int j = lo + static_cast<int>(threadIdx.x); j < hi; j += kSelThreads) c += bits[j] < T;
-    need = E - ops.sum(c);
+};
+
+__device__ __forceinline__ unsigned lanes_below(int lane) { return (1u << lane) - 1u; }
+
+// The E-th smallest bit pattern T among bits[lo, hi) (1 <= E <= hi - lo) and
+// how many of the E smallest equal T (`need`), by radix selection: four
+// passes over 8-bit digits, most significant first, each a histogram of the
+// digit among the patterns that share the digits found so far (increments
+// aggregated over the lanes holding the same digit).
+__device__ void radix_threshold(const uint32_t *bits, int lo, int hi, int E, int *hist, int *bc, uint32_t &T,
+                                int &need)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const WarpRange R(lo, hi, warp);
+    uint32_t prefix = 0, mask = 0;
+    int rank = E;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+        __syncthreads();
+        for (int j0 = R.base; j0 < R.end; j0 += 32) {
+            const int j = j0 + lane;
+            const uint32_t bt = j < R.end ? bits[j] : 0u;
+            const bool m = j < R.end && (bt & mask) == prefix;
+            const unsigned act = __ballot_sync(0xffffffffu, m);
+            if (m) {
+                const uint32_t d = (bt >> shift) & 255u;
+                const unsigned peers = __match_any_sync(act, d);
+                if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {  // lane l holds bins 8 l .. 8 l + 7; the one holding the rank-th picks the digit
+            int c[8], sum = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                c[k] = hist[lane * 8 + k];
+                sum += c[k];
+            }
+            const int incl = warp_incl_scan(sum, lane), excl = incl - sum;
+            if (excl < rank && rank <= incl) {
+                int acc = excl, d = 7;
+                for (int k = 0; k < 8; ++k) {
+                    if (acc + c[k] >= rank) {
+                        d = k;
+                        break;
+                    }
+                    acc += c[k];
+                }
+                bc[0] = lane * 8 + d;
+                bc[1] = rank - acc;
+            }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(bc[0]) << shift;
+        mask |= 255u << shift;
+        rank = bc[1];
+    }
+    T = prefix;
+    need = rank;
 }
 
-// Copies K and V rows of the slots [0, kept) from the prompt rows named by pos.
+// Exclusive prefix over the warps (in order) of one value per warp, and the
+// total; every lane of a warp gets its warp's prefix.
+__device__ __forceinline__ int2 warp_prefix(const BlockOps &ops, int v, int lane)
+{
+    const int2 r = ops.scan(lane == 0 ? v : 0);
+    return make_int2(__shfl_sync(0xffffffffu, r.x, 0), r.y);
+}
+
+// Copies K and V rows of the slots [0, kept) from the prompt rows named by
+// pos; each warp moves four rows per step (all loads, then all stores).
 __device__ void copy_kept_rows(const void *K, const void *V, void *kc, void *vc, const int32_t *pos, size_t unit,
                                int P, int C, int row_bytes, int kept, int warp, int lane)
 {
+    constexpr int kRows = 4;
     const int vecs = row_bytes / 16;
-    for (int s = warp; s < kept; s += kSelWarps) {
-        const int j = pos[s];
+    for (int s0 = warp * kRows; s0 < kept; s0 += kSelWarps * kRows) {
         for (int vi = lane; vi < 2 * vecs; vi += 32) {
             const int which = vi / vecs, off = vi - which * vecs;
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(which ? V : K) +
-                                                               (unit * P + j) * static_cast<size_t>(row_bytes));
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(which ? vc : kc) +
-                                                   (unit * C + s) * static_cast<size_t>(row_bytes));
-            dst[off] = src[off];
+            const uint8_t *src = static_cast<const uint8_t *>(which ? V : K);
+            uint8_t *dst = static_cast<uint8_t *>(which ? vc : kc);
+            uint4 v[kRows];
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+                if (s0 + r < kept)
+                    v[r] = reinterpret_cast<const uint4 *>(src + (unit * P + pos[s0 + r]) * static_cast<size_t>(row_bytes))[off];
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+                if (s0 + r < kept)
+                    reinterpret_cast<uint4 *>(dst + (unit * C + s0 + r) * static_cast<size_t>(row_bytes))[off] = v[r];
         }
     }
 }
@@ -504,51 +787,68 @@ __device__ void copy_kept_rows(const void *K, const void *V, void *kc, void *vc,
 // but the P - K smallest (score, position) keys; the kept tokens fill slots
 // 0, 1, ... in ascending position order. One CTA per unit: the unit's score
 // bits (non-negative floats, so their bit patterns order like the values) in
-// shared memory; the cut threshold by binary search on the bit pattern; ties
-// at the threshold go in position order, oldest first.
+// shared memory; the cut threshold by radix selection on the bit pattern;
+// ties at the threshold go in position order, oldest first.
 __global__ void __launch_bounds__(kSelThreads) prompt_select_kernel(const PromptSelectParams p)
 {
     extern __shared__ uint32_t sbits[];
     __shared__ int red[kSelWarps];
     __shared__ int total;
+    __shared__ int hist[256];
+    __shared__ int bc[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const BlockOps ops{red, &total, lane, warp};
     const size_t unit = blockIdx.x;
     const int P = p.P;
     const int e_lo = p.n_sink, e_hi = P - p.n_recent;  // eligible positions [e_lo, e_hi)
     for (int j = tid; j < P; j += kSelThreads) {
-        const float s = p.score[unit * P + j];
-        if (!(s >= 0.f && s <= FLT_MAX)) atomicOr(p.err, KVEVICT_DEV_NONFINITE);
-        sbits[j] = __float_as_uint(s);
+        const float sv = p.score[unit * P + j];
+        if (!(sv >= 0.f && sv <= FLT_MAX)) atomicOr(p.err, KVEVICT_DEV_NONFINITE);
+        sbits[j] = __float_as_uint(sv);
     }
     __syncthreads();
 
     const int E = P > p.budget ? P - p.budget : 0;  // tokens to remove
     uint32_t T = 0;
     int need = 0;
-    if (E > 0) cut_threshold(sbits, e_lo, e_hi, E, ops, T, need);
+    if (E > 0) radix_threshold(sbits, e_lo, e_hi, E, hist, bc, T, need);
 
-    int tie_base = 0, slot_base = 0;
-    for (int j0 = 0; j0 < P; j0 += kSelThreads) {
-        const int j = j0 + tid;
-        const bool in = j < P;
-        const bool elig = in && j >= e_lo && j < e_hi;
-        const uint32_t b = in ? sbits[j] : 0u;
-        const bool tie = E > 0 && elig && b == T;
-        const int2 ts = ops.scan(tie ? 1 : 0);
-        const bool evict = E > 0 && elig && (b < T || (tie && tie_base + ts.x < need));
-        const bool keep = in && !evict;
-        const int2 ks = ops.scan(keep ? 1 : 0);
-        const int slot = slot_base + ks.x;
-        if (keep && slot < p.C) {
-            p.pos[unit * p.cstride + slot] = j;
-            p.cscore[unit * p.cstride + slot] = __uint_as_float(b);
+    // leaves: eligible and (below T, or among the first `need` ties in position order)
+    const WarpRange R(0, P, warp);
+    auto walk = [&](int tie_base, int slot_base, bool write) {  // returns (ties, kept) of this warp
+        int ties = 0, kept = 0;
+        for (int j0 = R.base; j0 < R.end; j0 += 32) {
+            const int j = j0 + lane;
+            const bool in = j < R.end;
+            const bool elig = in && j >= e_lo && j < e_hi;
+            const uint32_t bt = in ? sbits[j] : 0u;
+            const bool tie = E > 0 && elig && bt == T;
+            const unsigned tm = __ballot_sync(0xffffffffu, tie);
+            const bool leave = E > 0 && elig && (bt < T || (tie && tie_base + ties + __popc(tm & lanes_below(lane)) < need));
+            const bool keep = in && !leave;
+            const unsigned km = __ballot_sync(0xffffffffu, keep);
+            if (write && keep) {
+                const int slot = slot_base + kept + __popc(km & lanes_below(lane));
+                if (slot < p.C) {
+                    p.pos[unit * p.cstride + slot] = j;
+                    p.cscore[unit * p.cstride + slot] = __uint_as_float(bt);
+                }
+            }
+            ties += __popc(tm);
+            kept += __popc(km);
         }
-        tie_base += ts.y;
-        slot_base += ks.y;
+        return make_int2(ties, kept);
+    };
+    int ties = 0;
+    for (int j0 = R.base; j0 < R.end; j0 += 32) {
+        const int j = j0 + lane;
+        ties += __popc(__ballot_sync(0xffffffffu, E > 0 && j < R.end && j >= e_lo && j < e_hi && sbits[j] == T));
     }
+    const int tie_base = warp_prefix(ops, ties, lane).x;
+    const int2 kb = warp_prefix(ops, walk(tie_base, 0, false).y, lane);
+    walk(tie_base, kb.x, true);
     __syncthreads();  // the positions written above are visible to the whole CTA
-    copy_kept_rows(p.K, p.V, p.kc, p.vc, p.pos + unit * p.cstride, unit, P, p.C, p.row_bytes, min(slot_base, p.C),
+    copy_kept_rows(p.K, p.V, p.kc, p.vc, p.pos + unit * p.cstride, unit, P, p.C, p.row_bytes, min(kb.y, p.C),
                    warp, lane);
 }
 
@@ -558,7 +858,12 @@ __global__ void __launch_bounds__(kSelThreads) prompt_select_kernel(const Prompt
 // largest pooled votes (ties: the newer position); the unit keeps the union
 // over its G query heads plus the window, in slots 0, 1, ... in ascending
 // position order, each token with the mean over g of its votes. One CTA per
-// unit: a head's pooled bits and the kept bitmap in shared memory.
+// unit: a head's pooled bits and the kept bitmap in shared memory; each head's
+// cut by radix selection, its ties in position order through one scan over
+// the warps' spans.
+__device__ void snap_union_tail(const SnapSelectParams &p, const uint32_t *keep, const BlockOps &ops, size_t unit,
+                                int b, int kvh);
+
 __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(const SnapSelectParams p)
 {
     extern __shared__ uint32_t ssm[];
@@ -567,6 +872,8 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(const SnapSe
     uint32_t *keep = ssm + n_pre;        // [ceil(P / 32)] bitmap
     __shared__ int red[kSelWarps];
     __shared__ int total;
+    __shared__ int hist[256];
+    __shared__ int bc[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const BlockOps ops{red, &total, lane, warp};
     const size_t unit = blockIdx.x;
@@ -578,6 +885,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(const SnapSe
 
     const int take = min(p.topk, n_pre);
     const int E = n_pre - take;  // prefix positions a head does not take
+    const WarpRange R(0, n_pre, warp);
     for (int g = 0; g < p.G; ++g) {
         const float *vg = p.votes + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * P;
         __syncthreads();  // the previous head is done with pbits
@@ -591,40 +899,209 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(const SnapSe
         if (take == 0) continue;
         uint32_t T = 0;
         int need = 0;
-        if (E > 0) cut_threshold(pbits, 0, n_pre, E, ops, T, need);
-        // taken: not among the E smallest (bits, position)
-        int tie_base = 0;
-        for (int j0 = 0; j0 < n_pre; j0 += kSelThreads) {
-            const int j = j0 + tid;
-            const bool in = j < n_pre;
+        if (E > 0) radix_threshold(pbits, 0, n_pre, E, hist, bc, T, need);
+        // taken: not among the E smallest (bits, position); a warp's span starts on a
+        // multiple of 32, so each step of its walk fills one bitmap word
+        int ties = 0;
+        for (int j0 = R.base; j0 < R.end; j0 += 32) {
+            const int j = j0 + lane;
+            ties += __popc(__ballot_sync(0xffffffffu, E > 0 && j < R.end && pbits[j] == T));
+        }
+        int tb = warp_prefix(ops, ties, lane).x;
+        for (int j0 = R.base; j0 < R.end; j0 += 32) {
+            const int j = j0 + lane;
+            const bool in = j < R.end;
             const uint32_t bt = in ? pbits[j] : 0u;
             const bool tie = E > 0 && in && bt == T;
-            const int2 ts = ops.scan(tie ? 1 : 0);
-            const bool left = E > 0 && in && (bt < T || (tie && tie_base + ts.x < need));
-            if (in && !left) atomicOr(&keep[j >> 5], 1u << (j & 31));
-            tie_base += ts.y;
+            const unsigned tm = __ballot_sync(0xffffffffu, tie);
+            const bool left = E > 0 && in && (bt < T || (tie && tb + __popc(tm & lanes_below(lane)) < need));
+            const unsigned km = __ballot_sync(0xffffffffu, in && !left);
+            if (lane == 0 && km) keep[j0 >> 5] |= km;
+            tb += __popc(tm);
         }
     }
     __syncthreads();
+    snap_union_tail(p, keep, ops, unit, b, kvh);
+}
 
-    int slot_base = 0;
-    for (int j0 = 0; j0 < P; j0 += kSelThreads) {
-        const int j = j0 + tid;
-        const bool k = j < P && ((keep[j >> 5] >> (j & 31)) & 1u);
-        const int2 ks = ops.scan(k ? 1 : 0);
-        const int slot = slot_base + ks.x;
-        if (k && slot < p.C) {
-            float sc = 0.f;
-            for (int g = 0; g < p.G; ++g) sc += p.votes[static_cast<size_t>(b * p.Hq + kvh * p.G + g) * P + j];
-            p.pos[unit * p.cstride + slot] = j;
-            p.cscore[unit * p.cstride + slot] = sc * (1.f / p.G);
-        }
-        slot_base += ks.y;
+// The union's tail, shared by both selection kernels: the kept positions (the
+// bitmap) in ascending order fill slots 0, 1, ..., each with the mean over
+// its G heads of its votes; then the K/V rows are copied.
+__device__ void snap_union_tail(const SnapSelectParams &p, const uint32_t *keep, const BlockOps &ops, size_t unit,
+                                int b, int kvh)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = p.P, nw = (P + 31) / 32;
+    // slots: the kept positions in ascending order, one bitmap word per lane and step
+    const WarpRange RW(0, nw, warp);
+    int cnt = 0;
+    for (int w0 = RW.base; w0 < RW.end; w0 += 32) {
+        const int w = w0 + lane;
+        cnt += __reduce_add_sync(0xffffffffu, w < RW.end ? __popc(keep[w]) : 0);
     }
-    if (slot_base > p.C && tid == 0) atomicOr(p.err, KVEVICT_DEV_BAD_SLOT);
+    const int2 sb = warp_prefix(ops, cnt, lane);
+    int slot_base = sb.x;
+    for (int w0 = RW.base; w0 < RW.end; w0 += 32) {
+        const int w = w0 + lane;
+        uint32_t word = w < RW.end ? keep[w] : 0u;
+        const int c = __popc(word);
+        const int incl = warp_incl_scan(c, lane);
+        int slot = slot_base + incl - c;
+        while (word) {
+            const int j = w * 32 + __ffs(word) - 1;
+            word &= word - 1u;
+            if (slot < p.C) {
+                float sc = 0.f;
+                for (int g = 0; g < p.G; ++g) sc += p.votes[static_cast<size_t>(b * p.Hq + kvh * p.G + g) * P + j];
+                p.pos[unit * p.cstride + slot] = j;
+                p.cscore[unit * p.cstride + slot] = sc * (1.f / p.G);
+            }
+            ++slot;
+        }
+        slot_base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (sb.y > p.C && tid == 0) atomicOr(p.err, KVEVICT_DEV_BAD_SLOT);
     __syncthreads();
-    copy_kept_rows(p.K, p.V, p.kc, p.vc, p.pos + unit * p.cstride, unit, P, p.C, p.row_bytes, min(slot_base, p.C),
+    copy_kept_rows(p.K, p.V, p.kc, p.vc, p.pos + unit * p.cstride, unit, P, p.C, p.row_bytes, min(sb.y, p.C),
                    warp, lane);
+}
+
+// The same selection with a head's pooled votes in registers: warp w owns the
+// prefix positions [32 R w, 32 R (w + 1)), its lane l the positions
+// 32 R w + 32 r + l (r < R). The pooling loads every vote once and takes the
+// neighbours from the lanes and registers around it (shuffles), with three
+// halo values on each side of the warp's span. The cut threshold is a binary
+// search on the bit pattern (the E-th smallest), each step counting with
+// per-thread compares, a warp reduction and one barrier (per-warp counts
+// double-buffered by step parity). For n_pre <= 512 R.
+template <int R>
+__global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const SnapSelectParams p)
+{
+    extern __shared__ uint32_t keep[];  // [ceil(P / 32)] bitmap
+    __shared__ int red[kSelWarps];
+    __shared__ int total;
+    __shared__ int wcnt[2][kSelWarps];
+    __shared__ uint32_t wlim[2][kSelWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const BlockOps ops{red, &total, lane, warp};
+    const size_t unit = blockIdx.x;
+    const int P = p.P, n_pre = P - p.window;
+    const int b = static_cast<int>(unit) / p.Hkv, kvh = static_cast<int>(unit) - b * p.Hkv;
+    const int nw = (P + 31) / 32;
+    for (int i = tid; i < nw; i += kSelThreads) keep[i] = 0u;
+    __syncthreads();
+    for (int j = n_pre + tid; j < P; j += kSelThreads) atomicOr(&keep[j >> 5], 1u << (j & 31));  // the window
+
+    const int take = min(p.topk, n_pre);
+    const int E = n_pre - take;
+    const int base = warp * 32 * R + lane;
+    constexpr uint32_t kNone = 0xFFFFFFFFu;  // past the prefix: above every finite pattern, never counted
+    for (int g = 0; g < p.G && take > 0; ++g) {
+        const float *vg = p.votes + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * P;
+        // raw votes (0 outside the prefix: neutral for the max of non-negative values)
+        float x[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int j = base + 32 * r;
+            x[r] = j < n_pre ? __ldg(vg + j) : 0.f;
+        }
+        // lanes 0-2: the three positions before the span (hl) and after it (hr)
+        const int span0 = base - lane;
+        const int jl = span0 - 3 + lane, jr = span0 + 32 * R + lane;
+        const float hl = (lane < 3 && jl >= 0 && jl < n_pre) ? __ldg(vg + jl) : 0.f;
+        const float hr = (lane < 3 && jr < n_pre) ? __ldg(vg + jr) : 0.f;
+        uint32_t v[R];
+        uint32_t lo = kNone, hi = 0;
+        bool bad = false;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float mx = x[r];
+#pragma unroll
+            for (int k = 1; k <= 3; ++k) {
+                // position + k: lane + k of this step, or lane + k - 32 of the next (or the right halo)
+                const float up_same = __shfl_sync(0xffffffffu, x[r], (lane + k) & 31);
+                const float up_next = __shfl_sync(0xffffffffu, r + 1 < R ? x[r + 1 < R ? r + 1 : r] : hr, (lane + k) & 31);
+                mx = fmaxf(mx, lane + k < 32 ? up_same : up_next);
+                // position - k: lane - k of this step, or lane - k + 32 of the previous (or the left halo)
+                const float dn_same = __shfl_sync(0xffffffffu, x[r], (lane - k) & 31);
+                const float dn_prev = r > 0 ? __shfl_sync(0xffffffffu, x[r > 0 ? r - 1 : 0], (lane - k) & 31)
+                                            : __shfl_sync(0xffffffffu, hl, lane - k + 3 >= 0 ? lane - k + 3 : 0);
+                mx = fmaxf(mx, lane - k >= 0 ? dn_same : dn_prev);
+            }
+            const int j = base + 32 * r;
+            v[r] = kNone;
+            if (j < n_pre) {
+                bad |= !(mx >= 0.f && mx <= FLT_MAX);
+                v[r] = __float_as_uint(mx);
+                lo = min(lo, v[r]);
+                hi = max(hi, v[r]);
+            }
+        }
+        if (bad) atomicOr(p.err, KVEVICT_DEV_NONFINITE);
+        if (E == 0) {  // every prefix position is taken
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const unsigned km = __ballot_sync(0xffffffffu, v[r] != kNone);
+                if (lane == 0 && km) atomicOr(&keep[(base - lane + 32 * r) >> 5], km);
+            }
+            continue;
+        }
+        // the search interval [a, bb] from the block's smallest and largest pattern
+        lo = __reduce_min_sync(0xffffffffu, lo);
+        hi = __reduce_max_sync(0xffffffffu, hi);
+        if (lane == 0) {
+            wlim[0][warp] = lo;
+            wlim[1][warp] = hi;
+        }
+        __syncthreads();
+        uint32_t a = kNone, bb = 0;
+        for (int w = 0; w < kSelWarps; ++w) {
+            a = min(a, wlim[0][w]);
+            bb = max(bb, wlim[1][w]);
+        }
+        // smallest T in [a, bb] with #{v <= T} >= E
+        for (int it = 0; a < bb; ++it) {
+            const uint32_t mid = a + (bb - a) / 2;
+            int c0 = 0, c1 = 0;
+#pragma unroll
+            for (int r = 0; r < R; r += 2) {
+                c0 += v[r] <= mid;
+                if (r + 1 < R) c1 += v[r + 1] <= mid;
+            }
+            const int c = __reduce_add_sync(0xffffffffu, c0 + c1);
+            if (lane == 0) wcnt[it & 1][warp] = c;
+            __syncthreads();
+            int tot = 0;
+#pragma unroll
+            for (int w = 0; w < kSelWarps; ++w) tot += wcnt[it & 1][w];
+            if (tot >= E) bb = mid;
+            else a = mid + 1;
+        }
+        const uint32_t T = a;
+        // ties at T: the first `need` in position order leave, the newer ones are taken
+        int below = 0, ties = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            below += v[r] < T;
+            ties += v[r] == T;
+        }
+        below = __reduce_add_sync(0xffffffffu, below);
+        ties = __reduce_add_sync(0xffffffffu, ties);
+        const int2 bs = warp_prefix(ops, below, lane);  // (synchronises: wcnt of the search is free again)
+        const int need = E - bs.y;
+        int tb = warp_prefix(ops, ties, lane).x;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool tie = v[r] == T;
+            const unsigned tm = __ballot_sync(0xffffffffu, tie);
+            const bool left = v[r] < T || (tie && tb + __popc(tm & lanes_below(lane)) < need);
+            const unsigned km = __ballot_sync(0xffffffffu, v[r] != kNone && !left);
+            if (lane == 0 && km) atomicOr(&keep[(base - lane + 32 * r) >> 5], km);
+            tb += __popc(tm);
+        }
+    }
+    __syncthreads();
+    snap_union_tail(p, keep, ops, unit, b, kvh);
 }
 
 template <int D, int MODE, bool STACK> cudaError_t launch_attn_t(const PromptAttnParams &p, int B, cudaStream_t st)
@@ -661,8 +1138,38 @@ cudaError_t launch_prompt_colsum(const PromptAttnParams &p, int head_dim, int B,
     return head_dim == 64 ? launch_attn<64, kColSum>(p, B, st) : launch_attn<128, kColSum>(p, B, st);
 }
 
+cudaError_t launch_snapkv_votes(const SnapVotesParams &p, int head_dim, int sms, cudaStream_t st)
+{
+    if (p.Lq < 32 || p.Lq > kSnapVotesMaxRows || p.Lq % 32 || p.w % 32) return cudaErrorInvalidValue;
+    const long long items = static_cast<long long>(p.units) * ((p.P + kPT - 1) / kPT);
+    const int grid = static_cast<int>(std::min<long long>(sms, items));
+    if (grid <= 0) return cudaSuccess;
+    auto go = [&](auto kern, int smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kPThreads, smem, st>>>(p);
+        return cudaGetLastError();
+    };
+    return head_dim == 64 ? go(snap_votes_kernel<64>, VotesLayout<64>::kBytes)
+                          : go(snap_votes_kernel<128>, VotesLayout<128>::kBytes);
+}
+
+template <int R> cudaError_t launch_select_reg(const SnapSelectParams &p, int units, cudaStream_t st)
+{
+    const size_t smem = static_cast<size_t>((p.P + 31) / 32) * 4;
+    cudaError_t e = cudaFuncSetAttribute(snapkv_select_reg_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    snapkv_select_reg_kernel<R><<<units, kSelThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_snapkv_select(const SnapSelectParams &p, int units, cudaStream_t st)
 {
+    const int n_pre = p.P - p.window;
+    if (n_pre <= kSelThreads * 4) return launch_select_reg<4>(p, units, st);
+    if (n_pre <= kSelThreads * 16) return launch_select_reg<16>(p, units, st);
+    if (n_pre <= kSelThreads * 64) return launch_select_reg<64>(p, units, st);
     const size_t smem = static_cast<size_t>(p.P - p.window) * 4 + static_cast<size_t>((p.P + 31) / 32) * 4;
     cudaError_t e = cudaFuncSetAttribute(snapkv_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

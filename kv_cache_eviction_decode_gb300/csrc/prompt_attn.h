@@ -58,11 +58,29 @@ struct SnapSelectParams {
     uint32_t *err;
 };
 
+// SnapKV votes, streamed: one persistent CTA per SM walks a contiguous range of
+// (unit, 128-key tile) items. The unit's stacked window queries (Lq = G * w
+// rows, a multiple of 32, at most 256) stay in shared memory as the MMA's B
+// operand; key tiles stream through a TMA ring as A.
+struct SnapVotesParams {
+    PromptTmap tmk;       // prompt K, rows [B * Hkv * P], boxes of 128 rows x 64
+    PromptTmap tmq;       // window queries, rows [B * Hq * w] (a unit's Lq rows are contiguous), boxes of Lq rows x 64
+    const float *stats;   // [B * Hkv][Ps]: minus the log2 normaliser of each stacked window row
+    float *votes;         // [B * Hq][P]
+    int P, Ps, w, G, Hq, Hkv, Lq;
+    int units;
+    float scale_log2;
+    uint32_t *err;
+};
+constexpr int kSnapVotesMaxRows = 256;  // Lq limit of the streamed votes kernel (one MMA's N)
+
 // Bytes of shared memory the scoring kernels use for head_dim d.
 size_t prompt_attn_smem(int head_dim);
 // Pass 1 (row statistics) and pass 2 (column sums); d in {64, 128}.
 cudaError_t launch_prompt_rowstats(const PromptAttnParams &p, int head_dim, int B, cudaStream_t st);
 cudaError_t launch_prompt_colsum(const PromptAttnParams &p, int head_dim, int B, cudaStream_t st);
+// SnapKV votes with the stacked window resident (Lq <= kSnapVotesMaxRows); `sms` CTAs.
+cudaError_t launch_snapkv_votes(const SnapVotesParams &p, int head_dim, int sms, cudaStream_t st);
 // The cut to the budget and the copy of the kept rows into the cache.
 cudaError_t launch_prompt_select(const PromptSelectParams &p, int units, cudaStream_t st);
 // SnapKV: pooling, per-head top-k, the union with the window, the copy.

@@ -102,7 +102,10 @@ def _cache(device, B, Hq, Hkv, d, n_sink, n_heavy, n_recent):
 
 @pytest.mark.parametrize("G,d,P,w,k", [(1, 64, 90, 8, 10), (4, 128, 300, 32, 20), (8, 128, 700, 32, 12),
                                        (2, 64, 257, 16, 100), (4, 64, 140, 20, 0), (4, 128, 500, 64, 30),
-                                       (8, 64, 333, 96, 10)])
+                                       (8, 64, 333, 96, 10), (2, 64, 400, 32, 40), (1, 128, 333, 32, 50),
+                                       # half of a long prefix kept: the sampled bracket holds more values than
+                                       # the selection keeps on chip, so the full search runs
+                                       (1, 64, 32800, 32, 16000)])
 def test_snapkv_prefill_small(cuda_device, G, d, P, w, k):
     gen = torch.Generator().manual_seed(7000 + G * P + k)
     B, Hkv = 2, 2
@@ -114,6 +117,23 @@ def test_snapkv_prefill_small(cuda_device, G, d, P, w, k):
     assert cache.check() == 0
     np.testing.assert_allclose(votes.float().sum(-1).cpu().numpy(), w, rtol=1e-4)  # each window row sums to 1
     _check_prefill(cache, Qo, K, V, votes, k, [(b, h) for b in range(B) for h in range(Hkv)])
+
+
+@pytest.mark.parametrize("G,w", [(4, 32), (8, 32), (2, 64)])
+def test_snapkv_votes_many_units(cuda_device, G, w):
+    """More (unit, key tile) items than SMs: the streamed votes kernel's CTAs
+    cross unit boundaries (the window rows reloaded); sampled units against
+    the oracle, every window row's votes summing to 1."""
+    gen = torch.Generator().manual_seed(8100 + G * w)
+    B, Hkv, d, P, k = 16, 4, 128, 1000, 20
+    Hq = G * Hkv
+    Qo, K, V = _rand((B, Hq, w, d), gen), _rand((B, Hkv, P, d), gen), _rand((B, Hkv, P, d), gen)
+    cap = G * k + w + 8
+    cache = _cache(cuda_device, B, Hq, Hkv, d, 4, cap - 4 - 2, 2)
+    votes = cache.prefill_snapkv(0, Qo.to(cuda_device), K.to(cuda_device), V.to(cuda_device), k)
+    assert cache.check() == 0
+    np.testing.assert_allclose(votes.float().sum(-1).cpu().numpy(), w, rtol=1e-4)
+    _check_prefill(cache, Qo, K, V, votes, k, [(0, 0), (5, 1), (10, 2), (15, 3)])
 
 
 def test_snapkv_then_decode_lockstep(cuda_device):
