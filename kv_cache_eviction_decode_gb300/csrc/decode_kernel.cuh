@@ -268,6 +268,11 @@ __device__ __forceinline__ int32_t warp_min_s32(int32_t v)
     return v;
 }
 
+// A compile-time flag as a value (selects a specialisation of a generic lambda).
+template <bool B> struct Flag {
+    static constexpr bool value = B;
+};
+
 // Two consecutive elements, moved as one naturally aligned access.
 template <typename T> struct alignas(2 * sizeof(T)) TPair {
     T x, y;
@@ -930,6 +935,47 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         auto candidate = [&](int ps) {
             return pools ? ps >= 0 : (ps >= P.n_sink && ps <= P.p - P.n_recent);
         };
+        // The score pass over this CTA's slots [s_lo, s_lo + n_mine): every retained
+        // score s <- keep * s + a (a: this step's probability, mean over the G heads,
+        // from the logits and the factors fself), and, evicting, the lowest
+        // (score, position) candidate (two-pool: one per pool) and the lowest empty
+        // slot. GEN = false is the plain H2O eviction with fp32 scores (no binary16,
+        // fill or pool branches in the loop); GEN = true handles every mode.
+        const bool general_scores = P.score_half || fill || pools;
+        auto score_pass = [&](auto gen, const float(&fself)[G], uint64_t &best, int32_t &bslot, uint64_t &best2,
+                              int32_t &bslot2, int32_t &emin) {
+            constexpr bool GEN = decltype(gen)::value;
+            for (int j = tid; j < W.n_mine; j += kThreads) {
+                float a = 0.f;
+#pragma unroll
+                for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
+                const size_t si = unit * CS + W.s_lo + j;
+                float sc;
+                if constexpr (GEN) {
+                    sc = score_store(P, si, fmaf(P.score_keep, stored_score(j), a));
+                } else {
+                    sc = fmaf(P.score_keep, ascore[j], a);
+                    static_cast<float *>(P.score)[si] = sc;
+                }
+                if (evict) {
+                    const int ps = apos[j];
+                    if (GEN && (fill || pools) && ps < 0 && W.s_lo + j < emin) emin = W.s_lo + j;
+                    if (GEN ? candidate(ps) : (ps >= P.n_sink && ps <= P.p - P.n_recent)) {
+                        const uint64_t key =
+                            (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
+                        if (GEN && pools && apool[j] != 0) {
+                            if (key < best2) {
+                                best2 = key;
+                                bslot2 = W.s_lo + j;
+                            }
+                        } else if (key < best) {
+                            best = key;
+                            bslot = W.s_lo + j;
+                        }
+                    }
+                }
+            }
+        };
 
         if (S == 1) {
             // ------------------------------ output, one CTA per unit: o / l
@@ -959,29 +1005,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 }
                 uint64_t best = ~0ull, best2 = ~0ull;
                 int32_t bslot = -1, bslot2 = -1, emin = INT_MAX;
-                for (int j = tid; j < W.n_mine; j += kThreads) {
-                    float a = 0.f;
-#pragma unroll
-                    for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
-                    const float sc = score_store(P, unit * CS + j, fmaf(P.score_keep, stored_score(j), a));
-                    if (evict) {
-                        const int ps = apos[j];
-                        if ((fill || pools) && ps < 0 && j < emin) emin = j;
-                        if (candidate(ps)) {
-                            const uint64_t key =
-                                (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
-                            if (pools && apool[j] != 0) {
-                                if (key < best2) {
-                                    best2 = key;
-                                    bslot2 = j;
-                                }
-                            } else if (key < best) {
-                                best = key;
-                                bslot = j;
-                            }
-                        }
-                    }
-                }
+                if (general_scores) score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin);
+                else score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin);
                 if (tid == 0) {
                     float a = 0.f;
 #pragma unroll
@@ -1097,30 +1122,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
                 uint64_t best = ~0ull, best2 = ~0ull;
                 int32_t bslot = -1, bslot2 = -1, emin = INT_MAX;
-                for (int j = tid; j < W.n_mine; j += kThreads) {
-                    float a = 0.f;
-#pragma unroll
-                    for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
-                    const float sc =
-                        score_store(P, unit * CS + W.s_lo + j, fmaf(P.score_keep, stored_score(j), a));
-                    if (evict) {
-                        const int ps = apos[j];
-                        if ((fill || pools) && ps < 0 && W.s_lo + j < emin) emin = W.s_lo + j;
-                        if (candidate(ps)) {
-                            const uint64_t key =
-                                (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
-                            if (pools && apool[j] != 0) {
-                                if (key < best2) {
-                                    best2 = key;
-                                    bslot2 = W.s_lo + j;
-                                }
-                            } else if (key < best) {
-                                best = key;
-                                bslot = W.s_lo + j;
-                            }
-                        }
-                    }
-                }
+                if (general_scores) score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin);
+                else score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin);
                 if (rank == 0 && tid == 0) {
                     float a = 0.f;
 #pragma unroll
