@@ -207,8 +207,10 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
  *         Layout: per query row minus the log2 of its softmax normaliser, fp32
  *         [batch * n_q_heads][Ps] with Ps = prompt_len rounded up to 128; then,
  *         at the next 256-byte boundary, every prompt token's score before the
- *         cut, fp32 [batch][n_kv_heads][prompt_len]. Both are valid once the
- *         stream has passed the call; the caller may reuse the memory after.
+ *         cut, fp32 [batch][n_kv_heads][prompt_len]; then, at the next 256-byte
+ *         boundary, 256 bytes of work counters that the call zeroes and the
+ *         scoring kernels use. The first two are valid once the stream has
+ *         passed the call; the caller may reuse the memory after.
  * The attention statistics run on the tcgen05 tensor cores (bf16 in, fp32
  * accumulate). INVALID_ARG unless the policy is H2O and the dtype bf16, for
  * prompt_len outside 1..49152, for null or misaligned pointers or a short
@@ -239,7 +241,9 @@ int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K,
  *          kvevict_prefill_snapkv_workspace_bytes() bytes, owned by the caller.
  *          Layout: the window rows' normalisers, fp32 [batch * n_q_heads][Ps]
  *          (Ps: the window's tiles of 128 rows); then, at the next 256-byte
- *          boundary, the votes, fp32 [batch][n_q_heads][prompt_len].
+ *          boundary, the votes, fp32 [batch][n_q_heads][prompt_len]; then, at
+ *          the next 256-byte boundary, 256 bytes of work counters that the call
+ *          zeroes and the scoring kernels use.
  * INVALID_ARG unless the policy is H2O and the dtype bf16, for 1 <= window <
  * prompt_len <= 49152 not holding, for G * k_per_head + window above the
  * capacity (the union must fit), for null or misaligned pointers or a short

@@ -746,7 +746,7 @@ namespace {
 // ([B * Hq][Ps], Ps = P rounded up to a tile, so each tile's 128 entries are
 // addressable), then per key its score ([B * Hkv][P]).
 struct ScoredWorkspace {
-    size_t stats_off = 0, score_off = 0, bytes = 0;
+    size_t stats_off = 0, score_off = 0, work_off = 0, bytes = 0;
     int Ps = 0;
 };
 
@@ -756,7 +756,8 @@ ScoredWorkspace scored_workspace(const kvevict_config &c, int P)
     w.Ps = (P + kPromptTile - 1) / kPromptTile * kPromptTile;
     w.stats_off = 0;
     w.score_off = align_up(static_cast<size_t>(c.batch) * c.n_q_heads * w.Ps * 4);
-    w.bytes = w.score_off + align_up(static_cast<size_t>(c.batch) * c.n_kv_heads * P * 4);
+    w.work_off = w.score_off + align_up(static_cast<size_t>(c.batch) * c.n_kv_heads * P * 4);
+    w.bytes = w.work_off + kAlign;  // the scoring passes' work counters
     return w;
 }
 
@@ -811,13 +812,17 @@ int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K,
     ap.per_head = 0;
     ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
     ap.err = at<uint32_t>(h, L.off_err);
+    int *work = reinterpret_cast<int *>(wsb + ws.work_off);  // [0]: pass 1, [1]: pass 2
     // pass 1: A = query tiles, B = key tiles; pass 2: A = key tiles, B = query tiles
     std::memcpy(&ap.tma, &tq, sizeof tq);
     std::memcpy(&ap.tmb, &tk, sizeof tk);
-    cudaError_t e = launch_prompt_rowstats(ap, c.head_dim, c.batch, h->stream);
+    ap.work = work;
+    cudaError_t e = cudaMemsetAsync(work, 0, 2 * sizeof(int), h->stream);
+    if (e == cudaSuccess) e = launch_prompt_rowstats(ap, c.head_dim, c.batch, h->stream);
     if (e == cudaSuccess) {
         std::memcpy(&ap.tma, &tk, sizeof tk);
         std::memcpy(&ap.tmb, &tq, sizeof tq);
+        ap.work = work + 1;
         e = launch_prompt_colsum(ap, c.head_dim, c.batch, h->stream);
     }
     if (e == cudaSuccess) {
@@ -853,7 +858,7 @@ namespace {
 // ([B * Hq][Ps], from the window's first tile on), then the votes of every
 // query head on every prompt key ([B * Hq][P]).
 struct SnapWorkspace {
-    size_t stats_off = 0, votes_off = 0, bytes = 0;
+    size_t stats_off = 0, votes_off = 0, work_off = 0, bytes = 0;
     int Ps = 0, qs0 = 0;
 };
 
@@ -864,7 +869,8 @@ SnapWorkspace snap_workspace(const kvevict_config &c, int P, int window)
     w.Ps = (P - w.qs0 + kPromptTile - 1) / kPromptTile * kPromptTile;
     w.stats_off = 0;
     w.votes_off = align_up(static_cast<size_t>(c.batch) * c.n_q_heads * w.Ps * 4);
-    w.bytes = w.votes_off + align_up(static_cast<size_t>(c.batch) * c.n_q_heads * P * 4);
+    w.work_off = w.votes_off + align_up(static_cast<size_t>(c.batch) * c.n_q_heads * P * 4);
+    w.bytes = w.work_off + kAlign;  // the scoring passes' work counters
     return w;
 }
 
@@ -927,7 +933,10 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
     ap.err = at<uint32_t>(h, L.off_err);
     std::memcpy(&ap.tma, &tq, sizeof tq);
     std::memcpy(&ap.tmb, &tk, sizeof tk);
-    cudaError_t e = launch_prompt_rowstats(ap, c.head_dim, c.batch, h->stream);
+    int *work = reinterpret_cast<int *>(wsb + ws.work_off);  // [0]: pass 1, [1]: pass 2
+    ap.work = work;
+    cudaError_t e = cudaMemsetAsync(work, 0, 2 * sizeof(int), h->stream);
+    if (e == cudaSuccess) e = launch_prompt_rowstats(ap, c.head_dim, c.batch, h->stream);
     const int Lq = L.G * window;
     if (e == cudaSuccess && ap.stacked && Lq <= kSnapVotesMaxRows) {
         // the votes streamed: the unit's stacked window rows stay resident, key tiles stream
@@ -955,6 +964,7 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
     } else if (e == cudaSuccess) {
         std::memcpy(&ap.tma, &tk, sizeof tk);
         std::memcpy(&ap.tmb, &tq, sizeof tq);
+        ap.work = work + 1;
         e = launch_prompt_colsum(ap, c.head_dim, c.batch, h->stream);
     }
     if (e == cudaSuccess) {

@@ -46,11 +46,11 @@ enum PromptMode : int { kRowStats = 0, kColSum = 1 };
 template <int D> struct PromptLayout {
     static constexpr int kTileBytes = kPT * D * 2;
     static constexpr int kBoxBytes = kPT * 128;  // one 128-row x 64-column box
-    static constexpr int kOffA = 0;
-    static constexpr int kOffB = kTileBytes;
+    static constexpr int kOffA = 0;              // two A tiles: the current item's and the next one's
+    static constexpr int kOffB = 2 * kTileBytes;
     static constexpr int kOffBar = kOffB + kPStages * kTileBytes;
-    static constexpr int kOffXchg = kOffBar + 256;
-    static constexpr int kOffPart = kOffXchg + (kSlices - 1) * kPT * 8;  // per-head partials [8][kSlices][128]
+    static constexpr int kOffXchg = kOffBar + 512;  // [2 items][kSlices - 1][128]
+    static constexpr int kOffPart = kOffXchg + 2 * (kSlices - 1) * kPT * 8;  // per-head partials [8][kSlices][128]
     static constexpr int kBytes = kOffPart + 8 * kSlices * kPT * 4 + 1024;  // + slack to align the base to 1 KB
 };
 
@@ -115,110 +115,192 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
     extern __shared__ uint8_t praw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(praw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
-    uint64_t *a_full = bars;
-    uint64_t *b_full = bars + 1;
-    uint64_t *b_empty = b_full + kPStages;
-    uint64_t *s_full = b_empty + kPStages;
-    uint64_t *s_empty = s_full + 2;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(s_empty + 2);
-    float2 *xchg = reinterpret_cast<float2 *>(sm + L::kOffXchg);
+    uint64_t *a_full = bars;                 // [2] an item's A tile landed
+    uint64_t *a_empty = a_full + 2;          // [2] every MMA on that A tile completed
+    uint64_t *b_full = a_empty + 2;          // [kPStages]
+    uint64_t *b_empty = b_full + kPStages;   // [kPStages]
+    uint64_t *s_full = b_empty + kPStages;   // [2] accumulators
+    uint64_t *s_empty = s_full + 2;          // [2]
+    uint64_t *i_full = s_empty + 2;          // [2] the next item's index is posted
+    uint64_t *i_empty = i_full + 2;          // [2] every consumer has read it
+    int *item_idx = reinterpret_cast<int *>(i_empty + 2);  // [2]
+    int *eagree = item_idx + 2;                            // [kEpiWarps] what each epilogue warp read
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(eagree + kEpiWarps);
+    float2 *xchg_all = reinterpret_cast<float2 *>(sm + L::kOffXchg);
     float *hpart = reinterpret_cast<float *>(sm + L::kOffPart);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nT = (p.P + kPT - 1) / kPT;
     const int qlo_t = p.q_lo / kPT;
     const int qs0 = qlo_t * kPT;  // first query row with statistics
-    // This CTA: pass 1 -- query tile `tile` of query head `head` (= b * Hq + qh),
-    // B tiles = key tiles 0..tile of its KV head; pass 2 -- key tile `tile` of
-    // unit `head` (= b * Hkv + kvh), B tiles = (query head g, query tile qt)
-    // for g < G and qt from max(tile, first query tile) on.
-    const int head = blockIdx.y;
     const int Lq = p.G * p.q_stride;  // STACK: stacked rows per unit
     const int nLq = (Lq + kPT - 1) / kPT;
-    const int tile = MODE == kRowStats && !STACK ? nT - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
-    const int qt0 = max(tile, qlo_t), nq = nT - qt0;
-    const int n_b = STACK ? (MODE == kRowStats ? nT : nLq) : (MODE == kRowStats ? tile + 1 : p.G * nq);
-    // Q rows: query i of query head h is row h * q_stride + i - q_first (rows
-    // before a head's first given query belong to the previous head or lie
-    // before the tensor: they only feed masked rows and columns)
-    const int a_row = STACK ? (MODE == kRowStats ? head * Lq + tile * kPT : head * p.P + tile * kPT)
-                            : (MODE == kRowStats ? head * p.q_stride + tile * kPT - p.q_first : head * p.P + tile * kPT);
-    auto b_row = [&](int n) -> int {
-        if (STACK) return MODE == kRowStats ? head * p.P + n * kPT : head * Lq + n * kPT;
+    // Persistent: the CTAs take items of p.nheads x p.ntiles, head-major, from
+    // a work counter (the producer fetches the next index while the current
+    // item streams and posts it to the MMA and epilogue warps), so the items in
+    // flight at one time are consecutive: a few heads, whose B tiles are read
+    // once into L2. Each head's tiles come the most work first. An item: pass 1 --
+    // query tile `tile` of query head `head` (= b * Hq + qh), B tiles = key
+    // tiles 0..tile of its KV head; pass 2 -- key tile `tile` of unit `head`
+    // (= b * Hkv + kvh), B tiles = (query head g, query tile qt) for g < G and
+    // qt from max(tile, first query tile) on.
+    const int n_items = p.ntiles * p.nheads;
+    struct Item {
+        int tile, head, qt0, nq, n_b, a_row;
+    };
+    auto item_at = [&](int k) {
+        Item it;
+        it.head = k / p.ntiles;
+        const int ti = k - it.head * p.ntiles;
+        it.tile = MODE == kRowStats && !STACK ? nT - 1 - ti : ti;
+        it.qt0 = max(it.tile, qlo_t);
+        it.nq = nT - it.qt0;
+        it.n_b = STACK ? (MODE == kRowStats ? nT : nLq) : (MODE == kRowStats ? it.tile + 1 : p.G * it.nq);
+        // Q rows: query i of query head h is row h * q_stride + i - q_first (rows
+        // before a head's first given query belong to the previous head or lie
+        // before the tensor: they only feed masked rows and columns)
+        it.a_row = STACK ? (MODE == kRowStats ? it.head * Lq + it.tile * kPT : it.head * p.P + it.tile * kPT)
+                         : (MODE == kRowStats ? it.head * p.q_stride + it.tile * kPT - p.q_first
+                                              : it.head * p.P + it.tile * kPT);
+        return it;
+    };
+    auto b_row = [&](const Item &it, int n) -> int {
+        if (STACK) return MODE == kRowStats ? it.head * p.P + n * kPT : it.head * Lq + n * kPT;
         if (MODE == kRowStats) {
-            const int b = head / p.Hq, qh = head - b * p.Hq;
+            const int b = it.head / p.Hq, qh = it.head - b * p.Hq;
             return (b * p.Hkv + qh / p.G) * p.P + n * kPT;
         } else {
-            const int b = head / p.Hkv, kvh = head - b * p.Hkv;
-            const int g = n / nq, qt = qt0 + (n - g * nq);
+            const int b = it.head / p.Hkv, kvh = it.head - b * p.Hkv;
+            const int g = n / it.nq, qt = it.qt0 + (n - g * it.nq);
             return (b * p.Hq + kvh * p.G + g) * p.q_stride + qt * kPT - p.q_first;
         }
     };
 
     if (tid == 0) {
-        mbar_init(a_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_empty[s], kEpiWarps);
+        }
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(&b_full[s], 1);
             mbar_init(&b_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&s_full[s], 1);
-            mbar_init(&s_empty[s], kEpiWarps);
+            mbar_init(&i_full[s], 1);
+            mbar_init(&i_empty[s], kEpiWarps + 1);
         }
         mbar_fence_init();
     }
     if (warp == kProdWarp) tmem_alloc(tslot, kTmemCols);
+    // The i-th item of this CTA (slot i & 1): its index, or -1 when the work is
+    // done. `whole_warp`: every lane of the warp calls (the epilogue warps; one
+    // arrival per warp after all lanes have read), else lane 0 alone (the MMA issuer).
+    auto take_item = [&](int i, bool &ok, bool whole_warp) -> int {
+        const int ib = i & 1;
+        if (!mbar_wait(&i_full[ib], (i >> 1) & 1)) {
+            ok = false;
+            return -1;
+        }
+        const int k = *reinterpret_cast<volatile int *>(&item_idx[ib]);
+        if (whole_warp) __syncwarp();
+        if (lane == 0) mbar_arrive(&i_empty[ib]);
+        return k;
+    };
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tslot);
 
+    // Counters over the CTA's whole run: B tiles (ring stage and phase) and
+    // MMA tiles (accumulator and phase) continue across items; A tiles
+    // alternate between two buffers by item.
     int issued_b = 0;     // producer: B tiles whose copies were issued
+    int issued_a = 0;     // producer: A tiles whose copies were issued
     int issued_mma = 0;   // MMA issuer: tiles whose MMAs were issued
+    int freed_a = 0;      // MMA issuer: items whose A tile release was committed
 
     if (warp == kProdWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(a_full, L::kTileBytes);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_2d_plain(sm + L::kOffA + c * L::kBoxBytes, &p.tma, c * 64, a_row, a_full);
-            for (int n = 0; n < n_b; ++n) {
-                const int s = n % kPStages;
-                if (n >= kPStages && !mbar_wait(&b_empty[s], ((n / kPStages) - 1) & 1)) {
-                    flag_timeout(p.err);
+            bool ok = true;
+            for (int i = 0;; ++i) {
+                const int ib = i & 1;
+                if (i >= 2 && !mbar_wait(&i_empty[ib], ((i >> 1) - 1) & 1)) {
+                    ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&b_full[s], L::kTileBytes);
-                const int row = b_row(n);
+                int k = atomicAdd(p.work, 1);
+                if (k >= n_items) k = -1;
+                item_idx[ib] = k;
+                mbar_arrive(&i_full[ib]);
+                if (k < 0) break;
+                const Item it = item_at(k);
+                const int ab = i & 1;
+                if (i >= 2 && !mbar_wait(&a_empty[ab], ((i >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&a_full[ab], L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d_plain(sm + L::kOffB + s * L::kTileBytes + c * L::kBoxBytes, &p.tmb, c * 64, row,
-                                      &b_full[s]);
-                issued_b = n + 1;
+                    tma_load_2d_plain(sm + L::kOffA + ab * L::kTileBytes + c * L::kBoxBytes, &p.tma, c * 64, it.a_row,
+                                      &a_full[ab]);
+                issued_a = i + 1;
+                for (int n = 0; n < it.n_b; ++n) {
+                    const int g = issued_b, s = g % kPStages;
+                    if (g >= kPStages && !mbar_wait(&b_empty[s], ((g / kPStages) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&b_full[s], L::kTileBytes);
+                    const int row = b_row(it, n);
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d_plain(sm + L::kOffB + s * L::kTileBytes + c * L::kBoxBytes, &p.tmb, c * 64, row,
+                                          &b_full[s]);
+                    issued_b = g + 1;
+                }
             }
+            if (!ok) flag_timeout(p.err);
         }
     } else if (warp == kMmaWarp) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kPT, kPT);
-            bool ok = mbar_wait(a_full, 0);
-            for (int n = 0; ok && n < n_b; ++n) {
-                const int s = n % kPStages, acc = n & 1;
-                if (!mbar_wait(&b_full[s], (n / kPStages) & 1)) ok = false;
-                else if (n >= 2 && !mbar_wait(&s_empty[acc], ((n >> 1) - 1) & 1)) ok = false;
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(sm + L::kOffA), b0 = smem_u32(sm + L::kOffB + s * L::kTileBytes);
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t koff = static_cast<uint32_t>((k >> 2) * L::kBoxBytes + (k & 3) * 32);
-                    tc_mma_bf16(tmem + static_cast<uint32_t>(acc * kPT), smem_desc_sw128(a0 + koff),
-                                smem_desc_sw128(b0 + koff), idesc, k > 0);
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int k = take_item(i, ok, false);
+                if (k < 0) break;
+                const Item it = item_at(k);
+                const int ab = i & 1;
+                if (!mbar_wait(&a_full[ab], (i >> 1) & 1)) {
+                    ok = false;
+                    break;
                 }
-                tc_commit(&b_empty[s]);
-                tc_commit(&s_full[acc]);
-                issued_mma = n + 1;
+                const uint32_t a0 = smem_u32(sm + L::kOffA + ab * L::kTileBytes);
+                for (int n = 0; n < it.n_b; ++n) {
+                    const int g = issued_mma, s = g % kPStages, acc = g & 1;
+                    if (!mbar_wait(&b_full[s], (g / kPStages) & 1)) ok = false;
+                    else if (g >= 2 && !mbar_wait(&s_empty[acc], ((g >> 1) - 1) & 1)) ok = false;
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t b0 = smem_u32(sm + L::kOffB + s * L::kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = static_cast<uint32_t>((kk >> 2) * L::kBoxBytes + (kk & 3) * 32);
+                        tc_mma_bf16(tmem + static_cast<uint32_t>(acc * kPT), smem_desc_sw128(a0 + koff),
+                                    smem_desc_sw128(b0 + koff), idesc, kk > 0);
+                    }
+                    tc_commit(&b_empty[s]);
+                    tc_commit(&s_full[acc]);
+                    issued_mma = g + 1;
+                }
+                if (ok) {
+                    tc_commit(&a_empty[ab]);  // the A tile is free once these MMAs complete
+                    freed_a = i + 1;
+                }
             }
             if (!ok) flag_timeout(p.err);
         }
@@ -226,82 +308,143 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
         // ----------------------------------------------------------- epilogue
         const int quad = warp & 3, slice = warp >> 2;
         const int row = quad * 32 + lane;      // TMEM lane = row of the A tile
-        const int a_idx = tile * kPT + row;    // pass 1: query i; pass 2: key j
         const uint32_t lane_field = static_cast<uint32_t>(quad * 32) << 16;
         const int col0 = slice * 32;           // this warp's 32 columns of each tile
         const float c = p.scale_log2;
-        float m = -INFINITY, l = 0.f;          // pass 1: running max and sum (log2 units)
-        float acc = 0.f;                       // pass 2: mass received
         bool ok = true;
-        int cur_g = 0;                         // STACK pass 2: query head of the running sum
-        if (MODE == kColSum && STACK)
-            for (int g = 0; g < p.G; ++g) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
-        // STACK pass 1: a warp whose 32 rows all lie past the stacked rows has nothing to do
-        const bool idle = MODE == kRowStats && STACK && tile * kPT + quad * 32 >= Lq;
-        for (int n = 0; n < n_b; ++n) {
-            const int sb = n & 1;
-            // the TMEM load below is warp-collective: the whole warp agrees on `ok`
-            if (ok && !__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (n >> 1) & 1))) {
-                ok = false;
-                if (lane == 0) flag_timeout(p.err);
+        int gt = 0;                            // tiles consumed over the CTA's run
+        for (int i = 0;; ++i) {
+            // Every epilogue warp takes the posted index (bounded wait), then they all
+            // agree on one through a barrier every warp reaches, so that they leave
+            // the loop together: -1 (no more work) or a failed wait ends it for all.
+            bool okk = true;
+            const int kw = take_item(i, okk, true);
+            if (lane == 0) eagree[warp] = okk ? kw : -2;
+            named_bar_sync(3, kEpiWarps * 32);
+            int k = eagree[0];
+            for (int w = 1; w < kEpiWarps; ++w)
+                if (eagree[w] != k) k = -2;
+            named_bar_sync(3, kEpiWarps * 32);  // eagree may be written again
+            if (k == -2 && lane == 0) flag_timeout(p.err);
+            if (k < 0) break;
+            const Item it = item_at(k);
+            const int tile = it.tile, head = it.head, qt0 = it.qt0, nq = it.nq, n_b = it.n_b;
+            const int a_idx = tile * kPT + row;    // pass 1: query i; pass 2: key j
+            float2 *xchg = xchg_all + (i & 1) * (kSlices - 1) * kPT;
+            float m = -INFINITY, l = 0.f;          // pass 1: running max and sum (log2 units)
+            float acc = 0.f;                       // pass 2: mass received
+            int cur_g = 0;                         // STACK pass 2: query head of the running sum
+            if (MODE == kColSum && (STACK || p.per_head)) {
+                // the previous item's per-head partials have been read (slice 0, after its barrier)
+                if (i > 0) named_bar_sync(2, kEpiWarps * 32);
+                if (STACK)
+                    for (int g = 0; g < p.G; ++g) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
             }
-            tc_fence_after();
-            if (ok && !idle) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_field + static_cast<uint32_t>(sb * kPT + col0), r);
-                tc_wait_ld();
-                if (MODE == kRowStats) {
-                    // keys j = n * 128 + col0 + e; only the diagonal tile is masked (STACK: the
-                    // keys from the window on, against this row's query position)
-                    const int j0 = n * kPT + col0;
-                    const int qi = STACK ? p.P - p.q_stride + a_idx % p.q_stride : a_idx;
-                    float v[32];
-                    if (STACK ? j0 + 32 > p.P - p.q_stride : n == tile) {
+            // STACK pass 1: a warp whose 32 rows all lie past the stacked rows has nothing to do
+            const bool idle = MODE == kRowStats && STACK && tile * kPT + quad * 32 >= Lq;
+            for (int n = 0; n < n_b; ++n, ++gt) {
+                const int sb = gt & 1;
+                // the TMEM load below is warp-collective: the whole warp agrees on `ok`
+                if (ok && !__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gt >> 1) & 1))) {
+                    ok = false;
+                    if (lane == 0) flag_timeout(p.err);
+                }
+                tc_fence_after();
+                if (ok && !idle) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_field + static_cast<uint32_t>(sb * kPT + col0), r);
+                    tc_wait_ld();
+                    if (MODE == kRowStats) {
+                        // keys j = n * 128 + col0 + e; only the diagonal tile is masked (STACK: the
+                        // keys from the window on, against this row's query position)
+                        const int j0 = n * kPT + col0;
+                        const int qi = STACK ? p.P - p.q_stride + a_idx % p.q_stride : a_idx;
+                        float v[32];
+                        if (STACK ? j0 + 32 > p.P - p.q_stride : n == tile) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = (j0 + e <= qi && j0 + e < p.P) ? __uint_as_float(r[e]) : -INFINITY;
+                            for (int e = 0; e < 32; ++e)
+                                v[e] = (j0 + e <= qi && j0 + e < p.P) ? __uint_as_float(r[e]) : -INFINITY;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+                        }
+                        float cm = v[0];
+#pragma unroll
+                        for (int e = 1; e < 32; ++e) cm = fmaxf(cm, v[e]);
+                        cm *= c;  // c > 0: the max of the scaled logits
+                        if (cm > m) {
+                            l *= ex2(m - cm);
+                            m = cm;
+                        }
+                        if (m != -INFINITY) {
+                            const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
+                            float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const float2 z = ffma2(make_float2(v[e], v[e + 1]), c2, nm2);
+                                s2 = fadd2(s2, make_float2(ex2(z.x), ex2(z.y)));
+                            }
+                            l += s2.x + s2.y;
+                        }
+                    } else if (STACK) {
+                        // stacked rows r0 .. r0 + 31 (one query head: w is a multiple of 32)
+                        const int r0 = n * kPT + col0;
+                        if (r0 < Lq) {
+                            const int g = r0 / p.q_stride, i0 = p.P - p.q_stride + (r0 - g * p.q_stride);
+                            if (g != cur_g) {
+                                hpart[(cur_g * kSlices + slice) * kPT + row] = acc;
+                                acc = 0.f;
+                                cur_g = g;
+                            }
+                            const float4 *st = reinterpret_cast<const float4 *>(p.stats + static_cast<size_t>(head) * p.Ps + r0);
+                            const float2 c2 = make_float2(c, c);
+                            float2 s2 = make_float2(0.f, 0.f);
+                            if (a_idx < p.P - p.q_stride) {  // a key before the window: every window query sees it
+#pragma unroll
+                                for (int e4 = 0; e4 < 8; ++e4) {
+                                    const float4 nms = __ldg(st + e4);
+                                    const int e = e4 * 4;
+                                    const float2 za = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                                            c2, make_float2(nms.x, nms.y));
+                                    const float2 zb = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])),
+                                                            c2, make_float2(nms.z, nms.w));
+                                    s2 = fadd2(s2, make_float2(ex2(za.x), ex2(za.y)));
+                                    s2 = fadd2(s2, make_float2(ex2(zb.x), ex2(zb.y)));
+                                }
+                            } else {
+#pragma unroll
+                                for (int e4 = 0; e4 < 8; ++e4) {
+                                    const float4 nms = __ldg(st + e4);
+                                    const float mv[4] = {nms.x, nms.y, nms.z, nms.w};
+#pragma unroll
+                                    for (int t = 0; t < 4; ++t) {
+                                        const int e = e4 * 4 + t;
+                                        const float pr = ex2(fmaf(__uint_as_float(r[e]), c, mv[t]));
+                                        const float add = (i0 + e >= a_idx) ? pr : 0.f;
+                                        if (t & 1) s2.y += add;
+                                        else s2.x += add;
+                                    }
+                                }
+                            }
+                            acc += s2.x + s2.y;
+                        }
                     } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-                    }
-                    float cm = v[0];
-#pragma unroll
-                    for (int e = 1; e < 32; ++e) cm = fmaxf(cm, v[e]);
-                    cm *= c;  // c > 0: the max of the scaled logits
-                    if (cm > m) {
-                        l *= ex2(m - cm);
-                        m = cm;
-                    }
-                    if (m != -INFINITY) {
-                        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
-                        float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float2 z = ffma2(make_float2(v[e], v[e + 1]), c2, nm2);
-                            s2 = fadd2(s2, make_float2(ex2(z.x), ex2(z.y)));
-                        }
-                        l += s2.x + s2.y;
-                    }
-                } else if (STACK) {
-                    // stacked rows r0 .. r0 + 31 (one query head: w is a multiple of 32)
-                    const int r0 = n * kPT + col0;
-                    if (r0 < Lq) {
-                        const int g = r0 / p.q_stride, i0 = p.P - p.q_stride + (r0 - g * p.q_stride);
-                        if (g != cur_g) {
-                            hpart[(cur_g * kSlices + slice) * kPT + row] = acc;
-                            acc = 0.f;
-                            cur_g = g;
-                        }
-                        const float4 *st = reinterpret_cast<const float4 *>(p.stats + static_cast<size_t>(head) * p.Ps + r0);
+                        // queries i = qt * 128 + col0 + e of query head g
+                        const int g = n / nq, qt = qt0 + (n - g * nq);
+                        const int i0 = qt * kPT + col0;
+                        const int b = head / p.Hkv, kvh = head - b * p.Hkv;
+                        const float4 *st = reinterpret_cast<const float4 *>(
+                            p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + (i0 - qs0));
+                        const bool full = qt > tile && i0 + 32 <= p.P && i0 >= p.q_lo;
                         const float2 c2 = make_float2(c, c);
                         float2 s2 = make_float2(0.f, 0.f);
-                        if (a_idx < p.P - p.q_stride) {  // a key before the window: every window query sees it
+                        if (full) {  // every query of these 32 columns attends this key
 #pragma unroll
                             for (int e4 = 0; e4 < 8; ++e4) {
-                                const float4 nms = __ldg(st + e4);
+                                const float4 nms = __ldg(st + e4);  // minus the log2 normalisers
                                 const int e = e4 * 4;
-                                const float2 za = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
-                                                        c2, make_float2(nms.x, nms.y));
+                                const float2 za = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2,
+                                                        make_float2(nms.x, nms.y));
                                 const float2 zb = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])),
                                                         c2, make_float2(nms.z, nms.w));
                                 s2 = fadd2(s2, make_float2(ex2(za.x), ex2(za.y)));
@@ -314,99 +457,61 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                                 const float mv[4] = {nms.x, nms.y, nms.z, nms.w};
 #pragma unroll
                                 for (int t = 0; t < 4; ++t) {
-                                    const int e = e4 * 4 + t;
+                                    const int e = e4 * 4 + t, i = i0 + e;
                                     const float pr = ex2(fmaf(__uint_as_float(r[e]), c, mv[t]));
-                                    const float add = (i0 + e >= a_idx) ? pr : 0.f;
+                                    const float add = (i >= a_idx && i < p.P && i >= p.q_lo) ? pr : 0.f;
                                     if (t & 1) s2.y += add;
                                     else s2.x += add;
                                 }
                             }
                         }
                         acc += s2.x + s2.y;
+                        if (p.per_head && n - g * nq == nq - 1) {  // the last tile of query head g
+                            hpart[(g * kSlices + slice) * kPT + row] = acc;
+                            acc = 0.f;
+                        }
+                    }
+                } else if (MODE == kColSum && p.per_head && !STACK) {
+                    const int g = n / nq;
+                    if (n - g * nq == nq - 1) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
+            }
+            if (MODE == kColSum && STACK) hpart[(cur_g * kSlices + slice) * kPT + row] = acc;
+            // the column slices of each row meet: slices 1.. hand over to slice 0
+            if (slice > 0) xchg[(slice - 1) * kPT + row] = MODE == kRowStats ? make_float2(m, l) : make_float2(acc, 0.f);
+            named_bar_sync(1, kEpiWarps * 32);
+            if (slice == 0 && ok) {
+                if (MODE == kRowStats) {
+                    float mm = m;
+#pragma unroll
+                    for (int k = 0; k < kSlices - 1; ++k) mm = fmaxf(mm, xchg[k * kPT + row].x);
+                    float ll = m == -INFINITY ? 0.f : l * ex2(m - mm);
+#pragma unroll
+                    for (int k = 0; k < kSlices - 1; ++k) {
+                        const float2 o = xchg[k * kPT + row];
+                        if (o.x != -INFINITY) ll += o.y * ex2(o.x - mm);
+                    }
+                    if (STACK ? a_idx < Lq : a_idx < p.P)
+                        p.stats[static_cast<size_t>(head) * p.Ps + (STACK ? a_idx : a_idx - qs0)] = -(mm + log2f(ll));
+                } else if (p.per_head || STACK) {
+                    if (a_idx < p.P) {
+                        const int b = head / p.Hkv, kvh = head - b * p.Hkv;
+                        for (int g = 0; g < p.G; ++g) {
+                            float tot = 0.f;
+#pragma unroll
+                            for (int k = 0; k < kSlices; ++k) tot += hpart[(g * kSlices + k) * kPT + row];
+                            p.score[static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.P + a_idx] = tot;
+                        }
                     }
                 } else {
-                    // queries i = qt * 128 + col0 + e of query head g
-                    const int g = n / nq, qt = qt0 + (n - g * nq);
-                    const int i0 = qt * kPT + col0;
-                    const int b = head / p.Hkv, kvh = head - b * p.Hkv;
-                    const float4 *st = reinterpret_cast<const float4 *>(
-                        p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + (i0 - qs0));
-                    const bool full = qt > tile && i0 + 32 <= p.P && i0 >= p.q_lo;
-                    const float2 c2 = make_float2(c, c);
-                    float2 s2 = make_float2(0.f, 0.f);
-                    if (full) {  // every query of these 32 columns attends this key
+                    float tot = acc;
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 nms = __ldg(st + e4);  // minus the log2 normalisers
-                            const int e = e4 * 4;
-                            const float2 za = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2,
-                                                    make_float2(nms.x, nms.y));
-                            const float2 zb = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])),
-                                                    c2, make_float2(nms.z, nms.w));
-                            s2 = fadd2(s2, make_float2(ex2(za.x), ex2(za.y)));
-                            s2 = fadd2(s2, make_float2(ex2(zb.x), ex2(zb.y)));
-                        }
-                    } else {
-#pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 nms = __ldg(st + e4);
-                            const float mv[4] = {nms.x, nms.y, nms.z, nms.w};
-#pragma unroll
-                            for (int t = 0; t < 4; ++t) {
-                                const int e = e4 * 4 + t, i = i0 + e;
-                                const float pr = ex2(fmaf(__uint_as_float(r[e]), c, mv[t]));
-                                const float add = (i >= a_idx && i < p.P && i >= p.q_lo) ? pr : 0.f;
-                                if (t & 1) s2.y += add;
-                                else s2.x += add;
-                            }
-                        }
-                    }
-                    acc += s2.x + s2.y;
-                    if (p.per_head && n - g * nq == nq - 1) {  // the last tile of query head g
-                        hpart[(g * kSlices + slice) * kPT + row] = acc;
-                        acc = 0.f;
-                    }
+                    for (int k = 0; k < kSlices - 1; ++k) tot += xchg[k * kPT + row].x;
+                    if (a_idx < p.P) p.score[static_cast<size_t>(head) * p.P + a_idx] = tot * (1.f / p.G);
                 }
-            } else if (MODE == kColSum && p.per_head && !STACK) {
-                const int g = n / nq;
-                if (n - g * nq == nq - 1) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[sb]);
-        }
-        if (MODE == kColSum && STACK) hpart[(cur_g * kSlices + slice) * kPT + row] = acc;
-        // the column slices of each row meet: slices 1.. hand over to slice 0
-        if (slice > 0) xchg[(slice - 1) * kPT + row] = MODE == kRowStats ? make_float2(m, l) : make_float2(acc, 0.f);
-        named_bar_sync(1, kEpiWarps * 32);
-        if (slice == 0 && ok) {
-            if (MODE == kRowStats) {
-                float mm = m;
-#pragma unroll
-                for (int k = 0; k < kSlices - 1; ++k) mm = fmaxf(mm, xchg[k * kPT + row].x);
-                float ll = m == -INFINITY ? 0.f : l * ex2(m - mm);
-#pragma unroll
-                for (int k = 0; k < kSlices - 1; ++k) {
-                    const float2 o = xchg[k * kPT + row];
-                    if (o.x != -INFINITY) ll += o.y * ex2(o.x - mm);
-                }
-                if (STACK ? a_idx < Lq : a_idx < p.P)
-                    p.stats[static_cast<size_t>(head) * p.Ps + (STACK ? a_idx : a_idx - qs0)] = -(mm + log2f(ll));
-            } else if (p.per_head || STACK) {
-                if (a_idx < p.P) {
-                    const int b = head / p.Hkv, kvh = head - b * p.Hkv;
-                    for (int g = 0; g < p.G; ++g) {
-                        float tot = 0.f;
-#pragma unroll
-                        for (int k = 0; k < kSlices; ++k) tot += hpart[(g * kSlices + k) * kPT + row];
-                        p.score[static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.P + a_idx] = tot;
-                    }
-                }
-            } else {
-                float tot = acc;
-#pragma unroll
-                for (int k = 0; k < kSlices - 1; ++k) tot += xchg[k * kPT + row].x;
-                if (a_idx < p.P) p.score[static_cast<size_t>(head) * p.P + a_idx] = tot * (1.f / p.G);
             }
         }
     }
@@ -416,9 +521,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
     if (warp == kProdWarp && lane == 0) {
         for (int n = max(0, issued_b - kPStages); n < issued_b; ++n)
             mbar_wait(&b_full[n % kPStages], (n / kPStages) & 1);
+        for (int i = max(0, issued_a - 2); i < issued_a; ++i) mbar_wait(&a_full[i & 1], (i >> 1) & 1);
     }
     if (warp == kMmaWarp && lane == 0) {
         for (int n = max(0, issued_mma - 2); n < issued_mma; ++n) mbar_wait(&s_full[n & 1], (n >> 1) & 1);
+        for (int i = max(0, freed_a - 2); i < freed_a; ++i) mbar_wait(&a_empty[i & 1], (i >> 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -1104,18 +1211,26 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const Sn
     snap_union_tail(p, keep, ops, unit, b, kvh);
 }
 
-template <int D, int MODE, bool STACK> cudaError_t launch_attn_t(const PromptAttnParams &p, int B, cudaStream_t st)
+template <int D, int MODE, bool STACK> cudaError_t launch_attn_t(const PromptAttnParams &p0, int B, cudaStream_t st)
 {
     const int smem = PromptLayout<D>::kBytes;
     cudaError_t e =
         cudaFuncSetAttribute(prompt_attn_kernel<D, MODE, STACK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    PromptAttnParams p = p0;
     const int nT = (p.P + kPT - 1) / kPT;
     const int nLq = (p.G * p.q_stride + kPT - 1) / kPT;
-    const int tiles = STACK ? (MODE == kRowStats ? nLq : nT) : (MODE == kRowStats ? nT - p.q_lo / kPT : nT);
-    const int heads = STACK ? B * p.Hkv : (MODE == kRowStats ? B * p.Hq : B * p.Hkv);
-    if (tiles <= 0 || heads <= 0) return cudaSuccess;
-    prompt_attn_kernel<D, MODE, STACK><<<dim3(tiles, heads), kPThreads, smem, st>>>(p);
+    p.ntiles = STACK ? (MODE == kRowStats ? nLq : nT) : (MODE == kRowStats ? nT - p.q_lo / kPT : nT);
+    p.nheads = STACK ? B * p.Hkv : (MODE == kRowStats ? B * p.Hq : B * p.Hkv);
+    if (p.ntiles <= 0 || p.nheads <= 0) return cudaSuccess;
+    // persistent: one CTA per SM (the shared memory admits one), at most one per item
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long items = static_cast<long long>(p.ntiles) * p.nheads;
+    const int grid = static_cast<int>(std::min<long long>(items, std::max(sms, 1)));
+    prompt_attn_kernel<D, MODE, STACK><<<grid, kPThreads, smem, st>>>(p);
     return cudaGetLastError();
 }
 

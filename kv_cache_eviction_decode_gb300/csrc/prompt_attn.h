@@ -34,6 +34,8 @@ struct PromptAttnParams {
                           // (row g * q_stride + t); stats then [B * Hkv][Ps] over the stacked rows
     float scale_log2;     // log2(e) / sqrt(d)
     uint32_t *err;
+    int ntiles, nheads;   // set by the launcher: the items (tile, head) of the persistent grid
+    int *work;            // the launch's work counter (zero before it; the CTAs take items from it)
 };
 
 struct PromptSelectParams {
