@@ -74,11 +74,11 @@ def test_score_storage_rejected_where_unsupported(cuda_device):
     c.close()
 
 
-def test_fp16_scores_full_shape(cuda_device):
-    """H2O 4 + 510 + 510 on the MHA shape with binary16 scores: B=16, 32x32
-    heads, d=128, prompt 2048, 200 steps; sequences {0, 15} x every head of
-    layers {0, 31} in lockstep."""
-    w = configs.H2O_MHA_FP16
+@pytest.mark.parametrize("w", [configs.H2O_MHA_FP16, configs.H2O_MHA_EMA], ids=["binary16", "moving_average"])
+def test_score_storage_full_shape(cuda_device, w):
+    """H2O 4 + 510 + 510 on the MHA shape with binary16 scores, and with the
+    moving average (forget 0.01): B=16, 32x32 heads, d=128, prompt 2048, 200
+    steps; sequences {0, 15} x every head of layers {0, 31} in lockstep."""
     T = 200
     layers = [0, w.n_layers - 1]
     checked = [(s, l, h) for l in layers for s in (0, w.batch - 1) for h in range(w.n_kv_heads)]
@@ -87,7 +87,7 @@ def test_fp16_scores_full_shape(cuda_device):
     run = ls.run_gpu(w, layers, T, inputs, w.prompt_len, cuda_device, snap_steps=snaps)
     assert run.err == 0
     reps = ls.replay_all(w, checked, inputs, run, T, out_steps=range(0, T, 7))
-    print("fp16 scores full shape: near ties", sum(r.near_ties for r in reps),
+    print(w.name, "full shape: near ties", sum(r.near_ties for r in reps),
           "max out err", max(r.max_out_err for r in reps))
     for layer in layers:
         assert ls.check_selector(w, run, layer, w.prompt_len) == len(snaps)
