@@ -97,3 +97,39 @@ def test_create_rejects_bad_state_without_touching_the_gpu(L):
     assert L.kvevict_create(ctypes.byref(h), ctypes.byref(c), ctypes.c_void_p(0x1001), 1 << 30, None) == -1  # misaligned
     assert L.kvevict_create(ctypes.byref(h), ctypes.byref(c), ctypes.c_void_p(0x1000), 16, None) == -2  # too small
     assert not h.value
+
+
+@pytest.mark.parametrize("bad", [
+    dict(policy=3, r=7),                                          # block H2O: budget not whole blocks
+    dict(policy=3, r=0),                                          # block H2O: no block size
+    dict(policy=3, n_sink=4, n_heavy=4, n_recent=120, r=16),      # no block outside sinks and the window
+    dict(policy=4),                                               # two-pool H2O has no sinks
+    dict(policy=4, n_sink=0, n_heavy=60, n_recent=64),            # pools do not add up to the budget
+    dict(policy=4, n_sink=0, n_heavy=128, n_recent=0),            # an empty recent pool
+    dict(policy=4, n_sink=0, n_heavy=64, n_recent=64, hh_threshold=float("nan")),
+    dict(score_forget=1.0),                                       # the moving average needs forget < 1
+    dict(score_forget=-0.1),
+    dict(policy=1, n_heavy=0, n_recent=124, score_forget=0.1),    # StreamingLLM keeps no scores
+    dict(policy=3, r=16, score_half=1),                           # binary16 scores: not block H2O
+    dict(score_half=2),
+])
+def test_invalid_next_row_configs_rejected_on_host(L, bad):
+    rc, _ = _bytes(L, _cfg(**bad))
+    assert rc == -1
+
+
+def test_state_bytes_of_the_next_rows(L):
+    rc, n_h2o = _bytes(L, _cfg())
+    assert rc == 0
+    # binary16 scores: half the score region (within the 256-byte alignment of each region)
+    rc, n_half = _bytes(L, _cfg(score_half=1))
+    assert rc == 0 and n_h2o - n_half >= 3 * 16 * 128 * 2 - 2 * 256
+    # two-pool H2O: a one-byte pool flag per slot on top of H2O's regions
+    rc, n_pools = _bytes(L, _cfg(policy=4, n_sink=0, n_heavy=64, n_recent=64, hh_threshold=0.01))
+    assert rc == 0 and n_pools - n_h2o >= 3 * 16 * 128
+    # block H2O: a free list of r entries per unit
+    rc, n_block = _bytes(L, _cfg(policy=3, r=16))
+    assert rc == 0 and n_block - n_h2o >= 3 * 16 * 16 * 4
+    # the moving average changes no layout
+    rc, n_ema = _bytes(L, _cfg(score_forget=0.25))
+    assert rc == 0 and n_ema == n_h2o
