@@ -319,7 +319,10 @@ def run_ours(args, w, rank, world, device):
             kh = kn[:2].cpu().pin_memory()
             vh = vn[:2].cpu().pin_memory()
             oh = torch.empty((L, B, Hq, D), dtype=q.dtype).pin_memory()
-            dech = Lb.kvevict_decode_step_host
+            # every layer-step through the host-buffer call that does not wait (inputs
+            # in on the copy stream while the previous step runs, output back), one
+            # kvevict_sync per token-step: its outputs are on the host when it returns
+            dech = Lb.kvevict_decode_step_host_async
             n_e2e = max(2, min(args.steps, 10))
             barrier(device)
             torch.cuda.synchronize(device)
@@ -329,7 +332,10 @@ def run_ours(args, w, rank, world, device):
                     rc = dech(h, layer, qh[s & 1, layer].data_ptr(), kh[s & 1, layer].data_ptr(),
                               vh[s & 1, layer].data_ptr(), oh[layer].data_ptr())
                     if rc:
-                        raise RuntimeError(f"kvevict_decode_step_host failed: {rc}")
+                        raise RuntimeError(f"kvevict_decode_step_host_async failed: {rc}")
+                rc = Lb.kvevict_sync(h)
+                if rc:
+                    raise RuntimeError(f"kvevict_sync failed: {rc}")
             e2e_s = reduce_max(time.perf_counter() - t0, device)
             h2d = L * (q[0, 0].numel() + kn[0, 0].numel() + vn[0, 0].numel()) * q.element_size()
             d2h = L * out[0, 0].numel() * q.element_size()

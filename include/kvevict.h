@@ -160,7 +160,7 @@ typedef struct {
 } kvevict_stats;
 
 /* Bytes of device memory a handle with this configuration needs (cache,
- * positions, scores, free lists, error word, host-path staging). Host only:
+ * positions, scores, free lists, error word, two slots of host-path staging). Host only:
  * launches nothing, needs no GPU. Returns INVALID_ARG for a configuration
  * the library does not accept. */
 int kvevict_state_bytes(const kvevict_config *cfg, size_t *bytes);
@@ -287,6 +287,23 @@ int kvevict_decode_step(kvevict_t h, int layer, const void *q, const void *k_new
  * out back on the handle's stream, then waits for the stream. */
 int kvevict_decode_step_host(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new,
                              void *out);
+
+/* kvevict_decode_step_host without waiting, for pipelining host-buffer steps:
+ * the inputs are copied in on an internal copy-in stream, into one of two
+ * staging slots that alternate between calls; the step runs on the handle's
+ * stream once they are in; the output is copied back on an internal copy-out
+ * stream once the step is done. A call's copy-in overlaps the previous call's
+ * step, and its copy-out the next call's. The host buffers (pinned memory) must
+ * stay valid, and the inputs unchanged, until kvevict_sync returns; the output
+ * holds the result only then. Steps run in call order on the handle's stream.
+ * kvevict_decode_step_host waits for the pending calls first. The streams and
+ * their events are created on the first call. */
+int kvevict_decode_step_host_async(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new,
+                                   void *out);
+
+/* Waits for every call queued on the handle: its stream and the copy streams
+ * of kvevict_decode_step_host_async. Returns CUDA if any reported an error. */
+int kvevict_sync(kvevict_t h);
 
 /* Position held by every slot of `layer`, -1 for an empty slot:
  * dst [batch][n_kv_heads][C] int32, device (dst_is_device = 1, asynchronous)

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.kvevict_prefill_snapkv.argtypes = [P, I, P, P, P, I, I, I, P, SZ]
             L.kvevict_decode_step.argtypes = [P, I, P, P, P, P]
             L.kvevict_decode_step_host.argtypes = [P, I, P, P, P, P]
+            L.kvevict_decode_step_host_async.argtypes = [P, I, P, P, P, P]
+            L.kvevict_sync.argtypes = [P]
             L.kvevict_slot_positions.argtypes = [P, I, P, I]
             L.kvevict_scores.argtypes = [P, I, P, I]
             L.kvevict_slot_pools.argtypes = [P, I, P, I]
@@ -81,7 +83,7 @@ def lib() -> ctypes.CDLL:
             for n in ("kvevict_state_bytes", "kvevict_create", "kvevict_prefill", "kvevict_prefill_scored_workspace_bytes",
                       "kvevict_prefill_scored", "kvevict_prefill_scored_static",
                       "kvevict_prefill_snapkv_workspace_bytes", "kvevict_prefill_snapkv", "kvevict_decode_step",
-                      "kvevict_decode_step_host", "kvevict_slot_positions", "kvevict_scores", "kvevict_slot_pools",
+                      "kvevict_decode_step_host", "kvevict_decode_step_host_async", "kvevict_sync", "kvevict_slot_positions", "kvevict_scores", "kvevict_slot_pools",
                       "kvevict_set_trace",
                       "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",

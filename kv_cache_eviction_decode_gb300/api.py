@@ -163,6 +163,21 @@ class KVEvictCache:
               "kvevict_decode_step_host")
         return out
 
+    def decode_step_host_async(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                               out: torch.Tensor) -> torch.Tensor:
+        """decode_step_host without waiting: pinned CPU tensors that must stay
+        alive and unchanged until sync(); out holds the result after sync()."""
+        self._host(q, (self.B, self.Hq, self.D), "q")
+        self._host(k_new, (self.B, self.Hkv, self.D), "k_new")
+        self._host(v_new, (self.B, self.Hkv, self.D), "v_new")
+        self._host(out, (self.B, self.Hq, self.D), "out")
+        check(self._L.kvevict_decode_step_host_async(self.h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out)),
+              "kvevict_decode_step_host_async")
+        return out
+
+    def sync(self) -> None:
+        check(self._L.kvevict_sync(self.h), "kvevict_sync")
+
     # ----------------------------------------------------------------- state
     def slot_positions(self, layer: int, out: torch.Tensor | None = None) -> torch.Tensor:
         shp = (self.B, self.Hkv, self.capacity)

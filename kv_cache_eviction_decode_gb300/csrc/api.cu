@@ -48,7 +48,7 @@ struct Layout {
     size_t layer_pslots = 0;  // units * Cs (pos/score entries)
     size_t kv_layer_bytes = 0;
     size_t off_k = 0, off_v = 0, off_pos = 0, off_score = 0, off_pool = 0, off_free = 0, off_err = 0;
-    size_t off_sq = 0, off_sk = 0, off_sv = 0, off_so = 0;
+    size_t off_sq[2] = {}, off_sk[2] = {}, off_sv[2] = {}, off_so[2] = {};  // host-path staging, two slots
     size_t total = 0;
     size_t q_bytes = 0, kvtok_bytes = 0;  // one layer-step's q/out and k_new/v_new
 };
@@ -136,10 +136,12 @@ Layout make_layout(const kvevict_config *c)
     L.off_err = off; off = align_up(off + 16);
     L.q_bytes = static_cast<size_t>(c->batch) * c->n_q_heads * c->head_dim * L.elem;
     L.kvtok_bytes = L.units * c->head_dim * L.elem;
-    L.off_sq = off; off = align_up(off + L.q_bytes);
-    L.off_sk = off; off = align_up(off + L.kvtok_bytes);
-    L.off_sv = off; off = align_up(off + L.kvtok_bytes);
-    L.off_so = off; off = align_up(off + L.q_bytes);
+    for (int i = 0; i < 2; ++i) {
+        L.off_sq[i] = off; off = align_up(off + L.q_bytes);
+        L.off_sk[i] = off; off = align_up(off + L.kvtok_bytes);
+        L.off_sv[i] = off; off = align_up(off + L.kvtok_bytes);
+        L.off_so[i] = off; off = align_up(off + L.q_bytes);
+    }
     L.total = off;
     return L;
 }
@@ -176,6 +178,27 @@ struct kvevict_handle {
     std::vector<CUtensorMap> tmk, tmv;  // per layer (bf16 caches)
     std::vector<LayerState> layers;
     kvevict_stats stats{};
+    // host-buffer path without waiting: a stream for the copies in, one for the
+    // copies out, and per staging slot the events "inputs are in", "the step is
+    // done" and "the output is out" (created on first use)
+    cudaStream_t in_stream = nullptr, out_stream = nullptr;
+    cudaEvent_t ev_in[2] = {}, ev_step[2] = {}, ev_out[2] = {};
+    int async_calls = 0;
+    bool async_pending = false;
+    ~kvevict_handle()
+    {
+        if (in_stream) {
+            cudaStreamSynchronize(in_stream);
+            cudaStreamSynchronize(out_stream);
+            for (int i = 0; i < 2; ++i) {
+                cudaEventDestroy(ev_in[i]);
+                cudaEventDestroy(ev_step[i]);
+                cudaEventDestroy(ev_out[i]);
+            }
+            cudaStreamDestroy(in_stream);
+            cudaStreamDestroy(out_stream);
+        }
+    }
     // decode kernel configured for (split, holes): function, shared memory, zcap
     struct Configured {
         int split = 0, clusters_req = -1, ring_req = -1;
@@ -1012,13 +1035,81 @@ int kvevict_decode_step(kvevict_t h, int layer, const void *q, const void *k_new
     return launch_decode(h, layer, q, k_new, v_new, out);
 }
 
+int kvevict_sync(kvevict_t h)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    if (h->in_stream) {
+        e = cudaStreamSynchronize(h->in_stream);
+        cudaError_t e1 = cudaStreamSynchronize(h->out_stream);
+        if (e == cudaSuccess) e = e1;
+    }
+    cudaError_t e2 = cudaStreamSynchronize(h->stream);
+    h->async_pending = false;
+    return cuda_status(e != cudaSuccess ? e : e2);
+}
+
+int kvevict_decode_step_host_async(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new,
+                                   void *out)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
+    if (h->layers[layer].prompt_len + static_cast<long long>(h->layers[layer].t) >= (1LL << 31) - 1)
+        return KVEVICT_ERR_STATE;
+    cudaError_t e = cudaSuccess;
+    if (!h->in_stream) {
+        e = cudaStreamCreateWithFlags(&h->in_stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->out_stream, cudaStreamNonBlocking);
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_step[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    const Layout &L = h->L;
+    const int sl = h->async_calls & 1;
+    void *dq = h->state + L.off_sq[sl], *dk = h->state + L.off_sk[sl], *dv = h->state + L.off_sv[sl];
+    void *dout = h->state + L.off_so[sl];
+    // Inputs in on the copy-in stream, once the step two calls back (same slot)
+    // has read them; a wait on an event never recorded passes at once.
+    e = cudaStreamWaitEvent(h->in_stream, h->ev_step[sl], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, q, L.q_bytes, cudaMemcpyHostToDevice, h->in_stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k_new, L.kvtok_bytes, cudaMemcpyHostToDevice, h->in_stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v_new, L.kvtok_bytes, cudaMemcpyHostToDevice, h->in_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_in[sl], h->in_stream);
+    // the step on the handle's stream once the inputs are in and the copy-out two
+    // calls back has drained this slot's output
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, h->ev_in[sl], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, h->ev_out[sl], 0);
+    if (e != cudaSuccess) return cuda_status(e);
+    h->last_layer = -1;  // the launch follows event waits, not a kernel of this handle
+    int rc = launch_decode(h, layer, dq, dk, dv, dout);
+    if (rc) return rc;
+    // the output back on the copy-out stream once the step (and a Random cut) is done
+    e = cudaEventRecord(h->ev_step[sl], h->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->out_stream, h->ev_step[sl], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(out, dout, L.q_bytes, cudaMemcpyDeviceToHost, h->out_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_out[sl], h->out_stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    h->async_calls++;
+    h->async_pending = true;
+    return KVEVICT_OK;
+}
+
 int kvevict_decode_step_host(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new, void *out)
 {
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
+    if (h->async_pending) {  // calls without waiting may still use the staging slots
+        int rc0 = kvevict_sync(h);
+        if (rc0) return rc0;
+    }
     const Layout &L = h->L;
-    void *dq = h->state + L.off_sq, *dk = h->state + L.off_sk, *dv = h->state + L.off_sv, *dout = h->state + L.off_so;
+    void *dq = h->state + L.off_sq[0], *dk = h->state + L.off_sk[0], *dv = h->state + L.off_sv[0];
+    void *dout = h->state + L.off_so[0];
     h->last_layer = -1;  // the launch follows copies, not a kernel of this handle
     cudaError_t e = cudaMemcpyAsync(dq, q, L.q_bytes, cudaMemcpyHostToDevice, h->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k_new, L.kvtok_bytes, cudaMemcpyHostToDevice, h->stream);

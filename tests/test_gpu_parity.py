@@ -227,6 +227,43 @@ def test_host_buffer_path_matches_device_path(cuda_device):
     assert torch.equal(a.scores(0), b.scores(0))
 
 
+@pytest.mark.parametrize("policy", [configs.POLICY_H2O, configs.POLICY_RANDOM])
+def test_host_async_path_matches_device_path(cuda_device, policy):
+    """The host-buffer calls that do not wait, three layers a token and one
+    sync per token (staging slots reused across layers and tokens; Random's cut
+    launches inside): outputs, slot tables and scores equal the device path's."""
+    kw = dict(n_sink=2, n_heavy=20, n_recent=10, budget=32, prompt_len=40) if policy == configs.POLICY_H2O else \
+        dict(budget=12, r=4, max_prompt=40, prompt_len=40)
+    w = _small(policy, configs.DTYPE_BF16, G=4, d=128, B=2, L=3, decode_steps=14, **kw)
+    a = KVEvictCache.from_workload(w, device=cuda_device)
+    b = KVEvictCache.from_workload(w, device=cuda_device)
+    for layer in range(w.n_layers):
+        K, V = synth.device_prompt(w, layer, cuda_device, w.prompt_len)
+        a.prefill(layer, K, V)
+        b.prefill(layer, K, V)
+    g = torch.Generator(device=cuda_device)
+    g.manual_seed(6)
+    for t in range(w.decode_steps):
+        host = []
+        for layer in range(w.n_layers):
+            q = torch.randn((2, 16, 128), generator=g, device=cuda_device).to(torch.bfloat16)
+            k = torch.randn((2, 4, 128), generator=g, device=cuda_device).to(torch.bfloat16)
+            v = torch.randn((2, 4, 128), generator=g, device=cuda_device).to(torch.bfloat16)
+            o1 = a.decode_step(layer, q, k, v)
+            ins = (q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory())
+            o2 = torch.empty((2, 16, 128), dtype=torch.bfloat16).pin_memory()
+            b.decode_step_host_async(layer, *ins, o2)
+            host.append((o1, ins, o2))  # the host buffers stay alive until the sync
+        b.sync()
+        for o1, _, o2 in host:
+            assert torch.equal(o1.cpu(), o2)
+    for layer in range(w.n_layers):
+        assert torch.equal(a.slot_positions(layer), b.slot_positions(layer))
+        if policy == configs.POLICY_H2O:
+            assert torch.equal(a.scores(layer), b.scores(layer))
+    assert a.check() == 0 and b.check() == 0
+
+
 def test_nonfinite_query_sets_error_bit_and_continues(cuda_device):
     """A NaN planted in q: the step completes, the device error word reports
     it, nothing traps, and the handle keeps working."""
