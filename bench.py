@@ -161,10 +161,11 @@ def barrier(device=None):
 # CPU baseline: the oracle as it stands, on the host cores, on a sample
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(w, n_units: int, target_s: float, max_steps: int = 4096):
-    """Times the oracle on n_units units of one layer, already in steady state
-    (prompt or fill built by the oracle's own prefill), over as many decode
-    steps as fit ~target_s. Returns (unit_steps_per_s, threads, description, seconds)."""
+def oracle_sampler(w, n_units: int, target_s: float, max_steps: int = 4096):
+    """Builds n_units units of one layer in the oracle, already in steady state
+    (prompt or fill built by the oracle's own prefill), and sizes one sample to
+    as many decode steps as fit ~target_s. Returns (sample, unit_steps, threads,
+    description): sample() runs one sample and returns its seconds."""
     import numpy as np
     import oracle
     P = w.prompt_len if w.prompt_len else w.capacity  # stream-from-empty workloads: fill the cache first
@@ -185,23 +186,31 @@ def oracle_sample_rate(w, n_units: int, target_s: float, max_steps: int = 4096):
         units.append(u)
     threads = min(oracle.online_cores(), n_units)
 
-    def timed(xs, a, b):
-        q = np.stack([x.q[a:b] for x in xs])
-        k = np.stack([x.k_new[a:b] for x in xs])
-        v = np.stack([x.v_new[a:b] for x in xs])
+    def stacked(xs, a, b):
+        return (np.stack([x.q[a:b] for x in xs]), np.stack([x.k_new[a:b] for x in xs]),
+                np.stack([x.v_new[a:b] for x in xs]))
+
+    def timed(qkv):
         t0 = time.perf_counter()
-        oracle.run(units, q, k, v, n_threads=threads)
+        oracle.run(units, *qkv, n_threads=threads)
         return time.perf_counter() - t0
 
-    xs = [synth.UnitInputs(w, seq, 0, h, 1, P) for seq, h in ids]
-    one = timed(xs, 0, 1)
+    one = timed(stacked([synth.UnitInputs(w, seq, 0, h, 1, P) for seq, h in ids], 0, 1))
     M = int(max(1, min(max_steps, target_s / max(one, 1e-6))))
-    xs = [synth.UnitInputs(w, seq, 0, h, 1 + M, P) for seq, h in ids]
-    dt = timed(xs, 1, 1 + M)
+    # the same M inputs for every sample: a unit's work per step does not depend on them
+    qkv = stacked([synth.UnitInputs(w, seq, 0, h, 1 + M, P) for seq, h in ids], 1, 1 + M)
     start = "the cache after the prompt" if w.policy == configs.POLICY_H2O_POOLS else "a full cache"
     desc = (f"{n_units} units of one layer (of {w.batch * w.n_kv_heads} per layer, {w.n_layers} layers) "
-            f"x {M} decode steps from {start}, {dt:.1f} s")
-    return n_units * M / dt, threads, desc, dt
+            f"x {M} decode steps from {start}")
+    return (lambda: timed(qkv)), n_units * M, threads, desc
+
+
+def oracle_sample_rate(w, n_units: int, target_s: float, max_steps: int = 4096):
+    """One timed sample of the oracle (see oracle_sampler). Returns
+    (unit_steps_per_s, threads, description, seconds)."""
+    sample, work, threads, desc = oracle_sampler(w, n_units, target_s, max_steps)
+    dt = sample()
+    return work / dt, threads, f"{desc}, {dt:.1f} s", dt
 
 
 def cpu_tokens_per_s(w, unit_steps_per_s: float) -> float:
@@ -694,16 +703,18 @@ def main():
         # cores; rank 0 only.
         if rank != 0:
             return
-        rate, threads, desc, dt = oracle_sample_rate(w, n_units=min(256, w.batch * w.n_kv_heads),
-                                                     target_s=max(1.0, args.cpu_seconds / 2))
-        vals = []
-        for _ in range(max(1, min(args.steps, 3))):
-            r, threads, desc, dt = oracle_sample_rate(w, n_units=min(256, w.batch * w.n_kv_heads),
-                                                      target_s=max(1.0, args.cpu_seconds / 2))
-            vals.append(cpu_tokens_per_s(w, r))
-        v = statistics.median(vals)
+        # W untimed and K timed samples of the same size, sized so that the whole
+        # run takes about two and a half minutes of host time
+        per_step = min(max(1.0, args.cpu_seconds / 2), max(0.2, 150.0 / (args.steps + args.warmup)))
+        sample, work, threads, desc = oracle_sampler(w, n_units=min(256, w.batch * w.n_kv_heads),
+                                                     target_s=per_step)
+        for _ in range(args.warmup):
+            sample()
+        dts = [sample() for _ in range(args.steps)]
+        v = cpu_tokens_per_s(w, work * args.steps / sum(dts))
+        desc = f"{desc}, per bench step; {args.steps} timed steps after {args.warmup} untimed, {sum(dts):.1f} s"
         print(json.dumps({"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 1,
-                          "steps": len(vals), "warmup": 1, "ms_per_step": 1000.0 * w.batch / v,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.batch / v,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic", "config": cfg,
                           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
