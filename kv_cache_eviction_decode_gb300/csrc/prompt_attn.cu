@@ -1075,12 +1075,14 @@ __device__ void snap_union_tail(const SnapSelectParams &p, const uint32_t *keep,
 
 // The same selection with a head's pooled votes in registers: warp w owns the
 // prefix positions [32 R w, 32 R (w + 1)), its lane l the positions
-// 32 R w + 32 r + l (r < R). The pooling loads every vote once and takes the
-// neighbours from the lanes and registers around it (shuffles), with three
-// halo values on each side of the warp's span. The cut threshold is a binary
-// search on the bit pattern (the E-th smallest), each step counting with
-// per-thread compares, a warp reduction and one barrier (per-warp counts
-// double-buffered by step parity). For n_pre <= 512 R.
+// 32 R w + 32 r + l (r < R). The pooling loads every vote once, with three
+// halo values on each side of the warp's span, and builds the 7-wide max by
+// doubling: m1(s) = max x[s, s+1], m2(s) = max m1(s), m1(s+2) = max x[s, s+3],
+// then max m2(s-3), m2(s) = max x[s-3, s+3]; each shifted read takes the value
+// from the lanes and registers around it (two shuffles). The cut threshold is
+// a binary search on the bit pattern (the E-th smallest), each step counting
+// with per-thread compares, a warp reduction, one barrier and a reduction of
+// the warps' counts (double-buffered by step parity). For n_pre <= 512 R.
 template <int R>
 __global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const SnapSelectParams p)
 {
@@ -1105,7 +1107,8 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const Sn
     constexpr uint32_t kNone = 0xFFFFFFFFu;  // past the prefix: above every finite pattern, never counted
     for (int g = 0; g < p.G && take > 0; ++g) {
         const float *vg = p.votes + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * P;
-        // raw votes (0 outside the prefix: neutral for the max of non-negative values)
+        // raw votes (0 outside the prefix: neutral for the max of non-negative
+        // values); x holds them, then m1, then m2
         float x[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -1117,24 +1120,47 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const Sn
         const int jl = span0 - 3 + lane, jr = span0 + 32 * R + lane;
         const float hl = (lane < 3 && jl >= 0 && jl < n_pre) ? __ldg(vg + jl) : 0.f;
         const float hr = (lane < 3 && jr < n_pre) ? __ldg(vg + jr) : 0.f;
+        // span offsets s = 32 r + lane; the halos hold s = -3..-1 (left, lanes
+        // 0-2) and s = 32 R.. (right, lanes 0-2 for x, 0-1 for m1)
+        // m1 at s = -3..-1: x(s) and x(s + 1), the latter hl of the next lane or x(0)
+        float m1l;
+        {
+            const float t = __shfl_sync(0xffffffffu, hl, (lane + 1) & 31);
+            const float u = __shfl_sync(0xffffffffu, x[0], 0);
+            m1l = fmaxf(hl, lane < 2 ? t : u);
+        }
+        const float m1r = fmaxf(hr, __shfl_sync(0xffffffffu, hr, (lane + 1) & 31));
+        // m1 in place, ascending r (x[r + 1] is still raw when m1[r] reads it)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float same = __shfl_sync(0xffffffffu, x[r], (lane + 1) & 31);
+            const float next = __shfl_sync(0xffffffffu, r + 1 < R ? x[r + 1 < R ? r + 1 : r] : hr, 0);
+            x[r] = fmaxf(x[r], lane < 31 ? same : next);
+        }
+        // m2 at s = -3..-1: m1(s) and m1(s + 2), the latter m1l two lanes up or m1(lane - 1)
+        float m2l;
+        {
+            const float t = __shfl_sync(0xffffffffu, m1l, (lane + 2) & 31);
+            const float u = __shfl_sync(0xffffffffu, x[0], (lane - 1) & 31);
+            m2l = fmaxf(m1l, lane == 0 ? t : u);
+        }
+        // m2 in place, ascending r
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float same = __shfl_sync(0xffffffffu, x[r], (lane + 2) & 31);
+            const float next = __shfl_sync(0xffffffffu, r + 1 < R ? x[r + 1 < R ? r + 1 : r] : m1r, (lane - 30) & 31);
+            x[r] = fmaxf(x[r], lane < 30 ? same : next);
+        }
+        // the pooled vote max(m2(s - 3), m2(s)) as a bit pattern
         uint32_t v[R];
         uint32_t lo = kNone, hi = 0;
         bool bad = false;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            float mx = x[r];
-#pragma unroll
-            for (int k = 1; k <= 3; ++k) {
-                // position + k: lane + k of this step, or lane + k - 32 of the next (or the right halo)
-                const float up_same = __shfl_sync(0xffffffffu, x[r], (lane + k) & 31);
-                const float up_next = __shfl_sync(0xffffffffu, r + 1 < R ? x[r + 1 < R ? r + 1 : r] : hr, (lane + k) & 31);
-                mx = fmaxf(mx, lane + k < 32 ? up_same : up_next);
-                // position - k: lane - k of this step, or lane - k + 32 of the previous (or the left halo)
-                const float dn_same = __shfl_sync(0xffffffffu, x[r], (lane - k) & 31);
-                const float dn_prev = r > 0 ? __shfl_sync(0xffffffffu, x[r > 0 ? r - 1 : 0], (lane - k) & 31)
-                                            : __shfl_sync(0xffffffffu, hl, lane - k + 3 >= 0 ? lane - k + 3 : 0);
-                mx = fmaxf(mx, lane - k >= 0 ? dn_same : dn_prev);
-            }
+            const float same = __shfl_sync(0xffffffffu, x[r], (lane - 3) & 31);
+            const float prev = r > 0 ? __shfl_sync(0xffffffffu, x[r > 0 ? r - 1 : 0], (lane + 29) & 31)
+                                     : __shfl_sync(0xffffffffu, m2l, lane & 31);
+            const float mx = fmaxf(x[r], lane >= 3 ? same : prev);
             const int j = base + 32 * r;
             v[r] = kNone;
             if (j < n_pre) {
@@ -1161,11 +1187,9 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const Sn
             wlim[1][warp] = hi;
         }
         __syncthreads();
-        uint32_t a = kNone, bb = 0;
-        for (int w = 0; w < kSelWarps; ++w) {
-            a = min(a, wlim[0][w]);
-            bb = max(bb, wlim[1][w]);
-        }
+        static_assert(kSelWarps <= 32, "one warp reduces the per-warp values");
+        uint32_t a = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? wlim[0][lane] : kNone);
+        uint32_t bb = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? wlim[1][lane] : 0u);
         // smallest T in [a, bb] with #{v <= T} >= E
         for (int it = 0; a < bb; ++it) {
             const uint32_t mid = a + (bb - a) / 2;
@@ -1178,9 +1202,7 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const Sn
             const int c = __reduce_add_sync(0xffffffffu, c0 + c1);
             if (lane == 0) wcnt[it & 1][warp] = c;
             __syncthreads();
-            int tot = 0;
-#pragma unroll
-            for (int w = 0; w < kSelWarps; ++w) tot += wcnt[it & 1][w];
+            const int tot = __reduce_add_sync(0xffffffffu, lane < kSelWarps ? wcnt[it & 1][lane] : 0);
             if (tot >= E) bb = mid;
             else a = mid + 1;
         }

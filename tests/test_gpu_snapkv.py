@@ -103,9 +103,11 @@ def _cache(device, B, Hq, Hkv, d, n_sink, n_heavy, n_recent):
 @pytest.mark.parametrize("G,d,P,w,k", [(1, 64, 90, 8, 10), (4, 128, 300, 32, 20), (8, 128, 700, 32, 12),
                                        (2, 64, 257, 16, 100), (4, 64, 140, 20, 0), (4, 128, 500, 64, 30),
                                        (8, 64, 333, 96, 10), (2, 64, 400, 32, 40), (1, 128, 333, 32, 50),
-                                       # half of a long prefix kept: the sampled bracket holds more values than
-                                       # the selection keeps on chip, so the full search runs
-                                       (1, 64, 32800, 32, 16000)])
+                                       # prefixes past 2048 and 8192 positions: 16 and 64 pooled votes per
+                                       # thread (pooling across the warps' spans, a wide cut with ties)
+                                       (2, 64, 5000, 32, 300), (1, 64, 32800, 32, 16000),
+                                       # past 32768: the selection with the pooled votes in shared memory
+                                       (1, 64, 33000, 32, 100)])
 def test_snapkv_prefill_small(cuda_device, G, d, P, w, k):
     gen = torch.Generator().manual_seed(7000 + G * P + k)
     B, Hkv = 2, 2
