@@ -749,6 +749,7 @@ __global__ void __launch_bounds__(kPThreads, 1) snap_votes_kernel(const __grid_c
 // ------------------------------------------------------------------ cut
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelCand = 2 * kSelThreads;  // patterns the in-register search gathers once its interval is narrow
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane)
 {
@@ -1091,6 +1092,8 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const Sn
     __shared__ int total;
     __shared__ int wcnt[2][kSelWarps];
     __shared__ uint32_t wlim[2][kSelWarps];
+    __shared__ uint32_t cand[kSelCand];  // the patterns inside the search interval, once few enough
+    __shared__ int ncand_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const BlockOps ops{red, &total, lane, warp};
     const size_t unit = blockIdx.x;
@@ -1186,25 +1189,56 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_reg_kernel(const Sn
             wlim[0][warp] = lo;
             wlim[1][warp] = hi;
         }
+        if (tid == 0) ncand_s = 0;  // the previous head read it before its tie scan's barriers
         __syncthreads();
         static_assert(kSelWarps <= 32, "one warp reduces the per-warp values");
         uint32_t a = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? wlim[0][lane] : kNone);
         uint32_t bb = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? wlim[1][lane] : 0u);
-        // smallest T in [a, bb] with #{v <= T} >= E
+        // smallest T in [a, bb] with #{v <= T} >= E. lt_a = #{v < a} and
+        // le_bb = #{v <= bb} are exact (block-uniform); once [a, bb] holds at most
+        // kSelCand patterns they are gathered into shared memory, and every later
+        // step (its mid inside that interval) counts them plus the lt_a of the
+        // gather, lt_g.
+        int lt_a = 0, le_bb = n_pre, ncand = -1, lt_g = 0;  // ncand < 0: counting in registers
         for (int it = 0; a < bb; ++it) {
             const uint32_t mid = a + (bb - a) / 2;
-            int c0 = 0, c1 = 0;
+            int cnt;
+            if (ncand < 0) {
+                int c0 = 0, c1 = 0;
 #pragma unroll
-            for (int r = 0; r < R; r += 2) {
-                c0 += v[r] <= mid;
-                if (r + 1 < R) c1 += v[r + 1] <= mid;
+                for (int r = 0; r < R; r += 2) {
+                    c0 += v[r] <= mid;
+                    if (r + 1 < R) c1 += v[r + 1] <= mid;
+                }
+                cnt = c0 + c1;
+            } else {
+                cnt = 0;
+                for (int i = tid; i < ncand; i += kSelThreads) cnt += cand[i] <= mid;
             }
-            const int c = __reduce_add_sync(0xffffffffu, c0 + c1);
+            const int c = __reduce_add_sync(0xffffffffu, cnt);
             if (lane == 0) wcnt[it & 1][warp] = c;
             __syncthreads();
-            const int tot = __reduce_add_sync(0xffffffffu, lane < kSelWarps ? wcnt[it & 1][lane] : 0);
-            if (tot >= E) bb = mid;
-            else a = mid + 1;
+            const int tot = (ncand < 0 ? 0 : lt_g) +
+                            __reduce_add_sync(0xffffffffu, lane < kSelWarps ? wcnt[it & 1][lane] : 0);
+            if (tot >= E) {
+                bb = mid;
+                le_bb = tot;
+            } else {
+                a = mid + 1;
+                lt_a = tot;
+            }
+            if (ncand < 0 && a < bb && le_bb - lt_a <= kSelCand) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (v[r] >= a && v[r] <= bb) {
+                        const int k = atomicAdd(&ncand_s, 1);
+                        if (k < kSelCand) cand[k] = v[r];
+                    }
+                }
+                __syncthreads();
+                ncand = min(ncand_s, kSelCand);
+                lt_g = lt_a;
+            }
         }
         const uint32_t T = a;
         // ties at T: the first `need` in position order leave, the newer ones are taken
