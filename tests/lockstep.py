@@ -44,7 +44,7 @@ def torch_dtype(w: Workload):
 
 
 @dataclass
-class GpuRun:
+class DeviceRun:
     trace: dict = field(default_factory=dict)       # layer -> int32 [T, B, Hkv, 4]
     out: dict = field(default_factory=dict)         # layer -> {seq: float32 [T, Hq, D]}
     pos_snap: dict = field(default_factory=dict)    # layer -> {t: int32 [B, Hkv, C]}; t = -1 after prefill
@@ -63,7 +63,7 @@ def host_inputs(w, units, n_steps, prompt_len):
 
 def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, device, snap_steps=(),
             split: int | None = None, out_seqs=None, seed: int = 0, clusters: int | None = None,
-            interleave: bool = True, path: int | None = None) -> GpuRun:
+            interleave: bool = True, path: int | None = None) -> DeviceRun:
     """Runs n_steps decode steps of the given layers at the workload's shape.
 
     interleave=True issues the steps token by token over the layers, as a
@@ -81,7 +81,7 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
     gen = torch.Generator(device=device)
     gen.manual_seed(seed * 1000 + 17)
     st = cache.stats()
-    run = GpuRun(split=st["split"], tensor_cores=st["tensor_cores"])
+    run = DeviceRun(split=st["split"], tensor_cores=st["tensor_cores"])
     snap_steps = set(snap_steps)
     bufs = {}
     for layer in layers:
@@ -172,7 +172,7 @@ def score_error(w, got, ref):
     return float(np.max(diff))
 
 
-def replay_unit(w: Workload, unit, x, run: GpuRun, n_steps: int, out_steps=None,
+def replay_unit(w: Workload, unit, x, run: DeviceRun, n_steps: int, out_steps=None,
                 inputs_needed: bool = True) -> UnitReport:
     """Replays one unit on the oracle and checks it against the GPU run."""
     seq, layer, h = unit
@@ -259,7 +259,7 @@ def replay_all(w, units, inputs, run, n_steps, out_steps=None, threads=None):
         return [f.result() for f in futs]
 
 
-def check_selector(w: Workload, run: GpuRun, layer: int, prompt_len: int):
+def check_selector(w: Workload, run: DeviceRun, layer: int, prompt_len: int):
     """Bit-exact check of the H2O selector on the GPU's own fp32 values: at
     every snapshot step the evicted token's (score, position) key is below
     the key of every other candidate left in the cache."""
