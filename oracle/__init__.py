@@ -82,6 +82,11 @@ def lib():
             L.orc_prompt_tail_scores.restype = I
             L.orc_set_score_storage.argtypes = [P, ctypes.c_double, I]
             L.orc_set_score_storage.restype = I
+            L.orc_set_score_int8.argtypes = [P, I]
+            L.orc_set_score_int8.restype = I
+            L.orc_score_scale.argtypes = [P]
+            L.orc_score_scale.restype = ctypes.c_float
+            L.orc_score_codes.argtypes = [P, P]
             L.orc_set_hh_threshold.argtypes = [P, ctypes.c_double]
             L.orc_set_hh_threshold.restype = I
             L.orc_pools.argtypes = [P, P]
@@ -135,6 +140,8 @@ class Unit:
         forget, half = getattr(w, "score_forget", 0.0), getattr(w, "score_half", False)
         if forget or half:
             u.set_score_storage(forget, half)
+        if getattr(w, "score_int8", False):
+            u.set_score_int8(True)
         if w.policy == H2O_POOLS:
             u.set_hh_threshold(w.hh_threshold)
         return u
@@ -155,6 +162,22 @@ class Unit:
         rc = self._L.orc_set_score_storage(self.h, forget, 1 if half else 0)
         if rc:
             raise RuntimeError(f"oracle set_score_storage failed: {rc}")
+
+    def set_score_int8(self, on: bool = True) -> None:
+        """INT8 score storage: per unit, codes round(s * 255 / max) times max / 255."""
+        rc = self._L.orc_set_score_int8(self.h, 1 if on else 0)
+        if rc:
+            raise RuntimeError(f"oracle set_score_int8 failed: {rc}")
+
+    def score_scale(self) -> float:
+        """INT8 storage: the unit's scale (its largest score / 255, fp32)."""
+        return float(self._L.orc_score_scale(self.h))
+
+    def score_codes(self) -> np.ndarray:
+        """INT8 storage: the code of every slot (0 for empty slots)."""
+        a = np.empty(self.cap, dtype=np.uint8)
+        self._L.orc_score_codes(self.h, _ptr(a))
+        return a
 
     def set_hh_threshold(self, theta: float) -> None:
         """Two-pool H2O: promotion needs a score strictly above theta."""

@@ -92,6 +92,8 @@ typedef struct orc_unit {
     int last_block;      /* H2O_BLOCK: block released for the token of the last step, -1 if none */
     double forget;       /* score storage: s <- (1 - forget) s + a each step (0: exact accumulation) */
     int half;            /* score storage: every stored score rounded to IEEE binary16 */
+    int int8;            /* score storage: unsigned 8-bit codes times one scale per unit (absmax) */
+    float qscale;        /* INT8: the unit's scale, its largest score / 255 (0 before any step) */
     /* two-pool H2O */
     signed char *pool;   /* [cap] 0: recent pool, 1: heavy-hitter pool (slots with pos >= 0) */
     double hh_threshold; /* promotion needs a score strictly above this */
@@ -243,11 +245,61 @@ int orc_set_score_storage(orc_unit *u, double forget, int half)
 {
     if (u->policy != ORC_H2O && u->policy != ORC_H2O_BLOCK && u->policy != ORC_H2O_POOLS) return ORC_EINVAL;
     if (half && u->policy == ORC_H2O_BLOCK) return ORC_EINVAL;
+    if (half && u->int8) return ORC_EINVAL;
     if (!(forget >= 0.0 && forget < 1.0)) return ORC_EINVAL;
     if (u->prompt_len != 0 || u->t != 0 || u->have_new) return ORC_ESTATE;
     u->forget = forget;
     u->half = half != 0;
     return ORC_OK;
+}
+
+/* INT8 score storage (the same section names "INT8 quantisation" of the
+ * scores and gives no scale or zero point; the reading here is symmetric
+ * absmax quantisation per unit, zero point 0 as scores are >= 0): after each
+ * step's update, with M the largest score of the unit's retained tokens and
+ * the new token, every score becomes the code c = round(s * 255 / M) (nearest,
+ * ties to even; 0..255) and is stored as c * (M / 255). The rounding decides
+ * an integer, so it is taken in fp32 as the kernel takes it: s and M rounded
+ * to fp32, 255 / M and M / 255 fp32 divisions, the product and c * scale fp32
+ * multiplications. Plain H2O only; not with binary16; on an empty unit. */
+int orc_set_score_int8(orc_unit *u, int on)
+{
+    if (u->policy != ORC_H2O || (on && u->half)) return ORC_EINVAL;
+    if (u->prompt_len != 0 || u->t != 0 || u->have_new) return ORC_ESTATE;
+    u->int8 = on != 0;
+    return ORC_OK;
+}
+
+/* The code and the stored value of an fp32 score under inverse scale inv. */
+static float int8_code(float s, float inv)
+{
+    float c = rintf(s * inv);
+    if (c > 255.0f) c = 255.0f;
+    if (!(c >= 0.0f)) c = 0.0f;
+    return c;
+}
+
+/* Requantises every retained score and the new token's after an update. */
+static void quantise_int8(orc_unit *u)
+{
+    float M = (float)u->score_new;
+    for (int s = 0; s < u->cap; ++s)
+        if (u->pos[s] >= 0 && (float)u->score[s] > M) M = (float)u->score[s];
+    const float inv = M > 0.0f ? 255.0f / M : 0.0f;
+    const float scale = M / 255.0f;
+    for (int s = 0; s < u->cap; ++s)
+        if (u->pos[s] >= 0) u->score[s] = (double)(int8_code((float)u->score[s], inv) * scale);
+    u->score_new = (double)(int8_code((float)u->score_new, inv) * scale);
+    u->qscale = scale;
+}
+
+float orc_score_scale(const orc_unit *u) { return u->qscale; }
+
+/* The INT8 codes of the unit's slots (0 for empty slots and before any step). */
+void orc_score_codes(const orc_unit *u, uint8_t *dst)
+{
+    for (int s = 0; s < u->cap; ++s)
+        dst[s] = (u->pos[s] >= 0 && u->qscale > 0.0f) ? (uint8_t)rintf((float)u->score[s] / u->qscale) : 0;
 }
 
 void orc_free(orc_unit *u)
@@ -419,6 +471,7 @@ int orc_attend(orc_unit *u, const float *q, const float *k_new, const float *v_n
         }
         u->score_new = mass[cap] / (double)G;
         if (u->half) u->score_new = orc_round_half(u->score_new);
+        if (u->int8) quantise_int8(u);
     } else {
         u->score_new = 0.0;
     }

@@ -140,3 +140,173 @@ def test_storage_modes_checked():
     u.prefill(np.zeros((2, 4), np.float32), np.zeros((2, 4), np.float32))
     with pytest.raises(RuntimeError):
         u.set_score_storage(0.1, False)  # only on an empty unit
+
+
+# INT8 storage (section 6.2 names INT8 quantisation of the scores with no
+# scale or zero point; the reading is absmax per unit: codes round(s * 255 / M),
+# M the unit's largest score after the update, the new token's included,
+# stored as code * M / 255; the rounding in fp32).
+
+
+def _q8(x, M):
+    """numpy float32 absmax quantisation of fp64 values x with absmax M."""
+    M32 = np.float32(M)
+    inv, scale = np.float32(255.0) / M32, M32 / np.float32(255.0)
+    c = np.minimum(np.rint(np.float32(x) * inv), np.float32(255.0))
+    return (c * scale).astype(np.float64), c.astype(np.int64), float(scale)
+
+
+@pytest.mark.parametrize("forget", [0.0, 0.1])
+def test_int8_recursion_against_sdpa(forget):
+    """Never evicting: the stored scores follow s <- q((1 - forget) s + a), a
+    from torch's fp64 SDPA, q the numpy float32 absmax quantisation over the
+    unit (the new token included); codes, scale and values agree."""
+    rng = np.random.default_rng(81 + int(forget * 10))
+    P, T, G, d = 6, 30, 2, 8
+    n = P + T
+    u = Unit(H2O, 2, n, 3, n + 5, 0, 0, G, d)
+    u.set_score_storage(forget, False)
+    u.set_score_int8(True)
+    K = rng.standard_normal((n, d)).astype(np.float32)
+    Q = rng.standard_normal((T, G, d)).astype(np.float32)
+    u.prefill(K[:P], K[:P])
+    ref = np.zeros(n)
+    moved = 0
+    for t in range(T):
+        u.step(Q[t], K[P + t], K[P + t])
+        w = _sdpa_weights(Q, K, t, P).mean(axis=0)
+        m = P + t + 1
+        upd = np.concatenate([(1.0 - forget) * ref[:m - 1] + w[:m - 1], w[m - 1:m]])
+        M = float(np.max(np.float32(upd)))
+        q, codes, scale = _q8(upd, M)
+        pos, sc = u.positions(), u.scores()
+        got = np.zeros(n)
+        got[pos[pos >= 0]] = sc[pos >= 0]
+        gc = np.zeros(n, np.int64)
+        gc[pos[pos >= 0]] = u.score_codes()[pos >= 0]
+        assert u.score_scale() == pytest.approx(scale, rel=1e-6)
+        assert gc[:m].max() == 255 and gc[:m].min() >= 0
+        # the stored values are code * scale in fp32, within half a step of the update
+        assert np.all(np.float32(got[:m]) == got[:m])
+        np.testing.assert_array_equal(np.float32(gc[:m]) * np.float32(u.score_scale()), np.float32(got[:m]))
+        assert np.all(np.abs(got[:m] - upd) <= 0.5 * scale * (1 + 1e-5) + 1e-12)
+        # codes equal numpy's except where fp64 vs fp32 attention sits on a rounding midpoint
+        diff = np.abs(gc[:m] - codes)
+        assert diff.max() <= 1
+        moved += int(diff.sum())
+        ref[:m] = got[:m]  # the recursion continues from the stored values
+    assert moved <= 2
+
+
+def test_int8_selection_equals_brute_force_on_stored_scores():
+    rng = np.random.default_rng(90)
+    n_sink, n_heavy, n_recent = 1, 3, 2
+    K_ = n_sink + n_heavy + n_recent
+    P, T, G, d = 10, 60, 2, 4
+    u = Unit(H2O, n_sink, n_heavy, n_recent, K_, 0, 0, G, d)
+    u.set_score_int8(True)
+    Kk = rng.standard_normal((P + T, d)).astype(np.float32)
+    # a sink that takes nearly all the weight: the prompt tokens held past the
+    # window keep code 0 with the tokens leaving it, so equal codes meet
+    Kk[0] = 10.0 * np.abs(Kk[0])
+    Q = np.abs(rng.standard_normal((T, G, d))).astype(np.float32)
+    u.prefill(Kk[:P], Kk[:P])
+    ties = 0
+    for t in range(T):
+        p = P + t
+        u.attend(Q[t], Kk[p], Kk[p])
+        pos, sc, codes = u.positions(), u.scores(), u.score_codes()
+        cand = {int(pos[s]): sc[s] for s in range(K_) if pos[s] >= 0}
+        cand[p] = u.new_score
+        assert max(codes.max(), round(u.new_score / u.score_scale())) == 255
+        slot = u.choose()
+        u.commit(slot)
+        if len(cand) <= K_:
+            continue
+        after = set(int(x) for x in u.positions() if x >= 0)
+        protected = {q for q in cand if q < n_sink or q > p - n_recent}
+        elig = sorted(set(cand) - protected, key=lambda q: (cand[q], q))
+        ties += len(elig) > 1 and cand[elig[0]] == cand[elig[1]]
+        best = None
+        for keep in itertools.combinations(sorted(cand), K_):
+            if not protected <= set(keep):
+                continue
+            f = math.fsum(cand[q] for q in keep)
+            gone = (set(cand) - set(keep)).pop()
+            key = (-f, cand[gone], gone)
+            if best is None or key < best[0]:
+                best = (key, set(keep))
+        assert after == best[1]
+    assert u.greedy_disagreements == 0
+    assert ties > 0  # 256 levels: equal codes happen, and the older token leaves
+
+
+def test_int8_identical_keys_closed_form():
+    """Identical keys, no eviction: every step spreads weight 1/n_t evenly, so
+    tokens present for equal numbers of steps hold bit-identical codes, the
+    prompt tokens (present longest) hold 255 and their stored value is the
+    exact score, and each code stays within the rounding drift of the ratio
+    of closed-form scores: half a code per step so far (the scale only grows,
+    so an earlier step's half code is at most half a code now)."""
+    P, T, G, d = 4, 25, 1, 4
+    n = P + T
+    u = Unit(H2O, 1, n, 1, n + 2, 0, 0, G, d)
+    u.set_score_int8(True)
+    k = np.ones((n, d), np.float32)
+    u.prefill(k[:P], k[:P])
+    q = np.ones((G, d), np.float32)
+    for t in range(T):
+        u.step(q, k[0], k[0])
+        pos, codes = u.positions(), u.score_codes()
+        by_pos = {int(pos[s]): int(codes[s]) for s in range(len(pos)) if pos[s] >= 0}
+        assert all(by_pos[j] == 255 for j in range(P))
+        # exact scores: a token first attended at step t0 holds sum_{t0 <= s <= t} 1/(P + s + 1)
+        exact = {j: sum(1.0 / (P + s + 1) for s in range(max(0, j - P), t + 1)) for j in by_pos}
+        top = exact[0]
+        assert u.score_scale() * 255 == pytest.approx(top, rel=1e-6)
+        for j, c in by_pos.items():
+            assert abs(c - 255 * exact[j] / top) <= 0.5 * (t + 1) + 1e-3, (t, j, c)
+        for j in range(P, P + t):  # monotone in age
+            assert by_pos[j] >= by_pos[j + 1]
+
+
+def test_int8_modes_checked():
+    with pytest.raises(RuntimeError):
+        Unit(SINK_WINDOW, 1, 0, 4, 5, 0, 0, 1, 4).set_score_int8(True)
+    with pytest.raises(RuntimeError):
+        Unit(H2O_BLOCK, 1, 8, 3, 12, 3, 0, 1, 4).set_score_int8(True)
+    u = Unit(H2O, 1, 2, 1, 4, 0, 0, 1, 4)
+    u.set_score_storage(0.0, True)
+    with pytest.raises(RuntimeError):
+        u.set_score_int8(True)  # not with binary16
+    u = Unit(H2O, 1, 2, 1, 4, 0, 0, 1, 4)
+    u.prefill(np.zeros((2, 4), np.float32), np.zeros((2, 4), np.float32))
+    with pytest.raises(RuntimeError):
+        u.set_score_int8(True)  # on an empty unit only
+
+
+def test_int8_new_token_sets_the_scale():
+    """Right after a prefill (scores 0) a new token whose key points along
+    the query takes the largest weight: it alone sets the scale (code 255),
+    and the prompt tokens' codes are their SDPA weights over its weight,
+    rounded in float32."""
+    rng = np.random.default_rng(12)
+    P, G, d = 6, 1, 8
+    u = Unit(H2O, 1, P, 2, P + 3, 0, 0, G, d)
+    u.set_score_int8(True)
+    K = rng.standard_normal((P + 1, d)).astype(np.float32)
+    Q = rng.standard_normal((1, G, d)).astype(np.float32)
+    K[P] = 2.0 * Q[0, 0]
+    u.prefill(K[:P], K[:P])
+    u.attend(Q[0], K[P], K[P])
+    w = _sdpa_weights(Q, K, 0, P).mean(axis=0)
+    assert np.argmax(w) == P
+    q, codes, scale = _q8(w, float(np.float32(w[P])))
+    assert u.score_scale() == pytest.approx(scale, rel=1e-6)
+    assert round(u.new_score / u.score_scale()) == 255
+    pos = u.positions()
+    got = u.score_codes()
+    for s in range(len(pos)):
+        if pos[s] >= 0:
+            assert abs(int(got[s]) - int(codes[pos[s]])) <= 0  # no midpoint at these values
+    assert int(codes[:P].max()) < 255
