@@ -131,6 +131,17 @@ typedef enum {
  *     returns fp32. score_forget also applies to H2O_POOLS.
  *   hh_threshold: H2O_POOLS only, the promotion threshold (any value but NaN;
  *     the pages leave it open; -INFINITY promotes every token).
+ *   score_int8: 1 stores the H2O scores as unsigned 8-bit codes with one fp32
+ *     scale per (sequence, KV head) unit (the same section names INT8
+ *     quantisation of the scores and gives no scale; the reading is absmax
+ *     per unit, zero point 0): after each step's update (score_forget applies)
+ *     every score becomes c = round(s * 255 / M), M the unit's largest score
+ *     (the new token's included), stored as c * M / 255; eviction compares
+ *     the stored values, ties to the older position. A quarter of the fp32
+ *     score traffic. H2O only, not with score_half, nor with
+ *     kvevict_prefill_scored / kvevict_prefill_snapkv; one CTA per unit
+ *     (kvevict_create and kvevict_set_split refuse a split above 1 with
+ *     INVALID_ARG). kvevict_scores returns c * scale as fp32.
  * Slot capacity per unit: C = budget (H2O, SINK_WINDOW, H2O_BLOCK) or
  * max_prompt + budget + r (RANDOM).
  */
@@ -144,6 +155,7 @@ typedef struct {
     float score_forget;
     int score_half;
     float hh_threshold;
+    int score_int8;
 } kvevict_config;
 
 typedef struct {
@@ -314,6 +326,11 @@ int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_devi
  * fp32 (empty slots hold stale values; read them with the positions).
  * INVALID_ARG for policies that keep no scores. Same dst rules as above. */
 int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device);
+
+/* INT8 score storage only (else INVALID_ARG): every unit's scale for `layer`,
+ * its largest score / 255 after the last step (0 before the first);
+ * dst [batch][n_kv_heads] fp32. Same dst rules as kvevict_slot_positions. */
+int kvevict_score_scales(kvevict_t h, int layer, float *dst, int dst_is_device);
 
 /* Pool of every slot of `layer` (H2O_POOLS only, else INVALID_ARG): 0 the
  * recent pool, 1 the heavy-hitter pool, meaningful where the slot holds a

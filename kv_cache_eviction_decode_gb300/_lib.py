@@ -24,7 +24,7 @@ class Config(ctypes.Structure):
                 ("seed", ctypes.c_uint64), ("batch", ctypes.c_int), ("n_layers", ctypes.c_int),
                 ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("max_prompt", ctypes.c_int), ("score_forget", ctypes.c_float),
-                ("score_half", ctypes.c_int), ("hh_threshold", ctypes.c_float)]
+                ("score_half", ctypes.c_int), ("hh_threshold", ctypes.c_float), ("score_int8", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):
@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             L.kvevict_slot_positions.argtypes = [P, I, P, I]
             L.kvevict_scores.argtypes = [P, I, P, I]
             L.kvevict_slot_pools.argtypes = [P, I, P, I]
+            L.kvevict_score_scales.argtypes = [P, I, P, I]
             L.kvevict_set_trace.argtypes = [P, I, P, I]
             L.kvevict_layer_state.argtypes = [P, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
             L.kvevict_set_split.argtypes = [P, I]
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
                       "kvevict_prefill_scored", "kvevict_prefill_scored_static",
                       "kvevict_prefill_snapkv_workspace_bytes", "kvevict_prefill_snapkv", "kvevict_decode_step",
                       "kvevict_decode_step_host", "kvevict_decode_step_host_async", "kvevict_sync", "kvevict_slot_positions", "kvevict_scores", "kvevict_slot_pools",
+                      "kvevict_score_scales",
                       "kvevict_set_trace",
                       "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",

@@ -25,11 +25,12 @@ class KVEvictCache:
     def __init__(self, *, policy: int, budget: int, batch: int, n_layers: int, n_q_heads: int, n_kv_heads: int,
                  head_dim: int, dtype: int, n_sink: int = 0, n_heavy: int = 0, n_recent: int = 0, r: int = 0,
                  seed: int = 0, max_prompt: int = 0, score_forget: float = 0.0, score_half: bool = False,
-                 hh_threshold: float = 0.0, device=None, stream: torch.cuda.Stream | None = None):
+                 hh_threshold: float = 0.0, score_int8: bool = False, device=None,
+                 stream: torch.cuda.Stream | None = None):
         self._L = lib()
         self.cfg = Config(policy, n_sink, n_heavy, n_recent, budget, r, seed, batch, n_layers, n_q_heads,
                           n_kv_heads, head_dim, dtype, max_prompt, score_forget, 1 if score_half else 0,
-                          hh_threshold)
+                          hh_threshold, 1 if score_int8 else 0)
         nbytes = ctypes.c_size_t(0)
         check(self._L.kvevict_state_bytes(ctypes.byref(self.cfg), ctypes.byref(nbytes)), "kvevict_state_bytes")
         self.device = torch.device(device if device is not None else "cuda")
@@ -49,7 +50,8 @@ class KVEvictCache:
                    r=w.r, seed=w.seed, batch=w.batch, n_layers=w.n_layers, n_q_heads=w.n_q_heads,
                    n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, dtype=w.dtype, max_prompt=w.max_prompt,
                    score_forget=getattr(w, "score_forget", 0.0), score_half=getattr(w, "score_half", False),
-                   hh_threshold=getattr(w, "hh_threshold", 0.0), device=device, stream=stream)
+                   hh_threshold=getattr(w, "hh_threshold", 0.0), score_int8=getattr(w, "score_int8", False),
+                   device=device, stream=stream)
 
     def close(self) -> None:
         if getattr(self, "h", None) and self.h.value:
@@ -197,6 +199,17 @@ class KVEvictCache:
         if on_dev:
             self._dev(out, shp, "out", torch.float32)
         check(self._L.kvevict_scores(self.h, layer, _ptr(out), 1 if on_dev else 0), "kvevict_scores")
+        return out
+
+    def score_scales(self, layer: int, out: torch.Tensor | None = None) -> torch.Tensor:
+        """INT8 score storage: every unit's scale (its largest score / 255)."""
+        shp = (self.B, self.Hkv)
+        if out is None:
+            out = torch.empty(shp, dtype=torch.float32, device=self.device)
+        on_dev = out.device.type == "cuda"
+        if on_dev:
+            self._dev(out, shp, "out", torch.float32)
+        check(self._L.kvevict_score_scales(self.h, layer, _ptr(out), 1 if on_dev else 0), "kvevict_score_scales")
         return out
 
     def pools(self, layer: int, out: torch.Tensor | None = None) -> torch.Tensor:

@@ -42,6 +42,7 @@ struct Layout {
     int C = 0, G = 0, elem = 0;
     int Cs = 0;               // per-unit stride of pos/score (rows start on 16 bytes)
     int score_elem = 4;       // bytes per stored score
+    size_t off_qscale = 0;    // INT8 scores: [L][B][Hkv] fp32 scale per unit
     int Ps = 0;               // per-unit stride of the pool flags (two-pool H2O; rows start on 16 bytes)
     size_t units = 0;         // B * Hkv
     size_t layer_slots = 0;   // units * C (K/V rows)
@@ -103,6 +104,8 @@ int validate(const kvevict_config *c)
         return KVEVICT_ERR_INVALID_ARG;
     if (c->score_forget != 0.f && !scored(c->policy)) return KVEVICT_ERR_INVALID_ARG;
     if (c->score_half && c->policy != KVEVICT_H2O && c->policy != KVEVICT_H2O_POOLS) return KVEVICT_ERR_INVALID_ARG;
+    if (c->score_int8 != 0 && (c->score_int8 != 1 || c->policy != KVEVICT_H2O || c->score_half))
+        return KVEVICT_ERR_INVALID_ARG;
     const long long C = c->policy == KVEVICT_RANDOM ? static_cast<long long>(c->max_prompt) + c->budget + c->r
                                                     : c->budget;
     if (C > (1 << 24)) return KVEVICT_ERR_INVALID_ARG;
@@ -116,9 +119,9 @@ Layout make_layout(const kvevict_config *c)
     L.elem = c->dtype == KVEVICT_F32 ? 4 : 2;
     L.C = c->policy == KVEVICT_RANDOM ? c->max_prompt + c->budget + c->r : c->budget;
     // pos/score rows start on 16 bytes for the bulk copies: 4-byte entries need
-    // a multiple of 4, binary16 scores a multiple of 8
-    L.Cs = c->score_half ? (L.C + 7) / 8 * 8 : (L.C + 3) / 4 * 4;
-    L.score_elem = c->score_half ? 2 : 4;
+    // a multiple of 4, binary16 scores a multiple of 8, 8-bit codes of 16
+    L.Cs = c->score_int8 ? (L.C + 15) / 16 * 16 : c->score_half ? (L.C + 7) / 8 * 8 : (L.C + 3) / 4 * 4;
+    L.score_elem = c->score_int8 ? 1 : c->score_half ? 2 : 4;
     L.Ps = c->policy == KVEVICT_H2O_POOLS ? (L.C + 15) / 16 * 16 : 0;
     L.units = static_cast<size_t>(c->batch) * c->n_kv_heads;
     L.layer_slots = L.units * L.C;
@@ -130,6 +133,7 @@ Layout make_layout(const kvevict_config *c)
     L.off_v = off; off = align_up(off + nl * L.kv_layer_bytes);
     L.off_pos = off; off = align_up(off + nl * L.layer_pslots * 4);
     L.off_score = off; if (scored(c->policy)) off = align_up(off + nl * L.layer_pslots * L.score_elem);
+    L.off_qscale = off; if (c->score_int8) off = align_up(off + nl * L.units * 4);
     L.off_pool = off; off = align_up(off + nl * L.units * L.Ps);
     L.off_free = off;
     if (c->policy == KVEVICT_RANDOM || c->policy == KVEVICT_H2O_BLOCK) off = align_up(off + nl * L.units * c->r * 4);
@@ -394,6 +398,8 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     P.score = scored(c.policy) ? layer_scores(h, layer) : nullptr;
     P.score_keep = 1.f - c.score_forget;
     P.score_half = c.score_half;
+    P.score_int8 = c.score_int8;
+    P.qscale = c.score_int8 ? at<float>(h, L.off_qscale) + static_cast<size_t>(layer) * L.units : nullptr;
     P.freelist = (c.policy == KVEVICT_RANDOM || c.policy == KVEVICT_H2O_BLOCK)
                      ? at<int32_t>(h, L.off_free) + layer * L.units * c.r
                      : nullptr;
@@ -644,12 +650,18 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
         }
     }
     h->split = auto_split(h);
+    if (cfg->score_int8 && h->split > 1) {  // INT8 scores need one CTA per unit
+        delete h;
+        return KVEVICT_ERR_INVALID_ARG;
+    }
     // Empty cache: K/V zero (every row a tile may touch is finite), every
     // position -1, every score 0, no error bits.
     cudaError_t e = cudaMemsetAsync(h->state + L.off_k, 0, L.off_pos - L.off_k, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_pos, 0xFF, cfg->n_layers * L.layer_pslots * 4, h->stream);
     if (e == cudaSuccess && scored(cfg->policy))
         e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_pslots * L.score_elem, h->stream);
+    if (e == cudaSuccess && cfg->score_int8)
+        e = cudaMemsetAsync(h->state + L.off_qscale, 0, cfg->n_layers * L.units * 4, h->stream);
     if (e == cudaSuccess && L.Ps > 0)
         e = cudaMemsetAsync(h->state + L.off_pool, 0, cfg->n_layers * L.units * L.Ps, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
@@ -683,6 +695,7 @@ int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_
     P.pos = at<int32_t>(h, L.off_pos) + layer * L.layer_pslots;
     P.score = scored(c.policy) ? layer_scores(h, layer) : nullptr;
     P.score_half = c.score_half;
+    P.score_int8 = c.score_int8;
     P.n_tok = n_tokens;
     P.p0 = ls.prompt_len;
     P.C = L.C;
@@ -801,7 +814,8 @@ int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K,
     const kvevict_config &c = h->cfg;
     const Layout &L = h->L;
     const int P = prompt_len;
-    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16 || c.score_half) return KVEVICT_ERR_INVALID_ARG;
+    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16 || c.score_half || c.score_int8)
+        return KVEVICT_ERR_INVALID_ARG;
     if (P < 1 || P > kPromptMaxLen) return KVEVICT_ERR_INVALID_ARG;
     if (!Q || !K || !V || !workspace || !aligned16(Q) || !aligned16(K) || !aligned16(V) ||
         (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
@@ -915,7 +929,8 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
     const kvevict_config &c = h->cfg;
     const Layout &L = h->L;
     const int P = prompt_len;
-    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16 || c.score_half) return KVEVICT_ERR_INVALID_ARG;
+    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16 || c.score_half || c.score_int8)
+        return KVEVICT_ERR_INVALID_ARG;
     if (P < 2 || P > kPromptMaxLen || window < 1 || window >= P || k_per_head < 0) return KVEVICT_ERR_INVALID_ARG;
     // the union of the G heads' top-k lists plus the window must fit the unit
     if (static_cast<long long>(L.G) * k_per_head + window > L.C) return KVEVICT_ERR_INVALID_ARG;
@@ -1141,6 +1156,21 @@ int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     const Layout &L = h->L;
     const void *src = layer_scores(h, layer);
+    if (L.score_elem == 1) {  // INT8 codes times each unit's scale, returned as fp32
+        const float *scl = at<float>(h, L.off_qscale) + static_cast<size_t>(layer) * L.units;
+        if (dst_is_device)
+            return cuda_status(launch_scores_int8_to_f32(dst, src, scl, L.C, L.Cs, L.units, h->stream));
+        std::vector<uint8_t> codes(static_cast<size_t>(L.units) * L.C);
+        std::vector<float> scales(L.units);
+        cudaError_t e = cudaMemcpy2DAsync(codes.data(), L.C, src, L.Cs, L.C, L.units, cudaMemcpyDeviceToHost,
+                                          h->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(scales.data(), scl, L.units * 4, cudaMemcpyDeviceToHost, h->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        if (e != cudaSuccess) return cuda_status(e);
+        for (size_t i = 0; i < codes.size(); ++i) dst[i] = static_cast<float>(codes[i]) * scales[i / L.C];
+        return KVEVICT_OK;
+    }
     if (L.score_elem == 2) {  // binary16 storage, returned as fp32
         if (dst_is_device) return cuda_status(launch_scores_to_f32(dst, src, L.C, L.Cs, L.units, h->stream));
         std::vector<__half> tmp(static_cast<size_t>(L.units) * L.C);
@@ -1153,6 +1183,19 @@ int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
     }
     cudaError_t e = cudaMemcpy2DAsync(dst, L.C * 4, src, L.Cs * 4, L.C * 4, L.units,
                                       dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
+    return cuda_status(e);
+}
+
+int kvevict_score_scales(kvevict_t h, int layer, float *dst, int dst_is_device)
+{
+    if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
+    if (!h->cfg.score_int8) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    const Layout &L = h->L;
+    const float *src = at<float>(h, L.off_qscale) + static_cast<size_t>(layer) * L.units;
+    cudaError_t e = cudaMemcpyAsync(dst, src, L.units * 4,
+                                    dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
     if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
     return cuda_status(e);
 }
@@ -1200,6 +1243,7 @@ int kvevict_set_split(kvevict_t h, int split)
         h->split = auto_split(h);
     } else {
         if (split < 1 || split > kMaxSplit || (split & (split - 1))) return KVEVICT_ERR_INVALID_ARG;
+        if (split > 1 && h->cfg.score_int8) return KVEVICT_ERR_INVALID_ARG;  // one CTA per unit
         if (decode_smem(h, split, holes_policy(h->cfg)) > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
         h->split = split;
     }

@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillParams P)
         P.pos[unit * P.cstride + slot] = p;
         if (P.pool) P.pool[unit * P.pstride + slot] = p < P.hh_below ? 1 : 0;
         if (P.score) {
-            if (P.score_half) static_cast<uint16_t *>(P.score)[unit * P.cstride + slot] = 0;  // +0 in binary16
+            if (P.score_int8) static_cast<uint8_t *>(P.score)[unit * P.cstride + slot] = 0;  // code 0
+            else if (P.score_half) static_cast<uint16_t *>(P.score)[unit * P.cstride + slot] = 0;  // +0 in binary16
             else static_cast<float *>(P.score)[unit * P.cstride + slot] = 0.f;
         }
     }
@@ -282,6 +283,26 @@ cudaError_t launch_scores_to_f32(float *dst, const void *src, int C, int cstride
     const size_t n = units * C;
     const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
     scores_to_f32_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const __half *>(src), C, cstride, n);
+    return cudaGetLastError();
+}
+
+__global__ void scores_int8_to_f32_kernel(float *dst, const uint8_t *src, const float *scale, int C, int cstride,
+                                          size_t n)
+{
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t u = i / C, j = i - u * C;
+        dst[i] = static_cast<float>(src[u * cstride + j]) * scale[u];
+    }
+}
+
+cudaError_t launch_scores_int8_to_f32(float *dst, const void *src, const float *scale, int C, int cstride,
+                                      size_t units, cudaStream_t st)
+{
+    const size_t n = units * C;
+    if (n == 0) return cudaSuccess;
+    const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
+    scores_int8_to_f32_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const uint8_t *>(src), scale, C, cstride, n);
     return cudaGetLastError();
 }
 

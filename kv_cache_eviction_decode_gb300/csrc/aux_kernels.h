@@ -14,8 +14,9 @@ struct PrefillParams {
     const void *K, *V;  // [B][Hkv][n_tok][D]
     void *kc, *vc;      // layer cache [B][Hkv][C][D]
     int32_t *pos;
-    void *score;        // fp32 or binary16 (score_half), or null
+    void *score;        // fp32, binary16 (score_half) or 8-bit codes (score_int8), or null
     int score_half;
+    int score_int8;
     int n_tok, p0, C, cstride, Hkv, head_dim, elem_bytes;
     int n_sink, ring_len;  // ring_len = C - n_sink for ring policies, 0 for Random
     int a0, a1, b0, b1;    // chunk rows to copy
@@ -58,6 +59,9 @@ struct BlockReleaseParams {
 void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st);
 // binary16 scores [units][cstride] -> fp32 [units][C]
 cudaError_t launch_scores_to_f32(float *dst, const void *src, int C, int cstride, size_t units, cudaStream_t st);
+// INT8 score storage read back as fp32: code * the unit's scale.
+cudaError_t launch_scores_int8_to_f32(float *dst, const void *src, const float *scale, int C, int cstride,
+                                      size_t units, cudaStream_t st);
 void launch_block_prefill(const BlockPrefillParams &p, int B, cudaStream_t st);
 cudaError_t launch_block_release(const BlockReleaseParams &p, int units, cudaStream_t st);
 size_t cut_smem_bytes(int n_pow2, int r);

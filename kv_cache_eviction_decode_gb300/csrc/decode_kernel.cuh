@@ -116,6 +116,8 @@ struct DecodeParams {
     float scale_log2;    // log2(e) / sqrt(D)
     float score_keep;    // each step s <- score_keep * s + a (1: the exact cumulative score)
     int score_half;      // scores stored as IEEE binary16 (cstride a multiple of 8)
+    int score_int8;      // scores stored as 8-bit codes, one scale per unit (cstride a multiple of 16; split 1)
+    float *qscale;       // score_int8: [B][Hkv] each unit's scale, its largest score / 255
     // two-pool H2O (kTwoPool)
     uint8_t *pool;       // [B][Hkv][pstride]: 0 recent pool, 1 heavy-hitter pool (slots holding a token)
     int pstride;         // per-unit stride of the pool flags (C rounded up to 16)
@@ -185,6 +187,7 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
         int32_t xslot2[2][kMaxSplit];
         float xanew[2];
         float anew;  // the new token's score (one CTA per unit)
+        float wqmax[kWarps];  // INT8 scores: every warp's largest updated score
         uint64_t wkey[kWarps];
         int32_t wslot[kWarps];
         int32_t wempty[kWarps];
@@ -414,6 +417,12 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = static_cast<int>(cluster_rank());
     const int S = P.split;
+    // INT8 scores need the unit's largest score before any code is written:
+    // one CTA per unit only (the host refuses a split); a cluster leaves at once
+    if (S > 1 && P.score_int8) {
+        if (tid == 0 && blockIdx.x == 0) atomicOr(P.err, KVEVICT_DEV_BAD_SLOT);
+        return;
+    }
     const size_t C = static_cast<size_t>(P.C);
     const size_t CS = static_cast<size_t>(P.cstride);
     const bool has_score = P.score != nullptr;
@@ -463,14 +472,18 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     auto issue_aux = [&](int i) {
         const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
         const uint32_t bytes = static_cast<uint32_t>(((W.n_mine * 4 + 15) / 16) * 16);
-        const uint32_t sbytes = P.score_half ? static_cast<uint32_t>(((W.n_mine * 2 + 15) / 16) * 16) : bytes;
+        const uint32_t sbytes = P.score_int8   ? static_cast<uint32_t>(((W.n_mine + 15) / 16) * 16)
+                                : P.score_half ? static_cast<uint32_t>(((W.n_mine * 2 + 15) / 16) * 16)
+                                               : bytes;
         const uint32_t pbytes = pools ? static_cast<uint32_t>(((W.n_mine + 15) / 16) * 16) : 0u;
         const uint32_t tx = (has_score ? bytes + sbytes : bytes) + pbytes;
         mbar_arrive_expect_tx(&M.auxbar, tx);
         bulk_g2s(aux, P.pos + unit * CS + W.s_lo, bytes, &M.auxbar);
         if (has_score)
             bulk_g2s(aux + auxb,
-                     static_cast<const uint8_t *>(P.score) + (unit * CS + W.s_lo) * (P.score_half ? 2 : 4), sbytes,
+                     static_cast<const uint8_t *>(P.score) +
+                         (unit * CS + W.s_lo) * (P.score_int8 ? 1 : (P.score_half ? 2 : 4)),
+                     sbytes,
                      &M.auxbar);
         if (pools)
             bulk_g2s(aux + 2 * auxb, P.pool + unit * static_cast<size_t>(P.pstride) + W.s_lo, pbytes, &M.auxbar);
@@ -593,9 +606,16 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         const int32_t *apos = reinterpret_cast<const int32_t *>(aux);
         const float *ascore = reinterpret_cast<const float *>(aux + auxb);
         const __half *ascore_h = reinterpret_cast<const __half *>(aux + auxb);
+        const uint8_t *ascore8 = aux + auxb;
         const uint8_t *apool = aux + 2 * auxb;
+        // INT8 scores: this unit's scale before this step (0 before its first step)
+        const float qscale_u = P.score_int8 ? P.qscale[unit] : 0.f;
         // this unit's stored score of local slot j, before this step
-        auto stored_score = [&](int j) { return P.score_half ? __half2float(ascore_h[j]) : ascore[j]; };
+        auto stored_score = [&](int j) {
+            return P.score_int8   ? static_cast<float>(ascore8[j]) * qscale_u
+                   : P.score_half ? __half2float(ascore_h[j])
+                                  : ascore[j];
+        };
 
         // This unit's q (prefetched during the previous unit); start the
         // next unit's loads.
@@ -929,6 +949,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         bool writer = false;       // this CTA writes it
         uint64_t win_key = ~0ull;  // H2O eviction: (score bits, position) of the evicted token
         float anew = 0.f;          // the new token's score (rank 0)
+        uint8_t anew_code = 0;     // INT8 scores: its code
         PoolDecision pd{-1, 0, -1, kEmptyKey};  // two-pool mode
         // a held token is a candidate: sinks and the recent window excepted (H2O),
         // or any held token, in the pool its flag names (two-pool)
@@ -941,9 +962,13 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         // (score, position) candidate (two-pool: one per pool) and the lowest empty
         // slot. GEN = false is the plain H2O eviction with fp32 scores (no binary16,
         // fill or pool branches in the loop); GEN = true handles every mode.
-        const bool general_scores = P.score_half || fill || pools;
+        // INT8 (one CTA per unit): this pass only updates, keeping the value in
+        // the slot's head-0 logit cell (read by this thread alone) and the
+        // largest retained one in qmax; the codes and candidates follow once
+        // the unit's largest score is known.
+        const bool general_scores = P.score_half || P.score_int8 || fill || pools;
         auto score_pass = [&](auto gen, const float(&fself)[G], uint64_t &best, int32_t &bslot, uint64_t &best2,
-                              int32_t &bslot2, int32_t &emin) {
+                              int32_t &bslot2, int32_t &emin, float &qmax) {
             constexpr bool GEN = decltype(gen)::value;
             for (int j = tid; j < W.n_mine; j += kThreads) {
                 float a = 0.f;
@@ -952,6 +977,12 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 const size_t si = unit * CS + W.s_lo + j;
                 float sc;
                 if constexpr (GEN) {
+                    if (P.score_int8) {
+                        sc = fmaf(P.score_keep, stored_score(j), a);
+                        zbuf[j] = sc;
+                        if (apos[j] >= 0) qmax = fmaxf(qmax, sc);
+                        continue;
+                    }
                     sc = score_store(P, si, fmaf(P.score_keep, stored_score(j), a));
                 } else {
                     sc = fmaf(P.score_keep, ascore[j], a);
@@ -1005,9 +1036,50 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 }
                 uint64_t best = ~0ull, best2 = ~0ull;
                 int32_t bslot = -1, bslot2 = -1, emin = INT_MAX;
-                if (general_scores) score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin);
-                else score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin);
-                if (tid == 0) {
+                float qmax = 0.f;
+                if (general_scores) score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin, qmax);
+                else score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin, qmax);
+                if (P.score_int8) {
+                    // the unit's largest score, the new token's included (every
+                    // thread forms that one as thread 0 does); then the codes
+                    // c = round(s * 255 / max) (0..255) and the stored values c * scale
+                    float a = 0.f;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], invl[g], a);
+                    a *= 1.0f / G;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+                    if (lane == 0) M.wqmax[warp] = qmax;
+                    __syncthreads();  // every warp's largest; every read of the old scale is done
+                    float mx = a;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, M.wqmax[w]);
+                    const float inv = mx > 0.f ? 255.f / mx : 0.f;
+                    const float scl = mx / 255.f;
+                    auto code = [&](float v) {
+                        const float c = fminf(rintf(v * inv), 255.f);
+                        return c >= 0.f ? c : 0.f;
+                    };
+                    for (int j = tid; j < W.n_mine; j += kThreads) {
+                        const float c = code(zbuf[j]);
+                        static_cast<uint8_t *>(P.score)[unit * CS + W.s_lo + j] = static_cast<uint8_t>(c);
+                        const int ps = apos[j];
+                        if (evict && ps >= P.n_sink && ps <= P.p - P.n_recent) {
+                            const uint64_t key =
+                                (static_cast<uint64_t>(__float_as_uint(c * scl)) << 32) | static_cast<uint32_t>(ps);
+                            if (key < best) {
+                                best = key;
+                                bslot = W.s_lo + j;
+                            }
+                        }
+                    }
+                    anew_code = static_cast<uint8_t>(code(a));
+                    anew = code(a) * scl;
+                    if (tid == 0) {
+                        M.anew = anew;
+                        P.qscale[unit] = scl;
+                    }
+                } else if (tid == 0) {
                     float a = 0.f;
 #pragma unroll
                     for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], invl[g], a);
@@ -1122,8 +1194,9 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
                 uint64_t best = ~0ull, best2 = ~0ull;
                 int32_t bslot = -1, bslot2 = -1, emin = INT_MAX;
-                if (general_scores) score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin);
-                else score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin);
+                float qmax = 0.f;  // (INT8 scores never reach a cluster)
+                if (general_scores) score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin, qmax);
+                else score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin, qmax);
                 if (rank == 0 && tid == 0) {
                     float a = 0.f;
 #pragma unroll
@@ -1238,10 +1311,12 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 float old_score = __uint_as_float(static_cast<uint32_t>(win_key >> 32));
                 if (!evict && P.trace != nullptr) {
                     old_pos = P.pos[unit * CS + dest];
-                    old_score = has_score ? score_load(P, unit * CS + dest) : 0.f;
+                    // (INT8: the codes were rewritten above; the slot is an empty one, score 0)
+                    old_score = has_score && !P.score_int8 ? score_load(P, unit * CS + dest) : 0.f;
                 }
                 P.pos[unit * CS + dest] = P.p;
-                if (has_score) score_store(P, unit * CS + dest, anew);
+                if (P.score_int8) static_cast<uint8_t *>(P.score)[unit * CS + dest] = anew_code;
+                else if (has_score) score_store(P, unit * CS + dest, anew);
                 if (pools) P.pool[unit * P.pstride + dest] = static_cast<uint8_t>(pd.new_pool);
                 if (P.trace != nullptr)
                     reinterpret_cast<int4 *>(P.trace)[unit] =

@@ -112,6 +112,11 @@ def test_create_rejects_bad_state_without_touching_the_gpu(L):
     dict(policy=1, n_heavy=0, n_recent=124, score_forget=0.1),    # StreamingLLM keeps no scores
     dict(policy=3, r=16, score_half=1),                           # binary16 scores: not block H2O
     dict(score_half=2),
+    dict(score_int8=2),
+    dict(score_int8=1, score_half=1),                             # INT8 or binary16, not both
+    dict(policy=3, r=16, score_int8=1),                           # INT8 scores: plain H2O only
+    dict(policy=4, n_sink=0, n_heavy=64, n_recent=64, score_int8=1),
+    dict(policy=1, n_heavy=0, n_recent=124, score_int8=1),
 ])
 def test_invalid_next_row_configs_rejected_on_host(L, bad):
     rc, _ = _bytes(L, _cfg(**bad))
@@ -133,3 +138,8 @@ def test_state_bytes_of_the_next_rows(L):
     # the moving average changes no layout
     rc, n_ema = _bytes(L, _cfg(score_forget=0.25))
     assert rc == 0 and n_ema == n_h2o
+    # INT8 scores: a byte per slot instead of four, plus a 4-byte scale per unit
+    rc, n_int8 = _bytes(L, _cfg(score_int8=1))
+    assert rc == 0 and n_h2o - n_int8 >= 3 * 16 * 128 * 3 - 3 * 16 * 4 - 3 * 256
+    rc, n_int8_ema = _bytes(L, _cfg(score_int8=1, score_forget=0.1))
+    assert rc == 0 and n_int8_ema == n_int8

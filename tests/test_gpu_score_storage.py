@@ -1,13 +1,16 @@
 """GPU parity of H2O's score-storage variants ("Attention Sinks 与 KV Cache 淘汰策略"
-section 6.2): the moving average s <- (1 - forget) s + a and binary16 storage,
-through the C ABI, in lockstep with the CPU oracle.
+section 6.2): the moving average s <- (1 - forget) s + a, binary16 storage and
+INT8 storage (per-unit absmax codes), through the C ABI, in lockstep with the
+CPU oracle.
 
 Outputs and scores as for H2O (2e-2 relative for bf16, 1e-4 max-abs for fp32;
 binary16 scores also within one binary16 step). Victims identical, except at
 near-ties, which the oracle adopts: within 1e-5 relative for fp32 scores,
 within one binary16 step for binary16 scores (the GPU sums in fp32, the
-oracle in fp64, before the same rounding). The selector is also checked
-bit-exact on the GPU's own stored values.
+oracle in fp64, before the same rounding). INT8: stored values within two
+codes of the oracle's, victims within two and a half codes (a midpoint may
+round one code apart, and the difference persists). The selector is also
+checked bit-exact on the GPU's own stored values.
 """
 import numpy as np
 import pytest
@@ -74,7 +77,69 @@ def test_score_storage_rejected_where_unsupported(cuda_device):
     c.close()
 
 
-@pytest.mark.parametrize("w", [configs.H2O_MHA_FP16, configs.H2O_MHA_EMA], ids=["binary16", "moving_average"])
+@pytest.mark.parametrize("dtype,forget", [(BF16, 0.0), (BF16, 0.05), (F32, 0.0)])
+def test_int8_scores_lockstep(cuda_device, dtype, forget):
+    w = _small(dtype, forget, False).with_(score_int8=True)
+    T = 160
+    units = [(s, 0, h) for s in range(w.batch) for h in range(w.n_kv_heads)]
+    inputs = ls.host_inputs(w, units, T, w.prompt_len)
+    snaps = list(range(0, T, 16))
+    run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=snaps)
+    assert run.err == 0
+    reps = ls.replay_all(w, units, inputs, run, T)
+    print(f"int8 forget {forget}: out {max(r.max_out_err for r in reps):.2e}, "
+          f"score {max(r.max_score_err for r in reps):.2e}, near ties {sum(r.near_ties for r in reps)}")
+    assert ls.check_selector(w, run, 0, w.prompt_len) == sum(t >= w.budget - w.prompt_len for t in snaps)
+
+
+def test_int8_codes_and_scales(cuda_device):
+    """After decode steps every stored score is an integer code 0..255 times
+    its unit's scale, and every unit holds code 255 (its largest score) until
+    that token leaves; the scales are the unit maxima over 255."""
+    import torch
+    B, Hq, Hkv, d, P, T = 2, 8, 4, 64, 20, 30
+    c = KVEvictCache(policy=H2O, budget=64, n_sink=2, n_heavy=40, n_recent=22, batch=B, n_layers=1, n_q_heads=Hq,
+                     n_kv_heads=Hkv, head_dim=d, dtype=BF16, score_int8=True, device=cuda_device)
+    g = torch.Generator(device=cuda_device).manual_seed(4)
+    K = torch.randn((B, Hkv, P, d), generator=g, device=cuda_device).to(torch.bfloat16)
+    c.prefill(0, K, K)
+    assert torch.all(c.score_scales(0) == 0)
+    for _ in range(T):
+        q = torch.randn((B, Hq, d), generator=g, device=cuda_device).to(torch.bfloat16)
+        k = torch.randn((B, Hkv, d), generator=g, device=cuda_device).to(torch.bfloat16)
+        c.decode_step(0, q, k, k)
+    assert c.check() == 0
+    sc, scl, pos = c.scores(0).cpu(), c.score_scales(0).cpu(), c.slot_positions(0).cpu()
+    assert torch.all(scl > 0)
+    codes = sc / scl[..., None]
+    assert torch.all(torch.abs(codes - torch.round(codes)) < 1e-3)
+    held = codes.masked_fill(pos < 0, 0)
+    assert torch.all(torch.round(codes).min() >= 0) and torch.all(torch.round(codes).max() <= 255)
+    assert torch.all(torch.round(held).amax(dim=2) == 255)
+    c.close()
+
+
+def test_int8_scores_rejected_where_unsupported(cuda_device):
+    import torch
+    base = dict(batch=1, n_layers=1, n_q_heads=2, n_kv_heads=2, head_dim=64, dtype=BF16, device=cuda_device)
+    with pytest.raises(KVEvictError):  # INT8 scores: plain H2O only
+        KVEvictCache(policy=H2O_BLOCK, budget=64, n_sink=2, n_heavy=40, n_recent=22, r=8, score_int8=True, **base)
+    with pytest.raises(KVEvictError):  # not with binary16
+        KVEvictCache(policy=H2O, budget=64, n_sink=2, n_heavy=40, n_recent=22, score_half=True, score_int8=True,
+                     **base)
+    c = KVEvictCache(policy=H2O, budget=64, n_sink=2, n_heavy=40, n_recent=22, score_int8=True, **base)
+    with pytest.raises(KVEvictError):  # one CTA per unit
+        c.set_split(2)
+    c.set_split(1)
+    Q = torch.zeros((1, 2, 100, 64), dtype=torch.bfloat16, device=cuda_device)
+    K = torch.zeros((1, 2, 100, 64), dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(KVEvictError):  # the scored prefill writes fp32 scores
+        c.prefill_scored(0, Q, K, K)
+    c.close()
+
+
+@pytest.mark.parametrize("w", [configs.H2O_MHA_FP16, configs.H2O_MHA_EMA, configs.H2O_MHA_INT8],
+                         ids=["binary16", "moving_average", "int8"])
 def test_score_storage_full_shape(cuda_device, w):
     """H2O 4 + 510 + 510 on the MHA shape with binary16 scores, and with the
     moving average (forget 0.01): B=16, 32x32 heads, d=128, prompt 2048, 200

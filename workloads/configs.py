@@ -48,6 +48,7 @@ class Workload:
     max_prompt: int = 0
     score_forget: float = 0.0  # H2O score storage: s <- (1 - score_forget) s + a
     score_half: bool = False   # H2O score storage: binary16
+    score_int8: bool = False   # H2O score storage: 8-bit codes, one absmax scale per unit
     hh_threshold: float = 0.0  # two-pool H2O: promotion needs a score above this
 
     @property
@@ -128,6 +129,8 @@ H2O_BLOCK256 = H2O_MHA.with_(name="h2o_block256_bf16_b16_l32_h32_d128_k1024", po
 # traffic), and with a moving average (forget 0.01 per step) in place of the sum.
 H2O_MHA_FP16 = H2O_MHA.with_(name="h2o_fp16scores_bf16_b16_l32_h32_d128_k1024", score_half=True)
 H2O_MHA_EMA = H2O_MHA.with_(name="h2o_ema0.01_bf16_b16_l32_h32_d128_k1024", score_forget=0.01)
+# ... and as 8-bit codes with one absmax scale per (sequence, KV head): a quarter of the score traffic.
+H2O_MHA_INT8 = H2O_MHA.with_(name="h2o_int8scores_bf16_b16_l32_h32_d128_k1024", score_int8=True)
 
 # Two-pool H2O on the MHA shape: a recent pool of 512 and a heavy-hitter pool of
 # 512 (no sinks); a token leaving the recent pool is promoted if its score is
@@ -136,7 +139,7 @@ H2O_POOLS_MHA = H2O_MHA.with_(name="h2o_pools_bf16_b16_l32_h32_d128_r512_hh512",
                               n_heavy=512, n_recent=512, hh_threshold=2.0**-10)
 
 ALL = {w.name: w for w in (H2O_TINY, SINK_WINDOW, H2O_MHA, H2O_GQA, RANDOM_REASONING, H2O_REASONING, H2O_BLOCK16,
-                           H2O_BLOCK256, H2O_MHA_FP16, H2O_MHA_EMA, H2O_POOLS_MHA)}
+                           H2O_BLOCK256, H2O_MHA_FP16, H2O_MHA_EMA, H2O_MHA_INT8, H2O_POOLS_MHA)}
 
 # Short names used on command lines.
 ALIASES = {
@@ -150,6 +153,7 @@ ALIASES = {
     "h2o_block256": H2O_BLOCK256.name,
     "h2o_fp16scores": H2O_MHA_FP16.name,
     "h2o_ema": H2O_MHA_EMA.name,
+    "h2o_int8scores": H2O_MHA_INT8.name,
     "h2o_pools": H2O_POOLS_MHA.name,
 }
 

@@ -34,7 +34,10 @@ def unit_step_bytes(w: Workload, n_retained: int, n_slots: int | None = None, cu
     d, e, G = w.head_dim, w.elem_bytes, w.group
     b = (n_retained + 1) * 2 * d * e + 2 * d * e + 2 * G * d * e
     if w.policy in (POLICY_H2O, POLICY_H2O_BLOCK, POLICY_H2O_POOLS):
-        b += (4 if w.score_half else 8) * n_retained + (6 if w.score_half else 8)
+        if w.score_int8:  # codes read and written, the new token's code, the unit's scale read and written
+            b += 2 * n_retained + 9
+        else:
+            b += (4 if w.score_half else 8) * n_retained + (6 if w.score_half else 8)
     if w.policy == POLICY_H2O_POOLS:
         b += n_retained + 2
     if w.policy == POLICY_RANDOM:
