@@ -378,11 +378,13 @@ def measured_bf16_peak():
         return 1900.0, "fallback"
 
 
-def oracle_prefill_rate(w, P: int, target_s: float):
-    """Oracle units (one sequence's KV head) scored per second, timed as the
-    oracle stands, one unit per thread on every host core. A unit whose full
-    prompt would not finish within the budget is timed on a shorter prompt and
-    scaled by the FLOP ratio (said in the sample text)."""
+def oracle_prefill_sampler(w, P: int, target_s: float):
+    """One sample = one oracle unit (one sequence's KV head) scored per host
+    core, in parallel, timed as the oracle stands. A unit whose full prompt
+    would take more than about target_s is sampled on a shorter prompt and
+    scaled by the FLOP ratio (said in the description). Returns (sample,
+    units per sample, threads, description, scale): sample() runs one sample
+    and returns its seconds."""
     import concurrent.futures as cf
     import oracle
     threads = oracle.online_cores()
@@ -391,27 +393,64 @@ def oracle_prefill_rate(w, P: int, target_s: float):
     # per-unit cost model from the oracle's own loop: G * P^2 / 2 rows-by-keys products of d
     Pt = P
     est = G * P * P / 2 * d / 4e8  # about 0.4 G multiply-adds per second per core
-    if est > target_s / 2:
-        Pt = max(256, int(P * (target_s / 2 / est) ** 0.5))
+    if est > target_s:
+        Pt = max(256, int(P * (target_s / est) ** 0.5))
+    inputs = [(rng.standard_normal((G, Pt, d)).astype(np.float32), rng.standard_normal((Pt, d)).astype(np.float32),
+               rng.standard_normal((Pt, d)).astype(np.float32)) for _ in range(threads)]
+
     def unit(i):
-        q = rng.standard_normal((G, Pt, d)).astype(np.float32)
-        k = rng.standard_normal((Pt, d)).astype(np.float32)
-        v = rng.standard_normal((Pt, d)).astype(np.float32)
         u = oracle.Unit(oracle.H2O, w.n_sink, w.n_heavy, w.n_recent, w.budget, 0, 0, G, d)
-        u.prefill_scored(q, k, v)
-    t0 = time.perf_counter()
-    done = 0
-    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        while time.perf_counter() - t0 < target_s or done == 0:
-            list(ex.map(unit, range(threads)))
-            done += threads
-    dt = time.perf_counter() - t0
-    rate = done / dt
+        u.prefill_scored(*inputs[i])
+
+    ex = cf.ThreadPoolExecutor(max_workers=threads)
+
+    def sample():
+        t0 = time.perf_counter()
+        list(ex.map(unit, range(threads)))
+        return time.perf_counter() - t0
+
     scale = (Pt * (Pt + 1)) / (P * (P + 1))
-    desc = f"{done} units (one sequence x KV head) of prompt {Pt}, {dt:.1f} s"
+    desc = f"{threads} units (one sequence x KV head) of prompt {Pt} per round"
     if Pt != P:
         desc += f"; scaled to prompt {P} by the FLOP ratio {scale:.4g}"
-    return rate * scale, threads, desc
+    return sample, threads, threads, desc, scale
+
+
+def oracle_prefill_rate(w, P: int, target_s: float):
+    """Oracle units scored per second over about target_s (see oracle_prefill_sampler)."""
+    sample, n, threads, desc, scale = oracle_prefill_sampler(w, P, target_s / 2)
+    dt, done = 0.0, 0
+    while dt < target_s or done == 0:
+        dt += sample()
+        done += n
+    return done / dt * scale, threads, f"{done // n} rounds of {desc}, {dt:.1f} s"
+
+
+def run_reference_samples(args, one_round, n):
+    """The reference arm's W untimed and K timed bench steps. A step repeats
+    one_round (n units, returning its seconds) until it has run for
+    reference_step_seconds; returns (units per second over the timed steps,
+    their summed seconds)."""
+    target = reference_step_seconds(args)
+
+    def step():
+        dt, units = 0.0, 0
+        while dt < target or units == 0:
+            dt += one_round()
+            units += n
+        return dt, units
+
+    for _ in range(args.warmup):
+        step()
+    timed = [step() for _ in range(args.steps)]
+    secs = sum(t for t, _ in timed)
+    return sum(u for _, u in timed) / secs, secs
+
+
+def reference_step_seconds(args) -> float:
+    """Seconds per reference bench step: half of --cpu-seconds (at least 1 s),
+    capped so that the whole run takes about 150 s."""
+    return min(max(1.0, args.cpu_seconds / 2), max(0.2, 150.0 / (args.steps + args.warmup)))
 
 
 def prefill_phase(args, w, rank, world, local):
@@ -427,10 +466,14 @@ def prefill_phase(args, w, rank, world, local):
     if args.impl == "reference":
         if rank != 0:
             return
-        rate, threads, desc = oracle_prefill_rate(w, P, max(2.0, args.cpu_seconds))
-        v = rate * P / w.n_kv_heads
+        sample, n, threads, desc, scale = oracle_prefill_sampler(w, P, reference_step_seconds(args))
+        rate, tsum = run_reference_samples(args, sample, n)
+        v = rate * scale * P / w.n_kv_heads
+        desc = (f"{desc}; rounds of them repeated for {reference_step_seconds(args):.1f} s per bench step, "
+                f"{args.steps} timed steps after {args.warmup} untimed, {tsum:.1f} s")
         print(json.dumps({"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 1,
-                          "steps": 1, "warmup": 0, "ms_per_step": 1000.0 * tokens / v, "higher_is_better": True,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * tokens / v,
+                          "higher_is_better": True,
                           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                           "config": cfg,
                           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -543,21 +586,27 @@ def snapkv_phase(args, w, rank, world, local):
         threads = oracle.online_cores()
         G, d = w.group, w.head_dim
         rng = np.random.default_rng(w.seed)
+        inputs = [(rng.standard_normal((G, win, d)).astype(np.float32), rng.standard_normal((P, d)).astype(np.float32))
+                  for _ in range(threads)]
+
         def unit(i):
-            q = rng.standard_normal((G, win, d)).astype(np.float32)
-            k = rng.standard_normal((P, d)).astype(np.float32)
+            q, k = inputs[i]
             u = oracle.Unit(oracle.H2O, w.n_sink, w.n_heavy, w.n_recent, w.budget, 0, 0, G, d)
             u.prefill_snapkv(q, k, k, topk)
-        t0, done = time.perf_counter(), 0
+
         with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-            while time.perf_counter() - t0 < max(2.0, args.cpu_seconds) or done == 0:
+            def sample():  # one unit per host core, in parallel
+                t0 = time.perf_counter()
                 list(ex.map(unit, range(threads)))
-                done += threads
-        dt = time.perf_counter() - t0
-        v = done / dt * P / w.n_kv_heads
-        desc = f"{done} units (one sequence x KV head) of prompt {P}, {dt:.1f} s"
+                return time.perf_counter() - t0
+            rate, tsum = run_reference_samples(args, sample, threads)
+        v = rate * P / w.n_kv_heads
+        desc = (f"{threads} units (one sequence x KV head) of prompt {P} per round, rounds repeated for "
+                f"{reference_step_seconds(args):.1f} s per bench step; {args.steps} timed steps after "
+                f"{args.warmup} untimed, {tsum:.1f} s")
         print(json.dumps({"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 1,
-                          "steps": 1, "warmup": 0, "ms_per_step": 1000.0 * tokens / v, "higher_is_better": True,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * tokens / v,
+                          "higher_is_better": True,
                           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                           "config": cfg,
                           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",

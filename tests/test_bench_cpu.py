@@ -1,12 +1,15 @@
 """The benchmark's reference arm (the CPU oracle timed as it stands) keeps the
 JSON-line contract: exactly W untimed and K timed steps, reported as given;
 one line from rank 0 under a two-rank launch, the other rank exiting 0
-without work. Runs on CPU on the smallest workload."""
+without work. Runs on CPU on the smallest workload, and for the prefill
+phases on the MHA shape."""
 import json
 import os
 import socket
 import subprocess
 import sys
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 ARGS = ["bench.py", "--impl", "reference", "--workload", "h2o_tiny", "--steps", "3", "--warmup", "3",
@@ -49,3 +52,18 @@ def test_reference_arm_two_ranks_prints_once():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check(lines[0])
+
+
+@pytest.mark.parametrize("phase", ["prefill", "snapkv"])
+def test_reference_arm_prefill_phases(phase):
+    args = ["bench.py", "--impl", "reference", "--phase", phase, "--workload", "h2o_mha", "--steps", "3",
+            "--warmup", "3", "--cpu-seconds", "1"]
+    r = subprocess.run([sys.executable] + args, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["impl"] == "reference" and line["steps"] == 3 and line["warmup"] == 3
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert "3 timed steps after 3 untimed" in line["cpu_baseline"]["sample"]
+    assert line["config"]["prompt_len"] == 2048
