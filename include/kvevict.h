@@ -327,6 +327,15 @@ int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_devi
  * INVALID_ARG for policies that keep no scores. Same dst rules as above. */
 int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device);
 
+/* Failure detection, exercised without a fault: queues on the handle's stream
+ * one kernel in which a thread waits, through the same bounded wait as the
+ * decode pipeline, on a barrier that nothing completes. After the wait limit
+ * (2 s of device time) the kernel records KVEVICT_DEV_WAIT_TIMEOUT in the
+ * handle's error word and ends; kvevict_check then reports the bit and clears
+ * it, and the handle and the CUDA context stay usable. Returns OK or CUDA
+ * (launch failure). */
+int kvevict_probe_wait_timeout(kvevict_t h);
+
 /* INT8 score storage only (else INVALID_ARG): every unit's scale for `layer`,
  * its largest score / 255 after the last step (0 before the first);
  * dst [batch][n_kv_heads] fp32. Same dst rules as kvevict_slot_positions. */

@@ -201,6 +201,11 @@ class KVEvictCache:
         check(self._L.kvevict_scores(self.h, layer, _ptr(out), 1 if on_dev else 0), "kvevict_scores")
         return out
 
+    def probe_wait_timeout(self) -> None:
+        """Queues the failure-detection probe: a bounded wait that runs out and
+        sets DEV_WAIT_TIMEOUT in the error word (read by check())."""
+        check(self._L.kvevict_probe_wait_timeout(self.h), "kvevict_probe_wait_timeout")
+
     def score_scales(self, layer: int, out: torch.Tensor | None = None) -> torch.Tensor:
         """INT8 score storage: every unit's scale (its largest score / 255)."""
         shp = (self.B, self.Hkv)

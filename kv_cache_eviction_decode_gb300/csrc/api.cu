@@ -1187,6 +1187,12 @@ int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
     return cuda_status(e);
 }
 
+int kvevict_probe_wait_timeout(kvevict_t h)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    return cuda_status(launch_wait_timeout_probe(at<uint32_t>(h, h->L.off_err), h->stream));
+}
+
 int kvevict_score_scales(kvevict_t h, int layer, float *dst, int dst_is_device)
 {
     if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;

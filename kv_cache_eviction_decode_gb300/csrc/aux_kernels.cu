@@ -306,6 +306,25 @@ cudaError_t launch_scores_int8_to_f32(float *dst, const void *src, const float *
     return cudaGetLastError();
 }
 
+// Failure detection, exercised without a fault: one thread waits through the
+// pipelines' bounded wait on an mbarrier that nothing arrives at. The wait
+// gives up after its limit; the kernel records KVEVICT_DEV_WAIT_TIMEOUT and
+// ends normally, so the context stays usable.
+__global__ void wait_timeout_probe_kernel(uint32_t *err)
+{
+    __shared__ alignas(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    if (!mbar_wait(&bar, 0)) atomicOr(err, KVEVICT_DEV_WAIT_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout_probe(uint32_t *err, cudaStream_t st)
+{
+    wait_timeout_probe_kernel<<<1, 32, 0, st>>>(err);
+    return cudaGetLastError();
+}
+
 void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st)
 {
     if (rows <= 0) return;

@@ -59,6 +59,9 @@ struct BlockReleaseParams {
 void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st);
 // binary16 scores [units][cstride] -> fp32 [units][C]
 cudaError_t launch_scores_to_f32(float *dst, const void *src, int C, int cstride, size_t units, cudaStream_t st);
+// One thread's bounded wait on an mbarrier nothing completes: records
+// KVEVICT_DEV_WAIT_TIMEOUT in err after the wait limit.
+cudaError_t launch_wait_timeout_probe(uint32_t *err, cudaStream_t st);
 // INT8 score storage read back as fp32: code * the unit's scale.
 cudaError_t launch_scores_int8_to_f32(float *dst, const void *src, const float *scale, int C, int cstride,
                                       size_t units, cudaStream_t st);

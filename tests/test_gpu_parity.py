@@ -286,6 +286,32 @@ def test_nonfinite_query_sets_error_bit_and_continues(cuda_device):
     assert cache.layer_state(0)[1] == 3
 
 
+def test_wait_timeout_is_reported_and_the_handle_keeps_working(cuda_device):
+    """A bounded wait on a barrier nothing completes (the decode pipeline's own
+    wait) gives up after its limit: the device error word reports
+    DEV_WAIT_TIMEOUT, nothing faults, and decode steps go on with a clean word."""
+    from kv_cache_eviction_decode_gb300 import DEV_WAIT_TIMEOUT
+    import time
+    w = _small(configs.POLICY_H2O, configs.DTYPE_F32, G=1, d=64, B=1, L=1, n_sink=1, n_heavy=4, n_recent=3,
+               budget=8, prompt_len=8, decode_steps=3)
+    cache = KVEvictCache.from_workload(w, device=cuda_device)
+    K, V = synth.device_prompt(w, 0, cuda_device, 8)
+    cache.prefill(0, K, V)
+    q = torch.randn((1, 4, 64), device=cuda_device)
+    k = torch.randn((1, 4, 64), device=cuda_device)
+    cache.decode_step(0, q, k, k)
+    assert cache.check() == 0
+    t0 = time.perf_counter()
+    cache.probe_wait_timeout()
+    assert cache.check() == DEV_WAIT_TIMEOUT
+    assert time.perf_counter() - t0 >= 1.5  # the wait ran to its limit
+    assert cache.check() == 0  # read and cleared
+    out = cache.decode_step(0, q, k, k)
+    assert cache.check() == 0 and torch.isfinite(out).all()
+    assert cache.layer_state(0)[1] == 2
+    cache.close()
+
+
 def test_state_errors_on_device_handle(cuda_device):
     from kv_cache_eviction_decode_gb300 import KVEvictError
     w = _small(configs.POLICY_RANDOM, configs.DTYPE_F32, G=1, d=64, B=1, L=2, budget=8, r=2, max_prompt=10)
