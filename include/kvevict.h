@@ -327,6 +327,25 @@ int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_devi
  * INVALID_ARG for policies that keep no scores. Same dst rules as above. */
 int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device);
 
+/* Checkpoint and resume. A handle's state is the device buffer the caller
+ * gave kvevict_create (caller-owned: the caller copies it) plus host-side
+ * counters (per layer: prompt length, decode steps, tokens held, the Random,
+ * fill, pool and block bookkeeping; the cumulative stats), which these calls
+ * serialise as 64-bit fields with the configuration. Save: call
+ * kvevict_checkpoint_save, then copy the state buffer once the handle's
+ * stream has passed every queued call; the record describes the state after
+ * the calls issued so far. Resume: kvevict_create with the same configuration
+ * on a buffer of state_bytes, copy the saved bytes into it, then
+ * kvevict_checkpoint_restore (it waits for the handle's queued calls first).
+ * Eviction decisions (and the counter-based Random keys) then continue
+ * exactly as in the run that was saved. kvevict_checkpoint_bytes gives the
+ * record size; save returns CAPACITY if `bytes` is smaller; restore returns
+ * INVALID_ARG if the record is not one of this format and configuration. A
+ * trace set on the restoring handle is dropped. */
+int kvevict_checkpoint_bytes(kvevict_t h, size_t *bytes);
+int kvevict_checkpoint_save(kvevict_t h, void *dst, size_t bytes);
+int kvevict_checkpoint_restore(kvevict_t h, const void *src, size_t bytes);
+
 /* Failure detection, exercised without a fault: queues on the handle's stream
  * one kernel in which a thread waits, through the same bounded wait as the
  * decode pipeline, on a barrier that nothing completes. After the wait limit

@@ -201,6 +201,32 @@ class KVEvictCache:
         check(self._L.kvevict_scores(self.h, layer, _ptr(out), 1 if on_dev else 0), "kvevict_scores")
         return out
 
+    def checkpoint(self) -> dict:
+        """The handle's host record and a device copy of its state buffer,
+        taken once every queued call has run."""
+        n = ctypes.c_size_t(0)
+        check(self._L.kvevict_checkpoint_bytes(self.h, ctypes.byref(n)), "kvevict_checkpoint_bytes")
+        rec = (ctypes.c_uint8 * n.value)()
+        check(self._L.kvevict_checkpoint_save(self.h, rec, n.value), "kvevict_checkpoint_save")
+        self.stream.synchronize()
+        with torch.cuda.stream(self.stream):
+            state = self.state.clone()
+        self.stream.synchronize()
+        return {"record": bytes(rec), "state": state}
+
+    def restore(self, ckpt: dict) -> None:
+        """Resumes from checkpoint(): the saved state bytes into this handle's
+        buffer, then its host record (same configuration required)."""
+        if ckpt["state"].numel() != self.state.numel():
+            raise ValueError("checkpoint state size differs from this handle's")
+        self.stream.synchronize()
+        with torch.cuda.stream(self.stream):
+            self.state.copy_(ckpt["state"])
+        self.stream.synchronize()
+        rec = ckpt["record"]
+        buf = (ctypes.c_uint8 * len(rec)).from_buffer_copy(rec)
+        check(self._L.kvevict_checkpoint_restore(self.h, buf, len(rec)), "kvevict_checkpoint_restore")
+
     def probe_wait_timeout(self) -> None:
         """Queues the failure-detection probe: a bounded wait that runs out and
         sets DEV_WAIT_TIMEOUT in the error word (read by check())."""

@@ -9,6 +9,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
@@ -24,6 +26,19 @@
 #include "prompt_attn.h"
 
 using namespace kvevict;
+
+namespace {
+
+// An NVTX range around a public call (visible in Nsight timelines; a no-op
+// without a tool attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
+}  // namespace
 
 namespace {
 
@@ -622,6 +637,7 @@ int kvevict_state_bytes(const kvevict_config *cfg, size_t *bytes)
 
 int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_t state_bytes, void *cuda_stream)
 {
+    NvtxRange nvtx("kvevict_create");
     if (!out) return KVEVICT_ERR_INVALID_ARG;
     *out = nullptr;
     int rc = validate(cfg);
@@ -677,6 +693,7 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
 
 int kvevict_prefill(kvevict_t h, int layer, const void *K, const void *V, int n_tokens)
 {
+    NvtxRange nvtx("kvevict_prefill");
     if (!h || layer < 0 || layer >= h->cfg.n_layers) return h ? KVEVICT_ERR_STATE : KVEVICT_ERR_INVALID_ARG;
     if (n_tokens < 0 || (n_tokens > 0 && (!K || !V || !aligned16(K) || !aligned16(V)))) return KVEVICT_ERR_INVALID_ARG;
     LayerState &ls = h->layers[layer];
@@ -809,6 +826,7 @@ int kvevict_prefill_scored_workspace_bytes(kvevict_t h, int prompt_len, size_t *
 int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K, const void *V, int prompt_len,
                            void *workspace, size_t workspace_bytes)
 {
+    NvtxRange nvtx("kvevict_prefill_scored");
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     const kvevict_config &c = h->cfg;
@@ -924,6 +942,7 @@ int kvevict_prefill_snapkv_workspace_bytes(kvevict_t h, int prompt_len, int wind
 int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void *K, const void *V, int prompt_len,
                            int window, int k_per_head, void *workspace, size_t workspace_bytes)
 {
+    NvtxRange nvtx("kvevict_prefill_snapkv");
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     const kvevict_config &c = h->cfg;
@@ -1041,6 +1060,7 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
 
 int kvevict_decode_step(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new, void *out)
 {
+    NvtxRange nvtx("kvevict_decode_step");
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
@@ -1067,6 +1087,7 @@ int kvevict_sync(kvevict_t h)
 int kvevict_decode_step_host_async(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new,
                                    void *out)
 {
+    NvtxRange nvtx("kvevict_decode_step_host_async");
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
@@ -1115,6 +1136,7 @@ int kvevict_decode_step_host_async(kvevict_t h, int layer, const void *q, const 
 
 int kvevict_decode_step_host(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new, void *out)
 {
+    NvtxRange nvtx("kvevict_decode_step_host");
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
     if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
@@ -1185,6 +1207,96 @@ int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device)
                                       dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
     if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
     return cuda_status(e);
+}
+
+namespace {
+
+constexpr int64_t kCkptMagic = 0x31504b4356454b56ll;  // "VKEVCKP1" little-endian
+constexpr int64_t kCkptVersion = 1;
+
+int64_t f32_bits(float f)
+{
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return static_cast<int64_t>(u);
+}
+
+// The handle's host-side state as 64-bit fields: magic, version, the config,
+// the counters of every layer, the cumulative stats.
+std::vector<int64_t> checkpoint_record(const kvevict_handle *h)
+{
+    const kvevict_config &c = h->cfg;
+    std::vector<int64_t> r = {kCkptMagic, kCkptVersion, c.policy, c.n_sink, c.n_heavy, c.n_recent, c.budget, c.r,
+                              static_cast<int64_t>(c.seed), c.batch, c.n_layers, c.n_q_heads, c.n_kv_heads,
+                              c.head_dim, c.dtype, c.max_prompt, f32_bits(c.score_forget), c.score_half,
+                              f32_bits(c.hh_threshold), c.score_int8};
+    for (const LayerState &ls : h->layers) {
+        const int64_t f[] = {ls.prompt_len, ls.t,         ls.count,    ls.n_gen,    ls.cut_done ? 1 : 0,
+                             ls.fl_idx,     ls.fill_left, ls.n_rec,    ls.blk_left, ls.blk_next,
+                             ls.blk_uniform ? 1 : 0};
+        r.insert(r.end(), std::begin(f), std::end(f));
+    }
+    const int64_t s[] = {h->stats.decode_steps, h->stats.prefill_tokens, h->stats.evictions, h->stats.cuts};
+    r.insert(r.end(), std::begin(s), std::end(s));
+    return r;
+}
+
+constexpr size_t kCkptHead = 20;   // magic, version, 18 config fields
+constexpr size_t kCkptLayer = 11;  // fields per layer
+
+}  // namespace
+
+int kvevict_checkpoint_bytes(kvevict_t h, size_t *bytes)
+{
+    if (!h || !bytes) return KVEVICT_ERR_INVALID_ARG;
+    *bytes = checkpoint_record(h).size() * sizeof(int64_t);
+    return KVEVICT_OK;
+}
+
+int kvevict_checkpoint_save(kvevict_t h, void *dst, size_t bytes)
+{
+    NvtxRange nvtx("kvevict_checkpoint_save");
+    if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
+    const std::vector<int64_t> r = checkpoint_record(h);
+    if (bytes < r.size() * sizeof(int64_t)) return KVEVICT_ERR_CAPACITY;
+    std::memcpy(dst, r.data(), r.size() * sizeof(int64_t));
+    return KVEVICT_OK;
+}
+
+int kvevict_checkpoint_restore(kvevict_t h, const void *src, size_t bytes)
+{
+    NvtxRange nvtx("kvevict_checkpoint_restore");
+    if (!h || !src) return KVEVICT_ERR_INVALID_ARG;
+    const std::vector<int64_t> mine = checkpoint_record(h);
+    if (bytes != mine.size() * sizeof(int64_t)) return KVEVICT_ERR_INVALID_ARG;
+    std::vector<int64_t> r(mine.size());
+    std::memcpy(r.data(), src, bytes);
+    // same format and the same configuration, field by field
+    if (!std::equal(r.begin(), r.begin() + kCkptHead, mine.begin())) return KVEVICT_ERR_INVALID_ARG;
+    const int rc = kvevict_sync(h);  // no call of this handle in flight while its counters change
+    if (rc) return rc;
+    const int64_t *f = r.data() + kCkptHead;
+    for (LayerState &ls : h->layers) {
+        ls = LayerState{};  // (a trace set on this handle is dropped)
+        ls.prompt_len = static_cast<int>(f[0]);
+        ls.t = static_cast<int>(f[1]);
+        ls.count = static_cast<int>(f[2]);
+        ls.n_gen = static_cast<int>(f[3]);
+        ls.cut_done = f[4] != 0;
+        ls.fl_idx = static_cast<int>(f[5]);
+        ls.fill_left = static_cast<int>(f[6]);
+        ls.n_rec = static_cast<int>(f[7]);
+        ls.blk_left = static_cast<int>(f[8]);
+        ls.blk_next = static_cast<int>(f[9]);
+        ls.blk_uniform = f[10] != 0;
+        f += kCkptLayer;
+    }
+    h->stats.decode_steps = f[0];
+    h->stats.prefill_tokens = f[1];
+    h->stats.evictions = f[2];
+    h->stats.cuts = f[3];
+    h->last_layer = -1;  // the state buffer was just written by the caller: no early prefetch
+    return KVEVICT_OK;
 }
 
 int kvevict_probe_wait_timeout(kvevict_t h)
@@ -1301,6 +1413,7 @@ int kvevict_get_stats(kvevict_t h, kvevict_stats *out)
 
 int kvevict_check(kvevict_t h, uint32_t *device_error)
 {
+    NvtxRange nvtx("kvevict_check");
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     cudaError_t e = cudaStreamSynchronize(h->stream);
     if (e != cudaSuccess) return cuda_status(e);

@@ -85,6 +85,12 @@ def test_null_handle_and_strerror(L):
     assert L.kvevict_prefill(None, 0, None, None, 0) == -1
     assert L.kvevict_check(None, None) == -1
     assert L.kvevict_state_bytes(None, None) == -1
+    n = ctypes.c_size_t(0)
+    assert L.kvevict_checkpoint_bytes(None, ctypes.byref(n)) == -1
+    assert L.kvevict_checkpoint_save(None, None, 0) == -1
+    assert L.kvevict_checkpoint_restore(None, None, 0) == -1
+    assert L.kvevict_probe_wait_timeout(None) == -1
+    assert L.kvevict_score_scales(None, 0, None, 0) == -1
     assert L.kvevict_strerror(0) == b"ok"
     assert L.kvevict_strerror(-2) == b"capacity exceeded"
     L.kvevict_destroy(None)
