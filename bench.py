@@ -384,7 +384,7 @@ def oracle_prefill_sampler(w, P: int, target_s: float):
     would take more than about target_s is sampled on a shorter prompt and
     scaled by the FLOP ratio (said in the description). Returns (sample,
     units per sample, threads, description, scale): sample() runs one sample
-    and returns its seconds."""
+    and returns its seconds; call sample.close() when done."""
     import concurrent.futures as cf
     import oracle
     threads = oracle.online_cores()
@@ -409,6 +409,7 @@ def oracle_prefill_sampler(w, P: int, target_s: float):
         list(ex.map(unit, range(threads)))
         return time.perf_counter() - t0
 
+    sample.close = ex.shutdown
     scale = (Pt * (Pt + 1)) / (P * (P + 1))
     desc = f"{threads} units (one sequence x KV head) of prompt {Pt} per round"
     if Pt != P:
@@ -423,6 +424,7 @@ def oracle_prefill_rate(w, P: int, target_s: float):
     while dt < target_s or done == 0:
         dt += sample()
         done += n
+    sample.close()
     return done / dt * scale, threads, f"{done // n} rounds of {desc}, {dt:.1f} s"
 
 
@@ -468,6 +470,7 @@ def prefill_phase(args, w, rank, world, local):
             return
         sample, n, threads, desc, scale = oracle_prefill_sampler(w, P, reference_step_seconds(args))
         rate, tsum = run_reference_samples(args, sample, n)
+        sample.close()
         v = rate * scale * P / w.n_kv_heads
         desc = (f"{desc}; rounds of them repeated for {reference_step_seconds(args):.1f} s per bench step, "
                 f"{args.steps} timed steps after {args.warmup} untimed, {tsum:.1f} s")
