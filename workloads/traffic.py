@@ -8,6 +8,8 @@ These count what the method itself has to move through HBM per unit (one
   * the G queries read and the G outputs written:          2 * G * d * e
   * H2O: the cumulative scores read and written (fp32), the new token's
     score and position written:                            8 * n_ret + 8
+    (binary16 scores: 4 * n_ret + 6; INT8 codes: 2 * n_ret + 9, the
+    unit's scale read and written)
   * two-pool H2O: as H2O, plus the pool flags read and the
     new token's and a promoted token's flags written:      n_ret + 2
   * Random: the slot-position table read to skip holes:   4 * n_slots
