@@ -85,7 +85,12 @@ def lib():
             L.orc_set_score_int8.argtypes = [P, I]
             L.orc_set_score_int8.restype = I
             L.orc_score_scale.argtypes = [P]
-            L.orc_score_scale.restype = ctypes.c_float
+            L.orc_score_scale.restype = ctypes.c_double
+            L.orc_int8_unrounded.argtypes = [P, P, P]
+            L.orc_adopt_int8_code.argtypes = [P, I, I]
+            L.orc_adopt_int8_code.restype = I
+            L.orc_set_scores.argtypes = [P, P, ctypes.c_double]
+            L.orc_set_scores.restype = I
             L.orc_score_codes.argtypes = [P, P]
             L.orc_set_hh_threshold.argtypes = [P, ctypes.c_double]
             L.orc_set_hh_threshold.restype = I
@@ -170,8 +175,33 @@ class Unit:
             raise RuntimeError(f"oracle set_score_int8 failed: {rc}")
 
     def score_scale(self) -> float:
-        """INT8 storage: the unit's scale (its largest score / 255, fp32)."""
+        """INT8 storage: the unit's scale (its largest score / 255)."""
         return float(self._L.orc_score_scale(self.h))
+
+    def int8_unrounded(self):
+        """INT8 storage: every slot's s * 255 / max before the last rounding
+        (0 for empty slots), and the pending new token's."""
+        a = np.empty(self.cap, dtype=np.float64)
+        x_new = ctypes.c_double(0.0)
+        self._L.orc_int8_unrounded(self.h, _ptr(a), ctypes.byref(x_new))
+        return a, x_new.value
+
+    def adopt_int8_code(self, slot: int, code: int) -> None:
+        """Test hook: the token in `slot` (slot == capacity: the pending new
+        token) takes `code`, one code from its own (a midpoint rounded apart)."""
+        rc = self._L.orc_adopt_int8_code(self.h, int(slot), int(code))
+        if rc:
+            raise RuntimeError(f"oracle adopt_int8_code failed: {rc}")
+
+    def set_scores(self, scores, new_score: float) -> None:
+        """Test hook: replaces the retained tokens' stored scores (per slot)
+        and the pending new token's; the next choose() decides on them."""
+        a = np.ascontiguousarray(scores, dtype=np.float64)
+        if a.shape != (self.cap,):
+            raise ValueError("oracle set_scores: one score per slot")
+        rc = self._L.orc_set_scores(self.h, _ptr(a), float(new_score))
+        if rc:
+            raise RuntimeError(f"oracle set_scores failed: {rc}")
 
     def score_codes(self) -> np.ndarray:
         """INT8 storage: the code of every slot (0 for empty slots)."""

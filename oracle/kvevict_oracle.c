@@ -93,7 +93,10 @@ typedef struct orc_unit {
     double forget;       /* score storage: s <- (1 - forget) s + a each step (0: exact accumulation) */
     int half;            /* score storage: every stored score rounded to IEEE binary16 */
     int int8;            /* score storage: unsigned 8-bit codes times one scale per unit (absmax) */
-    float qscale;        /* INT8: the unit's scale, its largest score / 255 (0 before any step) */
+    double qscale;       /* INT8: the unit's scale, its largest score / 255 (0 before any step) */
+    double qmax;         /* INT8: that largest score M */
+    double *qx;          /* INT8: [cap] each slot's s * 255 / M before rounding, at the last update */
+    double qx_new;       /* INT8: the same for the new token */
     /* two-pool H2O */
     signed char *pool;   /* [cap] 0: recent pool, 1: heavy-hitter pool (slots with pos >= 0) */
     double hh_threshold; /* promotion needs a score strictly above this */
@@ -208,8 +211,10 @@ orc_unit *orc_new(int policy, int n_sink, int n_heavy, int n_recent, int budget,
     u->k_new = (float *)calloc((size_t)d, sizeof(float));
     u->v_new = (float *)calloc((size_t)d, sizeof(float));
     u->pool = (signed char *)calloc((size_t)u->cap, 1);
-    if (!u->pos || !u->k || !u->v || !u->score || !u->k_new || !u->v_new || !u->pool) {
+    u->qx = (double *)calloc((size_t)u->cap, sizeof(double));
+    if (!u->pos || !u->k || !u->v || !u->score || !u->k_new || !u->v_new || !u->pool || !u->qx) {
         free(u->pos); free(u->k); free(u->v); free(u->score); free(u->k_new); free(u->v_new); free(u->pool);
+        free(u->qx);
         free(u);
         return NULL;
     }
@@ -257,11 +262,10 @@ int orc_set_score_storage(orc_unit *u, double forget, int half)
  * scores and gives no scale or zero point; the reading here is symmetric
  * absmax quantisation per unit, zero point 0 as scores are >= 0): after each
  * step's update, with M the largest score of the unit's retained tokens and
- * the new token, every score becomes the code c = round(s * 255 / M) (nearest,
- * ties to even; 0..255) and is stored as c * (M / 255). The rounding decides
- * an integer, so it is taken in fp32 as the kernel takes it: s and M rounded
- * to fp32, 255 / M and M / 255 fp32 divisions, the product and c * scale fp32
- * multiplications. Plain H2O only; not with binary16; on an empty unit. */
+ * the new token, every score s becomes the code c = round(s * 255 / M)
+ * (nearest, ties to even; 0..255) and is stored as c * M / 255. Written from
+ * that definition, in fp64 like the rest of the oracle. Plain H2O only; not
+ * with binary16; on an empty unit. */
 int orc_set_score_int8(orc_unit *u, int on)
 {
     if (u->policy != ORC_H2O || (on && u->half)) return ORC_EINVAL;
@@ -270,42 +274,83 @@ int orc_set_score_int8(orc_unit *u, int on)
     return ORC_OK;
 }
 
-/* The code and the stored value of an fp32 score under inverse scale inv. */
-static float int8_code(float s, float inv)
+/* The code of score s under absmax M: round(s * 255 / M), ties to even (the
+ * default rounding mode), within 0..255; *x receives s * 255 / M unrounded. */
+static double int8_code(double s, double M, double *x)
 {
-    float c = rintf(s * inv);
-    if (c > 255.0f) c = 255.0f;
-    if (!(c >= 0.0f)) c = 0.0f;
+    *x = M > 0.0 ? s * 255.0 / M : 0.0;
+    double c = nearbyint(*x);
+    if (c > 255.0) c = 255.0;
+    if (!(c >= 0.0)) c = 0.0;
     return c;
 }
 
 /* Requantises every retained score and the new token's after an update. */
 static void quantise_int8(orc_unit *u)
 {
-    float M = (float)u->score_new;
+    double M = u->score_new;
     for (int s = 0; s < u->cap; ++s)
-        if (u->pos[s] >= 0 && (float)u->score[s] > M) M = (float)u->score[s];
-    const float inv = M > 0.0f ? 255.0f / M : 0.0f;
-    const float scale = M / 255.0f;
-    for (int s = 0; s < u->cap; ++s)
-        if (u->pos[s] >= 0) u->score[s] = (double)(int8_code((float)u->score[s], inv) * scale);
-    u->score_new = (double)(int8_code((float)u->score_new, inv) * scale);
-    u->qscale = scale;
+        if (u->pos[s] >= 0 && u->score[s] > M) M = u->score[s];
+    for (int s = 0; s < u->cap; ++s) {
+        u->qx[s] = 0.0;
+        if (u->pos[s] >= 0) u->score[s] = int8_code(u->score[s], M, &u->qx[s]) * M / 255.0;
+    }
+    u->score_new = int8_code(u->score_new, M, &u->qx_new) * M / 255.0;
+    u->qmax = M;
+    u->qscale = M / 255.0;
 }
 
-float orc_score_scale(const orc_unit *u) { return u->qscale; }
+double orc_score_scale(const orc_unit *u) { return u->qscale; }
 
 /* The INT8 codes of the unit's slots (0 for empty slots and before any step). */
 void orc_score_codes(const orc_unit *u, uint8_t *dst)
 {
     for (int s = 0; s < u->cap; ++s)
-        dst[s] = (u->pos[s] >= 0 && u->qscale > 0.0f) ? (uint8_t)rintf((float)u->score[s] / u->qscale) : 0;
+        dst[s] = (u->pos[s] >= 0 && u->qmax > 0.0) ? (uint8_t)nearbyint(u->score[s] * 255.0 / u->qmax) : 0;
+}
+
+/* INT8: each slot's s * 255 / M before the last rounding (0 for empty slots),
+ * and the pending new token's (test use: how close a code was to a midpoint). */
+void orc_int8_unrounded(const orc_unit *u, double *dst, double *new_x)
+{
+    for (int s = 0; s < u->cap; ++s) dst[s] = u->pos[s] >= 0 ? u->qx[s] : 0.0;
+    *new_x = u->qx_new;
+}
+
+/* Test hook: replaces the code of the token in `slot` (slot == cap: the
+ * pending new token) by `code`, one code away from its own, so that a caller
+ * checking another implementation can continue from that implementation's
+ * value where the two rounded a midpoint apart. Nothing else changes. */
+int orc_adopt_int8_code(orc_unit *u, int slot, int code)
+{
+    if (!u->int8 || !(u->qmax > 0.0) || code < 0 || code > 255 || slot < 0 || slot > u->cap) return ORC_EINVAL;
+    if (slot == u->cap && !u->have_new) return ORC_ESTATE;
+    if (slot < u->cap && u->pos[slot] < 0) return ORC_EINVAL;
+    double *v = slot == u->cap ? &u->score_new : &u->score[slot];
+    const double own = nearbyint(*v * 255.0 / u->qmax);
+    if (fabs(own - (double)code) > 1.0) return ORC_EINVAL;
+    *v = (double)code * u->qmax / 255.0;
+    return ORC_OK;
+}
+
+/* Test hook: replaces the stored cumulative scores of the retained tokens
+ * (scores[slot]; empty slots ignored) and of the pending new token, for
+ * checking another selector on the same values: the choice that follows is
+ * made by the steps of this file, on these values. */
+int orc_set_scores(orc_unit *u, const double *scores, double score_new)
+{
+    if (!u->have_new) return ORC_ESTATE;
+    for (int s = 0; s < u->cap; ++s)
+        if (u->pos[s] >= 0) u->score[s] = scores[s];
+    u->score_new = score_new;
+    return ORC_OK;
 }
 
 void orc_free(orc_unit *u)
 {
     if (!u) return;
     free(u->pos); free(u->k); free(u->v); free(u->score); free(u->k_new); free(u->v_new); free(u->pool);
+    free(u->qx);
     free(u);
 }
 

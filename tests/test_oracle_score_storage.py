@@ -144,22 +144,57 @@ def test_storage_modes_checked():
 
 # INT8 storage (section 6.2 names INT8 quantisation of the scores with no
 # scale or zero point; the reading is absmax per unit: codes round(s * 255 / M),
-# M the unit's largest score after the update, the new token's included,
-# stored as code * M / 255; the rounding in fp32).
+# ties to even, M the unit's largest score after the update, the new token's
+# included, stored as code * M / 255; fp64 like the rest of the oracle).
 
 
 def _q8(x, M):
-    """numpy float32 absmax quantisation of fp64 values x with absmax M."""
+    """numpy fp64 absmax quantisation of values x with absmax M (np.rint
+    rounds ties to even)."""
+    x = np.asarray(x, dtype=np.float64)
+    c = np.clip(np.rint(x * 255.0 / M), 0.0, 255.0)
+    return c * M / 255.0, c.astype(np.int64), M / 255.0
+
+
+def _q8_fp32_rule(x, M):
+    """The same codes taken in fp32, the order a GPU kernel takes them: s and
+    M rounded to fp32, inv = 255 / M and the product in fp32, then rint."""
     M32 = np.float32(M)
-    inv, scale = np.float32(255.0) / M32, M32 / np.float32(255.0)
+    inv = np.float32(255.0) / M32
     c = np.minimum(np.rint(np.float32(x) * inv), np.float32(255.0))
-    return (c * scale).astype(np.float64), c.astype(np.int64), float(scale)
+    return c.astype(np.int64)
+
+
+def test_int8_fp32_rule_differs_from_the_definition_only_at_midpoints():
+    """The fp32 order of the codes (three roundings of at most 2^-24 relative
+    each, plus those of s and M) moves s * 255 / M by at most 255 * 4 * 2^-24
+    = 6.1e-5 codes: its code equals the fp64 definition's except where the
+    unrounded value lies within 1e-4 of a midpoint k + 1/2, and then by one.
+    Values placed exactly at midpoints show that such differences happen."""
+    rng = np.random.default_rng(2026)
+    M = rng.uniform(1e-3, 50.0, 4000)
+    x = rng.uniform(0.0, 1.0, (4000, 64)) * M[:, None]
+    # values right at midpoints of the code grid (k + 1/2) * M / 255
+    k = rng.integers(0, 255, (4000, 16))
+    mids = (k + 0.5) * M[:, None] / 255.0
+    vals = np.concatenate([x, mids], axis=1)
+    moved = 0
+    for i in range(len(M)):
+        _, c64, _ = _q8(vals[i], M[i])
+        c32 = _q8_fp32_rule(vals[i], M[i])
+        d = np.abs(c64 - c32)
+        assert d.max() <= 1
+        u = vals[i] * 255.0 / M[i]
+        frac = np.abs(u - np.floor(u) - 0.5)
+        assert np.all(frac[d == 1] < 1e-4)
+        moved += int(d.sum())
+    assert moved > 0  # midpoint values do round apart
 
 
 @pytest.mark.parametrize("forget", [0.0, 0.1])
 def test_int8_recursion_against_sdpa(forget):
     """Never evicting: the stored scores follow s <- q((1 - forget) s + a), a
-    from torch's fp64 SDPA, q the numpy float32 absmax quantisation over the
+    from torch's fp64 SDPA, q the numpy fp64 absmax quantisation over the
     unit (the new token included); codes, scale and values agree."""
     rng = np.random.default_rng(81 + int(forget * 10))
     P, T, G, d = 6, 30, 2, 8
@@ -177,25 +212,25 @@ def test_int8_recursion_against_sdpa(forget):
         w = _sdpa_weights(Q, K, t, P).mean(axis=0)
         m = P + t + 1
         upd = np.concatenate([(1.0 - forget) * ref[:m - 1] + w[:m - 1], w[m - 1:m]])
-        M = float(np.max(np.float32(upd)))
+        M = float(np.max(upd))
         q, codes, scale = _q8(upd, M)
         pos, sc = u.positions(), u.scores()
         got = np.zeros(n)
         got[pos[pos >= 0]] = sc[pos >= 0]
         gc = np.zeros(n, np.int64)
         gc[pos[pos >= 0]] = u.score_codes()[pos >= 0]
-        assert u.score_scale() == pytest.approx(scale, rel=1e-6)
+        assert u.score_scale() == pytest.approx(scale, rel=1e-12)
         assert gc[:m].max() == 255 and gc[:m].min() >= 0
-        # the stored values are code * scale in fp32, within half a step of the update
-        assert np.all(np.float32(got[:m]) == got[:m])
-        np.testing.assert_array_equal(np.float32(gc[:m]) * np.float32(u.score_scale()), np.float32(got[:m]))
-        assert np.all(np.abs(got[:m] - upd) <= 0.5 * scale * (1 + 1e-5) + 1e-12)
-        # codes equal numpy's except where fp64 vs fp32 attention sits on a rounding midpoint
+        # the stored values are code * M / 255, within half a step of the update
+        np.testing.assert_allclose(got[:m], gc[:m] * (255.0 * u.score_scale()) / 255.0, rtol=1e-15, atol=0)
+        assert np.all(np.abs(got[:m] - upd) <= 0.5 * scale * (1 + 1e-12) + 1e-15)
+        # codes equal numpy's: both fp64, from attention weights that agree to
+        # rounding (SDPA and the oracle sum in different orders)
         diff = np.abs(gc[:m] - codes)
         assert diff.max() <= 1
         moved += int(diff.sum())
         ref[:m] = got[:m]  # the recursion continues from the stored values
-    assert moved <= 2
+    assert moved == 0
 
 
 def test_int8_selection_equals_brute_force_on_stored_scores():
@@ -289,7 +324,7 @@ def test_int8_new_token_sets_the_scale():
     """Right after a prefill (scores 0) a new token whose key points along
     the query takes the largest weight: it alone sets the scale (code 255),
     and the prompt tokens' codes are their SDPA weights over its weight,
-    rounded in float32."""
+    rounded (fp64)."""
     rng = np.random.default_rng(12)
     P, G, d = 6, 1, 8
     u = Unit(H2O, 1, P, 2, P + 3, 0, 0, G, d)
@@ -301,8 +336,8 @@ def test_int8_new_token_sets_the_scale():
     u.attend(Q[0], K[P], K[P])
     w = _sdpa_weights(Q, K, 0, P).mean(axis=0)
     assert np.argmax(w) == P
-    q, codes, scale = _q8(w, float(np.float32(w[P])))
-    assert u.score_scale() == pytest.approx(scale, rel=1e-6)
+    q, codes, scale = _q8(w, float(w[P]))
+    assert u.score_scale() == pytest.approx(scale, rel=1e-12)
     assert round(u.new_score / u.score_scale()) == 255
     pos = u.positions()
     got = u.score_codes()
