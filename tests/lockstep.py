@@ -14,6 +14,14 @@ retained set. For two-pool H2O the trace also records the promotion; a
 different decision is accepted only when one of the comparisons that made
 the oracle's (the two lowest of a pool, a score against the threshold) was
 within the same relative tolerance, and is then adopted whole.
+
+INT8 score storage is compared code by code at every step: the GPU's codes
+(read after the step) must equal the oracle's, except one code apart where
+the oracle's unrounded value s * 255 / M lay within MIDPOINT_TOL of a
+rounding midpoint (the GPU sums and rounds in fp32, the oracle in fp64);
+such a code is counted and adopted by the oracle. With equal codes both
+sides order the candidates identically, so INT8 victims must then agree
+exactly.
 """
 from __future__ import annotations
 
@@ -32,6 +40,10 @@ from workloads.configs import DTYPE_BF16, POLICY_H2O, POLICY_H2O_BLOCK, POLICY_H
 NEAR_TIE_REL = 1e-5
 BF16_REL_TOL = 2e-2
 F32_ABS_TOL = 1e-4
+# INT8 codes: how far from a midpoint k + 1/2 (in codes) an fp32-vs-fp64
+# difference may move the unrounded value. The scores agree to about 1e-6
+# relative (fp32 accumulation over the steps), i.e. 2.6e-4 codes at code 255.
+MIDPOINT_TOL = 1e-3
 
 
 def scored(w: Workload) -> bool:
@@ -50,6 +62,8 @@ class DeviceRun:
     pos_snap: dict = field(default_factory=dict)    # layer -> {t: int32 [B, Hkv, C]}; t = -1 after prefill
     score_snap: dict = field(default_factory=dict)  # layer -> {t: float32 [B, Hkv, C]}
     pool_snap: dict = field(default_factory=dict)   # layer -> {t: uint8 [B, Hkv, C]} (two-pool H2O)
+    code_snap: dict = field(default_factory=dict)   # layer -> {t: uint8 [B, Hkv, C]} INT8 codes after step t
+    scale_snap: dict = field(default_factory=dict)  # layer -> {t: float32 [B, Hkv]} INT8 scales after step t
     err: int = 0
     split: int = 0
     tensor_cores: int = 0
@@ -68,7 +82,8 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
 
     interleave=True issues the steps token by token over the layers, as a
     model does (layer 0, 1, ... of token t, then token t + 1); otherwise all
-    steps of one layer, then the next layer."""
+    steps of one layer, then the next layer. INT8 score storage: the codes
+    and scales are read after every step."""
     cache = KVEvictCache.from_workload(w, device=device)
     if split:
         cache.set_split(split)
@@ -106,6 +121,8 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
         run.pos_snap[layer] = {-1: cache.slot_positions(layer).cpu()}
         run.score_snap[layer] = {}
         run.pool_snap[layer] = {}
+        run.code_snap[layer] = {}
+        run.scale_snap[layer] = {}
         if scored(w):
             run.score_snap[layer][-1] = cache.scores(layer).cpu()
         if w.policy == POLICY_H2O_POOLS:
@@ -113,9 +130,17 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
         seqs = out_seqs if out_seqs is not None else sorted({u[0] for u in mine})
         bufs[layer] = (q, k, v, out, trace, seqs)
 
+    int8 = getattr(w, "score_int8", False)
+
     def step(layer, t):
         q, k, v, out, _, _ = bufs[layer]
         cache.decode_step(layer, q[t], k[t], v[t], out[t])
+        if int8:  # stored value = code * scale exactly: the code is the rounded ratio
+            scl = cache.score_scales(layer)
+            codes = torch.round(cache.scores(layer) / scl.clamp_min(1e-38)[..., None])
+            assert bool(((codes >= 0) & (codes <= 255)).all()), f"layer {layer} step {t}: INT8 code out of range"
+            run.code_snap[layer][t] = codes.to(torch.uint8).cpu()
+            run.scale_snap[layer][t] = scl.cpu()
         if t in snap_steps:
             run.pos_snap[layer][t] = cache.slot_positions(layer).cpu()
             if scored(w):
@@ -146,7 +171,10 @@ class UnitReport:
     unit: tuple
     max_out_err: float = 0.0
     max_score_err: float = 0.0
-    near_ties: int = 0
+    near_ties: int = 0       # victims (or two-pool decisions) that differed at a near-tie, adopted
+    decisions: int = 0       # steps at which a victim was chosen among scored candidates
+    midpoints: int = 0       # INT8 codes one apart at a rounding midpoint, adopted
+    codes_compared: int = 0  # INT8 codes compared
     steps: int = 0
     out_checks: int = 0
 
@@ -161,13 +189,8 @@ def out_tol(w):
     return BF16_REL_TOL if w.dtype == DTYPE_BF16 else F32_ABS_TOL
 
 
-def score_error(w, got, ref, qscale: float = 0.0):
+def score_error(w, got, ref):
     diff = np.abs(got - ref)
-    if getattr(w, "score_int8", False):
-        # INT8 storage: both quantise with their own unit maximum (fp32 vs fp64
-        # sums before the same rounding); a midpoint may round one code apart
-        # and the difference then persists: allow two codes of the oracle's scale
-        diff = np.maximum(diff - 2.0 * qscale * (1 + 1e-3), 0.0)
     if getattr(w, "score_half", False):
         # binary16 storage: the GPU rounds its fp32 sum, the oracle its fp64 sum;
         # they may land one binary16 step apart (at most 2^-10 of the value)
@@ -196,6 +219,43 @@ def replay_unit(w: Workload, unit, x, run: DeviceRun, n_steps: int, out_steps=No
     pools_policy = w.policy == POLICY_H2O_POOLS
     tie_rel = 2.0**-10 if getattr(w, "score_half", False) else NEAR_TIE_REL  # one binary16 step
     int8 = getattr(w, "score_int8", False)
+    csnaps = run.code_snap.get(layer, {})
+    scsnaps = run.scale_snap.get(layer, {})
+
+    def sync_int8_codes(t, gslot, gold):
+        """INT8: compares the oracle's codes after its update at step t with
+        the GPU's (read after the step: the destination slot then holds the
+        new token, the evicted token's code is in the trace); a code one apart
+        at a rounding midpoint is counted and adopted, any other difference
+        fails."""
+        assert t in csnaps, f"{unit} step {t}: INT8 codes not read"
+        gcodes = csnaps[t][seq, h].numpy().astype(np.int64)
+        gscale = float(scsnaps[t][seq, h])
+        sc_err = abs(gscale - u.score_scale()) / max(u.score_scale(), 1e-300)
+        assert sc_err <= out_tol(w), f"{unit} step {t}: INT8 scale {gscale:.9g}, oracle {u.score_scale():.9g}"
+        xo, xnew = u.int8_unrounded()
+        pos = u.positions()
+        ocodes = u.score_codes().astype(np.int64)
+        pairs = []  # (oracle slot or cap for the new token, GPU code)
+        for s in np.nonzero(pos >= 0)[0]:
+            if s != gslot:
+                pairs.append((int(s), int(gcodes[s])))
+        if gold >= 0 and 0 <= gslot < u.cap:  # the evicted token's code is in the trace
+            ev = np.array([tr[t, 2]], dtype=np.int32).view(np.float32)[0]
+            pairs.append((gslot, int(np.rint(ev / np.float32(gscale)))))
+        gnew = np.array([tr[t, 3]], dtype=np.int32).view(np.float32)[0]
+        pairs.append((u.cap, int(np.rint(gnew / np.float32(gscale)))))
+        rep.codes_compared += len(pairs)
+        for s, gc in pairs:
+            oc = int(ocodes[s]) if s < u.cap else int(np.rint(u.new_score / u.score_scale()))
+            if gc == oc:
+                continue
+            x = xo[s] if s < u.cap else xnew
+            mid = abs(x - np.floor(x) - 0.5)
+            assert abs(gc - oc) == 1 and mid < MIDPOINT_TOL, \
+                f"{unit} step {t}: slot {s} GPU code {gc}, oracle {oc} (unrounded {x:.6f})"
+            u.adopt_int8_code(s, gc)
+            rep.midpoints += 1
 
     def check_pools(t):
         if t in psnaps:
@@ -218,10 +278,16 @@ def replay_unit(w: Workload, unit, x, run: DeviceRun, n_steps: int, out_steps=No
                 assert e <= out_tol(w), f"{unit} step {t}: output error {e:.3e}"
         else:
             u.stage(x.k_new[t] if x is not None else zero, x.v_new[t] if x is not None else zero)
-        slot = u.choose()
         gslot, gold = int(tr[t, 0]), int(tr[t, 1])
+        if int8:
+            sync_int8_codes(t, gslot, gold)
+        slot = u.choose()
+        if scored(w) and not pools_policy and gold >= 0:
+            rep.decisions += 1
         if pools_policy:
             mine = u.decision()
+            if u.decision_margin != np.inf:  # the recent pool overflowed: a decision among scores
+                rep.decisions += 1
             grec = int(tr[t, 3])
             gdec = (u.cap if gslot < 0 else gslot, 1 if grec == -2 else 0, grec if grec >= 0 else -1)
             if gdec != mine:
@@ -232,14 +298,10 @@ def replay_unit(w: Workload, unit, x, run: DeviceRun, n_steps: int, out_steps=No
             assert gold == want_old, f"{unit} step {t}: GPU evicted position {gold}, oracle {want_old}"
             u.commit_pools(*gdec)
         elif gslot != slot:
-            assert w.policy == POLICY_H2O, f"{unit} step {t}: GPU slot {gslot}, oracle slot {slot}"
+            assert w.policy == POLICY_H2O and not int8, f"{unit} step {t}: GPU slot {gslot}, oracle slot {slot}"
             sc = u.scores()
             a, b = sc[slot], sc[gslot]
             rel = abs(a - b) / max(a, b, 1e-300)
-            tie_rel = 2.0**-10 if getattr(w, "score_half", False) else NEAR_TIE_REL  # one binary16 step
-            if int8:  # within two and a half codes of the oracle's scale (see score_error)
-                rel = abs(a - b) / max(2.5 * u.score_scale(), 1e-300)
-                tie_rel = 1.0
             assert 0 <= gslot < u.cap and rel < tie_rel, \
                 f"{unit} step {t}: GPU evicted slot {gslot} (pos {u.pos_at(gslot)}, score {b:.9g}), " \
                 f"oracle slot {slot} (pos {u.pos_at(slot)}, score {a:.9g}), rel {rel:.3e}"
@@ -254,11 +316,29 @@ def replay_unit(w: Workload, unit, x, run: DeviceRun, n_steps: int, out_steps=No
         if t in ssnaps:
             pos = u.positions()
             occ = pos >= 0
-            e = score_error(w, ssnaps[t][seq, h].numpy()[occ], u.scores()[occ], u.score_scale() if int8 else 0.0)
+            e = score_error(w, ssnaps[t][seq, h].numpy()[occ], u.scores()[occ])
             rep.max_score_err = max(rep.max_score_err, e)
             assert e <= out_tol(w), f"{unit} step {t}: score error {e:.3e}"
         rep.steps += 1
     return rep
+
+
+def record_ties(record_property, reps, max_near_ties: int, max_midpoint_rate: float = 0.0,
+                max_near_tie_rate: float = 0.0) -> dict:
+    """Records a lockstep run's counts as test properties (a junit report
+    carries them): victims that differed at a near-tie, eviction decisions,
+    INT8 codes one apart at a midpoint and INT8 codes compared. Asserts the
+    near-tie count (at most max_near_ties + max_near_tie_rate * decisions)
+    and the midpoint rate against their bounds."""
+    n = dict(near_ties=sum(r.near_ties for r in reps), decisions=sum(r.decisions for r in reps),
+             midpoints=sum(r.midpoints for r in reps), codes_compared=sum(r.codes_compared for r in reps))
+    for k, v in n.items():
+        record_property(k, v)
+    assert n["near_ties"] <= max_near_ties + max_near_tie_rate * n["decisions"], \
+        f"{n['near_ties']} near-ties in {n['decisions']} decisions"
+    assert n["midpoints"] <= max_midpoint_rate * n["codes_compared"], \
+        f"{n['midpoints']} INT8 midpoint codes in {n['codes_compared']}"
+    return n
 
 
 def replay_all(w, units, inputs, run, n_steps, out_steps=None, threads=None):

@@ -40,7 +40,7 @@ def _all_units(w, layers):
 # The tiny H2O workload, every unit, every step (fp32)
 # ----------------------------------------------------------------------------
 
-def test_h2o_tiny_lockstep(cuda_device):
+def test_h2o_tiny_lockstep(cuda_device, record_property):
     w = configs.H2O_TINY
     units = _all_units(w, [0])
     inputs = ls.host_inputs(w, units, w.decode_steps, w.prompt_len)
@@ -50,12 +50,13 @@ def test_h2o_tiny_lockstep(cuda_device):
     reps = ls.replay_all(w, units, inputs, run, w.decode_steps)
     rep = _report(reps)
     print("h2o tiny:", rep)
+    ls.record_ties(record_property, reps, max_near_ties=1)
     assert rep["max_out_err"] <= 1e-4 and rep["max_score_err"] <= 1e-4
     assert ls.check_selector(w, run, 0, w.prompt_len) == w.decode_steps
 
 
 @pytest.mark.parametrize("split", [1, 2, 4])
-def test_h2o_small_splits(cuda_device, split):
+def test_h2o_small_splits(cuda_device, split, record_property):
     """Ragged slot counts over several CTAs per unit; the cache fills during
     decode (prompt shorter than the budget) and then evicts."""
     w = _small(configs.POLICY_H2O, configs.DTYPE_F32, G=2, d=64, n_sink=3, n_heavy=40, n_recent=27, budget=70,
@@ -67,6 +68,7 @@ def test_h2o_small_splits(cuda_device, split):
     assert run.split == split and run.err == 0
     reps = ls.replay_all(w, units, inputs, run, w.decode_steps)
     print(f"split {split}:", _report(reps))
+    ls.record_ties(record_property, reps, max_near_ties=1)
     for layer in (0, 1):
         ls.check_selector(w, run, layer, w.prompt_len)
 
@@ -74,7 +76,7 @@ def test_h2o_small_splits(cuda_device, split):
 @pytest.mark.parametrize("policy,split,clusters", [
     (configs.POLICY_H2O, 1, 3), (configs.POLICY_H2O, 2, 5), (configs.POLICY_SINK_WINDOW, 1, 2),
     (configs.POLICY_SINK_WINDOW, 4, 3), (configs.POLICY_RANDOM, 2, 3)])
-def test_persistent_loop_with_refills(cuda_device, policy, split, clusters):
+def test_persistent_loop_with_refills(cuda_device, policy, split, clusters, record_property):
     """Few clusters, many units each, and more K/V tiles per unit than ring
     stages: the ring keeps streaming across unit boundaries and every stage is
     refilled many times."""
@@ -90,11 +92,12 @@ def test_persistent_loop_with_refills(cuda_device, policy, split, clusters):
     assert run.err == 0
     reps = ls.replay_all(w, units, inputs, run, T)
     print(f"persistent policy {policy} split {split} clusters {clusters}:", _report(reps))
+    ls.record_ties(record_property, reps, max_near_ties=1)
 
 
 @pytest.mark.parametrize("path", [1, 2])
 @pytest.mark.parametrize("G,d", [(1, 128), (2, 64), (4, 128), (8, 64), (8, 128)])
-def test_h2o_small_bf16_gqa(cuda_device, G, d, path):
+def test_h2o_small_bf16_gqa(cuda_device, G, d, path, record_property):
     """bf16 GQA on both decode paths: CUDA cores (1) and tensor cores (2)."""
     w = _small(configs.POLICY_H2O, configs.DTYPE_BF16, G=G, d=d, n_sink=2, n_heavy=50, n_recent=44, budget=96,
                prompt_len=150, decode_steps=70)
@@ -105,6 +108,7 @@ def test_h2o_small_bf16_gqa(cuda_device, G, d, path):
     assert run.err == 0 and run.tensor_cores == (path == 2)
     reps = ls.replay_all(w, units, inputs, run, w.decode_steps)
     print(f"G={G} d={d} path={path}:", _report(reps))
+    ls.record_ties(record_property, reps, max_near_ties=1)
     ls.check_selector(w, run, 0, w.prompt_len)
 
 
@@ -353,7 +357,7 @@ def test_sink_window_full_shape(cuda_device):
             assert np.all(tr[t, ..., 0] == want)
 
 
-def test_h2o_mha_full_shape(cuda_device):
+def test_h2o_mha_full_shape(cuda_device, record_property):
     """H2O 4 + 510 + 510 at B=16, 32x32 heads, d=128, prompt 2048."""
     w = configs.H2O_MHA
     T = 320
@@ -366,11 +370,12 @@ def test_h2o_mha_full_shape(cuda_device):
     reps = ls.replay_all(w, checked, inputs, run, T)
     rep = _report(reps)
     print("h2o mha full shape:", rep, "split", run.split)
+    ls.record_ties(record_property, reps, max_near_ties=5)
     for layer in layers:
         assert ls.check_selector(w, run, layer, w.prompt_len) == len(snaps)
 
 
-def test_h2o_gqa_full_shape(cuda_device):
+def test_h2o_gqa_full_shape(cuda_device, record_property):
     """H2O GQA 64 query / 8 KV heads, K=2048, B=64, context 32768, 512 steps."""
     w = configs.H2O_GQA
     T = w.decode_steps
@@ -381,6 +386,7 @@ def test_h2o_gqa_full_shape(cuda_device):
     assert run.err == 0
     reps = ls.replay_all(w, checked, inputs, run, T)
     print("h2o gqa full shape:", _report(reps), "split", run.split)
+    ls.record_ties(record_property, reps, max_near_ties=5)
     assert ls.check_selector(w, run, 0, w.prompt_len) == len(snaps)
 
 
@@ -406,7 +412,7 @@ def test_random_full_shape(cuda_device):
     assert sum(r.out_checks for r in reps) == len(with_values) * len(out_steps)
 
 
-def test_h2o_reasoning_full_shape(cuda_device):
+def test_h2o_reasoning_full_shape(cuda_device, record_property):
     """H2O on the long-reasoning shape: the 8192-token prompt protected, 1024
     heavy + 1024 recent, K=10240; the cache fills for 2048 steps, then
     evicts."""
@@ -419,4 +425,5 @@ def test_h2o_reasoning_full_shape(cuda_device):
     assert run.err == 0
     reps = ls.replay_all(w, checked, inputs, run, T)
     print("h2o reasoning full shape:", _report(reps), "split", run.split)
+    ls.record_ties(record_property, reps, max_near_ties=5)
     assert ls.check_selector(w, run, 0, w.prompt_len) >= 3

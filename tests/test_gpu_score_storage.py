@@ -7,10 +7,11 @@ Outputs and scores as for H2O (2e-2 relative for bf16, 1e-4 max-abs for fp32;
 binary16 scores also within one binary16 step). Victims identical, except at
 near-ties, which the oracle adopts: within 1e-5 relative for fp32 scores,
 within one binary16 step for binary16 scores (the GPU sums in fp32, the
-oracle in fp64, before the same rounding). INT8: stored values within two
-codes of the oracle's, victims within two and a half codes (a midpoint may
-round one code apart, and the difference persists). The selector is also
-checked bit-exact on the GPU's own stored values.
+oracle in fp64, before the same rounding). INT8: the codes are compared at
+every step and must be equal, except one code apart where the oracle's
+unrounded value sat at a rounding midpoint (counted, adopted by the oracle);
+with equal codes the victims must be identical. The selector is also checked
+bit-exact on the GPU's own stored values.
 """
 import numpy as np
 import pytest
@@ -30,7 +31,7 @@ def _small(dtype, forget, half, policy=H2O, r=0):
 
 @pytest.mark.parametrize("dtype,forget,half", [(BF16, 0.1, False), (BF16, 0.0, True), (BF16, 0.05, True),
                                                (F32, 0.02, True), (F32, 0.2, False)])
-def test_score_storage_lockstep(cuda_device, dtype, forget, half):
+def test_score_storage_lockstep(cuda_device, dtype, forget, half, record_property):
     w = _small(dtype, forget, half)
     T = 160
     units = [(s, 0, h) for s in range(w.batch) for h in range(w.n_kv_heads)]
@@ -43,6 +44,7 @@ def test_score_storage_lockstep(cuda_device, dtype, forget, half):
     worst_sc = max(r.max_score_err for r in reps)
     ties = sum(r.near_ties for r in reps)
     print(f"forget {forget} half {half}: out {worst_out:.2e}, score {worst_sc:.2e}, near ties {ties}")
+    ls.record_ties(record_property, reps, max_near_ties=3, max_near_tie_rate=2e-3 if half else 0.0)
     # the cache fills during the first budget - prompt steps: the selector decides from then on
     assert ls.check_selector(w, run, 0, w.prompt_len) == sum(t >= w.budget - w.prompt_len for t in snaps)
     if half:  # every stored score is a binary16 value
@@ -78,7 +80,7 @@ def test_score_storage_rejected_where_unsupported(cuda_device):
 
 
 @pytest.mark.parametrize("dtype,forget", [(BF16, 0.0), (BF16, 0.05), (F32, 0.0)])
-def test_int8_scores_lockstep(cuda_device, dtype, forget):
+def test_int8_scores_lockstep(cuda_device, dtype, forget, record_property):
     w = _small(dtype, forget, False).with_(score_int8=True)
     T = 160
     units = [(s, 0, h) for s in range(w.batch) for h in range(w.n_kv_heads)]
@@ -87,8 +89,9 @@ def test_int8_scores_lockstep(cuda_device, dtype, forget):
     run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=snaps)
     assert run.err == 0
     reps = ls.replay_all(w, units, inputs, run, T)
+    n = ls.record_ties(record_property, reps, max_near_ties=0, max_midpoint_rate=1e-3)
     print(f"int8 forget {forget}: out {max(r.max_out_err for r in reps):.2e}, "
-          f"score {max(r.max_score_err for r in reps):.2e}, near ties {sum(r.near_ties for r in reps)}")
+          f"score {max(r.max_score_err for r in reps):.2e}, {n}")
     assert ls.check_selector(w, run, 0, w.prompt_len) == sum(t >= w.budget - w.prompt_len for t in snaps)
 
 
@@ -140,7 +143,7 @@ def test_int8_scores_rejected_where_unsupported(cuda_device):
 
 @pytest.mark.parametrize("w", [configs.H2O_MHA_FP16, configs.H2O_MHA_EMA, configs.H2O_MHA_INT8],
                          ids=["binary16", "moving_average", "int8"])
-def test_score_storage_full_shape(cuda_device, w):
+def test_score_storage_full_shape(cuda_device, w, record_property):
     """H2O 4 + 510 + 510 on the MHA shape with binary16 scores, and with the
     moving average (forget 0.01): B=16, 32x32 heads, d=128, prompt 2048, 200
     steps; sequences {0, 15} x every head of layers {0, 31} in lockstep."""
@@ -152,7 +155,10 @@ def test_score_storage_full_shape(cuda_device, w):
     run = ls.run_gpu(w, layers, T, inputs, w.prompt_len, cuda_device, snap_steps=snaps)
     assert run.err == 0
     reps = ls.replay_all(w, checked, inputs, run, T, out_steps=range(0, T, 7))
-    print(w.name, "full shape: near ties", sum(r.near_ties for r in reps),
-          "max out err", max(r.max_out_err for r in reps))
+    # binary16: a one-step rounding difference reorders candidates within one
+    # binary16 step of each other (observed 11 in 25600 decisions)
+    n = ls.record_ties(record_property, reps, max_near_ties=8, max_midpoint_rate=1e-3,
+                       max_near_tie_rate=2e-3 if w.score_half else 0.0)
+    print(w.name, "full shape:", n, "max out err", max(r.max_out_err for r in reps))
     for layer in layers:
         assert ls.check_selector(w, run, layer, w.prompt_len) == len(snaps)
