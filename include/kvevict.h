@@ -41,6 +41,8 @@
  *    pointers passed in must stay valid until the stream has passed the call.
  *  - Device tensors are dense, row-major, of the handle's dtype (fp32 or
  *    bf16), 16-byte aligned.
+ *  - Calls are made with the handle's device current: the device that holds
+ *    the state buffer given to kvevict_create (its stream belongs to it).
  *  - Not thread-safe: one host thread drives one handle at a time.
  */
 #ifndef KVEVICT_H
@@ -269,15 +271,18 @@ int kvevict_prefill_snapkv(kvevict_t h, int layer, const void *Q_obs, const void
  * they prefill -- a serving framework that reserved the GPU's free memory for
  * its own pool at start-up, or a latency-bound path that cannot take the
  * device-wide synchronisation cudaMalloc and cudaFree may cause. It does what
- * kvevict_prefill_scored does (same arguments, results and errors), but its
- * scratch is a fixed 16 MiB array inside the library that every GPU loading
- * the library holds until the process exits; it calls no allocator.
- *   - Returns CAPACITY (and says so on stderr) when the prompt needs more
- *     scratch than 16 MiB (kvevict_prefill_scored_workspace_bytes tells how
- *     much); use kvevict_prefill_scored with a workspace then.
- *   - The first call on a device, made with that device current, looks up the
- *     array's address on that device; make that first call before any stream
- *     capture.
+ * kvevict_prefill_scored does (same arguments and results), but its scratch
+ * is a fixed 16 MiB array inside the library that every GPU loading the
+ * library holds until the process exits; it calls no allocator.
+ *   - Errors: first every check of kvevict_prefill_scored except those on the
+ *     workspace, with the same status; then INVALID_ARG (and a line on
+ *     stderr) if the handle's device is not the current device; then
+ *     CAPACITY (and a line on stderr) when the prompt needs more scratch than
+ *     16 MiB (kvevict_prefill_scored_workspace_bytes tells how much): use
+ *     kvevict_prefill_scored with a workspace then.
+ *   - kvevict_create looks up the array's address on the handle's device for
+ *     every handle that may call this (H2O, bf16, fp32 scores), so the call
+ *     itself does no lookup and needs no warm-up call first.
  *   - All calls share the one array: calls whose work overlaps on the GPU
  *     (other streams, other handles) race and corrupt each other; order them.
  *     Nothing in it needs to start at zero. */
@@ -326,6 +331,27 @@ int kvevict_slot_positions(kvevict_t h, int layer, int32_t *dst, int dst_is_devi
  * fp32 (empty slots hold stale values; read them with the positions).
  * INVALID_ARG for policies that keep no scores. Same dst rules as above. */
 int kvevict_scores(kvevict_t h, int layer, float *dst, int dst_is_device);
+
+/* The H2O eviction decision alone, on scores the caller supplies (a test and
+ * diagnostic entry point: it checks the decode step's selector against another
+ * implementation's scores). For every unit of `layer`, among the slots whose
+ * token is a candidate for the layer's next decode step -- n_sink <= pos <=
+ * p - n_recent, p = the position that step appends (the layer's prompt length
+ * plus its decode steps so far), empty slots never -- the one with the
+ * smallest (score, position): the victim that step evicts when the cache is
+ * full and its updated scores are `scores` ("h2o: heavy-hitter oracle"
+ * summary, Algorithm 1: remove the token whose removal leaves the highest
+ * cumulative score; ties to the older position). The kernel uses the decode
+ * step's own candidate rule, key (fp32 score bits, then position) and
+ * reductions, on the decode kernel's CTA shape.
+ *   scores:  device, [batch][n_kv_heads][C] fp32, 16-byte aligned; values of
+ *            empty slots are ignored. Scores are >= 0 (as the decode step's).
+ *   victims: device, [batch][n_kv_heads] int32: the victim's slot, -1 where
+ *            no slot is a candidate.
+ * Reads the layer's slot positions, changes nothing in the handle; one launch
+ * on the handle's stream. INVALID_ARG unless the policy is H2O, for null or
+ * misaligned pointers; STATE for a layer out of range. */
+int kvevict_select_victims(kvevict_t h, int layer, const float *scores, int32_t *victims);
 
 /* Checkpoint and resume. A handle's state is the device buffer the caller
  * gave kvevict_create (caller-owned: the caller copies it) plus host-side

@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
             L.kvevict_slot_pools.argtypes = [P, I, P, I]
             L.kvevict_score_scales.argtypes = [P, I, P, I]
             L.kvevict_probe_wait_timeout.argtypes = [P]
+            L.kvevict_select_victims.argtypes = [P, I, P, P]
             L.kvevict_checkpoint_bytes.argtypes = [P, ctypes.POINTER(SZ)]
             L.kvevict_checkpoint_save.argtypes = [P, P, SZ]
             L.kvevict_checkpoint_restore.argtypes = [P, P, SZ]
@@ -89,7 +90,7 @@ def lib() -> ctypes.CDLL:
                       "kvevict_prefill_scored", "kvevict_prefill_scored_static",
                       "kvevict_prefill_snapkv_workspace_bytes", "kvevict_prefill_snapkv", "kvevict_decode_step",
                       "kvevict_decode_step_host", "kvevict_decode_step_host_async", "kvevict_sync", "kvevict_slot_positions", "kvevict_scores", "kvevict_slot_pools",
-                      "kvevict_score_scales", "kvevict_probe_wait_timeout", "kvevict_checkpoint_bytes",
+                      "kvevict_score_scales", "kvevict_probe_wait_timeout", "kvevict_select_victims", "kvevict_checkpoint_bytes",
                       "kvevict_checkpoint_save", "kvevict_checkpoint_restore",
                       "kvevict_set_trace",
                       "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path", "kvevict_set_ring",

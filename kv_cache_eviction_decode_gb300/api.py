@@ -201,6 +201,16 @@ class KVEvictCache:
         check(self._L.kvevict_scores(self.h, layer, _ptr(out), 1 if on_dev else 0), "kvevict_scores")
         return out
 
+    def select_victims(self, layer: int, scores: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        """H2O: the slot the layer's next decode step would evict per unit with
+        these fp32 scores [batch][n_kv_heads][C] (-1: no candidate)."""
+        self._dev(scores, (self.B, self.Hkv, self.capacity), "scores", torch.float32)
+        if out is None:
+            out = torch.empty((self.B, self.Hkv), dtype=torch.int32, device=self.device)
+        self._dev(out, (self.B, self.Hkv), "out", torch.int32)
+        check(self._L.kvevict_select_victims(self.h, layer, _ptr(scores), _ptr(out)), "kvevict_select_victims")
+        return out
+
     def checkpoint(self) -> dict:
         """The handle's host record and a device copy of its state buffer,
         taken once every queued call has run."""

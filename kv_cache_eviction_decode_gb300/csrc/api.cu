@@ -19,6 +19,7 @@
 #include <new>
 #include <vector>
 
+#include "api_internal.h"
 #include "aux_kernels.h"
 #include "decode_dispatch.h"
 #include "decode_kernel.cuh"
@@ -187,6 +188,7 @@ struct kvevict_handle {
     kvevict_config cfg;
     Layout L;
     uint8_t *state = nullptr;
+    int device = -1;  // the CUDA device holding `state`
     cudaStream_t stream = nullptr;
     int split = 1;
     int clusters_req = 0;  // persistent grid size in clusters; 0 = automatic
@@ -645,8 +647,14 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
     Layout L = make_layout(cfg);
     if (!state || (reinterpret_cast<uintptr_t>(state) & (kAlign - 1))) return KVEVICT_ERR_INVALID_ARG;
     if (state_bytes < L.total) return KVEVICT_ERR_CAPACITY;
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, state) != cudaSuccess || pa.type != cudaMemoryTypeDevice) {
+        cudaGetLastError();  // clear the sticky-free error of a failed query
+        return KVEVICT_ERR_INVALID_ARG;
+    }
     kvevict_handle *h = new (std::nothrow) kvevict_handle();
     if (!h) return KVEVICT_ERR_CAPACITY;
+    h->device = pa.device;
     h->cfg = *cfg;
     h->L = L;
     h->state = static_cast<uint8_t *>(state);
@@ -669,6 +677,17 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
     if (cfg->score_int8 && h->split > 1) {  // INT8 scores need one CTA per unit
         delete h;
         return KVEVICT_ERR_INVALID_ARG;
+    }
+    // A handle that may call kvevict_prefill_scored_static: look up the fixed
+    // scratch array's address on this device now, so that call does no lookup
+    // of its own (and can be captured in a stream like the other calls).
+    if (cfg->policy == KVEVICT_H2O && cfg->dtype == KVEVICT_BF16 && !cfg->score_half && !cfg->score_int8) {
+        void *scratch = nullptr;
+        int rc0 = kvevict_static_scratch_address(h->device, &scratch);
+        if (rc0) {
+            delete h;
+            return rc0;
+        }
     }
     // Empty cache: K/V zero (every row a tile may touch is finite), every
     // position -1, every score 0, no error bits.
@@ -816,6 +835,26 @@ ScoredWorkspace scored_workspace(const kvevict_config &c, int P)
 
 }  // namespace
 
+int kvevict_handle_device(kvevict_t h) { return h ? h->device : -1; }
+
+int kvevict_prefill_scored_check(kvevict_t h, int layer, const void *Q, const void *K, const void *V, int prompt_len)
+{
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    const kvevict_config &c = h->cfg;
+    const int P = prompt_len;
+    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16 || c.score_half || c.score_int8)
+        return KVEVICT_ERR_INVALID_ARG;
+    if (P < 1 || P > kPromptMaxLen) return KVEVICT_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !aligned16(Q) || !aligned16(K) || !aligned16(V)) return KVEVICT_ERR_INVALID_ARG;
+    const long long q_rows = static_cast<long long>(c.batch) * c.n_q_heads * P;
+    if (q_rows >= (1LL << 31)) return KVEVICT_ERR_INVALID_ARG;  // tensor-map row coordinates are int32
+    if (static_cast<long long>(c.batch) * c.n_q_heads > 65535) return KVEVICT_ERR_INVALID_ARG;  // grid height
+    const LayerState &ls = h->layers[layer];
+    if (ls.prompt_len != 0 || ls.t != 0) return KVEVICT_ERR_STATE;
+    return KVEVICT_OK;
+}
+
 int kvevict_prefill_scored_workspace_bytes(kvevict_t h, int prompt_len, size_t *bytes)
 {
     if (!h || !bytes || prompt_len < 1 || prompt_len > kPromptMaxLen) return KVEVICT_ERR_INVALID_ARG;
@@ -827,29 +866,21 @@ int kvevict_prefill_scored(kvevict_t h, int layer, const void *Q, const void *K,
                            void *workspace, size_t workspace_bytes)
 {
     NvtxRange nvtx("kvevict_prefill_scored");
-    if (!h) return KVEVICT_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    int rc = kvevict_prefill_scored_check(h, layer, Q, K, V, prompt_len);
+    if (rc) return rc;
     const kvevict_config &c = h->cfg;
     const Layout &L = h->L;
     const int P = prompt_len;
-    if (c.policy != KVEVICT_H2O || c.dtype != KVEVICT_BF16 || c.score_half || c.score_int8)
-        return KVEVICT_ERR_INVALID_ARG;
-    if (P < 1 || P > kPromptMaxLen) return KVEVICT_ERR_INVALID_ARG;
-    if (!Q || !K || !V || !workspace || !aligned16(Q) || !aligned16(K) || !aligned16(V) ||
-        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
-        return KVEVICT_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return KVEVICT_ERR_INVALID_ARG;
     const ScoredWorkspace ws = scored_workspace(c, P);
     if (workspace_bytes < ws.bytes) return KVEVICT_ERR_INVALID_ARG;
     const long long q_rows = static_cast<long long>(c.batch) * c.n_q_heads * P;
-    if (q_rows >= (1LL << 31)) return KVEVICT_ERR_INVALID_ARG;  // tensor-map row coordinates are int32
-    if (static_cast<long long>(c.batch) * c.n_q_heads > 65535) return KVEVICT_ERR_INVALID_ARG;  // grid height
     LayerState &ls = h->layers[layer];
-    if (ls.prompt_len != 0 || ls.t != 0) return KVEVICT_ERR_STATE;
 
     uint8_t *wsb = static_cast<uint8_t *>(workspace);
     PromptAttnParams ap{};
     CUtensorMap tq, tk;
-    int rc = make_tensor_map(&tq, Q, static_cast<uint64_t>(q_rows), c.head_dim, kPromptTile);
+    rc = make_tensor_map(&tq, Q, static_cast<uint64_t>(q_rows), c.head_dim, kPromptTile);
     if (rc == KVEVICT_OK)
         rc = make_tensor_map(&tk, K, static_cast<uint64_t>(c.batch) * c.n_kv_heads * P, c.head_dim, kPromptTile);
     if (rc) return rc;
@@ -1296,6 +1327,31 @@ int kvevict_checkpoint_restore(kvevict_t h, const void *src, size_t bytes)
     h->stats.evictions = f[2];
     h->stats.cuts = f[3];
     h->last_layer = -1;  // the state buffer was just written by the caller: no early prefetch
+    return KVEVICT_OK;
+}
+
+int kvevict_select_victims(kvevict_t h, int layer, const float *scores, int32_t *victims)
+{
+    NvtxRange nvtx("kvevict_select_victims");
+    if (!h) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    if (h->cfg.policy != KVEVICT_H2O) return KVEVICT_ERR_INVALID_ARG;
+    if (!scores || !victims || !aligned16(scores) || (reinterpret_cast<uintptr_t>(victims) & 3u))
+        return KVEVICT_ERR_INVALID_ARG;
+    const LayerState &ls = h->layers[layer];
+    SelectParams sp{};
+    sp.score = scores;
+    sp.pos = at<int32_t>(h, h->L.off_pos) + static_cast<size_t>(layer) * h->L.layer_pslots;
+    sp.victim = victims;
+    sp.C = h->L.C;
+    sp.cstride = h->L.Cs;
+    sp.n_active = h->L.C;  // empty slots hold position -1: never a candidate
+    sp.n_sink = h->cfg.n_sink;
+    sp.n_recent = h->cfg.n_recent;
+    sp.p = ls.prompt_len + ls.t;
+    int rc = cuda_status(launch_h2o_select(sp, static_cast<int>(h->L.units), h->stream));
+    if (rc) return rc;
+    h->last_layer = -1;  // a launch that is not a decode step of any layer came last
     return KVEVICT_OK;
 }
 

@@ -4,6 +4,8 @@
 
 #include <cstddef>
 
+#include <cuda_runtime.h>
+
 namespace kvevict {
 
 struct DecodeKernelInfo {
@@ -19,6 +21,10 @@ struct DecodeKernelInfo {
 // false if the combination is not built.
 bool decode_kernel_f32(int head_dim, int G, bool holes, DecodeKernelInfo *out);
 bool decode_kernel_bf16(int head_dim, int G, bool holes, bool mma, DecodeKernelInfo *out);
+
+struct SelectParams;
+// The H2O selector alone (one CTA per unit), on the decode kernel's CTA shape.
+cudaError_t launch_h2o_select(const SelectParams &p, int units, cudaStream_t stream);
 
 inline bool decode_kernel(int dtype, int head_dim, int G, bool holes, bool mma, DecodeKernelInfo *out)
 {

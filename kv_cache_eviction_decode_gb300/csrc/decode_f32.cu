@@ -26,6 +26,14 @@ template <int D, bool H, bool MMA> bool pick_g(int G, DecodeKernelInfo *out)
 
 }  // namespace
 
+cudaError_t launch_h2o_select(const SelectParams &p, int units, cudaStream_t stream)
+{
+    constexpr int kWarps = warps_for<1, false>();  // the decode kernel's warps per CTA
+    if (units < 1) return cudaSuccess;
+    h2o_select_kernel<kWarps><<<units, kWarps * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 bool decode_kernel_f32(int head_dim, int G, bool holes, DecodeKernelInfo *out)
 {
     if (head_dim == 64) return holes ? pick_g<64, true, false>(G, out) : pick_g<64, false, false>(G, out);

@@ -125,6 +125,16 @@ struct DecodeParams {
     float hh_threshold;  // a token leaving the recent pool is promoted iff its score is above this
 };
 
+// The standalone H2O selector (h2o_select_kernel).
+struct SelectParams {
+    const float *score;    // [units][C] fp32 scores supplied by the caller
+    const int32_t *pos;    // this layer's slot positions [units][cstride]
+    int32_t *victim;       // [units] the slot to evict, -1 if no slot is a candidate
+    int C, cstride, n_active;
+    int n_sink, n_recent;
+    int p;                 // position of the token the next decode step appends
+};
+
 // Stored cumulative scores: fp32, or binary16 rounded to nearest even.
 __device__ __forceinline__ float score_load(const DecodeParams &P, size_t i)
 {
@@ -269,6 +279,49 @@ __device__ __forceinline__ int32_t warp_min_s32(int32_t v)
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
+}
+
+// ------------------------------------------------------------ H2O selector
+// The pieces of the H2O eviction decision ("h2o: heavy-hitter oracle" summary,
+// Algorithm 1: remove the token whose removal leaves the remaining set with
+// the highest cumulative score -- with an additive score, the lowest-score
+// token). The fused decode epilogue and the standalone selector kernel
+// (h2o_select_kernel) decide with this same code.
+//
+// A retained token at position ps is a candidate at the step that appends
+// position p iff it is neither a sink nor inside the recent window.
+__device__ __forceinline__ bool h2o_candidate(int32_t ps, int n_sink, int p, int n_recent)
+{
+    return ps >= n_sink && ps <= p - n_recent;
+}
+// The eviction order: the lower score first, then the older position. Scores
+// are >= 0, so their fp32 bit patterns order as the values do, and (score
+// bits << 32 | position) orders as (score, position).
+__device__ __forceinline__ uint64_t h2o_key(float score, int32_t ps)
+{
+    return (static_cast<uint64_t>(__float_as_uint(score)) << 32) | static_cast<uint32_t>(ps);
+}
+// Folds the token in `slot` (stored score `score`, position ps) into this
+// thread's running minimum (best, bslot) if it is a candidate.
+__device__ __forceinline__ void h2o_fold(uint64_t &best, int32_t &bslot, float score, int32_t ps, int slot,
+                                         int n_sink, int p, int n_recent)
+{
+    if (h2o_candidate(ps, n_sink, p, n_recent)) {
+        const uint64_t key = h2o_key(score, ps);
+        if (key < best) {
+            best = key;
+            bslot = slot;
+        }
+    }
+}
+// The smallest of n <= 32 candidates (one per warp or per CTA) in shared
+// memory, in every lane: (~0, -1) when none is a candidate.
+__device__ __forceinline__ void argmin_of(const uint64_t *key, const int32_t *slot, int n, int lane, uint64_t &k,
+                                          int32_t &sl)
+{
+    k = lane < n ? key[lane] : ~0ull;
+    sl = lane < n ? slot[lane] : -1;
+    warp_argmin(k, sl);
 }
 
 // A compile-time flag as a value (selects a specialisation of a generic lambda).
@@ -951,11 +1004,6 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         float anew = 0.f;          // the new token's score (rank 0)
         uint8_t anew_code = 0;     // INT8 scores: its code
         PoolDecision pd{-1, 0, -1, kEmptyKey};  // two-pool mode
-        // a held token is a candidate: sinks and the recent window excepted (H2O),
-        // or any held token, in the pool its flag names (two-pool)
-        auto candidate = [&](int ps) {
-            return pools ? ps >= 0 : (ps >= P.n_sink && ps <= P.p - P.n_recent);
-        };
         // The score pass over this CTA's slots [s_lo, s_lo + n_mine): every retained
         // score s <- keep * s + a (a: this step's probability, mean over the G heads,
         // from the logits and the factors fself), and, evicting, the lowest
@@ -991,18 +1039,22 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 if (evict) {
                     const int ps = apos[j];
                     if (GEN && (fill || pools) && ps < 0 && W.s_lo + j < emin) emin = W.s_lo + j;
-                    if (GEN ? candidate(ps) : (ps >= P.n_sink && ps <= P.p - P.n_recent)) {
-                        const uint64_t key =
-                            (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | static_cast<uint32_t>(ps);
-                        if (GEN && pools && apool[j] != 0) {
-                            if (key < best2) {
-                                best2 = key;
-                                bslot2 = W.s_lo + j;
+                    if (GEN && pools) {
+                        // two-pool: every held token is a candidate of the pool its flag names
+                        if (ps >= 0) {
+                            const uint64_t key = h2o_key(sc, ps);
+                            if (apool[j] != 0) {
+                                if (key < best2) {
+                                    best2 = key;
+                                    bslot2 = W.s_lo + j;
+                                }
+                            } else if (key < best) {
+                                best = key;
+                                bslot = W.s_lo + j;
                             }
-                        } else if (key < best) {
-                            best = key;
-                            bslot = W.s_lo + j;
                         }
+                    } else {
+                        h2o_fold(best, bslot, sc, ps, W.s_lo + j, P.n_sink, P.p, P.n_recent);
                     }
                 }
             }
@@ -1063,15 +1115,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     for (int j = tid; j < W.n_mine; j += kThreads) {
                         const float c = code(zbuf[j]);
                         static_cast<uint8_t *>(P.score)[unit * CS + W.s_lo + j] = static_cast<uint8_t>(c);
-                        const int ps = apos[j];
-                        if (evict && ps >= P.n_sink && ps <= P.p - P.n_recent) {
-                            const uint64_t key =
-                                (static_cast<uint64_t>(__float_as_uint(c * scl)) << 32) | static_cast<uint32_t>(ps);
-                            if (key < best) {
-                                best = key;
-                                bslot = W.s_lo + j;
-                            }
-                        }
+                        if (evict) h2o_fold(best, bslot, c * scl, apos[j], W.s_lo + j, P.n_sink, P.p, P.n_recent);
                     }
                     anew_code = static_cast<uint8_t>(code(a));
                     anew = code(a) * scl;
@@ -1101,17 +1145,16 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 __syncthreads();  // (B) candidates visible; every read of this unit's aux data is done
                 if (evict) {
                     // every warp reduces the warps' candidates itself
-                    uint64_t k = lane < kWarps ? M.wkey[lane] : ~0ull;
-                    int32_t sl = lane < kWarps ? M.wslot[lane] : -1;
-                    warp_argmin(k, sl);
+                    uint64_t k;
+                    int32_t sl;
+                    argmin_of(M.wkey, M.wslot, kWarps, lane, k, sl);
                     int32_t em = (fill || pools) ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
                     if (pools) {
-                        uint64_t k2 = lane < kWarps ? M.wkey2[lane] : ~0ull;
-                        int32_t sl2 = lane < kWarps ? M.wslot2[lane] : -1;
-                        warp_argmin(k2, sl2);
+                        uint64_t k2;
+                        int32_t sl2;
+                        argmin_of(M.wkey2, M.wslot2, kWarps, lane, k2, sl2);
                         if (P.n_active < P.C) em = min(em, P.n_active);  // the slots past the scanned ones are empty
-                        const uint64_t kn =
-                            (static_cast<uint64_t>(__float_as_uint(M.anew)) << 32) | static_cast<uint32_t>(P.p);
+                        const uint64_t kn = h2o_key(M.anew, P.p);
                         pd = pool_decide(P.recent_full != 0, P.hh_threshold, k, sl, k2, sl2, em, kn);
                         if (pd.dest == INT_MAX) {  // no room where the rule needs an empty slot
                             if (tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
@@ -1219,12 +1262,10 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 if (evict && warp == 0) {
                     // this CTA's candidates (and, filling, its lowest empty slot) to every
                     // CTA; rank 0's new-token score too
-                    uint64_t k = lane < kWarps ? M.wkey[lane] : ~0ull;
-                    int32_t sl = lane < kWarps ? M.wslot[lane] : -1;
-                    warp_argmin(k, sl);
-                    uint64_t k2 = lane < kWarps ? M.wkey2[lane] : ~0ull;
-                    int32_t sl2 = lane < kWarps ? M.wslot2[lane] : -1;
-                    if (pools) warp_argmin(k2, sl2);
+                    uint64_t k, k2 = ~0ull;
+                    int32_t sl, sl2 = -1;
+                    argmin_of(M.wkey, M.wslot, kWarps, lane, k, sl);
+                    if (pools) argmin_of(M.wkey2, M.wslot2, kWarps, lane, k2, sl2);
                     const int32_t em =
                         (fill || pools) ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
                     if (lane < S) {
@@ -1246,17 +1287,16 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             // --------------------------------------------------------- victim
             if (evict) {
                 cluster_sync();  // (2) every CTA's candidate is here
-                uint64_t k = lane < S ? M.xkey[b][lane] : ~0ull;
-                int32_t sl = lane < S ? M.xslot[b][lane] : -1;
-                warp_argmin(k, sl);
+                uint64_t k;
+                int32_t sl;
+                argmin_of(M.xkey[b], M.xslot[b], S, lane, k, sl);
                 int32_t em = (fill || pools) ? warp_min_s32(lane < S ? M.xempty[b][lane] : INT_MAX) : INT_MAX;
                 if (pools) {
-                    uint64_t k2 = lane < S ? M.xkey2[b][lane] : ~0ull;
-                    int32_t sl2 = lane < S ? M.xslot2[b][lane] : -1;
-                    warp_argmin(k2, sl2);
+                    uint64_t k2;
+                    int32_t sl2;
+                    argmin_of(M.xkey2[b], M.xslot2[b], S, lane, k2, sl2);
                     if (P.n_active < P.C) em = min(em, P.n_active);  // the slots past the scanned ones are empty
-                    const uint64_t kn =
-                        (static_cast<uint64_t>(__float_as_uint(M.xanew[b])) << 32) | static_cast<uint32_t>(P.p);
+                    const uint64_t kn = h2o_key(M.xanew[b], P.p);
                     pd = pool_decide(P.recent_full != 0, P.hh_threshold, k, sl, k2, sl2, em, kn);
                     if (pd.dest == INT_MAX) {  // no room where the rule needs an empty slot
                         if (rank == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
@@ -1333,6 +1373,35 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         for (int st = 0; st < NST; ++st)
             if (M.issued[st] > 0) mbar_wait(&M.full[st], (M.issued[st] - 1) & 1);
         if (M.aux_issued > 0) mbar_wait(&M.auxbar, (M.aux_issued - 1) & 1);
+    }
+}
+
+// The H2O eviction decision alone, on caller-supplied fp32 scores: for every
+// unit (one CTA), the candidate with the smallest (score, position) among
+// slots [0, n_active) -- the victim the fused decode epilogue would take with
+// these scores. Same candidate rule, key and reductions (h2o_fold,
+// warp_argmin, argmin_of) as that epilogue, same CTA shape.
+template <int kWarps> __global__ void __launch_bounds__(kWarps * 32) h2o_select_kernel(const SelectParams P)
+{
+    __shared__ uint64_t wkey[kWarps];
+    __shared__ int32_t wslot[kWarps];
+    const size_t unit = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t best = ~0ull;
+    int32_t bslot = -1;
+    for (int j = tid; j < P.n_active; j += kWarps * 32)
+        h2o_fold(best, bslot, P.score[unit * P.C + j], P.pos[unit * P.cstride + j], j, P.n_sink, P.p, P.n_recent);
+    warp_argmin(best, bslot);
+    if (lane == 0) {
+        wkey[warp] = best;
+        wslot[warp] = bslot;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        uint64_t k;
+        int32_t sl;
+        argmin_of(wkey, wslot, kWarps, lane, k, sl);
+        if (lane == 0) P.victim[unit] = sl;
     }
 }
 

@@ -35,6 +35,13 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), f"{n} declared in include/ but not exported"
 
 
+def test_internal_helpers_are_not_exported(L):
+    """The helpers shared between the library's own translation units stay
+    out of the C ABI."""
+    for n in ("kvevict_handle_device", "kvevict_prefill_scored_check", "kvevict_static_scratch_address"):
+        assert not hasattr(L, n), f"{n} is internal but exported"
+
+
 def _cfg(**kw):
     from kv_cache_eviction_decode_gb300._lib import Config
     base = dict(policy=0, n_sink=4, n_heavy=60, n_recent=64, budget=128, r=0, seed=1, batch=2, n_layers=3,
@@ -91,6 +98,8 @@ def test_null_handle_and_strerror(L):
     assert L.kvevict_checkpoint_restore(None, None, 0) == -1
     assert L.kvevict_probe_wait_timeout(None) == -1
     assert L.kvevict_score_scales(None, 0, None, 0) == -1
+    assert L.kvevict_select_victims(None, 0, None, None) == -1
+    assert L.kvevict_prefill_scored_static(None, 0, None, None, None, 1) == -1
     assert L.kvevict_strerror(0) == b"ok"
     assert L.kvevict_strerror(-2) == b"capacity exceeded"
     L.kvevict_destroy(None)
