@@ -171,6 +171,10 @@ typedef struct {
     int clusters;           /* clusters in the last decode launch's persistent grid (0 before any) */
     int tensor_cores;       /* 1 if the decode path uses the tensor cores (mma), 0 for CUDA cores */
     int ring_stages;        /* shared-memory ring stages of the last decode launch (32 slots of K or V each) */
+    int tail_split;         /* 1 if clusters split only their leftover units (kvevict_set_tail_split) */
+    int partials_alias;     /* 1 if the last decode launch wrote its warps' partial outputs over the logits */
+    double evicted_mass;    /* policies with scores: the stored scores of every token that left the cache,
+                               summed over layers and units in fp64 (kvevict_evicted_mass per unit) */
 } kvevict_stats;
 
 /* Bytes of device memory a handle with this configuration needs (cache,
@@ -381,6 +385,19 @@ int kvevict_checkpoint_restore(kvevict_t h, const void *src, size_t bytes);
  * (launch failure). */
 int kvevict_probe_wait_timeout(kvevict_t h);
 
+/* Evicted-mass ledger of `layer` (policies with scores, else INVALID_ARG):
+ * for every unit, the sum in fp64 of the stored cumulative scores of the
+ * tokens that left it through decode steps -- the victim of an H2O step, a
+ * released block (H2O_BLOCK), the token leaving the two pools (H2O_POOLS) --
+ * since the handle was created. With exact scores (no moving average, fp32
+ * storage) the retained scores plus this mass equal the mass the unit has
+ * received: one per decode step (the G query heads' mean of a softmax), plus
+ * what the prompt brought (kvevict_prefill_scored: the kept tokens' scores).
+ * dst [batch][n_kv_heads] fp64; same dst rules as kvevict_slot_positions.
+ * ("KV Cache 驱逐策略：从 LRU 到 H2O" names the evicted mass among the
+ * quantities to watch.) */
+int kvevict_evicted_mass(kvevict_t h, int layer, double *dst, int dst_is_device);
+
 /* INT8 score storage only (else INVALID_ARG): every unit's scale for `layer`,
  * its largest score / 255 after the last step (0 before the first);
  * dst [batch][n_kv_heads] fp32. Same dst rules as kvevict_slot_positions. */
@@ -413,6 +430,35 @@ int kvevict_layer_state(kvevict_t h, int layer, int *prompt_len, int *steps, int
  * A tuning knob: results do not depend on it beyond fp32 rounding order. */
 int kvevict_set_split(kvevict_t h, int split);
 
+/* Tail splitting of the decode launch (-1 automatic, the default; 0 off; 1
+ * on; a tuning knob like kvevict_set_split, results do not depend on it beyond
+ * fp32 rounding order). Automatic turns it on, at clusters of two, where one
+ * CTA per SM holds a whole unit and the units do not divide evenly over the
+ * SMs; setting it (0 or 1) keeps the current split.
+ * On, a cluster of `split` CTAs gives each CTA an equal number of its units to
+ * process alone and splits only the units left over (its unit count mod
+ * split) across all its CTAs, so that every resident CTA gets work and the
+ * grid's load differs by less than one unit between CTAs; only those
+ * leftover units pay for the cluster exchange. The persistent grid is then
+ * every cluster the GPU holds at once. A whole unit must fit one CTA's shared
+ * memory: INVALID_ARG otherwise, and with INT8 score storage. */
+int kvevict_set_tail_split(kvevict_t h, int on);
+
+/* Where the decode launch keeps its warps' partial outputs: -1 automatic
+ * (the default), 0 in an area of their own, 1 over the unit's logits once the
+ * score pass has read them, wherever they fit there (that frees shared memory
+ * for more ring stages and costs one barrier per unit; automatic takes it
+ * where it buys at least two stages). A tuning knob: results do not depend on
+ * it. INVALID_ARG outside -1..1. */
+int kvevict_set_partials_alias(kvevict_t h, int mode);
+
+/* L2 prefetch depth of the decode launch: each CTA keeps `tiles` more K/V
+ * tiles (32 slots each) on their way from HBM into L2 beyond the tiles its
+ * shared-memory ring holds, so a CTA keeps more bytes in flight than its
+ * shared memory can hold (0..64; 0, the default: no prefetch). A tuning knob:
+ * results do not depend on it. */
+int kvevict_set_l2_prefetch(kvevict_t h, int tiles);
+
 /* Decode arithmetic: 0 = automatic (tensor cores for bf16 caches, CUDA
  * cores for fp32), 1 = CUDA cores, 2 = tensor cores (bf16 only; mma.sync
  * m16n8k16 with 16 slots / 16 head_dim rows as M and the G query heads,
@@ -425,8 +471,9 @@ int kvevict_set_path(kvevict_t h, int path);
 
 /* At most this many shared-memory ring stages (32-slot K or V tiles) per CTA
  * in the decode launch; 0 = as many as the shared-memory budget allows (the
- * default). A tuning knob: results do not depend on it. INVALID_ARG outside
- * 4..32. */
+ * default). Kernels that run two CTAs per SM switch to one CTA per SM (twice
+ * the shared memory) when the request does not fit the two-CTA budget. A
+ * tuning knob: results do not depend on it. INVALID_ARG outside 4..32. */
 int kvevict_set_ring(kvevict_t h, int stages);
 
 /* Number of clusters in the decode launch's persistent grid (each cluster
@@ -435,6 +482,8 @@ int kvevict_set_ring(kvevict_t h, int stages);
  * kvevict_set_split; results do not depend on it. */
 int kvevict_set_clusters(kvevict_t h, int clusters);
 
+/* The handle's counters. For policies with scores it reads the evicted-mass
+ * ledgers from the device and so waits for the handle's stream. */
 int kvevict_get_stats(kvevict_t h, kvevict_stats *out);
 
 /* Waits for the stream, reads the device error word into *device_error (may

@@ -31,7 +31,8 @@ class Stats(ctypes.Structure):
     _fields_ = [("decode_steps", ctypes.c_int64), ("prefill_tokens", ctypes.c_int64),
                 ("evictions", ctypes.c_int64), ("cuts", ctypes.c_int64), ("split", ctypes.c_int),
                 ("capacity", ctypes.c_int), ("clusters", ctypes.c_int), ("tensor_cores", ctypes.c_int),
-                ("ring_stages", ctypes.c_int)]
+                ("ring_stages", ctypes.c_int), ("tail_split", ctypes.c_int),
+                ("partials_alias", ctypes.c_int), ("evicted_mass", ctypes.c_double)]
 
 
 class KVEvictError(RuntimeError):
@@ -69,6 +70,7 @@ def lib() -> ctypes.CDLL:
             L.kvevict_scores.argtypes = [P, I, P, I]
             L.kvevict_slot_pools.argtypes = [P, I, P, I]
             L.kvevict_score_scales.argtypes = [P, I, P, I]
+            L.kvevict_evicted_mass.argtypes = [P, I, P, I]
             L.kvevict_probe_wait_timeout.argtypes = [P]
             L.kvevict_select_victims.argtypes = [P, I, P, P]
             L.kvevict_checkpoint_bytes.argtypes = [P, ctypes.POINTER(SZ)]
@@ -78,6 +80,9 @@ def lib() -> ctypes.CDLL:
             L.kvevict_layer_state.argtypes = [P, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
             L.kvevict_set_split.argtypes = [P, I]
             L.kvevict_set_clusters.argtypes = [P, I]
+            L.kvevict_set_tail_split.argtypes = [P, I]
+            L.kvevict_set_l2_prefetch.argtypes = [P, I]
+            L.kvevict_set_partials_alias.argtypes = [P, I]
             L.kvevict_set_path.argtypes = [P, I]
             L.kvevict_set_ring.argtypes = [P, I]
             L.kvevict_get_stats.argtypes = [P, ctypes.POINTER(Stats)]
@@ -90,10 +95,10 @@ def lib() -> ctypes.CDLL:
                       "kvevict_prefill_scored", "kvevict_prefill_scored_static",
                       "kvevict_prefill_snapkv_workspace_bytes", "kvevict_prefill_snapkv", "kvevict_decode_step",
                       "kvevict_decode_step_host", "kvevict_decode_step_host_async", "kvevict_sync", "kvevict_slot_positions", "kvevict_scores", "kvevict_slot_pools",
-                      "kvevict_score_scales", "kvevict_probe_wait_timeout", "kvevict_select_victims", "kvevict_checkpoint_bytes",
+                      "kvevict_score_scales", "kvevict_evicted_mass", "kvevict_probe_wait_timeout", "kvevict_select_victims", "kvevict_checkpoint_bytes",
                       "kvevict_checkpoint_save", "kvevict_checkpoint_restore",
                       "kvevict_set_trace",
-                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_path", "kvevict_set_ring",
+                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_tail_split", "kvevict_set_l2_prefetch", "kvevict_set_partials_alias", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",
                       "kvevict_check"):
                 getattr(L, n).restype = I

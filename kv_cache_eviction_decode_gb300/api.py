@@ -242,6 +242,17 @@ class KVEvictCache:
         sets DEV_WAIT_TIMEOUT in the error word (read by check())."""
         check(self._L.kvevict_probe_wait_timeout(self.h), "kvevict_probe_wait_timeout")
 
+    def evicted_mass(self, layer: int, out: torch.Tensor | None = None) -> torch.Tensor:
+        """Every unit's evicted score mass (fp64, [batch][n_kv_heads])."""
+        shp = (self.B, self.Hkv)
+        if out is None:
+            out = torch.empty(shp, dtype=torch.float64, device=self.device)
+        on_dev = out.device.type == "cuda"
+        if on_dev:
+            self._dev(out, shp, "out", torch.float64)
+        check(self._L.kvevict_evicted_mass(self.h, layer, _ptr(out), 1 if on_dev else 0), "kvevict_evicted_mass")
+        return out
+
     def score_scales(self, layer: int, out: torch.Tensor | None = None) -> torch.Tensor:
         """INT8 score storage: every unit's scale (its largest score / 255)."""
         shp = (self.B, self.Hkv)
@@ -283,6 +294,20 @@ class KVEvictCache:
 
     def set_split(self, split: int) -> None:
         check(self._L.kvevict_set_split(self.h, split), "kvevict_set_split")
+
+    def set_tail_split(self, on) -> None:
+        """Clusters split only their leftover units; each CTA's others are whole
+        (True / False, or -1 for automatic)."""
+        mode = on if isinstance(on, int) and not isinstance(on, bool) else (1 if on else 0)
+        check(self._L.kvevict_set_tail_split(self.h, mode), "kvevict_set_tail_split")
+
+    def set_partials_alias(self, mode: int) -> None:
+        """-1 automatic, 0 own area, 1 the warps' partial outputs over the logits."""
+        check(self._L.kvevict_set_partials_alias(self.h, mode), "kvevict_set_partials_alias")
+
+    def set_l2_prefetch(self, tiles: int) -> None:
+        """K/V tiles each CTA prefetches into L2 ahead of its shared-memory ring."""
+        check(self._L.kvevict_set_l2_prefetch(self.h, tiles), "kvevict_set_l2_prefetch")
 
     def set_path(self, path: int) -> None:
         """0 automatic, 1 CUDA cores, 2 tensor cores (bf16 only)."""

@@ -65,6 +65,7 @@ struct Layout {
     size_t layer_pslots = 0;  // units * Cs (pos/score entries)
     size_t kv_layer_bytes = 0;
     size_t off_k = 0, off_v = 0, off_pos = 0, off_score = 0, off_pool = 0, off_free = 0, off_err = 0;
+    size_t off_ledger = 0;  // [L][B][Hkv] fp64 evicted score mass (policies with scores)
     size_t off_sq[2] = {}, off_sk[2] = {}, off_sv[2] = {}, off_so[2] = {};  // host-path staging, two slots
     size_t total = 0;
     size_t q_bytes = 0, kvtok_bytes = 0;  // one layer-step's q/out and k_new/v_new
@@ -150,6 +151,7 @@ Layout make_layout(const kvevict_config *c)
     L.off_pos = off; off = align_up(off + nl * L.layer_pslots * 4);
     L.off_score = off; if (scored(c->policy)) off = align_up(off + nl * L.layer_pslots * L.score_elem);
     L.off_qscale = off; if (c->score_int8) off = align_up(off + nl * L.units * 4);
+    L.off_ledger = off; if (scored(c->policy)) off = align_up(off + nl * L.units * 8);
     L.off_pool = off; off = align_up(off + nl * L.units * L.Ps);
     L.off_free = off;
     if (c->policy == KVEVICT_RANDOM || c->policy == KVEVICT_H2O_BLOCK) off = align_up(off + nl * L.units * c->r * 4);
@@ -191,10 +193,14 @@ struct kvevict_handle {
     int device = -1;  // the CUDA device holding `state`
     cudaStream_t stream = nullptr;
     int split = 1;
+    bool tail_split = false;  // clusters split only their leftover units (each CTA's others whole)
+    int tail_req = -1;        // tail splitting requested: -1 automatic, 0 off, 1 on
     int clusters_req = 0;  // persistent grid size in clusters; 0 = automatic
     int last_layer = -1;   // layer of the last kernel this handle queued (-1: none, or unknown)
     int path_req = 0;      // 0 automatic, 1 CUDA cores, 2 tensor cores
     int ring_req = 0;      // ring stages requested (0 = fill the shared-memory budget)
+    int l2_ahead = 0;      // tiles prefetched into L2 ahead of the decode ring
+    int alias_req = -1;    // warp partials over the logits: -1 automatic, 0 never, 1 where they fit
     bool use_mma = false;  // decode path in use
     std::vector<CUtensorMap> tmk, tmv;  // per layer (bf16 caches)
     std::vector<LayerState> layers;
@@ -222,8 +228,8 @@ struct kvevict_handle {
     }
     // decode kernel configured for (split, holes): function, shared memory, zcap
     struct Configured {
-        int split = 0, clusters_req = -1, ring_req = -1;
-        bool mma = false;
+        int split = 0, clusters_req = -1, ring_req = -1, alias_req = -2;
+        bool mma = false, tail_split = false, alias = false;
         DecodeKernelInfo ki{};
         size_t smem = 0;
         int zc = 0, nst = 0;
@@ -259,27 +265,53 @@ int n_aux_arrays(const kvevict_config &c, bool holes)
 bool holes_policy(const kvevict_config &c) { return c.policy == KVEVICT_RANDOM || c.policy == KVEVICT_H2O_POOLS; }
 
 constexpr size_t kMaxSmem = 227 * 1024;
+constexpr int kMaxL2Ahead = 64;  // tiles of L2 prefetch ahead of the decode ring
 
 // Ring stages filling the shared-memory budget of the kernel's target
 // occupancy (two CTAs per SM when its registers allow, else one).
-int ring_stages(const DecodeKernelInfo &ki, size_t fixed)
+// A ring request above what the two-CTA budget holds selects the one-CTA
+// budget (a deeper ring for one CTA per SM).
+int ring_stages(const DecodeKernelInfo &ki, size_t fixed, int ring_req = 0)
 {
     const size_t budget2 = 113 * 1024, budget1 = kMaxSmem;
-    const size_t budget = (ki.ctas_per_sm >= 2 && fixed + kMinStages * ki.stage_bytes <= budget2) ? budget2 : budget1;
+    bool two = ki.ctas_per_sm >= 2 && fixed + kMinStages * ki.stage_bytes <= budget2;
+    if (two && ring_req > 0 && fixed + static_cast<size_t>(ring_req) * ki.stage_bytes > budget2) two = false;
+    const size_t budget = two ? budget2 : budget1;
     if (fixed + kMinStages * static_cast<size_t>(ki.stage_bytes) > budget) return 0;
     return static_cast<int>(std::min<size_t>(kMaxStages, (budget - fixed) / ki.stage_bytes));
 }
 
-size_t decode_smem(const kvevict_handle *h, int S, bool holes, int *nst_out = nullptr)
+// Shared memory of the decode launch with clusters of S CTAs; with tail
+// splitting a CTA also holds whole units, so it is sized as at S = 1. The
+// warps' partial outputs get an area of their own, or are written over the
+// logits (alias): that costs one barrier per unit, and is taken automatically
+// where it fits and buys at least two more ring stages.
+size_t decode_smem(const kvevict_handle *h, int S, bool holes, int *nst_out = nullptr, bool tail = false,
+                   bool *alias_out = nullptr)
 {
     DecodeKernelInfo ki;
     if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, &ki)) return ~size_t(0);
-    const size_t fixed = ki.fixed_bytes(ki.zcap(max_slots_per_cta(h->L, S)), n_aux_arrays(h->cfg, holes));
-    int nst = ring_stages(ki, fixed);
-    if (h->ring_req > 0 && nst > 0) nst = std::min(nst, h->ring_req);
-    if (nst_out) *nst_out = nst;
-    if (nst == 0) return ~size_t(0);
-    return fixed + static_cast<size_t>(nst) * ki.stage_bytes;
+    const int zc = ki.zcap(max_slots_per_cta(h->L, tail ? 1 : S));
+    const int na = n_aux_arrays(h->cfg, holes);
+    size_t best = ~size_t(0);
+    int best_nst = 0;
+    bool best_alias = false;
+    for (int a = 0; a < 2; ++a) {
+        const bool alias = a == 1;
+        if (alias && (h->alias_req == 0 || !ki.alias_fits(zc))) continue;
+        if (!alias && h->alias_req == 1 && ki.alias_fits(zc)) continue;
+        const size_t fixed = ki.fixed_bytes(zc, na, alias);
+        int nst = ring_stages(ki, fixed, h->ring_req);
+        if (h->ring_req > 0 && nst > 0) nst = std::min(nst, h->ring_req);
+        if (nst == 0) continue;
+        if (alias && h->alias_req < 0 && best_nst > 0 && nst < best_nst + 2) continue;
+        best = fixed + static_cast<size_t>(nst) * ki.stage_bytes;
+        best_nst = nst;
+        best_alias = alias;
+    }
+    if (nst_out) *nst_out = best_nst;
+    if (alias_out) *alias_out = best_alias;
+    return best;
 }
 
 // CTAs per unit. The persistent kernel streams best with one CTA per unit: a
@@ -291,6 +323,7 @@ int auto_split(const kvevict_handle *h)
 {
     const Layout &L = h->L;
     const bool holes = holes_policy(h->cfg);
+    if (h->cfg.score_int8) return 1;  // INT8 scores need the unit's largest score in one CTA
     for (int S = 1; S <= kMaxSplit; S *= 2) {
         if (decode_smem(h, S, holes) > kMaxSmem) continue;
         if (S < 8 && static_cast<long long>(L.units) * S < 2LL * kSMs && L.C / (2 * S) >= 256) continue;
@@ -299,11 +332,38 @@ int auto_split(const kvevict_handle *h)
     return kMaxSplit;
 }
 
-int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInfo *ki, size_t *smem, int *zc, int *nst)
+// Tail splitting, automatically: where one CTA per SM holds a whole unit
+// (the kernel's shared memory or registers allow no second CTA) and the
+// whole-unit grid cannot give every SM the same number of units, clusters of
+// two CTAs split the leftover units, so every SM streams until the end
+// (measured on the GQA layer: 512 units on 152 SMs, 98 -> 93 us per launch).
+// Kernels at two CTAs per SM do not gain (their SMs already overlap two CTAs).
+void auto_tail(kvevict_handle *h)
+{
+    h->tail_split = false;
+    if (h->tail_req == 0 || h->cfg.score_int8) return;
+    const bool holes = holes_policy(h->cfg);
+    if (h->tail_req == 1) {
+        h->tail_split = decode_smem(h, h->split, holes, nullptr, true) <= kMaxSmem;
+        return;
+    }
+    DecodeKernelInfo ki;
+    if (h->split != 1 || !decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, &ki)) return;
+    const size_t smem1 = decode_smem(h, 1, holes);
+    const bool one_per_sm = ki.ctas_per_sm < 2 || smem1 > 113 * 1024;
+    const long long units = static_cast<long long>(h->L.units);
+    if (!one_per_sm || units <= kSMs || units % kSMs == 0) return;
+    if (decode_smem(h, 2, holes, nullptr, true) > kMaxSmem) return;
+    h->split = 2;
+    h->tail_split = true;
+}
+
+int configure_kernel(const kvevict_handle *h, int S, bool holes, DecodeKernelInfo *ki, size_t *smem, int *zc, int *nst,
+                     bool *alias)
 {
     if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, ki)) return KVEVICT_ERR_INVALID_ARG;
-    *zc = ki->zcap(max_slots_per_cta(h->L, S));
-    *smem = decode_smem(h, S, holes, nst);
+    *zc = ki->zcap(max_slots_per_cta(h->L, h->tail_split ? 1 : S));
+    *smem = decode_smem(h, S, holes, nst, h->tail_split, alias);
     if (*smem > kMaxSmem || *nst == 0) return KVEVICT_ERR_INVALID_ARG;
     cudaError_t e = cudaFuncSetAttribute(ki->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(*smem));
     if (e == cudaSuccess && S > 8) e = cudaFuncSetAttribute(ki->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -376,6 +436,10 @@ int pick_clusters(const kvevict_handle *h, int S, const DecodeKernelInfo &ki, si
         *clusters = std::min(h->clusters_req, units);
         return KVEVICT_OK;
     }
+    if (h->tail_split) {  // every resident cluster: the load differs by less than a unit between CTAs
+        *clusters = std::min(maxc, units);
+        return KVEVICT_OK;
+    }
     if (units <= maxc) {
         *clusters = units;
         return KVEVICT_OK;
@@ -424,6 +488,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     P.cstride = L.Cs;
     P.freelist_len = c.r;
     P.err = at<uint32_t>(h, L.off_err);
+    P.ledger = scored(c.policy) ? at<double>(h, L.off_ledger) + static_cast<size_t>(layer) * L.units : nullptr;
     P.C = L.C;
     P.p = ls.prompt_len + ls.t;
     P.n_sink = c.n_sink;
@@ -457,6 +522,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
                 bp.n_sink = c.n_sink;
                 bp.n_recent = c.n_recent;
                 bp.p = P.p;
+                bp.ledger = P.ledger;
                 bp.err = P.err;
                 int rc0 = cuda_status(launch_block_release(bp, static_cast<int>(L.units), h->stream));
                 if (rc0) return rc0;
@@ -522,8 +588,8 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
 
     auto &cfgd = h->configured[holes ? 1 : 0];
     if (cfgd.split != h->split || cfgd.clusters_req != h->clusters_req || cfgd.mma != h->use_mma ||
-        cfgd.ring_req != h->ring_req) {
-        int rc0 = configure_kernel(h, h->split, holes, &cfgd.ki, &cfgd.smem, &cfgd.zc, &cfgd.nst);
+        cfgd.ring_req != h->ring_req || cfgd.tail_split != h->tail_split || cfgd.alias_req != h->alias_req) {
+        int rc0 = configure_kernel(h, h->split, holes, &cfgd.ki, &cfgd.smem, &cfgd.zc, &cfgd.nst, &cfgd.alias);
         if (rc0) return rc0;
         rc0 = pick_clusters(h, h->split, cfgd.ki, cfgd.smem, &cfgd.clusters);
         if (rc0) return rc0;
@@ -531,13 +597,18 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
         cfgd.clusters_req = h->clusters_req;
         cfgd.mma = h->use_mma;
         cfgd.ring_req = h->ring_req;
+        cfgd.tail_split = h->tail_split;
+        cfgd.alias_req = h->alias_req;
     }
     const DecodeKernelInfo &ki = cfgd.ki;
     const size_t smem = cfgd.smem;
     int rc = KVEVICT_OK;
     P.split = h->split;
+    P.tail_split = h->tail_split ? 1 : 0;
     P.zcap = cfgd.zc;
     P.nst = cfgd.nst;
+    P.l2_ahead = h->l2_ahead;
+    P.part_alias = cfgd.alias ? 1 : 0;
     P.prefetch_early = (h->last_layer >= 0 && h->last_layer != layer) ? 1 : 0;
     if (h->use_mma) {
         static_assert(sizeof(CUtensorMap) == sizeof(TensorMapBytes), "tensor map size");
@@ -674,7 +745,10 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
         }
     }
     h->split = auto_split(h);
-    if (cfg->score_int8 && h->split > 1) {  // INT8 scores need one CTA per unit
+    auto_tail(h);
+    h->stats.tail_split = h->tail_split ? 1 : 0;
+    // INT8 scores need one CTA per unit: a unit must fit one CTA's shared memory
+    if (cfg->score_int8 && decode_smem(h, 1, holes_policy(*cfg)) > kMaxSmem) {
         delete h;
         return KVEVICT_ERR_INVALID_ARG;
     }
@@ -697,6 +771,8 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
         e = cudaMemsetAsync(h->state + L.off_score, 0, cfg->n_layers * L.layer_pslots * L.score_elem, h->stream);
     if (e == cudaSuccess && cfg->score_int8)
         e = cudaMemsetAsync(h->state + L.off_qscale, 0, cfg->n_layers * L.units * 4, h->stream);
+    if (e == cudaSuccess && scored(cfg->policy))
+        e = cudaMemsetAsync(h->state + L.off_ledger, 0, cfg->n_layers * L.units * 8, h->stream);
     if (e == cudaSuccess && L.Ps > 0)
         e = cudaMemsetAsync(h->state + L.off_pool, 0, cfg->n_layers * L.units * L.Ps, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
@@ -1361,6 +1437,18 @@ int kvevict_probe_wait_timeout(kvevict_t h)
     return cuda_status(launch_wait_timeout_probe(at<uint32_t>(h, h->L.off_err), h->stream));
 }
 
+int kvevict_evicted_mass(kvevict_t h, int layer, double *dst, int dst_is_device)
+{
+    if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    if (!scored(h->cfg.policy)) return KVEVICT_ERR_INVALID_ARG;
+    const size_t n = h->L.units;
+    cudaError_t e = cudaMemcpyAsync(dst, at<double>(h, h->L.off_ledger) + static_cast<size_t>(layer) * n, n * 8,
+                                    dst_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess && !dst_is_device) e = cudaStreamSynchronize(h->stream);
+    return cuda_status(e);
+}
+
 int kvevict_score_scales(kvevict_t h, int layer, float *dst, int dst_is_device)
 {
     if (!h || !dst) return KVEVICT_ERR_INVALID_ARG;
@@ -1415,13 +1503,53 @@ int kvevict_set_split(kvevict_t h, int split)
     if (!h) return KVEVICT_ERR_INVALID_ARG;
     if (split == 0) {
         h->split = auto_split(h);
+        auto_tail(h);
+        h->stats.tail_split = h->tail_split ? 1 : 0;
     } else {
         if (split < 1 || split > kMaxSplit || (split & (split - 1))) return KVEVICT_ERR_INVALID_ARG;
         if (split > 1 && h->cfg.score_int8) return KVEVICT_ERR_INVALID_ARG;  // one CTA per unit
-        if (decode_smem(h, split, holes_policy(h->cfg)) > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
+        // an explicit split keeps tail splitting only where it was asked for
+        const bool tail = h->tail_req == 1;
+        if (decode_smem(h, split, holes_policy(h->cfg), nullptr, tail) > kMaxSmem) return KVEVICT_ERR_INVALID_ARG;
         h->split = split;
+        h->tail_split = tail;
+        h->stats.tail_split = tail ? 1 : 0;
     }
     h->stats.split = h->split;
+    return KVEVICT_OK;
+}
+
+int kvevict_set_partials_alias(kvevict_t h, int mode)
+{
+    if (!h || mode < -1 || mode > 1) return KVEVICT_ERR_INVALID_ARG;
+    h->alias_req = mode;
+    return KVEVICT_OK;
+}
+
+int kvevict_set_l2_prefetch(kvevict_t h, int tiles)
+{
+    if (!h || tiles < 0 || tiles > kMaxL2Ahead) return KVEVICT_ERR_INVALID_ARG;
+    h->l2_ahead = tiles;
+    return KVEVICT_OK;
+}
+
+int kvevict_set_tail_split(kvevict_t h, int on)
+{
+    if (!h || on < -1 || on > 1) return KVEVICT_ERR_INVALID_ARG;
+    if (on == 1) {
+        if (h->cfg.score_int8) return KVEVICT_ERR_INVALID_ARG;  // INT8 scores: one CTA per unit
+        if (decode_smem(h, h->split, holes_policy(h->cfg), nullptr, true) > kMaxSmem)
+            return KVEVICT_ERR_INVALID_ARG;  // a whole unit does not fit one CTA
+    }
+    h->tail_req = on;
+    if (on >= 0) {
+        h->tail_split = on == 1;
+    } else {  // automatic: from the automatic split
+        h->split = auto_split(h);
+        auto_tail(h);
+        h->stats.split = h->split;
+    }
+    h->stats.tail_split = h->tail_split ? 1 : 0;
     return KVEVICT_OK;
 }
 
@@ -1461,9 +1589,19 @@ int kvevict_get_stats(kvevict_t h, kvevict_stats *out)
 {
     if (!h || !out) return KVEVICT_ERR_INVALID_ARG;
     *out = h->stats;
+    out->evicted_mass = 0.0;
+    if (scored(h->cfg.policy)) {  // the ledger of every layer and unit, summed on the host in fp64
+        std::vector<double> led(static_cast<size_t>(h->cfg.n_layers) * h->L.units);
+        cudaError_t e = cudaMemcpyAsync(led.data(), h->state + h->L.off_ledger, led.size() * 8,
+                                        cudaMemcpyDeviceToHost, h->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        if (e != cudaSuccess) return cuda_status(e);
+        for (double v : led) out->evicted_mass += v;
+    }
     out->clusters = h->configured[0].clusters ? h->configured[0].clusters : h->configured[1].clusters;
     out->tensor_cores = h->use_mma ? 1 : 0;
     out->ring_stages = h->configured[0].nst ? h->configured[0].nst : h->configured[1].nst;
+    out->partials_alias = (h->configured[0].nst ? h->configured[0].alias : h->configured[1].alias) ? 1 : 0;
     return KVEVICT_OK;
 }
 

@@ -240,6 +240,12 @@ __global__ void __launch_bounds__(256) block_release_kernel(const BlockReleasePa
     }
     __syncthreads();
     const int blk = chosen;
+    if (blk >= 0 && tid == 0 && P.ledger) {  // the released tokens' scores leave the cache
+        double m = 0.0;
+        for (int o = 0; o < P.bs; ++o) m += static_cast<double>(sc[blk * P.bs + o]);
+        P.ledger[unit] += m;
+    }
+    __syncthreads();  // the scores are read before they are cleared
     int32_t *posw = P.pos + unit * P.cstride;
     for (int o = tid; o < P.bs; o += blockDim.x) {
         P.freelist[unit * P.bs + o] = blk < 0 ? -1 : blk * P.bs + o;  // -1: the decode step drops its token

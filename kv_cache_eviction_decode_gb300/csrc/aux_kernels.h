@@ -53,6 +53,7 @@ struct BlockReleaseParams {
     void *kc, *vc;      // layer cache [B][Hkv][C][D]: freed rows are zeroed
     int row_bytes, C, cstride, bs;
     int n_sink, n_recent, p;  // p: position of the token the release makes room for
+    double *ledger;     // layer [B][Hkv]: evicted score mass, the released block's added
     uint32_t *err;
 };
 

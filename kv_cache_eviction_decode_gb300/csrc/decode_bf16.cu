@@ -9,7 +9,8 @@ template <int D, int G, bool H, bool MMA> DecodeKernelInfo info()
 {
     using L = DecodeLayout<__nv_bfloat16, D, G, MMA>;
     return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<__nv_bfloat16, D, G, H, MMA>),
-                            [](int zc, int n_aux) { return L::fixed_bytes(zc, n_aux); }, [](int n) { return L::zcap(n); },
+                            [](int zc, int n_aux, bool alias) { return L::fixed_bytes(zc, n_aux, alias); },
+                            [](int zc) { return L::alias_fits(zc); }, [](int n) { return L::zcap(n); },
                             L::kStageBytes, min_blocks<G, MMA>(), L::kThreads};
 }
 

@@ -10,7 +10,9 @@ namespace kvevict {
 
 struct DecodeKernelInfo {
     const void *fn;                    // __global__ decode_step_kernel<...>
-    size_t (*fixed_bytes)(int zcap, int n_aux);  // dynamic shared memory besides the ring (n_aux: 0, 1 or 2)
+    size_t (*fixed_bytes)(int zcap, int n_aux, bool alias);  // dynamic shared memory besides the ring (n_aux: 0..3;
+                                                             // alias: warp partials over the logits)
+    bool (*alias_fits)(int zcap);      // the warp partials fit in the logit area
     int (*zcap)(int max_slots_per_cta);
     int stage_bytes;   // one ring stage
     int ctas_per_sm;   // register-limited target occupancy (1 or 2)

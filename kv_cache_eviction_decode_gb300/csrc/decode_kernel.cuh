@@ -101,6 +101,7 @@ struct DecodeParams {
     const int32_t *freelist;  // [B][Hkv][freelist_len]
     int32_t *trace;      // [B][Hkv][4] or null: slot, evicted position, evicted score, new score
     uint32_t *err;
+    double *ledger;      // [B][Hkv] evicted score mass of this layer (policies with scores), or null
     int units;           // B * Hkv
     int C;
     int cstride;         // per-unit stride of pos/score (C rounded up to 4: 16-byte rows)
@@ -108,9 +109,13 @@ struct DecodeParams {
     int p;               // position of the new token
     int mode, dest_slot, freelist_idx, freelist_len;
     int n_sink, n_recent;
-    int split;           // CTAs per unit (cluster size)
+    int split;           // CTAs per cluster
+    int tail_split;      // 1: a cluster's CTAs process whole units alone and split only the units left over
+                         // (n_units mod split, processed first); 0: every unit is split over the cluster
     int zcap;            // per-head stride of the logit buffer (and aux slots)
     int nst;             // ring stages, kMinStages..kMaxStages
+    int l2_ahead;        // tiles prefetched into L2 ahead of the ring (0: none)
+    int part_alias;      // the warps' partial outputs are written over the logits (after the score pass)
     int prefetch_early;  // the launch before this one did not touch this layer: cache tiles may be
                          // fetched before the programmatic-dependency wait (inputs still after it)
     float scale_log2;    // log2(e) / sqrt(D)
@@ -214,17 +219,20 @@ template <typename T, int D, int G, bool MMA> struct DecodeLayout {
         int z = ((max_slots_per_cta + kTile - 1) / kTile) * kTile;
         return MMA ? z + 8 : (G > 1 ? z + kR : z);
     }
-    // Layout: [ring: nst stages][logits][warp partials][aux][misc].
+    // Layout: [ring: nst stages][logits][warp partials][aux][misc]. With
+    // `alias` the warp partials have no area of their own: they are written
+    // over the logits once every read of those is done (alias_fits: they fit).
     __host__ __device__ static size_t off_z(int nst) { return static_cast<size_t>(nst) * kStageBytes; }
     __host__ __device__ static size_t off_part(int zc, int nst) { return off_z(nst) + ((static_cast<size_t>(G) * zc * 4 + 127) / 128) * 128; }
+    __host__ __device__ static bool alias_fits(int zc) { return static_cast<size_t>(kPartBytes) <= static_cast<size_t>(G) * zc * 4; }
     // aux: the unit's slot positions, with scores (H2O) the cumulative scores,
     // and in two-pool mode the pool flags: n_arrays = 0 (none), 1, 2 or 3.
-    __host__ __device__ static size_t off_aux(int zc, int nst) { return off_part(zc, nst) + kPartBytes; }
+    __host__ __device__ static size_t off_aux(int zc, int nst, bool alias) { return off_part(zc, nst) + (alias ? 0 : kPartBytes); }
     __host__ __device__ static size_t aux_bytes(int zc) { return ((static_cast<size_t>(zc) * 4 + 15) / 16) * 16; }
-    __host__ __device__ static size_t off_misc(int zc, int n_arrays, int nst) { return off_aux(zc, nst) + n_arrays * aux_bytes(zc); }
-    __host__ __device__ static size_t bytes(int zc, int n_arrays, int nst) { return off_misc(zc, n_arrays, nst) + sizeof(Misc) + kSmemAlign; }
+    __host__ __device__ static size_t off_misc(int zc, int n_arrays, int nst, bool alias) { return off_aux(zc, nst, alias) + n_arrays * aux_bytes(zc); }
+    __host__ __device__ static size_t bytes(int zc, int n_arrays, int nst, bool alias) { return off_misc(zc, n_arrays, nst, alias) + sizeof(Misc) + kSmemAlign; }
     // Shared memory besides the ring.
-    __host__ __device__ static size_t fixed_bytes(int zc, int n_arrays) { return bytes(zc, n_arrays, 0); }
+    __host__ __device__ static size_t fixed_bytes(int zc, int n_arrays, bool alias) { return bytes(zc, n_arrays, 0, alias); }
 };
 
 // Butterfly transpose-reduce: lane L holds 32 partial sums v[0..31]; after
@@ -378,12 +386,34 @@ __device__ __forceinline__ PoolDecision pool_decide(bool recent_full, float thet
     return d;
 }
 
-// The CTA's share of one launch: which units, which tiles of each.
+// The CTA's share of one launch. Cluster c (of n_clusters, S CTAs each)
+// owns the units c, c + n_clusters, ... (n_units of them). The CTA works
+// through a sequence of items:
+//   - first n_split "split" items, units k = 0 .. n_split - 1 of the
+//     cluster, each divided over the cluster's S CTAs (this CTA: the slots
+//     [s_lo, s_hi), nt tiles) and combined through distributed shared memory;
+//   - then its "whole" units, k = n_split + j S + rank, each processed by
+//     this CTA alone (slots [0, n_all), ntw tiles).
+// Without tail splitting every unit is a split item (n_split = n_units; at
+// S = 1 a split item is the whole unit). With it (tail = 1), a cluster
+// splits only the n_units mod S units left over once every CTA has an equal
+// number of whole units: the grid's load then differs by less than one unit
+// between CTAs, and only those few units pay for the cluster exchange.
 struct Work {
     int cluster_id, n_clusters, n_units;  // units this cluster processes
-    int nt, s_lo, s_hi, n_mine;           // tiles / slot range per unit
-    int total_seq;                        // K and V tiles over all units
+    int S, rank;                          // cluster size, this CTA's rank
+    int n_split, n_items;                 // split items (first), all items of this CTA
+    int nt, s_lo, s_hi, n_mine;           // a split item: this CTA's tiles / slot range
+    int ntw, n_all;                       // a whole unit: its tiles / slots
+    int total_seq;                        // K and V tiles over all items
 };
+
+// Item i of the CTA: its unit.
+__device__ __forceinline__ size_t item_unit(const Work &W, int i)
+{
+    const int k = i < W.n_split ? i : W.n_split + (i - W.n_split) * W.S + W.rank;
+    return static_cast<size_t>(W.cluster_id) + static_cast<size_t>(k) * W.n_clusters;
+}
 
 // Tile s of the CTA's sequence: unit, K or V, which 32 slots.
 struct TileAt {
@@ -394,13 +424,23 @@ struct TileAt {
 
 __device__ __forceinline__ TileAt tile_at(const Work &W, int s)
 {
-    const int two_nt = 2 * W.nt;
-    const int i = s / two_nt, loc = s - i * two_nt;
+    const int split_seq = W.n_split * 2 * W.nt;
     TileAt t;
-    t.unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
-    t.is_k = loc < W.nt;
-    t.slot0 = W.s_lo + (t.is_k ? loc : loc - W.nt) * kTile;
-    t.rows = min(kTile, W.s_hi - t.slot0);
+    if (s < split_seq) {
+        const int two_nt = 2 * W.nt;
+        const int i = s / two_nt, loc = s - i * two_nt;
+        t.unit = item_unit(W, i);
+        t.is_k = loc < W.nt;
+        t.slot0 = W.s_lo + (t.is_k ? loc : loc - W.nt) * kTile;
+        t.rows = min(kTile, W.s_hi - t.slot0);
+    } else {
+        const int two_nt = 2 * W.ntw;
+        const int j = (s - split_seq) / two_nt, loc = (s - split_seq) - j * two_nt;
+        t.unit = item_unit(W, W.n_split + j);
+        t.is_k = loc < W.ntw;
+        t.slot0 = (t.is_k ? loc : loc - W.ntw) * kTile;
+        t.rows = min(kTile, W.n_all - t.slot0);
+    }
     return t;
 }
 
@@ -415,6 +455,12 @@ template <typename T, int D> struct BulkTileSource {
         const T *src = (t.is_k ? kc : vc) + (t.unit * C + t.slot0) * D;
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s_stream(stage, src, bytes, bar, l2_policy_evict_first());
+    }
+    // the same rows into L2 only
+    __device__ __forceinline__ void prefetch(const Work &W, int s) const
+    {
+        const TileAt t = tile_at(W, s);
+        bulk_prefetch_l2((t.is_k ? kc : vc) + (t.unit * C + t.slot0) * D, static_cast<uint32_t>(t.rows * D * sizeof(T)));
     }
 };
 
@@ -434,6 +480,15 @@ template <int D> struct TmaTileSource {
 #pragma unroll
         for (int b = 0; b < D / 64; ++b)
             tma_load_2d(reinterpret_cast<uint8_t *>(stage) + b * kTile * 128, tm, b * 64, row, bar, pol);
+    }
+    // the same boxes into L2 only
+    __device__ __forceinline__ void prefetch(const Work &W, int s) const
+    {
+        const TileAt t = tile_at(W, s);
+        const int row = static_cast<int>(t.unit * C + t.slot0);
+        const void *tm = t.is_k ? tmk : tmv;
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) tma_prefetch_2d(tm, b * 64, row);
     }
 };
 
@@ -458,14 +513,15 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     T *ring = reinterpret_cast<T *>(smem);
     const int zc = P.zcap;
     float *zbuf = reinterpret_cast<float *>(smem + L::off_z(NST));
-    float *part = reinterpret_cast<float *>(smem + L::off_part(zc, NST));
-    uint8_t *aux = smem + L::off_aux(zc, NST);
+    const bool alias = P.part_alias != 0;
+    float *part = alias ? zbuf : reinterpret_cast<float *>(smem + L::off_part(zc, NST));
+    uint8_t *aux = smem + L::off_aux(zc, NST, alias);
     const size_t auxb = L::aux_bytes(zc);
     // slot positions (and H2O scores, pool flags) are prefetched per unit only when used
     const bool need_aux = P.score != nullptr || HOLES;
     const bool pools = P.mode == kTwoPool;
     const int n_aux = pools ? 3 : (P.score != nullptr ? 2 : (HOLES ? 1 : 0));
-    auto &M = *reinterpret_cast<typename L::Misc *>(smem + L::off_misc(zc, n_aux, NST));
+    auto &M = *reinterpret_cast<typename L::Misc *>(smem + L::off_misc(zc, n_aux, NST, alias));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = static_cast<int>(cluster_rank());
@@ -484,6 +540,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     W.cluster_id = blockIdx.x / S;
     W.n_clusters = gridDim.x / S;
     W.n_units = W.cluster_id < P.units ? (P.units - W.cluster_id + W.n_clusters - 1) / W.n_clusters : 0;
+    W.S = S;
+    W.rank = rank;
     {
         const int nt_all = (P.n_active + kTile - 1) / kTile;
         const int t_lo = static_cast<int>(static_cast<long long>(rank) * nt_all / S);
@@ -492,8 +550,21 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         W.s_lo = t_lo * kTile;
         W.s_hi = min(t_hi * kTile, P.n_active);
         W.n_mine = max(0, W.s_hi - W.s_lo);
-        W.total_seq = W.n_units * 2 * W.nt;
+        W.ntw = nt_all;
+        W.n_all = P.n_active;
+        W.n_split = P.tail_split ? W.n_units % S : W.n_units;
+        W.n_items = W.n_split + (W.n_units - W.n_split) / S;
+        W.total_seq = W.n_split * 2 * W.nt + (W.n_items - W.n_split) * 2 * W.ntw;
     }
+    // item i's slots: [lo, lo + n) and the index of its aux copy among the
+    // items that copy any (a CTA with no slots of a split item copies none)
+    auto item_slots = [&](int i, int &lo, int &n) {
+        lo = i < W.n_split ? W.s_lo : 0;
+        n = i < W.n_split ? W.n_mine : W.n_all;
+    };
+    auto aux_index = [&](int i) {
+        return i < W.n_split ? (W.n_mine > 0 ? i : 0) : (W.n_mine > 0 ? W.n_split : 0) + (i - W.n_split);
+    };
     BulkTileSource<T, D> bulk_src{static_cast<const T *>(P.kc), static_cast<const T *>(P.vc), C};
     TmaTileSource<D> tma_src{&P.tmk, &P.tmv, C};
     auto issue_tile = [&](int s, int st) {
@@ -502,6 +573,15 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             tma_src.issue(W, s, reinterpret_cast<__nv_bfloat16 *>(stage), &M.full[st]);
         else
             bulk_src.issue(W, s, stage, &M.full[st]);
+    };
+    // Tile s into L2 ahead of its ring copy: tile s + nst + l2_ahead is
+    // prefetched when tile s is issued, so HBM sees l2_ahead more tiles in
+    // flight than the ring holds.
+    auto prefetch_tile = [&](int s) {
+        if (s < W.total_seq) {
+            if constexpr (MMA) tma_src.prefetch(W, s);
+            else bulk_src.prefetch(W, s);
+        }
     };
 
     if (tid == 0) {
@@ -523,29 +603,33 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     // Bulk copy of the i-th unit's slot positions (and scores) into the aux
     // area; it completes phase i of the aux mbarrier.
     auto issue_aux = [&](int i) {
-        const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
-        const uint32_t bytes = static_cast<uint32_t>(((W.n_mine * 4 + 15) / 16) * 16);
-        const uint32_t sbytes = P.score_int8   ? static_cast<uint32_t>(((W.n_mine + 15) / 16) * 16)
-                                : P.score_half ? static_cast<uint32_t>(((W.n_mine * 2 + 15) / 16) * 16)
+        const size_t unit = item_unit(W, i);
+        int lo, n;
+        item_slots(i, lo, n);
+        if (n <= 0) return;
+        const uint32_t bytes = static_cast<uint32_t>(((n * 4 + 15) / 16) * 16);
+        const uint32_t sbytes = P.score_int8   ? static_cast<uint32_t>(((n + 15) / 16) * 16)
+                                : P.score_half ? static_cast<uint32_t>(((n * 2 + 15) / 16) * 16)
                                                : bytes;
-        const uint32_t pbytes = pools ? static_cast<uint32_t>(((W.n_mine + 15) / 16) * 16) : 0u;
+        const uint32_t pbytes = pools ? static_cast<uint32_t>(((n + 15) / 16) * 16) : 0u;
         const uint32_t tx = (has_score ? bytes + sbytes : bytes) + pbytes;
         mbar_arrive_expect_tx(&M.auxbar, tx);
-        bulk_g2s(aux, P.pos + unit * CS + W.s_lo, bytes, &M.auxbar);
+        bulk_g2s(aux, P.pos + unit * CS + lo, bytes, &M.auxbar);
         if (has_score)
             bulk_g2s(aux + auxb,
                      static_cast<const uint8_t *>(P.score) +
-                         (unit * CS + W.s_lo) * (P.score_int8 ? 1 : (P.score_half ? 2 : 4)),
+                         (unit * CS + lo) * (P.score_int8 ? 1 : (P.score_half ? 2 : 4)),
                      sbytes,
                      &M.auxbar);
         if (pools)
-            bulk_g2s(aux + 2 * auxb, P.pool + unit * static_cast<size_t>(P.pstride) + W.s_lo, pbytes, &M.auxbar);
+            bulk_g2s(aux + 2 * auxb, P.pool + unit * static_cast<size_t>(P.pstride) + lo, pbytes, &M.auxbar);
         M.aux_issued++;
     };
 
     auto issue_first = [&]() {
         for (int s = 0; s < min(NST, W.total_seq); ++s) issue_tile(s, s);
-        if (need_aux && W.n_units > 0 && W.n_mine > 0) issue_aux(0);
+        for (int s = NST; s < NST + P.l2_ahead; ++s) prefetch_tile(s);
+        if (need_aux && W.n_items > 0) issue_aux(0);
         for (int s = 0; s < min(NST, W.total_seq); ++s) st_release_cta(&M.issued[s], 1u);
     };
     // This layer's cache (and positions/scores) can only be written by a
@@ -598,6 +682,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             const int st = s % NST;
             issue_tile(nx, st);
             st_release_cta(&M.issued[st], M.issued[st] + 1);  // after the arrive.expect_tx
+            if (P.l2_ahead > 0) prefetch_tile(nx + P.l2_ahead);
         }
     };
 
@@ -609,8 +694,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     constexpr int kHeadLanes = MMA ? 4 : R;  // lanes sharing one head's partials
 
     // Register prefetch of a unit's q (CUDA-core path: d-slices; mma path: A
-    // fragments) and, for rank 0 warp 0, the new token's key in the same
-    // layout.
+    // fragments) and, for warp 0, the new token's key in the same layout
+    // (used where this CTA is the unit's rank 0).
     constexpr int QG = MMA ? 1 : G, QE = MMA ? 1 : EPL, QK = MMA ? KSTEPS : 1;
     float qn[QG][QE];
     uint32_t qan[QK][2];
@@ -636,7 +721,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 } else {
                     qan[kk][0] = qan[kk][1] = 0u;
                 }
-                if (rank == 0 && warp == 0) {
+                if (warp == 0) {
                     kan[kk][0] = *reinterpret_cast<const uint32_t *>(kp + 16 * kk);
                     kan[kk][1] = *reinterpret_cast<const uint32_t *>(kp + 16 * kk + 8);
                 }
@@ -644,18 +729,25 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         } else {
 #pragma unroll
             for (int g = 0; g < G; ++g) load_f32<T, EPL>(qp + g * D + lane * EPL, qn[g]);
-            if (rank == 0 && warp == 0)
-                load_f32<T, EPL>(static_cast<const T *>(P.k_new) + u * D + lane * EPL, kn_next);
+            if (warp == 0) load_f32<T, EPL>(static_cast<const T *>(P.k_new) + u * D + lane * EPL, kn_next);
         }
         kpair_next = *reinterpret_cast<const TPair<T> *>(static_cast<const T *>(P.k_new) + u * D + dp);
         vpair_next = *reinterpret_cast<const TPair<T> *>(static_cast<const T *>(P.v_new) + u * D + dp);
         dest_next = P.mode == kFromFreeList ? P.freelist[u * P.freelist_len + P.freelist_idx] : P.dest_slot;
     };
-    if (W.n_units > 0) load_unit_inputs(static_cast<size_t>(W.cluster_id));
+    if (W.n_items > 0) load_unit_inputs(item_unit(W, 0));
 
-    for (int i = 0; i < W.n_units; ++i) {
-        const size_t unit = static_cast<size_t>(W.cluster_id) + static_cast<size_t>(i) * W.n_clusters;
-        const int seq0 = i * 2 * W.nt;
+    for (int i = 0; i < W.n_items; ++i) {
+        const size_t unit = item_unit(W, i);
+        // this item: split over the cluster (Si CTAs, this one rank ri) or
+        // this CTA's whole unit (Si = 1, ri = 0); its slots, tiles and first
+        // tile in the CTA's sequence
+        const bool split_item = i < W.n_split;
+        const int Si = split_item ? S : 1, ri = split_item ? rank : 0;
+        const int s_lo = split_item ? W.s_lo : 0, s_hi = split_item ? W.s_hi : W.n_all;
+        const int n_mine = split_item ? W.n_mine : W.n_all;
+        const int nt = split_item ? W.nt : W.ntw;
+        const int seq0 = split_item ? i * 2 * W.nt : W.n_split * 2 * W.nt + (i - W.n_split) * 2 * W.ntw;
         const int32_t *apos = reinterpret_cast<const int32_t *>(aux);
         const float *ascore = reinterpret_cast<const float *>(aux + auxb);
         const __half *ascore_h = reinterpret_cast<const __half *>(aux + auxb);
@@ -692,9 +784,9 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
 #pragma unroll
             for (int e = 0; e < EPL; ++e) kf_new[e] = kn_next[e];
         }
-        if (i + 1 < W.n_units) load_unit_inputs(unit + W.n_clusters);
+        if (i + 1 < W.n_items) load_unit_inputs(item_unit(W, i + 1));
         // the new token's logits (rank 0, warp 0)
-        if (rank == 0 && warp == 0) {
+        if (ri == 0 && warp == 0) {
             if constexpr (MMA) {
                 // lane (g, t) holds q[g][16kk + 2t + {0,1,8,9}] and the same
                 // coordinates of k_new: partial dot, then sum over t.
@@ -723,13 +815,13 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         // prefetched them waits for them exactly once
         bool aux_ready = false;
         auto wait_aux = [&]() {
-            if (aux_ready || W.n_mine == 0 || !need_aux) return;
+            if (aux_ready || n_mine == 0 || !need_aux) return;
             aux_ready = true;
             if (!ok || *abort_flag) {
                 ok = false;
                 return;
             }
-            if (!mbar_wait(&M.auxbar, i & 1)) {
+            if (!mbar_wait(&M.auxbar, aux_index(i) & 1)) {
                 atomicOr(P.err, KVEVICT_DEV_WAIT_TIMEOUT);
                 ok = false;
                 *abort_flag = 1;
@@ -740,12 +832,12 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         // ---------------------------------------------------------- K phase
         float mx = -INFINITY;   // max of this lane's head (mma path: head 2t)
         float mx1 = -INFINITY;  // mma path: head 2t + 1
-        for (int s_loc = warp; s_loc < W.nt; s_loc += kWarps) {
+        for (int s_loc = warp; s_loc < nt; s_loc += kWarps) {
             const int s = seq0 + s_loc;
             if (!wait_stage(s)) break;
             const T *tk = ring + static_cast<size_t>(s % NST) * kTile * D;
             const int base = s_loc * kTile;
-            const int rows = min(kTile, W.n_mine - base);
+            const int rows = min(kTile, n_mine - base);
             if constexpr (MMA) {
                 // S^T (32 slots x 8 heads) = K (32 x D) Q^T, two 16-slot
                 // m-tiles; fragment c = (slot g, heads 2t, 2t+1), (slot g+8, ...)
@@ -838,7 +930,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         if (warp == 0 && lane < G) {
             float m = -INFINITY;
             for (int w = 0; w < kWarps; ++w) m = fmaxf(m, M.wmax[w][lane]);
-            if (rank == 0) m = fmaxf(m, M.znew[lane]);
+            if (ri == 0) m = fmaxf(m, M.znew[lane]);
             M.m[lane] = m;
         }
         __syncthreads();
@@ -857,12 +949,12 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
         }
-        const int first_v = W.nt + ((warp - W.nt % kWarps) % kWarps + kWarps) % kWarps;
-        for (int s_loc = first_v; s_loc < 2 * W.nt; s_loc += kWarps) {
+        const int first_v = nt + ((warp - nt % kWarps) % kWarps + kWarps) % kWarps;
+        for (int s_loc = first_v; s_loc < 2 * nt; s_loc += kWarps) {
             const int s = seq0 + s_loc;
             if (!wait_stage(s)) break;
-            const int base = (s_loc - W.nt) * kTile;
-            const int rows = min(kTile, W.n_mine - base);
+            const int base = (s_loc - nt) * kTile;
+            const int rows = min(kTile, n_mine - base);
             const T *tv = ring + static_cast<size_t>(s % NST) * kTile * D;
             if constexpr (MMA) {
                 const uint32_t sb = smem_u32(tv);
@@ -950,24 +1042,28 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         for (int off = 1; off < kHeadLanes; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
         if (lane % kHeadLanes == 0 && lane_has_head) M.wsum[warp][g_lane] = lsum;
         // rank 0 adds the new token: p_new = 2^(z_new - m)
-        if (rank == 0 && tid < G) M.pnew[tid] = exp2f(M.znew[tid] - M.m[tid]);
-        // every warp's partial output, compact: part[warp][head][kPS]
-        if constexpr (MMA) {
-            // O^T fragment: (d = 16 md + g | + 8, heads 2t, 2t + 1)
+        if (ri == 0 && tid < G) M.pnew[tid] = exp2f(M.znew[tid] - M.m[tid]);
+        // every warp's partial output, compact: part[warp][head][kPS]; with
+        // `alias` over the logits, once the score pass has read them
+        auto write_partials = [&]() {
+            if constexpr (MMA) {
+                // O^T fragment: (d = 16 md + g | + 8, heads 2t, 2t + 1)
 #pragma unroll
-            for (int md = 0; md < D / 16; ++md)
+                for (int md = 0; md < D / 16; ++md)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = 2 * t4 + (e & 1), d = md * 16 + g_lane + (e >> 1) * 8;
-                    if (h < G) part[(warp * G + h) * kPS + d] = oacc[md][e];
-                }
-        } else {
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = 2 * t4 + (e & 1), d = md * 16 + g_lane + (e >> 1) * 8;
+                        if (h < G) part[(warp * G + h) * kPS + d] = oacc[md][e];
+                    }
+            } else {
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+                for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) part[(warp * G + g) * kPS + lane * EPL + e] = acc[g][e];
-        }
-        __syncthreads();  // (A) partials and p_new visible; every read of this unit's tiles is done
+                    for (int e = 0; e < EPL; ++e) part[(warp * G + g) * kPS + lane * EPL + e] = acc[g][e];
+            }
+        };
+        if (!alias) write_partials();
+        __syncthreads();  // (A) sums, p_new (and unaliased partials) visible; every read of this unit's tiles is done
 
         // This CTA's totals of head g: l_g = sum over the warps (+ p_new on
         // rank 0), o_g[d] likewise (+ p_new v_new[d] on rank 0). A thread
@@ -977,7 +1073,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             float l = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) l += M.wsum[w][g];
-            if (rank == 0) l += M.pnew[g];
+            if (ri == 0) l += M.pnew[g];
             return l;
         };
         auto cta_o = [&](int g, float &ox, float &oy) {
@@ -989,7 +1085,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 ox += v.x;
                 oy += v.y;
             }
-            if (rank == 0) {
+            if (ri == 0) {
                 ox = fmaf(M.pnew[g], E::to_f32(vpair.x), ox);
                 oy = fmaf(M.pnew[g], E::to_f32(vpair.y), oy);
             }
@@ -1018,11 +1114,11 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         auto score_pass = [&](auto gen, const float(&fself)[G], uint64_t &best, int32_t &bslot, uint64_t &best2,
                               int32_t &bslot2, int32_t &emin, float &qmax) {
             constexpr bool GEN = decltype(gen)::value;
-            for (int j = tid; j < W.n_mine; j += kThreads) {
+            for (int j = tid; j < n_mine; j += kThreads) {
                 float a = 0.f;
 #pragma unroll
                 for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
-                const size_t si = unit * CS + W.s_lo + j;
+                const size_t si = unit * CS + s_lo + j;
                 float sc;
                 if constexpr (GEN) {
                     if (P.score_int8) {
@@ -1038,7 +1134,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 }
                 if (evict) {
                     const int ps = apos[j];
-                    if (GEN && (fill || pools) && ps < 0 && W.s_lo + j < emin) emin = W.s_lo + j;
+                    if (GEN && (fill || pools) && ps < 0 && s_lo + j < emin) emin = s_lo + j;
                     if (GEN && pools) {
                         // two-pool: every held token is a candidate of the pool its flag names
                         if (ps >= 0) {
@@ -1046,33 +1142,36 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                             if (apool[j] != 0) {
                                 if (key < best2) {
                                     best2 = key;
-                                    bslot2 = W.s_lo + j;
+                                    bslot2 = s_lo + j;
                                 }
                             } else if (key < best) {
                                 best = key;
-                                bslot = W.s_lo + j;
+                                bslot = s_lo + j;
                             }
                         }
                     } else {
-                        h2o_fold(best, bslot, sc, ps, W.s_lo + j, P.n_sink, P.p, P.n_recent);
+                        h2o_fold(best, bslot, sc, ps, s_lo + j, P.n_sink, P.p, P.n_recent);
                     }
                 }
             }
         };
 
-        if (S == 1) {
+        if (Si == 1) {
             // ------------------------------ output, one CTA per unit: o / l
-            T *outp = static_cast<T *>(P.out) + unit * (G * D);
-            for (int jp = tid; jp < kPairs; jp += kThreads) {
-                const int g = (2 * jp) / D;
-                float ox, oy;
-                cta_o(g, ox, oy);
-                const float inv = 1.f / cta_l(g);
-                TPair<T> o2;
-                o2.x = E::from_f32(ox * inv);
-                o2.y = E::from_f32(oy * inv);
-                *reinterpret_cast<TPair<T> *>(outp + 2 * jp) = o2;
-            }
+            auto write_output = [&]() {
+                T *outp = static_cast<T *>(P.out) + unit * (G * D);
+                for (int jp = tid; jp < kPairs; jp += kThreads) {
+                    const int g = (2 * jp) / D;
+                    float ox, oy;
+                    cta_o(g, ox, oy);
+                    const float inv = 1.f / cta_l(g);
+                    TPair<T> o2;
+                    o2.x = E::from_f32(ox * inv);
+                    o2.y = E::from_f32(oy * inv);
+                    *reinterpret_cast<TPair<T> *>(outp + 2 * jp) = o2;
+                }
+            };
+            if (!alias) write_output();
             if (tid < G) {
                 const float l = cta_l(tid);
                 if (!(l > 0.f && l <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
@@ -1112,10 +1211,10 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                         const float c = fminf(rintf(v * inv), 255.f);
                         return c >= 0.f ? c : 0.f;
                     };
-                    for (int j = tid; j < W.n_mine; j += kThreads) {
+                    for (int j = tid; j < n_mine; j += kThreads) {
                         const float c = code(zbuf[j]);
-                        static_cast<uint8_t *>(P.score)[unit * CS + W.s_lo + j] = static_cast<uint8_t>(c);
-                        if (evict) h2o_fold(best, bslot, c * scl, apos[j], W.s_lo + j, P.n_sink, P.p, P.n_recent);
+                        static_cast<uint8_t *>(P.score)[unit * CS + s_lo + j] = static_cast<uint8_t>(c);
+                        if (evict) h2o_fold(best, bslot, c * scl, apos[j], s_lo + j, P.n_sink, P.p, P.n_recent);
                     }
                     anew_code = static_cast<uint8_t>(code(a));
                     anew = code(a) * scl;
@@ -1142,7 +1241,12 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                         M.wslot2[warp] = bslot2;
                     }
                 }
-                __syncthreads();  // (B) candidates visible; every read of this unit's aux data is done
+                __syncthreads();  // (B) candidates visible; every read of this unit's aux data and logits is done
+                if (alias) {
+                    write_partials();
+                    __syncthreads();
+                    write_output();
+                }
                 if (evict) {
                     // every warp reduces the warps' candidates itself
                     uint64_t k;
@@ -1172,34 +1276,43 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                         if (sl < 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
                     }
                 }
+            } else if (alias) {  // no score pass: every read of the logits was done by (A)
+                write_partials();
+                __syncthreads();
+                write_output();
             }
             // the next unit's positions/scores may come in
-            if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
+            if (tid == 0 && need_aux && i + 1 < W.n_items) issue_aux(i + 1);
             if (!evict) dest = dest_mine;
             writer = true;
         } else {
             // ------------------------------------------ cluster exchange
             // Every CTA pushes its (m, l) to all CTAs of the cluster and its
             // output partial to the CTA that owns those coordinates (CTA r
-            // owns the slice [r SL, (r + 1) SL), SL = G D / S), then all wait
-            // once. The buffers alternate between units: a CTA writes a
-            // peer's buffer of parity b again only after both passed this
-            // barrier of the next unit, when the peer has finished reading it.
+            // owns the slice [r SL, (r + 1) SL), SL = G D / S). Unaliased, both
+            // go before barrier (1); aliased, the output partials exist only
+            // after the score pass and go, with the eviction candidates,
+            // before barrier (2). The buffers alternate between units: a CTA
+            // writes a peer's buffer of parity b again only after both passed
+            // barrier (1) of the next unit, when the peer has finished reading it.
             const int b = i & 1;
             constexpr int GD = G * D;
             const int SL = GD / S;
-            for (int jp = tid; jp < kPairs; jp += kThreads) {
-                const int g = (2 * jp) / D;
-                float ox, oy;
-                cta_o(g, ox, oy);
-                const int j = 2 * jp, r = j / SL;
-                st_peer_f32x2(peer_addr(&M.xo[b][rank * SL + (j - r * SL)], r), make_float2(ox, oy));
-            }
+            auto push_partials = [&]() {
+                for (int jp = tid; jp < kPairs; jp += kThreads) {
+                    const int g = (2 * jp) / D;
+                    float ox, oy;
+                    cta_o(g, ox, oy);
+                    const int j = 2 * jp, r = j / SL;
+                    st_peer_f32x2(peer_addr(&M.xo[b][ri * SL + (j - r * SL)], r), make_float2(ox, oy));
+                }
+            };
+            if (!alias) push_partials();
             if (tid < G) {
                 const float2 ml = make_float2(M.m[tid], cta_l(tid));
-                for (int c = 0; c < S; ++c) st_peer_f32x2(peer_addr(&M.xml[b][rank][tid], c), ml);
+                for (int c = 0; c < S; ++c) st_peer_f32x2(peer_addr(&M.xml[b][ri][tid], c), ml);
             }
-            cluster_sync();  // (1) every CTA's (m, l) and partials are here
+            cluster_sync();  // (1) every CTA's (m, l) (and unaliased partials) are here
 
             // -------------------------------------------------------- combine
             if (tid < G) {
@@ -1210,7 +1323,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     const float2 ml = M.xml[b][c][tid];
                     if (ml.x != -INFINITY) lg += ml.y * exp2f(ml.x - mg);
                 }
-                if (rank == 0 && !(lg > 0.f && lg <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
+                if (ri == 0 && !(lg > 0.f && lg <= FLT_MAX)) atomicOr(P.err, KVEVICT_DEV_NONFINITE);
                 const float inv = 1.f / lg;
                 for (int c = 0; c < S; ++c) {
                     const float mc = M.xml[b][c][tid].x;
@@ -1218,8 +1331,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 }
             }
             __syncthreads();
-            {
-                const int i0 = rank * SL;
+            auto write_slice = [&]() {
+                const int i0 = ri * SL;
                 T *outp = static_cast<T *>(P.out) + unit * GD;
                 for (int k = tid; k < SL; k += kThreads) {
                     const int g = (i0 + k) / D;
@@ -1227,20 +1340,21 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     for (int c = 0; c < S; ++c) o = fmaf(M.xo[b][c * SL + k], M.fac[c][g], o);
                     outp[i0 + k] = E::from_f32(o);
                 }
-            }
+            };
+            if (!alias) write_slice();
 
             // ------------------------------------------ cumulative scores (H2O)
             if (has_score) {
                 wait_aux();
                 float fself[G];
 #pragma unroll
-                for (int g = 0; g < G; ++g) fself[g] = M.fac[rank][g] * (1.0f / G);
+                for (int g = 0; g < G; ++g) fself[g] = M.fac[ri][g] * (1.0f / G);
                 uint64_t best = ~0ull, best2 = ~0ull;
                 int32_t bslot = -1, bslot2 = -1, emin = INT_MAX;
                 float qmax = 0.f;  // (INT8 scores never reach a cluster)
                 if (general_scores) score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin, qmax);
                 else score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin, qmax);
-                if (rank == 0 && tid == 0) {
+                if (ri == 0 && tid == 0) {
                     float a = 0.f;
 #pragma unroll
                     for (int g = 0; g < G; ++g) a = fmaf(M.pnew[g], M.fac[0][g], a);
@@ -1269,24 +1383,33 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     const int32_t em =
                         (fill || pools) ? warp_min_s32(lane < kWarps ? M.wempty[lane] : INT_MAX) : INT_MAX;
                     if (lane < S) {
-                        st_peer_u64(peer_addr(&M.xkey[b][rank], lane), k);
-                        st_peer_s32(peer_addr(&M.xslot[b][rank], lane), sl);
-                        st_peer_s32(peer_addr(&M.xempty[b][rank], lane), em);
+                        st_peer_u64(peer_addr(&M.xkey[b][ri], lane), k);
+                        st_peer_s32(peer_addr(&M.xslot[b][ri], lane), sl);
+                        st_peer_s32(peer_addr(&M.xempty[b][ri], lane), em);
                         if (pools) {
-                            st_peer_u64(peer_addr(&M.xkey2[b][rank], lane), k2);
-                            st_peer_s32(peer_addr(&M.xslot2[b][rank], lane), sl2);
+                            st_peer_u64(peer_addr(&M.xkey2[b][ri], lane), k2);
+                            st_peer_s32(peer_addr(&M.xslot2[b][ri], lane), sl2);
                         }
                     }
-                    if (rank == 0 && lane == 0)
+                    if (ri == 0 && lane == 0)
                         for (int c = 0; c < S; ++c) st_peer_f32(peer_addr(&M.xanew[b], c), anew);
                 }
             }
+            if (alias) {
+                // every read of the logits is done: the score pass ended with a
+                // barrier, and without scores nothing read them after (A)
+                write_partials();
+                __syncthreads();
+                push_partials();
+                cluster_sync();  // (2) every CTA's partials (and candidates) are here
+                write_slice();
+            }
             // the next unit's positions/scores may come in
-            if (tid == 0 && need_aux && i + 1 < W.n_units && W.n_mine > 0) issue_aux(i + 1);
+            if (tid == 0 && need_aux && i + 1 < W.n_items) issue_aux(i + 1);
 
             // --------------------------------------------------------- victim
             if (evict) {
-                cluster_sync();  // (2) every CTA's candidate is here
+                if (!alias) cluster_sync();  // (2) every CTA's candidate is here
                 uint64_t k;
                 int32_t sl;
                 argmin_of(M.xkey[b], M.xslot[b], S, lane, k, sl);
@@ -1299,7 +1422,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                     const uint64_t kn = h2o_key(M.xanew[b], P.p);
                     pd = pool_decide(P.recent_full != 0, P.hh_threshold, k, sl, k2, sl2, em, kn);
                     if (pd.dest == INT_MAX) {  // no room where the rule needs an empty slot
-                        if (rank == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                        if (ri == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
                         pd.dest = -1;
                         pd.promote = -1;
                     }
@@ -1311,14 +1434,14 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 } else {
                     win_key = k;
                     dest = sl;
-                    if (sl < 0 && rank == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
+                    if (sl < 0 && ri == 0 && tid == 0) atomicOr(P.err, KVEVICT_DEV_NO_CANDIDATE);
                 }
                 // the CTA that attended the victim; a slot past the scanned ones: rank 0
-                writer = (dest >= W.s_lo && dest < W.s_hi) || (dest >= P.n_active && rank == 0);
+                writer = (dest >= s_lo && dest < s_hi) || (dest >= P.n_active && ri == 0);
                 if (has_score) anew = M.xanew[b];
             } else {
                 dest = dest_mine;
-                writer = rank == 0;
+                writer = ri == 0;
             }
         }
 
@@ -1332,12 +1455,15 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         // two-pool: the promotion record of the trace (-2: the new token itself)
         const int prec = pd.promote >= 0 ? pd.promote : (pd.new_pool ? -2 : -1);
         if (pools && tid == 0) {
-            const bool mine = S == 1 || (pd.promote >= W.s_lo && pd.promote < W.s_hi);
+            const bool mine = Si == 1 || (pd.promote >= s_lo && pd.promote < s_hi);
             if (pd.promote >= 0 && mine) P.pool[unit * P.pstride + pd.promote] = 1;
-            if (dest < 0 && rank == 0 && P.trace != nullptr)  // the new token itself left
-                reinterpret_cast<int4 *>(P.trace)[unit] = make_int4(
-                    -1, static_cast<int32_t>(static_cast<uint32_t>(win_key)),
-                    static_cast<int32_t>(static_cast<uint32_t>(win_key >> 32)), prec);
+            if (dest < 0 && ri == 0) {  // the new token itself left: its score leaves the cache
+                if (P.ledger) P.ledger[unit] += static_cast<double>(__uint_as_float(static_cast<uint32_t>(win_key >> 32)));
+                if (P.trace != nullptr)
+                    reinterpret_cast<int4 *>(P.trace)[unit] = make_int4(
+                        -1, static_cast<int32_t>(static_cast<uint32_t>(win_key)),
+                        static_cast<int32_t>(static_cast<uint32_t>(win_key >> 32)), prec);
+            }
         }
         if (writer && dest >= 0) {
             if (tid < D / 2) {
@@ -1349,6 +1475,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 // otherwise they are read only when a trace is kept
                 int32_t old_pos = static_cast<int32_t>(static_cast<uint32_t>(win_key));
                 float old_score = __uint_as_float(static_cast<uint32_t>(win_key >> 32));
+                // an evicted token's stored score leaves the cache: the ledger keeps it
+                if (evict && old_pos >= 0 && P.ledger) P.ledger[unit] += static_cast<double>(old_score);
                 if (!evict && P.trace != nullptr) {
                     old_pos = P.pos[unit * CS + dest];
                     // (INT8: the codes were rewritten above; the slot is an empty one, score 0)

@@ -63,10 +63,13 @@ class DeviceRun:
     score_snap: dict = field(default_factory=dict)  # layer -> {t: float32 [B, Hkv, C]}
     pool_snap: dict = field(default_factory=dict)   # layer -> {t: uint8 [B, Hkv, C]} (two-pool H2O)
     code_snap: dict = field(default_factory=dict)   # layer -> {t: uint8 [B, Hkv, C]} INT8 codes after step t
+    ledger: dict = field(default_factory=dict)      # layer -> float64 [B, Hkv] evicted mass after the last step
     scale_snap: dict = field(default_factory=dict)  # layer -> {t: float32 [B, Hkv]} INT8 scales after step t
     err: int = 0
     split: int = 0
     tensor_cores: int = 0
+    tail_split: int = 0
+    partials_alias: int = 0
 
 
 def host_inputs(w, units, n_steps, prompt_len):
@@ -77,7 +80,8 @@ def host_inputs(w, units, n_steps, prompt_len):
 
 def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, device, snap_steps=(),
             split: int | None = None, out_seqs=None, seed: int = 0, clusters: int | None = None,
-            interleave: bool = True, path: int | None = None) -> DeviceRun:
+            interleave: bool = True, path: int | None = None, tail_split: bool | None = None,
+            alias: int | None = None) -> DeviceRun:
     """Runs n_steps decode steps of the given layers at the workload's shape.
 
     interleave=True issues the steps token by token over the layers, as a
@@ -85,6 +89,10 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
     steps of one layer, then the next layer. INT8 score storage: the codes
     and scales are read after every step."""
     cache = KVEvictCache.from_workload(w, device=device)
+    if tail_split is not None:
+        cache.set_tail_split(tail_split)
+    if alias is not None:
+        cache.set_partials_alias(alias)
     if split:
         cache.set_split(split)
     if clusters:
@@ -96,7 +104,8 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
     gen = torch.Generator(device=device)
     gen.manual_seed(seed * 1000 + 17)
     st = cache.stats()
-    run = DeviceRun(split=st["split"], tensor_cores=st["tensor_cores"])
+    run = DeviceRun(split=st["split"], tensor_cores=st["tensor_cores"], tail_split=st["tail_split"])
+    first_step = [True]
     snap_steps = set(snap_steps)
     bufs = {}
     for layer in layers:
@@ -135,6 +144,9 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
     def step(layer, t):
         q, k, v, out, _, _ = bufs[layer]
         cache.decode_step(layer, q[t], k[t], v[t], out[t])
+        if first_step[0]:  # the launch configuration is known after the first step
+            run.partials_alias = cache.stats()["partials_alias"]
+            first_step[0] = False
         if int8:  # stored value = code * scale exactly: the code is the rounded ratio
             scl = cache.score_scales(layer)
             codes = torch.round(cache.scores(layer) / scl.clamp_min(1e-38)[..., None])
@@ -158,6 +170,8 @@ def run_gpu(w: Workload, layers, n_steps: int, inputs: dict, prompt_len: int, de
                 step(layer, t)
     run.err |= cache.check()
     for layer in layers:
+        if scored(w):
+            run.ledger[layer] = cache.evicted_mass(layer).cpu().numpy()
         q, k, v, out, trace, seqs = bufs.pop(layer)
         run.trace[layer] = trace.cpu().numpy()
         run.out[layer] = {s: out[:, s].float().cpu().numpy() for s in seqs}
@@ -320,6 +334,11 @@ def replay_unit(w: Workload, unit, x, run: DeviceRun, n_steps: int, out_steps=No
             rep.max_score_err = max(rep.max_score_err, e)
             assert e <= out_tol(w), f"{unit} step {t}: score error {e:.3e}"
         rep.steps += 1
+    if layer in run.ledger and rep.steps == n_steps:
+        # the GPU's evicted-mass ledger against the oracle's, after the last step
+        got, want = float(run.ledger[layer][seq, h]), u.evicted_mass
+        err = abs(got - want) / max(abs(want), 1.0) if w.dtype == DTYPE_BF16 else abs(got - want)
+        assert err <= out_tol(w), f"{unit}: evicted mass {got:.9g}, oracle {want:.9g}"
     return rep
 
 

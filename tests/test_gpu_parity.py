@@ -88,11 +88,81 @@ def test_persistent_loop_with_refills(cuda_device, policy, split, clusters, reco
     units = _all_units(w, [0])
     inputs = ls.host_inputs(w, units, T, w.prompt_len)
     run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=range(0, T, 9), split=split,
-                     clusters=clusters)
-    assert run.err == 0
+                     clusters=clusters, alias=0)
+    assert run.err == 0 and run.partials_alias == 0
     reps = ls.replay_all(w, units, inputs, run, T)
     print(f"persistent policy {policy} split {split} clusters {clusters}:", _report(reps))
     ls.record_ties(record_property, reps, max_near_ties=1)
+
+
+@pytest.mark.parametrize("policy,G,dtype,B,split,clusters,budget,P,alias", [
+    (configs.POLICY_H2O, 8, configs.DTYPE_BF16, 7, 2, 3, 96, 150, 0),     # tails of 0 and 1 unit
+    (configs.POLICY_H2O, 1, configs.DTYPE_BF16, 9, 4, 2, 96, 150, 0),     # 4 whole + 2 split per cluster
+    (configs.POLICY_H2O, 2, configs.DTYPE_F32, 5, 4, 3, 40, 20, 0),       # ranks with no tile; cache fills
+    (configs.POLICY_SINK_WINDOW, 4, configs.DTYPE_BF16, 11, 2, 5, 70, 90, 0),
+    (configs.POLICY_RANDOM, 4, configs.DTYPE_BF16, 7, 2, 3, 48, 60, 0),   # holes, free list, cuts
+    (configs.POLICY_H2O_POOLS, 2, configs.DTYPE_BF16, 7, 2, 3, 64, 40, 0),
+])
+def test_tail_split_lockstep(cuda_device, policy, G, dtype, B, split, clusters, budget, P, alias, record_property):
+    """Tail splitting: each CTA processes whole units alone and a cluster
+    splits only its leftover units. Clusters with and without a tail, ranks
+    with no tile of a split unit, the cache filling, Random's free list and
+    the two-pool decision in split units."""
+    kw = {configs.POLICY_H2O: dict(n_sink=2, n_heavy=budget - 2 - budget // 3, n_recent=budget // 3),
+          configs.POLICY_SINK_WINDOW: dict(n_sink=4, n_recent=budget - 4),
+          configs.POLICY_RANDOM: dict(budget=budget - 16, r=16, max_prompt=P),
+          configs.POLICY_H2O_POOLS: dict(n_heavy=budget // 2, n_recent=budget - budget // 2,
+                                         hh_threshold=0.012)}[policy]
+    kw.setdefault("budget", budget)
+    T = 90
+    w = _small(policy, dtype, G=G, d=128 if dtype == configs.DTYPE_BF16 else 64, B=B, L=1, prompt_len=P,
+               decode_steps=T, **kw)
+    units = _all_units(w, [0])
+    inputs = ls.host_inputs(w, units, T, P)
+    run = ls.run_gpu(w, [0], T, inputs, P, cuda_device, snap_steps=range(0, T, 6), split=split, clusters=clusters,
+                     tail_split=True, alias=alias)
+    assert run.err == 0 and run.split == split and run.tail_split == 1 and run.partials_alias == alias
+    reps = ls.replay_all(w, units, inputs, run, T)
+    print(f"tail split policy {policy} G={G} S={split} clusters={clusters}:", _report(reps))
+    ls.record_ties(record_property, reps, max_near_ties=1)
+    if policy == configs.POLICY_H2O:
+        ls.check_selector(w, run, 0, P)
+
+
+@pytest.mark.parametrize("policy,split,tail,G,dtype", [
+    (configs.POLICY_H2O, 1, False, 2, configs.DTYPE_F32),
+    (configs.POLICY_H2O, 1, False, 8, configs.DTYPE_BF16),
+    (configs.POLICY_H2O, 2, False, 4, configs.DTYPE_BF16),
+    (configs.POLICY_H2O, 2, True, 8, configs.DTYPE_BF16),
+    (configs.POLICY_SINK_WINDOW, 2, False, 2, configs.DTYPE_BF16),
+    (configs.POLICY_SINK_WINDOW, 1, False, 4, configs.DTYPE_F32),
+    (configs.POLICY_RANDOM, 2, False, 4, configs.DTYPE_BF16),
+    (configs.POLICY_RANDOM, 2, True, 2, configs.DTYPE_BF16),
+    (configs.POLICY_H2O_POOLS, 2, False, 2, configs.DTYPE_BF16),
+    (configs.POLICY_H2O_POOLS, 1, False, 2, configs.DTYPE_BF16)])
+def test_partials_over_logits_lockstep(cuda_device, policy, split, tail, G, dtype, record_property):
+    """The warps' partial outputs written over the logits after the score
+    pass (the layout that frees shared memory for ring stages), on units
+    large enough for them to fit (>= 544 slots per CTA at head_dim 64): one
+    CTA per unit, clusters, tail splitting; every policy's epilogue."""
+    C = 1216
+    kw = {configs.POLICY_H2O: dict(n_sink=4, n_heavy=C - 4 - 300, n_recent=300, budget=C, prompt_len=C + 30),
+          configs.POLICY_SINK_WINDOW: dict(n_sink=4, n_recent=C - 4, budget=C, prompt_len=C + 10),
+          configs.POLICY_RANDOM: dict(budget=64, r=16, max_prompt=C - 80, prompt_len=C - 80),
+          configs.POLICY_H2O_POOLS: dict(n_heavy=C // 2, n_recent=C - C // 2, budget=C, prompt_len=C - 20,
+                                         hh_threshold=0.0008)}[policy]
+    T = 100
+    w = _small(policy, dtype, G=G, d=64, B=3, L=1, decode_steps=T, **kw)
+    units = _all_units(w, [0])
+    inputs = ls.host_inputs(w, units, T, w.prompt_len)
+    run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=range(0, T, 10), split=split,
+                     clusters=5 if tail else None, tail_split=tail, alias=1)
+    assert run.err == 0 and run.split == split and run.partials_alias == 1
+    reps = ls.replay_all(w, units, inputs, run, T)
+    print(f"partials over logits policy {policy} S={split} tail={tail} G={G}:", _report(reps))
+    ls.record_ties(record_property, reps, max_near_ties=1)
+    if policy == configs.POLICY_H2O:
+        ls.check_selector(w, run, 0, w.prompt_len)
 
 
 @pytest.mark.parametrize("path", [1, 2])
@@ -386,6 +456,22 @@ def test_h2o_gqa_full_shape(cuda_device, record_property):
     assert run.err == 0
     reps = ls.replay_all(w, checked, inputs, run, T)
     print("h2o gqa full shape:", _report(reps), "split", run.split)
+    ls.record_ties(record_property, reps, max_near_ties=5)
+    assert ls.check_selector(w, run, 0, w.prompt_len) == len(snaps)
+
+
+def test_h2o_gqa_full_shape_tail_split(cuda_device, record_property):
+    """The GQA workload with tail splitting at clusters of two: every CTA of
+    the GPU processes whole units and the clusters split their leftover unit."""
+    w = configs.H2O_GQA
+    T = 160
+    checked = [(s, 0, h) for s in (0, 1, w.batch - 2, w.batch - 1) for h in range(w.n_kv_heads)]
+    inputs = ls.host_inputs(w, checked, T, w.prompt_len)
+    snaps = [0, 80, T - 1]
+    run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=snaps, split=2, tail_split=True)
+    assert run.err == 0 and run.split == 2 and run.tail_split == 1
+    reps = ls.replay_all(w, checked, inputs, run, T)
+    print("h2o gqa full shape, tail split:", _report(reps))
     ls.record_ties(record_property, reps, max_near_ties=5)
     assert ls.check_selector(w, run, 0, w.prompt_len) == len(snaps)
 

@@ -95,6 +95,23 @@ def test_int8_scores_lockstep(cuda_device, dtype, forget, record_property):
     assert ls.check_selector(w, run, 0, w.prompt_len) == sum(t >= w.budget - w.prompt_len for t in snaps)
 
 
+def test_int8_scores_partials_over_logits(cuda_device, record_property):
+    """INT8 scores with the warps' partial outputs written over the logits:
+    the code pass reads the updated scores from the logit area before the
+    partials overwrite it (units of 1200 slots, where they fit)."""
+    w = configs.Workload(name="int8_alias", policy=H2O, dtype=BF16, batch=2, n_layers=1, n_q_heads=8, n_kv_heads=4,
+                         head_dim=64, n_sink=4, n_heavy=896, n_recent=300, budget=1200, r=0, prompt_len=1230,
+                         decode_steps=0, seed=93, score_int8=True)
+    T = 60
+    units = [(s, 0, h) for s in range(w.batch) for h in range(w.n_kv_heads)]
+    inputs = ls.host_inputs(w, units, T, w.prompt_len)
+    run = ls.run_gpu(w, [0], T, inputs, w.prompt_len, cuda_device, snap_steps=range(0, T, 10), alias=1)
+    assert run.err == 0 and run.partials_alias == 1
+    reps = ls.replay_all(w, units, inputs, run, T)
+    n = ls.record_ties(record_property, reps, max_near_ties=0, max_midpoint_rate=1e-3)
+    print("int8, partials over logits:", n)
+
+
 def test_int8_codes_and_scales(cuda_device):
     """After decode steps every stored score is an integer code 0..255 times
     its unit's scale, and every unit holds code 255 (its largest score) until
