@@ -240,14 +240,25 @@ def steady_state(cache, w, device):
     return P
 
 
-def run_ours(args, w, rank, world, device):
+def run_ours(args, w, rank, world, device, steps=None, warmup=None, extras=True):
+    """Times `steps` token-steps (after `warmup` untimed) of the workload at
+    steady state. extras: also the isolated launch times, the end-to-end
+    host-buffer run and (two-pool H2O) the held fraction."""
     import torch
     from kv_cache_eviction_decode_gb300 import KVEvictCache, lib
 
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
     with torch.cuda.stream(stream):
         cache = KVEvictCache.from_workload(w, device=device, stream=stream)
+        if args.tail_split >= 0:
+            cache.set_tail_split(bool(args.tail_split))
+        if args.l2_ahead >= 0:
+            cache.set_l2_prefetch(args.l2_ahead)
+        if args.alias != -1:
+            cache.set_partials_alias(args.alias)
         if args.split:
             cache.set_split(args.split)
         if args.clusters:
@@ -270,7 +281,7 @@ def run_ours(args, w, rank, world, device):
             # the prompt leaves the recent pool only; the heavy-hitter pool fills with
             # the promotions of the next steps (held counts are read after timing)
             n_pre = 2 * w.capacity
-        n_win = args.warmup + args.steps
+        n_win = warmup + steps
         q, kn, vn = synth.device_window(w, P + n_pre, n_win, device)
         out = torch.empty((2, L, B, Hq, D), dtype=q.dtype, device=device)
         Lb = lib()
@@ -286,7 +297,7 @@ def run_ours(args, w, rank, world, device):
 
         for i in range(n_pre):  # Random: generated tokens up to the first cut
             token_step(i % n_win)
-        for s in range(args.warmup):
+        for s in range(warmup):
             token_step(s)
         stream.synchronize()
         launches_before = cache.stats()
@@ -295,7 +306,7 @@ def run_ours(args, w, rank, world, device):
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(device.index) as clk:
             ev0.record(stream)
-            for s in range(args.warmup, n_win):
+            for s in range(warmup, n_win):
                 token_step(s)
             ev1.record(stream)
             ev1.synchronize()
@@ -312,7 +323,7 @@ def run_ours(args, w, rank, world, device):
 
         # isolated kernel time of single launches (events around each), for context
         iso = []
-        for s in range(min(8, n_win)):
+        for s in range(min(8, n_win) if extras else 0):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             dec(h, s % L, q[s, s % L].data_ptr(), kn[s, s % L].data_ptr(), vn[s, s % L].data_ptr(),
@@ -323,7 +334,7 @@ def run_ours(args, w, rank, world, device):
 
         # end to end through the host-buffer C-ABI call
         e2e = None
-        if not args.no_e2e:
+        if extras and not args.no_e2e:
             qh = q[:2].cpu().pin_memory()
             kh = kn[:2].cpu().pin_memory()
             vh = vn[:2].cpu().pin_memory()
@@ -332,7 +343,7 @@ def run_ours(args, w, rank, world, device):
             # in on the copy stream while the previous step runs, output back), one
             # kvevict_sync per token-step: its outputs are on the host when it returns
             dech = Lb.kvevict_decode_step_host_async
-            n_e2e = max(2, min(args.steps, 10))
+            n_e2e = max(2, min(steps, 10))
             barrier(device)
             torch.cuda.synchronize(device)
             t0 = time.perf_counter()
@@ -356,7 +367,68 @@ def run_ours(args, w, rank, world, device):
         cache.close()
     return dict(dt_ms=dt_ms, clocks=clk.summary(), decode_launches=decode_launches, cut_launches=cut_launches,
                 iso_ms=iso, e2e=e2e, split=st["split"], clusters=st["clusters"], tensor_cores=st["tensor_cores"],
-                ring_stages=st["ring_stages"], held=held)
+                ring_stages=st["ring_stages"], held=held, tail_split=st["tail_split"],
+                partials_alias=st["partials_alias"])
+
+
+# ---------------------------------------------------------------------------
+# The score-keeping and Random workloads, measured beside the headline
+# ---------------------------------------------------------------------------
+
+# (alias, steps per repeat, repeats): the GQA layer is one ~0.1 ms launch per
+# step, so it is timed as several repeats, each on a fresh one-layer handle
+# (its own prompt; every repeat within the workload's 512 decode steps)
+EXTRA_WORKLOADS = (("h2o_mha", None, 1), ("h2o_gqa", 200, 5), ("random", None, 1), ("h2o_reasoning", None, 1))
+
+
+def workload_summary(w, r, steps):
+    """One workload's figures from a run_ours result."""
+    dt_s = r["dt_ms"] / 1e3
+    launches = max(1, r["decode_launches"])
+    avg = dt_s / launches
+    layer_bytes = traffic.steady_layer_step_bytes(w)
+    achieved = layer_bytes / avg / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    tr = profiled_traffic(w.name)
+    return {"tokens_per_s": w.batch * steps / dt_s, "layer_step_us": 1e6 * avg,
+            "algorithmic_bytes_per_launch": layer_bytes, "achieved_gbs": achieved, "peak_gbs": peak,
+            "peak_kind": peak_kind, "frac": achieved / peak, "frac_of_8TBs": achieved / 8000.0,
+            "dram_traffic_over_algorithmic": (tr / layer_bytes) if tr else None,
+            "steps": steps, "gpu_launches": r["decode_launches"] + r["cut_launches"],
+            "split": r["split"], "tail_split": bool(r["tail_split"]), "partials_alias": bool(r["partials_alias"]),
+            "clusters": r["clusters"], "ring_stages": r["ring_stages"], "clocks": r["clocks"]}
+
+
+def extra_workloads(args, rank, world, device):
+    """Every score-keeping configuration and Random at full shape, each with
+    its own clock record: per layer-step time, algorithmic bytes per launch,
+    fractions of the measured copy peak and of 8 TB/s, and the ncu DRAM bytes
+    over the algorithmic bytes where a capture of the current kernel exists."""
+    res = {}
+    for name, rep_steps, reps in EXTRA_WORKLOADS:
+        w = configs.get(name)
+        if reps == 1:
+            r = run_ours(args, w, rank, world, device, extras=False)
+            res[w.name] = workload_summary(w, r, args.steps)
+            continue
+        one = w.with_(n_layers=1)  # GQA: one layer; a fresh handle and prompt per repeat
+        runs = [run_ours(args, one, rank, world, device, steps=rep_steps, extras=False) for _ in range(reps)]
+        per = [workload_summary(one, r, rep_steps) for r in runs]
+        us = sorted(p["layer_step_us"] for p in per)
+        best = min(per, key=lambda p: p["layer_step_us"])
+        mid = sorted(per, key=lambda p: p["layer_step_us"])[len(per) // 2]
+        mhz = [p["clocks"]["sm_mhz"] for p in per if p["clocks"]["sm_mhz"] is not None]
+        e = dict(mid)
+        e.update({"repeats": reps, "steps_per_repeat": rep_steps, "layer_step_us_median": mid["layer_step_us"],
+                  "layer_step_us_min": best["layer_step_us"], "layer_step_us_all": us,
+                  "frac_min_time": best["frac"], "sm_mhz_median": statistics.median(mhz) if mhz else None,
+                  "clocks": {"sm_mhz": statistics.median(mhz) if mhz else None,
+                             "sm_max_mhz": max((p["clocks"]["sm_max_mhz"] or 0) for p in per) or None,
+                             "reasons": sorted({x for p in per for x in p["clocks"]["reasons"]}),
+                             "samples": sum(p["clocks"]["samples"] for p in per)},
+                  "note": "median repeat; each repeat a fresh one-layer handle, steps within the 512 decode steps"})
+        res[w.name] = e
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -709,10 +781,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--split", type=int, default=0)
     ap.add_argument("--clusters", type=int, default=0, help="persistent grid size in clusters (0 = automatic)")
+    ap.add_argument("--alias", type=int, default=-1,
+                    help="warp partial outputs over the logits: 1 where they fit, 0 never, -1 automatic")
+    ap.add_argument("--l2-ahead", type=int, default=-1,
+                    help="K/V tiles each CTA prefetches into L2 ahead of its ring (-1: automatic)")
+    ap.add_argument("--tail-split", type=int, default=-1,
+                    help="1: clusters split only their leftover units, 0: every unit split, -1: automatic")
     ap.add_argument("--path", type=int, default=0, help="0 automatic, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--ring", type=int, default=0, help="cap on ring stages per CTA (0 = fill shared memory)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the score-keeping and Random workloads measured beside the default one")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling captures only; the line then names it)")
@@ -799,7 +879,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded N(0,1) Q/K/V with hub and sink keys, generated on the device)",
         "config": dict(cfg, split=r["split"], clusters=r["clusters"], tensor_cores=bool(r["tensor_cores"]),
-                       ring_stages=r["ring_stages"],
+                       ring_stages=r["ring_stages"], tail_split=bool(r["tail_split"]),
+                       partials_alias=bool(r["partials_alias"]),
                        timing="CUDA events on the launching stream; no L2 flush needed"),
         "layer_step_us": 1e6 * avg_launch_s,
         "kernel_us_isolated": 1e3 * statistics.median(r["iso_ms"]) if r["iso_ms"] else None,
@@ -812,6 +893,9 @@ def main():
         "clocks": r["clocks"],
         "e2e": r["e2e"],
     }
+    headline = args.workload == "sink_window" and not args.layers and args.prompt < 0
+    if world == 1 and headline and not args.no_workloads:
+        out["workloads"] = extra_workloads(args, rank, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, threads, desc, _ = oracle_sample_rate(w, n_units=min(256, w.batch * w.n_kv_heads),
                                                     target_s=args.cpu_seconds)
