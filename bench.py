@@ -255,8 +255,6 @@ def run_ours(args, w, rank, world, device, steps=None, warmup=None, extras=True)
         cache = KVEvictCache.from_workload(w, device=device, stream=stream)
         if args.tail_split >= 0:
             cache.set_tail_split(bool(args.tail_split))
-        if args.l2_ahead >= 0:
-            cache.set_l2_prefetch(args.l2_ahead)
         if args.alias != -1:
             cache.set_partials_alias(args.alias)
         if args.split:
@@ -305,6 +303,10 @@ def run_ours(args, w, rank, world, device, steps=None, warmup=None, extras=True)
         torch.cuda.synchronize(device)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(device.index) as clk:
+            # the device sleeps ~1 ms before the start event, so the host has
+            # queued the first steps when it is recorded: the timed region
+            # holds the steps' own work, not the first launch's host latency
+            torch.cuda._sleep(2_000_000)
             ev0.record(stream)
             for s in range(warmup, n_win):
                 token_step(s)
@@ -783,8 +785,6 @@ def main():
     ap.add_argument("--clusters", type=int, default=0, help="persistent grid size in clusters (0 = automatic)")
     ap.add_argument("--alias", type=int, default=-1,
                     help="warp partial outputs over the logits: 1 where they fit, 0 never, -1 automatic")
-    ap.add_argument("--l2-ahead", type=int, default=-1,
-                    help="K/V tiles each CTA prefetches into L2 ahead of its ring (-1: automatic)")
     ap.add_argument("--tail-split", type=int, default=-1,
                     help="1: clusters split only their leftover units, 0: every unit split, -1: automatic")
     ap.add_argument("--path", type=int, default=0, help="0 automatic, 1 CUDA cores, 2 tensor cores")

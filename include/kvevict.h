@@ -441,23 +441,18 @@ int kvevict_set_split(kvevict_t h, int split);
  * grid's load differs by less than one unit between CTAs; only those
  * leftover units pay for the cluster exchange. The persistent grid is then
  * every cluster the GPU holds at once. A whole unit must fit one CTA's shared
- * memory: INVALID_ARG otherwise, and with INT8 score storage. */
+ * memory: INVALID_ARG otherwise, with INT8 score storage, and for kernels run two
+ * CTAs per SM (group sizes 1 and 2), which do not build it. */
 int kvevict_set_tail_split(kvevict_t h, int on);
 
 /* Where the decode launch keeps its warps' partial outputs: -1 automatic
  * (the default), 0 in an area of their own, 1 over the unit's logits once the
  * score pass has read them, wherever they fit there (that frees shared memory
  * for more ring stages and costs one barrier per unit; automatic takes it
- * where it buys at least two stages). A tuning knob: results do not depend on
+ * where it buys at least two stages). Kernels run two CTAs per SM (group sizes
+ * 1 and 2) always use their own area. A tuning knob: results do not depend on
  * it. INVALID_ARG outside -1..1. */
 int kvevict_set_partials_alias(kvevict_t h, int mode);
-
-/* L2 prefetch depth of the decode launch: each CTA keeps `tiles` more K/V
- * tiles (32 slots each) on their way from HBM into L2 beyond the tiles its
- * shared-memory ring holds, so a CTA keeps more bytes in flight than its
- * shared memory can hold (0..64; 0, the default: no prefetch). A tuning knob:
- * results do not depend on it. */
-int kvevict_set_l2_prefetch(kvevict_t h, int tiles);
 
 /* Decode arithmetic: 0 = automatic (tensor cores for bf16 caches, CUDA
  * cores for fp32), 1 = CUDA cores, 2 = tensor cores (bf16 only; mma.sync

@@ -81,7 +81,6 @@ def lib() -> ctypes.CDLL:
             L.kvevict_set_split.argtypes = [P, I]
             L.kvevict_set_clusters.argtypes = [P, I]
             L.kvevict_set_tail_split.argtypes = [P, I]
-            L.kvevict_set_l2_prefetch.argtypes = [P, I]
             L.kvevict_set_partials_alias.argtypes = [P, I]
             L.kvevict_set_path.argtypes = [P, I]
             L.kvevict_set_ring.argtypes = [P, I]
@@ -98,7 +97,7 @@ def lib() -> ctypes.CDLL:
                       "kvevict_score_scales", "kvevict_evicted_mass", "kvevict_probe_wait_timeout", "kvevict_select_victims", "kvevict_checkpoint_bytes",
                       "kvevict_checkpoint_save", "kvevict_checkpoint_restore",
                       "kvevict_set_trace",
-                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_tail_split", "kvevict_set_l2_prefetch", "kvevict_set_partials_alias", "kvevict_set_path", "kvevict_set_ring",
+                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_tail_split", "kvevict_set_partials_alias", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",
                       "kvevict_check"):
                 getattr(L, n).restype = I

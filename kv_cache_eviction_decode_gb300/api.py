@@ -305,10 +305,6 @@ class KVEvictCache:
         """-1 automatic, 0 own area, 1 the warps' partial outputs over the logits."""
         check(self._L.kvevict_set_partials_alias(self.h, mode), "kvevict_set_partials_alias")
 
-    def set_l2_prefetch(self, tiles: int) -> None:
-        """K/V tiles each CTA prefetches into L2 ahead of its shared-memory ring."""
-        check(self._L.kvevict_set_l2_prefetch(self.h, tiles), "kvevict_set_l2_prefetch")
-
     def set_path(self, path: int) -> None:
         """0 automatic, 1 CUDA cores, 2 tensor cores (bf16 only)."""
         check(self._L.kvevict_set_path(self.h, path), "kvevict_set_path")

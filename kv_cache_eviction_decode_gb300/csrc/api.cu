@@ -199,7 +199,6 @@ struct kvevict_handle {
     int last_layer = -1;   // layer of the last kernel this handle queued (-1: none, or unknown)
     int path_req = 0;      // 0 automatic, 1 CUDA cores, 2 tensor cores
     int ring_req = 0;      // ring stages requested (0 = fill the shared-memory budget)
-    int l2_ahead = 0;      // tiles prefetched into L2 ahead of the decode ring
     int alias_req = -1;    // warp partials over the logits: -1 automatic, 0 never, 1 where they fit
     bool use_mma = false;  // decode path in use
     std::vector<CUtensorMap> tmk, tmv;  // per layer (bf16 caches)
@@ -265,7 +264,6 @@ int n_aux_arrays(const kvevict_config &c, bool holes)
 bool holes_policy(const kvevict_config &c) { return c.policy == KVEVICT_RANDOM || c.policy == KVEVICT_H2O_POOLS; }
 
 constexpr size_t kMaxSmem = 227 * 1024;
-constexpr int kMaxL2Ahead = 64;  // tiles of L2 prefetch ahead of the decode ring
 
 // Ring stages filling the shared-memory budget of the kernel's target
 // occupancy (two CTAs per SM when its registers allow, else one).
@@ -296,10 +294,11 @@ size_t decode_smem(const kvevict_handle *h, int S, bool holes, int *nst_out = nu
     size_t best = ~size_t(0);
     int best_nst = 0;
     bool best_alias = false;
+    const bool can_alias = ki.flex && ki.alias_fits(zc);
     for (int a = 0; a < 2; ++a) {
         const bool alias = a == 1;
-        if (alias && (h->alias_req == 0 || !ki.alias_fits(zc))) continue;
-        if (!alias && h->alias_req == 1 && ki.alias_fits(zc)) continue;
+        if (alias && (h->alias_req == 0 || !can_alias)) continue;
+        if (!alias && h->alias_req == 1 && can_alias) continue;
         const size_t fixed = ki.fixed_bytes(zc, na, alias);
         int nst = ring_stages(ki, fixed, h->ring_req);
         if (h->ring_req > 0 && nst > 0) nst = std::min(nst, h->ring_req);
@@ -348,7 +347,8 @@ void auto_tail(kvevict_handle *h)
         return;
     }
     DecodeKernelInfo ki;
-    if (h->split != 1 || !decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, &ki)) return;
+    if (h->split != 1 || !decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes, h->use_mma, &ki) || !ki.flex)
+        return;
     const size_t smem1 = decode_smem(h, 1, holes);
     const bool one_per_sm = ki.ctas_per_sm < 2 || smem1 > 113 * 1024;
     const long long units = static_cast<long long>(h->L.units);
@@ -607,7 +607,6 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     P.tail_split = h->tail_split ? 1 : 0;
     P.zcap = cfgd.zc;
     P.nst = cfgd.nst;
-    P.l2_ahead = h->l2_ahead;
     P.part_alias = cfgd.alias ? 1 : 0;
     P.prefetch_early = (h->last_layer >= 0 && h->last_layer != layer) ? 1 : 0;
     if (h->use_mma) {
@@ -1526,18 +1525,14 @@ int kvevict_set_partials_alias(kvevict_t h, int mode)
     return KVEVICT_OK;
 }
 
-int kvevict_set_l2_prefetch(kvevict_t h, int tiles)
-{
-    if (!h || tiles < 0 || tiles > kMaxL2Ahead) return KVEVICT_ERR_INVALID_ARG;
-    h->l2_ahead = tiles;
-    return KVEVICT_OK;
-}
-
 int kvevict_set_tail_split(kvevict_t h, int on)
 {
     if (!h || on < -1 || on > 1) return KVEVICT_ERR_INVALID_ARG;
     if (on == 1) {
         if (h->cfg.score_int8) return KVEVICT_ERR_INVALID_ARG;  // INT8 scores: one CTA per unit
+        DecodeKernelInfo ki;
+        if (!decode_kernel(h->cfg.dtype, h->cfg.head_dim, h->L.G, holes_policy(h->cfg), h->use_mma, &ki) || !ki.flex)
+            return KVEVICT_ERR_INVALID_ARG;  // built into the one-CTA-per-SM kernels only
         if (decode_smem(h, h->split, holes_policy(h->cfg), nullptr, true) > kMaxSmem)
             return KVEVICT_ERR_INVALID_ARG;  // a whole unit does not fit one CTA
     }

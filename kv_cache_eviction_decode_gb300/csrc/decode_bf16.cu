@@ -11,7 +11,7 @@ template <int D, int G, bool H, bool MMA> DecodeKernelInfo info()
     return DecodeKernelInfo{reinterpret_cast<const void *>(&decode_step_kernel<__nv_bfloat16, D, G, H, MMA>),
                             [](int zc, int n_aux, bool alias) { return L::fixed_bytes(zc, n_aux, alias); },
                             [](int zc) { return L::alias_fits(zc); }, [](int n) { return L::zcap(n); },
-                            L::kStageBytes, min_blocks<G, MMA>(), L::kThreads};
+                            L::kStageBytes, min_blocks<G, MMA>(), L::kThreads, flex_layout<G, MMA>()};
 }
 
 template <int D, bool H, bool MMA> bool pick_g(int G, DecodeKernelInfo *out)

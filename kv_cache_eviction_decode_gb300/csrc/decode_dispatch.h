@@ -17,6 +17,7 @@ struct DecodeKernelInfo {
     int stage_bytes;   // one ring stage
     int ctas_per_sm;   // register-limited target occupancy (1 or 2)
     int threads;       // CTA size
+    bool flex;         // tail splitting and partials over the logits are built in
 };
 
 // dtype: 0 fp32, 1 bf16; mma: the tensor-core path (bf16 only). Returns

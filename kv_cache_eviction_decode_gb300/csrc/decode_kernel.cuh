@@ -114,7 +114,6 @@ struct DecodeParams {
                          // (n_units mod split, processed first); 0: every unit is split over the cluster
     int zcap;            // per-head stride of the logit buffer (and aux slots)
     int nst;             // ring stages, kMinStages..kMaxStages
-    int l2_ahead;        // tiles prefetched into L2 ahead of the ring (0: none)
     int part_alias;      // the warps' partial outputs are written over the logits (after the score pass)
     int prefetch_early;  // the launch before this one did not touch this layer: cache tiles may be
                          // fetched before the programmatic-dependency wait (inputs still after it)
@@ -332,6 +331,16 @@ __device__ __forceinline__ void argmin_of(const uint64_t *key, const int32_t *sl
     warp_argmin(k, sl);
 }
 
+// Adds an evicted token's stored score to its unit's fp64 ledger. One thread
+// per unit and step adds, and steps of a layer run in stream order, so the
+// sum is deterministic; the reduction is issued without waiting for it
+// (a plain load-add-store would hold the thread, and at the next barrier its
+// CTA, for a global load's latency).
+__device__ __forceinline__ void ledger_add(double *slot, float v)
+{
+    asm volatile("red.relaxed.gpu.global.add.f64 [%0], %1;" ::"l"(slot), "d"(static_cast<double>(v)) : "memory");
+}
+
 // A compile-time flag as a value (selects a specialisation of a generic lambda).
 template <bool B> struct Flag {
     static constexpr bool value = B;
@@ -422,11 +431,11 @@ struct TileAt {
     int slot0, rows;
 };
 
-__device__ __forceinline__ TileAt tile_at(const Work &W, int s)
+template <bool FLEX> __device__ __forceinline__ TileAt tile_at(const Work &W, int s)
 {
     const int split_seq = W.n_split * 2 * W.nt;
     TileAt t;
-    if (s < split_seq) {
+    if (!FLEX || s < split_seq) {
         const int two_nt = 2 * W.nt;
         const int i = s / two_nt, loc = s - i * two_nt;
         t.unit = item_unit(W, i);
@@ -445,34 +454,28 @@ __device__ __forceinline__ TileAt tile_at(const Work &W, int s)
 }
 
 // CUDA-core path: one contiguous bulk copy per tile (only the valid rows).
-template <typename T, int D> struct BulkTileSource {
+template <typename T, int D, bool FLEX> struct BulkTileSource {
     const T *kc, *vc;
     size_t C;
     __device__ __forceinline__ void issue(const Work &W, int s, T *stage, uint64_t *bar) const
     {
-        const TileAt t = tile_at(W, s);
+        const TileAt t = tile_at<FLEX>(W, s);
         const uint32_t bytes = static_cast<uint32_t>(t.rows * D * sizeof(T));
         const T *src = (t.is_k ? kc : vc) + (t.unit * C + t.slot0) * D;
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s_stream(stage, src, bytes, bar, l2_policy_evict_first());
-    }
-    // the same rows into L2 only
-    __device__ __forceinline__ void prefetch(const Work &W, int s) const
-    {
-        const TileAt t = tile_at(W, s);
-        bulk_prefetch_l2((t.is_k ? kc : vc) + (t.unit * C + t.slot0) * D, static_cast<uint32_t>(t.rows * D * sizeof(T)));
     }
 };
 
 // Tensor-core path: D/64 tensor-map boxes of 32 rows x 64 bf16 per tile,
 // 128-byte swizzled. A box always moves 32 full rows (rows past the unit's
 // range belong to the next unit or are zero-filled past the tensor's end).
-template <int D> struct TmaTileSource {
+template <int D, bool FLEX> struct TmaTileSource {
     const void *tmk, *tmv;
     size_t C;
     __device__ __forceinline__ void issue(const Work &W, int s, __nv_bfloat16 *stage, uint64_t *bar) const
     {
-        const TileAt t = tile_at(W, s);
+        const TileAt t = tile_at<FLEX>(W, s);
         const int row = static_cast<int>(t.unit * C + t.slot0);
         const void *tm = t.is_k ? tmk : tmv;
         const uint64_t pol = l2_policy_evict_first();
@@ -481,20 +484,16 @@ template <int D> struct TmaTileSource {
         for (int b = 0; b < D / 64; ++b)
             tma_load_2d(reinterpret_cast<uint8_t *>(stage) + b * kTile * 128, tm, b * 64, row, bar, pol);
     }
-    // the same boxes into L2 only
-    __device__ __forceinline__ void prefetch(const Work &W, int s) const
-    {
-        const TileAt t = tile_at(W, s);
-        const int row = static_cast<int>(t.unit * C + t.slot0);
-        const void *tm = t.is_k ? tmk : tmv;
-#pragma unroll
-        for (int b = 0; b < D / 64; ++b) tma_prefetch_2d(tm, b * 64, row);
-    }
 };
 
 // Two CTAs per SM (registers <= 128) for G <= 2; for larger G shared memory
 // holds one CTA and the registers are left free.
-template <int G, bool MMA> constexpr int min_blocks() { return G <= 2 ? 2 : 1; }
+template <int G, bool MMA> __host__ __device__ constexpr int min_blocks() { return G <= 2 ? 2 : 1; }
+// Tail splitting and partials over the logits are built into the kernels
+// that run one CTA per SM only: the two-CTA kernels (G <= 2) gain nothing from
+// them (measured) and run at the 128-register limit, where the extra state
+// cost them about 2% per launch.
+template <int G, bool MMA> __host__ __device__ constexpr bool flex_layout() { return min_blocks<G, MMA>() == 1; }
 
 template <typename T, int D, int G, bool HOLES, bool MMA>
 __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA>()))
@@ -513,7 +512,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     T *ring = reinterpret_cast<T *>(smem);
     const int zc = P.zcap;
     float *zbuf = reinterpret_cast<float *>(smem + L::off_z(NST));
-    const bool alias = P.part_alias != 0;
+    constexpr bool kFlex = flex_layout<G, MMA>();
+    const bool alias = kFlex && P.part_alias != 0;
     float *part = alias ? zbuf : reinterpret_cast<float *>(smem + L::off_part(zc, NST));
     uint8_t *aux = smem + L::off_aux(zc, NST, alias);
     const size_t auxb = L::aux_bytes(zc);
@@ -552,7 +552,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         W.n_mine = max(0, W.s_hi - W.s_lo);
         W.ntw = nt_all;
         W.n_all = P.n_active;
-        W.n_split = P.tail_split ? W.n_units % S : W.n_units;
+        W.n_split = (kFlex && P.tail_split) ? W.n_units % S : W.n_units;
         W.n_items = W.n_split + (W.n_units - W.n_split) / S;
         W.total_seq = W.n_split * 2 * W.nt + (W.n_items - W.n_split) * 2 * W.ntw;
     }
@@ -565,8 +565,8 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
     auto aux_index = [&](int i) {
         return i < W.n_split ? (W.n_mine > 0 ? i : 0) : (W.n_mine > 0 ? W.n_split : 0) + (i - W.n_split);
     };
-    BulkTileSource<T, D> bulk_src{static_cast<const T *>(P.kc), static_cast<const T *>(P.vc), C};
-    TmaTileSource<D> tma_src{&P.tmk, &P.tmv, C};
+    BulkTileSource<T, D, kFlex> bulk_src{static_cast<const T *>(P.kc), static_cast<const T *>(P.vc), C};
+    TmaTileSource<D, kFlex> tma_src{&P.tmk, &P.tmv, C};
     auto issue_tile = [&](int s, int st) {
         T *stage = ring + static_cast<size_t>(st) * kTile * D;
         if constexpr (MMA)
@@ -574,15 +574,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         else
             bulk_src.issue(W, s, stage, &M.full[st]);
     };
-    // Tile s into L2 ahead of its ring copy: tile s + nst + l2_ahead is
-    // prefetched when tile s is issued, so HBM sees l2_ahead more tiles in
-    // flight than the ring holds.
-    auto prefetch_tile = [&](int s) {
-        if (s < W.total_seq) {
-            if constexpr (MMA) tma_src.prefetch(W, s);
-            else bulk_src.prefetch(W, s);
-        }
-    };
+
 
     if (tid == 0) {
         for (int i = 0; i < NST; ++i) {
@@ -628,7 +620,6 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
 
     auto issue_first = [&]() {
         for (int s = 0; s < min(NST, W.total_seq); ++s) issue_tile(s, s);
-        for (int s = NST; s < NST + P.l2_ahead; ++s) prefetch_tile(s);
         if (need_aux && W.n_items > 0) issue_aux(0);
         for (int s = 0; s < min(NST, W.total_seq); ++s) st_release_cta(&M.issued[s], 1u);
     };
@@ -682,7 +673,6 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             const int st = s % NST;
             issue_tile(nx, st);
             st_release_cta(&M.issued[st], M.issued[st] + 1);  // after the arrive.expect_tx
-            if (P.l2_ahead > 0) prefetch_tile(nx + P.l2_ahead);
         }
     };
 
@@ -742,7 +732,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         // this item: split over the cluster (Si CTAs, this one rank ri) or
         // this CTA's whole unit (Si = 1, ri = 0); its slots, tiles and first
         // tile in the CTA's sequence
-        const bool split_item = i < W.n_split;
+        const bool split_item = !kFlex || i < W.n_split;
         const int Si = split_item ? S : 1, ri = split_item ? rank : 0;
         const int s_lo = split_item ? W.s_lo : 0, s_hi = split_item ? W.s_hi : W.n_all;
         const int n_mine = split_item ? W.n_mine : W.n_all;
@@ -1458,7 +1448,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
             const bool mine = Si == 1 || (pd.promote >= s_lo && pd.promote < s_hi);
             if (pd.promote >= 0 && mine) P.pool[unit * P.pstride + pd.promote] = 1;
             if (dest < 0 && ri == 0) {  // the new token itself left: its score leaves the cache
-                if (P.ledger) P.ledger[unit] += static_cast<double>(__uint_as_float(static_cast<uint32_t>(win_key >> 32)));
+                if (P.ledger) ledger_add(P.ledger + unit, __uint_as_float(static_cast<uint32_t>(win_key >> 32)));
                 if (P.trace != nullptr)
                     reinterpret_cast<int4 *>(P.trace)[unit] = make_int4(
                         -1, static_cast<int32_t>(static_cast<uint32_t>(win_key)),
@@ -1476,7 +1466,7 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 int32_t old_pos = static_cast<int32_t>(static_cast<uint32_t>(win_key));
                 float old_score = __uint_as_float(static_cast<uint32_t>(win_key >> 32));
                 // an evicted token's stored score leaves the cache: the ledger keeps it
-                if (evict && old_pos >= 0 && P.ledger) P.ledger[unit] += static_cast<double>(old_score);
+                if (evict && old_pos >= 0 && P.ledger) ledger_add(P.ledger + unit, old_score);
                 if (!evict && P.trace != nullptr) {
                     old_pos = P.pos[unit * CS + dest];
                     // (INT8: the codes were rewritten above; the slot is an empty one, score 0)

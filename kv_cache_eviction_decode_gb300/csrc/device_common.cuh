@@ -106,25 +106,10 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
 }
 
 
-// Bulk prefetch of [src, src + bytes) into L2 (no completion to track; src
-// and bytes 16-byte aligned): raises the bytes a CTA has in flight from HBM
-// without spending shared memory.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // ------------------------------------------------- tensor-map (TMA) copies
 // 2-D tiled copy global -> shared through a tensor map (boxes of 32 rows x 64
 // bf16, 128-byte swizzle); x (the innermost coordinate) is 0 or 64, so the
 // byte offset x * 2 is a multiple of 16.
-// Prefetch of one box of a 2-D tensor map into L2 (x aligned as for a load).
-__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar, uint64_t policy)
 {
     asm volatile(

@@ -97,11 +97,11 @@ def test_persistent_loop_with_refills(cuda_device, policy, split, clusters, reco
 
 @pytest.mark.parametrize("policy,G,dtype,B,split,clusters,budget,P,alias", [
     (configs.POLICY_H2O, 8, configs.DTYPE_BF16, 7, 2, 3, 96, 150, 0),     # tails of 0 and 1 unit
-    (configs.POLICY_H2O, 1, configs.DTYPE_BF16, 9, 4, 2, 96, 150, 0),     # 4 whole + 2 split per cluster
-    (configs.POLICY_H2O, 2, configs.DTYPE_F32, 5, 4, 3, 40, 20, 0),       # ranks with no tile; cache fills
+    (configs.POLICY_H2O, 4, configs.DTYPE_BF16, 9, 4, 2, 96, 150, 0),     # 4 whole + 2 split per cluster
+    (configs.POLICY_H2O, 4, configs.DTYPE_F32, 5, 4, 3, 40, 20, 0),       # ranks with no tile; cache fills
     (configs.POLICY_SINK_WINDOW, 4, configs.DTYPE_BF16, 11, 2, 5, 70, 90, 0),
     (configs.POLICY_RANDOM, 4, configs.DTYPE_BF16, 7, 2, 3, 48, 60, 0),   # holes, free list, cuts
-    (configs.POLICY_H2O_POOLS, 2, configs.DTYPE_BF16, 7, 2, 3, 64, 40, 0),
+    (configs.POLICY_H2O_POOLS, 4, configs.DTYPE_BF16, 7, 2, 3, 64, 40, 0),
 ])
 def test_tail_split_lockstep(cuda_device, policy, G, dtype, B, split, clusters, budget, P, alias, record_property):
     """Tail splitting: each CTA processes whole units alone and a cluster
@@ -130,21 +130,22 @@ def test_tail_split_lockstep(cuda_device, policy, G, dtype, B, split, clusters, 
 
 
 @pytest.mark.parametrize("policy,split,tail,G,dtype", [
-    (configs.POLICY_H2O, 1, False, 2, configs.DTYPE_F32),
+    (configs.POLICY_H2O, 1, False, 4, configs.DTYPE_F32),
     (configs.POLICY_H2O, 1, False, 8, configs.DTYPE_BF16),
     (configs.POLICY_H2O, 2, False, 4, configs.DTYPE_BF16),
     (configs.POLICY_H2O, 2, True, 8, configs.DTYPE_BF16),
-    (configs.POLICY_SINK_WINDOW, 2, False, 2, configs.DTYPE_BF16),
+    (configs.POLICY_SINK_WINDOW, 2, False, 4, configs.DTYPE_BF16),
     (configs.POLICY_SINK_WINDOW, 1, False, 4, configs.DTYPE_F32),
     (configs.POLICY_RANDOM, 2, False, 4, configs.DTYPE_BF16),
-    (configs.POLICY_RANDOM, 2, True, 2, configs.DTYPE_BF16),
-    (configs.POLICY_H2O_POOLS, 2, False, 2, configs.DTYPE_BF16),
-    (configs.POLICY_H2O_POOLS, 1, False, 2, configs.DTYPE_BF16)])
+    (configs.POLICY_RANDOM, 2, True, 8, configs.DTYPE_BF16),
+    (configs.POLICY_H2O_POOLS, 2, False, 4, configs.DTYPE_BF16),
+    (configs.POLICY_H2O_POOLS, 1, False, 8, configs.DTYPE_BF16)])
 def test_partials_over_logits_lockstep(cuda_device, policy, split, tail, G, dtype, record_property):
     """The warps' partial outputs written over the logits after the score
     pass (the layout that frees shared memory for ring stages), on units
     large enough for them to fit (>= 544 slots per CTA at head_dim 64): one
-    CTA per unit, clusters, tail splitting; every policy's epilogue."""
+    CTA per unit, clusters, tail splitting; every policy's epilogue. (Built
+    into the one-CTA-per-SM kernels, group sizes 4 and 8.)"""
     C = 1216
     kw = {configs.POLICY_H2O: dict(n_sink=4, n_heavy=C - 4 - 300, n_recent=300, budget=C, prompt_len=C + 30),
           configs.POLICY_SINK_WINDOW: dict(n_sink=4, n_recent=C - 4, budget=C, prompt_len=C + 10),
@@ -458,6 +459,26 @@ def test_h2o_gqa_full_shape(cuda_device, record_property):
     print("h2o gqa full shape:", _report(reps), "split", run.split)
     ls.record_ties(record_property, reps, max_near_ties=5)
     assert ls.check_selector(w, run, 0, w.prompt_len) == len(snaps)
+
+
+def test_tail_split_refused_by_two_cta_kernels(cuda_device):
+    """Group sizes 1 and 2 run two CTAs per SM and do not build tail
+    splitting; asking for it is an argument error and changes nothing."""
+    from kv_cache_eviction_decode_gb300 import KVEvictError
+    w = _small(configs.POLICY_H2O, configs.DTYPE_BF16, G=2, d=128, B=2, L=1, n_sink=2, n_heavy=60, n_recent=34,
+               budget=96, prompt_len=10)
+    cache = KVEvictCache.from_workload(w, device=cuda_device)
+    with pytest.raises(KVEvictError):
+        cache.set_tail_split(True)
+    assert cache.stats()["tail_split"] == 0
+    cache.set_partials_alias(1)  # accepted, and never applied: the partials keep their own area
+    K, V = synth.device_prompt(w, 0, cuda_device, 10)
+    cache.prefill(0, K, V)
+    q = torch.zeros((2, 8, 128), dtype=torch.bfloat16, device=cuda_device)
+    k = torch.zeros((2, 4, 128), dtype=torch.bfloat16, device=cuda_device)
+    cache.decode_step(0, q, k, k)
+    assert cache.check() == 0 and cache.stats()["partials_alias"] == 0
+    cache.close()
 
 
 def test_h2o_gqa_full_shape_tail_split(cuda_device, record_property):

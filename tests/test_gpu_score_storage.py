@@ -98,8 +98,9 @@ def test_int8_scores_lockstep(cuda_device, dtype, forget, record_property):
 def test_int8_scores_partials_over_logits(cuda_device, record_property):
     """INT8 scores with the warps' partial outputs written over the logits:
     the code pass reads the updated scores from the logit area before the
-    partials overwrite it (units of 1200 slots, where they fit)."""
-    w = configs.Workload(name="int8_alias", policy=H2O, dtype=BF16, batch=2, n_layers=1, n_q_heads=8, n_kv_heads=4,
+    partials overwrite it (units of 1200 slots, where they fit; group size 4,
+    a one-CTA-per-SM kernel)."""
+    w = configs.Workload(name="int8_alias", policy=H2O, dtype=BF16, batch=2, n_layers=1, n_q_heads=16, n_kv_heads=4,
                          head_dim=64, n_sink=4, n_heavy=896, n_recent=300, budget=1200, r=0, prompt_len=1230,
                          decode_steps=0, seed=93, score_int8=True)
     T = 60
