@@ -1104,28 +1104,59 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
         auto score_pass = [&](auto gen, const float(&fself)[G], uint64_t &best, int32_t &bslot, uint64_t &best2,
                               int32_t &bslot2, int32_t &emin, float &qmax) {
             constexpr bool GEN = decltype(gen)::value;
+            if constexpr (!GEN) {
+                // plain H2O, fp32 scores: four consecutive slots per thread, with
+                // 16-byte accesses to the logits, the scores (shared and global) and
+                // the positions (every row and offset here is a multiple of 4 floats);
+                // the same fmaf order per slot as the general loop
+                float *sp = static_cast<float *>(P.score) + unit * CS + s_lo;
+                for (int j0 = 4 * tid; j0 < n_mine; j0 += 4 * kThreads) {
+                    float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float4 z = *reinterpret_cast<const float4 *>(zbuf + g * zc + j0);
+                        a4.x = fmaf(z.x, fself[g], a4.x);
+                        a4.y = fmaf(z.y, fself[g], a4.y);
+                        a4.z = fmaf(z.z, fself[g], a4.z);
+                        a4.w = fmaf(z.w, fself[g], a4.w);
+                    }
+                    const float4 s4 = *reinterpret_cast<const float4 *>(ascore + j0);
+                    const float4 n4 = make_float4(fmaf(P.score_keep, s4.x, a4.x), fmaf(P.score_keep, s4.y, a4.y),
+                                                  fmaf(P.score_keep, s4.z, a4.z), fmaf(P.score_keep, s4.w, a4.w));
+                    const int left = n_mine - j0;  // valid slots in this group of four
+                    if (left >= 4) {
+                        *reinterpret_cast<float4 *>(sp + j0) = n4;
+                    } else {
+                        sp[j0] = n4.x;
+                        if (left > 1) sp[j0 + 1] = n4.y;
+                        if (left > 2) sp[j0 + 2] = n4.z;
+                    }
+                    if (evict) {
+                        const int4 p4 = *reinterpret_cast<const int4 *>(apos + j0);
+                        h2o_fold(best, bslot, n4.x, p4.x, s_lo + j0, P.n_sink, P.p, P.n_recent);
+                        if (left > 1) h2o_fold(best, bslot, n4.y, p4.y, s_lo + j0 + 1, P.n_sink, P.p, P.n_recent);
+                        if (left > 2) h2o_fold(best, bslot, n4.z, p4.z, s_lo + j0 + 2, P.n_sink, P.p, P.n_recent);
+                        if (left > 3) h2o_fold(best, bslot, n4.w, p4.w, s_lo + j0 + 3, P.n_sink, P.p, P.n_recent);
+                    }
+                }
+                return;
+            }
             for (int j = tid; j < n_mine; j += kThreads) {
                 float a = 0.f;
 #pragma unroll
                 for (int g = 0; g < G; ++g) a = fmaf(zbuf[g * zc + j], fself[g], a);
                 const size_t si = unit * CS + s_lo + j;
-                float sc;
-                if constexpr (GEN) {
-                    if (P.score_int8) {
-                        sc = fmaf(P.score_keep, stored_score(j), a);
-                        zbuf[j] = sc;
-                        if (apos[j] >= 0) qmax = fmaxf(qmax, sc);
-                        continue;
-                    }
-                    sc = score_store(P, si, fmaf(P.score_keep, stored_score(j), a));
-                } else {
-                    sc = fmaf(P.score_keep, ascore[j], a);
-                    static_cast<float *>(P.score)[si] = sc;
+                if (P.score_int8) {
+                    const float v = fmaf(P.score_keep, stored_score(j), a);
+                    zbuf[j] = v;
+                    if (apos[j] >= 0) qmax = fmaxf(qmax, v);
+                    continue;
                 }
+                const float sc = score_store(P, si, fmaf(P.score_keep, stored_score(j), a));
                 if (evict) {
                     const int ps = apos[j];
-                    if (GEN && (fill || pools) && ps < 0 && s_lo + j < emin) emin = s_lo + j;
-                    if (GEN && pools) {
+                    if ((fill || pools) && ps < 0 && s_lo + j < emin) emin = s_lo + j;
+                    if (pools) {
                         // two-pool: every held token is a candidate of the pool its flag names
                         if (ps >= 0) {
                             const uint64_t key = h2o_key(sc, ps);
