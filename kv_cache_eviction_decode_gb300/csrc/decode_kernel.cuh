@@ -1209,8 +1209,42 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                 uint64_t best = ~0ull, best2 = ~0ull;
                 int32_t bslot = -1, bslot2 = -1, emin = INT_MAX;
                 float qmax = 0.f;
-                if (general_scores) score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin, qmax);
-                else score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin, qmax);
+                // INT8 with at most kI8Groups groups of four slots per thread: the
+                // updated values stay in registers across the barrier that finds the
+                // unit's largest score (no second pass over the logit cells)
+                constexpr int kI8Groups = 1;
+                const bool int8_regs = P.score_int8 && n_mine <= 4 * kI8Groups * kThreads;
+                float v8[kI8Groups][4];
+                if (int8_regs) {
+                    const uint8_t *codes = ascore8;
+#pragma unroll
+                    for (int it = 0; it < kI8Groups; ++it) {
+                        const int j0 = 4 * tid + it * 4 * kThreads;
+                        if (j0 >= n_mine) break;
+                        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float4 z = *reinterpret_cast<const float4 *>(zbuf + g * zc + j0);
+                            a4[0] = fmaf(z.x, fself[g], a4[0]);
+                            a4[1] = fmaf(z.y, fself[g], a4[1]);
+                            a4[2] = fmaf(z.z, fself[g], a4[2]);
+                            a4[3] = fmaf(z.w, fself[g], a4[3]);
+                        }
+                        const uint32_t c4 = *reinterpret_cast<const uint32_t *>(codes + j0);
+                        const int4 p4 = *reinterpret_cast<const int4 *>(apos + j0);
+                        const int pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float old = static_cast<float>((c4 >> (8 * e)) & 0xFFu) * qscale_u;
+                            v8[it][e] = fmaf(P.score_keep, old, a4[e]);
+                            if (j0 + e < n_mine && pp[e] >= 0) qmax = fmaxf(qmax, v8[it][e]);
+                        }
+                    }
+                } else if (general_scores) {
+                    score_pass(Flag<true>{}, fself, best, bslot, best2, bslot2, emin, qmax);
+                } else {
+                    score_pass(Flag<false>{}, fself, best, bslot, best2, bslot2, emin, qmax);
+                }
                 if (P.score_int8) {
                     // the unit's largest score, the new token's included (every
                     // thread forms that one as thread 0 does); then the codes
@@ -1232,10 +1266,34 @@ __global__ void __launch_bounds__((warps_for<G, MMA>() * 32), (min_blocks<G, MMA
                         const float c = fminf(rintf(v * inv), 255.f);
                         return c >= 0.f ? c : 0.f;
                     };
-                    for (int j = tid; j < n_mine; j += kThreads) {
-                        const float c = code(zbuf[j]);
-                        static_cast<uint8_t *>(P.score)[unit * CS + s_lo + j] = static_cast<uint8_t>(c);
-                        if (evict) h2o_fold(best, bslot, c * scl, apos[j], s_lo + j, P.n_sink, P.p, P.n_recent);
+                    uint8_t *codes_out = static_cast<uint8_t *>(P.score) + unit * CS + s_lo;
+                    if (int8_regs) {
+#pragma unroll
+                        for (int it = 0; it < kI8Groups; ++it) {
+                            const int j0 = 4 * tid + it * 4 * kThreads;
+                            if (j0 >= n_mine) break;
+                            const int left = n_mine - j0;
+                            const int4 p4 = *reinterpret_cast<const int4 *>(apos + j0);
+                            const int pp[4] = {p4.x, p4.y, p4.z, p4.w};
+                            uint32_t packed = 0;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float c = code(v8[it][e]);
+                                packed |= static_cast<uint32_t>(c) << (8 * e);
+                                if (evict && e < left) h2o_fold(best, bslot, c * scl, pp[e], s_lo + j0 + e, P.n_sink, P.p, P.n_recent);
+                            }
+                            if (left >= 4) {
+                                *reinterpret_cast<uint32_t *>(codes_out + j0) = packed;
+                            } else {
+                                for (int e = 0; e < left; ++e) codes_out[j0 + e] = static_cast<uint8_t>(packed >> (8 * e));
+                            }
+                        }
+                    } else {
+                        for (int j = tid; j < n_mine; j += kThreads) {
+                            const float c = code(zbuf[j]);
+                            codes_out[j] = static_cast<uint8_t>(c);
+                            if (evict) h2o_fold(best, bslot, c * scl, apos[j], s_lo + j, P.n_sink, P.p, P.n_recent);
+                        }
                     }
                     anew_code = static_cast<uint8_t>(code(a));
                     anew = code(a) * scl;
