@@ -37,6 +37,13 @@ constexpr int kPT = kPromptTile;
 constexpr int kPStages = 4;
 constexpr int kEpiWarps = 16;
 constexpr int kSlices = kEpiWarps / 4;  // column slices per row (warps sharing a lane quadrant)
+// Pass 2 (unstacked): each B tile's 128 query normalisers are copied into one
+// of kNrmSlots shared-memory slots, beside the tile, completing on the slot's
+// own mbarrier. The copy for tile t is issued once the producer has seen the
+// MMAs of tile t - 4 complete (one ring turn), and those were issued after the
+// epilogue released tile t - 6: with 6 slots or more, the slot's previous tile
+// (t - kNrmSlots) is always released before its next copy starts.
+constexpr int kNrmSlots = 8;
 constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
 constexpr int kPThreads = (kEpiWarps + 2) * 32;
 constexpr uint32_t kTmemCols = 256;  // two 128-column fp32 accumulators
@@ -51,7 +58,8 @@ template <int D> struct PromptLayout {
     static constexpr int kOffBar = kOffB + kPStages * kTileBytes;
     static constexpr int kOffXchg = kOffBar + 512;  // [2 items][kSlices - 1][128]
     static constexpr int kOffPart = kOffXchg + 2 * (kSlices - 1) * kPT * 8;  // per-head partials [8][kSlices][128]
-    static constexpr int kBytes = kOffPart + 8 * kSlices * kPT * 4 + 1024;  // + slack to align the base to 1 KB
+    static constexpr int kOffNrm = kOffPart + 8 * kSlices * kPT * 4;          // pass 2: [kNrmSlots][128] normalisers
+    static constexpr int kBytes = kOffNrm + kNrmSlots * kPT * 4 + 1024;  // + slack to align the base to 1 KB
 };
 
 __device__ __forceinline__ void flag_timeout(uint32_t *err) { atomicOr(err, KVEVICT_DEV_WAIT_TIMEOUT); }
@@ -123,11 +131,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
     uint64_t *s_empty = s_full + 2;          // [2]
     uint64_t *i_full = s_empty + 2;          // [2] the next item's index is posted
     uint64_t *i_empty = i_full + 2;          // [2] every consumer has read it
-    int *item_idx = reinterpret_cast<int *>(i_empty + 2);  // [2]
+    uint64_t *n_full = i_empty + 2;          // [kNrmSlots] pass 2: a B tile's normalisers landed
+    int *item_idx = reinterpret_cast<int *>(n_full + kNrmSlots);  // [2]
     int *eagree = item_idx + 2;                            // [kEpiWarps] what each epilogue warp read
     uint32_t *tslot = reinterpret_cast<uint32_t *>(eagree + kEpiWarps);
     float2 *xchg_all = reinterpret_cast<float2 *>(sm + L::kOffXchg);
     float *hpart = reinterpret_cast<float *>(sm + L::kOffPart);
+    float *nrm = reinterpret_cast<float *>(sm + L::kOffNrm);
+    constexpr bool kNrm = MODE == kColSum && !STACK;  // normalisers staged in shared memory
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nT = (p.P + kPT - 1) / kPT;
@@ -191,6 +202,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
             mbar_init(&i_full[s], 1);
             mbar_init(&i_empty[s], kEpiWarps + 1);
         }
+        for (int s = 0; s < kNrmSlots; ++s) mbar_init(&n_full[s], 1);
         mbar_fence_init();
     }
     if (warp == kProdWarp) tmem_alloc(tslot, kTmemCols);
@@ -260,6 +272,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                     for (int c = 0; c < D / 64; ++c)
                         tma_load_2d_plain(sm + L::kOffB + s * L::kTileBytes + c * L::kBoxBytes, &p.tmb, c * 64, row,
                                           &b_full[s]);
+                    if constexpr (kNrm) {
+                        // the 128 queries' normalisers of this tile (query head gq, query tile qt)
+                        const int b = it.head / p.Hkv, kvh = it.head - b * p.Hkv;
+                        const int gq = n / it.nq, qt = it.qt0 + (n - gq * it.nq);
+                        const float *src = p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + gq) * p.Ps + (qt * kPT - qs0);
+                        const int ns = g % kNrmSlots;
+                        mbar_arrive_expect_tx(&n_full[ns], kPT * 4);
+                        bulk_g2s(nrm + ns * kPT, src, kPT * 4, &n_full[ns]);
+                    }
                     issued_b = g + 1;
                 }
             }
@@ -349,6 +370,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                     ok = false;
                     if (lane == 0) flag_timeout(p.err);
                 }
+                if (kNrm && ok &&
+                    !__all_sync(0xffffffffu, mbar_wait(&n_full[gt % kNrmSlots], (gt / kNrmSlots) & 1))) {
+                    ok = false;
+                    if (lane == 0) flag_timeout(p.err);
+                }
                 tc_fence_after();
                 if (ok && !idle) {
                     uint32_t r[32];
@@ -432,16 +458,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                         // queries i = qt * 128 + col0 + e of query head g
                         const int g = n / nq, qt = qt0 + (n - g * nq);
                         const int i0 = qt * kPT + col0;
-                        const int b = head / p.Hkv, kvh = head - b * p.Hkv;
-                        const float4 *st = reinterpret_cast<const float4 *>(
-                            p.stats + static_cast<size_t>(b * p.Hq + kvh * p.G + g) * p.Ps + (i0 - qs0));
+                        // minus the log2 normalisers of these 32 queries, staged by the producer
+                        const float4 *st = reinterpret_cast<const float4 *>(nrm + (gt % kNrmSlots) * kPT + col0);
                         const bool full = qt > tile && i0 + 32 <= p.P && i0 >= p.q_lo;
                         const float2 c2 = make_float2(c, c);
                         float2 s2 = make_float2(0.f, 0.f);
                         if (full) {  // every query of these 32 columns attends this key
 #pragma unroll
                             for (int e4 = 0; e4 < 8; ++e4) {
-                                const float4 nms = __ldg(st + e4);  // minus the log2 normalisers
+                                const float4 nms = st[e4];
                                 const int e = e4 * 4;
                                 const float2 za = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2,
                                                         make_float2(nms.x, nms.y));
@@ -453,7 +478,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                         } else {
 #pragma unroll
                             for (int e4 = 0; e4 < 8; ++e4) {
-                                const float4 nms = __ldg(st + e4);
+                                const float4 nms = st[e4];
                                 const float mv[4] = {nms.x, nms.y, nms.z, nms.w};
 #pragma unroll
                                 for (int t = 0; t < 4; ++t) {
@@ -521,6 +546,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
     if (warp == kProdWarp && lane == 0) {
         for (int n = max(0, issued_b - kPStages); n < issued_b; ++n)
             mbar_wait(&b_full[n % kPStages], (n / kPStages) & 1);
+        if (kNrm)
+            for (int n = max(0, issued_b - kNrmSlots); n < issued_b; ++n)
+                mbar_wait(&n_full[n % kNrmSlots], (n / kNrmSlots) & 1);
         for (int i = max(0, issued_a - 2); i < issued_a; ++i) mbar_wait(&a_full[i & 1], (i >> 1) & 1);
     }
     if (warp == kMmaWarp && lane == 0) {
