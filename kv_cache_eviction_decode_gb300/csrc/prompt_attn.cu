@@ -73,6 +73,14 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// max(a, b, c) in one instruction (the three-input max.f32 of sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Two fp32 lanes per instruction (Blackwell's packed f32x2 FMA and add).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
 {
@@ -363,6 +371,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
             }
             // STACK pass 1: a warp whose 32 rows all lie past the stacked rows has nothing to do
             const bool idle = MODE == kRowStats && STACK && tile * kPT + quad * 32 >= Lq;
+            int gq = 0, jq = 0;  // pass 2 (unstacked): tile n is query tile qt0 + jq of query head gq
             for (int n = 0; n < n_b; ++n, ++gt) {
                 const int sb = gt & 1;
                 // the TMEM load below is warp-collective: the whole warp agrees on `ok`
@@ -394,9 +403,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
 #pragma unroll
                             for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
                         }
-                        float cm = v[0];
+                        // the tile's max, two values per three-input max
+                        float cm = fmax3(v[0], v[1], v[2]);
 #pragma unroll
-                        for (int e = 1; e < 32; ++e) cm = fmaxf(cm, v[e]);
+                        for (int e = 3; e < 31; e += 2) cm = fmax3(cm, v[e], v[e + 1]);
+                        cm = fmaxf(cm, v[31]);
                         cm *= c;  // c > 0: the max of the scaled logits
                         if (cm > m) {
                             l *= ex2(m - cm);
@@ -456,7 +467,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                         }
                     } else {
                         // queries i = qt * 128 + col0 + e of query head g
-                        const int g = n / nq, qt = qt0 + (n - g * nq);
+                        const int g = gq, qt = qt0 + jq;
                         const int i0 = qt * kPT + col0;
                         // minus the log2 normalisers of these 32 queries, staged by the producer
                         const float4 *st = reinterpret_cast<const float4 *>(nrm + (gt % kNrmSlots) * kPT + col0);
@@ -491,18 +502,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prompt_attn_kernel(const __grid_
                             }
                         }
                         acc += s2.x + s2.y;
-                        if (p.per_head && n - g * nq == nq - 1) {  // the last tile of query head g
+                        if (p.per_head && jq == nq - 1) {  // the last tile of query head g
                             hpart[(g * kSlices + slice) * kPT + row] = acc;
                             acc = 0.f;
                         }
                     }
                 } else if (MODE == kColSum && p.per_head && !STACK) {
-                    const int g = n / nq;
-                    if (n - g * nq == nq - 1) hpart[(g * kSlices + slice) * kPT + row] = 0.f;
+                    if (jq == nq - 1) hpart[(gq * kSlices + slice) * kPT + row] = 0.f;
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
+                if (++jq == nq) {
+                    jq = 0;
+                    ++gq;
+                }
             }
             if (MODE == kColSum && STACK) hpart[(cur_g * kSlices + slice) * kPT + row] = acc;
             // the column slices of each row meet: slices 1.. hand over to slice 0
@@ -706,8 +720,11 @@ __global__ void __launch_bounds__(kPThreads, 1) snap_votes_kernel(const __grid_c
         const float c = p.scale_log2;
         const int pre = p.P - p.w;  // keys before the window: every window query sees them
         bool ok = true;
+        // item it = (unit u, key tile kt), u = it / nT, kept by counters
+        int u = it0 / nT, kt = it0 - u * nT;
+        int b = u / p.Hkv, kvh = u - b * p.Hkv;
         for (int it = it0; it < it1; ++it) {
-            const int u = it / nT, kt = it - u * nT, n = it - it0, sb = n & 1;
+            const int n = it - it0, sb = n & 1;
             const int j = kt * kPT + row;  // this thread's key
             // the TMEM loads below are warp-collective: the whole warp agrees on `ok`
             if (ok && !__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (n >> 1) & 1))) {
@@ -715,7 +732,6 @@ __global__ void __launch_bounds__(kPThreads, 1) snap_votes_kernel(const __grid_c
                 if (lane == 0) flag_timeout(p.err);
             }
             tc_fence_after();
-            const int b = u / p.Hkv, kvh = u - b * p.Hkv;
             float *vout = p.votes + static_cast<size_t>(b * p.Hq + kvh * p.G) * p.P + j;
             // this slice's query heads: g = slice, slice + 4, ... (all chunks of each)
             for (int g = slice; ok && g < p.G; g += kSlices) {
@@ -753,6 +769,14 @@ __global__ void __launch_bounds__(kPThreads, 1) snap_votes_kernel(const __grid_c
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[sb]);
+            if (++kt == nT) {
+                kt = 0;
+                ++u;
+                if (++kvh == p.Hkv) {
+                    kvh = 0;
+                    ++b;
+                }
+            }
         }
     }
 
