@@ -302,16 +302,30 @@ def run_ours(args, w, rank, world, device, steps=None, warmup=None, extras=True)
         barrier(device)
         torch.cuda.synchronize(device)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        graph = None
+        if args.graph:
+            # the timed token-steps captured once on the handle's stream (each
+            # launch with its own step's arguments) and replayed once
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for s in range(warmup, n_win):
+                    token_step(s)
+            stream.synchronize()
         with ClockSampler(device.index) as clk:
             # the device sleeps ~1 ms before the start event, so the host has
             # queued the first steps when it is recorded: the timed region
             # holds the steps' own work, not the first launch's host latency
             torch.cuda._sleep(2_000_000)
             ev0.record(stream)
-            for s in range(warmup, n_win):
-                token_step(s)
+            if graph is not None:
+                with torch.cuda.stream(stream):
+                    graph.replay()
+            else:
+                for s in range(warmup, n_win):
+                    token_step(s)
             ev1.record(stream)
             ev1.synchronize()
+        del graph
         torch.cuda.synchronize(device)
         barrier(device)
         err = cache.check()
@@ -791,6 +805,8 @@ def main():
     ap.add_argument("--ring", type=int, default=0, help="cap on ring stages per CTA (0 = fill shared memory)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time the decode steps as stream launches instead of one replay of a CUDA graph of them")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the score-keeping and Random workloads measured beside the default one")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
@@ -881,7 +897,9 @@ def main():
         "config": dict(cfg, split=r["split"], clusters=r["clusters"], tensor_cores=bool(r["tensor_cores"]),
                        ring_stages=r["ring_stages"], tail_split=bool(r["tail_split"]),
                        partials_alias=bool(r["partials_alias"]),
-                       timing="CUDA events on the launching stream; no L2 flush needed"),
+                       timing=("CUDA events on the launching stream around one replay of a CUDA graph of the "
+                               "timed steps; no L2 flush needed") if args.graph else
+                       "CUDA events on the launching stream; no L2 flush needed"),
         "layer_step_us": 1e6 * avg_launch_s,
         "kernel_us_isolated": 1e3 * statistics.median(r["iso_ms"]) if r["iso_ms"] else None,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
