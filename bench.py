@@ -337,6 +337,21 @@ def run_ours(args, w, rank, world, device, steps=None, warmup=None, extras=True)
         decode_launches = st["decode_steps"] - launches_before["decode_steps"]
         cut_launches = st["cuts"] - launches_before["cuts"]
 
+        # validation mode, after the timed region: the H2O decisions whose runner-up
+        # candidate was within 1e-5 relative of the evicted token (kvevict_set_tie_audit)
+        near = None
+        if w.policy == configs.POLICY_H2O and args.tie_steps > 0:
+            n_dec = 0
+            cache.set_tie_audit(True)
+            for i in range(args.tie_steps):
+                token_step((warmup + i) % n_win)
+            stream.synchronize()
+            cache.set_tie_audit(False)
+            n_dec = args.tie_steps * L * B * Hkv  # at steady state every step evicts in every unit
+            cnt = cache.stats()["near_ties"]
+            near = {"count": cnt, "decisions": n_dec, "rate": cnt / n_dec, "steps": args.tie_steps,
+                    "rule": "runner-up candidate within 1e-5 relative of the evicted token's stored score"}
+
         # isolated kernel time of single launches (events around each), for context
         iso = []
         for s in range(min(8, n_win) if extras else 0):
@@ -384,7 +399,7 @@ def run_ours(args, w, rank, world, device, steps=None, warmup=None, extras=True)
     return dict(dt_ms=dt_ms, clocks=clk.summary(), decode_launches=decode_launches, cut_launches=cut_launches,
                 iso_ms=iso, e2e=e2e, split=st["split"], clusters=st["clusters"], tensor_cores=st["tensor_cores"],
                 ring_stages=st["ring_stages"], held=held, tail_split=st["tail_split"],
-                partials_alias=st["partials_alias"])
+                partials_alias=st["partials_alias"], near_ties=near)
 
 
 # ---------------------------------------------------------------------------
@@ -412,7 +427,8 @@ def workload_summary(w, r, steps):
             "dram_traffic_over_algorithmic": (tr / layer_bytes) if tr else None,
             "steps": steps, "gpu_launches": r["decode_launches"] + r["cut_launches"],
             "split": r["split"], "tail_split": bool(r["tail_split"]), "partials_alias": bool(r["partials_alias"]),
-            "clusters": r["clusters"], "ring_stages": r["ring_stages"], "clocks": r["clocks"]}
+            "clusters": r["clusters"], "ring_stages": r["ring_stages"], "clocks": r["clocks"],
+            "near_ties": r["near_ties"]}
 
 
 def extra_workloads(args, rank, world, device):
@@ -807,6 +823,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time the decode steps as stream launches instead of one replay of a CUDA graph of them")
+    ap.add_argument("--tie-steps", type=int, default=10,
+                    help="H2O: token-steps run in validation mode after the timed region to count near-ties (0: none)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the score-keeping and Random workloads measured beside the default one")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
@@ -911,6 +929,8 @@ def main():
         "clocks": r["clocks"],
         "e2e": r["e2e"],
     }
+    if r["near_ties"] is not None:
+        out["near_ties"] = r["near_ties"]
     headline = args.workload == "sink_window" and not args.layers and args.prompt < 0
     if world == 1 and headline and not args.no_workloads:
         out["workloads"] = extra_workloads(args, rank, world, device)

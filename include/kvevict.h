@@ -175,6 +175,9 @@ typedef struct {
     int partials_alias;     /* 1 if the last decode launch wrote its warps' partial outputs over the logits */
     double evicted_mass;    /* policies with scores: the stored scores of every token that left the cache,
                                summed over layers and units in fp64 (kvevict_evicted_mass per unit) */
+    int64_t near_ties;      /* validation mode (kvevict_set_tie_audit): H2O eviction decisions whose runner-up
+                               candidate's stored score was within 1e-5 relative of the evicted token's,
+                               summed over layers and units; 0 when the mode was never on */
 } kvevict_stats;
 
 /* Bytes of device memory a handle with this configuration needs (cache,
@@ -444,6 +447,27 @@ int kvevict_set_split(kvevict_t h, int split);
  * memory: INVALID_ARG otherwise, with INT8 score storage, and for kernels run two
  * CTAs per SM (group sizes 1 and 2), which do not build it. */
 int kvevict_set_tail_split(kvevict_t h, int on);
+
+/* Validation mode for H2O (policy KVEVICT_H2O): 1 on, 0 off (the default).
+ * On, every decode step that may evict is followed by a small kernel that
+ * counts, per unit, the decisions whose runner-up candidate (the smallest
+ * stored score among the candidates left, by the same candidate rule) lies
+ * within 1e-5 relative of the evicted token's stored score (|a - b| <
+ * 1e-5 max(a, b), equal scores included): the decisions that a different
+ * rounding of the scores could have flipped. The counts accumulate per layer
+ * on the device (kvevict_near_ties) and in kvevict_stats.near_ties. Costs one
+ * extra launch per layer-step; results of the decode itself are unchanged.
+ * The counters and a [B][Hkv][4] record area (used when no trace is set; with
+ * a trace the step's trace records are read) are part of the state buffer of
+ * every policy with scores, zeroed by kvevict_create. A step whose eviction
+ * found no candidate (KVEVICT_DEV_NO_CANDIDATE) is not counted reliably.
+ * INVALID_ARG outside 0..1, and for 1 with a policy other than KVEVICT_H2O. */
+int kvevict_set_tie_audit(kvevict_t h, int on);
+
+/* The near-tie count of one layer since the handle was created (validation
+ * mode, kvevict_set_tie_audit; 0 if it was never on). Waits for the handle's
+ * stream. STATE if the layer is out of range. */
+int kvevict_near_ties(kvevict_t h, int layer, uint64_t *out);
 
 /* Where the decode launch keeps its warps' partial outputs: -1 automatic
  * (the default), 0 in an area of their own, 1 over the unit's logits once the

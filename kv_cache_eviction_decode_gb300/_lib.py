@@ -32,7 +32,8 @@ class Stats(ctypes.Structure):
                 ("evictions", ctypes.c_int64), ("cuts", ctypes.c_int64), ("split", ctypes.c_int),
                 ("capacity", ctypes.c_int), ("clusters", ctypes.c_int), ("tensor_cores", ctypes.c_int),
                 ("ring_stages", ctypes.c_int), ("tail_split", ctypes.c_int),
-                ("partials_alias", ctypes.c_int), ("evicted_mass", ctypes.c_double)]
+                ("partials_alias", ctypes.c_int), ("evicted_mass", ctypes.c_double),
+                ("near_ties", ctypes.c_int64)]
 
 
 class KVEvictError(RuntimeError):
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
             L.kvevict_set_clusters.argtypes = [P, I]
             L.kvevict_set_tail_split.argtypes = [P, I]
             L.kvevict_set_partials_alias.argtypes = [P, I]
+            L.kvevict_set_tie_audit.argtypes = [P, I]
+            L.kvevict_near_ties.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint64)]
             L.kvevict_set_path.argtypes = [P, I]
             L.kvevict_set_ring.argtypes = [P, I]
             L.kvevict_get_stats.argtypes = [P, ctypes.POINTER(Stats)]
@@ -97,7 +100,7 @@ def lib() -> ctypes.CDLL:
                       "kvevict_score_scales", "kvevict_evicted_mass", "kvevict_probe_wait_timeout", "kvevict_select_victims", "kvevict_checkpoint_bytes",
                       "kvevict_checkpoint_save", "kvevict_checkpoint_restore",
                       "kvevict_set_trace",
-                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_tail_split", "kvevict_set_partials_alias", "kvevict_set_path", "kvevict_set_ring",
+                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_tail_split", "kvevict_set_partials_alias", "kvevict_set_tie_audit", "kvevict_near_ties", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",
                       "kvevict_check"):
                 getattr(L, n).restype = I

@@ -301,6 +301,17 @@ class KVEvictCache:
         mode = on if isinstance(on, int) and not isinstance(on, bool) else (1 if on else 0)
         check(self._L.kvevict_set_tail_split(self.h, mode), "kvevict_set_tail_split")
 
+    def set_tie_audit(self, on: bool) -> None:
+        """Validation mode: count the H2O decisions whose runner-up was within 1e-5
+        relative of the evicted token's score (kvevict_stats.near_ties)."""
+        check(self._L.kvevict_set_tie_audit(self.h, 1 if on else 0), "kvevict_set_tie_audit")
+
+    def near_ties(self, layer: int) -> int:
+        """This layer's near-tie count (validation mode)."""
+        v = ctypes.c_uint64(0)
+        check(self._L.kvevict_near_ties(self.h, layer, ctypes.byref(v)), "kvevict_near_ties")
+        return v.value
+
     def set_partials_alias(self, mode: int) -> None:
         """-1 automatic, 0 own area, 1 the warps' partial outputs over the logits."""
         check(self._L.kvevict_set_partials_alias(self.h, mode), "kvevict_set_partials_alias")

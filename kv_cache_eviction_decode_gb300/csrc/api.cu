@@ -45,6 +45,7 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int kSMs = 152;
+constexpr float kNearTieRel = 1e-5f;  // two candidate scores closer than this (relative) are a near-tie
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -66,6 +67,9 @@ struct Layout {
     size_t kv_layer_bytes = 0;
     size_t off_k = 0, off_v = 0, off_pos = 0, off_score = 0, off_pool = 0, off_free = 0, off_err = 0;
     size_t off_ledger = 0;  // [L][B][Hkv] fp64 evicted score mass (policies with scores)
+    size_t off_tie = 0;     // validation mode (policies with scores): [L] u64 near-tie counts, then [B][Hkv][4] int32
+                            // step records
+    size_t tie_trace_off = 0;  // the step records' offset inside that region
     size_t off_sq[2] = {}, off_sk[2] = {}, off_sv[2] = {}, off_so[2] = {};  // host-path staging, two slots
     size_t total = 0;
     size_t q_bytes = 0, kvtok_bytes = 0;  // one layer-step's q/out and k_new/v_new
@@ -152,6 +156,8 @@ Layout make_layout(const kvevict_config *c)
     L.off_score = off; if (scored(c->policy)) off = align_up(off + nl * L.layer_pslots * L.score_elem);
     L.off_qscale = off; if (c->score_int8) off = align_up(off + nl * L.units * 4);
     L.off_ledger = off; if (scored(c->policy)) off = align_up(off + nl * L.units * 8);
+    L.tie_trace_off = (nl * 8 + 15) / 16 * 16;
+    L.off_tie = off; if (scored(c->policy)) off = align_up(off + L.tie_trace_off + L.units * 16);
     L.off_pool = off; off = align_up(off + nl * L.units * L.Ps);
     L.off_free = off;
     if (c->policy == KVEVICT_RANDOM || c->policy == KVEVICT_H2O_BLOCK) off = align_up(off + nl * L.units * c->r * 4);
@@ -201,6 +207,10 @@ struct kvevict_handle {
     int ring_req = 0;      // ring stages requested (0 = fill the shared-memory budget)
     int alias_req = -1;    // warp partials over the logits: -1 automatic, 0 never, 1 where they fit
     bool use_mma = false;  // decode path in use
+    // Validation mode: near-ties of the H2O decisions counted on the device
+    // (per layer, in the state buffer), from each step's records (the caller's
+    // trace, else the state buffer's record area).
+    bool tie_audit = false;
     std::vector<CUtensorMap> tmk, tmv;  // per layer (bf16 caches)
     std::vector<LayerState> layers;
     kvevict_stats stats{};
@@ -495,6 +505,7 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     P.n_recent = c.n_recent;
     P.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
     P.trace = (ls.trace && ls.trace_t < ls.trace_len) ? ls.trace + static_cast<size_t>(ls.trace_t) * L.units * 4 : nullptr;
+    const bool user_trace = P.trace != nullptr;
 
     bool holes = false;
     long long evicted = 0;
@@ -629,13 +640,34 @@ int launch_decode(kvevict_handle *h, int layer, const void *q, const void *kn, c
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = 2;
+    // validation mode: the step's records feed the near-tie count
+    const bool audit = h->tie_audit && c.policy == KVEVICT_H2O && (P.mode == kH2OEvict || P.mode == kH2OFill);
+    if (audit && !P.trace) P.trace = at<int32_t>(h, L.off_tie + L.tie_trace_off);
     void *args[] = {&P};
     rc = cuda_status(cudaLaunchKernelExC(&lc, ki.fn, args));
     if (rc) return rc;
     h->last_layer = layer;
+    if (audit) {
+        TieAuditParams tp{};
+        tp.pos = P.pos;
+        tp.score = P.score;
+        tp.qscale = P.qscale;
+        tp.trace = P.trace;
+        tp.count = at<unsigned long long>(h, L.off_tie) + layer;
+        tp.score_half = P.score_half;
+        tp.score_int8 = P.score_int8;
+        tp.n_active = P.n_active;
+        tp.cstride = P.cstride;
+        tp.p = P.p;
+        tp.n_sink = P.n_sink;
+        tp.n_recent = P.n_recent;
+        tp.rel = kNearTieRel;
+        rc = cuda_status(launch_tie_audit(tp, static_cast<int>(L.units), h->stream));
+        if (rc) return rc;
+    }
 
     // Bookkeeping of what the step did.
-    if (P.trace) ls.trace_t++;
+    if (user_trace) ls.trace_t++;
     h->stats.decode_steps++;
     h->stats.evictions += evicted;
     switch (c.policy) {
@@ -772,6 +804,8 @@ int kvevict_create(kvevict_t *out, const kvevict_config *cfg, void *state, size_
         e = cudaMemsetAsync(h->state + L.off_qscale, 0, cfg->n_layers * L.units * 4, h->stream);
     if (e == cudaSuccess && scored(cfg->policy))
         e = cudaMemsetAsync(h->state + L.off_ledger, 0, cfg->n_layers * L.units * 8, h->stream);
+    if (e == cudaSuccess && scored(cfg->policy))
+        e = cudaMemsetAsync(h->state + L.off_tie, 0, L.tie_trace_off + L.units * 16, h->stream);
     if (e == cudaSuccess && L.Ps > 0)
         e = cudaMemsetAsync(h->state + L.off_pool, 0, cfg->n_layers * L.units * L.Ps, h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.off_err, 0, 16, h->stream);
@@ -1525,6 +1559,29 @@ int kvevict_set_partials_alias(kvevict_t h, int mode)
     return KVEVICT_OK;
 }
 
+int kvevict_set_tie_audit(kvevict_t h, int on)
+{
+    if (!h || on < 0 || on > 1) return KVEVICT_ERR_INVALID_ARG;
+    if (on && h->cfg.policy != KVEVICT_H2O) return KVEVICT_ERR_INVALID_ARG;
+    h->tie_audit = on == 1;
+    return KVEVICT_OK;
+}
+
+int kvevict_near_ties(kvevict_t h, int layer, uint64_t *out)
+{
+    if (!h || !out) return KVEVICT_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return KVEVICT_ERR_STATE;
+    *out = 0;
+    if (!scored(h->cfg.policy)) return KVEVICT_OK;
+    unsigned long long v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, at<unsigned long long>(h, h->L.off_tie) + layer, sizeof v,
+                                    cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    *out = v;
+    return KVEVICT_OK;
+}
+
 int kvevict_set_tail_split(kvevict_t h, int on)
 {
     if (!h || on < -1 || on > 1) return KVEVICT_ERR_INVALID_ARG;
@@ -1597,6 +1654,15 @@ int kvevict_get_stats(kvevict_t h, kvevict_stats *out)
     out->tensor_cores = h->use_mma ? 1 : 0;
     out->ring_stages = h->configured[0].nst ? h->configured[0].nst : h->configured[1].nst;
     out->partials_alias = (h->configured[0].nst ? h->configured[0].alias : h->configured[1].alias) ? 1 : 0;
+    out->near_ties = 0;
+    if (scored(h->cfg.policy)) {
+        std::vector<unsigned long long> cnt(h->cfg.n_layers);
+        cudaError_t e = cudaMemcpyAsync(cnt.data(), at<unsigned long long>(h, h->L.off_tie),
+                                        cnt.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost, h->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        if (e != cudaSuccess) return cuda_status(e);
+        for (unsigned long long v : cnt) out->near_ties += static_cast<int64_t>(v);
+    }
     return KVEVICT_OK;
 }
 

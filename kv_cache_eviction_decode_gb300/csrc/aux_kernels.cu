@@ -263,6 +263,53 @@ __global__ void __launch_bounds__(256) block_release_kernel(const BlockReleasePa
     }
 }
 
+// Near-ties of one H2O step ("h2o: heavy-hitter oracle" summary, Algorithm 1:
+// the greedy removal of the lowest-score candidate). For every unit whose
+// step evicted a token: the smallest stored score among the candidates left
+// (the step's candidate rule at position p: a token at ps >= n_sink and
+// <= p - n_recent; the new token is never one) is the runner-up of the
+// decision, since the step changes no other slot after its score pass. A
+// unit counts when the runner-up's score is within `rel` of the evicted one's
+// (|a - b| < rel max(a, b), equal scores included): there a different
+// rounding of the scores could have chosen the other token. One CTA per unit.
+__global__ void __launch_bounds__(256) tie_audit_kernel(const TieAuditParams P)
+{
+    __shared__ float wmin[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t unit = blockIdx.x;
+    const int32_t *tr = P.trace + unit * 4;
+    const int dest = tr[0], old_pos = tr[1];
+    if (old_pos < 0) return;  // an empty slot took the token: no decision between tokens
+    const float s1 = __int_as_float(tr[2]);
+    const int32_t *pos = P.pos + unit * P.cstride;
+    const float scl = P.score_int8 ? P.qscale[unit] : 0.f;
+    float mn = INFINITY;
+    for (int j = tid; j < P.n_active; j += blockDim.x) {
+        const int32_t ps = pos[j];
+        if (j == dest || ps < P.n_sink || ps > P.p - P.n_recent) continue;
+        const size_t i = unit * P.cstride + j;
+        const float s = P.score_int8   ? static_cast<float>(static_cast<const uint8_t *>(P.score)[i]) * scl
+                        : P.score_half ? __half2float(static_cast<const __half *>(P.score)[i])
+                                       : static_cast<const float *>(P.score)[i];
+        mn = fminf(mn, s);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    if (lane == 0) wmin[warp] = mn;
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) mn = fminf(mn, wmin[w]);
+        mn = fminf(mn, wmin[0]);
+        if (mn != INFINITY && (mn == s1 || fabsf(mn - s1) < P.rel * fmaxf(mn, s1))) atomicAdd(P.count, 1ull);
+    }
+}
+
+cudaError_t launch_tie_audit(const TieAuditParams &p, int units, cudaStream_t st)
+{
+    tie_audit_kernel<<<units, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
 void launch_block_prefill(const BlockPrefillParams &p, int B, cudaStream_t st)
 {
     dim3 grid((p.C + 7) / 8, p.Hkv, B);

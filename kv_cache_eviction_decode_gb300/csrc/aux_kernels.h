@@ -57,6 +57,18 @@ struct BlockReleaseParams {
     uint32_t *err;
 };
 
+// Validation mode: the near-ties of one H2O decode step's eviction decisions.
+struct TieAuditParams {
+    const int32_t *pos;          // layer [B][Hkv][cstride], after the step
+    const void *score;           // layer scores after the step: fp32, binary16 or 8-bit codes
+    const float *qscale;         // score_int8: layer [B][Hkv] scales after the step
+    const int32_t *trace;        // [B][Hkv][4] the step's records: slot, evicted position, evicted score bits, ...
+    unsigned long long *count;   // this layer's count of near-ties
+    int score_half, score_int8;
+    int n_active, cstride, p, n_sink, n_recent;
+    float rel;                   // relative gap below which two scores are a near-tie
+};
+
 void launch_prefill(const PrefillParams &p, int rows, int B, cudaStream_t st);
 // binary16 scores [units][cstride] -> fp32 [units][C]
 cudaError_t launch_scores_to_f32(float *dst, const void *src, int C, int cstride, size_t units, cudaStream_t st);
@@ -70,5 +82,6 @@ void launch_block_prefill(const BlockPrefillParams &p, int B, cudaStream_t st);
 cudaError_t launch_block_release(const BlockReleaseParams &p, int units, cudaStream_t st);
 size_t cut_smem_bytes(int n_pow2, int r);
 cudaError_t launch_random_cut(const CutParams &p, int B, cudaStream_t st);
+cudaError_t launch_tie_audit(const TieAuditParams &p, int units, cudaStream_t st);
 
 }  // namespace kvevict

@@ -99,6 +99,8 @@ def test_null_handle_and_strerror(L):
     assert L.kvevict_probe_wait_timeout(None) == -1
     assert L.kvevict_score_scales(None, 0, None, 0) == -1
     assert L.kvevict_select_victims(None, 0, None, None) == -1
+    assert L.kvevict_set_tie_audit(None, 1) == -1
+    assert L.kvevict_near_ties(None, 0, None) == -1
     assert L.kvevict_prefill_scored_static(None, 0, None, None, None, 1) == -1
     assert L.kvevict_strerror(0) == b"ok"
     assert L.kvevict_strerror(-2) == b"capacity exceeded"
