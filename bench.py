@@ -390,8 +390,11 @@ def run_ours(args, w, rank, world, device, steps=None, warmup=None, extras=True)
             e2e_s = reduce_max(time.perf_counter() - t0, device)
             h2d = L * (q[0, 0].numel() + kn[0, 0].numel() + vn[0, 0].numel()) * q.element_size()
             d2h = L * out[0, 0].numel() * q.element_size()
+            in_place = all(Lb.kvevict_host_buffer_mapped(t.data_ptr()) for t in (qh, kh, vh, oh))
             e2e = {"value": world * B * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h, "steps": n_e2e}
+                   "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                   "path": ("pinned host buffers read and written in place by the kernels over the CPU-GPU link"
+                            if in_place else "staging copies on copy-in/copy-out streams")}
         held = None
         if w.policy == configs.POLICY_H2O_POOLS:  # data-dependent occupancy: the mean held fraction
             held = float(np.mean([(cache.slot_positions(layer) >= 0).float().mean().item() for layer in range(L)]))

@@ -312,18 +312,28 @@ int kvevict_decode_step(kvevict_t h, int layer, const void *q, const void *k_new
 int kvevict_decode_step_host(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new,
                              void *out);
 
-/* kvevict_decode_step_host without waiting, for pipelining host-buffer steps:
- * the inputs are copied in on an internal copy-in stream, into one of two
- * staging slots that alternate between calls; the step runs on the handle's
- * stream once they are in; the output is copied back on an internal copy-out
- * stream once the step is done. A call's copy-in overlaps the previous call's
- * step, and its copy-out the next call's. The host buffers (pinned memory) must
- * stay valid, and the inputs unchanged, until kvevict_sync returns; the output
- * holds the result only then. Steps run in call order on the handle's stream.
- * kvevict_decode_step_host waits for the pending calls first. The streams and
- * their events are created on the first call. */
+/* kvevict_decode_step_host without waiting, for pipelining host-buffer steps.
+ * Where all four buffers are pinned host memory mapped into the device's
+ * address space (cudaPointerGetAttributes gives a device pointer; 16-byte
+ * aligned), the step's kernel reads the inputs and writes the output in place
+ * over the CPU-GPU link: no staging copies, and consecutive calls' launches
+ * follow each other on the handle's stream as kvevict_decode_step's do.
+ * Otherwise the inputs are copied in on an internal copy-in stream, into one
+ * of two staging slots that alternate between calls; the step runs on the
+ * handle's stream once they are in; the output is copied back on an internal
+ * copy-out stream once the step is done. A call's copy-in overlaps the
+ * previous call's step, and its copy-out the next call's. Either way the host
+ * buffers must stay valid, and the inputs unchanged, until kvevict_sync
+ * returns; the output holds the result only then. Steps run in call order on
+ * the handle's stream. kvevict_decode_step_host waits for the pending calls
+ * first. The copy streams and their events are created on the first call
+ * that copies. */
 int kvevict_decode_step_host_async(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new,
                                    void *out);
+
+/* 1 if p is pinned host memory that kernels may address in place (the
+ * in-place path of kvevict_decode_step_host_async), else 0 (also for null). */
+int kvevict_host_buffer_mapped(const void *p);
 
 /* Waits for every call queued on the handle: its stream and the copy streams
  * of kvevict_decode_step_host_async. Returns CUDA if any reported an error. */

@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
             L.kvevict_set_tail_split.argtypes = [P, I]
             L.kvevict_set_partials_alias.argtypes = [P, I]
             L.kvevict_set_tie_audit.argtypes = [P, I]
+            L.kvevict_host_buffer_mapped.argtypes = [P]
             L.kvevict_near_ties.argtypes = [P, I, ctypes.POINTER(ctypes.c_uint64)]
             L.kvevict_set_path.argtypes = [P, I]
             L.kvevict_set_ring.argtypes = [P, I]
@@ -100,7 +101,7 @@ def lib() -> ctypes.CDLL:
                       "kvevict_score_scales", "kvevict_evicted_mass", "kvevict_probe_wait_timeout", "kvevict_select_victims", "kvevict_checkpoint_bytes",
                       "kvevict_checkpoint_save", "kvevict_checkpoint_restore",
                       "kvevict_set_trace",
-                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_tail_split", "kvevict_set_partials_alias", "kvevict_set_tie_audit", "kvevict_near_ties", "kvevict_set_path", "kvevict_set_ring",
+                      "kvevict_layer_state", "kvevict_set_split", "kvevict_set_clusters", "kvevict_set_tail_split", "kvevict_set_partials_alias", "kvevict_set_tie_audit", "kvevict_near_ties", "kvevict_host_buffer_mapped", "kvevict_set_path", "kvevict_set_ring",
                       "kvevict_get_stats",
                       "kvevict_check"):
                 getattr(L, n).restype = I

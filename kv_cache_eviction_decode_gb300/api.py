@@ -167,8 +167,9 @@ class KVEvictCache:
 
     def decode_step_host_async(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                                out: torch.Tensor) -> torch.Tensor:
-        """decode_step_host without waiting: pinned CPU tensors that must stay
-        alive and unchanged until sync(); out holds the result after sync()."""
+        """decode_step_host without waiting: CPU tensors that must stay alive and
+        unchanged until sync(); out holds the result after sync(). Pinned tensors
+        the GPU can address are read and written in place by the kernels."""
         self._host(q, (self.B, self.Hq, self.D), "q")
         self._host(k_new, (self.B, self.Hkv, self.D), "k_new")
         self._host(v_new, (self.B, self.Hkv, self.D), "v_new")

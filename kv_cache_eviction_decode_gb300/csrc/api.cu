@@ -1224,6 +1224,20 @@ int kvevict_sync(kvevict_t h)
     return cuda_status(e != cudaSuccess ? e : e2);
 }
 
+// The device address of a pinned host buffer that kernels may read and write in
+// place (mapped into the device's address space), or null (any other memory).
+static void *mapped_host(const void *p)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the error of a failed query
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+int kvevict_host_buffer_mapped(const void *p) { return p && mapped_host(p) ? 1 : 0; }
+
 int kvevict_decode_step_host_async(kvevict_t h, int layer, const void *q, const void *k_new, const void *v_new,
                                    void *out)
 {
@@ -1233,6 +1247,17 @@ int kvevict_decode_step_host_async(kvevict_t h, int layer, const void *q, const 
     if (!q || !k_new || !v_new || !out) return KVEVICT_ERR_INVALID_ARG;
     if (h->layers[layer].prompt_len + static_cast<long long>(h->layers[layer].t) >= (1LL << 31) - 1)
         return KVEVICT_ERR_STATE;
+    // Pinned buffers the GPU can address (over the CPU-GPU link): the kernel reads
+    // the inputs and writes the output in place, with no staging copies and no
+    // event waits between the launches of consecutive calls.
+    void *mq = mapped_host(q), *mk = mapped_host(k_new), *mv = mapped_host(v_new), *mo = mapped_host(out);
+    if (mq && mk && mv && mo && aligned16(mq) && aligned16(mk) && aligned16(mv) && aligned16(mo)) {
+        const int rc = launch_decode(h, layer, mq, mk, mv, mo);
+        if (rc) return rc;
+        h->async_calls++;
+        h->async_pending = true;
+        return KVEVICT_OK;
+    }
     cudaError_t e = cudaSuccess;
     if (!h->in_stream) {
         e = cudaStreamCreateWithFlags(&h->in_stream, cudaStreamNonBlocking);
@@ -1283,6 +1308,13 @@ int kvevict_decode_step_host(kvevict_t h, int layer, const void *q, const void *
     if (h->async_pending) {  // calls without waiting may still use the staging slots
         int rc0 = kvevict_sync(h);
         if (rc0) return rc0;
+    }
+    // pinned buffers the GPU can address: read and written in place, as in the call without waiting
+    void *mq = mapped_host(q), *mk = mapped_host(k_new), *mv = mapped_host(v_new), *mo = mapped_host(out);
+    if (mq && mk && mv && mo && aligned16(mq) && aligned16(mk) && aligned16(mv) && aligned16(mo)) {
+        const int rc = launch_decode(h, layer, mq, mk, mv, mo);
+        if (rc) return rc;
+        return cuda_status(cudaStreamSynchronize(h->stream));
     }
     const Layout &L = h->L;
     void *dq = h->state + L.off_sq[0], *dk = h->state + L.off_sk[0], *dv = h->state + L.off_sv[0];

@@ -302,11 +302,16 @@ def test_host_buffer_path_matches_device_path(cuda_device):
     assert torch.equal(a.scores(0), b.scores(0))
 
 
-@pytest.mark.parametrize("policy", [configs.POLICY_H2O, configs.POLICY_RANDOM])
-def test_host_async_path_matches_device_path(cuda_device, policy):
+@pytest.mark.parametrize("policy,pinned", [(configs.POLICY_H2O, True), (configs.POLICY_RANDOM, True),
+                                           (configs.POLICY_H2O, False)])
+def test_host_async_path_matches_device_path(cuda_device, policy, pinned):
     """The host-buffer calls that do not wait, three layers a token and one
-    sync per token (staging slots reused across layers and tokens; Random's cut
-    launches inside): outputs, slot tables and scores equal the device path's."""
+    sync per token (Random's cut launches inside): outputs, slot tables and
+    scores equal the device path's. Pinned buffers the GPU can address are read
+    and written in place by the kernels; pageable ones go through the staging
+    slots and the copy streams."""
+    from kv_cache_eviction_decode_gb300 import lib
+    mapped = lib().kvevict_host_buffer_mapped
     kw = dict(n_sink=2, n_heavy=20, n_recent=10, budget=32, prompt_len=40) if policy == configs.POLICY_H2O else \
         dict(budget=12, r=4, max_prompt=40, prompt_len=40)
     w = _small(policy, configs.DTYPE_BF16, G=4, d=128, B=2, L=3, decode_steps=14, **kw)
@@ -325,8 +330,12 @@ def test_host_async_path_matches_device_path(cuda_device, policy):
             k = torch.randn((2, 4, 128), generator=g, device=cuda_device).to(torch.bfloat16)
             v = torch.randn((2, 4, 128), generator=g, device=cuda_device).to(torch.bfloat16)
             o1 = a.decode_step(layer, q, k, v)
-            ins = (q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory())
-            o2 = torch.empty((2, 16, 128), dtype=torch.bfloat16).pin_memory()
+            ins = tuple(x.cpu().pin_memory() if pinned else x.cpu() for x in (q, k, v))
+            o2 = torch.empty((2, 16, 128), dtype=torch.bfloat16)
+            if pinned:
+                o2 = o2.pin_memory()
+            if not pinned:
+                assert not any(mapped(x.data_ptr()) for x in (*ins, o2))
             b.decode_step_host_async(layer, *ins, o2)
             host.append((o1, ins, o2))  # the host buffers stay alive until the sync
         b.sync()

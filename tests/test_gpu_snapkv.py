@@ -121,6 +121,24 @@ def test_snapkv_prefill_small(cuda_device, G, d, P, w, k):
     _check_prefill(cache, Qo, K, V, votes, k, [(b, h) for b in range(B) for h in range(Hkv)])
 
 
+@pytest.mark.parametrize("G,P,k", [(4, 1000, 20), (8, 5000, 40), (2, 9000, 300)])
+def test_snapkv_select_many_units(cuda_device, G, P, k):
+    """More units than SMs (B=40, 4 KV heads: 160 units, a second wave of
+    selection CTAs). Every unit's slot table equals the selection rule applied
+    to the GPU's votes; sampled units against the oracle. Prefixes of 1000,
+    5000 and 9000 positions take the 4, 16 and 64 votes-per-thread kernels."""
+    gen = torch.Generator().manual_seed(8300 + G * P + k)
+    B, Hkv, d, w = 40, 4, 128, 32
+    Hq = G * Hkv
+    Qo, K, V = _rand((B, Hq, w, d), gen), _rand((B, Hkv, P, d), gen), _rand((B, Hkv, P, d), gen)
+    cap = G * k + w + 8
+    cache = _cache(cuda_device, B, Hq, Hkv, d, 4, cap - 4 - 2, 2)
+    votes = cache.prefill_snapkv(0, Qo.to(cuda_device), K.to(cuda_device), V.to(cuda_device), k)
+    assert cache.check() == 0
+    np.testing.assert_allclose(votes.float().sum(-1).cpu().numpy(), w, rtol=1e-4)
+    _check_prefill(cache, Qo, K, V, votes, k, [(0, 0), (17, 2), (39, 3)])
+
+
 @pytest.mark.parametrize("G,w", [(4, 32), (8, 32), (2, 64)])
 def test_snapkv_votes_many_units(cuda_device, G, w):
     """More (unit, key tile) items than SMs: the streamed votes kernel's CTAs
