@@ -181,7 +181,9 @@ typedef struct {
 } kvevict_stats;
 
 /* Bytes of device memory a handle with this configuration needs (cache,
- * positions, scores, free lists, error word, two slots of host-path staging). Host only:
+ * positions, scores, the evicted-mass ledger and the near-tie counters of
+ * policies with scores, free lists, error word, two slots of host-path
+ * staging). Host only:
  * launches nothing, needs no GPU. Returns INVALID_ARG for a configuration
  * the library does not accept. */
 int kvevict_state_bytes(const kvevict_config *cfg, size_t *bytes);
